@@ -1,0 +1,253 @@
+"""Benchmark of the stage forward on GB300.
+
+Default workload: the dense 8B-shape decoder (32 blocks, hidden 4096, 32 q / 8 kv heads x
+128, SwiGLU 14336, vocab 32000, int8 block-32 weights) as 2 stages split 16/16 on one GPU,
+batch-1 greedy decode at context 2048.  A step = one token through both stages, the
+final norm, the readout and the greedy argmax (every row of the hot path).
+
+value : decode tok/s, device-timed (CUDA events on the stages' stream) over K graph-replayed
+        steps with everything resident in HBM; weights (7.5 GB) exceed L2, so every step
+        streams them from HBM.
+e2e   : the same through the C ABI with host buffers (stage_pipeline_step per token: host
+        seq/pos/token arrays copied in, the greedy token read back each step).
+roofline: bytes per token (weights once + KV at the context) / step time against the
+        measured HBM peak; the dominant kernel is timed on its own in a second pass.
+--impl reference: the CPU oracle on the host cores, on a bounded sample of the workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+CFG_ID = 1
+CONTEXT = 2048
+BOUNDS = [0, 16, 32]
+
+
+def measured_peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except Exception:
+        return {}
+
+
+def bytes_per_token(model, context):
+    """Algorithmic bytes of one decode token: every weight byte once (1 B int8 + 2 B per 32
+    scale = 1.0625 B/param) plus the fp16 K and V rows of every position attended."""
+    H, D = model.hidden, model.head_dim
+    per_layer = (model.q_dim + 2 * model.kv_dim) * H + H * model.q_dim + 3 * model.ffn * H
+    params = per_layer * model.n_layers + model.vocab * H  # readout; the embedding reads one row
+    w = params * 1.0625 + H * 1.0625
+    kv = model.n_layers * 2 * model.n_kv_heads * context * D * 2
+    return w, kv
+
+
+class ClockSampler:
+    def __init__(self, period_s=0.2):
+        self.samples, self.period, self._stop = [], period_s, threading.Event()
+        self._t = None
+
+    def start(self):
+        def run():
+            q = ("--query-gpu=clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+                 "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+                 "clocks_event_reasons.sw_power_cap")
+            while not self._stop.is_set():
+                try:
+                    out = subprocess.run(["nvidia-smi", q, "--format=csv,noheader,nounits", "-i", "0"],
+                                         capture_output=True, text=True, timeout=5).stdout.strip()
+                    if out:
+                        self.samples.append([x.strip() for x in out.split(",")])
+                except Exception:
+                    pass
+                self._stop.wait(self.period)
+        self._t = threading.Thread(target=run, daemon=True)
+        self._t.start()
+
+    def stop(self):
+        self._stop.set()
+        if self._t:
+            self._t.join(timeout=10)
+        sm = [float(s[0]) for s in self.samples if s[0].replace(".", "").isdigit()]
+        mx = [float(s[1]) for s in self.samples if s[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for s in self.samples for i in range(4) if len(s) > 2 + i and "Active" in s[2 + i]
+                          and "Not" not in s[2 + i]})
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.samples)}
+
+
+def build_gpu_pipeline(model, bounds, max_seq_len, max_tokens, max_seqs=1):
+    from layer_range_stage_gb300.pipeline import StagePipeline
+    return StagePipeline(model, bounds, lambda l: synth.layer_weights(model, l),
+                         lambda a, b: synth.stage_weights(model, a, b, with_layers=False),
+                         max_seqs=max_seqs, max_seq_len=max_seq_len, max_tokens=max_tokens)
+
+
+def run_gpu(args):
+    import torch
+    import layer_range_stage_gb300 as L  # noqa: F401
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    model = synth.CONFIGS[CFG_ID]
+    steps, warmup = args.steps, args.warmup
+    max_len = CONTEXT + warmup + 2 * steps + 8
+    t_build = time.time()
+    gp = build_gpu_pipeline(model, BOUNDS, max_len, max_tokens=512)
+    # prefill the seeded context in chunks of 512 tokens through the stages
+    prompt = synth.prompt_tokens(model, rank, CONTEXT)
+    tok = None
+    for c0 in range(0, CONTEXT, 512):
+        c1 = min(CONTEXT, c0 + 512)
+        tok = gp.step(True, np.zeros(c1 - c0), np.arange(c0, c1), prompt[c0:c1], rows=[c1 - c0 - 1])
+    torch.cuda.synchronize()
+    build_s = time.time() - t_build
+    stream = torch.cuda.current_stream()
+    # warm-up (captures the step graph), then K timed graph replays
+    first = gp.generate([0], tok, warmup, use_graph=True)[-1]
+    if dist:
+        dist.barrier()
+    clocks = ClockSampler()
+    clocks.start()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    last = gp.generate([0], first, steps, use_graph=True)[-1]
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1)
+    if dist:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+        dist.barrier()
+    ctx_mid = CONTEXT + warmup + steps / 2
+    w_bytes, kv_bytes = bytes_per_token(model, ctx_mid)
+    ms_step = ms / steps
+    tok_s = world * 1000.0 / ms_step
+    gbs = (w_bytes + kv_bytes) / (ms_step * 1e-3) / 1e9
+
+    # e2e: stage_pipeline_step per token with host buffers (token read back every step)
+    cur = CONTEXT + warmup + steps
+    tk = int(last[0])
+    for _ in range(2):
+        tk = int(gp.step(False, [0], [cur], [tk], rows=[0])[0])
+        cur += 1
+    torch.cuda.synchronize()
+    n_e2e = max(4, steps // 2)
+    t0 = time.perf_counter()
+    for _ in range(n_e2e):
+        tk = int(gp.step(False, [0], [cur], [tk], rows=[0])[0])
+        cur += 1
+    e2e_s = time.perf_counter() - t0
+    e2e = {"value": n_e2e * world / e2e_s, "unit": "tok/s", "h2d_bytes_per_step": 4 * (3 + 2 + 1),
+           "d2h_bytes_per_step": 4, "steps": n_e2e}
+    gp.close()
+
+    peaks = measured_peaks()
+    peak = peaks.get("hbm_gbs")
+    line = {
+        "metric": "decode tok/s (batch-1 greedy, 8B-shape int8 block-32, 2 stages 16/16, ctx 2048)",
+        "value": round(tok_s, 2), "unit": "tok/s", "n_gpus": world, "steps": steps, "warmup": warmup,
+        "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32 (int8 block-32 weights, fp16 KV)", "data": "synthetic (seeded N(0,0.02) weights, seeded prompt)",
+        "config": {"workload": "dense 8B-shape decode, 32 blocks as 2 stages 16/16, batch 1, context 2048",
+                   "parallelism": "replicas only" if world > 1 else "single GPU, 2 chained stages",
+                   "l2": "weights 7.5 GB > L2 each step (no flush needed)"},
+        "hbm_gbs_achieved": round(gbs, 1),
+        "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(gbs / peak, 4) if peak else None, "traffic": None,
+                     "kernel": "whole decode step (weights + KV bytes per token / step time)",
+                     "peak_source": "measured" if peak else "fallback"},
+        "e2e": e2e,
+        "clocks": clk,
+        "gpu_launches": None,
+        "build_s": round(build_s, 1),
+    }
+    if rank == 0 and not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline(args)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def cpu_baseline(args, budget_s=20.0):
+    """The oracle as it stands, on a bounded sample: one decode token through 2 of the 32
+    blocks at context 2048 (KV filled with seeded fp16 values; the oracle's time does not
+    depend on their values) plus the readout, scaled to the 32-block token."""
+    import oracle
+    model = synth.CONFIGS[CFG_ID]
+    n_blk = 2
+    cores = os.cpu_count()
+    sub = synth.reduced(model, n_blk)
+    w = synth.stage_weights(sub, 0, n_blk)
+    st = oracle.Stage(sub, 0, n_blk, w, max_len=CONTEXT + 1)
+    rng = np.random.default_rng(0)
+    st.k_cache[:] = rng.standard_normal(st.k_cache.shape).astype(np.float16)
+    st.v_cache[:] = rng.standard_normal(st.v_cache.shape).astype(np.float16)
+    t0 = time.perf_counter()
+    st.forward([0], [CONTEXT], tokens=[1], cache_dequant=False)
+    t_blocks = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    st.logits()
+    t_head = time.perf_counter() - t0
+    per_token = t_blocks * model.n_layers / n_blk + t_head
+    return {"value": round(1.0 / per_token, 5), "unit": "tok/s", "cores": cores, "kind": "oracle",
+            "sample": f"1 decode token through {n_blk} of {model.n_layers} blocks at context {CONTEXT} + readout, "
+                      f"block time scaled x{model.n_layers // n_blk}; measured {t_blocks + t_head:.1f} s"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    cb = cpu_baseline(args)
+    line = {"impl": "reference", "metric": "decode tok/s (batch-1 greedy, 8B-shape int8 block-32, 2 stages 16/16, ctx 2048)",
+            "value": cb["value"], "unit": "tok/s", "n_gpus": int(os.environ.get("WORLD_SIZE", "1")),
+            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "dense 8B-shape decode, 32 blocks as 2 stages 16/16, batch 1, context 2048"},
+            "cpu_baseline": cb, "e2e": {"value": cb["value"], "unit": "tok/s", "h2d_bytes_per_step": 0,
+                                        "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=64)
+    ap.add_argument("--warmup", type=int, default=8)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,241 @@
+/*
+ * layer_range_stage (GB300) -- C ABI of one pipeline stage.
+ *
+ * A stage owns a contiguous range [begin, end) of decoder blocks, the resident
+ * weights of exactly those blocks, their fp16 KV cache and its workspace.  It
+ * takes an F32 hidden activation in and hands an F32 hidden activation out; the
+ * first stage (begin == 0) embeds tokens instead of taking a hidden activation,
+ * the last stage (end == n_layers) applies the final RMSNorm and owns the
+ * readout.
+ *   - "RFC: pipeline placement across multiple GPUs for models larger than one
+ *     device", section "What I found": each stage owns its resident weights,
+ *     model state / KV, heap, workspace and prepared kernels; only the hidden
+ *     activation crosses the boundary; a logical step is accepted only after
+ *     every stage completes.
+ *   - "Multi-node layer splitting and tensor parallelism", section "Supported
+ *     stage executors": the dense pipeline transfers F32 hidden activations; each
+ *     node loads only its layer weights and KV state; the first stage embeds and
+ *     the last computes logits.  Section "Launch a layer pipeline" onwards: the
+ *     stage executors accept serialized forward / refill / reset / truncate
+ *     controls and keep cache ownership across them.
+ *   - "41. Many GPUs: tensor, pipeline, expert and data parallelism", section
+ *     "Pipeline parallelism": PipelineStage.forward -- embed on the first stage,
+ *     the per-block add_norm / attention / add_norm / MLP loop, one residual
+ *     tensor across each boundary, final norm at the end.
+ *
+ * Conventions for every function below:
+ *   - Return 0 (STAGE_OK) on success, a negative STAGE_E_* code on failure.  No
+ *     C++ exception crosses this boundary.  stage_last_error() gives a message.
+ *   - After any error no committed sequence length changes; KV rows written by a
+ *     failed or uncommitted call are simply overwritten by the retry.
+ *   - Arrays named *_host are read on the host before the call returns; device
+ *     buffers (hidden activations, logits) are used asynchronously on the
+ *     stage's CUDA stream and must stay alive until that stream reaches the work.
+ *   - One call at a time per stage.  A call that finds another call of the same
+ *     stage in progress returns STAGE_E_BUSY without side effects.
+ *   - Every stage of a pipeline runs on one GPU and one stream; the handoff is a
+ *     device buffer, no copy through the host.
+ */
+#ifndef LAYER_RANGE_STAGE_H
+#define LAYER_RANGE_STAGE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define STAGE_API __attribute__((visibility("default")))
+#else
+#define STAGE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+  STAGE_OK = 0,
+  STAGE_E_INVALID = -1,      /* bad config, range, shape, null where required, value out of range */
+  STAGE_E_DOES_NOT_FIT = -2, /* stage_required_bytes exceeds the budget or the device's free memory */
+  STAGE_E_HANDOFF = -3,      /* tokens given to a non-first stage, hidden given to the first, wrong n/width */
+  STAGE_E_POSITION = -4,     /* positions not committed_len + i, or >= max_seq_len */
+  STAGE_E_BUSY = -5,         /* another call of this stage is in progress */
+  STAGE_E_NOT_LAST = -6,     /* readout requested from a stage that does not own it */
+  STAGE_E_CUDA = -7,         /* a CUDA runtime error; the message is in stage_last_error */
+  STAGE_E_STATE = -8,        /* weights not loaded, or commit beyond what was written */
+  STAGE_E_INJECTED = -9      /* host-side fault injection (stage_debug_inject) */
+};
+
+typedef struct stage* stage_t;
+
+/* Model shape.  Dense models set n_experts = top_k = expert_ffn = 0.  ffn and
+ * expert_ffn need not be multiples of 32 (the last weight block of a row is then
+ * partial).  max_seqs / max_seq_len size the KV cache; max_tokens bounds the
+ * tokens of one prefill or decode call.  gemm_bf16_min_tokens: calls with at least
+ * this many tokens run their projections on the tensor cores with bf16 operands;
+ * smaller calls use the float32 dequant-fused GEMV (0 = never use bf16). */
+typedef struct {
+  int n_layers, hidden, n_q_heads, n_kv_heads, head_dim, ffn, vocab;
+  int n_experts, top_k, expert_ffn;
+  float rms_eps, rope_theta;
+  int max_seqs, max_seq_len, max_tokens;
+  int gemm_bf16_min_tokens;
+} stage_model_cfg;
+
+/* Global block range [begin, end): begin == 0 => the stage embeds; end == n_layers
+ * => the stage applies the final norm and owns the readout. */
+typedef struct {
+  int begin, end;
+} stage_layer_range;
+
+/* Host int8 block-32 matrix, row-major [rows x cols]: q[rows][cols] int8 and
+ * scale[rows][ceil(cols/32)] IEEE fp16 bit patterns; weight (r, c) is
+ * scale[r][c/32] * q[r][c].  Blocks run along the input dimension (cols). */
+typedef struct {
+  const int8_t* q;
+  const uint16_t* scale;
+  int64_t rows, cols;
+} stage_q8;
+
+/* Host weights of one block.  Shapes: norms [hidden] f32; wq [Hq*D x hidden];
+ * wk, wv [Hkv*D x hidden]; wo [hidden x Hq*D]; dense: w_gate, w_up [ffn x hidden],
+ * w_down [hidden x ffn]; MoE: router [n_experts x hidden] and arrays of n_experts
+ * matrices e_gate, e_up [expert_ffn x hidden], e_down [hidden x expert_ffn]. */
+typedef struct {
+  const float *attn_norm, *ffn_norm;
+  stage_q8 wq, wk, wv, wo;
+  stage_q8 w_gate, w_up, w_down;
+  stage_q8 router;
+  const stage_q8 *e_gate, *e_up, *e_down;
+} stage_layer_w;
+
+/* Host weights of a stage: embed [vocab x hidden] only if begin == 0; final_norm
+ * [hidden] and lm_head [vocab x hidden] only if end == n_layers; layers has
+ * end - begin entries, the owned blocks in order.  Nothing outside the range is
+ * read ("each stage loads its owned weights"). */
+typedef struct {
+  stage_q8 embed;
+  const float* final_norm;
+  stage_q8 lm_head;
+  const stage_layer_w* layers;
+} stage_weights;
+
+/* A device float32 activation, row-major [rows x cols] (one row per token).  The
+ * stage checks rows == n_tokens and cols == hidden: the checked handoff. */
+typedef struct {
+  float* data;
+  int rows, cols;
+} stage_act;
+
+/* Bytes stage_create allocates on the device for this range: owned weights (in the
+ * device layout), KV cache, RoPE table and workspace.  0 if cfg/range are invalid. */
+STAGE_API size_t stage_required_bytes(const stage_model_cfg* cfg, stage_layer_range range);
+
+/* Create a stage on the current CUDA device.  Fails with STAGE_E_DOES_NOT_FIT --
+ * before allocating anything -- when stage_required_bytes exceeds
+ * device_budget_bytes or the device's free memory (the per-device fit rule of the
+ * RFC page, section "Heterogeneous GPUs": required(stage_i) <= budget(device_i)).
+ * weights may be NULL: then load blocks with stage_load_layer and the endpoints
+ * with stage_load_endpoints before the first forward.  Host weights are copied;
+ * the caller may free them after return.  cuda_stream: a cudaStream_t (NULL = the
+ * legacy default stream); every kernel of this stage runs on it. */
+STAGE_API int stage_create(const stage_model_cfg* cfg, stage_layer_range range, const stage_weights* weights,
+                 size_t device_budget_bytes, void* cuda_stream, stage_t* out);
+
+/* Import the weights of one owned block (global index in [begin, end)). */
+STAGE_API int stage_load_layer(stage_t st, int global_layer, const stage_layer_w* w);
+
+/* Import the embedding (first stage) and/or final norm + readout (last stage). */
+STAGE_API int stage_load_endpoints(stage_t st, const stage_weights* w);
+
+/* Prefill / refill: n_tokens tokens, possibly of several sequences.  For each
+ * sequence its tokens appear in order with positions committed_len, committed_len
+ * + 1, ...  (seq_ids_host, positions_host, tokens_host: host int32 [n_tokens]).
+ * First stage: tokens_host set, hidden_in NULL.  Other stages: tokens_host NULL,
+ * hidden_in [n_tokens x hidden].  hidden_out [n_tokens x hidden] receives the
+ * residual stream (last stage: the final features rmsnorm(x) * gamma_f); it may be
+ * the same buffer as hidden_in.  K/V of every token are written to the cache;
+ * attention is causal within each sequence. */
+STAGE_API int stage_prefill(stage_t st, int n_tokens, const int32_t* seq_ids_host, const int32_t* positions_host,
+                  const int32_t* tokens_host, const stage_act* hidden_in, const stage_act* hidden_out);
+
+/* Decode: one token for each of `batch` distinct sequences, at position
+ * committed_len[seq].  Same conventions as stage_prefill. */
+STAGE_API int stage_decode(stage_t st, int batch, const int32_t* seq_ids_host, const int32_t* positions_host,
+                 const int32_t* tokens_host, const stage_act* hidden_in, const stage_act* hidden_out);
+
+/* Readout of the last stage for rows row_index_host[0..n_rows) of its last forward:
+ * logits = W_head * features.  logits_out: device f32 [n_rows x vocab] or NULL;
+ * argmax_out: device int32 [n_rows] or NULL (greedy token, lowest index on ties). */
+STAGE_API int stage_logits(stage_t st, int n_rows, const int32_t* row_index_host, float* logits_out, int32_t* argmax_out);
+
+/* Publish the written rows: committed_len[seq_ids[i]] = new_len[i].  new_len must
+ * lie between the committed length and the highest position written since. */
+STAGE_API int stage_commit(stage_t st, int n, const int32_t* seq_ids_host, const int32_t* new_len_host);
+
+/* Truncate one sequence to len <= committed_len (later rows are overwritten). */
+STAGE_API int stage_truncate(stage_t st, int seq_id, int len);
+
+/* Forget every sequence (committed lengths to 0). */
+STAGE_API int stage_reset(stage_t st);
+
+STAGE_API int stage_committed_len(stage_t st, int seq_id, int* len_out);
+
+/* Copy the cached K and V of one owned block and sequence to the host: positions
+ * [0, n_pos) of every KV head, fp16 bit patterns, each [n_kv_heads x n_pos x head_dim].
+ * Synchronises the stage's stream.  For inspection and equivalence checks. */
+STAGE_API int stage_read_kv(stage_t st, int global_layer, int seq_id, int n_pos, uint16_t* k_host, uint16_t* v_host);
+
+/* Which arithmetic a call with n_tokens tokens uses: 0 = float32 GEMV, 1 = bf16 tensor cores. */
+STAGE_API int stage_gemm_mode(stage_t st, int n_tokens, int* mode_out);
+
+STAGE_API const char* stage_last_error(stage_t st);
+
+/* Message of the last failed stage_create on the calling thread ("" if none). */
+STAGE_API const char* stage_create_error(void);
+
+STAGE_API void stage_destroy(stage_t st);
+
+/* Host-side fault injection for tests (no GPU fault is ever caused):
+ *   what = 1: mark the stage busy (value 1) or idle (value 0) as if a call were in progress;
+ *   what = 2: the next prefill/decode returns STAGE_E_INJECTED before launching anything. */
+STAGE_API int stage_debug_inject(stage_t st, int what, int value);
+
+/* ------------------------------------------------------------------------- pipeline
+ * Stages chained in order on one GPU and one stream.  Stage k's hidden_out buffer
+ * is stage k+1's hidden_in (a pointer handoff).  A step is published jointly:
+ * every stage's committed lengths advance only if every stage succeeded (RFC page,
+ * "What I propose upstreaming", PR 1: checked activation handoff, joint
+ * completion / state publication). */
+typedef struct stage_pipeline* stage_pipeline_t;
+
+/* stages: n_stages created stages whose ranges tile [0, n_layers) in order, on one
+ * device and stream.  The pipeline does not own them. */
+STAGE_API int stage_pipeline_create(stage_t* stages, int n_stages, stage_pipeline_t* out);
+
+/* One step of all stages: prefill (is_prefill = 1) or decode, then the readout of
+ * rows row_index_host[0..n_rows) on the last stage.  logits_out (device, may be
+ * NULL), next_tokens_host (host int32 [n_rows], may be NULL: the greedy tokens,
+ * read back after the step).  Commits every stage to the new lengths on success. */
+STAGE_API int stage_pipeline_step(stage_pipeline_t p, int is_prefill, int n_tokens, const int32_t* seq_ids_host,
+                        const int32_t* positions_host, const int32_t* tokens_host, int n_rows,
+                        const int32_t* row_index_host, float* logits_out, int32_t* next_tokens_host);
+
+/* n_steps greedy decode steps for `batch` sequences, feeding each greedy token back
+ * on the device.  first_tokens_host: the token to feed at each sequence's committed
+ * length.  tokens_out_host: host int32 [n_steps x batch], the greedy token of each
+ * step.  use_graph = 1 replays one captured CUDA graph per step.  Commits n_steps
+ * positions on every stage at the end. */
+STAGE_API int stage_pipeline_generate(stage_pipeline_t p, int batch, const int32_t* seq_ids_host,
+                            const int32_t* first_tokens_host, int n_steps, int use_graph,
+                            int32_t* tokens_out_host);
+
+/* Bytes handed across boundary k (0-based) so far, and the number of handoffs. */
+STAGE_API int stage_pipeline_handoff_stats(stage_pipeline_t p, int boundary, int64_t* calls, int64_t* bytes);
+
+STAGE_API const char* stage_pipeline_last_error(stage_pipeline_t p);
+STAGE_API void stage_pipeline_destroy(stage_pipeline_t p);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* LAYER_RANGE_STAGE_H */

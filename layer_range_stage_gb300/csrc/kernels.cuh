@@ -1,0 +1,77 @@
+// Launch interface of the stage kernels (host side).
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace lrs {
+
+enum GemvEpi { EPI_STORE = 0, EPI_RESID = 1, EPI_SWIGLU = 2, EPI_QKV = 3 };
+
+// Device int8 block-32 matrix: q [N][Kp] int8, s [N][Kp/32] fp16 bits, Kp = K rounded up to 32
+// (the padding columns hold q = 0).  Row order is the device order chosen at import.
+struct DevQ8 {
+  int8_t* q = nullptr;
+  uint16_t* s = nullptr;
+  int N = 0, K = 0, Kp = 0;
+};
+
+// y[t][n] = sum_k W[n][k] * h[t][k], h = x (or rmsnorm(x) * gamma when gamma != nullptr),
+// followed by the epilogue `epi`:
+//   EPI_STORE : out[t][n] = y
+//   EPI_RESID : out[t][n] = resid[t][n] + y            (the residual add; may run in place)
+//   EPI_SWIGLU: device rows (2j, 2j+1) are (gate_j, up_j); out[t][j] = silu(g) * u
+//   EPI_QKV   : device rows (2i, 2i+1) of each head are its dims (i, i + D/2); q heads, then
+//               k heads, then v heads.  q, k are rotated (rotate-half RoPE at pos[t]); q goes
+//               to qout[t][head][D] (f32), k and v to the fp16 cache at (seq[t], kv head, pos[t]).
+struct GemvArgs {
+  DevQ8 w;
+  const float* x = nullptr;
+  int ldx = 0;
+  const int* x_rows = nullptr;  // optional: token t reads input row x_rows[t]
+  int ntok = 0;
+  const float* gamma = nullptr;
+  float eps = 0.f;
+  int epi = EPI_STORE;
+  float* out = nullptr;
+  int ldo = 0;
+  const float* resid = nullptr;
+  int ldr = 0;
+  // EPI_QKV
+  float* qout = nullptr;
+  __half* kc = nullptr;
+  __half* vc = nullptr;
+  const int* seq = nullptr;
+  const int* pos = nullptr;
+  const float2* rope = nullptr;  // [max_len][D/2] (cos, sin)
+  int n_q_heads = 0, n_kv_heads = 0, head_dim = 0, max_len = 0;
+};
+
+// Split-K grouped-query decode attention over the fp16 cache with a deterministic merge of
+// the chunk partials by the last CTA of each (token, kv head).
+struct AttnArgs {
+  const float* q = nullptr;      // [ntok][Hq][D]
+  const __half* kc = nullptr;    // [max_seqs][Hkv][max_len][D] (this layer)
+  const __half* vc = nullptr;
+  const int* seq = nullptr;      // [ntok]
+  const int* pos = nullptr;      // [ntok]; token t attends to positions 0..pos[t]
+  float* out = nullptr;          // [ntok][Hq][D]
+  float* part_o = nullptr;       // scratch [ntok][Hq][n_chunks][D]
+  float2* part_ml = nullptr;     // scratch [ntok][Hq][n_chunks] (running max, sum)
+  int* counters = nullptr;       // scratch [ntok][Hkv], zero between launches (the kernel re-zeroes)
+  int ntok = 0, Hq = 0, Hkv = 0, D = 0, max_len = 0, n_chunks = 1;
+  float scale = 1.f;
+};
+
+int sm_count();
+cudaError_t launch_gemv(const GemvArgs& a, cudaStream_t st);
+cudaError_t launch_attn_decode(const AttnArgs& a, cudaStream_t st);
+bool attn_decode_supported(int head_dim, int group);
+cudaError_t launch_embed(const DevQ8& table, const int* tok, int ntok, float* out, int ldo, cudaStream_t st);
+cudaError_t launch_final_norm(const float* x, int ldx, const float* gamma, float eps, int H, int ntok,
+                              float* feat, float* out, int ldo, cudaStream_t st);
+cudaError_t launch_argmax(const float* logits, int V, int n_rows, int* out, cudaStream_t st);
+cudaError_t launch_advance(int* pos, const int* tok, int* hist, int* step, int batch, cudaStream_t st);
+
+}  // namespace lrs

@@ -1,0 +1,97 @@
+"""The C-ABI library loads, exports every declared symbol, and its host-side checks work
+without a GPU (config validation, the device-budget fit rule, the byte plan)."""
+import ctypes
+import json
+import os
+import subprocess
+
+import pytest
+
+import synth
+import layer_range_stage_gb300 as L
+from layer_range_stage_gb300 import build as lbuild
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    lbuild.build()
+
+
+def test_library_exports_every_declared_symbol():
+    declared = L.declared_symbols()
+    assert len(declared) >= 20
+    out = subprocess.run(["nm", "-D", "--defined-only", lbuild.LIB], capture_output=True, text=True, check=True).stdout
+    exported = {ln.split()[-1] for ln in out.splitlines() if " T " in ln}
+    assert set(declared) <= exported, set(declared) - exported
+    lib = L.lib()
+    for name in declared:
+        assert getattr(lib, name) is not None
+
+
+def cfg_of(model, **kw):
+    d = dict(max_seqs=1, max_seq_len=256, max_tokens=64)
+    d.update(kw)
+    return L.make_cfg(model, **d)
+
+
+def test_required_bytes_covers_weights_and_kv():
+    m = synth.CONFIGS[1]
+    c = cfg_of(m, max_seq_len=2048 + 64, max_tokens=64)
+    per_layer_params = (m.q_dim + 2 * m.kv_dim) * m.hidden + m.hidden * m.q_dim + 3 * m.ffn * m.hidden
+    total = 0
+    for a, b in ((0, 16), (16, 32)):
+        req = L.stage_required_bytes(c, a, b)
+        params = per_layer_params * (b - a) + (m.vocab * m.hidden if a == 0 else 0) + \
+            (m.vocab * m.hidden if b == m.n_layers else 0)
+        kv = 2 * (b - a) * m.n_kv_heads * (2048 + 64) * m.head_dim * 2
+        assert req >= params * 1.0625 + kv
+        assert req <= params * 1.0625 + kv + (256 << 20)     # workspace stays small at batch 1
+        total += req
+    assert L.stage_required_bytes(c, 0, 32) < total          # the split adds only workspace
+
+
+def test_invalid_configs_are_rejected_before_any_device_call():
+    m = synth.CONFIGS[0]
+    for kw in (dict(max_seqs=0), dict(max_tokens=0)):
+        c = cfg_of(m, **kw)
+        assert L.stage_required_bytes(c, 0, 4) == 0
+        with pytest.raises(L.StageError) as e:
+            L.stage_create(c, 0, 4, budget=1 << 40, stream=0)
+        assert e.value.code == L.STAGE_E_INVALID
+    c = cfg_of(m)
+    for a, b in ((2, 2), (3, 2), (-1, 2), (0, 5)):
+        assert L.stage_required_bytes(c, a, b) == 0
+        with pytest.raises(L.StageError) as e:
+            L.stage_create(c, a, b, budget=1 << 40, stream=0)
+        assert e.value.code == L.STAGE_E_INVALID
+    bad = synth.reduced(m, 4, n_kv_heads=3)
+    with pytest.raises(L.StageError) as e:
+        L.stage_create(cfg_of(bad), 0, 4, budget=1 << 40, stream=0)
+    assert e.value.code == L.STAGE_E_INVALID
+
+
+def test_does_not_fit_is_per_device_not_summed():
+    """The RFC's rule: a placement is legal only if every stage fits its own device's
+    budget; the summed budget never counts.  With the page's numbers the whole model
+    (40.396 GB) fits neither 22.76 GB device while the two stage charges fit."""
+    g = json.load(open(os.path.join(GOLDEN, "rfc_fit_budgets.json")))
+    budgets = g["device_budgets"]
+    assert [g["single_device_required"] <= b for b in budgets] == g["expected"]["single_device_fits"]
+    assert all(st["total_charge"] <= budgets[st["device"]] for st in g["stages"]) == g["expected"]["placement_fits"]
+    assert (g["single_device_required"] <= sum(budgets)) == g["expected"]["summed_vram_would_fit"]
+    # the same rule through stage_create: each stage against its own budget, checked
+    # before anything is allocated
+    m = synth.CONFIGS[2]
+    c = cfg_of(m, max_seq_len=4096 + 64)
+    whole = L.stage_required_bytes(c, 0, 40)
+    s0, s1 = L.stage_required_bytes(c, 0, 21), L.stage_required_bytes(c, 21, 40)
+    budget = max(s0, s1)
+    assert whole > budget and s0 <= budget and s1 <= budget
+    with pytest.raises(L.StageError) as e:
+        L.stage_create(c, 0, 40, budget=budget, stream=0)
+    assert e.value.code == L.STAGE_E_DOES_NOT_FIT and "DoesNotFit" in str(e.value)
+    with pytest.raises(L.StageError) as e:
+        L.stage_create(c, 0, 21, budget=s0 - 1, stream=0)
+    assert e.value.code == L.STAGE_E_DOES_NOT_FIT
