@@ -109,15 +109,20 @@ def run_gpu(args):
         import torch.distributed as dist
         dist.init_process_group("nccl")
     model = synth.CONFIGS[CFG_ID]
+    bounds = BOUNDS
+    context = args.context
+    if args.layers:  # reduced depth: profiling of a small case only, never a bench line
+        model = synth.reduced(model, args.layers)
+        bounds = [0, args.layers // 2, args.layers] if args.layers > 1 else [0, 1]
     steps, warmup = args.steps, args.warmup
-    max_len = CONTEXT + warmup + 2 * steps + 8
+    max_len = context + warmup + 2 * steps + 8
     t_build = time.time()
-    gp = build_gpu_pipeline(model, BOUNDS, max_len, max_tokens=512)
+    gp = build_gpu_pipeline(model, bounds, max_len, max_tokens=512)
     # prefill the seeded context in chunks of 512 tokens through the stages
-    prompt = synth.prompt_tokens(model, rank, CONTEXT)
+    prompt = synth.prompt_tokens(model, rank, context)
     tok = None
-    for c0 in range(0, CONTEXT, 512):
-        c1 = min(CONTEXT, c0 + 512)
+    for c0 in range(0, context, 512):
+        c1 = min(context, c0 + 512)
         tok = gp.step(True, np.zeros(c1 - c0), np.arange(c0, c1), prompt[c0:c1], rows=[c1 - c0 - 1])
     torch.cuda.synchronize()
     build_s = time.time() - t_build
@@ -141,14 +146,14 @@ def run_gpu(args):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms = float(t.item())
         dist.barrier()
-    ctx_mid = CONTEXT + warmup + steps / 2
+    ctx_mid = context + warmup + steps / 2
     w_bytes, kv_bytes = bytes_per_token(model, ctx_mid)
     ms_step = ms / steps
     tok_s = world * 1000.0 / ms_step
     gbs = (w_bytes + kv_bytes) / (ms_step * 1e-3) / 1e9
 
     # e2e: stage_pipeline_step per token with host buffers (token read back every step)
-    cur = CONTEXT + warmup + steps
+    cur = context + warmup + steps
     tk = int(last[0])
     for _ in range(2):
         tk = int(gp.step(False, [0], [cur], [tk], rows=[0])[0])
@@ -184,6 +189,8 @@ def run_gpu(args):
         "gpu_launches": None,
         "build_s": round(build_s, 1),
     }
+    if args.layers or args.context != CONTEXT:
+        line["config"]["profiling_case"] = f"{model.n_layers} blocks, context {context}: not the benchmark workload"
     if rank == 0 and not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(args)
     if rank == 0:
@@ -240,6 +247,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=8)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=0, help="reduced depth, for profiling small cases only")
+    ap.add_argument("--context", type=int, default=CONTEXT)
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

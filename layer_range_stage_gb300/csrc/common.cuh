@@ -36,44 +36,21 @@ __device__ __forceinline__ uint16_t ld_stream_u16(const void* p) {
   return r;
 }
 
-// Exact int8 -> float for the 4 bytes of a word.  The byte is biased by 128 (xor 0x80),
-// placed as the low mantissa byte of 2^23 (exponent byte 0x4B) with one byte permute,
-// and the bias 2^23 + 128 is subtracted: 2^23 + (q + 128) - (2^23 + 128) = q, exactly.
-__device__ __forceinline__ void i8x4_to_f32(uint32_t w, float& a, float& b, float& c, float& d) {
-  const uint32_t x = w ^ 0x80808080u;
-  const float bias = 8388736.0f;
-  a = __uint_as_float(__byte_perm(x, 0x4B000000u, 0x7540)) - bias;
-  b = __uint_as_float(__byte_perm(x, 0x4B000000u, 0x7541)) - bias;
-  c = __uint_as_float(__byte_perm(x, 0x4B000000u, 0x7542)) - bias;
-  d = __uint_as_float(__byte_perm(x, 0x4B000000u, 0x7543)) - bias;
+// 16-byte asynchronous global -> shared copy (no register staging; all copies of a thread
+// stay in flight until cp_async_wait_all).
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem) : "memory");
 }
 
-// sum_j q_j * x_j over the 16 int8 weights of w and 16 floats of x.
-__device__ __forceinline__ float dot16_i8(const uint4 w, const float4 x0, const float4 x1, const float4 x2,
-                                          const float4 x3) {
-  float a, b, c, d, acc;
-  i8x4_to_f32(w.x, a, b, c, d);
-  acc = a * x0.x;
-  acc = fmaf(b, x0.y, acc);
-  acc = fmaf(c, x0.z, acc);
-  acc = fmaf(d, x0.w, acc);
-  i8x4_to_f32(w.y, a, b, c, d);
-  acc = fmaf(a, x1.x, acc);
-  acc = fmaf(b, x1.y, acc);
-  acc = fmaf(c, x1.z, acc);
-  acc = fmaf(d, x1.w, acc);
-  i8x4_to_f32(w.z, a, b, c, d);
-  acc = fmaf(a, x2.x, acc);
-  acc = fmaf(b, x2.y, acc);
-  acc = fmaf(c, x2.z, acc);
-  acc = fmaf(d, x2.w, acc);
-  i8x4_to_f32(w.w, a, b, c, d);
-  acc = fmaf(a, x3.x, acc);
-  acc = fmaf(b, x3.y, acc);
-  acc = fmaf(c, x3.z, acc);
-  acc = fmaf(d, x3.w, acc);
-  return acc;
-}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// Programmatic dependent launch: a kernel launched with programmatic stream serialization
+// may start before its predecessor on the stream has finished.  Everything it reads that
+// the predecessor writes must come after pdl_wait(); pdl_trigger() lets the successor
+// start launching.  Both are no-ops for a kernel launched without the attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 __device__ __forceinline__ float h2f_bits(uint16_t h) { return __half2float(__ushort_as_half(h)); }
 

@@ -9,10 +9,11 @@ namespace lrs {
 
 enum GemvEpi { EPI_STORE = 0, EPI_RESID = 1, EPI_SWIGLU = 2, EPI_QKV = 3 };
 
-// Device int8 block-32 matrix: q [N][Kp] int8, s [N][Kp/32] fp16 bits, Kp = K rounded up to 32
-// (the padding columns hold q = 0).  Row order is the device order chosen at import.
+// Device int8 block-32 matrix: q [N][Kp] stored biased (byte = q + 128), s [N][Kp/32] fp16 bits,
+// Kp = K rounded up to 32 (the padding columns face zero inputs).  Row order is the device
+// order chosen at import.
 struct DevQ8 {
-  int8_t* q = nullptr;
+  uint8_t* q = nullptr;
   uint16_t* s = nullptr;
   int N = 0, K = 0, Kp = 0;
 };
@@ -57,7 +58,7 @@ struct AttnArgs {
   const int* seq = nullptr;      // [ntok]
   const int* pos = nullptr;      // [ntok]; token t attends to positions 0..pos[t]
   float* out = nullptr;          // [ntok][Hq][D]
-  float* part_o = nullptr;       // scratch [ntok][Hq][n_chunks][D]
+  float* part_o = nullptr;       // scratch [ntok][Hkv][n_chunks][Hq/Hkv][D]
   float2* part_ml = nullptr;     // scratch [ntok][Hq][n_chunks] (running max, sum)
   int* counters = nullptr;       // scratch [ntok][Hkv], zero between launches (the kernel re-zeroes)
   int ntok = 0, Hq = 0, Hkv = 0, D = 0, max_len = 0, n_chunks = 1;
@@ -65,8 +66,15 @@ struct AttnArgs {
 };
 
 int sm_count();
+// Sets kernel attributes and records launch limits; call once per process before any
+// launch, outside stream capture.
+cudaError_t prepare_kernels();
+// Programmatic dependent launch of the stage kernels (on by default).
+void set_pdl(bool on);
+bool pdl_enabled();
 cudaError_t launch_gemv(const GemvArgs& a, cudaStream_t st);
 cudaError_t launch_attn_decode(const AttnArgs& a, cudaStream_t st);
+constexpr int kAttnMaxChunks = 64;
 bool attn_decode_supported(int head_dim, int group);
 cudaError_t launch_embed(const DevQ8& table, const int* tok, int ntok, float* out, int ldo, cudaStream_t st);
 cudaError_t launch_final_norm(const float* x, int ldx, const float* gamma, float eps, int H, int ntok,

@@ -13,53 +13,148 @@
 #include <algorithm>
 #include <cfloat>
 #include <climits>
+#include <utility>
 
 #include "common.cuh"
 #include "kernels.cuh"
 
 namespace lrs {
 
-// ------------------------------------------------------------------------------------------
-// Dequant-fused GEMV.  A CTA of 256 threads owns a group of R consecutive device rows at a
-// time (grid-stride over groups).  Every thread streams 16 weight bytes per row per chunk
-// (one 128-bit load; 256 threads cover 4096 weights of a row per pass) and multiplies them
-// with 16 activations kept in shared memory; the fp16 block scale multiplies each 16-term
-// partial sum.  Warp shuffles, then a fixed-order sum over the 8 warps, give each row.
-// The input is read into shared memory once per pass of BT tokens, normalised on the way
-// when the RMSNorm prologue is on.  Shared memory holds the activations with an XOR swizzle
-// of the four float4 of every 16-float chunk, which makes the per-thread 64-byte reads
-// bank-conflict free.
+static bool g_pdl = true;
+void set_pdl(bool on) { g_pdl = on; }
+bool pdl_enabled() { return g_pdl; }
 
-constexpr int kGemvThreads = 256;
-
-__device__ __forceinline__ int swz(int k) {
-  const int c = k >> 4, j = (k >> 2) & 3;
-  return (c << 4) | ((j ^ ((c >> 1) & 3)) << 2) | (k & 3);
+// Every kernel of the stage chain is launched with programmatic stream serialization, so
+// it can start (and, for the GEMVs, begin streaming its weights) while its predecessor
+// drains; each kernel orders its reads of predecessor outputs after pdl_wait().
+template <typename... KArgs, typename... Args>
+static cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                            Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = g_pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
-template <int R, int BT>
-__global__ void __launch_bounds__(kGemvThreads) gemv_q8_kernel(const GemvArgs a) {
+// ------------------------------------------------------------------------------------------
+// Dequant-fused GEMV.
+//
+// Weights are stored biased, b = q + 128 in [1, 255] (one byte per weight), with one fp16
+// scale per block of 32 along K.  For 16 weights w_j = s * (b_j - 128) and inputs x_j:
+//   sum_j w_j x_j = s * (sum_j b_j x_j - 128 * X),   X = sum_j x_j (per 16-input chunk).
+// b_j is turned into a float without any arithmetic: the byte moved into an otherwise
+// zero word is the denormal b_j * 2^-149, exactly.  With inputs pre-scaled by 2^64 the
+// products b_j * x_j * 2^-85 are normal floats, so one FFMA per weight accumulates them
+// (IEEE denormal operands, no flush-to-zero); the chunk sum is rescaled by 2^85 (exact) and
+// corrected by -128 X in one FFMA, then multiplied by the block scale.  Per weight byte:
+// one byte extract + one FFMA.
+//
+// Work split: each warp owns R consecutive rows at a time (grid-stride over row groups of
+// the whole grid), its lanes stream 16 bytes per row per chunk with U chunks in flight
+// per row, and reduce with warp shuffles only -- no block barrier in the main loop.  The
+// first batch of weights is requested before waiting for the predecessor kernel.  The
+// CTA's shared memory holds the (normalised, scaled) input once per pass of BT tokens,
+// copied in with cp.async, and its chunk sums; an XOR swizzle of the four float4 of each
+// 16-float chunk keeps the lanes' 64-byte reads bank-conflict free.
+
+constexpr int kGemvThreads = 256;
+constexpr size_t kGemvSmemBudget = 200 * 1024;
+constexpr float kXScale = 18446744073709551616.0f;        // 2^64
+constexpr float kPScale = 38685626227668133590597632.0f;  // 2^85
+
+// sum_j b_j * x'_j * 2^-149 over the 16 biased weight bytes of w (see above).
+__device__ __forceinline__ float dot16_u8(const uint4 w, const float4 x0, const float4 x1, const float4 x2,
+                                          const float4 x3) {
+  float acc = __uint_as_float(w.x & 0xFFu) * x0.x;
+  acc = fmaf(__uint_as_float(__byte_perm(w.x, 0u, 0x4441)), x0.y, acc);
+  acc = fmaf(__uint_as_float(__byte_perm(w.x, 0u, 0x4442)), x0.z, acc);
+  acc = fmaf(__uint_as_float(w.x >> 24), x0.w, acc);
+  acc = fmaf(__uint_as_float(w.y & 0xFFu), x1.x, acc);
+  acc = fmaf(__uint_as_float(__byte_perm(w.y, 0u, 0x4441)), x1.y, acc);
+  acc = fmaf(__uint_as_float(__byte_perm(w.y, 0u, 0x4442)), x1.z, acc);
+  acc = fmaf(__uint_as_float(w.y >> 24), x1.w, acc);
+  acc = fmaf(__uint_as_float(w.z & 0xFFu), x2.x, acc);
+  acc = fmaf(__uint_as_float(__byte_perm(w.z, 0u, 0x4441)), x2.y, acc);
+  acc = fmaf(__uint_as_float(__byte_perm(w.z, 0u, 0x4442)), x2.z, acc);
+  acc = fmaf(__uint_as_float(w.z >> 24), x2.w, acc);
+  acc = fmaf(__uint_as_float(w.w & 0xFFu), x3.x, acc);
+  acc = fmaf(__uint_as_float(__byte_perm(w.w, 0u, 0x4441)), x3.y, acc);
+  acc = fmaf(__uint_as_float(__byte_perm(w.w, 0u, 0x4442)), x3.z, acc);
+  acc = fmaf(__uint_as_float(w.w >> 24), x3.w, acc);
+  return acc;
+}
+
+template <int R, int U, int BT>
+__global__ void __launch_bounds__(kGemvThreads, BT == 1 ? 3 : 2) gemv_q8_kernel(const GemvArgs a) {
   extern __shared__ __align__(16) float smem[];
   const int Kp = a.w.Kp, K = a.w.K, N = a.w.N;
-  float* xs = smem;                  // [BT][Kp], swizzled
-  float* red = xs + BT * Kp;         // [8][R*BT]
-  float* yv = red + 8 * R * BT;      // [R*BT]
-  float* nrm = yv + R * BT;          // [8]
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nchunk = Kp >> 4, nblk = Kp >> 5;
+  float* xs = smem;                  // [BT][Kp] inputs * 2^64, swizzled
+  float* xc = xs + BT * Kp;          // [BT][nchunk] chunk sums of the inputs
+  float* nrm = xc + BT * nchunk;     // [8]
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int ngroups = (N + R - 1) / R;
+  const int gwarp = blockIdx.x * (kGemvThreads / 32) + warp, nwarps = gridDim.x * (kGemvThreads / 32);
+
+  uint4 w[U][R];
+  float sc[U][R];
+  auto load_batch = [&](int row0, int cb) {
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int c = cb + 32 * u + lane;
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const int row = row0 + r;
+        if (c < nchunk && row < N) {
+          w[u][r] = ld_stream_u4(a.w.q + (size_t)row * Kp + (size_t)c * 16);
+          sc[u][r] = h2f_bits(ld_stream_u16(a.w.s + (size_t)row * nblk + (c >> 1)));
+        } else {
+          w[u][r] = make_uint4(0u, 0u, 0u, 0u);
+          sc[u][r] = 0.f;
+        }
+      }
+    }
+  };
+  // The weights do not depend on the predecessor kernel: fetch this warp's first batch
+  // before waiting for it (single-pass launches only).
+  pdl_trigger();
+  bool prefetched = false;
+  if (a.ntok <= BT && gwarp < ngroups) {
+    load_batch(gwarp * R, 0);
+    prefetched = true;
+  }
+  pdl_wait();
 
   for (int t0 = 0; t0 < a.ntok; t0 += BT) {
     const int nt = min(BT, a.ntok - t0);
     __syncthreads();
+    // 1. raw inputs -> shared memory, every copy in flight at once
+    const int k4 = K >> 2;
+    for (int b = 0; b < nt; ++b) {
+      const float* xr = a.x + (size_t)(a.x_rows ? a.x_rows[t0 + b] : (t0 + b)) * a.ldx;
+      for (int i = tid; i < k4; i += kGemvThreads) cp_async16(xs + b * Kp + 4 * i, xr + 4 * i);
+      for (int k = 4 * k4 + tid; k < K; k += kGemvThreads) xs[b * Kp + k] = xr[k];
+    }
+    cp_async_wait_all();
+    for (int b = 0; b < BT; ++b)
+      for (int k = (b < nt ? K : 0) + tid; k < Kp; k += kGemvThreads) xs[b * Kp + k] = 0.f;
+    __syncthreads();
+    // 2. RMSNorm scale per token (fixed reduction order)
+    float rinv[BT];
+#pragma unroll
     for (int b = 0; b < BT; ++b) {
-      const float* xr = nullptr;
-      if (b < nt) xr = a.x + (size_t)(a.x_rows ? a.x_rows[t0 + b] : (t0 + b)) * a.ldx;
-      float rinv = 1.0f;
-      if (a.gamma && xr) {
+      rinv[b] = 1.0f;
+      if (a.gamma && b < nt) {
         float ss = 0.f;
         for (int k = tid; k < K; k += kGemvThreads) {
-          const float v = xr[k];
+          const float v = xs[b * Kp + k];
           ss = fmaf(v, v, ss);
         }
         ss = warp_sum(ss);
@@ -67,19 +162,43 @@ __global__ void __launch_bounds__(kGemvThreads) gemv_q8_kernel(const GemvArgs a)
         __syncthreads();
         float tot = 0.f;
 #pragma unroll
-        for (int w = 0; w < 8; ++w) tot += nrm[w];
-        rinv = 1.0f / sqrtf(tot / (float)K + a.eps);
+        for (int w8 = 0; w8 < 8; ++w8) tot += nrm[w8];
+        rinv[b] = 1.0f / sqrtf(tot / (float)K + a.eps);
         __syncthreads();
       }
-      for (int k = tid; k < Kp; k += kGemvThreads) {
-        float v = 0.f;
-        if (xr && k < K) v = a.gamma ? xr[k] * rinv * a.gamma[k] : xr[k];
-        xs[b * Kp + swz(k)] = v;
+    }
+    // 3. in place, one thread per 16-input chunk: normalise, scale by 2^64, swizzle, chunk sum
+    for (int i = tid; i < BT * nchunk; i += kGemvThreads) {
+      const int b = i / nchunk, c = i - b * nchunk;
+      float* xp = xs + b * Kp + c * 16;
+      float v[16];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float4 t4 = reinterpret_cast<const float4*>(xp)[j];
+        v[4 * j] = t4.x;
+        v[4 * j + 1] = t4.y;
+        v[4 * j + 2] = t4.z;
+        v[4 * j + 3] = t4.w;
       }
+      float sum = 0.f;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int k = c * 16 + j;
+        float h = v[j];
+        if (a.gamma) h = (k < K) ? h * rinv[b] * a.gamma[k] : 0.f;
+        v[j] = h;
+        sum += h;
+      }
+      const int sw = (c >> 1) & 3;
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        reinterpret_cast<float4*>(xp)[j ^ sw] =
+            make_float4(v[4 * j] * kXScale, v[4 * j + 1] * kXScale, v[4 * j + 2] * kXScale, v[4 * j + 3] * kXScale);
+      xc[i] = sum;
     }
     __syncthreads();
 
-    for (int g = blockIdx.x; g < ngroups; g += gridDim.x) {
+    for (int g = gwarp; g < ngroups; g += nwarps) {
       const int row0 = g * R;
       float acc[R][BT];
 #pragma unroll
@@ -87,278 +206,324 @@ __global__ void __launch_bounds__(kGemvThreads) gemv_q8_kernel(const GemvArgs a)
 #pragma unroll
         for (int b = 0; b < BT; ++b) acc[r][b] = 0.f;
 
-      for (int c = tid; c < nchunk; c += kGemvThreads) {
-        uint4 w[R];
-        float sc[R];
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-          const int row = row0 + r;
-          if (row < N) {
-            w[r] = ld_stream_u4(a.w.q + (size_t)row * Kp + (size_t)c * 16);
-            sc[r] = h2f_bits(ld_stream_u16(a.w.s + (size_t)row * nblk + (c >> 1)));
-          } else {
-            w[r] = make_uint4(0u, 0u, 0u, 0u);
-            sc[r] = 0.f;
-          }
+      for (int cb = 0; cb < nchunk; cb += 32 * U) {
+        if (prefetched) {
+          prefetched = false;  // the first batch of the first task is already in registers
+        } else {
+          load_batch(row0, cb);
         }
-        const int sw = (c >> 1) & 3;
 #pragma unroll
-        for (int b = 0; b < BT; ++b) {
-          const float4* xp = reinterpret_cast<const float4*>(xs + b * Kp + c * 16);
-          const float4 x0 = xp[0 ^ sw], x1 = xp[1 ^ sw], x2 = xp[2 ^ sw], x3 = xp[3 ^ sw];
+        for (int u = 0; u < U; ++u) {
+          const int c = cb + 32 * u + lane;
+          if (c < nchunk) {
+            const int sw = (c >> 1) & 3;
 #pragma unroll
-          for (int r = 0; r < R; ++r) acc[r][b] = fmaf(sc[r], dot16_i8(w[r], x0, x1, x2, x3), acc[r][b]);
-        }
-      }
-
+            for (int b = 0; b < BT; ++b) {
+              const float4* xp = reinterpret_cast<const float4*>(xs + b * Kp + c * 16);
+              const float4 x0 = xp[0 ^ sw], x1 = xp[1 ^ sw], x2 = xp[2 ^ sw], x3 = xp[3 ^ sw];
+              const float corr = -128.0f * xc[b * nchunk + c];
 #pragma unroll
-      for (int r = 0; r < R; ++r)
-#pragma unroll
-        for (int b = 0; b < BT; ++b) {
-          const float v = warp_sum(acc[r][b]);
-          if (lane == 0) red[warp * (R * BT) + r * BT + b] = v;
-        }
-      __syncthreads();
-      if (tid < R * BT) {
-        float y = 0.f;
-#pragma unroll
-        for (int w = 0; w < 8; ++w) y += red[w * (R * BT) + tid];
-        yv[tid] = y;
-      }
-      __syncthreads();
-
-      if (a.epi == EPI_STORE || a.epi == EPI_RESID) {
-        if (tid < R * BT) {
-          const int r = tid / BT, b = tid % BT, row = row0 + r;
-          if (row < N && b < nt) {
-            const size_t t = (size_t)(t0 + b);
-            float y = yv[tid];
-            if (a.epi == EPI_RESID) y = __fadd_rn(a.resid[t * a.ldr + row], y);
-            a.out[t * a.ldo + row] = y;
-          }
-        }
-      } else if (tid < (R / 2) * BT) {
-        const int j = tid / BT, b = tid % BT, row = row0 + 2 * j;
-        if (row < N && b < nt) {
-          const size_t t = (size_t)(t0 + b);
-          const float y0 = yv[(2 * j) * BT + b], y1 = yv[(2 * j + 1) * BT + b];
-          if (a.epi == EPI_SWIGLU) {
-            a.out[t * a.ldo + (row >> 1)] = silu(y0) * y1;
-          } else {  // EPI_QKV
-            const int hd = a.head_dim >> 1, P = row >> 1, head = P / hd, i = P - head * hd;
-            const int p = a.pos[t];
-            if (head < a.n_q_heads) {
-              const float2 cs = a.rope[(size_t)p * hd + i];
-              float* qo = a.qout + (t * a.n_q_heads + head) * a.head_dim;
-              qo[i] = y0 * cs.x - y1 * cs.y;
-              qo[i + hd] = y1 * cs.x + y0 * cs.y;
-            } else {
-              const bool is_k = head < a.n_q_heads + a.n_kv_heads;
-              const int kvh = head - a.n_q_heads - (is_k ? 0 : a.n_kv_heads);
-              const size_t base = (((size_t)a.seq[t] * a.n_kv_heads + kvh) * a.max_len + p) * a.head_dim;
-              if (is_k) {
-                const float2 cs = a.rope[(size_t)p * hd + i];
-                a.kc[base + i] = __float2half_rn(y0 * cs.x - y1 * cs.y);
-                a.kc[base + i + hd] = __float2half_rn(y1 * cs.x + y0 * cs.y);
-              } else {
-                a.vc[base + i] = __float2half_rn(y0);
-                a.vc[base + i + hd] = __float2half_rn(y1);
+              for (int r = 0; r < R; ++r) {
+                const float t = fmaf(dot16_u8(w[u][r], x0, x1, x2, x3), kPScale, corr);
+                acc[r][b] = fmaf(sc[u][r], t, acc[r][b]);
               }
             }
           }
         }
       }
-      __syncthreads();
+#pragma unroll
+      for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int b = 0; b < BT; ++b) acc[r][b] = warp_sum(acc[r][b]);
+
+      // epilogue: lane i takes value i (rows) or pair i (row pairs)
+      if (a.epi == EPI_STORE || a.epi == EPI_RESID) {
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+          for (int b = 0; b < BT; ++b) {
+            const int row = row0 + r;
+            if (lane == r * BT + b && row < N && b < nt) {
+              const size_t t = (size_t)(t0 + b);
+              float y = acc[r][b];
+              if (a.epi == EPI_RESID) y = __fadd_rn(a.resid[t * a.ldr + row], y);
+              a.out[t * a.ldo + row] = y;
+            }
+          }
+      } else {
+#pragma unroll
+        for (int j = 0; j < R / 2; ++j)
+#pragma unroll
+          for (int b = 0; b < BT; ++b) {
+            const int row = row0 + 2 * j;
+            if (lane != j * BT + b || row >= N || b >= nt) continue;
+            const size_t t = (size_t)(t0 + b);
+            const float y0 = acc[2 * j][b], y1 = acc[2 * j + 1][b];
+            if (a.epi == EPI_SWIGLU) {
+              a.out[t * a.ldo + (row >> 1)] = silu(y0) * y1;
+            } else {  // EPI_QKV
+              const int hd = a.head_dim >> 1, P = row >> 1, head = P / hd, i = P - head * hd;
+              const int p = a.pos[t];
+              if (head < a.n_q_heads) {
+                const float2 cs = a.rope[(size_t)p * hd + i];
+                float* qo = a.qout + (t * a.n_q_heads + head) * a.head_dim;
+                qo[i] = y0 * cs.x - y1 * cs.y;
+                qo[i + hd] = y1 * cs.x + y0 * cs.y;
+              } else {
+                const bool is_k = head < a.n_q_heads + a.n_kv_heads;
+                const int kvh = head - a.n_q_heads - (is_k ? 0 : a.n_kv_heads);
+                const size_t base = (((size_t)a.seq[t] * a.n_kv_heads + kvh) * a.max_len + p) * a.head_dim;
+                if (is_k) {
+                  const float2 cs = a.rope[(size_t)p * hd + i];
+                  a.kc[base + i] = __float2half_rn(y0 * cs.x - y1 * cs.y);
+                  a.kc[base + i + hd] = __float2half_rn(y1 * cs.x + y0 * cs.y);
+                } else {
+                  a.vc[base + i] = __float2half_rn(y0);
+                  a.vc[base + i + hd] = __float2half_rn(y1);
+                }
+              }
+            }
+          }
+      }
     }
   }
 }
 
-template <int R, int BT>
+template <int BT>
 static size_t gemv_smem(int Kp) {
-  return sizeof(float) * ((size_t)BT * Kp + 8 * R * BT + R * BT + 8);
+  return sizeof(float) * ((size_t)BT * Kp + (size_t)BT * (Kp / 16) + 8);
 }
 
-template <int R, int BT>
+// Launch attributes are fixed once, outside any stream capture (prepare_kernels); the
+// launch itself only computes the grid from the recorded register count.
+template <int R, int U, int BT>
+struct GemvInfo {
+  static int regs;
+};
+template <int R, int U, int BT>
+int GemvInfo<R, U, BT>::regs = 0;
+
+template <int R, int U, int BT>
+static cudaError_t prepare_gemv() {
+  cudaError_t e = cudaFuncSetAttribute(gemv_q8_kernel<R, U, BT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)kGemvSmemBudget + 4096);
+  if (e != cudaSuccess) return e;
+  cudaFuncAttributes fa;
+  e = cudaFuncGetAttributes(&fa, gemv_q8_kernel<R, U, BT>);
+  if (e != cudaSuccess) return e;
+  GemvInfo<R, U, BT>::regs = fa.numRegs;
+  return cudaSuccess;
+}
+
+// Resident CTAs per SM from the per-SM limits (threads, registers, shared memory).
+static int occupancy(int regs, int threads, size_t smem) {
+  const int by_threads = 2048 / threads;
+  const int regs_rounded = (regs + 7) / 8 * 8;
+  const int by_regs = std::max(1, 65536 / (regs_rounded * threads));
+  const int by_smem = std::max(1, (int)((228 * 1024) / (smem + 1024)));
+  return std::max(1, std::min(by_threads, std::min(by_regs, by_smem)));
+}
+
+template <int R, int U, int BT>
 static cudaError_t launch_gemv_t(const GemvArgs& a, cudaStream_t st) {
-  // occupancy per shared-memory size, computed once per size (host-side only)
-  static size_t cached_smem[16];
-  static int cached_occ[16];
-  static int n_cached = 0;
-  static bool attr_set = false;
-  const size_t smem = gemv_smem<R, BT>(a.w.Kp);
-  cudaError_t e = cudaSuccess;
-  if (!attr_set) {
-    e = cudaFuncSetAttribute(gemv_q8_kernel<R, BT>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024 + 1024);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
-  int occ = -1;
-  for (int i = 0; i < n_cached; ++i)
-    if (cached_smem[i] == smem) occ = cached_occ[i];
-  if (occ < 0) {
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, gemv_q8_kernel<R, BT>, kGemvThreads, smem);
-    if (e != cudaSuccess) return e;
-    if (n_cached < 16) {
-      cached_smem[n_cached] = smem;
-      cached_occ[n_cached] = occ;
-      ++n_cached;
-    }
-  }
-  if (occ < 1) return cudaErrorInvalidConfiguration;
+  if (GemvInfo<R, U, BT>::regs == 0) return cudaErrorNotReady;  // prepare_kernels() was not called
+  const size_t smem = gemv_smem<BT>(a.w.Kp);
+  int occ = occupancy(GemvInfo<R, U, BT>::regs, kGemvThreads, smem);
+  if (g_pdl && occ > 2) occ -= 1;  // leave one CTA slot per SM for the successor to prefetch into
   const int ngroups = (a.w.N + R - 1) / R;
-  const int grid = std::max(1, std::min(ngroups, sm_count() * occ));
-  gemv_q8_kernel<R, BT><<<grid, kGemvThreads, smem, st>>>(a);
-  return cudaGetLastError();
+  const int warps_per_cta = kGemvThreads / 32;
+  const int grid = std::max(1, std::min((ngroups + warps_per_cta - 1) / warps_per_cta, sm_count() * occ));
+  return launch_k(gemv_q8_kernel<R, U, BT>, dim3(grid), dim3(kGemvThreads), smem, st, a);
 }
 
 cudaError_t launch_gemv(const GemvArgs& a, cudaStream_t st) {
   if (a.ntok <= 0 || a.w.N <= 0) return cudaSuccess;
-  const size_t budget = 200 * 1024;
-  if (a.ntok >= 4 && gemv_smem<4, 4>(a.w.Kp) <= budget) return launch_gemv_t<4, 4>(a, st);
-  if (a.ntok >= 2 && gemv_smem<4, 2>(a.w.Kp) <= budget) return launch_gemv_t<4, 2>(a, st);
-  return launch_gemv_t<4, 1>(a, st);
+  const size_t budget = kGemvSmemBudget;
+  if (a.ntok >= 4 && gemv_smem<4>(a.w.Kp) <= budget) return launch_gemv_t<2, 2, 4>(a, st);
+  if (a.ntok >= 2 && gemv_smem<2>(a.w.Kp) <= budget) return launch_gemv_t<2, 4, 2>(a, st);
+  return launch_gemv_t<2, 4, 1>(a, st);
 }
 
 // ------------------------------------------------------------------------------------------
 // Split-K GQA decode attention.  Grid (n_chunks, Hkv, ntok), 128 threads.  The CTA takes the
 // G = Hq / Hkv query heads that share KV head blockIdx.y and the positions of its chunk of
-// 0..pos[t]; it walks the chunk in tiles of 128 positions (one per thread for the scores)
-// with a running max / sum, then writes its partial (unnormalised output, max, sum).  The
+// 0..pos[t].  It walks the chunk in tiles of TP positions: all threads first copy the K and
+// V rows of the tile into shared memory with cp.async (every copy of the tile in flight at
+// once), then compute the scores, a running max / sum per head, and the probability-
+// weighted V rows.  The chunk's partial (unnormalised output, max, sum) goes to scratch; the
 // last CTA of a (token, kv head) to finish -- found with one integer atomic, no waiting --
-// merges the chunks in chunk order.
+// merges the chunks in chunk order, reading each partial with coalesced, batched loads.
+
+constexpr int kAttnThreads = 128;
+constexpr int kAttnTile = 64;
 
 template <int D, int G>
-__global__ void __launch_bounds__(128) attn_decode_kernel(const AttnArgs a) {
-  constexpr int NT = 128;
-  constexpr int TPR = D / 4;       // threads per V row (4 dims each)
-  constexpr int NPG = NT / TPR;    // position groups in the PV product
-  __shared__ __align__(16) float qs[G][D];
-  __shared__ float ps[G][NT];
-  __shared__ float red[4][G];
-  __shared__ __align__(16) float ored[NPG][G][D];
+struct AttnSmem {
+  static constexpr int KROW = D + 8;  // halves per K/V row in shared memory (16-byte pad)
+  static constexpr int TPR = D / 4;   // threads per V row in the PV product (4 dims each)
+  static constexpr int NPG = kAttnThreads / TPR;
+  static constexpr size_t kv = (size_t)kAttnTile * KROW * 2;  // bytes of one K or V tile
+  static constexpr size_t q = (size_t)G * D * 4;
+  static constexpr size_t p = (size_t)G * kAttnTile * 4;
+  static constexpr size_t o = (size_t)NPG * G * D * 4;
+  static constexpr size_t w = (size_t)kAttnMaxChunks * G * 4;
+  static constexpr size_t stats = (size_t)4 * G * 4;
+  static constexpr size_t total = 2 * kv + q + p + o + w + stats;
+};
+
+template <int D, int G>
+__global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const AttnArgs a) {
+  using S = AttnSmem<D, G>;
+  constexpr int NT = kAttnThreads, TP = kAttnTile, KROW = S::KROW, TPR = S::TPR, NPG = S::NPG;
+  extern __shared__ __align__(16) unsigned char sm_raw[];
+  __half* ks = reinterpret_cast<__half*>(sm_raw);
+  __half* vs = ks + TP * KROW;
+  float* qs = reinterpret_cast<float*>(sm_raw + 2 * S::kv);
+  float* ps = qs + G * D;                   // [G][TP]
+  float* ored = ps + G * TP;                // [NPG][G][D]
+  float* wts = ored + NPG * G * D;          // [n_chunks][G]
+  float* st_m = wts + kAttnMaxChunks * G;   // [G] running max
+  float* st_l = st_m + G;                   // [G] running sum
+  float* st_a = st_l + G;                   // [G] rescale of this tile
+  float* st_L = st_a + G;                   // [G] merged sum (merge phase)
   __shared__ int is_last;
 
   const int chunk = blockIdx.x, kvh = blockIdx.y, t = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  pdl_trigger();
+  pdl_wait();
   const int L = a.pos[t] + 1, sid = a.seq[t];
   const int clen = (L + a.n_chunks - 1) / a.n_chunks;
   const int c0 = min(L, chunk * clen), c1 = min(L, c0 + clen);
   const size_t head0 = (size_t)t * a.Hq + (size_t)kvh * G;
 
-  for (int i = tid; i < G * D; i += NT) qs[i / D][i % D] = a.q[head0 * D + i];
-  __syncthreads();
-
+  for (int i = tid; i < G * D / 4; i += NT)
+    reinterpret_cast<float4*>(qs)[i] = reinterpret_cast<const float4*>(a.q + head0 * D)[i];
+  if (tid < G) {
+    st_m[tid] = -INFINITY;
+    st_l[tid] = 0.f;
+  }
   const __half* kb = a.kc + ((size_t)sid * a.Hkv + kvh) * (size_t)a.max_len * D;
   const __half* vb = a.vc + ((size_t)sid * a.Hkv + kvh) * (size_t)a.max_len * D;
 
-  float m[G], l[G], o[G][4];
+  float o[G][4];
 #pragma unroll
-  for (int g = 0; g < G; ++g) {
-    m[g] = -INFINITY;
-    l[g] = 0.f;
+  for (int g = 0; g < G; ++g)
 #pragma unroll
     for (int e = 0; e < 4; ++e) o[g][e] = 0.f;
-  }
   const int d0 = (tid % TPR) * 4, pg = tid / TPR;
 
-  for (int p0 = c0; p0 < c1; p0 += NT) {
-    const int np = min(NT, c1 - p0);
-    float sc[G];
+  for (int p0 = c0; p0 < c1; p0 += TP) {
+    const int np = min(TP, c1 - p0);
+    __syncthreads();  // previous tile fully consumed (and q / stats initialised)
+    constexpr int PIECES = D / 8;  // 16-byte pieces per row
+    for (int i = tid; i < np * PIECES; i += NT) {
+      const int r = i / PIECES, c = i - r * PIECES;
+      cp_async16(ks + r * KROW + c * 8, kb + (size_t)(p0 + r) * D + c * 8);
+      cp_async16(vs + r * KROW + c * 8, vb + (size_t)(p0 + r) * D + c * 8);
+    }
+    cp_async_wait_all();
+    __syncthreads();
+    // scores: thread -> (position, heads g == hh mod (NT / TP))
+    {
+      constexpr int HSTEP = NT / TP;
+      constexpr int NH = (G + HSTEP - 1) / HSTEP;
+      const int pp = tid % TP, hh = tid / TP;
+      if (pp < np && hh < G) {
+        float sc[NH];
 #pragma unroll
-    for (int g = 0; g < G; ++g) sc[g] = -INFINITY;
-    if (tid < np) {
-#pragma unroll
-      for (int g = 0; g < G; ++g) sc[g] = 0.f;
-      const uint4* kr = reinterpret_cast<const uint4*>(kb + (size_t)(p0 + tid) * D);
+        for (int j = 0; j < NH; ++j) sc[j] = 0.f;
+        const __half* kr = ks + pp * KROW;
 #pragma unroll 4
-      for (int i = 0; i < D / 8; ++i) {
-        const uint4 kk = kr[i];
-        const float2 k01 = __half22float2(*reinterpret_cast<const __half2*>(&kk.x));
-        const float2 k23 = __half22float2(*reinterpret_cast<const __half2*>(&kk.y));
-        const float2 k45 = __half22float2(*reinterpret_cast<const __half2*>(&kk.z));
-        const float2 k67 = __half22float2(*reinterpret_cast<const __half2*>(&kk.w));
+        for (int i = 0; i < D / 8; ++i) {
+          const uint4 kk = *reinterpret_cast<const uint4*>(kr + 8 * i);
+          const float2 k01 = __half22float2(*reinterpret_cast<const __half2*>(&kk.x));
+          const float2 k23 = __half22float2(*reinterpret_cast<const __half2*>(&kk.y));
+          const float2 k45 = __half22float2(*reinterpret_cast<const __half2*>(&kk.z));
+          const float2 k67 = __half22float2(*reinterpret_cast<const __half2*>(&kk.w));
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-          const float4 qa = *reinterpret_cast<const float4*>(&qs[g][8 * i]);
-          const float4 qb = *reinterpret_cast<const float4*>(&qs[g][8 * i + 4]);
-          float s = sc[g];
-          s = fmaf(qa.x, k01.x, s);
-          s = fmaf(qa.y, k01.y, s);
-          s = fmaf(qa.z, k23.x, s);
-          s = fmaf(qa.w, k23.y, s);
-          s = fmaf(qb.x, k45.x, s);
-          s = fmaf(qb.y, k45.y, s);
-          s = fmaf(qb.z, k67.x, s);
-          s = fmaf(qb.w, k67.y, s);
-          sc[g] = s;
+          for (int j = 0; j < NH; ++j) {
+            const int g = hh + j * HSTEP;
+            if (g < G) {
+              const float4 qa = *reinterpret_cast<const float4*>(qs + g * D + 8 * i);
+              const float4 qb = *reinterpret_cast<const float4*>(qs + g * D + 8 * i + 4);
+              float s = sc[j];
+              s = fmaf(qa.x, k01.x, s);
+              s = fmaf(qa.y, k01.y, s);
+              s = fmaf(qa.z, k23.x, s);
+              s = fmaf(qa.w, k23.y, s);
+              s = fmaf(qb.x, k45.x, s);
+              s = fmaf(qb.y, k45.y, s);
+              s = fmaf(qb.z, k67.x, s);
+              s = fmaf(qb.w, k67.y, s);
+              sc[j] = s;
+            }
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < NH; ++j) {
+          const int g = hh + j * HSTEP;
+          if (g < G) ps[g * TP + pp] = sc[j] * a.scale;
         }
       }
-#pragma unroll
-      for (int g = 0; g < G; ++g) sc[g] *= a.scale;
-    }
-    // tile max per head
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      const float v = warp_max(sc[g]);
-      if (lane == 0) red[warp][g] = v;
     }
     __syncthreads();
-    float mnew[G], alpha[G];
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      const float mt = fmaxf(fmaxf(red[0][g], red[1][g]), fmaxf(red[2][g], red[3][g]));
-      mnew[g] = fmaxf(m[g], mt);
-      alpha[g] = (m[g] == -INFINITY) ? 0.f : expf(m[g] - mnew[g]);
-      const float e = (tid < np) ? expf(sc[g] - mnew[g]) : 0.f;
-      ps[g][tid] = e;
-      sc[g] = e;
+    // per head: tile max, probabilities, running (max, sum); warp w handles heads w, w + 4, ...
+    for (int g = warp; g < G; g += NT / 32) {
+      const float s0 = lane < np ? ps[g * TP + lane] : -INFINITY;
+      const float s1 = lane + 32 < np ? ps[g * TP + lane + 32] : -INFINITY;
+      const float mt = warp_max(fmaxf(s0, s1));
+      const float mold = st_m[g];
+      const float mnew = fmaxf(mold, mt);
+      const float e0 = lane < np ? expf(s0 - mnew) : 0.f;
+      const float e1 = lane + 32 < np ? expf(s1 - mnew) : 0.f;
+      ps[g * TP + lane] = e0;
+      ps[g * TP + lane + 32] = e1;
+      const float lt = warp_sum(e0 + e1);
+      if (lane == 0) {
+        const float alpha = (mold == -INFINITY) ? 0.f : expf(mold - mnew);
+        st_a[g] = alpha;
+        st_l[g] = st_l[g] * alpha + lt;
+        st_m[g] = mnew;
+      }
     }
     __syncthreads();
+    // PV: thread -> 4 dims of V, positions pg, pg + NPG, ...
 #pragma unroll
     for (int g = 0; g < G; ++g) {
-      const float v = warp_sum(sc[g]);
-      if (lane == 0) red[warp][g] = v;
-    }
-    __syncthreads();
+      const float al = st_a[g];
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-      const float lt = (red[0][g] + red[1][g]) + (red[2][g] + red[3][g]);
-      l[g] = l[g] * alpha[g] + lt;
-      m[g] = mnew[g];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) o[g][e] *= alpha[g];
+      for (int e = 0; e < 4; ++e) o[g][e] *= al;
     }
-    for (int p = pg; p < np; p += NPG) {
-      const uint2 vv = *reinterpret_cast<const uint2*>(vb + (size_t)(p0 + p) * D + d0);
+    for (int pp = pg; pp < np; pp += NPG) {
+      const uint2 vv = *reinterpret_cast<const uint2*>(vs + pp * KROW + d0);
       const float2 v01 = __half22float2(*reinterpret_cast<const __half2*>(&vv.x));
       const float2 v23 = __half22float2(*reinterpret_cast<const __half2*>(&vv.y));
 #pragma unroll
       for (int g = 0; g < G; ++g) {
-        const float w = ps[g][p];
+        const float w = ps[g * TP + pp];
         o[g][0] = fmaf(w, v01.x, o[g][0]);
         o[g][1] = fmaf(w, v01.y, o[g][1]);
         o[g][2] = fmaf(w, v23.x, o[g][2]);
         o[g][3] = fmaf(w, v23.y, o[g][3]);
       }
     }
-    __syncthreads();
   }
-
+  __syncthreads();
 #pragma unroll
   for (int g = 0; g < G; ++g)
 #pragma unroll
-    for (int e = 0; e < 4; ++e) ored[pg][g][d0 + e] = o[g][e];
+    for (int e = 0; e < 4; ++e) ored[(pg * G + g) * D + d0 + e] = o[g][e];
   __syncthreads();
+  // partial of this chunk: [t][kvh][chunk][G][D] and (max, sum) per head
+  float* po = a.part_o + (((size_t)t * a.Hkv + kvh) * a.n_chunks + chunk) * (G * D);
   for (int i = tid; i < G * D; i += NT) {
-    const int g = i / D, d = i % D;
     float s = 0.f;
 #pragma unroll
-    for (int q = 0; q < NPG; ++q) s += ored[q][g][d];
-    a.part_o[((head0 + g) * a.n_chunks + chunk) * D + d] = s;
+    for (int q2 = 0; q2 < NPG; ++q2) s += ored[q2 * G * D + i];
+    po[i] = s;
   }
-#pragma unroll
-  for (int g = 0; g < G; ++g)
-    if (tid == g) a.part_ml[(head0 + g) * a.n_chunks + chunk] = make_float2(m[g], l[g]);
+  if (tid < G) a.part_ml[(head0 + tid) * a.n_chunks + chunk] = make_float2(st_m[tid], st_l[tid]);
 
   __threadfence();
   __syncthreads();
@@ -369,22 +534,38 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(const AttnArgs a) {
   __syncthreads();
   if (!is_last) return;
   __threadfence();
-  for (int i = tid; i < G * D; i += NT) {
-    const int g = i / D, d = i % D;
-    const float2* ml = a.part_ml + (head0 + g) * a.n_chunks;
-    const float* po = a.part_o + (head0 + g) * a.n_chunks * D + d;
+  // merge: chunk weights e^(m_c - M) per head, then coalesced weighted sums in chunk order
+  const int nch = a.n_chunks;
+  float2* mls = reinterpret_cast<float2*>(ored);  // [G][nch] (max, sum), reusing the PV scratch
+  for (int i = tid; i < G * nch; i += NT) mls[i] = __ldcg(a.part_ml + head0 * nch + i);
+  __syncthreads();
+  if (tid < G) {
     float M = -INFINITY;
-    for (int c = 0; c < a.n_chunks; ++c) M = fmaxf(M, __ldcg(ml + c).x);
-    float Ls = 0.f, acc = 0.f;
-    for (int c = 0; c < a.n_chunks; ++c) {
-      const float2 mc = __ldcg(ml + c);
-      if (mc.y > 0.f) {
-        const float w = expf(mc.x - M);
-        Ls = fmaf(mc.y, w, Ls);
-        acc = fmaf(w, __ldcg(po + (size_t)c * D), acc);
-      }
+    for (int c = 0; c < nch; ++c) M = fmaxf(M, mls[tid * nch + c].x);
+    float Ls = 0.f;
+    for (int c = 0; c < nch; ++c) {
+      const float2 mc = mls[tid * nch + c];
+      const float w = mc.y > 0.f ? expf(mc.x - M) : 0.f;
+      wts[c * G + tid] = w;
+      Ls = fmaf(mc.y, w, Ls);
     }
-    a.out[(head0 + g) * D + d] = acc / Ls;
+    st_L[tid] = Ls;
+  }
+  __syncthreads();
+  const float* pbase = a.part_o + ((size_t)t * a.Hkv + kvh) * nch * (G * D);
+  for (int i = tid; i < G * D; i += NT) {
+    const int g = i / D;
+    float acc = 0.f;
+    int c = 0;
+    for (; c + 8 <= nch; c += 8) {
+      float v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = __ldcg(pbase + (size_t)(c + j) * (G * D) + i);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc = fmaf(wts[(c + j) * G + g], v[j], acc);
+    }
+    for (; c < nch; ++c) acc = fmaf(wts[c * G + g], __ldcg(pbase + (size_t)c * (G * D) + i), acc);
+    a.out[head0 * D + i] = acc / st_L[g];
   }
   if (tid == 0) a.counters[(size_t)t * a.Hkv + kvh] = 0;
 }
@@ -393,50 +574,65 @@ bool attn_decode_supported(int head_dim, int group) {
   return (head_dim == 64 || head_dim == 128) && (group == 1 || group == 2 || group == 4 || group == 8);
 }
 
+template <int D, int G>
+static cudaError_t prepare_attn() {
+  return cudaFuncSetAttribute(attn_decode_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)AttnSmem<D, G>::total);
+}
+
+template <int D, int G>
+static cudaError_t launch_attn_dg(const AttnArgs& a, cudaStream_t st) {
+  const dim3 grid(a.n_chunks, a.Hkv, a.ntok);
+  return launch_k(attn_decode_kernel<D, G>, grid, dim3(kAttnThreads), AttnSmem<D, G>::total, st, a);
+}
+
 template <int D>
 static cudaError_t launch_attn_d(const AttnArgs& a, cudaStream_t st) {
-  const dim3 grid(a.n_chunks, a.Hkv, a.ntok);
   switch (a.Hq / a.Hkv) {
-    case 1: attn_decode_kernel<D, 1><<<grid, 128, 0, st>>>(a); break;
-    case 2: attn_decode_kernel<D, 2><<<grid, 128, 0, st>>>(a); break;
-    case 4: attn_decode_kernel<D, 4><<<grid, 128, 0, st>>>(a); break;
-    case 8: attn_decode_kernel<D, 8><<<grid, 128, 0, st>>>(a); break;
+    case 1: return launch_attn_dg<D, 1>(a, st);
+    case 2: return launch_attn_dg<D, 2>(a, st);
+    case 4: return launch_attn_dg<D, 4>(a, st);
+    case 8: return launch_attn_dg<D, 8>(a, st);
     default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 
 cudaError_t launch_attn_decode(const AttnArgs& a, cudaStream_t st) {
   if (a.ntok <= 0) return cudaSuccess;
   if (!attn_decode_supported(a.D, a.Hq / a.Hkv) || a.Hq % a.Hkv) return cudaErrorInvalidValue;
-  if (a.n_chunks < 1 || a.n_chunks > 65535) return cudaErrorInvalidValue;
+  if (a.n_chunks < 1 || a.n_chunks > kAttnMaxChunks) return cudaErrorInvalidValue;
   return a.D == 64 ? launch_attn_d<64>(a, st) : launch_attn_d<128>(a, st);
 }
 
 // ------------------------------------------------------------------------------------------
-// Embedding row gather: x[t][k] = scale[tok][k/32] * q[tok][k] (exact in float32).
+// Embedding row gather: x[t][k] = scale[tok][k/32] * q[tok][k] (exact in float32).  The
+// table is stored biased like every weight matrix (byte = q + 128).
 
 __global__ void embed_kernel(const DevQ8 tab, const int* tok, float* out, int ldo) {
+  pdl_trigger();
+  pdl_wait();
   const int t = blockIdx.x, row = tok[t];
-  const int8_t* q = tab.q + (size_t)row * tab.Kp;
+  const uint8_t* q = tab.q + (size_t)row * tab.Kp;
   const uint16_t* s = tab.s + (size_t)row * (tab.Kp >> 5);
-  for (int k = threadIdx.x; k < tab.K; k += blockDim.x) out[(size_t)t * ldo + k] = h2f_bits(s[k >> 5]) * (float)q[k];
+  for (int k = threadIdx.x; k < tab.K; k += blockDim.x)
+    out[(size_t)t * ldo + k] = h2f_bits(s[k >> 5]) * (float)((int)q[k] - 128);
 }
 
 cudaError_t launch_embed(const DevQ8& table, const int* tok, int ntok, float* out, int ldo, cudaStream_t st) {
   if (ntok <= 0) return cudaSuccess;
-  embed_kernel<<<ntok, 256, 0, st>>>(table, tok, out, ldo);
-  return cudaGetLastError();
+  return launch_k(embed_kernel, dim3(ntok), dim3(256), 0, st, table, tok, out, ldo);
 }
 
 // ------------------------------------------------------------------------------------------
-// Final RMSNorm of the last stage: f = x / sqrt(mean(x^2) + eps) * gamma, written to
-// the stage's feature buffer and to the caller's hidden_out.  Same reduction order as the
-// GEMV prologue.
+// Final RMSNorm of the last stage: f = x / sqrt(mean(x^2) + eps) * gamma, written to the
+// stage's feature buffer and to the caller's hidden_out.  Same reduction order as the GEMV
+// prologue.
 
 __global__ void final_norm_kernel(const float* x, int ldx, const float* gamma, float eps, int H, float* feat,
                                   float* out, int ldo) {
   __shared__ float nrm[8];
+  pdl_trigger();
+  pdl_wait();
   const int t = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const float* xr = x + (size_t)t * ldx;
   float ss = 0.f;
@@ -461,8 +657,7 @@ __global__ void final_norm_kernel(const float* x, int ldx, const float* gamma, f
 cudaError_t launch_final_norm(const float* x, int ldx, const float* gamma, float eps, int H, int ntok, float* feat,
                               float* out, int ldo, cudaStream_t st) {
   if (ntok <= 0) return cudaSuccess;
-  final_norm_kernel<<<ntok, 256, 0, st>>>(x, ldx, gamma, eps, H, feat, out, ldo);
-  return cudaGetLastError();
+  return launch_k(final_norm_kernel, dim3(ntok), dim3(256), 0, st, x, ldx, gamma, eps, H, feat, out, ldo);
 }
 
 // ------------------------------------------------------------------------------------------
@@ -478,6 +673,8 @@ __device__ __forceinline__ void better(float& v, int& i, float v2, int i2) {
 __global__ void argmax_kernel(const float* logits, int V, int* out) {
   __shared__ float sv[32];
   __shared__ int si[32];
+  pdl_trigger();
+  pdl_wait();
   const int r = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const float* lg = logits + (size_t)r * V;
   float v = -INFINITY;
@@ -502,8 +699,7 @@ __global__ void argmax_kernel(const float* logits, int V, int* out) {
 
 cudaError_t launch_argmax(const float* logits, int V, int n_rows, int* out, cudaStream_t st) {
   if (n_rows <= 0) return cudaSuccess;
-  argmax_kernel<<<n_rows, 1024, 0, st>>>(logits, V, out);
-  return cudaGetLastError();
+  return launch_k(argmax_kernel, dim3(n_rows), dim3(1024), 0, st, logits, V, out);
 }
 
 // ------------------------------------------------------------------------------------------
@@ -511,6 +707,8 @@ cudaError_t launch_argmax(const float* logits, int V, int n_rows, int* out, cuda
 // on, and the step's greedy tokens are appended to the history.
 
 __global__ void advance_kernel(int* pos, const int* tok, int* hist, int* step, int batch) {
+  pdl_trigger();
+  pdl_wait();
   const int i = threadIdx.x;
   const int s = *step;
   if (i < batch) {
@@ -522,8 +720,27 @@ __global__ void advance_kernel(int* pos, const int* tok, int* hist, int* step, i
 }
 
 cudaError_t launch_advance(int* pos, const int* tok, int* hist, int* step, int batch, cudaStream_t st) {
-  advance_kernel<<<1, std::max(32, ((batch + 31) / 32) * 32), 0, st>>>(pos, tok, hist, step, batch);
-  return cudaGetLastError();
+  return launch_k(advance_kernel, dim3(1), dim3(std::max(32, ((batch + 31) / 32) * 32)), 0, st, pos, tok, hist,
+                  step, batch);
+}
+
+cudaError_t prepare_kernels() {
+  static cudaError_t done = cudaErrorNotReady;
+  if (done == cudaSuccess) return done;
+  sm_count();
+  cudaError_t e = prepare_gemv<2, 4, 1>();
+  if (e == cudaSuccess) e = prepare_gemv<2, 4, 2>();
+  if (e == cudaSuccess) e = prepare_gemv<2, 2, 4>();
+  if (e == cudaSuccess) e = prepare_attn<64, 1>();
+  if (e == cudaSuccess) e = prepare_attn<64, 2>();
+  if (e == cudaSuccess) e = prepare_attn<64, 4>();
+  if (e == cudaSuccess) e = prepare_attn<64, 8>();
+  if (e == cudaSuccess) e = prepare_attn<128, 1>();
+  if (e == cudaSuccess) e = prepare_attn<128, 2>();
+  if (e == cudaSuccess) e = prepare_attn<128, 4>();
+  if (e == cudaSuccess) e = prepare_attn<128, 8>();
+  done = e;
+  return e;
 }
 
 int sm_count() {

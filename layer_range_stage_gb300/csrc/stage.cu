@@ -14,6 +14,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <new>
@@ -27,7 +28,7 @@ using lrs::DevQ8;
 
 namespace {
 
-constexpr int kMaxChunks = 64;
+constexpr int kMaxChunks = lrs::kAttnMaxChunks;
 constexpr size_t kAlign = 256;
 
 inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -122,6 +123,8 @@ bool cfg_valid(const stage_model_cfg* c, stage_layer_range r, std::string* why) 
       c->vocab <= 0)
     return bad("non-positive model dimension");
   if (c->n_q_heads % c->n_kv_heads) return bad("n_q_heads must be a multiple of n_kv_heads");
+  // every GEMV input row is staged with 16-byte copies
+  if (c->hidden % 4 || c->ffn % 4 || c->expert_ffn % 4) return bad("hidden, ffn and expert_ffn must be multiples of 4");
   if (!lrs::attn_decode_supported(c->head_dim, c->n_q_heads / c->n_kv_heads))
     return bad("unsupported head_dim / GQA group (head_dim 64 or 128; group 1, 2, 4 or 8)");
   const bool moe = c->n_experts > 0;
@@ -194,6 +197,11 @@ struct BusyGuard {
   }
 };
 
+// Device weights are stored biased: byte = q + 128 (two's complement int8 xor 0x80).
+void bias_bytes(std::vector<uint8_t>& q) {
+  for (auto& b : q) b ^= 0x80u;
+}
+
 // Copy rows of a host q8 matrix into device row order: dst row i <- src row perm(i).
 template <class Perm>
 int upload_q8(stage* st, const stage_q8& src, const DevQ8& dst, int64_t src_rows, Perm perm, const char* name) {
@@ -202,13 +210,14 @@ int upload_q8(stage* st, const stage_q8& src, const DevQ8& dst, int64_t src_rows
     return set_err(st, STAGE_E_INVALID, "%s: shape [%lld x %lld], expected [%lld x %d]", name, (long long)src.rows,
                    (long long)src.cols, (long long)src_rows, dst.K);
   const int nb_src = (dst.K + 31) / 32, nb = dst.Kp / 32;
-  std::vector<int8_t> q((size_t)dst.N * dst.Kp, 0);
+  std::vector<uint8_t> q((size_t)dst.N * dst.Kp, 0);
   std::vector<uint16_t> s((size_t)dst.N * nb, 0);
   for (int i = 0; i < dst.N; ++i) {
     const int64_t r = perm(i);
     std::memcpy(&q[(size_t)i * dst.Kp], src.q + r * src.cols, (size_t)dst.K);
     std::memcpy(&s[(size_t)i * nb], src.scale + r * nb_src, (size_t)nb_src * 2);
   }
+  bias_bytes(q);
   cudaError_t e = cudaMemcpy(dst.q, q.data(), q.size(), cudaMemcpyHostToDevice);
   if (e == cudaSuccess) e = cudaMemcpy(dst.s, s.data(), s.size() * 2, cudaMemcpyHostToDevice);
   if (e != cudaSuccess) return cuda_err(st, e, name);
@@ -273,7 +282,7 @@ int load_layer(stage* st, int gl, const stage_layer_w* w) {
       gu.q = L.egu.q + (size_t)e * 2 * EF * L.egu.Kp;
       gu.s = L.egu.s + (size_t)e * 2 * EF * (L.egu.Kp / 32);
       // even rows from gate, odd rows from up
-      std::vector<int8_t> q((size_t)2 * EF * gu.Kp, 0);
+      std::vector<uint8_t> q((size_t)2 * EF * gu.Kp, 0);
       std::vector<uint16_t> s((size_t)2 * EF * (gu.Kp / 32), 0);
       const stage_q8* srcs[2] = {&w->e_gate[e], &w->e_up[e]};
       for (int which = 0; which < 2; ++which) {
@@ -286,6 +295,7 @@ int load_layer(stage* st, int gl, const stage_layer_w* w) {
           std::memcpy(&s[(size_t)(2 * j + which) * nb], m.scale + (int64_t)j * nb_src, (size_t)nb_src * 2);
         }
       }
+      bias_bytes(q);
       cudaError_t ce = cudaMemcpy(gu.q, q.data(), q.size(), cudaMemcpyHostToDevice);
       if (ce == cudaSuccess) ce = cudaMemcpy(gu.s, s.data(), s.size() * 2, cudaMemcpyHostToDevice);
       if (ce != cudaSuccess) return cuda_err(st, ce, "expert gate/up");
@@ -293,7 +303,7 @@ int load_layer(stage* st, int gl, const stage_layer_w* w) {
     }
   } else {
     const int F = c.ffn;
-    std::vector<int8_t> q((size_t)2 * F * L.wgu.Kp, 0);
+    std::vector<uint8_t> q((size_t)2 * F * L.wgu.Kp, 0);
     std::vector<uint16_t> s((size_t)2 * F * (L.wgu.Kp / 32), 0);
     const stage_q8* srcs[2] = {&w->w_gate, &w->w_up};
     const int nb_src = (H + 31) / 32, nb = L.wgu.Kp / 32;
@@ -306,6 +316,7 @@ int load_layer(stage* st, int gl, const stage_layer_w* w) {
         std::memcpy(&s[(size_t)(2 * j + which) * nb], m.scale + (int64_t)j * nb_src, (size_t)nb_src * 2);
       }
     }
+    bias_bytes(q);
     cudaError_t ce = cudaMemcpy(L.wgu.q, q.data(), q.size(), cudaMemcpyHostToDevice);
     if (ce == cudaSuccess) ce = cudaMemcpy(L.wgu.s, s.data(), s.size() * 2, cudaMemcpyHostToDevice);
     if (ce != cudaSuccess) return cuda_err(st, ce, "gate/up");
@@ -334,10 +345,13 @@ bool weights_ready(stage* st) {
   return true;
 }
 
+// Split-K factor of decode attention: enough CTAs for two per SM, chunks of >= 32 positions,
+// bounded by the partial-result scratch.
 int attn_chunks(const stage* st, int ntok, int max_len_in_call) {
   const size_t pairs = std::max((size_t)st->cfg.max_seqs * kMaxChunks, (size_t)st->cfg.max_tokens * 4);
-  int n = (max_len_in_call + 127) / 128;
-  const int fill = std::max(1, 2 * lrs::sm_count() / std::max(1, ntok * st->cfg.n_kv_heads));
+  int n = (max_len_in_call + 31) / 32;
+  const int work = std::max(1, ntok * st->cfg.n_kv_heads);
+  const int fill = std::max(1, (2 * lrs::sm_count() + work - 1) / work);
   n = std::min(n, fill);
   n = std::min<int>(n, (int)std::min<size_t>(kMaxChunks, pairs / (size_t)ntok));
   return std::max(1, n);
@@ -346,10 +360,9 @@ int attn_chunks(const stage* st, int ntok, int max_len_in_call) {
 // The per-stage launch chain.  Inputs are device arrays; hout receives the residual stream
 // (the final features on the last stage).
 int forward_dev(stage* st, int n, const int* d_seq, const int* d_pos, const int* d_tok, const float* hin, float* hout,
-                int n_chunks) {
+                int n_chunks, cudaStream_t s) {
   const stage_model_cfg& c = st->cfg;
   const int H = c.hidden, D = c.head_dim, Hq = c.n_q_heads, Hkv = c.n_kv_heads;
-  cudaStream_t s = st->stream;
   cudaError_t e;
   if (st->first && (e = lrs::launch_embed(st->embed, d_tok, n, hout, H, s)) != cudaSuccess) return cuda_err(st, e, "embed");
   for (int li = 0; li < st->end - st->begin; ++li) {
@@ -457,6 +470,8 @@ int validate_call(stage* st, bool decode, int n, const int32_t* seq, const int32
       return set_err(st, STAGE_E_HANDOFF, "hidden_in is [%d x %d], expected [%d x %d]", hin->rows, hin->cols, n, c.hidden);
   }
   if (!hout || !hout->data) return set_err(st, STAGE_E_HANDOFF, "hidden_out required");
+  if (((uintptr_t)hout->data & 15) || (hin && hin->data && ((uintptr_t)hin->data & 15)))
+    return set_err(st, STAGE_E_HANDOFF, "hidden buffers must be 16-byte aligned");
   if (hout->rows != n || hout->cols != c.hidden)
     return set_err(st, STAGE_E_HANDOFF, "hidden_out is [%d x %d], expected [%d x %d]", hout->rows, hout->cols, n, c.hidden);
   std::vector<int> seen(c.max_seqs, 0);
@@ -500,7 +515,7 @@ int run_forward(stage* st, bool decode, int n, const int32_t* seq, const int32_t
   if (e == cudaSuccess) e = cudaEventRecord(st->staged, st->stream);
   if (e != cudaSuccess) return cuda_err(st, e, "stage inputs");
   rc = forward_dev(st, n, st->d_seq, st->d_pos, st->d_tok, hin ? hin->data : nullptr, hout->data,
-                   attn_chunks(st, n, max_len));
+                   attn_chunks(st, n, max_len), st->stream);
   if (rc) return rc;
   for (int i = 0; i < n; ++i) st->pending[seq[i]] = std::max(st->pending[seq[i]], pos[i] + 1);
   return STAGE_OK;
@@ -529,6 +544,15 @@ int stage_create(const stage_model_cfg* cfg, stage_layer_range range, const stag
   }
   const size_t need = plan_bytes(*cfg, range.begin, range.end);
   char msg[256];
+  if (need <= device_budget_bytes) {
+    const char* pdl = getenv("LRS_PDL");
+    if (pdl && pdl[0] == '0') lrs::set_pdl(false);
+    const cudaError_t pe = lrs::prepare_kernels();  // outside any stream capture
+    if (pe != cudaSuccess) {
+      g_create_error = std::string("kernel setup: ") + cudaGetErrorString(pe);
+      return STAGE_E_CUDA;
+    }
+  }
   if (need > device_budget_bytes) {
     snprintf(msg, sizeof msg, "DoesNotFit: stage needs %zu bytes, device budget is %zu", need, device_budget_bytes);
     g_create_error = msg;
@@ -640,7 +664,8 @@ int stage_decode(stage_t st, int batch, const int32_t* seq_ids_host, const int32
   return run_forward(st, true, batch, seq_ids_host, positions_host, tokens_host, hidden_in, hidden_out);
 }
 
-static int logits_dev(stage* st, int n_rows, const int* d_rows, float* logits_out, int32_t* argmax_out) {
+static int logits_dev(stage* st, int n_rows, const int* d_rows, float* logits_out, int32_t* argmax_out,
+                      cudaStream_t s) {
   const stage_model_cfg& c = st->cfg;
   float* lg = logits_out ? logits_out : st->logits;
   lrs::GemvArgs h;
@@ -652,9 +677,9 @@ static int logits_dev(stage* st, int n_rows, const int* d_rows, float* logits_ou
   h.epi = lrs::EPI_STORE;
   h.out = lg;
   h.ldo = c.vocab;
-  cudaError_t e = lrs::launch_gemv(h, st->stream);
+  cudaError_t e = lrs::launch_gemv(h, s);
   if (e != cudaSuccess) return cuda_err(st, e, "lm_head");
-  e = lrs::launch_argmax(lg, c.vocab, n_rows, argmax_out ? argmax_out : st->argmax, st->stream);
+  e = lrs::launch_argmax(lg, c.vocab, n_rows, argmax_out ? argmax_out : st->argmax, s);
   if (e != cudaSuccess) return cuda_err(st, e, "argmax");
   return STAGE_OK;
 }
@@ -674,7 +699,7 @@ int stage_logits(stage_t st, int n_rows, const int32_t* row_index_host, float* l
   e = cudaMemcpyAsync(st->d_rows, st->h_stage + 3 * st->cfg.max_tokens, n_rows * 4, cudaMemcpyHostToDevice, st->stream);
   if (e == cudaSuccess) e = cudaEventRecord(st->staged, st->stream);
   if (e != cudaSuccess) return cuda_err(st, e, "rows");
-  return logits_dev(st, n_rows, st->d_rows, logits_out, argmax_out);
+  return logits_dev(st, n_rows, st->d_rows, logits_out, argmax_out, st->stream);
 }
 
 int stage_commit(stage_t st, int n, const int32_t* seq_ids_host, const int32_t* new_len_host) {
@@ -789,6 +814,7 @@ struct stage_pipeline {
   int* d_hist = nullptr;
   int hist_cap = 0;
   int32_t* h_pin = nullptr;
+  cudaStream_t cap = nullptr;  // capture stream of the step graph
   cudaGraphExec_t graph = nullptr;
   std::vector<int> graph_seqs;
   int graph_chunks = 0;
@@ -848,6 +874,7 @@ int stage_pipeline_create(stage_t* stages, int n_stages, stage_pipeline_t* out) 
   cudaError_t e = cudaMalloc(&p->hbuf, (size_t)c0.max_tokens * c0.hidden * 4);
   if (e == cudaSuccess) e = cudaMalloc(&p->d_seq, (size_t)c0.max_seqs * 4 * 4);
   if (e == cudaSuccess) e = cudaMallocHost(&p->h_pin, (size_t)c0.max_seqs * 4 * 4);
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&p->cap, cudaStreamNonBlocking);
   if (e != cudaSuccess) {
     stage_pipeline_destroy(p);
     return STAGE_E_CUDA;
@@ -895,7 +922,7 @@ int stage_pipeline_step(stage_pipeline_t p, int is_prefill, int n_tokens, const 
     }
     if (e == cudaSuccess) e = cudaEventRecord(last->staged, last->stream);
     if (e != cudaSuccess) return pset(p, STAGE_E_CUDA, "rows: %s", cudaGetErrorString(e));
-    int rc = logits_dev(last, n_rows, last->d_rows, logits_out, nullptr);
+    int rc = logits_dev(last, n_rows, last->d_rows, logits_out, nullptr, last->stream);
     if (rc) return pset(p, rc, "%s", last->err.c_str());
     if (next_tokens_host) {
       e = cudaMemcpyAsync(next_tokens_host, last->argmax, n_rows * 4, cudaMemcpyDeviceToHost, last->stream);
@@ -956,15 +983,15 @@ int stage_pipeline_generate(stage_pipeline_t p, int batch, const int32_t* seq_id
   if (e != cudaSuccess) return pset(p, STAGE_E_CUDA, "%s", cudaGetErrorString(e));
   const int H = c.hidden;
   const int n_chunks = attn_chunks(s0, batch, max_len);
-  auto one_step = [&]() -> int {
+  auto one_step = [&](cudaStream_t s) -> int {
     for (size_t i = 0; i < p->stages.size(); ++i) {
       stage* st = p->stages[i];
-      int rc = forward_dev(st, batch, p->d_seq, p->d_pos, p->d_tok, p->hbuf, p->hbuf, n_chunks);
+      int rc = forward_dev(st, batch, p->d_seq, p->d_pos, p->d_tok, p->hbuf, p->hbuf, n_chunks, s);
       if (rc) return pset(p, rc, "stage %zu: %s", i, st->err.c_str());
     }
-    int rc = logits_dev(last, batch, nullptr, nullptr, p->d_tok);
+    int rc = logits_dev(last, batch, nullptr, nullptr, p->d_tok, s);
     if (rc) return pset(p, rc, "%s", last->err.c_str());
-    cudaError_t e2 = lrs::launch_advance(p->d_pos, p->d_tok, p->d_hist, p->d_step, batch, stream);
+    cudaError_t e2 = lrs::launch_advance(p->d_pos, p->d_tok, p->d_hist, p->d_step, batch, s);
     if (e2 != cudaSuccess) return pset(p, STAGE_E_CUDA, "advance: %s", cudaGetErrorString(e2));
     return STAGE_OK;
   };
@@ -973,11 +1000,14 @@ int stage_pipeline_generate(stage_pipeline_t p, int batch, const int32_t* seq_id
     if (!p->graph || p->graph_seqs != seqs || p->graph_chunks != n_chunks) {
       if (p->graph) cudaGraphExecDestroy(p->graph);
       p->graph = nullptr;
+      // capture on the pipeline's own non-blocking stream (the stages' stream may be the
+      // legacy default stream, which cannot be captured); replay on the stages' stream
       cudaGraph_t g = nullptr;
-      e = cudaStreamBeginCapture(stream, cudaStreamCaptureModeThreadLocal);
+      e = cudaStreamSynchronize(stream);
+      if (e == cudaSuccess) e = cudaStreamBeginCapture(p->cap, cudaStreamCaptureModeThreadLocal);
       if (e != cudaSuccess) return pset(p, STAGE_E_CUDA, "capture: %s", cudaGetErrorString(e));
-      int rc = one_step();
-      e = cudaStreamEndCapture(stream, &g);
+      int rc = one_step(p->cap);
+      e = cudaStreamEndCapture(p->cap, &g);
       if (rc) {
         if (g) cudaGraphDestroy(g);
         return rc;
@@ -995,7 +1025,7 @@ int stage_pipeline_generate(stage_pipeline_t p, int batch, const int32_t* seq_id
     }
   } else {
     for (int t = 0; t < n_steps; ++t) {
-      int rc = one_step();
+      int rc = one_step(stream);
       if (rc) return rc;
     }
   }
@@ -1033,6 +1063,7 @@ void stage_pipeline_destroy(stage_pipeline_t p) {
   if (p->d_seq) cudaFree(p->d_seq);
   if (p->d_hist) cudaFree(p->d_hist);
   if (p->h_pin) cudaFreeHost(p->h_pin);
+  if (p->cap) cudaStreamDestroy(p->cap);
   delete p;
 }
 
