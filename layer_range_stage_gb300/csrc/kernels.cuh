@@ -10,7 +10,7 @@ namespace lrs {
 enum GemvEpi { EPI_STORE = 0, EPI_RESID = 1, EPI_SWIGLU = 2, EPI_QKV = 3 };
 
 // Device int8 block-32 matrix: q [N][Kp] stored biased (byte = q + 128), s [N][Kp/32] fp16 bits,
-// Kp = K rounded up to 32 (the padding columns face zero inputs).  Row order is the device
+// Kp = K rounded up to 256 (the padding columns face zero inputs).  Row order is the device
 // order chosen at import.
 struct DevQ8 {
   uint8_t* q = nullptr;
@@ -47,6 +47,7 @@ struct GemvArgs {
   const int* pos = nullptr;
   const float2* rope = nullptr;  // [max_len][D/2] (cos, sin)
   int n_q_heads = 0, n_kv_heads = 0, head_dim = 0, max_len = 0;
+  int* err = nullptr;  // device error word: set (never cleared by kernels) when a bounded wait times out
 };
 
 // Split-K grouped-query decode attention over the fp16 cache with a deterministic merge of
@@ -72,6 +73,7 @@ cudaError_t prepare_kernels();
 // Programmatic dependent launch of the stage kernels (on by default).
 void set_pdl(bool on);
 bool pdl_enabled();
+
 cudaError_t launch_gemv(const GemvArgs& a, cudaStream_t st);
 cudaError_t launch_attn_decode(const AttnArgs& a, cudaStream_t st);
 constexpr int kAttnMaxChunks = 64;

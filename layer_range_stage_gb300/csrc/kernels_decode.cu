@@ -56,10 +56,12 @@ static cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_
 // corrected by -128 X in one FFMA, then multiplied by the block scale.  Per weight byte:
 // one byte extract + one FFMA.
 //
-// Work split: each warp owns R consecutive rows at a time (grid-stride over row groups of
-// the whole grid), its lanes stream 16 bytes per row per chunk with U chunks in flight
-// per row, and reduce with warp shuffles only -- no block barrier in the main loop.  The
-// first batch of weights is requested before waiting for the predecessor kernel.  The
+// Work split: KS warps of a CTA own R consecutive rows at a time (grid-stride over row
+// groups), each warp a 1/KS slice of K; its lanes stream 16 bytes per row per chunk with U
+// chunks in flight per row, so KS is chosen to let every warp issue all of its loads at
+// once.  Warps reduce with shuffles; the KS partial sums of a row meet in shared memory in
+// slice order behind a named barrier of those KS warps only.  The first batch of weights
+// is requested before waiting for the predecessor kernel.  The
 // CTA's shared memory holds the (normalised, scaled) input once per pass of BT tokens,
 // copied in with cp.async, and its chunk sums; an XOR swizzle of the four float4 of each
 // 16-float chunk keeps the lanes' 64-byte reads bank-conflict free.
@@ -91,17 +93,20 @@ __device__ __forceinline__ float dot16_u8(const uint4 w, const float4 x0, const 
   return acc;
 }
 
-template <int R, int U, int BT>
+template <int R, int U, int BT, int KS>
 __global__ void __launch_bounds__(kGemvThreads, BT == 1 ? 3 : 2) gemv_q8_kernel(const GemvArgs a) {
   extern __shared__ __align__(16) float smem[];
+  constexpr int NW = kGemvThreads / 32, RG = NW / KS;  // warps, row groups per CTA
   const int Kp = a.w.Kp, K = a.w.K, N = a.w.N;
   const int nchunk = Kp >> 4, nblk = Kp >> 5;
   float* xs = smem;                  // [BT][Kp] inputs * 2^64, swizzled
   float* xc = xs + BT * Kp;          // [BT][nchunk] chunk sums of the inputs
   float* nrm = xc + BT * nchunk;     // [8]
+  float* red = nrm + 8;              // [RG][KS][R*BT] slice partial sums
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int kslice = warp % KS, rgrp = warp / KS;
   const int ngroups = (N + R - 1) / R;
-  const int gwarp = blockIdx.x * (kGemvThreads / 32) + warp, nwarps = gridDim.x * (kGemvThreads / 32);
+  const int gwarp = blockIdx.x * RG + rgrp, nwarps = gridDim.x * RG;
 
   uint4 w[U][R];
   float sc[U][R];
@@ -127,7 +132,7 @@ __global__ void __launch_bounds__(kGemvThreads, BT == 1 ? 3 : 2) gemv_q8_kernel(
   pdl_trigger();
   bool prefetched = false;
   if (a.ntok <= BT && gwarp < ngroups) {
-    load_batch(gwarp * R, 0);
+    load_batch(gwarp * R, kslice * 32 * U);
     prefetched = true;
   }
   pdl_wait();
@@ -206,7 +211,7 @@ __global__ void __launch_bounds__(kGemvThreads, BT == 1 ? 3 : 2) gemv_q8_kernel(
 #pragma unroll
         for (int b = 0; b < BT; ++b) acc[r][b] = 0.f;
 
-      for (int cb = 0; cb < nchunk; cb += 32 * U) {
+      for (int cb = kslice * 32 * U; cb < nchunk; cb += KS * 32 * U) {
         if (prefetched) {
           prefetched = false;  // the first batch of the first task is already in registers
         } else {
@@ -235,6 +240,28 @@ __global__ void __launch_bounds__(kGemvThreads, BT == 1 ? 3 : 2) gemv_q8_kernel(
       for (int r = 0; r < R; ++r)
 #pragma unroll
         for (int b = 0; b < BT; ++b) acc[r][b] = warp_sum(acc[r][b]);
+      if (KS > 1) {
+        // the KS slices of this row group meet in shared memory, summed in slice order
+        float* rg = red + rgrp * KS * R * BT;
+        if (lane == 0) {
+#pragma unroll
+          for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int b = 0; b < BT; ++b) rg[kslice * R * BT + r * BT + b] = acc[r][b];
+        }
+        named_bar(1 + rgrp, KS * 32);
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+          for (int b = 0; b < BT; ++b) {
+            float sum = 0.f;
+#pragma unroll
+            for (int k = 0; k < KS; ++k) sum += rg[k * R * BT + r * BT + b];
+            acc[r][b] = sum;
+          }
+        named_bar(1 + rgrp, KS * 32);
+        if (kslice != 0) continue;
+      }
 
       // epilogue: lane i takes value i (rows) or pair i (row pairs)
       if (a.epi == EPI_STORE || a.epi == EPI_RESID) {
@@ -289,29 +316,30 @@ __global__ void __launch_bounds__(kGemvThreads, BT == 1 ? 3 : 2) gemv_q8_kernel(
   }
 }
 
-template <int BT>
+// xs [BT][Kp] + xc [BT][Kp/16] + nrm [8] + red [warps][R*BT]
+template <int R, int BT>
 static size_t gemv_smem(int Kp) {
-  return sizeof(float) * ((size_t)BT * Kp + (size_t)BT * (Kp / 16) + 8);
+  return sizeof(float) * ((size_t)BT * Kp + (size_t)BT * (Kp / 16) + 8 + (size_t)(kGemvThreads / 32) * R * BT);
 }
 
 // Launch attributes are fixed once, outside any stream capture (prepare_kernels); the
 // launch itself only computes the grid from the recorded register count.
-template <int R, int U, int BT>
+template <int R, int U, int BT, int KS>
 struct GemvInfo {
   static int regs;
 };
-template <int R, int U, int BT>
-int GemvInfo<R, U, BT>::regs = 0;
+template <int R, int U, int BT, int KS>
+int GemvInfo<R, U, BT, KS>::regs = 0;
 
-template <int R, int U, int BT>
+template <int R, int U, int BT, int KS>
 static cudaError_t prepare_gemv() {
-  cudaError_t e = cudaFuncSetAttribute(gemv_q8_kernel<R, U, BT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(gemv_q8_kernel<R, U, BT, KS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)kGemvSmemBudget + 4096);
   if (e != cudaSuccess) return e;
   cudaFuncAttributes fa;
-  e = cudaFuncGetAttributes(&fa, gemv_q8_kernel<R, U, BT>);
+  e = cudaFuncGetAttributes(&fa, gemv_q8_kernel<R, U, BT, KS>);
   if (e != cudaSuccess) return e;
-  GemvInfo<R, U, BT>::regs = fa.numRegs;
+  GemvInfo<R, U, BT, KS>::regs = fa.numRegs;
   return cudaSuccess;
 }
 
@@ -324,38 +352,43 @@ static int occupancy(int regs, int threads, size_t smem) {
   return std::max(1, std::min(by_threads, std::min(by_regs, by_smem)));
 }
 
-template <int R, int U, int BT>
+template <int R, int U, int BT, int KS>
 static cudaError_t launch_gemv_t(const GemvArgs& a, cudaStream_t st) {
-  if (GemvInfo<R, U, BT>::regs == 0) return cudaErrorNotReady;  // prepare_kernels() was not called
-  const size_t smem = gemv_smem<BT>(a.w.Kp);
-  int occ = occupancy(GemvInfo<R, U, BT>::regs, kGemvThreads, smem);
-  if (g_pdl && occ > 2) occ -= 1;  // leave one CTA slot per SM for the successor to prefetch into
+  if (GemvInfo<R, U, BT, KS>::regs == 0) return cudaErrorNotReady;  // prepare_kernels() was not called
+  const size_t smem = gemv_smem<R, BT>(a.w.Kp);
+  const int occ = occupancy(GemvInfo<R, U, BT, KS>::regs, kGemvThreads, smem);
   const int ngroups = (a.w.N + R - 1) / R;
-  const int warps_per_cta = kGemvThreads / 32;
-  const int grid = std::max(1, std::min((ngroups + warps_per_cta - 1) / warps_per_cta, sm_count() * occ));
-  return launch_k(gemv_q8_kernel<R, U, BT>, dim3(grid), dim3(kGemvThreads), smem, st, a);
+  const int groups_per_cta = (kGemvThreads / 32) / KS;
+  const int grid = std::max(1, std::min((ngroups + groups_per_cta - 1) / groups_per_cta, sm_count() * occ));
+  return launch_k(gemv_q8_kernel<R, U, BT, KS>, dim3(grid), dim3(kGemvThreads), smem, st, a);
 }
 
 cudaError_t launch_gemv(const GemvArgs& a, cudaStream_t st) {
   if (a.ntok <= 0 || a.w.N <= 0) return cudaSuccess;
   const size_t budget = kGemvSmemBudget;
-  if (a.ntok >= 4 && gemv_smem<4>(a.w.Kp) <= budget) return launch_gemv_t<2, 2, 4>(a, st);
-  if (a.ntok >= 2 && gemv_smem<2>(a.w.Kp) <= budget) return launch_gemv_t<2, 4, 2>(a, st);
-  return launch_gemv_t<2, 4, 1>(a, st);
+  if (a.ntok >= 4 && gemv_smem<2, 4>(a.w.Kp) <= budget) return launch_gemv_t<2, 2, 4, 1>(a, st);
+  if (a.ntok >= 2 && gemv_smem<2, 2>(a.w.Kp) <= budget) return launch_gemv_t<2, 4, 2, 1>(a, st);
+  // one load round per warp: K split over KS warps so that KS * 32 lanes * U chunks cover K
+  const int nchunk = a.w.Kp / 16;
+  if (nchunk > 4 * 32 * 4) return launch_gemv_t<2, 4, 1, 8>(a, st);
+  if (nchunk > 2 * 32 * 4) return launch_gemv_t<2, 4, 1, 4>(a, st);
+  if (nchunk > 32 * 4) return launch_gemv_t<2, 4, 1, 2>(a, st);
+  return launch_gemv_t<2, 4, 1, 1>(a, st);
 }
 
 // ------------------------------------------------------------------------------------------
-// Split-K GQA decode attention.  Grid (n_chunks, Hkv, ntok), 128 threads.  The CTA takes the
-// G = Hq / Hkv query heads that share KV head blockIdx.y and the positions of its chunk of
-// 0..pos[t].  It walks the chunk in tiles of TP positions: all threads first copy the K and
-// V rows of the tile into shared memory with cp.async (every copy of the tile in flight at
-// once), then compute the scores, a running max / sum per head, and the probability-
-// weighted V rows.  The chunk's partial (unnormalised output, max, sum) goes to scratch; the
-// last CTA of a (token, kv head) to finish -- found with one integer atomic, no waiting --
-// merges the chunks in chunk order, reading each partial with coalesced, batched loads.
+// Split-K GQA decode attention.  Grid (n_chunks, Hkv, ntok), 128 threads, about one wave of
+// CTAs.  The CTA takes the G = Hq / Hkv query heads that share KV head blockIdx.y and the
+// positions of its chunk of 0..pos[t].  It walks the chunk in tiles of 128 positions: all
+// threads first copy the K and V rows of the tile into shared memory with cp.async (every
+// copy of the tile in flight at once), then thread p scores position p for every head, a
+// running max / sum per head is kept, and the probability-weighted V rows accumulate.  The
+// chunk's partial (unnormalised output, max, sum) goes to scratch; the last CTA of a
+// (token, kv head) to finish -- found with one integer atomic, no waiting -- merges the
+// chunks in chunk order after copying every partial into shared memory in one round trip.
 
 constexpr int kAttnThreads = 128;
-constexpr int kAttnTile = 64;
+constexpr int kAttnTile = 128;
 
 template <int D, int G>
 struct AttnSmem {
@@ -369,6 +402,8 @@ struct AttnSmem {
   static constexpr size_t w = (size_t)kAttnMaxChunks * G * 4;
   static constexpr size_t stats = (size_t)4 * G * 4;
   static constexpr size_t total = 2 * kv + q + p + o + w + stats;
+  // chunks whose partials fit in the K/V tile area for the one-shot merge
+  static constexpr int merge_chunks = (int)((2 * kv) / ((size_t)G * D * 4));
 };
 
 template <int D, int G>
@@ -424,62 +459,61 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const AttnArg
     }
     cp_async_wait_all();
     __syncthreads();
-    // scores: thread -> (position, heads g == hh mod (NT / TP))
-    {
-      constexpr int HSTEP = NT / TP;
-      constexpr int NH = (G + HSTEP - 1) / HSTEP;
-      const int pp = tid % TP, hh = tid / TP;
-      if (pp < np && hh < G) {
-        float sc[NH];
+    // scores: thread tid -> position tid, every head
+    if (tid < np) {
+      float sc[G];
 #pragma unroll
-        for (int j = 0; j < NH; ++j) sc[j] = 0.f;
-        const __half* kr = ks + pp * KROW;
+      for (int g = 0; g < G; ++g) sc[g] = 0.f;
+      const __half* kr = ks + tid * KROW;
 #pragma unroll 4
-        for (int i = 0; i < D / 8; ++i) {
-          const uint4 kk = *reinterpret_cast<const uint4*>(kr + 8 * i);
-          const float2 k01 = __half22float2(*reinterpret_cast<const __half2*>(&kk.x));
-          const float2 k23 = __half22float2(*reinterpret_cast<const __half2*>(&kk.y));
-          const float2 k45 = __half22float2(*reinterpret_cast<const __half2*>(&kk.z));
-          const float2 k67 = __half22float2(*reinterpret_cast<const __half2*>(&kk.w));
+      for (int i = 0; i < D / 8; ++i) {
+        const uint4 kk = *reinterpret_cast<const uint4*>(kr + 8 * i);
+        const float2 k01 = __half22float2(*reinterpret_cast<const __half2*>(&kk.x));
+        const float2 k23 = __half22float2(*reinterpret_cast<const __half2*>(&kk.y));
+        const float2 k45 = __half22float2(*reinterpret_cast<const __half2*>(&kk.z));
+        const float2 k67 = __half22float2(*reinterpret_cast<const __half2*>(&kk.w));
 #pragma unroll
-          for (int j = 0; j < NH; ++j) {
-            const int g = hh + j * HSTEP;
-            if (g < G) {
-              const float4 qa = *reinterpret_cast<const float4*>(qs + g * D + 8 * i);
-              const float4 qb = *reinterpret_cast<const float4*>(qs + g * D + 8 * i + 4);
-              float s = sc[j];
-              s = fmaf(qa.x, k01.x, s);
-              s = fmaf(qa.y, k01.y, s);
-              s = fmaf(qa.z, k23.x, s);
-              s = fmaf(qa.w, k23.y, s);
-              s = fmaf(qb.x, k45.x, s);
-              s = fmaf(qb.y, k45.y, s);
-              s = fmaf(qb.z, k67.x, s);
-              s = fmaf(qb.w, k67.y, s);
-              sc[j] = s;
-            }
-          }
-        }
-#pragma unroll
-        for (int j = 0; j < NH; ++j) {
-          const int g = hh + j * HSTEP;
-          if (g < G) ps[g * TP + pp] = sc[j] * a.scale;
+        for (int g = 0; g < G; ++g) {
+          const float4 qa = *reinterpret_cast<const float4*>(qs + g * D + 8 * i);
+          const float4 qb = *reinterpret_cast<const float4*>(qs + g * D + 8 * i + 4);
+          float s = sc[g];
+          s = fmaf(qa.x, k01.x, s);
+          s = fmaf(qa.y, k01.y, s);
+          s = fmaf(qa.z, k23.x, s);
+          s = fmaf(qa.w, k23.y, s);
+          s = fmaf(qb.x, k45.x, s);
+          s = fmaf(qb.y, k45.y, s);
+          s = fmaf(qb.z, k67.x, s);
+          s = fmaf(qb.w, k67.y, s);
+          sc[g] = s;
         }
       }
+#pragma unroll
+      for (int g = 0; g < G; ++g) ps[g * TP + tid] = sc[g] * a.scale;
     }
     __syncthreads();
     // per head: tile max, probabilities, running (max, sum); warp w handles heads w, w + 4, ...
     for (int g = warp; g < G; g += NT / 32) {
-      const float s0 = lane < np ? ps[g * TP + lane] : -INFINITY;
-      const float s1 = lane + 32 < np ? ps[g * TP + lane + 32] : -INFINITY;
-      const float mt = warp_max(fmaxf(s0, s1));
+      float sv[TP / 32];
+      float mt = -INFINITY;
+#pragma unroll
+      for (int k2 = 0; k2 < TP / 32; ++k2) {
+        const int p = lane + 32 * k2;
+        sv[k2] = p < np ? ps[g * TP + p] : -INFINITY;
+        mt = fmaxf(mt, sv[k2]);
+      }
+      mt = warp_max(mt);
       const float mold = st_m[g];
       const float mnew = fmaxf(mold, mt);
-      const float e0 = lane < np ? expf(s0 - mnew) : 0.f;
-      const float e1 = lane + 32 < np ? expf(s1 - mnew) : 0.f;
-      ps[g * TP + lane] = e0;
-      ps[g * TP + lane + 32] = e1;
-      const float lt = warp_sum(e0 + e1);
+      float lsum = 0.f;
+#pragma unroll
+      for (int k2 = 0; k2 < TP / 32; ++k2) {
+        const int p = lane + 32 * k2;
+        const float e = p < np ? expf(sv[k2] - mnew) : 0.f;
+        ps[g * TP + p] = e;
+        lsum += e;
+      }
+      const float lt = warp_sum(lsum);
       if (lane == 0) {
         const float alpha = (mold == -INFINITY) ? 0.f : expf(mold - mnew);
         st_a[g] = alpha;
@@ -534,8 +568,13 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const AttnArg
   __syncthreads();
   if (!is_last) return;
   __threadfence();
-  // merge: chunk weights e^(m_c - M) per head, then coalesced weighted sums in chunk order
+  // merge: chunk weights e^(m_c - M) per head, then the weighted sums in chunk order
   const int nch = a.n_chunks;
+  const float* pbase = a.part_o + ((size_t)t * a.Hkv + kvh) * nch * (G * D);
+  const bool staged = nch <= S::merge_chunks;
+  float* pst = reinterpret_cast<float*>(sm_raw);  // [nch][G*D] partials, over the K/V tiles
+  if (staged)
+    for (int i = tid; i < nch * G * D / 4; i += NT) cp_async16(pst + 4 * i, pbase + 4 * i);
   float2* mls = reinterpret_cast<float2*>(ored);  // [G][nch] (max, sum), reusing the PV scratch
   for (int i = tid; i < G * nch; i += NT) mls[i] = __ldcg(a.part_ml + head0 * nch + i);
   __syncthreads();
@@ -551,20 +590,24 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const AttnArg
     }
     st_L[tid] = Ls;
   }
+  cp_async_wait_all();
   __syncthreads();
-  const float* pbase = a.part_o + ((size_t)t * a.Hkv + kvh) * nch * (G * D);
   for (int i = tid; i < G * D; i += NT) {
     const int g = i / D;
     float acc = 0.f;
-    int c = 0;
-    for (; c + 8 <= nch; c += 8) {
-      float v[8];
+    if (staged) {
+      for (int c = 0; c < nch; ++c) acc = fmaf(wts[c * G + g], pst[(size_t)c * (G * D) + i], acc);
+    } else {
+      int c = 0;
+      for (; c + 8 <= nch; c += 8) {
+        float v[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) v[j] = __ldcg(pbase + (size_t)(c + j) * (G * D) + i);
+        for (int j = 0; j < 8; ++j) v[j] = __ldcg(pbase + (size_t)(c + j) * (G * D) + i);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) acc = fmaf(wts[(c + j) * G + g], v[j], acc);
+        for (int j = 0; j < 8; ++j) acc = fmaf(wts[(c + j) * G + g], v[j], acc);
+      }
+      for (; c < nch; ++c) acc = fmaf(wts[c * G + g], __ldcg(pbase + (size_t)c * (G * D) + i), acc);
     }
-    for (; c < nch; ++c) acc = fmaf(wts[c * G + g], __ldcg(pbase + (size_t)c * (G * D) + i), acc);
     a.out[head0 * D + i] = acc / st_L[g];
   }
   if (tid == 0) a.counters[(size_t)t * a.Hkv + kvh] = 0;
@@ -728,9 +771,13 @@ cudaError_t prepare_kernels() {
   static cudaError_t done = cudaErrorNotReady;
   if (done == cudaSuccess) return done;
   sm_count();
-  cudaError_t e = prepare_gemv<2, 4, 1>();
-  if (e == cudaSuccess) e = prepare_gemv<2, 4, 2>();
-  if (e == cudaSuccess) e = prepare_gemv<2, 2, 4>();
+  cudaError_t e = prepare_gemv<2, 4, 1, 1>();
+  if (e == cudaSuccess) e = prepare_gemv<2, 4, 1, 2>();
+  if (e == cudaSuccess) e = prepare_gemv<2, 4, 1, 4>();
+  if (e == cudaSuccess) e = prepare_gemv<2, 4, 1, 8>();
+  if (e == cudaSuccess) e = prepare_gemv<2, 4, 2, 1>();
+  if (e == cudaSuccess) e = prepare_gemv<2, 2, 4, 1>();
+
   if (e == cudaSuccess) e = prepare_attn<64, 1>();
   if (e == cudaSuccess) e = prepare_attn<64, 2>();
   if (e == cudaSuccess) e = prepare_attn<64, 4>();

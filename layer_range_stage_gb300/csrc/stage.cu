@@ -32,7 +32,9 @@ constexpr int kMaxChunks = lrs::kAttnMaxChunks;
 constexpr size_t kAlign = 256;
 
 inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
-inline int kpad(int k) { return (k + 31) / 32 * 32; }
+// Device rows are padded to a multiple of 256 weights, so every row of int8 data and of
+// fp16 scales starts on a 16-byte boundary (the bulk copies of the streaming GEMV need it).
+inline int kpad(int k) { return (k + 255) / 256 * 256; }
 
 struct LayerDev {
   float* attn_norm = nullptr;
@@ -47,7 +49,8 @@ template <class F>
 void walk_plan(const stage_model_cfg& c, int begin, int end, std::vector<LayerDev>* layers, DevQ8* embed,
                DevQ8* head, float** final_norm, __half** kc, __half** vc, float2** rope, float** qbuf,
                float** obuf, float** abuf, float** feat, float** logits, int** argmax, float** part_o,
-               float2** part_ml, int** counters, int** d_seq, int** d_pos, int** d_tok, int** d_rows, F&& f) {
+               float2** part_ml, int** counters, int** d_seq, int** d_pos, int** d_tok, int** d_rows, int** err_word,
+               F&& f) {
   auto q8 = [&](DevQ8* m, int N, int K) {
     if (m) {
       m->N = N;
@@ -101,6 +104,7 @@ void walk_plan(const stage_model_cfg& c, int begin, int end, std::vector<LayerDe
   f(T * 4, (void**)d_pos);
   f(T * 4, (void**)d_tok);
   f(T * 4, (void**)d_rows);
+  f(4, (void**)err_word);
 }
 
 thread_local std::string g_create_error;
@@ -108,7 +112,7 @@ thread_local std::string g_create_error;
 size_t plan_bytes(const stage_model_cfg& c, int begin, int end) {
   size_t total = 0;
   walk_plan(c, begin, end, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
-            nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
+            nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
             [&](size_t b, void**) { total += round_up(b, kAlign); });
   return total;
 }
@@ -163,6 +167,7 @@ struct stage {
   float2* part_ml = nullptr;
   int* counters = nullptr;
   int *d_seq = nullptr, *d_pos = nullptr, *d_tok = nullptr, *d_rows = nullptr;
+  int* err_word = nullptr;     // device: set by a kernel whose bounded wait timed out
   int32_t* h_stage = nullptr;  // pinned host staging [4][max_tokens]
   cudaEvent_t staged = nullptr;  // recorded after the last copy out of h_stage
   std::vector<int> committed, pending;
@@ -345,13 +350,13 @@ bool weights_ready(stage* st) {
   return true;
 }
 
-// Split-K factor of decode attention: enough CTAs for two per SM, chunks of >= 32 positions,
+// Split-K factor of decode attention: about one CTA per SM, chunks of >= 32 positions,
 // bounded by the partial-result scratch.
 int attn_chunks(const stage* st, int ntok, int max_len_in_call) {
   const size_t pairs = std::max((size_t)st->cfg.max_seqs * kMaxChunks, (size_t)st->cfg.max_tokens * 4);
   int n = (max_len_in_call + 31) / 32;
   const int work = std::max(1, ntok * st->cfg.n_kv_heads);
-  const int fill = std::max(1, (2 * lrs::sm_count() + work - 1) / work);
+  const int fill = std::max(1, (lrs::sm_count() + work - 1) / work);  // about one wave
   n = std::min(n, fill);
   n = std::min<int>(n, (int)std::min<size_t>(kMaxChunks, pairs / (size_t)ntok));
   return std::max(1, n);
@@ -388,6 +393,7 @@ int forward_dev(stage* st, int n, const int* d_seq, const int* d_pos, const int*
     g.n_kv_heads = Hkv;
     g.head_dim = D;
     g.max_len = c.max_seq_len;
+    g.err = st->err_word;
     if ((e = lrs::launch_gemv(g, s)) != cudaSuccess) return cuda_err(st, e, "qkv");
 
     lrs::AttnArgs a;
@@ -419,6 +425,7 @@ int forward_dev(stage* st, int n, const int* d_seq, const int* d_pos, const int*
     o.ldr = H;
     o.out = hout;
     o.ldo = H;
+    o.err = st->err_word;
     if ((e = lrs::launch_gemv(o, s)) != cudaSuccess) return cuda_err(st, e, "o_proj");
 
     if (c.n_experts > 0) return set_err(st, STAGE_E_INVALID, "MoE forward not built yet");
@@ -432,6 +439,7 @@ int forward_dev(stage* st, int n, const int* d_seq, const int* d_pos, const int*
     gu.epi = lrs::EPI_SWIGLU;
     gu.out = st->abuf;
     gu.ldo = c.ffn;
+    gu.err = st->err_word;
     if ((e = lrs::launch_gemv(gu, s)) != cudaSuccess) return cuda_err(st, e, "gate_up");
 
     lrs::GemvArgs dn;
@@ -444,12 +452,25 @@ int forward_dev(stage* st, int n, const int* d_seq, const int* d_pos, const int*
     dn.ldr = H;
     dn.out = hout;
     dn.ldo = H;
+    dn.err = st->err_word;
     if ((e = lrs::launch_gemv(dn, s)) != cudaSuccess) return cuda_err(st, e, "down");
   }
   if (st->last &&
       (e = lrs::launch_final_norm(hout, H, st->final_norm, c.rms_eps, H, n, st->feat, hout, H, s)) != cudaSuccess)
     return cuda_err(st, e, "final_norm");
   st->last_n = n;
+  return STAGE_OK;
+}
+
+// After a synchronisation: report (and clear) a device-side wait timeout of this stage.
+int check_device_error(stage* st) {
+  int v = 0;
+  cudaError_t e = cudaMemcpy(&v, st->err_word, 4, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_err(st, e, "error word");
+  if (v) {
+    cudaMemset(st->err_word, 0, 4);
+    return set_err(st, STAGE_E_CUDA, "a kernel's bounded wait timed out; its outputs are invalid");
+  }
   return STAGE_OK;
 }
 
@@ -592,7 +613,8 @@ int stage_create(const stage_model_cfg* cfg, stage_layer_range range, const stag
   size_t off = 0;
   walk_plan(*cfg, range.begin, range.end, &st->layers, &st->embed, &st->head, &st->final_norm, &st->kc, &st->vc,
             &st->rope, &st->qbuf, &st->obuf, &st->abuf, &st->feat, &st->logits, &st->argmax, &st->part_o,
-            &st->part_ml, &st->counters, &st->d_seq, &st->d_pos, &st->d_tok, &st->d_rows, [&](size_t b, void** slot) {
+            &st->part_ml, &st->counters, &st->d_seq, &st->d_pos, &st->d_tok, &st->d_rows, &st->err_word,
+            [&](size_t b, void** slot) {
               if (slot) *slot = st->arena + off;
               off += round_up(b, kAlign);
             });
@@ -677,6 +699,7 @@ static int logits_dev(stage* st, int n_rows, const int* d_rows, float* logits_ou
   h.epi = lrs::EPI_STORE;
   h.out = lg;
   h.ldo = c.vocab;
+  h.err = st->err_word;
   cudaError_t e = lrs::launch_gemv(h, s);
   if (e != cudaSuccess) return cuda_err(st, e, "lm_head");
   e = lrs::launch_argmax(lg, c.vocab, n_rows, argmax_out ? argmax_out : st->argmax, s);
@@ -761,7 +784,7 @@ int stage_read_kv(stage_t st, int global_layer, int seq_id, int n_pos, uint16_t*
     if (e == cudaSuccess)
       e = cudaMemcpy(v_host + (size_t)h * n_pos * row, st->vc + off, (size_t)n_pos * row * 2, cudaMemcpyDeviceToHost);
   }
-  return e == cudaSuccess ? STAGE_OK : cuda_err(st, e, "read kv");
+  return e == cudaSuccess ? check_device_error(st) : cuda_err(st, e, "read kv");
 }
 
 int stage_gemm_mode(stage_t st, int n_tokens, int* mode_out) {
@@ -928,6 +951,8 @@ int stage_pipeline_step(stage_pipeline_t p, int is_prefill, int n_tokens, const 
       e = cudaMemcpyAsync(next_tokens_host, last->argmax, n_rows * 4, cudaMemcpyDeviceToHost, last->stream);
       if (e == cudaSuccess) e = cudaStreamSynchronize(last->stream);
       if (e != cudaSuccess) return pset(p, STAGE_E_CUDA, "tokens: %s", cudaGetErrorString(e));
+      for (stage* s2 : p->stages)
+        if (check_device_error(s2)) return pset(p, STAGE_E_CUDA, "%s", s2->err.c_str());
     }
   }
   // joint publication
@@ -1037,6 +1062,8 @@ int stage_pipeline_generate(stage_pipeline_t p, int batch, const int32_t* seq_id
   e = cudaMemcpyAsync(hist.data(), p->d_hist, hist.size() * 4, cudaMemcpyDeviceToHost, stream);
   if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
   if (e != cudaSuccess) return pset(p, STAGE_E_CUDA, "%s", cudaGetErrorString(e));
+  for (stage* s2 : p->stages)
+    if (check_device_error(s2)) return pset(p, STAGE_E_CUDA, "%s", s2->err.c_str());
   std::memcpy(tokens_out_host, hist.data(), hist.size() * 4);
   for (stage* st : p->stages)
     for (int i = 0; i < batch; ++i) {
