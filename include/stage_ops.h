@@ -1,0 +1,64 @@
+/*
+ * layer_range_stage (GB300) -- kernel-level entry points.
+ *
+ * The two dominant steps of a stage forward, callable on their own with caller-owned
+ * device buffers: the dequant-fused int8 block-32 GEMV and split-K grouped-query decode
+ * attention.  These run the same kernels stage_decode launches.  Return codes are the
+ * STAGE_* codes of stage.h; messages are read with stage_op_last_error().  All device
+ * pointers must be 16-byte aligned.
+ */
+#ifndef LAYER_RANGE_STAGE_OPS_H
+#define LAYER_RANGE_STAGE_OPS_H
+
+#include "stage.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Device bytes of a packed [rows x cols] int8 block-32 matrix: the weight bytes (biased,
+ * rows padded to a multiple of 256 weights) and the fp16 scale bytes. */
+STAGE_API int stage_op_q8_device_bytes(int64_t rows, int64_t cols, size_t* q_bytes, size_t* s_bytes);
+
+/* Pack a host matrix (layout of stage_q8) into caller device buffers of the sizes above.
+ * Synchronous. */
+STAGE_API int stage_op_q8_pack(const stage_q8* host, void* q_dev, void* s_dev);
+
+/* y[t][r] = sum_k W[r][k] * h[t][k] for t < n_tok, r < rows, where h = x, or
+ * h = x / sqrt(mean(x^2) + eps) * gamma when gamma_dev is not NULL (the RMSNorm that
+ * precedes every projection of a block: "41. Many GPUs: tensor, pipeline, expert and
+ * data parallelism", section "Pipeline parallelism").  W is a packed matrix
+ * (stage_op_q8_pack).  x_dev: f32 [n_tok][cols]; y_dev: f32 [n_tok][rows].  Runs on
+ * `stream` (a cudaStream_t); no allocation, no synchronisation. */
+STAGE_API int stage_op_gemv(const void* q_dev, const void* s_dev, int64_t rows, int64_t cols, const float* x_dev,
+                            int n_tok, const float* gamma_dev, float eps, float* y_dev, void* stream);
+
+/* Scratch bytes stage_op_attention_decode needs for these sizes. */
+STAGE_API size_t stage_op_attention_workspace_bytes(int n_tok, int n_q_heads, int n_kv_heads, int head_dim,
+                                                    int n_chunks);
+
+/* Split-K grouped-query decode attention over an fp16 KV cache ("41. Many GPUs: ...",
+ * section "Ring attention for very long contexts": partial attention with log-sum-exp
+ * and the merge o = sum_s e^(l_s - l) o_s; section "Tensor parallelism": query head j
+ * reads KV head j / (n_q_heads / n_kv_heads)).
+ *   q_dev: f32 [n_tok][n_q_heads][head_dim] (already rotated);
+ *   k_cache_dev, v_cache_dev: fp16 bits [seqs][n_kv_heads][max_len][head_dim];
+ *   seq_dev, pos_dev: device int32 [n_tok]: token t attends to positions 0..pos[t] of
+ *     sequence seq[t] (the caller guarantees pos[t] < max_len and seq[t] < seqs);
+ *   out_dev: f32 [n_tok][n_q_heads][head_dim], softmax(q k^T / sqrt(head_dim)) v;
+ *   n_chunks in [1, 64]: the positions of each token are split in n_chunks chunks;
+ *   workspace_dev: stage_op_attention_workspace_bytes(...) bytes of device scratch whose
+ *     contents must be zero before the first call (each call leaves it ready for the next).
+ * head_dim 64 or 128; n_q_heads / n_kv_heads in {1, 2, 4, 8}.  Runs on `stream`. */
+STAGE_API int stage_op_attention_decode(const float* q_dev, const uint16_t* k_cache_dev, const uint16_t* v_cache_dev,
+                                        const int32_t* seq_dev, const int32_t* pos_dev, int n_tok, int n_q_heads,
+                                        int n_kv_heads, int head_dim, int max_len, int n_chunks, float* out_dev,
+                                        void* workspace_dev, size_t workspace_bytes, void* stream);
+
+/* Message of the last failed stage_op_* call on the calling thread ("" if none). */
+STAGE_API const char* stage_op_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* LAYER_RANGE_STAGE_OPS_H */

@@ -93,14 +93,26 @@ _SIGS = {
     "stage_pipeline_handoff_stats": (C.c_int, [C.c_void_p, C.c_int, C.POINTER(C.c_int64), C.POINTER(C.c_int64)]),
     "stage_pipeline_last_error": (C.c_char_p, [C.c_void_p]),
     "stage_pipeline_destroy": (None, [C.c_void_p]),
+    "stage_op_q8_device_bytes": (C.c_int, [C.c_int64, C.c_int64, C.POINTER(C.c_size_t), C.POINTER(C.c_size_t)]),
+    "stage_op_q8_pack": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p]),
+    "stage_op_gemv": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int64, C.c_int64, C.c_void_p, C.c_int, C.c_void_p,
+                                C.c_float, C.c_void_p, C.c_void_p]),
+    "stage_op_attention_workspace_bytes": (C.c_size_t, [C.c_int] * 5),
+    "stage_op_attention_decode": (C.c_int, [C.c_void_p] * 5 + [C.c_int] * 6 + [C.c_void_p, C.c_void_p, C.c_size_t,
+                                                                              C.c_void_p]),
+    "stage_op_last_error": (C.c_char_p, []),
 }
 
 
 def declared_symbols() -> list:
-    """Every function include/stage.h declares (parsed from the header)."""
+    """Every function the headers in include/ declare (parsed from the headers)."""
     import re
-    hdr = os.path.join(_build.ROOT, "include", "stage.h")
-    return re.findall(r"^STAGE_API [^(]*?\b(stage_\w+)\(", open(hdr).read(), flags=re.M)
+    names = []
+    inc = os.path.join(_build.ROOT, "include")
+    for h in sorted(os.listdir(inc)):
+        if h.endswith(".h"):
+            names += re.findall(r"^STAGE_API [^(]*?\b(stage_\w+)\(", open(os.path.join(inc, h)).read(), flags=re.M)
+    return names
 
 
 def lib():
@@ -344,3 +356,41 @@ def stage_pipeline_handoff_stats(p, boundary: int):
 
 def stage_pipeline_destroy(p) -> None:
     lib().stage_pipeline_destroy(p)
+
+
+# ----------------------------------------------------------------------------- kernel-level entry points
+
+def _opcheck(rc):
+    if rc != STAGE_OK:
+        raise StageError(rc, lib().stage_op_last_error().decode())
+
+
+def stage_op_q8_device_bytes(rows: int, cols: int):
+    qb, sb = C.c_size_t(), C.c_size_t()
+    _opcheck(lib().stage_op_q8_device_bytes(rows, cols, C.byref(qb), C.byref(sb)))
+    return qb.value, sb.value
+
+
+def stage_op_q8_pack(m, q_dev, s_dev) -> None:
+    keep = _Keep()
+    h = keep.q8(m)
+    _opcheck(lib().stage_op_q8_pack(C.byref(h), q_dev.data_ptr(), s_dev.data_ptr()))
+
+
+def stage_op_gemv(q_dev, s_dev, rows: int, cols: int, x, y, gamma=None, eps: float = 1e-5, stream=None) -> None:
+    _opcheck(lib().stage_op_gemv(q_dev.data_ptr(), s_dev.data_ptr(), rows, cols, x.data_ptr(), x.shape[0],
+                                 None if gamma is None else gamma.data_ptr(), eps, y.data_ptr(), _stream(stream)))
+
+
+def stage_op_attention_workspace_bytes(n_tok, n_q_heads, n_kv_heads, head_dim, n_chunks) -> int:
+    return int(lib().stage_op_attention_workspace_bytes(n_tok, n_q_heads, n_kv_heads, head_dim, n_chunks))
+
+
+def stage_op_attention_decode(q, k_cache, v_cache, seq, pos, out, n_chunks: int, workspace, stream=None) -> None:
+    """q [n_tok, Hq, D] f32; k/v_cache [seqs, Hkv, max_len, D] f16; seq/pos int32 [n_tok] (device tensors)."""
+    n_tok, hq, d = q.shape
+    hkv, max_len = k_cache.shape[1], k_cache.shape[2]
+    _opcheck(lib().stage_op_attention_decode(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), seq.data_ptr(),
+                                             pos.data_ptr(), n_tok, hq, hkv, d, max_len, n_chunks, out.data_ptr(),
+                                             workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                                             _stream(stream)))

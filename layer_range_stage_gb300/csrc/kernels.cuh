@@ -12,6 +12,11 @@ enum GemvEpi { EPI_STORE = 0, EPI_RESID = 1, EPI_SWIGLU = 2, EPI_QKV = 3 };
 // Device int8 block-32 matrix: q [N][Kp] stored biased (byte = q + 128), s [N][Kp/32] fp16 bits,
 // Kp = K rounded up to 256 (the padding columns face zero inputs).  Row order is the device
 // order chosen at import.
+// Rows of a device matrix are padded to a multiple of this many weights (every row of bytes
+// and of fp16 scales then starts on a 16-byte boundary).
+constexpr int kRowPad = 256;
+inline int row_pad(int k) { return (k + kRowPad - 1) / kRowPad * kRowPad; }
+
 struct DevQ8 {
   uint8_t* q = nullptr;
   uint16_t* s = nullptr;

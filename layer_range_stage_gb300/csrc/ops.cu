@@ -1,0 +1,148 @@
+// Kernel-level entry points of include/stage_ops.h: the GEMV and decode-attention kernels
+// of the stage, on caller-owned device buffers.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "../../include/stage_ops.h"
+#include "kernels.cuh"
+
+namespace {
+
+thread_local std::string g_op_error;
+
+int op_err(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_op_error = buf;
+  return code;
+}
+
+int op_cuda(cudaError_t e, const char* where) { return op_err(STAGE_E_CUDA, "%s: %s", where, cudaGetErrorString(e)); }
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15) == 0; }
+
+int check_attention(const float* q, const uint16_t* kc, const uint16_t* vc, const int32_t* seq, const int32_t* pos,
+                    int n_tok, int hq, int hkv, int d, int max_len, int n_chunks, const float* out) {
+  if (!q || !kc || !vc || !seq || !pos || !out) return op_err(STAGE_E_INVALID, "null pointer");
+  if (!aligned16(q) || !aligned16(kc) || !aligned16(vc) || !aligned16(out))
+    return op_err(STAGE_E_INVALID, "q, caches and out must be 16-byte aligned");
+  if (n_tok <= 0 || hq <= 0 || hkv <= 0 || max_len <= 0) return op_err(STAGE_E_INVALID, "non-positive size");
+  if (hq % hkv || !lrs::attn_decode_supported(d, hq / hkv))
+    return op_err(STAGE_E_INVALID, "head_dim must be 64 or 128 and n_q_heads / n_kv_heads in {1, 2, 4, 8}");
+  if (n_chunks < 1 || n_chunks > lrs::kAttnMaxChunks) return op_err(STAGE_E_INVALID, "n_chunks outside [1, 64]");
+  if (n_tok > 65535) return op_err(STAGE_E_INVALID, "n_tok too large");
+  return STAGE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* stage_op_last_error(void) { return g_op_error.c_str(); }
+
+int stage_op_q8_device_bytes(int64_t rows, int64_t cols, size_t* q_bytes, size_t* s_bytes) {
+  if (rows <= 0 || cols <= 0 || cols > (1 << 30) || !q_bytes || !s_bytes) return op_err(STAGE_E_INVALID, "bad shape");
+  const int64_t kp = lrs::row_pad((int)cols);
+  *q_bytes = (size_t)(rows * kp);
+  *s_bytes = (size_t)(rows * (kp / 32) * 2);
+  return STAGE_OK;
+}
+
+int stage_op_q8_pack(const stage_q8* host, void* q_dev, void* s_dev) {
+  if (!host || !host->q || !host->scale || !q_dev || !s_dev) return op_err(STAGE_E_INVALID, "null pointer");
+  size_t qb = 0, sb = 0;
+  if (int rc = stage_op_q8_device_bytes(host->rows, host->cols, &qb, &sb)) return rc;
+  const int64_t rows = host->rows, cols = host->cols, kp = lrs::row_pad((int)cols);
+  const int64_t nb_src = (cols + 31) / 32, nb = kp / 32;
+  std::vector<uint8_t> q(qb, 0x80u);  // biased zero in the padding
+  std::vector<uint16_t> s(sb / 2, 0);
+  for (int64_t r = 0; r < rows; ++r) {
+    for (int64_t c = 0; c < cols; ++c) q[r * kp + c] = (uint8_t)host->q[r * cols + c] ^ 0x80u;
+    std::memcpy(&s[r * nb], host->scale + r * nb_src, (size_t)nb_src * 2);
+  }
+  cudaError_t e = cudaMemcpy(q_dev, q.data(), qb, cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = cudaMemcpy(s_dev, s.data(), sb, cudaMemcpyHostToDevice);
+  return e == cudaSuccess ? STAGE_OK : op_cuda(e, "pack");
+}
+
+int stage_op_gemv(const void* q_dev, const void* s_dev, int64_t rows, int64_t cols, const float* x_dev, int n_tok,
+                  const float* gamma_dev, float eps, float* y_dev, void* stream) {
+  if (!q_dev || !s_dev || !x_dev || !y_dev) return op_err(STAGE_E_INVALID, "null pointer");
+  if (rows <= 0 || cols <= 0 || rows > (1 << 30) || cols > (1 << 24) || n_tok <= 0)
+    return op_err(STAGE_E_INVALID, "bad shape");
+  if (cols % 4) return op_err(STAGE_E_INVALID, "cols must be a multiple of 4");
+  if (!aligned16(q_dev) || !aligned16(s_dev) || !aligned16(x_dev)) return op_err(STAGE_E_INVALID, "unaligned pointer");
+  cudaError_t e = lrs::prepare_kernels();
+  if (e != cudaSuccess) return op_cuda(e, "kernel setup");
+  lrs::GemvArgs g;
+  g.w.q = (uint8_t*)q_dev;
+  g.w.s = (uint16_t*)s_dev;
+  g.w.N = (int)rows;
+  g.w.K = (int)cols;
+  g.w.Kp = lrs::row_pad((int)cols);
+  g.x = x_dev;
+  g.ldx = (int)cols;
+  g.ntok = n_tok;
+  g.gamma = gamma_dev;
+  g.eps = eps;
+  g.epi = lrs::EPI_STORE;
+  g.out = y_dev;
+  g.ldo = (int)rows;
+  e = lrs::launch_gemv(g, (cudaStream_t)stream);
+  return e == cudaSuccess ? STAGE_OK : op_cuda(e, "gemv");
+}
+
+size_t stage_op_attention_workspace_bytes(int n_tok, int n_q_heads, int n_kv_heads, int head_dim, int n_chunks) {
+  if (n_tok <= 0 || n_q_heads <= 0 || n_kv_heads <= 0 || head_dim <= 0 || n_chunks <= 0) return 0;
+  const size_t part_o = (size_t)n_tok * n_q_heads * n_chunks * head_dim * 4;
+  const size_t part_ml = (size_t)n_tok * n_q_heads * n_chunks * 8;
+  const size_t counters = (size_t)n_tok * n_kv_heads * 4;
+  return (part_o + 255) / 256 * 256 + (part_ml + 255) / 256 * 256 + counters;
+}
+
+int stage_op_attention_decode(const float* q_dev, const uint16_t* k_cache_dev, const uint16_t* v_cache_dev,
+                              const int32_t* seq_dev, const int32_t* pos_dev, int n_tok, int n_q_heads, int n_kv_heads,
+                              int head_dim, int max_len, int n_chunks, float* out_dev, void* workspace_dev,
+                              size_t workspace_bytes, void* stream) {
+  if (int rc = check_attention(q_dev, k_cache_dev, v_cache_dev, seq_dev, pos_dev, n_tok, n_q_heads, n_kv_heads, head_dim,
+                               max_len, n_chunks, out_dev))
+    return rc;
+  const size_t need = stage_op_attention_workspace_bytes(n_tok, n_q_heads, n_kv_heads, head_dim, n_chunks);
+  if (!workspace_dev || workspace_bytes < need || !aligned16(workspace_dev))
+    return op_err(STAGE_E_INVALID, "workspace must be 16-byte aligned and hold %zu bytes", need);
+  cudaError_t e = lrs::prepare_kernels();
+  if (e != cudaSuccess) return op_cuda(e, "kernel setup");
+  char* ws = (char*)workspace_dev;
+  const size_t part_o = (size_t)n_tok * n_q_heads * n_chunks * head_dim * 4;
+  const size_t part_ml = (size_t)n_tok * n_q_heads * n_chunks * 8;
+  lrs::AttnArgs a;
+  a.q = q_dev;
+  a.kc = (const __half*)k_cache_dev;
+  a.vc = (const __half*)v_cache_dev;
+  a.seq = seq_dev;
+  a.pos = pos_dev;
+  a.out = out_dev;
+  a.part_o = (float*)ws;
+  a.part_ml = (float2*)(ws + (part_o + 255) / 256 * 256);
+  a.counters = (int*)(ws + (part_o + 255) / 256 * 256 + (part_ml + 255) / 256 * 256);
+  a.ntok = n_tok;
+  a.Hq = n_q_heads;
+  a.Hkv = n_kv_heads;
+  a.D = head_dim;
+  a.max_len = max_len;
+  a.n_chunks = n_chunks;
+  a.scale = (float)(1.0 / std::sqrt((double)head_dim));
+  e = lrs::launch_attn_decode(a, (cudaStream_t)stream);
+  return e == cudaSuccess ? STAGE_OK : op_cuda(e, "attention");
+}
+
+}  // extern "C"

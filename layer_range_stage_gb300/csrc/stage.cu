@@ -32,9 +32,7 @@ constexpr int kMaxChunks = lrs::kAttnMaxChunks;
 constexpr size_t kAlign = 256;
 
 inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
-// Device rows are padded to a multiple of 256 weights, so every row of int8 data and of
-// fp16 scales starts on a 16-byte boundary (the bulk copies of the streaming GEMV need it).
-inline int kpad(int k) { return (k + 255) / 256 * 256; }
+inline int kpad(int k) { return lrs::row_pad(k); }
 
 struct LayerDev {
   float* attn_norm = nullptr;
