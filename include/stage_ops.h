@@ -55,6 +55,27 @@ STAGE_API int stage_op_attention_decode(const float* q_dev, const uint16_t* k_ca
                                         int n_kv_heads, int head_dim, int max_len, int n_chunks, float* out_dev,
                                         void* workspace_dev, size_t workspace_bytes, void* stream);
 
+/* Decode attention that allocates nothing: the same computation and arguments as
+ * stage_op_attention_decode, without the workspace.  The pages have no counterpart; this
+ * is for callers that cannot allocate device memory at the point they run attention --
+ * a host process that owns all device memory through its own allocator and forbids
+ * untracked allocations, or a latency-critical loop that must not call cudaMalloc (which
+ * can synchronise the device and take unbounded time).
+ *   - Scratch is one fixed array inside this library, STAGE_OP_STATIC_SCRATCH_BYTES bytes,
+ *     resident on every GPU that loads the library until the process exits.  A request
+ *     needing more (stage_op_attention_workspace_bytes) fails with STAGE_E_INVALID.
+ *   - The first call on a device looks up that device's address of the array (with the
+ *     device current); make that first call before any stream capture.
+ *   - Every call reuses the same array and clears its counters on `stream` before the
+ *     kernel.  Calls whose kernels overlap on the GPU (on different streams, or different
+ *     host threads) race on the array and give wrong results: serialise them.
+ *   - No cudaMalloc, cudaFree or allocating library call is made. */
+#define STAGE_OP_STATIC_SCRATCH_BYTES (4u << 20)
+STAGE_API int stage_op_attention_decode_static(const float* q_dev, const uint16_t* k_cache_dev,
+                                               const uint16_t* v_cache_dev, const int32_t* seq_dev,
+                                               const int32_t* pos_dev, int n_tok, int n_q_heads, int n_kv_heads,
+                                               int head_dim, int max_len, int n_chunks, float* out_dev, void* stream);
+
 /* Message of the last failed stage_op_* call on the calling thread ("" if none). */
 STAGE_API const char* stage_op_last_error(void);
 

@@ -100,6 +100,7 @@ _SIGS = {
     "stage_op_attention_workspace_bytes": (C.c_size_t, [C.c_int] * 5),
     "stage_op_attention_decode": (C.c_int, [C.c_void_p] * 5 + [C.c_int] * 6 + [C.c_void_p, C.c_void_p, C.c_size_t,
                                                                               C.c_void_p]),
+    "stage_op_attention_decode_static": (C.c_int, [C.c_void_p] * 5 + [C.c_int] * 6 + [C.c_void_p, C.c_void_p]),
     "stage_op_last_error": (C.c_char_p, []),
 }
 
@@ -394,3 +395,13 @@ def stage_op_attention_decode(q, k_cache, v_cache, seq, pos, out, n_chunks: int,
                                              pos.data_ptr(), n_tok, hq, hkv, d, max_len, n_chunks, out.data_ptr(),
                                              workspace.data_ptr(), workspace.numel() * workspace.element_size(),
                                              _stream(stream)))
+
+
+def stage_op_attention_decode_static(q, k_cache, v_cache, seq, pos, out, n_chunks: int, stream=None) -> None:
+    """stage_op_attention_decode without a workspace: scratch is the library's fixed array
+    (no device allocation; calls must not overlap on the GPU)."""
+    n_tok, hq, d = q.shape
+    hkv, max_len = k_cache.shape[1], k_cache.shape[2]
+    _opcheck(lib().stage_op_attention_decode_static(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                                                    seq.data_ptr(), pos.data_ptr(), n_tok, hq, hkv, d, max_len,
+                                                    n_chunks, out.data_ptr(), _stream(stream)))

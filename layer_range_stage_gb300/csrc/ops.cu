@@ -6,11 +6,17 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <string>
 #include <vector>
 
 #include "../../include/stage_ops.h"
 #include "kernels.cuh"
+
+// Scratch of stage_op_attention_decode_static: one array per device for the life of the
+// process.  In host code this name is only a handle: its device address comes from
+// cudaGetSymbolAddress, looked up once per device with that device current.
+static __device__ __align__(256) unsigned char g_attn_static_scratch[STAGE_OP_STATIC_SCRATCH_BYTES];
 
 namespace {
 
@@ -29,6 +35,26 @@ int op_err(int code, const char* fmt, ...) {
 int op_cuda(cudaError_t e, const char* where) { return op_err(STAGE_E_CUDA, "%s: %s", where, cudaGetErrorString(e)); }
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15) == 0; }
+
+constexpr int kMaxDevices = 64;
+std::mutex g_static_mu;
+void* g_static_addr[kMaxDevices] = {};
+
+int static_scratch_address(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return op_cuda(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return op_err(STAGE_E_INVALID, "device %d beyond the supported %d", dev, kMaxDevices);
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  if (!g_static_addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_attn_static_scratch);
+    if (e != cudaSuccess || !p) return op_cuda(e == cudaSuccess ? cudaErrorInvalidSymbol : e, "cudaGetSymbolAddress");
+    g_static_addr[dev] = p;
+  }
+  *out = g_static_addr[dev];
+  return STAGE_OK;
+}
 
 int check_attention(const float* q, const uint16_t* kc, const uint16_t* vc, const int32_t* seq, const int32_t* pos,
                     int n_tok, int hq, int hkv, int d, int max_len, int n_chunks, const float* out) {
@@ -143,6 +169,29 @@ int stage_op_attention_decode(const float* q_dev, const uint16_t* k_cache_dev, c
   a.scale = (float)(1.0 / std::sqrt((double)head_dim));
   e = lrs::launch_attn_decode(a, (cudaStream_t)stream);
   return e == cudaSuccess ? STAGE_OK : op_cuda(e, "attention");
+}
+
+int stage_op_attention_decode_static(const float* q_dev, const uint16_t* k_cache_dev, const uint16_t* v_cache_dev,
+                                     const int32_t* seq_dev, const int32_t* pos_dev, int n_tok, int n_q_heads,
+                                     int n_kv_heads, int head_dim, int max_len, int n_chunks, float* out_dev,
+                                     void* stream) {
+  if (int rc = check_attention(q_dev, k_cache_dev, v_cache_dev, seq_dev, pos_dev, n_tok, n_q_heads, n_kv_heads, head_dim,
+                               max_len, n_chunks, out_dev))
+    return rc;
+  const size_t need = stage_op_attention_workspace_bytes(n_tok, n_q_heads, n_kv_heads, head_dim, n_chunks);
+  if (need > STAGE_OP_STATIC_SCRATCH_BYTES)
+    return op_err(STAGE_E_INVALID, "needs %zu bytes of scratch; the library's static scratch holds %u", need,
+                  (unsigned)STAGE_OP_STATIC_SCRATCH_BYTES);
+  void* scratch = nullptr;
+  if (int rc = static_scratch_address(&scratch)) return rc;
+  // the chunk counters must start at zero whatever an earlier call left behind
+  const size_t part_o = (size_t)n_tok * n_q_heads * n_chunks * head_dim * 4;
+  const size_t part_ml = (size_t)n_tok * n_q_heads * n_chunks * 8;
+  const size_t counters_off = (part_o + 255) / 256 * 256 + (part_ml + 255) / 256 * 256;
+  cudaError_t e = cudaMemsetAsync((char*)scratch + counters_off, 0, (size_t)n_tok * n_kv_heads * 4, (cudaStream_t)stream);
+  if (e != cudaSuccess) return op_cuda(e, "clear scratch counters");
+  return stage_op_attention_decode(q_dev, k_cache_dev, v_cache_dev, seq_dev, pos_dev, n_tok, n_q_heads, n_kv_heads,
+                                   head_dim, max_len, n_chunks, out_dev, scratch, STAGE_OP_STATIC_SCRATCH_BYTES, stream);
 }
 
 }  // extern "C"
