@@ -7,7 +7,7 @@
 
 namespace lrs {
 
-enum GemvEpi { EPI_STORE = 0, EPI_RESID = 1, EPI_SWIGLU = 2, EPI_QKV = 3 };
+enum GemvEpi { EPI_STORE = 0, EPI_RESID = 1, EPI_SWIGLU = 2, EPI_QKV = 3, EPI_MOE_SWIGLU = 4 };
 
 // Device int8 block-32 matrix: q [N][Kp] stored biased (byte = q + 128), s [N][Kp/32] fp16 bits,
 // Kp = K rounded up to 256 (the padding columns face zero inputs).  Row order is the device
@@ -53,6 +53,13 @@ struct GemvArgs {
   const float2* rope = nullptr;  // [max_len][D/2] (cos, sin)
   int n_q_heads = 0, n_kv_heads = 0, head_dim = 0, max_len = 0;
   int* err = nullptr;  // device error word: set (never cleared by kernels) when a bounded wait times out
+  // Expert gather (routed MoE).  Row gather: device row r of the launch is row r % rows_per_slot
+  // of expert ids[r / rows_per_slot].  K gather: 16-weight chunk c of a row is chunk
+  // c % seg_chunks of row `row` of expert ids[c / seg_chunks] (expert matrices of seg_rows
+  // rows, rows seg_chunks * 16 weights long).
+  const int* ids = nullptr;
+  const float* slot_w = nullptr;  // EPI_MOE_SWIGLU: out[slot * ldo_slot + i] = silu(g) * u * slot_w[slot]
+  int rows_per_slot = 0, seg_chunks = 0, seg_rows = 0, ldo_slot = 0;
 };
 
 // Split-K grouped-query decode attention over the fp16 cache with a deterministic merge of
@@ -88,5 +95,8 @@ cudaError_t launch_final_norm(const float* x, int ldx, const float* gamma, float
                               float* feat, float* out, int ldo, cudaStream_t st);
 cudaError_t launch_argmax(const float* logits, int V, int n_rows, int* out, cudaStream_t st);
 cudaError_t launch_advance(int* pos, const int* tok, int* hist, int* step, int batch, cudaStream_t st);
+// Top-k routing of each token over n_experts router logits [ntok][n_experts]: the k largest
+// (ties to the lower expert id) in descending order, weights softmax over the selected k.
+cudaError_t launch_topk(const float* logits, int n_experts, int k, int ntok, int* ids, float* wts, cudaStream_t st);
 
 }  // namespace lrs

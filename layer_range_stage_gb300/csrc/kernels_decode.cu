@@ -118,8 +118,22 @@ __global__ void __launch_bounds__(kGemvThreads, BT == 1 ? 3 : 2) gemv_q8_kernel(
       for (int r = 0; r < R; ++r) {
         const int row = row0 + r;
         if (c < nchunk && row < N) {
-          w[u][r] = ld_stream_u4(a.w.q + (size_t)row * Kp + (size_t)c * 16);
-          sc[u][r] = h2f_bits(ld_stream_u16(a.w.s + (size_t)row * nblk + (c >> 1)));
+          size_t qoff, soff;
+          if (a.rows_per_slot) {  // row gather: the row belongs to the expert of its slot
+            const size_t wrow = (size_t)a.ids[row / a.rows_per_slot] * a.rows_per_slot + row % a.rows_per_slot;
+            qoff = wrow * Kp + (size_t)c * 16;
+            soff = wrow * nblk + (c >> 1);
+          } else if (a.seg_chunks) {  // K gather: chunk c lies in the row of the expert of its segment
+            const int j = c / a.seg_chunks, cl = c - j * a.seg_chunks;
+            const size_t wrow = (size_t)a.ids[j] * a.seg_rows + row;
+            qoff = wrow * ((size_t)a.seg_chunks * 16) + (size_t)cl * 16;
+            soff = wrow * (size_t)(a.seg_chunks >> 1) + (cl >> 1);
+          } else {
+            qoff = (size_t)row * Kp + (size_t)c * 16;
+            soff = (size_t)row * nblk + (c >> 1);
+          }
+          w[u][r] = ld_stream_u4(a.w.q + qoff);
+          sc[u][r] = h2f_bits(ld_stream_u16(a.w.s + soff));
         } else {
           w[u][r] = make_uint4(0u, 0u, 0u, 0u);
           sc[u][r] = 0.f;
@@ -131,7 +145,8 @@ __global__ void __launch_bounds__(kGemvThreads, BT == 1 ? 3 : 2) gemv_q8_kernel(
   // before waiting for it (single-pass launches only).
   pdl_trigger();
   bool prefetched = false;
-  if (a.ntok <= BT && gwarp < ngroups) {
+  // (gathered weights depend on the router's output: no prefetch before the wait then)
+  if (a.ntok <= BT && gwarp < ngroups && !a.rows_per_slot && !a.seg_chunks) {
     load_batch(gwarp * R, kslice * 32 * U);
     prefetched = true;
   }
@@ -288,6 +303,9 @@ __global__ void __launch_bounds__(kGemvThreads, BT == 1 ? 3 : 2) gemv_q8_kernel(
             const float y0 = acc[2 * j][b], y1 = acc[2 * j + 1][b];
             if (a.epi == EPI_SWIGLU) {
               a.out[t * a.ldo + (row >> 1)] = silu(y0) * y1;
+            } else if (a.epi == EPI_MOE_SWIGLU) {
+              const int slot = row / a.rows_per_slot, i = (row % a.rows_per_slot) >> 1;
+              a.out[t * a.ldo + (size_t)slot * a.ldo_slot + i] = silu(y0) * y1 * a.slot_w[slot];
             } else {  // EPI_QKV
               const int hd = a.head_dim >> 1, P = row >> 1, head = P / hd, i = P - head * hd;
               const int p = a.pos[t];
@@ -765,6 +783,54 @@ __global__ void advance_kernel(int* pos, const int* tok, int* hist, int* step, i
 cudaError_t launch_advance(int* pos, const int* tok, int* hist, int* step, int batch, cudaStream_t st) {
   return launch_k(advance_kernel, dim3(1), dim3(std::max(32, ((batch + 31) / 32) * 32)), 0, st, pos, tok, hist,
                   step, batch);
+}
+
+// ------------------------------------------------------------------------------------------
+// Top-k routing ("41. Many GPUs: ...", section "MoE layers under tensor parallelism": the
+// gate returns per-token routing weights and expert ids).  One CTA per token, one thread
+// per expert: an expert's rank is the number of experts with a larger logit, or an equal
+// one and a lower id; the k lowest ranks are selected, in rank order.  Softmax over all
+// experts followed by renormalisation over the selected k equals a softmax over the
+// selected logits, which is what is computed.
+
+__global__ void topk_kernel(const float* logits, int E, int k, int* ids, float* wts) {
+  extern __shared__ float lg[];
+  __shared__ float sel[32];
+  __shared__ int sel_id[32];
+  pdl_trigger();
+  pdl_wait();
+  const int t = blockIdx.x;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) lg[e] = logits[(size_t)t * E + e];
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    const float v = lg[e];
+    int rank = 0;
+    for (int f = 0; f < E; ++f) {
+      const float u = lg[f];
+      rank += (u > v) || (u == v && f < e);
+    }
+    if (rank < k) {
+      sel[rank] = v;
+      sel_id[rank] = e;
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const float m = sel[0];
+    float z = 0.f;
+    for (int j = 0; j < k; ++j) z += expf(sel[j] - m);
+    for (int j = 0; j < k; ++j) {
+      ids[(size_t)t * k + j] = sel_id[j];
+      wts[(size_t)t * k + j] = expf(sel[j] - m) / z;
+    }
+  }
+}
+
+cudaError_t launch_topk(const float* logits, int n_experts, int k, int ntok, int* ids, float* wts, cudaStream_t st) {
+  if (ntok <= 0) return cudaSuccess;
+  if (k < 1 || k > 32 || k > n_experts) return cudaErrorInvalidValue;
+  const int threads = std::min(1024, ((n_experts + 31) / 32) * 32);
+  return launch_k(topk_kernel, dim3(ntok), dim3(threads), (size_t)n_experts * 4, st, logits, n_experts, k, ids, wts);
 }
 
 cudaError_t prepare_kernels() {

@@ -48,7 +48,7 @@ void walk_plan(const stage_model_cfg& c, int begin, int end, std::vector<LayerDe
                DevQ8* head, float** final_norm, __half** kc, __half** vc, float2** rope, float** qbuf,
                float** obuf, float** abuf, float** feat, float** logits, int** argmax, float** part_o,
                float2** part_ml, int** counters, int** d_seq, int** d_pos, int** d_tok, int** d_rows, int** err_word,
-               F&& f) {
+               float** moe_logits, int** moe_ids, float** moe_wts, F&& f) {
   auto q8 = [&](DevQ8* m, int N, int K) {
     if (m) {
       m->N = N;
@@ -85,7 +85,7 @@ void walk_plan(const stage_model_cfg& c, int begin, int end, std::vector<LayerDe
   f(kv, (void**)vc);
   f((size_t)c.max_seq_len * (D / 2) * 8, (void**)rope);
   const size_t T = (size_t)c.max_tokens;
-  const int ffn_w = moe ? c.top_k * c.expert_ffn : c.ffn;
+  const int ffn_w = moe ? c.top_k * kpad(c.expert_ffn) : c.ffn;
   f(T * Hq * D * 4, (void**)qbuf);
   f(T * Hq * D * 4, (void**)obuf);
   f(T * (size_t)std::max(ffn_w, H) * 4, (void**)abuf);
@@ -103,6 +103,11 @@ void walk_plan(const stage_model_cfg& c, int begin, int end, std::vector<LayerDe
   f(T * 4, (void**)d_tok);
   f(T * 4, (void**)d_rows);
   f(4, (void**)err_word);
+  if (moe) {
+    f(T * c.n_experts * 4, (void**)moe_logits);
+    f(T * c.top_k * 4, (void**)moe_ids);
+    f(T * c.top_k * 4, (void**)moe_wts);
+  }
 }
 
 thread_local std::string g_create_error;
@@ -110,8 +115,8 @@ thread_local std::string g_create_error;
 size_t plan_bytes(const stage_model_cfg& c, int begin, int end) {
   size_t total = 0;
   walk_plan(c, begin, end, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
-            nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
-            [&](size_t b, void**) { total += round_up(b, kAlign); });
+            nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
+            nullptr, nullptr, [&](size_t b, void**) { total += round_up(b, kAlign); });
   return total;
 }
 
@@ -166,6 +171,9 @@ struct stage {
   int* counters = nullptr;
   int *d_seq = nullptr, *d_pos = nullptr, *d_tok = nullptr, *d_rows = nullptr;
   int* err_word = nullptr;     // device: set by a kernel whose bounded wait timed out
+  float* moe_logits = nullptr;  // [max_tokens][n_experts] router logits
+  int* moe_ids = nullptr;       // [max_tokens][top_k] selected experts
+  float* moe_wts = nullptr;     // [max_tokens][top_k] routing weights
   int32_t* h_stage = nullptr;  // pinned host staging [4][max_tokens]
   cudaEvent_t staged = nullptr;  // recorded after the last copy out of h_stage
   std::vector<int> committed, pending;
@@ -426,7 +434,63 @@ int forward_dev(stage* st, int n, const int* d_seq, const int* d_pos, const int*
     o.err = st->err_word;
     if ((e = lrs::launch_gemv(o, s)) != cudaSuccess) return cuda_err(st, e, "o_proj");
 
-    if (c.n_experts > 0) return set_err(st, STAGE_E_INVALID, "MoE forward not built yet");
+    if (c.n_experts > 0) {
+      // routed experts: router GEMV (RMSNorm prologue) -> top-k -> per token the selected
+      // experts' gate/up (row gather, SwiGLU scaled by the routing weight) and down
+      // (K gather over the k slots, residual add)
+      const int E = c.n_experts, kk = c.top_k, EF = c.expert_ffn, KpE = kpad(EF);
+      lrs::GemvArgs r;
+      r.w = L.router;
+      r.x = hout;
+      r.ldx = H;
+      r.ntok = n;
+      r.gamma = L.ffn_norm;
+      r.eps = c.rms_eps;
+      r.epi = lrs::EPI_STORE;
+      r.out = st->moe_logits;
+      r.ldo = E;
+      r.err = st->err_word;
+      if ((e = lrs::launch_gemv(r, s)) != cudaSuccess) return cuda_err(st, e, "router");
+      if ((e = lrs::launch_topk(st->moe_logits, E, kk, n, st->moe_ids, st->moe_wts, s)) != cudaSuccess)
+        return cuda_err(st, e, "top-k");
+      for (int t = 0; t < n; ++t) {
+        lrs::GemvArgs gu;
+        gu.w = L.egu;
+        gu.w.N = kk * 2 * EF;
+        gu.x = hout + (size_t)t * H;
+        gu.ldx = H;
+        gu.ntok = 1;
+        gu.gamma = L.ffn_norm;
+        gu.eps = c.rms_eps;
+        gu.epi = lrs::EPI_MOE_SWIGLU;
+        gu.out = st->abuf + (size_t)t * kk * KpE;
+        gu.ids = st->moe_ids + (size_t)t * kk;
+        gu.slot_w = st->moe_wts + (size_t)t * kk;
+        gu.rows_per_slot = 2 * EF;
+        gu.ldo_slot = KpE;
+        gu.err = st->err_word;
+        if ((e = lrs::launch_gemv(gu, s)) != cudaSuccess) return cuda_err(st, e, "expert gate_up");
+        lrs::GemvArgs dn;
+        dn.w = L.edown;
+        dn.w.N = H;
+        dn.w.K = kk * KpE;
+        dn.w.Kp = kk * KpE;
+        dn.x = st->abuf + (size_t)t * kk * KpE;
+        dn.ldx = kk * KpE;
+        dn.ntok = 1;
+        dn.epi = lrs::EPI_RESID;
+        dn.resid = hout + (size_t)t * H;
+        dn.ldr = H;
+        dn.out = hout + (size_t)t * H;
+        dn.ldo = H;
+        dn.ids = st->moe_ids + (size_t)t * kk;
+        dn.seg_chunks = KpE / 16;
+        dn.seg_rows = H;
+        dn.err = st->err_word;
+        if ((e = lrs::launch_gemv(dn, s)) != cudaSuccess) return cuda_err(st, e, "expert down");
+      }
+      continue;
+    }
     lrs::GemvArgs gu;
     gu.w = L.wgu;
     gu.x = hout;
@@ -612,7 +676,7 @@ int stage_create(const stage_model_cfg* cfg, stage_layer_range range, const stag
   walk_plan(*cfg, range.begin, range.end, &st->layers, &st->embed, &st->head, &st->final_norm, &st->kc, &st->vc,
             &st->rope, &st->qbuf, &st->obuf, &st->abuf, &st->feat, &st->logits, &st->argmax, &st->part_o,
             &st->part_ml, &st->counters, &st->d_seq, &st->d_pos, &st->d_tok, &st->d_rows, &st->err_word,
-            [&](size_t b, void** slot) {
+            &st->moe_logits, &st->moe_ids, &st->moe_wts, [&](size_t b, void** slot) {
               if (slot) *slot = st->arena + off;
               off += round_up(b, kAlign);
             });

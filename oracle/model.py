@@ -266,7 +266,8 @@ class Stage:
     exposed as objects with ``.q`` and ``.s``.
     """
 
-    def __init__(self, cfg, begin: int, end: int, weights, max_seqs: int = 1, max_len: int = 256):
+    def __init__(self, cfg, begin: int, end: int, weights, max_seqs: int = 1, max_len: int = 256,
+                 cache_dequant: bool = True):
         if not (0 <= begin < end <= cfg.n_layers):
             raise ValueError("bad layer range")
         self.cfg, self.begin, self.end = cfg, begin, end
@@ -278,6 +279,7 @@ class Stage:
         self.v_cache = np.zeros(shape, dtype=np.float16)
         self.features: Optional[np.ndarray] = None
         self._deq_cache: Dict[int, np.ndarray] = {}
+        self.cache_dequant = cache_dequant
 
     # dequantised matrices (cached by identity; the oracle is allowed to be slow, not wasteful)
     def _deq(self, m) -> np.ndarray:
@@ -290,7 +292,7 @@ class Stage:
         self._deq_cache.clear()
 
     def forward(self, seq_ids, positions, tokens=None, hidden_in=None, gemm: str = "f32",
-                cache_dequant: bool = True) -> np.ndarray:
+                cache_dequant: Optional[bool] = None) -> np.ndarray:
         """Run n tokens through this stage's blocks; returns the float32 hidden [n, H].
 
         The first stage embeds ``tokens``; any other stage takes ``hidden_in`` (float32
@@ -306,6 +308,8 @@ class Stage:
         positions = np.asarray(positions, dtype=np.int64)
         n = len(positions)
         rnd = bf16 if gemm == "bf16" else (lambda t: t)
+        if cache_dequant is None:
+            cache_dequant = self.cache_dequant
         deq = (lambda m: rnd(self._deq(m))) if cache_dequant else (lambda m: rnd(dequant(m.q, m.s)))
         if self.first:
             if tokens is None or hidden_in is not None:
@@ -335,7 +339,7 @@ class Stage:
             # FFN sub-block: h = norm(x); x += FFN(h)
             h = f32(rmsnorm(x, lw.ffn_norm, c.rms_eps))
             if c.is_moe:
-                ffn, _, _ = moe_ffn(h, self._deq(lw.router), lambda e: deq(lw.e_gate[e]),
+                ffn, _, _ = moe_ffn(h, deq(lw.router) if gemm != "bf16" else self._deq(lw.router), lambda e: deq(lw.e_gate[e]),
                                     lambda e: deq(lw.e_up[e]), lambda e: deq(lw.e_down[e]), c.top_k, rnd)
             else:
                 ffn = swiglu(h, deq(lw.w_gate), deq(lw.w_up), deq(lw.w_down), rnd)
