@@ -31,9 +31,15 @@ sys.path.insert(0, ROOT)
 
 import synth  # noqa: E402
 
+# workloads: the dense 8B-shape decoder (default) and the 40-block MoE decoder
+WORKLOADS = {
+    1: dict(context=2048, bounds=[0, 16, 32],
+            name="dense 8B-shape decode, 32 blocks as 2 stages 16/16, batch 1, context 2048"),
+    2: dict(context=4096, bounds=[0, 21, 40],
+            name="MoE 40-block decode (128 experts top-8), 2 stages 21/19, batch 1, context 4096"),
+}
 CFG_ID = 1
 CONTEXT = 2048
-BOUNDS = [0, 16, 32]
 
 
 def measured_peaks():
@@ -44,10 +50,15 @@ def measured_peaks():
 
 
 def bytes_per_token(model, context):
-    """Algorithmic bytes of one decode token: every weight byte once (1 B int8 + 2 B per 32
-    scale = 1.0625 B/param) plus the fp16 K and V rows of every position attended."""
+    """Algorithmic bytes of one decode token: every weight byte the token needs once (1 B
+    int8 + 2 B per 32-weight scale = 1.0625 B/param; for MoE only the router and the top-k
+    experts) plus the fp16 K and V rows of every position attended."""
     H, D = model.hidden, model.head_dim
-    per_layer = (model.q_dim + 2 * model.kv_dim) * H + H * model.q_dim + 3 * model.ffn * H
+    per_layer = (model.q_dim + 2 * model.kv_dim) * H + H * model.q_dim
+    if model.is_moe:
+        per_layer += model.n_experts * H + model.top_k * 3 * model.expert_ffn * H
+    else:
+        per_layer += 3 * model.ffn * H
     params = per_layer * model.n_layers + model.vocab * H  # readout; the embedding reads one row
     w = params * 1.0625 + H * 1.0625
     kv = model.n_layers * 2 * model.n_kv_heads * context * D * 2
@@ -108,9 +119,10 @@ def run_gpu(args):
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl")
-    model = synth.CONFIGS[CFG_ID]
-    bounds = BOUNDS
-    context = args.context
+    wl = WORKLOADS[args.config]
+    model = synth.CONFIGS[args.config]
+    bounds = wl["bounds"]
+    context = args.context or wl["context"]
     if args.layers:  # reduced depth: profiling of a small case only, never a bench line
         model = synth.reduced(model, args.layers)
         bounds = [0, args.layers // 2, args.layers] if args.layers > 1 else [0, 1]
@@ -172,13 +184,13 @@ def run_gpu(args):
     peaks = measured_peaks()
     peak = peaks.get("hbm_gbs")
     line = {
-        "metric": "decode tok/s (batch-1 greedy, 8B-shape int8 block-32, 2 stages 16/16, ctx 2048)",
+        "metric": "decode tok/s",
         "value": round(tok_s, 2), "unit": "tok/s", "n_gpus": world, "steps": steps, "warmup": warmup,
         "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32 (int8 block-32 weights, fp16 KV)", "data": "synthetic (seeded N(0,0.02) weights, seeded prompt)",
-        "config": {"workload": "dense 8B-shape decode, 32 blocks as 2 stages 16/16, batch 1, context 2048",
+        "config": {"workload": wl["name"],
                    "parallelism": "replicas only" if world > 1 else "single GPU, 2 chained stages",
-                   "l2": "weights 7.5 GB > L2 each step (no flush needed)"},
+                   "l2": f"inputs larger than L2: {w_bytes / 1e9:.2f} GB of weights streamed per step"},
         "hbm_gbs_achieved": round(gbs, 1),
         "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(gbs / peak, 4) if peak else None, "traffic": None,
@@ -186,12 +198,12 @@ def run_gpu(args):
                      "peak_source": "measured" if peak else "fallback"},
         "e2e": e2e,
         "clocks": clk,
-        "gpu_launches": None,
+        "gpu_launches": steps * (1 + model.n_layers * (7 if model.is_moe else 5) + 4),
         "build_s": round(build_s, 1),
     }
-    if args.layers or args.context != CONTEXT:
+    if args.layers or args.context:
         line["config"]["profiling_case"] = f"{model.n_layers} blocks, context {context}: not the benchmark workload"
-    if rank == 0 and not args.no_cpu_baseline and world == 1:
+    if rank == 0 and not args.no_cpu_baseline and world == 1 and args.config == 1:
         line["cpu_baseline"] = cpu_baseline(args)
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -230,11 +242,11 @@ def run_reference(args):
     if rank != 0:
         return
     cb = cpu_baseline(args)
-    line = {"impl": "reference", "metric": "decode tok/s (batch-1 greedy, 8B-shape int8 block-32, 2 stages 16/16, ctx 2048)",
+    line = {"impl": "reference", "metric": "decode tok/s",
             "value": cb["value"], "unit": "tok/s", "n_gpus": int(os.environ.get("WORLD_SIZE", "1")),
             "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": "dense 8B-shape decode, 32 blocks as 2 stages 16/16, batch 1, context 2048"},
+            "config": {"workload": WORKLOADS[1]["name"]},
             "cpu_baseline": cb, "e2e": {"value": cb["value"], "unit": "tok/s", "h2d_bytes_per_step": 0,
                                         "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -248,7 +260,8 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=0, help="reduced depth, for profiling small cases only")
-    ap.add_argument("--context", type=int, default=CONTEXT)
+    ap.add_argument("--context", type=int, default=0, help="decode context (default: the workload's)")
+    ap.add_argument("--config", type=int, default=1, choices=sorted(WORKLOADS), help="1: dense 8B-shape, 2: MoE")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -93,7 +93,8 @@ __device__ __forceinline__ float dot16_u8(const uint4 w, const float4 x0, const 
   return acc;
 }
 
-template <int R, int U, int BT, int KS>
+// GATHER: 0 plain rows, 1 row gather (expert gate/up), 2 K gather (expert down).
+template <int R, int U, int BT, int KS, int GATHER = 0>
 __global__ void __launch_bounds__(kGemvThreads, BT == 1 ? 3 : 2) gemv_q8_kernel(const GemvArgs a) {
   extern __shared__ __align__(16) float smem[];
   constexpr int NW = kGemvThreads / 32, RG = NW / KS;  // warps, row groups per CTA
@@ -119,11 +120,11 @@ __global__ void __launch_bounds__(kGemvThreads, BT == 1 ? 3 : 2) gemv_q8_kernel(
         const int row = row0 + r;
         if (c < nchunk && row < N) {
           size_t qoff, soff;
-          if (a.rows_per_slot) {  // row gather: the row belongs to the expert of its slot
+          if (GATHER == 1) {  // row gather: the row belongs to the expert of its slot
             const size_t wrow = (size_t)a.ids[row / a.rows_per_slot] * a.rows_per_slot + row % a.rows_per_slot;
             qoff = wrow * Kp + (size_t)c * 16;
             soff = wrow * nblk + (c >> 1);
-          } else if (a.seg_chunks) {  // K gather: chunk c lies in the row of the expert of its segment
+          } else if (GATHER == 2) {  // K gather: chunk c lies in the row of the expert of its segment
             const int j = c / a.seg_chunks, cl = c - j * a.seg_chunks;
             const size_t wrow = (size_t)a.ids[j] * a.seg_rows + row;
             qoff = wrow * ((size_t)a.seg_chunks * 16) + (size_t)cl * 16;
@@ -146,7 +147,7 @@ __global__ void __launch_bounds__(kGemvThreads, BT == 1 ? 3 : 2) gemv_q8_kernel(
   pdl_trigger();
   bool prefetched = false;
   // (gathered weights depend on the router's output: no prefetch before the wait then)
-  if (a.ntok <= BT && gwarp < ngroups && !a.rows_per_slot && !a.seg_chunks) {
+  if (GATHER == 0 && a.ntok <= BT && gwarp < ngroups) {
     load_batch(gwarp * R, kslice * 32 * U);
     prefetched = true;
   }
@@ -342,22 +343,22 @@ static size_t gemv_smem(int Kp) {
 
 // Launch attributes are fixed once, outside any stream capture (prepare_kernels); the
 // launch itself only computes the grid from the recorded register count.
-template <int R, int U, int BT, int KS>
+template <int R, int U, int BT, int KS, int GATHER>
 struct GemvInfo {
   static int regs;
 };
-template <int R, int U, int BT, int KS>
-int GemvInfo<R, U, BT, KS>::regs = 0;
+template <int R, int U, int BT, int KS, int GATHER>
+int GemvInfo<R, U, BT, KS, GATHER>::regs = 0;
 
-template <int R, int U, int BT, int KS>
+template <int R, int U, int BT, int KS, int GATHER = 0>
 static cudaError_t prepare_gemv() {
-  cudaError_t e = cudaFuncSetAttribute(gemv_q8_kernel<R, U, BT, KS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)kGemvSmemBudget + 4096);
+  cudaError_t e = cudaFuncSetAttribute(gemv_q8_kernel<R, U, BT, KS, GATHER>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemvSmemBudget + 4096);
   if (e != cudaSuccess) return e;
   cudaFuncAttributes fa;
-  e = cudaFuncGetAttributes(&fa, gemv_q8_kernel<R, U, BT, KS>);
+  e = cudaFuncGetAttributes(&fa, gemv_q8_kernel<R, U, BT, KS, GATHER>);
   if (e != cudaSuccess) return e;
-  GemvInfo<R, U, BT, KS>::regs = fa.numRegs;
+  GemvInfo<R, U, BT, KS, GATHER>::regs = fa.numRegs;
   return cudaSuccess;
 }
 
@@ -370,15 +371,15 @@ static int occupancy(int regs, int threads, size_t smem) {
   return std::max(1, std::min(by_threads, std::min(by_regs, by_smem)));
 }
 
-template <int R, int U, int BT, int KS>
+template <int R, int U, int BT, int KS, int GATHER = 0>
 static cudaError_t launch_gemv_t(const GemvArgs& a, cudaStream_t st) {
-  if (GemvInfo<R, U, BT, KS>::regs == 0) return cudaErrorNotReady;  // prepare_kernels() was not called
+  if (GemvInfo<R, U, BT, KS, GATHER>::regs == 0) return cudaErrorNotReady;  // prepare_kernels() was not called
   const size_t smem = gemv_smem<R, BT>(a.w.Kp);
-  const int occ = occupancy(GemvInfo<R, U, BT, KS>::regs, kGemvThreads, smem);
+  const int occ = occupancy(GemvInfo<R, U, BT, KS, GATHER>::regs, kGemvThreads, smem);
   const int ngroups = (a.w.N + R - 1) / R;
   const int groups_per_cta = (kGemvThreads / 32) / KS;
   const int grid = std::max(1, std::min((ngroups + groups_per_cta - 1) / groups_per_cta, sm_count() * occ));
-  return launch_k(gemv_q8_kernel<R, U, BT, KS>, dim3(grid), dim3(kGemvThreads), smem, st, a);
+  return launch_k(gemv_q8_kernel<R, U, BT, KS, GATHER>, dim3(grid), dim3(kGemvThreads), smem, st, a);
 }
 
 cudaError_t launch_gemv(const GemvArgs& a, cudaStream_t st) {
@@ -388,6 +389,17 @@ cudaError_t launch_gemv(const GemvArgs& a, cudaStream_t st) {
   if (a.ntok >= 2 && gemv_smem<2, 2>(a.w.Kp) <= budget) return launch_gemv_t<2, 4, 2, 1>(a, st);
   // one load round per warp: K split over KS warps so that KS * 32 lanes * U chunks cover K
   const int nchunk = a.w.Kp / 16;
+  if (a.rows_per_slot || a.seg_chunks) {
+    if (a.ntok != 1) return cudaErrorInvalidValue;  // expert launches are per token
+    if (a.rows_per_slot) {
+      if (nchunk > 2 * 32 * 4) return launch_gemv_t<2, 4, 1, 4, 1>(a, st);
+      if (nchunk > 32 * 4) return launch_gemv_t<2, 4, 1, 2, 1>(a, st);
+      return launch_gemv_t<2, 4, 1, 1, 1>(a, st);
+    }
+    if (nchunk > 2 * 32 * 4) return launch_gemv_t<2, 4, 1, 4, 2>(a, st);
+    if (nchunk > 32 * 4) return launch_gemv_t<2, 4, 1, 2, 2>(a, st);
+    return launch_gemv_t<2, 4, 1, 1, 2>(a, st);
+  }
   if (nchunk > 4 * 32 * 4) return launch_gemv_t<2, 4, 1, 8>(a, st);
   if (nchunk > 2 * 32 * 4) return launch_gemv_t<2, 4, 1, 4>(a, st);
   if (nchunk > 32 * 4) return launch_gemv_t<2, 4, 1, 2>(a, st);
@@ -843,6 +855,12 @@ cudaError_t prepare_kernels() {
   if (e == cudaSuccess) e = prepare_gemv<2, 4, 1, 8>();
   if (e == cudaSuccess) e = prepare_gemv<2, 4, 2, 1>();
   if (e == cudaSuccess) e = prepare_gemv<2, 2, 4, 1>();
+  if (e == cudaSuccess) e = prepare_gemv<2, 4, 1, 1, 1>();
+  if (e == cudaSuccess) e = prepare_gemv<2, 4, 1, 2, 1>();
+  if (e == cudaSuccess) e = prepare_gemv<2, 4, 1, 4, 1>();
+  if (e == cudaSuccess) e = prepare_gemv<2, 4, 1, 1, 2>();
+  if (e == cudaSuccess) e = prepare_gemv<2, 4, 1, 2, 2>();
+  if (e == cudaSuccess) e = prepare_gemv<2, 4, 1, 4, 2>();
 
   if (e == cudaSuccess) e = prepare_attn<64, 1>();
   if (e == cudaSuccess) e = prepare_attn<64, 2>();
