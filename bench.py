@@ -40,6 +40,9 @@ WORKLOADS = {
 }
 CFG_ID = 1
 CONTEXT = 2048
+# DRAM bytes (read + write) of one launch of the dominant kernel from an ncu capture of the
+# same launch configuration (profiles/gemv_gateup_decode.md); None until captured.
+TRAFFIC = {1: 128_097_792}
 
 
 def measured_peaks():
@@ -127,7 +130,7 @@ def run_gpu(args):
         model = synth.reduced(model, args.layers)
         bounds = [0, args.layers // 2, args.layers] if args.layers > 1 else [0, 1]
     steps, warmup = args.steps, args.warmup
-    max_len = context + warmup + 2 * steps + 8
+    max_len = context + warmup + 2 * steps + 16
     t_build = time.time()
     gp = build_gpu_pipeline(model, bounds, max_len, max_tokens=512)
     # prefill the seeded context in chunks of 512 tokens through the stages
@@ -164,8 +167,19 @@ def run_gpu(args):
     tok_s = world * 1000.0 / ms_step
     gbs = (w_bytes + kv_bytes) / (ms_step * 1e-3) / 1e9
 
+    # the dominant kernel (the FFN up-projection GEMV, with its fused RMSNorm and SwiGLU)
+    # timed with CUDA events recorded around each of its launches inside a second run of
+    # the same graph-replayed steps (events between kernels cost overlap, so the headline
+    # number above comes from the run without them)
+    gp.kernel_timing(True)
+    nxt = gp.generate([0], last, 4, use_graph=True)[-1]
+    torch.cuda.synchronize()
+    k_us, k_n = gp.kernel_time()
+    gp.kernel_timing(False)
+    last = nxt
+    steps_extra = 4
     # e2e: stage_pipeline_step per token with host buffers (token read back every step)
-    cur = context + warmup + steps
+    cur = context + warmup + steps + steps_extra
     tk = int(last[0])
     for _ in range(2):
         tk = int(gp.step(False, [0], [cur], [tk], rows=[0])[0])
@@ -183,6 +197,10 @@ def run_gpu(args):
 
     peaks = measured_peaks()
     peak = peaks.get("hbm_gbs")
+    H = model.hidden
+    up_rows = (model.top_k * 2 * model.expert_ffn) if model.is_moe else 2 * model.ffn
+    up_bytes = up_rows * H * 1.0625 + H * 4   # weights + scales once, plus the input row
+    k_gbs = up_bytes / (k_us * 1e-6) / 1e9 if k_us else None
     line = {
         "metric": "decode tok/s",
         "value": round(tok_s, 2), "unit": "tok/s", "n_gpus": world, "steps": steps, "warmup": warmup,
@@ -192,10 +210,15 @@ def run_gpu(args):
                    "parallelism": "replicas only" if world > 1 else "single GPU, 2 chained stages",
                    "l2": f"inputs larger than L2: {w_bytes / 1e9:.2f} GB of weights streamed per step"},
         "hbm_gbs_achieved": round(gbs, 1),
-        "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(gbs / peak, 4) if peak else None, "traffic": None,
-                     "kernel": "whole decode step (weights + KV bytes per token / step time)",
-                     "peak_source": "measured" if peak else "fallback"},
+        "roofline": {"bound": "hbm", "achieved": round(k_gbs, 1) if k_gbs else None, "peak": peak, "unit": "GB/s",
+                     "frac": round(k_gbs / peak, 4) if (peak and k_gbs) else None,
+                     "traffic": TRAFFIC.get(args.config) if not args.layers else None,
+                     "kernel": "FFN up-projection GEMV (gate/up + RMSNorm prologue + SwiGLU epilogue)",
+                     "bytes_per_launch": round(up_bytes), "mean_launch_us": round(k_us, 3), "launches_timed": k_n,
+                     "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs)" if peak else "fallback"},
+        "step_roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                          "frac": round(gbs / peak, 4) if peak else None,
+                          "bytes_per_step": round(w_bytes + kv_bytes)},
         "e2e": e2e,
         "clocks": clk,
         "gpu_launches": steps * (1 + model.n_layers * (7 if model.is_moe else 5) + 4),

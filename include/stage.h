@@ -229,6 +229,14 @@ STAGE_API int stage_pipeline_generate(stage_pipeline_t p, int batch, const int32
                             const int32_t* first_tokens_host, int n_steps, int use_graph,
                             int32_t* tokens_out_host);
 
+/* Kernel timing for measurement: with enable = 1 the next captured generate step records a
+ * CUDA event pair around every gate/up (or expert gate/up) GEMV launch of every stage.
+ * stage_pipeline_kernel_time returns the mean duration (microseconds) of those launches in
+ * the last replayed step and their count.  Events sit between kernels, so a timed launch
+ * does not overlap its predecessor; leave timing off for the headline measurement. */
+STAGE_API int stage_pipeline_kernel_timing(stage_pipeline_t p, int enable);
+STAGE_API int stage_pipeline_kernel_time(stage_pipeline_t p, float* mean_us, int* count);
+
 /* Bytes handed across boundary k (0-based) so far, and the number of handoffs. */
 STAGE_API int stage_pipeline_handoff_stats(stage_pipeline_t p, int boundary, int64_t* calls, int64_t* bytes);
 

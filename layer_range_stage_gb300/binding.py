@@ -91,6 +91,8 @@ _SIGS = {
                                       C.c_void_p, C.c_void_p, C.c_void_p]),
     "stage_pipeline_generate": (C.c_int, [C.c_void_p, C.c_int, C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_void_p]),
     "stage_pipeline_handoff_stats": (C.c_int, [C.c_void_p, C.c_int, C.POINTER(C.c_int64), C.POINTER(C.c_int64)]),
+    "stage_pipeline_kernel_timing": (C.c_int, [C.c_void_p, C.c_int]),
+    "stage_pipeline_kernel_time": (C.c_int, [C.c_void_p, C.POINTER(C.c_float), C.POINTER(C.c_int)]),
     "stage_pipeline_last_error": (C.c_char_p, [C.c_void_p]),
     "stage_pipeline_destroy": (None, [C.c_void_p]),
     "stage_op_q8_device_bytes": (C.c_int, [C.c_int64, C.c_int64, C.POINTER(C.c_size_t), C.POINTER(C.c_size_t)]),
@@ -353,6 +355,17 @@ def stage_pipeline_handoff_stats(p, boundary: int):
     c, b = C.c_int64(), C.c_int64()
     _pcheck(p, lib().stage_pipeline_handoff_stats(p, boundary, C.byref(c), C.byref(b)))
     return c.value, b.value
+
+
+def stage_pipeline_kernel_timing(p, enable: bool) -> None:
+    _pcheck(p, lib().stage_pipeline_kernel_timing(p, int(bool(enable))))
+
+
+def stage_pipeline_kernel_time(p):
+    """(mean microseconds, count) of the FFN up-projection launches of the last timed step."""
+    m, n = C.c_float(), C.c_int()
+    _pcheck(p, lib().stage_pipeline_kernel_time(p, C.byref(m), C.byref(n)))
+    return m.value, n.value
 
 
 def stage_pipeline_destroy(p) -> None:

@@ -174,6 +174,8 @@ struct stage {
   float* moe_logits = nullptr;  // [max_tokens][n_experts] router logits
   int* moe_ids = nullptr;       // [max_tokens][top_k] selected experts
   float* moe_wts = nullptr;     // [max_tokens][top_k] routing weights
+  std::vector<cudaEvent_t> tev;  // measurement: event pair around each FFN up-projection launch
+  bool timing = false;
   int32_t* h_stage = nullptr;  // pinned host staging [4][max_tokens]
   cudaEvent_t staged = nullptr;  // recorded after the last copy out of h_stage
   std::vector<int> committed, pending;
@@ -469,7 +471,9 @@ int forward_dev(stage* st, int n, const int* d_seq, const int* d_pos, const int*
         gu.rows_per_slot = 2 * EF;
         gu.ldo_slot = KpE;
         gu.err = st->err_word;
+        if (st->timing && t == 0) cudaEventRecordWithFlags(st->tev[2 * li], s, cudaEventRecordExternal);
         if ((e = lrs::launch_gemv(gu, s)) != cudaSuccess) return cuda_err(st, e, "expert gate_up");
+        if (st->timing && t == 0) cudaEventRecordWithFlags(st->tev[2 * li + 1], s, cudaEventRecordExternal);
         lrs::GemvArgs dn;
         dn.w = L.edown;
         dn.w.N = H;
@@ -502,7 +506,9 @@ int forward_dev(stage* st, int n, const int* d_seq, const int* d_pos, const int*
     gu.out = st->abuf;
     gu.ldo = c.ffn;
     gu.err = st->err_word;
+    if (st->timing) cudaEventRecordWithFlags(st->tev[2 * li], s, cudaEventRecordExternal);
     if ((e = lrs::launch_gemv(gu, s)) != cudaSuccess) return cuda_err(st, e, "gate_up");
+    if (st->timing) cudaEventRecordWithFlags(st->tev[2 * li + 1], s, cudaEventRecordExternal);
 
     lrs::GemvArgs dn;
     dn.w = L.wdown;
@@ -866,6 +872,7 @@ void stage_destroy(stage_t st) {
   if (st->arena) cudaFree(st->arena);
   if (st->h_stage) cudaFreeHost(st->h_stage);
   if (st->staged) cudaEventDestroy(st->staged);
+  for (cudaEvent_t ev : st->tev) cudaEventDestroy(ev);
   delete st;
 }
 
@@ -1132,6 +1139,39 @@ int stage_pipeline_generate(stage_pipeline_t p, int batch, const int32_t* seq_id
       st->committed[seq_ids_host[i]] += n_steps;
       st->pending[seq_ids_host[i]] = st->committed[seq_ids_host[i]];
     }
+  return STAGE_OK;
+}
+
+int stage_pipeline_kernel_timing(stage_pipeline_t p, int enable) {
+  if (!p) return STAGE_E_INVALID;
+  for (stage* st : p->stages) {
+    if (enable && st->tev.empty()) {
+      st->tev.resize(2 * (st->end - st->begin));
+      for (auto& ev : st->tev)
+        if (cudaEventCreate(&ev) != cudaSuccess) return pset(p, STAGE_E_CUDA, "event create");
+    }
+    st->timing = enable != 0;
+  }
+  if (p->graph) cudaGraphExecDestroy(p->graph);  // recapture with (or without) the event nodes
+  p->graph = nullptr;
+  return STAGE_OK;
+}
+
+int stage_pipeline_kernel_time(stage_pipeline_t p, float* mean_us, int* count) {
+  if (!p || !mean_us || !count) return STAGE_E_INVALID;
+  double sum = 0;
+  int n = 0;
+  for (stage* st : p->stages) {
+    if (!st->timing) continue;
+    for (size_t i = 0; i + 1 < st->tev.size(); i += 2) {
+      float ms = 0;
+      if (cudaEventElapsedTime(&ms, st->tev[i], st->tev[i + 1]) != cudaSuccess) return pset(p, STAGE_E_STATE, "no timed step");
+      sum += ms;
+      ++n;
+    }
+  }
+  *count = n;
+  *mean_us = n ? (float)(sum * 1000.0 / n) : 0.f;
   return STAGE_OK;
 }
 

@@ -52,6 +52,12 @@ class StagePipeline:
     def generate(self, seq_ids, first_tokens, n_steps: int, use_graph: bool = True) -> np.ndarray:
         return B.stage_pipeline_generate(self.handle, seq_ids, first_tokens, n_steps, use_graph)
 
+    def kernel_timing(self, enable: bool) -> None:
+        B.stage_pipeline_kernel_timing(self.handle, enable)
+
+    def kernel_time(self):
+        return B.stage_pipeline_kernel_time(self.handle)
+
     def handoff_stats(self, boundary: int):
         return B.stage_pipeline_handoff_stats(self.handle, boundary)
 
