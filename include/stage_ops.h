@@ -33,6 +33,14 @@ STAGE_API int stage_op_q8_pack(const stage_q8* host, void* q_dev, void* s_dev);
 STAGE_API int stage_op_gemv(const void* q_dev, const void* s_dev, int64_t rows, int64_t cols, const float* x_dev,
                             int n_tok, const float* gamma_dev, float eps, float* y_dev, void* stream);
 
+/* Tensor-core GEMM of the prefill: y[m][r] = sum_k A[m][k] * W[r][k] for m < M, r < rows,
+ * with A bf16 (bit patterns) [M][lda] on the device, lda >= the packed row length
+ * (cols rounded up to 256) and multiple of 8, zero beyond cols; W a packed matrix whose
+ * weights are rounded to bf16 (bf16(f32(scale) * q)); f32 accumulation (tcgen05, TMEM).
+ * y_dev: f32 [M][rows].  Runs on `stream`. */
+STAGE_API int stage_op_gemm_bf16(const uint16_t* a_dev, int lda, int M, const void* q_dev, const void* s_dev,
+                                 int64_t rows, int64_t cols, float* y_dev, void* stream);
+
 /* Scratch bytes stage_op_attention_decode needs for these sizes. */
 STAGE_API size_t stage_op_attention_workspace_bytes(int n_tok, int n_q_heads, int n_kv_heads, int head_dim,
                                                     int n_chunks);

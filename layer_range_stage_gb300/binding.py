@@ -100,6 +100,8 @@ _SIGS = {
     "stage_op_gemv": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int64, C.c_int64, C.c_void_p, C.c_int, C.c_void_p,
                                 C.c_float, C.c_void_p, C.c_void_p]),
     "stage_op_attention_workspace_bytes": (C.c_size_t, [C.c_int] * 5),
+    "stage_op_gemm_bf16": (C.c_int, [C.c_void_p, C.c_int, C.c_int, C.c_void_p, C.c_void_p, C.c_int64, C.c_int64,
+                                     C.c_void_p, C.c_void_p]),
     "stage_op_attention_decode": (C.c_int, [C.c_void_p] * 5 + [C.c_int] * 6 + [C.c_void_p, C.c_void_p, C.c_size_t,
                                                                               C.c_void_p]),
     "stage_op_attention_decode_static": (C.c_int, [C.c_void_p] * 5 + [C.c_int] * 6 + [C.c_void_p, C.c_void_p]),
@@ -394,6 +396,13 @@ def stage_op_q8_pack(m, q_dev, s_dev) -> None:
 def stage_op_gemv(q_dev, s_dev, rows: int, cols: int, x, y, gamma=None, eps: float = 1e-5, stream=None) -> None:
     _opcheck(lib().stage_op_gemv(q_dev.data_ptr(), s_dev.data_ptr(), rows, cols, x.data_ptr(), x.shape[0],
                                  None if gamma is None else gamma.data_ptr(), eps, y.data_ptr(), _stream(stream)))
+
+
+def stage_op_gemm_bf16(a_bits, q_dev, s_dev, rows: int, cols: int, y, stream=None) -> None:
+    """a_bits: int16/uint16 device tensor [M, lda] of bf16 bit patterns; y: f32 [M, rows]."""
+    M, lda = a_bits.shape
+    _opcheck(lib().stage_op_gemm_bf16(a_bits.data_ptr(), lda, M, q_dev.data_ptr(), s_dev.data_ptr(), rows, cols,
+                                      y.data_ptr(), _stream(stream)))
 
 
 def stage_op_attention_workspace_bytes(n_tok, n_q_heads, n_kv_heads, head_dim, n_chunks) -> int:

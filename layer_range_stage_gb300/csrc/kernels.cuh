@@ -1,13 +1,14 @@
 // Launch interface of the stage kernels (host side).
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
 namespace lrs {
 
-enum GemvEpi { EPI_STORE = 0, EPI_RESID = 1, EPI_SWIGLU = 2, EPI_QKV = 3, EPI_MOE_SWIGLU = 4 };
+enum GemvEpi { EPI_STORE = 0, EPI_RESID = 1, EPI_SWIGLU = 2, EPI_QKV = 3, EPI_MOE_SWIGLU = 4, EPI_SWIGLU_BF16 = 5 };
 
 // Device int8 block-32 matrix: q [N][Kp] stored biased (byte = q + 128), s [N][Kp/32] fp16 bits,
 // Kp = K rounded up to 256 (the padding columns face zero inputs).  Row order is the device
@@ -77,6 +78,38 @@ struct AttnArgs {
   int ntok = 0, Hq = 0, Hkv = 0, D = 0, max_len = 0, n_chunks = 1;
   float scale = 1.f;
 };
+
+// Tensor-core GEMM of the prefill: C[m][n] = sum_k A[m][k] * W[n][k] with A bf16 activations
+// [M][lda] (zero beyond K up to Kp) and W the int8 block-32 matrix dequantised to bf16 in
+// shared memory; f32 accumulation in TMEM; epilogues as for the GEMV (EPI_STORE, EPI_RESID,
+// EPI_QKV with token t = row m, EPI_SWIGLU_BF16 writing bf16 [M][ldo_bf16]).
+struct GemmArgs {
+  const __nv_bfloat16* a = nullptr;
+  int lda = 0;
+  DevQ8 w;
+  int M = 0;
+  int epi = EPI_STORE;
+  float* out = nullptr;
+  int ldo = 0;
+  const float* resid = nullptr;
+  int ldr = 0;
+  __nv_bfloat16* out_bf16 = nullptr;
+  int ldo_bf16 = 0;
+  float* qout = nullptr;
+  __half* kc = nullptr;
+  __half* vc = nullptr;
+  const int* seq = nullptr;
+  const int* pos = nullptr;
+  const float2* rope = nullptr;
+  int n_q_heads = 0, n_kv_heads = 0, head_dim = 0, max_len = 0;
+  int* err = nullptr;
+};
+cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t st);
+cudaError_t prepare_gemm_tc();
+// RMSNorm (gamma != nullptr) or plain copy of f32 rows [ntok][ld_in] to bf16 rows [ntok][ld_out],
+// zero-filled from K to ld_out.
+cudaError_t launch_rows_to_bf16(const float* x, int ld_in, int K, const float* gamma, float eps, int ntok,
+                                __nv_bfloat16* out, int ld_out, cudaStream_t st);
 
 int sm_count();
 // Sets kernel attributes and records launch limits; call once per process before any

@@ -862,6 +862,7 @@ cudaError_t prepare_kernels() {
   if (e == cudaSuccess) e = prepare_gemv<2, 4, 1, 2, 2>();
   if (e == cudaSuccess) e = prepare_gemv<2, 4, 1, 4, 2>();
 
+  if (e == cudaSuccess) e = prepare_gemm_tc();
   if (e == cudaSuccess) e = prepare_attn<64, 1>();
   if (e == cudaSuccess) e = prepare_attn<64, 2>();
   if (e == cudaSuccess) e = prepare_attn<64, 4>();

@@ -127,6 +127,31 @@ int stage_op_gemv(const void* q_dev, const void* s_dev, int64_t rows, int64_t co
   return e == cudaSuccess ? STAGE_OK : op_cuda(e, "gemv");
 }
 
+int stage_op_gemm_bf16(const uint16_t* a_dev, int lda, int M, const void* q_dev, const void* s_dev, int64_t rows,
+                       int64_t cols, float* y_dev, void* stream) {
+  if (!a_dev || !q_dev || !s_dev || !y_dev) return op_err(STAGE_E_INVALID, "null pointer");
+  if (M <= 0 || rows <= 0 || cols <= 0 || rows > (1 << 30) || cols > (1 << 24)) return op_err(STAGE_E_INVALID, "bad shape");
+  const int kp = lrs::row_pad((int)cols);
+  if (lda < kp || lda % 8) return op_err(STAGE_E_INVALID, "lda must be >= %d and a multiple of 8", kp);
+  if (!aligned16(a_dev) || !aligned16(q_dev) || !aligned16(s_dev)) return op_err(STAGE_E_INVALID, "unaligned pointer");
+  cudaError_t e = lrs::prepare_kernels();
+  if (e != cudaSuccess) return op_cuda(e, "kernel setup");
+  lrs::GemmArgs g;
+  g.a = (const __nv_bfloat16*)a_dev;
+  g.lda = lda;
+  g.w.q = (uint8_t*)q_dev;
+  g.w.s = (uint16_t*)s_dev;
+  g.w.N = (int)rows;
+  g.w.K = (int)cols;
+  g.w.Kp = kp;
+  g.M = M;
+  g.epi = lrs::EPI_STORE;
+  g.out = y_dev;
+  g.ldo = (int)rows;
+  e = lrs::launch_gemm_tc(g, (cudaStream_t)stream);
+  return e == cudaSuccess ? STAGE_OK : op_cuda(e, "gemm");
+}
+
 size_t stage_op_attention_workspace_bytes(int n_tok, int n_q_heads, int n_kv_heads, int head_dim, int n_chunks) {
   if (n_tok <= 0 || n_q_heads <= 0 || n_kv_heads <= 0 || head_dim <= 0 || n_chunks <= 0) return 0;
   const size_t part_o = (size_t)n_tok * n_q_heads * n_chunks * head_dim * 4;
