@@ -12,6 +12,9 @@ e2e   : the same through the C ABI with host buffers (stage_pipeline_step per to
         seq/pos/token arrays copied in, the greedy token read back each step).
 roofline: bytes per token (weights once + KV at the context) / step time against the
         measured HBM peak; the dominant kernel is timed on its own in a second pass.
+prefill: on the same dense stages, 4 prompts x 512 tokens as one step (every projection a
+        tcgen05 GEMM with bf16 operands), prefill tok/s and the gate/up GEMM's TFLOP/s
+        against the measured bf16 peak.
 --impl reference: the CPU oracle on the host cores, on a bounded sample of the workload.
 """
 from __future__ import annotations
@@ -40,6 +43,10 @@ WORKLOADS = {
 }
 CFG_ID = 1
 CONTEXT = 2048
+# the prefill workload: the dense 8B-shape stages, a batch of 4 seeded prompts of 512 tokens
+PREFILL = dict(seqs=4, prompt=512, min_tokens=64,
+               name="dense 8B-shape prefill, 2 stages 16/16, 4 prompts x 512 tokens in one step, "
+                    "bf16 tcgen05 GEMMs with int8 block-32 weights dequantised in shared memory")
 # DRAM bytes (read + write) of one launch of the dominant kernel from an ncu capture of the
 # same launch configuration (profiles/gemv_gateup_decode.md); None until captured.
 TRAFFIC = {1: 128_097_792}
@@ -103,11 +110,66 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(self.samples)}
 
 
-def build_gpu_pipeline(model, bounds, max_seq_len, max_tokens, max_seqs=1):
+def build_gpu_pipeline(model, bounds, max_seq_len, max_tokens, max_seqs=1, gemm_bf16_min_tokens=0):
     from layer_range_stage_gb300.pipeline import StagePipeline
     return StagePipeline(model, bounds, lambda l: synth.layer_weights(model, l),
                          lambda a, b: synth.stage_weights(model, a, b, with_layers=False),
-                         max_seqs=max_seqs, max_seq_len=max_seq_len, max_tokens=max_tokens)
+                         max_seqs=max_seqs, max_seq_len=max_seq_len, max_tokens=max_tokens,
+                         gemm_bf16_min_tokens=gemm_bf16_min_tokens)
+
+
+def gemm_flops_per_token(model):
+    """2 x the projection weights one token multiplies (readout excluded)."""
+    H = model.hidden
+    per_layer = (model.q_dim + 2 * model.kv_dim) * H + H * model.q_dim + 3 * model.ffn * H
+    return 2.0 * per_layer * model.n_layers
+
+
+def run_prefill(gp, model, warm=2, reps=3):
+    """Prefill steps of PREFILL's batch, each from empty caches; returns the prefill fields."""
+    import torch
+    import layer_range_stage_gb300 as L
+    ns, plen = PREFILL["seqs"], PREFILL["prompt"]
+    T = ns * plen
+    toks = np.concatenate([synth.prompt_tokens(model, 100 + s, plen) for s in range(ns)])
+    seq, pos = np.repeat(np.arange(ns), plen), np.tile(np.arange(plen), ns)
+    rows = np.arange(1, ns + 1) * plen - 1
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    times = []
+    for i in range(warm + reps + 1):
+        for st in gp.stages:
+            L.stage_reset(st)
+        timed_kernel = i == warm + reps
+        if timed_kernel:  # one more step with events around every gate/up GEMM
+            gp.kernel_timing(True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        gp.step(True, seq, pos, toks, rows=rows)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if warm <= i < warm + reps:
+            times.append(e0.elapsed_time(e1))
+    k_us, k_n = gp.kernel_time()
+    gp.kernel_timing(False)
+    for st in gp.stages:
+        L.stage_reset(st)
+    ms = float(np.mean(times))
+    peak = measured_peaks().get("bf16_tflops")
+    k_flops = 2.0 * T * 2 * model.ffn * model.hidden
+    k_tf = k_flops / (k_us * 1e-6) / 1e12 if k_us else None
+    step_tf = gemm_flops_per_token(model) * T / (ms * 1e-3) / 1e12
+    return {"value": round(T * 1000.0 / ms, 1), "unit": "tok/s", "ms_per_step": round(ms, 3), "steps": reps,
+            "warmup": warm, "tokens_per_step": T, "workload": PREFILL["name"],
+            "dtype": "bf16 operands, f32 accumulation",
+            "roofline": {"bound": "tensor", "achieved": round(k_tf, 1) if k_tf else None, "peak": peak,
+                         "unit": "TFLOP/s", "frac": round(k_tf / peak, 4) if (k_tf and peak) else None,
+                         "traffic": None, "kernel": "FFN gate/up tcgen05 GEMM (SwiGLU epilogue)",
+                         "flops_per_launch": k_flops, "mean_launch_us": round(k_us, 2), "launches_timed": k_n,
+                         "peak_source": "measured burst (MEASURED_PEAKS.json bf16_tflops)" if peak else "fallback"},
+            "step_roofline": {"bound": "tensor", "achieved": round(step_tf, 1), "peak": peak, "unit": "TFLOP/s",
+                              "frac": round(step_tf / peak, 4) if peak else None,
+                              "flops_per_step": gemm_flops_per_token(model) * T}}
 
 
 def run_gpu(args):
@@ -132,7 +194,14 @@ def run_gpu(args):
     steps, warmup = args.steps, args.warmup
     max_len = context + warmup + 2 * steps + 16
     t_build = time.time()
-    gp = build_gpu_pipeline(model, bounds, max_len, max_tokens=512)
+    dense = not model.is_moe
+    if dense:  # room for the prefill batch; calls of >= 64 tokens run on the tensor cores
+        gp = build_gpu_pipeline(model, bounds, max(max_len, PREFILL["prompt"]), max_tokens=PREFILL["seqs"] * PREFILL["prompt"],
+                                max_seqs=PREFILL["seqs"], gemm_bf16_min_tokens=PREFILL["min_tokens"])
+    else:
+        gp = build_gpu_pipeline(model, bounds, max_len, max_tokens=512)
+    build_s = time.time() - t_build
+    prefill = run_prefill(gp, model) if dense else None
     # prefill the seeded context in chunks of 512 tokens through the stages
     prompt = synth.prompt_tokens(model, rank, context)
     tok = None
@@ -140,7 +209,6 @@ def run_gpu(args):
         c1 = min(context, c0 + 512)
         tok = gp.step(True, np.zeros(c1 - c0), np.arange(c0, c1), prompt[c0:c1], rows=[c1 - c0 - 1])
     torch.cuda.synchronize()
-    build_s = time.time() - t_build
     stream = torch.cuda.current_stream()
     # warm-up (captures the step graph), then K timed graph replays
     first = gp.generate([0], tok, warmup, use_graph=True)[-1]
@@ -220,6 +288,7 @@ def run_gpu(args):
                           "frac": round(gbs / peak, 4) if peak else None,
                           "bytes_per_step": round(w_bytes + kv_bytes)},
         "e2e": e2e,
+        "prefill": prefill,
         "clocks": clk,
         "gpu_launches": steps * (1 + model.n_layers * (7 if model.is_moe else 5) + 4),
         "build_s": round(build_s, 1),

@@ -70,9 +70,11 @@ typedef struct stage* stage_t;
 /* Model shape.  Dense models set n_experts = top_k = expert_ffn = 0.  ffn and
  * expert_ffn need not be multiples of 32 (the last weight block of a row is then
  * partial).  max_seqs / max_seq_len size the KV cache; max_tokens bounds the
- * tokens of one prefill or decode call.  gemm_bf16_min_tokens: calls with at least
- * this many tokens run their projections on the tensor cores with bf16 operands;
- * smaller calls use the float32 dequant-fused GEMV (0 = never use bf16). */
+ * tokens of one prefill or decode call.  gemm_bf16_min_tokens: on dense models, calls
+ * with at least this many tokens run their projections on the tensor cores (tcgen05)
+ * with bf16 operands -- activations rounded to bf16, weights as bf16(f32(scale) * q) --
+ * and f32 accumulation; smaller calls, and every call of a MoE model, use the float32
+ * dequant-fused GEMV (0 = never use bf16). */
 typedef struct {
   int n_layers, hidden, n_q_heads, n_kv_heads, head_dim, ffn, vocab;
   int n_experts, top_k, expert_ffn;
@@ -229,10 +231,11 @@ STAGE_API int stage_pipeline_generate(stage_pipeline_t p, int batch, const int32
                             const int32_t* first_tokens_host, int n_steps, int use_graph,
                             int32_t* tokens_out_host);
 
-/* Kernel timing for measurement: with enable = 1 the next captured generate step records a
- * CUDA event pair around every gate/up (or expert gate/up) GEMV launch of every stage.
- * stage_pipeline_kernel_time returns the mean duration (microseconds) of those launches in
- * the last replayed step and their count.  Events sit between kernels, so a timed launch
+/* Kernel timing for measurement: with enable = 1 every following step (generate or
+ * stage_pipeline_step) records a CUDA event pair around the FFN gate/up launch of every
+ * block -- the gate/up (or expert gate/up) GEMV, or the gate/up tensor-core GEMM of a call
+ * that runs on the tensor cores.  stage_pipeline_kernel_time returns the mean duration
+ * (microseconds) of those launches in the last step and their count.  Events sit between kernels, so a timed launch
  * does not overlap its predecessor; leave timing off for the headline measurement. */
 STAGE_API int stage_pipeline_kernel_timing(stage_pipeline_t p, int enable);
 STAGE_API int stage_pipeline_kernel_time(stage_pipeline_t p, float* mean_us, int* count);

@@ -21,6 +21,8 @@
 #include <string>
 #include <vector>
 
+#include <cuda_bf16.h>
+
 #include "../../include/stage.h"
 #include "kernels.cuh"
 
@@ -48,7 +50,8 @@ void walk_plan(const stage_model_cfg& c, int begin, int end, std::vector<LayerDe
                DevQ8* head, float** final_norm, __half** kc, __half** vc, float2** rope, float** qbuf,
                float** obuf, float** abuf, float** feat, float** logits, int** argmax, float** part_o,
                float2** part_ml, int** counters, int** d_seq, int** d_pos, int** d_tok, int** d_rows, int** err_word,
-               float** moe_logits, int** moe_ids, float** moe_wts, F&& f) {
+               float** moe_logits, int** moe_ids, float** moe_wts, __nv_bfloat16** act_bf16,
+               __nv_bfloat16** ffn_bf16, F&& f) {
   auto q8 = [&](DevQ8* m, int N, int K) {
     if (m) {
       m->N = N;
@@ -103,6 +106,10 @@ void walk_plan(const stage_model_cfg& c, int begin, int end, std::vector<LayerDe
   f(T * 4, (void**)d_tok);
   f(T * 4, (void**)d_rows);
   f(4, (void**)err_word);
+  if (!moe && c.gemm_bf16_min_tokens > 0) {  // bf16 operands of the tensor-core GEMMs
+    f(T * (size_t)std::max(kpad(H), kpad(Hq * D)) * 2, (void**)act_bf16);
+    f(T * (size_t)kpad(c.ffn) * 2, (void**)ffn_bf16);
+  }
   if (moe) {
     f(T * c.n_experts * 4, (void**)moe_logits);
     f(T * c.top_k * 4, (void**)moe_ids);
@@ -116,7 +123,7 @@ size_t plan_bytes(const stage_model_cfg& c, int begin, int end) {
   size_t total = 0;
   walk_plan(c, begin, end, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
             nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
-            nullptr, nullptr, [&](size_t b, void**) { total += round_up(b, kAlign); });
+            nullptr, nullptr, nullptr, nullptr, [&](size_t b, void**) { total += round_up(b, kAlign); });
   return total;
 }
 
@@ -174,6 +181,8 @@ struct stage {
   float* moe_logits = nullptr;  // [max_tokens][n_experts] router logits
   int* moe_ids = nullptr;       // [max_tokens][top_k] selected experts
   float* moe_wts = nullptr;     // [max_tokens][top_k] routing weights
+  __nv_bfloat16* act_bf16 = nullptr;  // [max_tokens][Kp] bf16 GEMM operand (normed x, attention out)
+  __nv_bfloat16* ffn_bf16 = nullptr;  // [max_tokens][Kp(ffn)] bf16 SwiGLU output
   std::vector<cudaEvent_t> tev;  // measurement: event pair around each FFN up-projection launch
   bool timing = false;
   int32_t* h_stage = nullptr;  // pinned host staging [4][max_tokens]
@@ -370,6 +379,111 @@ int attn_chunks(const stage* st, int ntok, int max_len_in_call) {
   return std::max(1, n);
 }
 
+// A kernel-timing event: an external event node when the stream is being captured (a plain
+// record there would become an internal graph dependency), a plain record otherwise.
+void timing_mark(cudaEvent_t ev, cudaStream_t s) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaStreamIsCapturing(s, &cs);
+  if (cs == cudaStreamCaptureStatusActive)
+    cudaEventRecordWithFlags(ev, s, cudaEventRecordExternal);
+  else
+    cudaEventRecord(ev, s);
+}
+
+// Arithmetic of a call with n tokens: the bf16 tensor-core GEMMs for dense stages once n
+// reaches gemm_bf16_min_tokens (when set), the float32 dequant-fused GEMV otherwise.
+bool use_tc(const stage* st, int n) {
+  return st->cfg.n_experts == 0 && st->cfg.gemm_bf16_min_tokens > 0 && n >= st->cfg.gemm_bf16_min_tokens;
+}
+
+// One block on the tensor cores (bf16 operands, f32 accumulation and residual).
+int block_tc(stage* st, int li, LayerDev& L, int n, const int* d_seq, const int* d_pos, const float* xin, float* hout,
+             __half* kc, __half* vc, int n_chunks, cudaStream_t s) {
+  const stage_model_cfg& c = st->cfg;
+  const int H = c.hidden, D = c.head_dim, Hq = c.n_q_heads, Hkv = c.n_kv_heads;
+  const int ldh = kpad(H), ldq = kpad(Hq * D), ldf = kpad(c.ffn);
+  cudaError_t e;
+  if ((e = lrs::launch_rows_to_bf16(xin, H, H, L.attn_norm, c.rms_eps, n, st->act_bf16, ldh, s)) != cudaSuccess)
+    return cuda_err(st, e, "norm 1");
+  lrs::GemmArgs g;
+  g.a = st->act_bf16;
+  g.lda = ldh;
+  g.w = L.wqkv;
+  g.M = n;
+  g.epi = lrs::EPI_QKV;
+  g.qout = st->qbuf;
+  g.kc = kc;
+  g.vc = vc;
+  g.seq = d_seq;
+  g.pos = d_pos;
+  g.rope = st->rope;
+  g.n_q_heads = Hq;
+  g.n_kv_heads = Hkv;
+  g.head_dim = D;
+  g.max_len = c.max_seq_len;
+  g.err = st->err_word;
+  if ((e = lrs::launch_gemm_tc(g, s)) != cudaSuccess) return cuda_err(st, e, "qkv gemm");
+  lrs::AttnArgs at;
+  at.q = st->qbuf;
+  at.kc = kc;
+  at.vc = vc;
+  at.seq = d_seq;
+  at.pos = d_pos;
+  at.out = st->obuf;
+  at.part_o = st->part_o;
+  at.part_ml = st->part_ml;
+  at.counters = st->counters;
+  at.ntok = n;
+  at.Hq = Hq;
+  at.Hkv = Hkv;
+  at.D = D;
+  at.max_len = c.max_seq_len;
+  at.n_chunks = n_chunks;
+  at.scale = (float)(1.0 / std::sqrt((double)D));
+  if ((e = lrs::launch_attn_decode(at, s)) != cudaSuccess) return cuda_err(st, e, "attention");
+  if ((e = lrs::launch_rows_to_bf16(st->obuf, Hq * D, Hq * D, nullptr, 0.f, n, st->act_bf16, ldq, s)) != cudaSuccess)
+    return cuda_err(st, e, "attention out");
+  lrs::GemmArgs o;
+  o.a = st->act_bf16;
+  o.lda = ldq;
+  o.w = L.wo;
+  o.M = n;
+  o.epi = lrs::EPI_RESID;
+  o.resid = xin;
+  o.ldr = H;
+  o.out = hout;
+  o.ldo = H;
+  o.err = st->err_word;
+  if ((e = lrs::launch_gemm_tc(o, s)) != cudaSuccess) return cuda_err(st, e, "o gemm");
+  if ((e = lrs::launch_rows_to_bf16(hout, H, H, L.ffn_norm, c.rms_eps, n, st->act_bf16, ldh, s)) != cudaSuccess)
+    return cuda_err(st, e, "norm 2");
+  lrs::GemmArgs gu;
+  gu.a = st->act_bf16;
+  gu.lda = ldh;
+  gu.w = L.wgu;
+  gu.M = n;
+  gu.epi = lrs::EPI_SWIGLU_BF16;
+  gu.out_bf16 = st->ffn_bf16;
+  gu.ldo_bf16 = ldf;
+  gu.err = st->err_word;
+  if (st->timing) timing_mark(st->tev[2 * li], s);
+  if ((e = lrs::launch_gemm_tc(gu, s)) != cudaSuccess) return cuda_err(st, e, "gate_up gemm");
+  if (st->timing) timing_mark(st->tev[2 * li + 1], s);
+  lrs::GemmArgs dn;
+  dn.a = st->ffn_bf16;
+  dn.lda = ldf;
+  dn.w = L.wdown;
+  dn.M = n;
+  dn.epi = lrs::EPI_RESID;
+  dn.resid = hout;
+  dn.ldr = H;
+  dn.out = hout;
+  dn.ldo = H;
+  dn.err = st->err_word;
+  if ((e = lrs::launch_gemm_tc(dn, s)) != cudaSuccess) return cuda_err(st, e, "down gemm");
+  return STAGE_OK;
+}
+
 // The per-stage launch chain.  Inputs are device arrays; hout receives the residual stream
 // (the final features on the last stage).
 int forward_dev(stage* st, int n, const int* d_seq, const int* d_pos, const int* d_tok, const float* hin, float* hout,
@@ -378,11 +492,17 @@ int forward_dev(stage* st, int n, const int* d_seq, const int* d_pos, const int*
   const int H = c.hidden, D = c.head_dim, Hq = c.n_q_heads, Hkv = c.n_kv_heads;
   cudaError_t e;
   if (st->first && (e = lrs::launch_embed(st->embed, d_tok, n, hout, H, s)) != cudaSuccess) return cuda_err(st, e, "embed");
+  const bool tc = use_tc(st, n);
   for (int li = 0; li < st->end - st->begin; ++li) {
     LayerDev& L = st->layers[li];
     const float* xin = (li == 0 && !st->first) ? hin : hout;
     __half* kc = st->kc + (size_t)li * st->layer_kv;
     __half* vc = st->vc + (size_t)li * st->layer_kv;
+    if (tc) {
+      const int rc = block_tc(st, li, L, n, d_seq, d_pos, xin, hout, kc, vc, n_chunks, s);
+      if (rc) return rc;
+      continue;
+    }
     lrs::GemvArgs g;
     g.w = L.wqkv;
     g.x = xin;
@@ -471,9 +591,9 @@ int forward_dev(stage* st, int n, const int* d_seq, const int* d_pos, const int*
         gu.rows_per_slot = 2 * EF;
         gu.ldo_slot = KpE;
         gu.err = st->err_word;
-        if (st->timing && t == 0) cudaEventRecordWithFlags(st->tev[2 * li], s, cudaEventRecordExternal);
+        if (st->timing && t == 0) timing_mark(st->tev[2 * li], s);
         if ((e = lrs::launch_gemv(gu, s)) != cudaSuccess) return cuda_err(st, e, "expert gate_up");
-        if (st->timing && t == 0) cudaEventRecordWithFlags(st->tev[2 * li + 1], s, cudaEventRecordExternal);
+        if (st->timing && t == 0) timing_mark(st->tev[2 * li + 1], s);
         lrs::GemvArgs dn;
         dn.w = L.edown;
         dn.w.N = H;
@@ -506,9 +626,9 @@ int forward_dev(stage* st, int n, const int* d_seq, const int* d_pos, const int*
     gu.out = st->abuf;
     gu.ldo = c.ffn;
     gu.err = st->err_word;
-    if (st->timing) cudaEventRecordWithFlags(st->tev[2 * li], s, cudaEventRecordExternal);
+    if (st->timing) timing_mark(st->tev[2 * li], s);
     if ((e = lrs::launch_gemv(gu, s)) != cudaSuccess) return cuda_err(st, e, "gate_up");
-    if (st->timing) cudaEventRecordWithFlags(st->tev[2 * li + 1], s, cudaEventRecordExternal);
+    if (st->timing) timing_mark(st->tev[2 * li + 1], s);
 
     lrs::GemvArgs dn;
     dn.w = L.wdown;
@@ -682,7 +802,7 @@ int stage_create(const stage_model_cfg* cfg, stage_layer_range range, const stag
   walk_plan(*cfg, range.begin, range.end, &st->layers, &st->embed, &st->head, &st->final_norm, &st->kc, &st->vc,
             &st->rope, &st->qbuf, &st->obuf, &st->abuf, &st->feat, &st->logits, &st->argmax, &st->part_o,
             &st->part_ml, &st->counters, &st->d_seq, &st->d_pos, &st->d_tok, &st->d_rows, &st->err_word,
-            &st->moe_logits, &st->moe_ids, &st->moe_wts, [&](size_t b, void** slot) {
+            &st->moe_logits, &st->moe_ids, &st->moe_wts, &st->act_bf16, &st->ffn_bf16, [&](size_t b, void** slot) {
               if (slot) *slot = st->arena + off;
               off += round_up(b, kAlign);
             });
@@ -857,8 +977,7 @@ int stage_read_kv(stage_t st, int global_layer, int seq_id, int n_pos, uint16_t*
 
 int stage_gemm_mode(stage_t st, int n_tokens, int* mode_out) {
   if (!st || !mode_out) return STAGE_E_INVALID;
-  *mode_out = 0;  // the float32 dequant-fused GEMV
-  (void)n_tokens;
+  *mode_out = use_tc(st, n_tokens) ? 1 : 0;
   return STAGE_OK;
 }
 
