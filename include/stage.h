@@ -187,7 +187,11 @@ STAGE_API int stage_committed_len(stage_t st, int seq_id, int* len_out);
  * Synchronises the stage's stream.  For inspection and equivalence checks. */
 STAGE_API int stage_read_kv(stage_t st, int global_layer, int seq_id, int n_pos, uint16_t* k_host, uint16_t* v_host);
 
-/* Which arithmetic a call with n_tokens tokens uses: 0 = float32 GEMV, 1 = bf16 tensor cores. */
+/* Which path a call with n_tokens tokens takes: 0 = float32 dequant-fused GEMV kernels,
+ * 1 = bf16 tensor-core GEMMs, 2 = float32 persistent decode (a single-token call on a dense
+ * stage: every block of the stage in one cooperative launch; same arithmetic per weight as
+ * 0, its own fixed summation order).  The environment variable LRS_PERSISTENT=0, read at
+ * stage_create, turns mode 2 off. */
 STAGE_API int stage_gemm_mode(stage_t st, int n_tokens, int* mode_out);
 
 STAGE_API const char* stage_last_error(stage_t st);

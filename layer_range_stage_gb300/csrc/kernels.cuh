@@ -111,6 +111,46 @@ cudaError_t prepare_gemm_tc();
 cudaError_t launch_rows_to_bf16(const float* x, int ld_in, int K, const float* gamma, float eps, int ntok,
                                 __nv_bfloat16* out, int ld_out, cudaStream_t st);
 
+// Persistent decode of a dense stage: every block of the stage for one token in one
+// cooperative launch (one CTA per SM).  Per block, five phases separated by grid barriers:
+// QKV GEMV (RMSNorm prologue; RoPE + fp16 KV append epilogue), split-K attention with the
+// last-arriving chunk merging, O GEMV + residual, gate/up GEMV (RMSNorm prologue, SwiGLU
+// epilogue), down GEMV + residual.  Weight rows stream through a per-warp ring of bulk
+// copies that runs ahead across phases and blocks.
+struct MegaLayer {
+  DevQ8 wqkv, wo, wgu, wdown;
+  const float* attn_norm = nullptr;
+  const float* ffn_norm = nullptr;
+  __half* kc = nullptr;  // [max_seqs][Hkv][max_len][D] of this block
+  __half* vc = nullptr;
+};
+struct MegaArgs {
+  const MegaLayer* layers = nullptr;  // device [nl]
+  int nl = 0;
+  const float* hin = nullptr;  // [H] block input of the first block (may equal hout)
+  float* hout = nullptr;       // [H] residual stream after the last block
+  float* x1 = nullptr;         // [H] scratch: residual after attention
+  float* qbuf = nullptr;       // [Hq * D] rotated q
+  float* obuf = nullptr;       // [Hq * D] attention output
+  float* abuf = nullptr;       // [F] SwiGLU output
+  float* part_o = nullptr;     // attention split-K partials (layout of AttnArgs, token 0)
+  float2* part_ml = nullptr;
+  const int* seq = nullptr;    // device [1]
+  const int* pos = nullptr;    // device [1]
+  const float2* rope = nullptr;
+  int H = 0, Hq = 0, Hkv = 0, D = 0, F = 0, max_len = 0, n_chunks = 1;
+  float eps = 1e-5f, scale = 1.f;
+  unsigned* bar = nullptr;  // [64]: grid barrier counter, exit counter, per-KV-head attention
+                            // counters; zero between launches (the last CTA out re-zeroes)
+  int* err = nullptr;
+};
+// Whether the persistent decode covers this shape (and the shared memory it needs fits).
+bool mega_supported(int H, int q_dim, int F, int head_dim, int group);
+// Attention chunks per KV head used by the persistent decode (about one item per SM).
+int mega_chunks(int n_kv_heads);
+cudaError_t launch_mega_decode(const MegaArgs& a, cudaStream_t st);
+cudaError_t prepare_mega();
+
 int sm_count();
 // Sets kernel attributes and records launch limits; call once per process before any
 // launch, outside stream capture.

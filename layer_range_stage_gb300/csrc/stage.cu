@@ -51,7 +51,7 @@ void walk_plan(const stage_model_cfg& c, int begin, int end, std::vector<LayerDe
                float** obuf, float** abuf, float** feat, float** logits, int** argmax, float** part_o,
                float2** part_ml, int** counters, int** d_seq, int** d_pos, int** d_tok, int** d_rows, int** err_word,
                float** moe_logits, int** moe_ids, float** moe_wts, __nv_bfloat16** act_bf16,
-               __nv_bfloat16** ffn_bf16, F&& f) {
+               __nv_bfloat16** ffn_bf16, lrs::MegaLayer** mlayers, float** mega_x1, unsigned** mega_bar, F&& f) {
   auto q8 = [&](DevQ8* m, int N, int K) {
     if (m) {
       m->N = N;
@@ -106,6 +106,11 @@ void walk_plan(const stage_model_cfg& c, int begin, int end, std::vector<LayerDe
   f(T * 4, (void**)d_tok);
   f(T * 4, (void**)d_rows);
   f(4, (void**)err_word);
+  if (!moe) {  // persistent decode: block descriptors, post-attention residual, grid barrier
+    f((size_t)(end - begin) * sizeof(lrs::MegaLayer), (void**)mlayers);
+    f((size_t)H * 4, (void**)mega_x1);
+    f(256, (void**)mega_bar);
+  }
   if (!moe && c.gemm_bf16_min_tokens > 0) {  // bf16 operands of the tensor-core GEMMs
     f(T * (size_t)std::max(kpad(H), kpad(Hq * D)) * 2, (void**)act_bf16);
     f(T * (size_t)kpad(c.ffn) * 2, (void**)ffn_bf16);
@@ -123,7 +128,8 @@ size_t plan_bytes(const stage_model_cfg& c, int begin, int end) {
   size_t total = 0;
   walk_plan(c, begin, end, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
             nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
-            nullptr, nullptr, nullptr, nullptr, [&](size_t b, void**) { total += round_up(b, kAlign); });
+            nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
+            [&](size_t b, void**) { total += round_up(b, kAlign); });
   return total;
 }
 
@@ -183,8 +189,13 @@ struct stage {
   float* moe_wts = nullptr;     // [max_tokens][top_k] routing weights
   __nv_bfloat16* act_bf16 = nullptr;  // [max_tokens][Kp] bf16 GEMM operand (normed x, attention out)
   __nv_bfloat16* ffn_bf16 = nullptr;  // [max_tokens][Kp(ffn)] bf16 SwiGLU output
+  lrs::MegaLayer* mlayers = nullptr;  // device block descriptors of the persistent decode
+  float* mega_x1 = nullptr;           // [H] its post-attention residual
+  unsigned* mega_bar = nullptr;       // its grid barrier counters
+  bool mega = false;                  // single-token decode calls use the persistent kernel
   std::vector<cudaEvent_t> tev;  // measurement: event pair around each FFN up-projection launch
   bool timing = false;
+  int timed_pairs = 0;           // event pairs recorded by the last forward
   int32_t* h_stage = nullptr;  // pinned host staging [4][max_tokens]
   cudaEvent_t staged = nullptr;  // recorded after the last copy out of h_stage
   std::vector<int> committed, pending;
@@ -343,6 +354,17 @@ int load_layer(stage* st, int gl, const stage_layer_w* w) {
     if (ce == cudaSuccess) ce = cudaMemcpy(L.wgu.s, s.data(), s.size() * 2, cudaMemcpyHostToDevice);
     if (ce != cudaSuccess) return cuda_err(st, ce, "gate/up");
     if ((rc = upload_plain(st, w->w_down, L.wdown, "w_down"))) return rc;
+    lrs::MegaLayer ml;
+    ml.wqkv = L.wqkv;
+    ml.wo = L.wo;
+    ml.wgu = L.wgu;
+    ml.wdown = L.wdown;
+    ml.attn_norm = L.attn_norm;
+    ml.ffn_norm = L.ffn_norm;
+    ml.kc = st->kc + (size_t)(gl - st->begin) * st->layer_kv;
+    ml.vc = st->vc + (size_t)(gl - st->begin) * st->layer_kv;
+    ce = cudaMemcpy(st->mlayers + (gl - st->begin), &ml, sizeof ml, cudaMemcpyHostToDevice);
+    if (ce != cudaSuccess) return cuda_err(st, ce, "block descriptor");
   }
   L.loaded = true;
   return STAGE_OK;
@@ -493,6 +515,38 @@ int forward_dev(stage* st, int n, const int* d_seq, const int* d_pos, const int*
   cudaError_t e;
   if (st->first && (e = lrs::launch_embed(st->embed, d_tok, n, hout, H, s)) != cudaSuccess) return cuda_err(st, e, "embed");
   const bool tc = use_tc(st, n);
+  st->timed_pairs = st->end - st->begin;
+  if (n == 1 && st->mega) {  // single-token decode: every block in one persistent launch
+    lrs::MegaArgs m;
+    m.layers = st->mlayers;
+    m.nl = st->end - st->begin;
+    m.hin = st->first ? hout : hin;
+    m.hout = hout;
+    m.x1 = st->mega_x1;
+    m.qbuf = st->qbuf;
+    m.obuf = st->obuf;
+    m.abuf = st->abuf;
+    m.part_o = st->part_o;
+    m.part_ml = st->part_ml;
+    m.seq = d_seq;
+    m.pos = d_pos;
+    m.rope = st->rope;
+    m.H = H;
+    m.Hq = Hq;
+    m.Hkv = Hkv;
+    m.D = D;
+    m.F = c.ffn;
+    m.max_len = c.max_seq_len;
+    m.n_chunks = lrs::mega_chunks(Hkv);
+    m.eps = c.rms_eps;
+    m.scale = (float)(1.0 / std::sqrt((double)D));
+    m.bar = st->mega_bar;
+    m.err = st->err_word;
+    if (st->timing) timing_mark(st->tev[0], s);
+    if ((e = lrs::launch_mega_decode(m, s)) != cudaSuccess) return cuda_err(st, e, "persistent decode");
+    if (st->timing) timing_mark(st->tev[1], s);
+    st->timed_pairs = 1;
+  } else
   for (int li = 0; li < st->end - st->begin; ++li) {
     LayerDev& L = st->layers[li];
     const float* xin = (li == 0 && !st->first) ? hin : hout;
@@ -802,7 +856,8 @@ int stage_create(const stage_model_cfg* cfg, stage_layer_range range, const stag
   walk_plan(*cfg, range.begin, range.end, &st->layers, &st->embed, &st->head, &st->final_norm, &st->kc, &st->vc,
             &st->rope, &st->qbuf, &st->obuf, &st->abuf, &st->feat, &st->logits, &st->argmax, &st->part_o,
             &st->part_ml, &st->counters, &st->d_seq, &st->d_pos, &st->d_tok, &st->d_rows, &st->err_word,
-            &st->moe_logits, &st->moe_ids, &st->moe_wts, &st->act_bf16, &st->ffn_bf16, [&](size_t b, void** slot) {
+            &st->moe_logits, &st->moe_ids, &st->moe_wts, &st->act_bf16, &st->ffn_bf16, &st->mlayers, &st->mega_x1,
+            &st->mega_bar, [&](size_t b, void** slot) {
               if (slot) *slot = st->arena + off;
               off += round_up(b, kAlign);
             });
@@ -820,6 +875,12 @@ int stage_create(const stage_model_cfg* cfg, stage_layer_range range, const stag
         tab[(size_t)p * hd + i] = make_float2((float)std::cos(ang), (float)std::sin(ang));
       }
     e = cudaMemcpy(st->rope, tab.data(), tab.size() * sizeof(float2), cudaMemcpyHostToDevice);
+  }
+  {
+    const char* mg = getenv("LRS_PERSISTENT");
+    st->mega = cfg->n_experts == 0 && !(mg && mg[0] == '0') &&
+               lrs::mega_supported(cfg->hidden, cfg->n_q_heads * cfg->head_dim, cfg->ffn, cfg->head_dim,
+                                   cfg->n_q_heads / cfg->n_kv_heads);
   }
   if (e == cudaSuccess) e = cudaMallocHost(&st->h_stage, (size_t)4 * cfg->max_tokens * 4);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&st->staged, cudaEventDisableTiming);
@@ -977,7 +1038,7 @@ int stage_read_kv(stage_t st, int global_layer, int seq_id, int n_pos, uint16_t*
 
 int stage_gemm_mode(stage_t st, int n_tokens, int* mode_out) {
   if (!st || !mode_out) return STAGE_E_INVALID;
-  *mode_out = use_tc(st, n_tokens) ? 1 : 0;
+  *mode_out = use_tc(st, n_tokens) ? 1 : (n_tokens == 1 && st->mega) ? 2 : 0;
   return STAGE_OK;
 }
 
@@ -1282,7 +1343,7 @@ int stage_pipeline_kernel_time(stage_pipeline_t p, float* mean_us, int* count) {
   int n = 0;
   for (stage* st : p->stages) {
     if (!st->timing) continue;
-    for (size_t i = 0; i + 1 < st->tev.size(); i += 2) {
+    for (size_t i = 0; i + 1 < st->tev.size() && (int)i < 2 * st->timed_pairs; i += 2) {
       float ms = 0;
       if (cudaEventElapsedTime(&ms, st->tev[i], st->tev[i + 1]) != cudaSuccess) return pset(p, STAGE_E_STATE, "no timed step");
       sum += ms;

@@ -60,7 +60,8 @@ def test_gemm_mode_selection(cuda):
     dense, moe = synth.CONFIGS[0], synth.reduced(synth.CONFIGS[2], 1)
     st = B.stage_create(B.make_cfg(dense, 1, 64, 32, 8), 0, 4, synth.stage_weights(dense, 0, 4))
     try:
-        assert [B.stage_gemm_mode(st, n) for n in (1, 7, 8, 32)] == [0, 0, 1, 1]
+        # single-token calls take the persistent decode kernel (2)
+        assert [B.stage_gemm_mode(st, n) for n in (1, 2, 7, 8, 32)] == [2, 0, 0, 1, 1]
     finally:
         B.stage_destroy(st)
     st = B.stage_create(B.make_cfg(dense, 1, 64, 32, 0), 0, 4, synth.stage_weights(dense, 0, 4))
@@ -71,7 +72,7 @@ def test_gemm_mode_selection(cuda):
     # MoE stages keep the GEMV (the expert gather) at every size
     st = B.stage_create(B.make_cfg(moe, 1, 64, 32, 8), 0, 1, synth.stage_weights(moe, 0, 1))
     try:
-        assert B.stage_gemm_mode(st, 32) == 0
+        assert B.stage_gemm_mode(st, 32) == 0 and B.stage_gemm_mode(st, 1) == 0
     finally:
         B.stage_destroy(st)
 
@@ -128,7 +129,7 @@ def test_tiny_bf16_prefill_then_f32_decode(cuda):
     toks_o, logits_o = op.generate([prompt], 17, prefill_gemm="bf16", decode_gemm="f32")
     import layer_range_stage_gb300 as L
     with gpu_pipeline(model, [0, 2, 4], max_seq_len=128, max_tokens=64, gemm_bf16_min_tokens=16) as gp:
-        assert L.stage_gemm_mode(gp.stages[0], 64) == 1 and L.stage_gemm_mode(gp.stages[0], 1) == 0
+        assert L.stage_gemm_mode(gp.stages[0], 64) == 1 and L.stage_gemm_mode(gp.stages[0], 1) == 2
         lg = torch.empty((1, model.vocab), dtype=torch.float32, device="cuda")
         tok = gp.step(True, np.zeros(n), np.arange(n), prompt, rows=[n - 1], logits_out=lg)
         toks, logits = [int(tok[0])], [lg.cpu().numpy().copy()]
