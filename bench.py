@@ -47,9 +47,10 @@ CONTEXT = 2048
 PREFILL = dict(seqs=4, prompt=512, min_tokens=64,
                name="dense 8B-shape prefill, 2 stages 16/16, 4 prompts x 512 tokens in one step, "
                     "bf16 tcgen05 GEMMs with int8 block-32 weights dequantised in shared memory")
-# DRAM bytes (read + write) per launch of the dominant kernel from an ncu capture of the same
-# launch configuration (profiles/); absent until captured for the current kernel.
-TRAFFIC = {}
+# DRAM bytes (read + write) per launch of the dominant kernel: the persistent stage decode of
+# the dense workload, from an ncu capture of one block in the same launch configuration scaled
+# by the 16 blocks of a launch (profiles/mega_decode_small.md).
+TRAFFIC = {1: 3_903_004_672}
 
 
 def measured_peaks():
