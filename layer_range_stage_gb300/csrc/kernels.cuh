@@ -161,6 +161,10 @@ bool pdl_enabled();
 
 cudaError_t launch_gemv(const GemvArgs& a, cudaStream_t st);
 cudaError_t launch_attn_decode(const AttnArgs& a, cudaStream_t st);
+// Causal attention of a prefill call (same arguments; n_chunks, part_o, part_ml, counters
+// unused): tiles of 64 positions shared by 64 query rows of one KV head.
+cudaError_t launch_attn_prefill(const AttnArgs& a, cudaStream_t st);
+cudaError_t prepare_attn_prefill();
 constexpr int kAttnMaxChunks = 64;
 bool attn_decode_supported(int head_dim, int group);
 cudaError_t launch_embed(const DevQ8& table, const int* tok, int ntok, float* out, int ldo, cudaStream_t st);

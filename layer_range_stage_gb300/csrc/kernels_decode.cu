@@ -840,6 +840,7 @@ cudaError_t prepare_kernels() {
   if (e == cudaSuccess) e = prepare_attn<128, 4>();
   if (e == cudaSuccess) e = prepare_attn<128, 8>();
   if (e == cudaSuccess) e = prepare_mega();
+  if (e == cudaSuccess) e = prepare_attn_prefill();
   done = e;
   return e;
 }

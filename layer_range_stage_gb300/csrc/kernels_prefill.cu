@@ -7,6 +7,7 @@
 // bf16 (activations rounded once, weights as bf16(f32(scale) * q)), accumulation is f32.
 
 #include <algorithm>
+#include <cfloat>
 
 #include "common.cuh"
 #include "kernels.cuh"
@@ -42,7 +43,9 @@ __global__ void __launch_bounds__(kGThreads, 1) gemm_tc_kernel(const GemmArgs a)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kGOffBar + 16);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kGOffBar + 32);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int m0 = blockIdx.y * kGBM, n0 = blockIdx.x * kGBN;
+  // M tiles vary fastest across the grid: the CTAs that share a weight tile run together
+  // and read it from DRAM once (the activations, a few MB, stay in L2 for every N tile)
+  const int m0 = blockIdx.x * kGBM, n0 = blockIdx.y * kGBN;
   const int N = a.w.N, Kp = a.w.Kp, M = a.M;
   const int nk = Kp / kGBK;
 
@@ -230,7 +233,7 @@ cudaError_t prepare_gemm_tc() {
 cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t st) {
   if (a.M <= 0 || a.w.N <= 0) return cudaSuccess;
   if (a.w.Kp % kGBK || a.lda < a.w.Kp || a.lda % 8) return cudaErrorInvalidValue;
-  const dim3 grid((a.w.N + kGBN - 1) / kGBN, (a.M + kGBM - 1) / kGBM);
+  const dim3 grid((a.M + kGBM - 1) / kGBM, (a.w.N + kGBN - 1) / kGBN);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(kGThreads);
@@ -291,6 +294,259 @@ cudaError_t launch_rows_to_bf16(const float* x, int ld_in, int K, const float* g
   cfg.attrs = attr;
   cfg.numAttrs = pdl_enabled() ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, rows_to_bf16_kernel, x, ld_in, K, gamma, eps, out, ld_out);
+}
+
+// ------------------------------------------------------------------------------------------
+// Causal attention of a prefill call, tiled (CUDA cores, f32 math over the fp16 cache).
+//
+// "41. Many GPUs: tensor, pipeline, expert and data parallelism", section "Ring attention for
+// very long contexts": softmax(q k^T / sqrt(D)) v with a running max and sum over tiles of
+// positions (the same log-sum-exp recurrence its merge uses), here over the tiles of one
+// sequence in order.  A CTA takes 64 query rows -- the G query heads of one KV head for 64 / G
+// consecutive tokens of the call -- and every K/V tile of 64 positions it loads serves all of
+// them.  Token t attends to positions 0..pos[t] of sequence seq[t]; a block that spans two
+// sequences walks each sequence's tiles in turn with the other rows masked.  The tokens' own
+// K/V rows are already in the cache (written by the QKV projection).
+
+constexpr int kPR = 64;       // query rows per CTA
+constexpr int kPT = 64;       // positions per K/V tile
+constexpr int kPThreads = 256;
+
+template <int D>
+struct PrefillSmem {
+  static constexpr int QROW = D + 4;   // floats per q row (bank offset between rows)
+  static constexpr int KROW = D + 8;   // halves per K/V row (16-byte pad)
+  static constexpr int SROW = kPT + 4; // floats per probability row
+  static constexpr size_t q = (size_t)kPR * QROW * 4;
+  static constexpr size_t kv = (size_t)kPT * KROW * 2;
+  static constexpr size_t p = (size_t)kPR * SROW * 4;
+  static constexpr size_t total = q + 2 * kv + p + 4 * kPR * 4;
+};
+
+template <int D, int G>
+__global__ void __launch_bounds__(kPThreads, 2) attn_prefill_kernel(const AttnArgs a) {
+  using S = PrefillSmem<D>;
+  constexpr int QB = kPR / G;  // tokens per CTA
+  extern __shared__ __align__(16) unsigned char ps_raw[];
+  float* qs = reinterpret_cast<float*>(ps_raw);
+  __half* ks = reinterpret_cast<__half*>(ps_raw + S::q);
+  __half* vs = ks + kPT * S::KROW;
+  float* pr = reinterpret_cast<float*>(ps_raw + S::q + 2 * S::kv);
+  int* rseq = reinterpret_cast<int*>(pr + kPR * S::SROW);  // [kPR] sequence of the row's token (-1: none)
+  int* rpos = rseq + kPR;                                   // [kPR] its position
+  pdl_trigger();
+  pdl_wait();
+  const int tid = threadIdx.x, tr = tid >> 3, tc = tid & 7;
+  const int kvh = blockIdx.y, t0 = blockIdx.x * QB;
+  // rows r = i * G + g: token t0 + i, query head kvh * G + g
+  for (int i = tid; i < kPR * (D / 4); i += kPThreads) {
+    const int r = i / (D / 4), c4 = i - r * (D / 4);
+    const int t = t0 + r / G, g = r % G;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (t < a.ntok) v = reinterpret_cast<const float4*>(a.q + ((size_t)t * a.Hq + (size_t)kvh * G + g) * D)[c4];
+    *reinterpret_cast<float4*>(qs + r * S::QROW + 4 * c4) = v;
+  }
+  for (int r = tid; r < kPR; r += kPThreads) {
+    const int t = t0 + r / G;
+    rseq[r] = t < a.ntok ? a.seq[t] : -1;
+    rpos[r] = t < a.ntok ? a.pos[t] : -1;
+  }
+  __syncthreads();
+  // this thread: rows tr and tr + 32; positions tc + 8 j of a tile; output dims tc + 8 k
+  const int r0 = tr, r1 = tr + 32;
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  float o0[D / 8], o1[D / 8];
+#pragma unroll
+  for (int k = 0; k < D / 8; ++k) o0[k] = o1[k] = 0.f;
+  const int sq0 = rseq[r0], sq1 = rseq[r1], pp0 = rpos[r0], pp1 = rpos[r1];
+
+  // walk the distinct sequences of the block in order of first appearance (rows of one
+  // sequence need not be adjacent); every thread reads the same row table, so the walk is
+  // uniform across the CTA
+  for (int rs = 0; rs < kPR; ++rs) {
+    const int sid = rseq[rs];
+    if (sid < 0) continue;
+    bool seen = false;
+    for (int q = 0; q < rs; ++q) seen |= rseq[q] == sid;
+    if (seen) continue;
+    int maxpos = -1;
+    for (int r = rs; r < kPR; ++r)
+      if (rseq[r] == sid) maxpos = max(maxpos, rpos[r]);
+    const __half* kb = a.kc + ((size_t)sid * a.Hkv + kvh) * (size_t)a.max_len * D;
+    const __half* vb = a.vc + ((size_t)sid * a.Hkv + kvh) * (size_t)a.max_len * D;
+    const bool own0 = sq0 == sid, own1 = sq1 == sid;
+    for (int p0 = 0; p0 <= maxpos; p0 += kPT) {
+      const int np = min(kPT, maxpos + 1 - p0);
+      __syncthreads();  // the previous tile is consumed
+      for (int i = tid; i < np * (D / 8); i += kPThreads) {
+        const int r = i / (D / 8), c = i - r * (D / 8);
+        cp_async16(ks + r * S::KROW + c * 8, kb + (size_t)(p0 + r) * D + c * 8);
+        cp_async16(vs + r * S::KROW + c * 8, vb + (size_t)(p0 + r) * D + c * 8);
+      }
+      cp_async_wait_all();
+      __syncthreads();
+      // scores of rows r0, r1 at positions tc + 8 j
+      float s0[8], s1[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) s0[j] = s1[j] = 0.f;
+      const float* q0 = qs + r0 * S::QROW;
+      const float* q1 = qs + r1 * S::QROW;
+#pragma unroll 2
+      for (int d = 0; d < D; d += 8) {
+        const float4 qa0 = *reinterpret_cast<const float4*>(q0 + d), qb0 = *reinterpret_cast<const float4*>(q0 + d + 4);
+        const float4 qa1 = *reinterpret_cast<const float4*>(q1 + d), qb1 = *reinterpret_cast<const float4*>(q1 + d + 4);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint4 kk = *reinterpret_cast<const uint4*>(ks + (tc + 8 * j) * S::KROW + d);
+          const float2 k01 = __half22float2(*reinterpret_cast<const __half2*>(&kk.x));
+          const float2 k23 = __half22float2(*reinterpret_cast<const __half2*>(&kk.y));
+          const float2 k45 = __half22float2(*reinterpret_cast<const __half2*>(&kk.z));
+          const float2 k67 = __half22float2(*reinterpret_cast<const __half2*>(&kk.w));
+          float x = s0[j];
+          x = fmaf(qa0.x, k01.x, x);
+          x = fmaf(qa0.y, k01.y, x);
+          x = fmaf(qa0.z, k23.x, x);
+          x = fmaf(qa0.w, k23.y, x);
+          x = fmaf(qb0.x, k45.x, x);
+          x = fmaf(qb0.y, k45.y, x);
+          x = fmaf(qb0.z, k67.x, x);
+          x = fmaf(qb0.w, k67.y, x);
+          s0[j] = x;
+          float y = s1[j];
+          y = fmaf(qa1.x, k01.x, y);
+          y = fmaf(qa1.y, k01.y, y);
+          y = fmaf(qa1.z, k23.x, y);
+          y = fmaf(qa1.w, k23.y, y);
+          y = fmaf(qb1.x, k45.x, y);
+          y = fmaf(qb1.y, k45.y, y);
+          y = fmaf(qb1.z, k67.x, y);
+          y = fmaf(qb1.w, k67.y, y);
+          s1[j] = y;
+        }
+      }
+      // causal mask, running max and sum per row (the 8 lanes of a row agree via shuffles)
+      float mt0 = -INFINITY, mt1 = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int p = p0 + tc + 8 * j;
+        s0[j] = (own0 && tc + 8 * j < np && p <= pp0) ? s0[j] * a.scale : -INFINITY;
+        s1[j] = (own1 && tc + 8 * j < np && p <= pp1) ? s1[j] * a.scale : -INFINITY;
+        mt0 = fmaxf(mt0, s0[j]);
+        mt1 = fmaxf(mt1, s1[j]);
+      }
+#pragma unroll
+      for (int o = 1; o < 8; o <<= 1) {
+        mt0 = fmaxf(mt0, __shfl_xor_sync(0xffffffffu, mt0, o));
+        mt1 = fmaxf(mt1, __shfl_xor_sync(0xffffffffu, mt1, o));
+      }
+      const float mn0 = fmaxf(m0, mt0), mn1 = fmaxf(m1, mt1);
+      const float al0 = (mn0 == -INFINITY || m0 == -INFINITY) ? (m0 == -INFINITY ? 0.f : 1.f) : expf(m0 - mn0);
+      const float al1 = (mn1 == -INFINITY || m1 == -INFINITY) ? (m1 == -INFINITY ? 0.f : 1.f) : expf(m1 - mn1);
+      float ls0 = 0.f, ls1 = 0.f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float e0 = s0[j] == -INFINITY ? 0.f : expf(s0[j] - mn0);
+        const float e1 = s1[j] == -INFINITY ? 0.f : expf(s1[j] - mn1);
+        pr[r0 * S::SROW + tc + 8 * j] = e0;
+        pr[r1 * S::SROW + tc + 8 * j] = e1;
+        ls0 += e0;
+        ls1 += e1;
+      }
+#pragma unroll
+      for (int o = 1; o < 8; o <<= 1) {
+        ls0 += __shfl_xor_sync(0xffffffffu, ls0, o);
+        ls1 += __shfl_xor_sync(0xffffffffu, ls1, o);
+      }
+      l0 = l0 * al0 + ls0;
+      l1 = l1 * al1 + ls1;
+      m0 = mn0;
+      m1 = mn1;
+      __syncwarp();  // the row's 8 lanes are in this warp: their probabilities are written
+      // o += P V for dims tc + 8 k
+#pragma unroll
+      for (int k = 0; k < D / 8; ++k) {
+        o0[k] *= al0;
+        o1[k] *= al1;
+      }
+      for (int p = 0; p < np; ++p) {
+        const float w0 = pr[r0 * S::SROW + p], w1 = pr[r1 * S::SROW + p];
+        const __half* vr = vs + p * S::KROW;
+#pragma unroll
+        for (int k = 0; k < D / 8; ++k) {
+          const float v = __half2float(vr[tc + 8 * k]);
+          o0[k] = fmaf(w0, v, o0[k]);
+          o1[k] = fmaf(w1, v, o1[k]);
+        }
+      }
+    }
+  }
+  // normalise and store
+  const int ta = t0 + r0 / G, tb = t0 + r1 / G;
+  if (sq0 >= 0 && ta < a.ntok) {
+    float* out = a.out + ((size_t)ta * a.Hq + (size_t)kvh * G + r0 % G) * D;
+    const float inv = 1.0f / l0;
+#pragma unroll
+    for (int k = 0; k < D / 8; ++k) out[tc + 8 * k] = o0[k] * inv;
+  }
+  if (sq1 >= 0 && tb < a.ntok) {
+    float* out = a.out + ((size_t)tb * a.Hq + (size_t)kvh * G + r1 % G) * D;
+    const float inv = 1.0f / l1;
+#pragma unroll
+    for (int k = 0; k < D / 8; ++k) out[tc + 8 * k] = o1[k] * inv;
+  }
+}
+
+template <int D, int G>
+static cudaError_t prepare_attn_prefill_dg() {
+  return cudaFuncSetAttribute(attn_prefill_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)PrefillSmem<D>::total);
+}
+
+cudaError_t prepare_attn_prefill() {
+  const cudaError_t r[] = {prepare_attn_prefill_dg<64, 1>(),  prepare_attn_prefill_dg<64, 2>(),
+                           prepare_attn_prefill_dg<64, 4>(),  prepare_attn_prefill_dg<64, 8>(),
+                           prepare_attn_prefill_dg<128, 1>(), prepare_attn_prefill_dg<128, 2>(),
+                           prepare_attn_prefill_dg<128, 4>(), prepare_attn_prefill_dg<128, 8>()};
+  for (cudaError_t x : r)
+    if (x != cudaSuccess) return x;
+  return cudaSuccess;
+}
+
+template <int D, int G>
+static cudaError_t launch_attn_prefill_dg(const AttnArgs& a, cudaStream_t st) {
+  constexpr int QB = kPR / G;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((a.ntok + QB - 1) / QB, a.Hkv);
+  cfg.blockDim = dim3(kPThreads);
+  cfg.dynamicSmemBytes = PrefillSmem<D>::total;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, attn_prefill_kernel<D, G>, a);
+}
+
+cudaError_t launch_attn_prefill(const AttnArgs& a, cudaStream_t st) {
+  if (a.ntok <= 0) return cudaSuccess;
+  const int G = a.Hq / a.Hkv;
+  if (a.D == 64) {
+    switch (G) {
+      case 1: return launch_attn_prefill_dg<64, 1>(a, st);
+      case 2: return launch_attn_prefill_dg<64, 2>(a, st);
+      case 4: return launch_attn_prefill_dg<64, 4>(a, st);
+      case 8: return launch_attn_prefill_dg<64, 8>(a, st);
+    }
+  } else if (a.D == 128) {
+    switch (G) {
+      case 1: return launch_attn_prefill_dg<128, 1>(a, st);
+      case 2: return launch_attn_prefill_dg<128, 2>(a, st);
+      case 4: return launch_attn_prefill_dg<128, 4>(a, st);
+      case 8: return launch_attn_prefill_dg<128, 8>(a, st);
+    }
+  }
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace lrs

@@ -193,6 +193,7 @@ struct stage {
   float* mega_x1 = nullptr;           // [H] its post-attention residual
   unsigned* mega_bar = nullptr;       // its grid barrier counters
   bool mega = false;                  // single-token decode calls use the persistent kernel
+  bool call_prefill = false;          // the current forward is a prefill call (causal attention kernel)
   std::vector<cudaEvent_t> tev;  // measurement: event pair around each FFN up-projection launch
   bool timing = false;
   int timed_pairs = 0;           // event pairs recorded by the last forward
@@ -462,7 +463,8 @@ int block_tc(stage* st, int li, LayerDev& L, int n, const int* d_seq, const int*
   at.max_len = c.max_seq_len;
   at.n_chunks = n_chunks;
   at.scale = (float)(1.0 / std::sqrt((double)D));
-  if ((e = lrs::launch_attn_decode(at, s)) != cudaSuccess) return cuda_err(st, e, "attention");
+  if ((e = (st->call_prefill ? lrs::launch_attn_prefill(at, s) : lrs::launch_attn_decode(at, s))) != cudaSuccess)
+    return cuda_err(st, e, "attention");
   if ((e = lrs::launch_rows_to_bf16(st->obuf, Hq * D, Hq * D, nullptr, 0.f, n, st->act_bf16, ldq, s)) != cudaSuccess)
     return cuda_err(st, e, "attention out");
   lrs::GemmArgs o;
@@ -595,7 +597,9 @@ int forward_dev(stage* st, int n, const int* d_seq, const int* d_pos, const int*
     a.max_len = c.max_seq_len;
     a.n_chunks = n_chunks;
     a.scale = (float)(1.0 / std::sqrt((double)D));
-    if ((e = lrs::launch_attn_decode(a, s)) != cudaSuccess) return cuda_err(st, e, "attention");
+    if ((e = ((st->call_prefill && n > 1) ? lrs::launch_attn_prefill(a, s) : lrs::launch_attn_decode(a, s))) !=
+        cudaSuccess)
+      return cuda_err(st, e, "attention");
 
     lrs::GemvArgs o;
     o.w = L.wo;
@@ -777,6 +781,7 @@ int run_forward(stage* st, bool decode, int n, const int32_t* seq, const int32_t
   if (e == cudaSuccess && tok) e = cudaMemcpyAsync(st->d_tok, st->h_stage + 2 * T, n * 4, cudaMemcpyHostToDevice, st->stream);
   if (e == cudaSuccess) e = cudaEventRecord(st->staged, st->stream);
   if (e != cudaSuccess) return cuda_err(st, e, "stage inputs");
+  st->call_prefill = !decode;
   rc = forward_dev(st, n, st->d_seq, st->d_pos, st->d_tok, hin ? hin->data : nullptr, hout->data,
                    attn_chunks(st, n, max_len), st->stream);
   if (rc) return rc;
@@ -1260,6 +1265,7 @@ int stage_pipeline_generate(stage_pipeline_t p, int batch, const int32_t* seq_id
   auto one_step = [&](cudaStream_t s) -> int {
     for (size_t i = 0; i < p->stages.size(); ++i) {
       stage* st = p->stages[i];
+      st->call_prefill = false;
       int rc = forward_dev(st, batch, p->d_seq, p->d_pos, p->d_tok, p->hbuf, p->hbuf, n_chunks, s);
       if (rc) return pset(p, rc, "stage %zu: %s", i, st->err.c_str());
     }
