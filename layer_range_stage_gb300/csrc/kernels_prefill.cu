@@ -9,6 +9,9 @@
 #include <algorithm>
 #include <cfloat>
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "common.cuh"
 #include "kernels.cuh"
 #include "tc.cuh"
@@ -16,19 +19,35 @@
 namespace lrs {
 
 // CTA tile: 256 tokens (two M = 128 MMAs) x 256 weight rows (N = 256) x 64 of K per step.
-constexpr int kGBM = 256, kGBN = 256, kGBK = 64, kGStages = 3, kGThreads = 256;
+// Warp roles during the main loop, coupled only by mbarriers:
+//   warps 0-7: dequantise each int8 weight tile into a 128B-swizzled bf16 tile,
+//     bf16(f32(scale) * q), one row per thread;
+//   warp 8 (one thread): TMA loads -- activations through a 128B-swizzled tensor map (they
+//     land in the tensor core's K-major layout), raw int8 weight tiles and fp16 scales through
+//     plain tensor maps; the weights do not depend on the previous kernel and are requested
+//     before waiting for it;
+//   warp 9 (one thread): issues the tcgen05 MMAs of a K step once its activation stage and
+//     bf16 weight tile are full, and commits their completion to the stages' "empty" barriers;
+// then warps 0-7 run the epilogue from TMEM.  Every wait is bounded (and gives up at once
+// when another role has given up); a CTA that gives up sets the error word, waits (bounded)
+// for the copies and MMAs it started, releases TMEM and leaves.
+constexpr int kGBM = 256, kGBN = 256, kGBK = 64, kGThreads = 320;
+constexpr int kGDeq = 256;  // dequantising threads (warps 0-7), one weight row each
+constexpr int kGSA = 3;  // activation stages
+constexpr int kGSR = 3;  // raw weight stages
 constexpr uint32_t kGTileA = kGBM * kGBK * 2;        // 32 KB bf16, 128B-swizzled K-major
 constexpr uint32_t kGTileB = kGBN * kGBK * 2;        // 32 KB bf16, 128B-swizzled K-major
-constexpr uint32_t kGRawB = kGBN * kGBK;             // 16 KB int8 (biased)
-constexpr uint32_t kGRawS = kGBN * 4;                // 2 fp16 scales per row
+constexpr uint32_t kGRawB = kGBN * kGBK;             // 16 KB int8 (biased), row-major
+constexpr uint32_t kGRawS = kGBN * 16;               // 8 fp16 scales per row = 4 K steps
 constexpr uint32_t kGOffA = 0;
-constexpr uint32_t kGOffB = kGOffA + kGStages * kGTileA;     // 2 dequantised B buffers
-constexpr uint32_t kGOffRB = kGOffB + 2 * kGTileB;
-constexpr uint32_t kGOffRS = kGOffRB + kGStages * kGRawB;
-constexpr uint32_t kGOffBar = kGOffRS + kGStages * kGRawS;
-constexpr uint32_t kGSmem = kGOffBar + 64 + 1024;          // + barriers, tmem slot, alignment slack
-constexpr uint32_t kGTmemCols = 512;                        // two 128 x 256 f32 accumulators
-constexpr uint64_t kGWaitNs = 2000000000ull;
+constexpr uint32_t kGOffB = kGOffA + kGSA * kGTileA;     // 2 dequantised B buffers
+constexpr uint32_t kGOffRB = kGOffB + 2 * kGTileB;       // raw weight stages
+constexpr uint32_t kGOffRS = kGOffRB + kGSR * kGRawB;    // 2 scale stages
+constexpr uint32_t kGOffBar = kGOffRS + 2 * kGRawS;
+constexpr uint32_t kGSmem = kGOffBar + 256 + 1024;       // + barriers, tmem slot, alignment slack
+constexpr uint32_t kGTmemCols = 512;                     // two 128 x 256 f32 accumulators
+constexpr uint64_t kGWaitNs = 500000000ull;              // 0.5 s
+constexpr uint64_t kGDrainNs = 100000000ull;
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
@@ -36,22 +55,66 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return r;
 }
 
-__global__ void __launch_bounds__(kGThreads, 1) gemm_tc_kernel(const GemmArgs a) {
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
+          "r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Bounded wait that also gives up as soon as another role of the CTA has given up.
+__device__ __forceinline__ bool gwait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (*abort_flag) return false;
+    if (global_ns() - t0 > kGWaitNs) {
+      *abort_flag = 1;
+      if (err) atomicExch(err, 1);
+      return false;
+    }
+  }
+  return true;
+}
+
+struct GBars {  // mbarriers of the main loop
+  uint64_t a_full[kGSA], a_empty[kGSA], r_full[kGSR], r_empty[kGSR];
+  uint64_t s_full[2], s_empty[2], b_full[2], b_empty[2], acc_full, mma_drain;
+};
+
+__global__ void __launch_bounds__(kGThreads, 1)
+    gemm_tc_kernel(const GemmArgs a, const __grid_constant__ CUtensorMap tA, const __grid_constant__ CUtensorMap tB,
+                   const __grid_constant__ CUtensorMap tS) {
   extern __shared__ unsigned char g_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(((uintptr_t)g_raw + 1023) & ~(uintptr_t)1023);
-  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + kGOffBar);  // [2] MMA completion
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kGOffBar + 16);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kGOffBar + 32);
+  GBars* B = reinterpret_cast<GBars*>(sm + kGOffBar);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kGOffBar + sizeof(GBars));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kGOffBar + sizeof(GBars) + 8);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // M tiles vary fastest across the grid: the CTAs that share a weight tile run together
   // and read it from DRAM once (the activations, a few MB, stay in L2 for every N tile)
   const int m0 = blockIdx.x * kGBM, n0 = blockIdx.y * kGBN;
-  const int N = a.w.N, Kp = a.w.Kp, M = a.M;
-  const int nk = Kp / kGBK;
+  const int N = a.w.N, M = a.M;
+  const int nk = a.w.Kp / kGBK;
 
   if (tid == 0) {
-    mbar_init(&bar[0], 1);
-    mbar_init(&bar[1], 1);
+    for (int i = 0; i < kGSA; ++i) {
+      mbar_init(&B->a_full[i], 1);
+      mbar_init(&B->a_empty[i], 1);
+    }
+    for (int i = 0; i < kGSR; ++i) {
+      mbar_init(&B->r_full[i], 1);
+      mbar_init(&B->r_empty[i], kGDeq);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&B->s_full[i], 1);
+      mbar_init(&B->s_empty[i], kGDeq);
+      mbar_init(&B->b_full[i], kGDeq);
+      mbar_init(&B->b_empty[i], 1);
+    }
+    mbar_init(&B->acc_full, 1);
+    mbar_init(&B->mma_drain, 1);
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -64,105 +127,131 @@ __global__ void __launch_bounds__(kGThreads, 1) gemm_tc_kernel(const GemmArgs a)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   pdl_trigger();
-  pdl_wait();
 
-  auto issue_loads = [&](int kt) {
-    if (kt < nk) {
-      const int s = kt % kGStages;
-      unsigned char* as = sm + kGOffA + s * kGTileA;
-      unsigned char* rb = sm + kGOffRB + s * kGRawB;
-      unsigned char* rs = sm + kGOffRS + s * kGRawS;
-#pragma unroll
-      for (int i = 0; i < (kGBM * 8) / kGThreads; ++i) {  // activations: 256 rows x 8 chunks of 16 B
-        const int idx = tid + i * kGThreads, r = idx >> 3, c = idx & 7;
-        const int gm = m0 + r;
-        const __nv_bfloat16* src = gm < M ? a.a + (size_t)gm * a.lda + kt * kGBK + c * 8 : a.a;
-        cp_async16_zfill(as + r * 128 + ((c ^ (r & 7)) << 4), src, gm < M ? 16u : 0u);
+  if (warp == 8) {
+    // ---------------- loads ----------------
+    int ia = 0, ir = 0, is = 0;  // loads issued per ring
+    if (lane == 0) {
+      auto load_r = [&](int kt) {  // raw weights (+ the scale group at its first K step)
+        const int r = kt % kGSR;
+        if (kt >= kGSR && !gwait(&B->r_empty[r], (uint32_t)((kt / kGSR) + 1) & 1u, abort_flag, a.err)) return false;
+        mbar_arrive_expect_tx(&B->r_full[r], kGRawB);
+        tma_load_2d(sm + kGOffRB + r * kGRawB, &tB, kt * kGBK, n0, &B->r_full[r]);
+        ++ir;
+        if ((kt & 3) == 0) {
+          const int g = kt >> 2, gs = g & 1;
+          if (g >= 2 && !gwait(&B->s_empty[gs], (uint32_t)((g / 2) + 1) & 1u, abort_flag, a.err)) return false;
+          mbar_arrive_expect_tx(&B->s_full[gs], kGRawS);
+          tma_load_2d(sm + kGOffRS + gs * kGRawS, &tS, g * 8, n0, &B->s_full[gs]);
+          ++is;
+        }
+        return true;
+      };
+      bool ok = true;
+      // weights first: they do not depend on the previous kernel
+      const int pre = min(nk, kGSR);
+      for (int kt = 0; kt < pre && ok; ++kt) ok = load_r(kt);
+      pdl_wait();  // the activations are the previous kernel's output
+      for (int kt = 0; kt < nk && ok; ++kt) {
+        const int s = kt % kGSA;
+        if (kt >= kGSA && !gwait(&B->a_empty[s], (uint32_t)((kt / kGSA) + 1) & 1u, abort_flag, a.err)) break;
+        mbar_arrive_expect_tx(&B->a_full[s], kGTileA);
+        tma_load_2d(sm + kGOffA + s * kGTileA, &tA, kt * kGBK, m0, &B->a_full[s]);
+        ++ia;
+        if (kt + kGSR < nk) ok = load_r(kt + kGSR);
       }
-#pragma unroll
-      for (int i = 0; i < (kGBN * 4) / kGThreads; ++i) {  // weights: 256 rows x 4 chunks of 16 int8
-        const int idx = tid + i * kGThreads, n = idx >> 2, j = idx & 3;
-        const int gn = n0 + n;
-        const uint8_t* src = gn < N ? a.w.q + (size_t)gn * Kp + kt * kGBK + j * 16 : a.w.q;
-        cp_async16_zfill(rb + n * 64 + j * 16, src, gn < N ? 16u : 0u);
-      }
-      {  // the 2 block scales of row tid for this K step
-        const int gn = n0 + tid;
-        if (gn < N)
-          cp_async4(rs + tid * 4, a.w.s + (size_t)gn * (Kp / 32) + kt * 2);
-        else
-          *reinterpret_cast<uint32_t*>(rs + tid * 4) = 0u;
+      // nothing may still be landing in shared memory when the CTA leaves
+      if (*abort_flag) {
+        for (int k = max(0, ia - kGSA); k < ia; ++k)
+          mbar_wait(&B->a_full[k % kGSA], (uint32_t)(k / kGSA) & 1u, kGDrainNs);
+        for (int k = max(0, ir - kGSR); k < ir; ++k)
+          mbar_wait(&B->r_full[k % kGSR], (uint32_t)(k / kGSR) & 1u, kGDrainNs);
+        for (int k = max(0, is - 2); k < is; ++k) mbar_wait(&B->s_full[k & 1], (uint32_t)(k / 2) & 1u, kGDrainNs);
       }
     }
-    cp_async_commit();
-  };
-
-  auto wait_mma = [&](int kt) {  // MMAs of K step kt (and all before) complete
-    if (!*abort_flag && !mbar_wait(&bar[kt & 1], (uint32_t)(kt >> 1) & 1u, kGWaitNs)) {
-      if (a.err) atomicExch(a.err, 1);
-      *abort_flag = 1;
-    }
-  };
-
-  constexpr uint32_t idesc = idesc_bf16_f32(128, kGBN);
-  issue_loads(0);
-  issue_loads(1);
-  for (int kt = 0; kt < nk; ++kt) {
-    const int s = kt % kGStages, buf = kt & 1;
-    cp_async_wait_group<1>();
-    __syncthreads();
-    if (kt >= 2) wait_mma(kt - 2);  // the B buffer about to be written was read by step kt - 2
-    {  // dequantise weight row `tid` of this step into the swizzled bf16 tile
-      const unsigned char* rb = sm + kGOffRB + s * kGRawB + tid * 64;
-      const uint32_t sraw = *reinterpret_cast<const uint32_t*>(sm + kGOffRS + s * kGRawS + tid * 4);
+  } else if (warp < 8) {
+    // ---------------- dequantise: row `tid` of every weight tile ----------------
+    // A byte b moved into the low mantissa bits of 2^23 is the float 2^23 + b; subtracting
+    // 2^23 + 128 gives q = b - 128 exactly, and f32(scale) * q is exact (11 + 8 bits).
+    const int row = tid;
+    for (int kt = 0; kt < nk; ++kt) {
+      const int r = kt % kGSR, bb = kt & 1, g = kt >> 2;
+      if (!gwait(&B->r_full[r], (uint32_t)(kt / kGSR) & 1u, abort_flag, a.err)) break;
+      if ((kt & 3) == 0 && !gwait(&B->s_full[g & 1], (uint32_t)(g / 2) & 1u, abort_flag, a.err)) break;
+      if (kt >= 2 && !gwait(&B->b_empty[bb], (uint32_t)((kt / 2) + 1) & 1u, abort_flag, a.err)) break;
+      const unsigned char* rb = sm + kGOffRB + r * kGRawB;
+      const unsigned char* rs = sm + kGOffRS + (g & 1) * kGRawS;
+      unsigned char* bt = sm + kGOffB + bb * kGTileB;
+      const uint32_t sraw = *reinterpret_cast<const uint32_t*>(rs + row * 16 + (kt & 3) * 4);
       const float s0 = __half2float(__ushort_as_half((uint16_t)(sraw & 0xFFFFu)));
       const float s1 = __half2float(__ushort_as_half((uint16_t)(sraw >> 16)));
-      unsigned char* bt = sm + kGOffB + buf * kGTileB;
+      constexpr float kBias = 8388736.0f;  // 2^23 + 128
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const uint4 w = *reinterpret_cast<const uint4*>(rb + j * 16);
+      for (int jj = 0; jj < 4; ++jj) {
+        const int j = (jj + row) & 3;  // rotated: neighbouring rows read different banks
+        const uint4 w = *reinterpret_cast<const uint4*>(rb + row * 64 + j * 16);
         const float sc = j < 2 ? s0 : s1;
         const uint32_t wd[4] = {w.x, w.y, w.z, w.w};
         uint32_t o[8];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const uint32_t x = wd[q];
-          const float f0 = sc * (float)((int)(x & 0xFFu) - 128);
-          const float f1 = sc * (float)((int)((x >> 8) & 0xFFu) - 128);
-          const float f2 = sc * (float)((int)((x >> 16) & 0xFFu) - 128);
-          const float f3 = sc * (float)((int)(x >> 24) - 128);
+          const float f0 = sc * (__uint_as_float(__byte_perm(x, 0x4B000000u, 0x7440)) - kBias);
+          const float f1 = sc * (__uint_as_float(__byte_perm(x, 0x4B000000u, 0x7441)) - kBias);
+          const float f2 = sc * (__uint_as_float(__byte_perm(x, 0x4B000000u, 0x7442)) - kBias);
+          const float f3 = sc * (__uint_as_float(__byte_perm(x, 0x4B000000u, 0x7443)) - kBias);
           o[2 * q] = pack_bf16x2(f0, f1);
           o[2 * q + 1] = pack_bf16x2(f2, f3);
         }
-        *reinterpret_cast<uint4*>(bt + sw128_offset(tid, 16 * j)) = make_uint4(o[0], o[1], o[2], o[3]);
-        *reinterpret_cast<uint4*>(bt + sw128_offset(tid, 16 * j + 8)) = make_uint4(o[4], o[5], o[6], o[7]);
+        *reinterpret_cast<uint4*>(bt + sw128_offset(row, 16 * j)) = make_uint4(o[0], o[1], o[2], o[3]);
+        *reinterpret_cast<uint4*>(bt + sw128_offset(row, 16 * j + 8)) = make_uint4(o[4], o[5], o[6], o[7]);
+      }
+      fence_async_smem();  // the bf16 tile is read next by the tensor core (async proxy)
+      mbar_arrive(&B->b_full[bb]);
+      mbar_arrive(&B->r_empty[r]);
+      if ((kt & 3) == 3) mbar_arrive(&B->s_empty[g & 1]);
+    }
+  } else if (warp == 9) {
+    // ---------------- MMA issue ----------------
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(128, kGBN);
+      int issued = 0;
+      for (int kt = 0; kt < nk; ++kt) {
+        const int s = kt % kGSA, bb = kt & 1;
+        if (!gwait(&B->a_full[s], (uint32_t)(kt / kGSA) & 1u, abort_flag, a.err)) break;
+        if (!gwait(&B->b_full[bb], (uint32_t)(kt / 2) & 1u, abort_flag, a.err)) break;
+        tc_fence_after();
+        const uint32_t a_base = smem_u32(sm + kGOffA + s * kGTileA);
+        const uint32_t b_base = smem_u32(sm + kGOffB + bb * kGTileB);
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int kk = 0; kk < kGBK / 16; ++kk)
+            umma_bf16(tmem + h * kGBN, desc_sw128(a_base + h * (128 * 128) + kk * 32), desc_sw128(b_base + kk * 32),
+                      idesc, (kt > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(&B->a_empty[s]);
+        umma_commit(&B->b_empty[bb]);
+        ++issued;
+      }
+      if (issued == nk) {
+        umma_commit(&B->acc_full);
+      } else if (issued > 0) {  // given up: let the MMAs already issued finish before TMEM is released
+        umma_commit(&B->mma_drain);
+        mbar_wait(&B->mma_drain, 0u, kGDrainNs);
       }
     }
-    fence_async_smem();
-    __syncthreads();
-    if (tid == 0 && !*abort_flag) {
-      tc_fence_after();
-      const uint32_t a_base = smem_u32(sm + kGOffA + s * kGTileA);
-      const uint32_t b_base = smem_u32(sm + kGOffB + buf * kGTileB);
-#pragma unroll
-      for (int h = 0; h < 2; ++h)
-#pragma unroll
-        for (int kk = 0; kk < kGBK / 16; ++kk)
-          umma_bf16(tmem + h * kGBN, desc_sw128(a_base + h * (128 * 128) + kk * 32), desc_sw128(b_base + kk * 32),
-                    idesc, (kt > 0 || kk > 0) ? 1u : 0u);
-      umma_commit(&bar[buf]);
-    }
-    if (kt >= 1) wait_mma(kt - 1);  // the stage about to be refilled was read by step kt - 1
-    issue_loads(kt + 2);
   }
-  wait_mma(nk - 1);
-  cp_async_wait_group<0>();
+  __syncthreads();
+  if (tid == 0 && !*abort_flag) gwait(&B->acc_full, 0u, abort_flag, a.err);
+  __syncthreads();
+  const bool ok = !*abort_flag;
   tc_fence_after();
+  pdl_wait();  // the epilogue reads the residual / writes outputs the previous kernel may touch
 
-  // ---- epilogue: warp w reads TMEM lanes 32 (w % 4) .. +31, columns of its half ----
-  const int p = warp & 3, chalf = warp >> 2;
+  // ---- epilogue (warps 0-7): warp w reads TMEM lanes 32 (w % 4) .. +31, columns of its half ----
+  const int p = warp & 3, chalf = (warp >> 2) & 1;
 #pragma unroll 1
-  for (int h = 0; h < 2; ++h) {
+  for (int h = 0; h < 2 && ok && warp < 8; ++h) {
     const int gm = m0 + h * 128 + 32 * p + lane;
 #pragma unroll 1
     for (int cc = 0; cc < 4; ++cc) {
@@ -170,7 +259,7 @@ __global__ void __launch_bounds__(kGThreads, 1) gemm_tc_kernel(const GemmArgs a)
       uint32_t r[32];
       tmem_ld32(tmem + ((uint32_t)(32 * p) << 16) + (uint32_t)(h * kGBN + c0), r);
       tmem_wait_ld();
-      if (*abort_flag || gm >= M) continue;
+      if (gm >= M) continue;
       const int gn0 = n0 + c0;
       if (a.epi == EPI_STORE || a.epi == EPI_RESID) {
         float* orow = a.out + (size_t)gm * a.ldo;
@@ -227,12 +316,50 @@ __global__ void __launch_bounds__(kGThreads, 1) gemm_tc_kernel(const GemmArgs a)
 }
 
 cudaError_t prepare_gemm_tc() {
+  static_assert(sizeof(GBars) + 16 <= 256, "barrier block");
   return cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGSmem);
 }
 
+namespace {
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
+               uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+}  // namespace
+
 cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t st) {
   if (a.M <= 0 || a.w.N <= 0) return cudaSuccess;
-  if (a.w.Kp % kGBK || a.lda < a.w.Kp || a.lda % 8) return cudaErrorInvalidValue;
+  // Kp a multiple of 256 (scale groups of 4 K steps), 16-byte aligned rows and bases
+  if (a.w.Kp % 256 || a.lda < a.w.Kp || a.lda % 8 || ((uintptr_t)a.a & 15) || ((uintptr_t)a.w.q & 15) ||
+      ((uintptr_t)a.w.s & 15))
+    return cudaErrorInvalidValue;
+  CUtensorMap tA, tB, tS;
+  if (!encode_2d(&tA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.a, (uint64_t)a.w.Kp, (uint64_t)a.M, (uint64_t)a.lda * 2,
+                 kGBK, kGBM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_2d(&tB, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.w.q, (uint64_t)a.w.Kp, (uint64_t)a.w.N, (uint64_t)a.w.Kp,
+                 kGBK, kGBN, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      !encode_2d(&tS, CU_TENSOR_MAP_DATA_TYPE_UINT16, a.w.s, (uint64_t)(a.w.Kp / 32), (uint64_t)a.w.N,
+                 (uint64_t)(a.w.Kp / 16), 8, kGBN, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return cudaErrorInvalidValue;
   const dim3 grid((a.M + kGBM - 1) / kGBM, (a.w.N + kGBN - 1) / kGBN);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
@@ -244,7 +371,7 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t st) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl_enabled() ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel, a);
+  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel, a, tA, tB, tS);
 }
 
 // ------------------------------------------------------------------------------------------
