@@ -22,16 +22,16 @@ namespace lrs {
 // Warp roles during the main loop, coupled only by mbarriers:
 //   warps 0-7: dequantise each int8 weight tile into a 128B-swizzled bf16 tile,
 //     bf16(f32(scale) * q), one row per thread;
-//   warp 8 (one thread): TMA loads -- activations through a 128B-swizzled tensor map (they
-//     land in the tensor core's K-major layout), raw int8 weight tiles and fp16 scales through
-//     plain tensor maps; the weights do not depend on the previous kernel and are requested
-//     before waiting for it;
+//   warp 8 (one thread): TMA loads of the activations through a 128B-swizzled tensor map
+//     (they land in the tensor core's K-major layout), after the programmatic-launch wait;
+//   warp 10 (one thread): TMA loads of the raw int8 weight tiles and fp16 scale groups through
+//     plain tensor maps; the weights do not depend on the previous kernel and start at once;
 //   warp 9 (one thread): issues the tcgen05 MMAs of a K step once its activation stage and
 //     bf16 weight tile are full, and commits their completion to the stages' "empty" barriers;
 // then warps 0-7 run the epilogue from TMEM.  Every wait is bounded (and gives up at once
 // when another role has given up); a CTA that gives up sets the error word, waits (bounded)
 // for the copies and MMAs it started, releases TMEM and leaves.
-constexpr int kGBM = 256, kGBN = 256, kGBK = 64, kGThreads = 320;
+constexpr int kGBM = 256, kGBN = 256, kGBK = 64, kGThreads = 352;
 constexpr int kGDeq = 256;  // dequantising threads (warps 0-7), one weight row each
 constexpr int kGSA = 3;  // activation stages
 constexpr int kGSR = 3;  // raw weight stages
@@ -129,41 +129,40 @@ __global__ void __launch_bounds__(kGThreads, 1)
   pdl_trigger();
 
   if (warp == 8) {
-    // ---------------- loads ----------------
-    int ia = 0, ir = 0, is = 0;  // loads issued per ring
+    // ---------------- activation loads ----------------
     if (lane == 0) {
-      auto load_r = [&](int kt) {  // raw weights (+ the scale group at its first K step)
-        const int r = kt % kGSR;
-        if (kt >= kGSR && !gwait(&B->r_empty[r], (uint32_t)((kt / kGSR) + 1) & 1u, abort_flag, a.err)) return false;
-        mbar_arrive_expect_tx(&B->r_full[r], kGRawB);
-        tma_load_2d(sm + kGOffRB + r * kGRawB, &tB, kt * kGBK, n0, &B->r_full[r]);
-        ++ir;
-        if ((kt & 3) == 0) {
-          const int g = kt >> 2, gs = g & 1;
-          if (g >= 2 && !gwait(&B->s_empty[gs], (uint32_t)((g / 2) + 1) & 1u, abort_flag, a.err)) return false;
-          mbar_arrive_expect_tx(&B->s_full[gs], kGRawS);
-          tma_load_2d(sm + kGOffRS + gs * kGRawS, &tS, g * 8, n0, &B->s_full[gs]);
-          ++is;
-        }
-        return true;
-      };
-      bool ok = true;
-      // weights first: they do not depend on the previous kernel
-      const int pre = min(nk, kGSR);
-      for (int kt = 0; kt < pre && ok; ++kt) ok = load_r(kt);
+      int ia = 0;
       pdl_wait();  // the activations are the previous kernel's output
-      for (int kt = 0; kt < nk && ok; ++kt) {
+      for (int kt = 0; kt < nk; ++kt) {
         const int s = kt % kGSA;
         if (kt >= kGSA && !gwait(&B->a_empty[s], (uint32_t)((kt / kGSA) + 1) & 1u, abort_flag, a.err)) break;
         mbar_arrive_expect_tx(&B->a_full[s], kGTileA);
         tma_load_2d(sm + kGOffA + s * kGTileA, &tA, kt * kGBK, m0, &B->a_full[s]);
         ++ia;
-        if (kt + kGSR < nk) ok = load_r(kt + kGSR);
       }
-      // nothing may still be landing in shared memory when the CTA leaves
-      if (*abort_flag) {
+      if (*abort_flag)  // nothing may still be landing in shared memory when the CTA leaves
         for (int k = max(0, ia - kGSA); k < ia; ++k)
           mbar_wait(&B->a_full[k % kGSA], (uint32_t)(k / kGSA) & 1u, kGDrainNs);
+    }
+  } else if (warp == 10) {
+    // ---------------- weight loads: raw tiles, and a scale group every 4 K steps ----------------
+    if (lane == 0) {
+      int ir = 0, is = 0;
+      for (int kt = 0; kt < nk; ++kt) {
+        const int r = kt % kGSR;
+        if (kt >= kGSR && !gwait(&B->r_empty[r], (uint32_t)((kt / kGSR) + 1) & 1u, abort_flag, a.err)) break;
+        if ((kt & 3) == 0) {
+          const int g = kt >> 2, gs = g & 1;
+          if (g >= 2 && !gwait(&B->s_empty[gs], (uint32_t)((g / 2) + 1) & 1u, abort_flag, a.err)) break;
+          mbar_arrive_expect_tx(&B->s_full[gs], kGRawS);
+          tma_load_2d(sm + kGOffRS + gs * kGRawS, &tS, g * 8, n0, &B->s_full[gs]);
+          ++is;
+        }
+        mbar_arrive_expect_tx(&B->r_full[r], kGRawB);
+        tma_load_2d(sm + kGOffRB + r * kGRawB, &tB, kt * kGBK, n0, &B->r_full[r]);
+        ++ir;
+      }
+      if (*abort_flag) {
         for (int k = max(0, ir - kGSR); k < ir; ++k)
           mbar_wait(&B->r_full[k % kGSR], (uint32_t)(k / kGSR) & 1u, kGDrainNs);
         for (int k = max(0, is - 2); k < is; ++k) mbar_wait(&B->s_full[k & 1], (uint32_t)(k / 2) & 1u, kGDrainNs);
@@ -249,38 +248,23 @@ __global__ void __launch_bounds__(kGThreads, 1)
   pdl_wait();  // the epilogue reads the residual / writes outputs the previous kernel may touch
 
   // ---- epilogue (warps 0-7): warp w reads TMEM lanes 32 (w % 4) .. +31, columns of its half ----
+  // Each 32 x 32 block goes through shared memory (the activation stages are idle now) so
+  // that a warp writes whole row segments: lane = column for the stores.
   const int p = warp & 3, chalf = (warp >> 2) & 1;
+  float* stg = reinterpret_cast<float*>(sm + kGOffA) + warp * (32 * 33);  // [32][33] per warp
 #pragma unroll 1
   for (int h = 0; h < 2 && ok && warp < 8; ++h) {
-    const int gm = m0 + h * 128 + 32 * p + lane;
+    const int rbase = m0 + h * 128 + 32 * p;
 #pragma unroll 1
     for (int cc = 0; cc < 4; ++cc) {
       const int c0 = chalf * 128 + cc * 32;
       uint32_t r[32];
       tmem_ld32(tmem + ((uint32_t)(32 * p) << 16) + (uint32_t)(h * kGBN + c0), r);
       tmem_wait_ld();
-      if (gm >= M) continue;
       const int gn0 = n0 + c0;
-      if (a.epi == EPI_STORE || a.epi == EPI_RESID) {
-        float* orow = a.out + (size_t)gm * a.ldo;
-        const float* rrow = a.epi == EPI_RESID ? a.resid + (size_t)gm * a.ldr : nullptr;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int gn = gn0 + i;
-          if (gn < N) {
-            float v = __uint_as_float(r[i]);
-            if (rrow) v = __fadd_rn(rrow[gn], v);
-            orow[gn] = v;
-          }
-        }
-      } else if (a.epi == EPI_SWIGLU_BF16) {
-        __nv_bfloat16* orow = a.out_bf16 + (size_t)gm * a.ldo_bf16;
-#pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          const int gn = gn0 + i;
-          if (gn < N) orow[gn >> 1] = __float2bfloat16_rn(silu(__uint_as_float(r[i])) * __uint_as_float(r[i + 1]));
-        }
-      } else {  // EPI_QKV: column pairs (2i, 2i+1) of a head are its dims (i, i + D/2)
+      if (a.epi == EPI_QKV) {  // column pairs (2i, 2i+1) of a head are its dims (i, i + D/2)
+        const int gm = rbase + lane;
+        if (gm >= M) continue;
         const int hd = a.head_dim >> 1, pp = a.pos[gm];
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
@@ -307,7 +291,32 @@ __global__ void __launch_bounds__(kGThreads, 1)
             }
           }
         }
+        continue;
       }
+#pragma unroll
+      for (int i = 0; i < 32; ++i) stg[lane * 33 + i] = __uint_as_float(r[i]);
+      __syncwarp();
+      const int gn = gn0 + lane;
+      if (a.epi == EPI_SWIGLU_BF16) {  // lanes 2i, 2i+1 hold gate_i, up_i of the row
+#pragma unroll 4
+        for (int j = 0; j < 32; ++j) {
+          const int gm = rbase + j;
+          const float v = stg[j * 33 + lane];
+          const float u = __shfl_down_sync(0xffffffffu, v, 1);
+          if (gm < M && !(lane & 1) && gn < N)
+            a.out_bf16[(size_t)gm * a.ldo_bf16 + (gn >> 1)] = __float2bfloat16_rn(silu(v) * u);
+        }
+      } else {  // EPI_STORE / EPI_RESID
+#pragma unroll 4
+        for (int j = 0; j < 32; ++j) {
+          const int gm = rbase + j;
+          if (gm >= M || gn >= N) continue;
+          float v = stg[j * 33 + lane];
+          if (a.epi == EPI_RESID) v = __fadd_rn(a.resid[(size_t)gm * a.ldr + gn], v);
+          a.out[(size_t)gm * a.ldo + gn] = v;
+        }
+      }
+      __syncwarp();
     }
   }
   tc_fence_before();
