@@ -262,16 +262,19 @@ __global__ void __launch_bounds__(kGThreads, 1)
       tmem_ld32(tmem + ((uint32_t)(32 * p) << 16) + (uint32_t)(h * kGBN + c0), r);
       tmem_wait_ld();
       const int gn0 = n0 + c0;
-      if (a.epi == EPI_QKV) {  // column pairs (2i, 2i+1) of a head are its dims (i, i + D/2)
-        const int gm = rbase + lane;
-        if (gm >= M) continue;
-        const int hd = a.head_dim >> 1, pp = a.pos[gm];
 #pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          const int gn = gn0 + i;
-          if (gn >= N) continue;
-          const float y0 = __uint_as_float(r[i]), y1 = __uint_as_float(r[i + 1]);
-          const int P = gn >> 1, head = P / hd, ii = P - head * hd;
+      for (int i = 0; i < 32; ++i) stg[lane * 33 + i] = __uint_as_float(r[i]);
+      __syncwarp();
+      const int gn = gn0 + lane;
+      if (a.epi == EPI_QKV) {  // column pairs (2i, 2i+1) of a head are its dims (i, i + D/2)
+        const int i = lane & 15, half = lane >> 4;  // two rows per pass, 16 pairs each
+        const int hd = a.head_dim >> 1, P = (gn0 >> 1) + i, head = P / hd, ii = P - head * hd;
+#pragma unroll 2
+        for (int j = 0; j < 32; j += 2) {
+          const int jr = j + half, gm = rbase + jr;
+          if (gm >= M || gn0 + 2 * i >= N) continue;
+          const float y0 = stg[jr * 33 + 2 * i], y1 = stg[jr * 33 + 2 * i + 1];
+          const int pp = a.pos[gm];
           if (head < a.n_q_heads) {
             const float2 cs = a.rope[(size_t)pp * hd + ii];
             float* qo = a.qout + ((size_t)gm * a.n_q_heads + head) * a.head_dim;
@@ -291,20 +294,14 @@ __global__ void __launch_bounds__(kGThreads, 1)
             }
           }
         }
-        continue;
-      }
-#pragma unroll
-      for (int i = 0; i < 32; ++i) stg[lane * 33 + i] = __uint_as_float(r[i]);
-      __syncwarp();
-      const int gn = gn0 + lane;
-      if (a.epi == EPI_SWIGLU_BF16) {  // lanes 2i, 2i+1 hold gate_i, up_i of the row
+      } else if (a.epi == EPI_SWIGLU_BF16) {  // columns (2i, 2i+1) are (gate_i, up_i): 16 outputs per row
+        const int i = lane & 15, half = lane >> 4;    // two rows per pass, 16 lanes each
+        const int go = (gn0 >> 1) + i;
 #pragma unroll 4
-        for (int j = 0; j < 32; ++j) {
-          const int gm = rbase + j;
-          const float v = stg[j * 33 + lane];
-          const float u = __shfl_down_sync(0xffffffffu, v, 1);
-          if (gm < M && !(lane & 1) && gn < N)
-            a.out_bf16[(size_t)gm * a.ldo_bf16 + (gn >> 1)] = __float2bfloat16_rn(silu(v) * u);
+        for (int j = 0; j < 32; j += 2) {
+          const int jr = j + half, gm = rbase + jr;
+          const float g = stg[jr * 33 + 2 * i], u = stg[jr * 33 + 2 * i + 1];
+          if (gm < M && gn0 + 2 * i < N) a.out_bf16[(size_t)gm * a.ldo_bf16 + go] = __float2bfloat16_rn(silu(g) * u);
         }
       } else {  // EPI_STORE / EPI_RESID
 #pragma unroll 4
