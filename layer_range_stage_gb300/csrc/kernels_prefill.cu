@@ -442,29 +442,36 @@ cudaError_t launch_rows_to_bf16(const float* x, int ld_in, int K, const float* g
 // K/V rows are already in the cache (written by the QKV projection).
 
 constexpr int kPR = 64;       // query rows per CTA
-constexpr int kPT = 64;       // positions per K/V tile
+constexpr int kPT = 32;       // positions per K/V tile
 constexpr int kPThreads = 256;
 
 template <int D>
 struct PrefillSmem {
-  static constexpr int QROW = D + 4;   // floats per q row (bank offset between rows)
-  static constexpr int KROW = D + 8;   // halves per K/V row (16-byte pad)
-  static constexpr int SROW = kPT + 4; // floats per probability row
+  static constexpr int QROW = D + 4;    // floats per q / K / V row (bank offset between rows)
+  static constexpr int HROW = D + 8;    // halves per raw K/V row (16-byte pad)
+  static constexpr int SROW = kPT + 4;  // floats per probability row
   static constexpr size_t q = (size_t)kPR * QROW * 4;
-  static constexpr size_t kv = (size_t)kPT * KROW * 2;
+  static constexpr size_t kf = (size_t)kPT * QROW * 4;      // K tile, f32
+  static constexpr size_t raw = (size_t)2 * kPT * HROW * 2;  // one raw K + V tile, fp16
   static constexpr size_t p = (size_t)kPR * SROW * 4;
-  static constexpr size_t total = q + 2 * kv + p + 4 * kPR * 4;
+  static constexpr size_t total = q + 2 * kf + 2 * raw + p + 2 * kPR * 4;
 };
 
+// Thread (tr, tc) = (tid / 8, tid % 8): query rows tr and tr + 32; scores at positions
+// tc + 8 j of a tile; output dims 4 tc + 32 m + e.  K and V tiles are converted to f32 in
+// shared memory once (one copy for all threads); the raw fp16 rows of the next tile stream in
+// with cp.async meanwhile.
 template <int D, int G>
 __global__ void __launch_bounds__(kPThreads, 2) attn_prefill_kernel(const AttnArgs a) {
   using S = PrefillSmem<D>;
-  constexpr int QB = kPR / G;  // tokens per CTA
+  constexpr int QB = kPR / G;    // tokens per CTA
+  constexpr int NM = D / 32;     // float4 groups of output dims per thread
   extern __shared__ __align__(16) unsigned char ps_raw[];
   float* qs = reinterpret_cast<float*>(ps_raw);
-  __half* ks = reinterpret_cast<__half*>(ps_raw + S::q);
-  __half* vs = ks + kPT * S::KROW;
-  float* pr = reinterpret_cast<float*>(ps_raw + S::q + 2 * S::kv);
+  float* kf = reinterpret_cast<float*>(ps_raw + S::q);
+  float* vf = kf + kPT * S::QROW;
+  __half* rawb = reinterpret_cast<__half*>(ps_raw + S::q + 2 * S::kf);  // [2 buffers][K, V][kPT][HROW]
+  float* pr = reinterpret_cast<float*>(ps_raw + S::q + 2 * S::kf + 2 * S::raw);
   int* rseq = reinterpret_cast<int*>(pr + kPR * S::SROW);  // [kPR] sequence of the row's token (-1: none)
   int* rpos = rseq + kPR;                                   // [kPR] its position
   pdl_trigger();
@@ -485,12 +492,11 @@ __global__ void __launch_bounds__(kPThreads, 2) attn_prefill_kernel(const AttnAr
     rpos[r] = t < a.ntok ? a.pos[t] : -1;
   }
   __syncthreads();
-  // this thread: rows tr and tr + 32; positions tc + 8 j of a tile; output dims tc + 8 k
   const int r0 = tr, r1 = tr + 32;
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-  float o0[D / 8], o1[D / 8];
+  float4 o0[NM], o1[NM];
 #pragma unroll
-  for (int k = 0; k < D / 8; ++k) o0[k] = o1[k] = 0.f;
+  for (int m = 0; m < NM; ++m) o0[m] = o1[m] = make_float4(0.f, 0.f, 0.f, 0.f);
   const int sq0 = rseq[r0], sq1 = rseq[r1], pp0 = rpos[r0], pp1 = rpos[r1];
 
   // walk the distinct sequences of the block in order of first appearance (rows of one
@@ -508,59 +514,85 @@ __global__ void __launch_bounds__(kPThreads, 2) attn_prefill_kernel(const AttnAr
     const __half* kb = a.kc + ((size_t)sid * a.Hkv + kvh) * (size_t)a.max_len * D;
     const __half* vb = a.vc + ((size_t)sid * a.Hkv + kvh) * (size_t)a.max_len * D;
     const bool own0 = sq0 == sid, own1 = sq1 == sid;
-    for (int p0 = 0; p0 <= maxpos; p0 += kPT) {
+    auto fetch = [&](int p0, int buf) {  // raw fp16 rows of the tile at p0 into buffer buf
       const int np = min(kPT, maxpos + 1 - p0);
-      __syncthreads();  // the previous tile is consumed
+      __half* rk = rawb + (size_t)buf * 2 * kPT * S::HROW;
+      __half* rv = rk + kPT * S::HROW;
       for (int i = tid; i < np * (D / 8); i += kPThreads) {
         const int r = i / (D / 8), c = i - r * (D / 8);
-        cp_async16(ks + r * S::KROW + c * 8, kb + (size_t)(p0 + r) * D + c * 8);
-        cp_async16(vs + r * S::KROW + c * 8, vb + (size_t)(p0 + r) * D + c * 8);
+        cp_async16(rk + r * S::HROW + c * 8, kb + (size_t)(p0 + r) * D + c * 8);
+        cp_async16(rv + r * S::HROW + c * 8, vb + (size_t)(p0 + r) * D + c * 8);
       }
-      cp_async_wait_all();
+      cp_async_commit();
+    };
+    __syncthreads();  // the previous walk is done with the raw buffers
+    fetch(0, 0);
+    int buf = 0;
+    for (int p0 = 0; p0 <= maxpos; p0 += kPT, buf ^= 1) {
+      const int np = min(kPT, maxpos + 1 - p0);
+      if (p0 + kPT <= maxpos) {
+        fetch(p0 + kPT, buf ^ 1);
+        cp_async_wait_group<1>();
+      } else {
+        cp_async_wait_group<0>();
+      }
+      __syncthreads();  // raw tile `buf` landed for every thread; the previous f32 tile is consumed
+      {  // convert to f32 (rows beyond np are zero)
+        const __half* rk = rawb + (size_t)buf * 2 * kPT * S::HROW;
+        const __half* rv = rk + kPT * S::HROW;
+        for (int i = tid; i < kPT * (D / 8); i += kPThreads) {
+          const int r = i / (D / 8), c = i - r * (D / 8);
+          float4 k0 = make_float4(0.f, 0.f, 0.f, 0.f), k1 = k0, v0 = k0, v1 = k0;
+          if (r < np) {
+            const uint4 kk = *reinterpret_cast<const uint4*>(rk + r * S::HROW + c * 8);
+            const uint4 vv = *reinterpret_cast<const uint4*>(rv + r * S::HROW + c * 8);
+            const float2 a0 = __half22float2(*reinterpret_cast<const __half2*>(&kk.x));
+            const float2 a1 = __half22float2(*reinterpret_cast<const __half2*>(&kk.y));
+            const float2 a2 = __half22float2(*reinterpret_cast<const __half2*>(&kk.z));
+            const float2 a3 = __half22float2(*reinterpret_cast<const __half2*>(&kk.w));
+            const float2 b0 = __half22float2(*reinterpret_cast<const __half2*>(&vv.x));
+            const float2 b1 = __half22float2(*reinterpret_cast<const __half2*>(&vv.y));
+            const float2 b2 = __half22float2(*reinterpret_cast<const __half2*>(&vv.z));
+            const float2 b3 = __half22float2(*reinterpret_cast<const __half2*>(&vv.w));
+            k0 = make_float4(a0.x, a0.y, a1.x, a1.y);
+            k1 = make_float4(a2.x, a2.y, a3.x, a3.y);
+            v0 = make_float4(b0.x, b0.y, b1.x, b1.y);
+            v1 = make_float4(b2.x, b2.y, b3.x, b3.y);
+          }
+          *reinterpret_cast<float4*>(kf + r * S::QROW + c * 8) = k0;
+          *reinterpret_cast<float4*>(kf + r * S::QROW + c * 8 + 4) = k1;
+          *reinterpret_cast<float4*>(vf + r * S::QROW + c * 8) = v0;
+          *reinterpret_cast<float4*>(vf + r * S::QROW + c * 8 + 4) = v1;
+        }
+      }
       __syncthreads();
       // scores of rows r0, r1 at positions tc + 8 j
-      float s0[8], s1[8];
+      float s0[kPT / 8], s1[kPT / 8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) s0[j] = s1[j] = 0.f;
+      for (int j = 0; j < kPT / 8; ++j) s0[j] = s1[j] = 0.f;
       const float* q0 = qs + r0 * S::QROW;
       const float* q1 = qs + r1 * S::QROW;
-#pragma unroll 2
-      for (int d = 0; d < D; d += 8) {
-        const float4 qa0 = *reinterpret_cast<const float4*>(q0 + d), qb0 = *reinterpret_cast<const float4*>(q0 + d + 4);
-        const float4 qa1 = *reinterpret_cast<const float4*>(q1 + d), qb1 = *reinterpret_cast<const float4*>(q1 + d + 4);
+#pragma unroll 4
+      for (int d = 0; d < D; d += 4) {
+        const float4 qa = *reinterpret_cast<const float4*>(q0 + d);
+        const float4 qb = *reinterpret_cast<const float4*>(q1 + d);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const uint4 kk = *reinterpret_cast<const uint4*>(ks + (tc + 8 * j) * S::KROW + d);
-          const float2 k01 = __half22float2(*reinterpret_cast<const __half2*>(&kk.x));
-          const float2 k23 = __half22float2(*reinterpret_cast<const __half2*>(&kk.y));
-          const float2 k45 = __half22float2(*reinterpret_cast<const __half2*>(&kk.z));
-          const float2 k67 = __half22float2(*reinterpret_cast<const __half2*>(&kk.w));
-          float x = s0[j];
-          x = fmaf(qa0.x, k01.x, x);
-          x = fmaf(qa0.y, k01.y, x);
-          x = fmaf(qa0.z, k23.x, x);
-          x = fmaf(qa0.w, k23.y, x);
-          x = fmaf(qb0.x, k45.x, x);
-          x = fmaf(qb0.y, k45.y, x);
-          x = fmaf(qb0.z, k67.x, x);
-          x = fmaf(qb0.w, k67.y, x);
-          s0[j] = x;
-          float y = s1[j];
-          y = fmaf(qa1.x, k01.x, y);
-          y = fmaf(qa1.y, k01.y, y);
-          y = fmaf(qa1.z, k23.x, y);
-          y = fmaf(qa1.w, k23.y, y);
-          y = fmaf(qb1.x, k45.x, y);
-          y = fmaf(qb1.y, k45.y, y);
-          y = fmaf(qb1.z, k67.x, y);
-          y = fmaf(qb1.w, k67.y, y);
-          s1[j] = y;
+        for (int j = 0; j < kPT / 8; ++j) {
+          const float4 kk = *reinterpret_cast<const float4*>(kf + (tc + 8 * j) * S::QROW + d);
+          s0[j] = fmaf(qa.x, kk.x, s0[j]);
+          s0[j] = fmaf(qa.y, kk.y, s0[j]);
+          s0[j] = fmaf(qa.z, kk.z, s0[j]);
+          s0[j] = fmaf(qa.w, kk.w, s0[j]);
+          s1[j] = fmaf(qb.x, kk.x, s1[j]);
+          s1[j] = fmaf(qb.y, kk.y, s1[j]);
+          s1[j] = fmaf(qb.z, kk.z, s1[j]);
+          s1[j] = fmaf(qb.w, kk.w, s1[j]);
         }
       }
       // causal mask, running max and sum per row (the 8 lanes of a row agree via shuffles)
       float mt0 = -INFINITY, mt1 = -INFINITY;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
+      for (int j = 0; j < kPT / 8; ++j) {
         const int p = p0 + tc + 8 * j;
         s0[j] = (own0 && tc + 8 * j < np && p <= pp0) ? s0[j] * a.scale : -INFINITY;
         s1[j] = (own1 && tc + 8 * j < np && p <= pp1) ? s1[j] * a.scale : -INFINITY;
@@ -577,7 +609,7 @@ __global__ void __launch_bounds__(kPThreads, 2) attn_prefill_kernel(const AttnAr
       const float al1 = (mn1 == -INFINITY || m1 == -INFINITY) ? (m1 == -INFINITY ? 0.f : 1.f) : expf(m1 - mn1);
       float ls0 = 0.f, ls1 = 0.f;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
+      for (int j = 0; j < kPT / 8; ++j) {
         const float e0 = s0[j] == -INFINITY ? 0.f : expf(s0[j] - mn0);
         const float e1 = s1[j] == -INFINITY ? 0.f : expf(s1[j] - mn1);
         pr[r0 * S::SROW + tc + 8 * j] = e0;
@@ -595,20 +627,21 @@ __global__ void __launch_bounds__(kPThreads, 2) attn_prefill_kernel(const AttnAr
       m0 = mn0;
       m1 = mn1;
       __syncwarp();  // the row's 8 lanes are in this warp: their probabilities are written
-      // o += P V for dims tc + 8 k
 #pragma unroll
-      for (int k = 0; k < D / 8; ++k) {
-        o0[k] *= al0;
-        o1[k] *= al1;
+      for (int m = 0; m < NM; ++m) {
+        o0[m].x *= al0; o0[m].y *= al0; o0[m].z *= al0; o0[m].w *= al0;
+        o1[m].x *= al1; o1[m].y *= al1; o1[m].z *= al1; o1[m].w *= al1;
       }
       for (int p = 0; p < np; ++p) {
         const float w0 = pr[r0 * S::SROW + p], w1 = pr[r1 * S::SROW + p];
-        const __half* vr = vs + p * S::KROW;
+        const float* vr = vf + p * S::QROW + 4 * tc;
 #pragma unroll
-        for (int k = 0; k < D / 8; ++k) {
-          const float v = __half2float(vr[tc + 8 * k]);
-          o0[k] = fmaf(w0, v, o0[k]);
-          o1[k] = fmaf(w1, v, o1[k]);
+        for (int m = 0; m < NM; ++m) {
+          const float4 v = *reinterpret_cast<const float4*>(vr + 32 * m);
+          o0[m].x = fmaf(w0, v.x, o0[m].x); o0[m].y = fmaf(w0, v.y, o0[m].y);
+          o0[m].z = fmaf(w0, v.z, o0[m].z); o0[m].w = fmaf(w0, v.w, o0[m].w);
+          o1[m].x = fmaf(w1, v.x, o1[m].x); o1[m].y = fmaf(w1, v.y, o1[m].y);
+          o1[m].z = fmaf(w1, v.z, o1[m].z); o1[m].w = fmaf(w1, v.w, o1[m].w);
         }
       }
     }
@@ -616,16 +649,18 @@ __global__ void __launch_bounds__(kPThreads, 2) attn_prefill_kernel(const AttnAr
   // normalise and store
   const int ta = t0 + r0 / G, tb = t0 + r1 / G;
   if (sq0 >= 0 && ta < a.ntok) {
-    float* out = a.out + ((size_t)ta * a.Hq + (size_t)kvh * G + r0 % G) * D;
+    float* out = a.out + ((size_t)ta * a.Hq + (size_t)kvh * G + r0 % G) * D + 4 * tc;
     const float inv = 1.0f / l0;
 #pragma unroll
-    for (int k = 0; k < D / 8; ++k) out[tc + 8 * k] = o0[k] * inv;
+    for (int m = 0; m < NM; ++m)
+      *reinterpret_cast<float4*>(out + 32 * m) = make_float4(o0[m].x * inv, o0[m].y * inv, o0[m].z * inv, o0[m].w * inv);
   }
   if (sq1 >= 0 && tb < a.ntok) {
-    float* out = a.out + ((size_t)tb * a.Hq + (size_t)kvh * G + r1 % G) * D;
+    float* out = a.out + ((size_t)tb * a.Hq + (size_t)kvh * G + r1 % G) * D + 4 * tc;
     const float inv = 1.0f / l1;
 #pragma unroll
-    for (int k = 0; k < D / 8; ++k) out[tc + 8 * k] = o1[k] * inv;
+    for (int m = 0; m < NM; ++m)
+      *reinterpret_cast<float4*>(out + 32 * m) = make_float4(o1[m].x * inv, o1[m].y * inv, o1[m].z * inv, o1[m].w * inv);
   }
 }
 
