@@ -53,6 +53,36 @@ PREFILL = dict(seqs=4, prompt=512, min_tokens=64,
 TRAFFIC = {1: 3_903_004_672}
 
 
+def dist_env():
+    """(rank, world size, local rank) from the launcher's environment (1 process by default)."""
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def init_dist(world, backend):
+    """The process group of a multi-replica run (None for one process)."""
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+    dist.init_process_group(backend)
+    return dist
+
+
+def max_over_ranks(x, dist, device=None):
+    """The maximum of x over all ranks: a replica run is as slow as its slowest replica."""
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_rate(units_per_rank, seconds, world):
+    """Whole-job throughput: every rank processed units_per_rank in at most `seconds`."""
+    return units_per_rank * world / seconds
+
+
 def measured_peaks():
     try:
         return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
@@ -177,14 +207,9 @@ def run_gpu(args):
     import torch
     import layer_range_stage_gb300 as L  # noqa: F401
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    rank, world, local = dist_env()
     torch.cuda.set_device(local)
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl")
+    dist = init_dist(world, "nccl")  # replicas only: the process group carries timing, no data
     wl = WORKLOADS[args.config]
     model = synth.CONFIGS[args.config]
     bounds = wl["bounds"]
@@ -224,16 +249,13 @@ def run_gpu(args):
     e1.record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop()
-    ms = e0.elapsed_time(e1)
+    ms = max_over_ranks(e0.elapsed_time(e1), dist, "cuda")
     if dist:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
         dist.barrier()
     ctx_mid = context + warmup + steps / 2
     w_bytes, kv_bytes = bytes_per_token(model, ctx_mid)
     ms_step = ms / steps
-    tok_s = world * 1000.0 / ms_step
+    tok_s = aggregate_rate(steps, ms * 1e-3, world)
     gbs = (w_bytes + kv_bytes) / (ms_step * 1e-3) / 1e9
 
     # the dominant kernel timed with CUDA events recorded around each of its launches inside
@@ -312,12 +334,14 @@ def run_gpu(args):
         dist.destroy_process_group()
 
 
-def cpu_baseline(args, budget_s=12.0):
+def cpu_baseline(args, budget_s=None):
     """The oracle as it stands, on a bounded sample: decode tokens through 2 of the 32
     blocks at context 2048 (KV filled with seeded fp16 values; the oracle's time does not
     depend on their values), repeated at successive positions until about budget_s seconds
     have passed, plus one readout; the mean block time is scaled to the 32-block token."""
     import oracle
+    if budget_s is None:
+        budget_s = getattr(args, "cpu_budget", 12.0)
     model = synth.CONFIGS[CFG_ID]
     n_blk = 2
     cores = os.cpu_count()
@@ -344,12 +368,14 @@ def cpu_baseline(args, budget_s=12.0):
 
 
 def run_reference(args):
-    rank = int(os.environ.get("RANK", "0"))
+    """The reference arm: the oracle on the host cores; under a multi-process launch rank 0
+    alone runs it and prints, the other ranks leave without work."""
+    rank, world, _ = dist_env()
     if rank != 0:
         return
     cb = cpu_baseline(args)
     line = {"impl": "reference", "metric": "decode tok/s",
-            "value": cb["value"], "unit": "tok/s", "n_gpus": int(os.environ.get("WORLD_SIZE", "1")),
+            "value": cb["value"], "unit": "tok/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": WORKLOADS[1]["name"]},
@@ -368,6 +394,7 @@ def main():
     ap.add_argument("--layers", type=int, default=0, help="reduced depth, for profiling small cases only")
     ap.add_argument("--context", type=int, default=0, help="decode context (default: the workload's)")
     ap.add_argument("--config", type=int, default=1, choices=sorted(WORKLOADS), help="1: dense 8B-shape, 2: MoE")
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work in the CPU baseline")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
