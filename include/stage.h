@@ -187,6 +187,16 @@ STAGE_API int stage_committed_len(stage_t st, int seq_id, int* len_out);
  * Synchronises the stage's stream.  For inspection and equivalence checks. */
 STAGE_API int stage_read_kv(stage_t st, int global_layer, int seq_id, int n_pos, uint16_t* k_host, uint16_t* v_host);
 
+/* Copy K and V rows from the host into the cache of one owned block and sequence:
+ * positions [pos0, pos0 + n_pos) of every KV head, fp16 bit patterns, each
+ * [n_kv_heads x n_pos x head_dim] (the layout stage_read_kv returns).  For restoring a cache
+ * saved with stage_read_kv, or for starting from a given cache.  pos0 may not leave a gap
+ * after the positions already written (STAGE_E_POSITION); the rows count as written, so a
+ * following stage_commit of the sequence up to pos0 + n_pos publishes them, jointly with
+ * the other stages.  Synchronises the stage's stream. */
+STAGE_API int stage_write_kv(stage_t st, int global_layer, int seq_id, int pos0, int n_pos, const uint16_t* k_host,
+                             const uint16_t* v_host);
+
 /* Which path a call with n_tokens tokens takes: 0 = float32 dequant-fused GEMV kernels,
  * 1 = bf16 tensor-core GEMMs, 2 = float32 persistent decode (a single-token call on a dense
  * stage: every block of the stage in one cooperative launch; same arithmetic per weight as

@@ -82,6 +82,7 @@ _SIGS = {
     "stage_committed_len": (C.c_int, [C.c_void_p, C.c_int, C.POINTER(C.c_int)]),
     "stage_gemm_mode": (C.c_int, [C.c_void_p, C.c_int, C.POINTER(C.c_int)]),
     "stage_read_kv": (C.c_int, [C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_void_p, C.c_void_p]),
+    "stage_write_kv": (C.c_int, [C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_int, C.c_void_p, C.c_void_p]),
     "stage_last_error": (C.c_char_p, [C.c_void_p]),
     "stage_create_error": (C.c_char_p, []),
     "stage_destroy": (None, [C.c_void_p]),
@@ -304,6 +305,16 @@ def stage_read_kv(st, global_layer: int, seq_id: int, n_pos: int, n_kv_heads: in
     v = np.zeros_like(k)
     _check(st, lib().stage_read_kv(st, global_layer, seq_id, n_pos, _ptr(k), _ptr(v)))
     return k.view(np.float16), v.view(np.float16)
+
+
+def stage_write_kv(st, global_layer: int, seq_id: int, pos0: int, k, v) -> None:
+    """Write (K, V) float16 [n_kv_heads, n_pos, head_dim] at positions pos0.. of one owned
+    block and sequence."""
+    k = np.ascontiguousarray(np.asarray(k, dtype=np.float16)).view(np.uint16)
+    v = np.ascontiguousarray(np.asarray(v, dtype=np.float16)).view(np.uint16)
+    if k.shape != v.shape or k.ndim != 3:
+        raise ValueError("k and v must both be [n_kv_heads, n_pos, head_dim]")
+    _check(st, lib().stage_write_kv(st, global_layer, seq_id, pos0, k.shape[1], _ptr(k), _ptr(v)))
 
 
 def stage_gemm_mode(st, n_tokens: int) -> int:

@@ -1041,6 +1041,33 @@ int stage_read_kv(stage_t st, int global_layer, int seq_id, int n_pos, uint16_t*
   return e == cudaSuccess ? check_device_error(st) : cuda_err(st, e, "read kv");
 }
 
+int stage_write_kv(stage_t st, int global_layer, int seq_id, int pos0, int n_pos, const uint16_t* k_host,
+                   const uint16_t* v_host) {
+  if (!st) return STAGE_E_INVALID;
+  BusyGuard g(st);
+  if (!g.ok) return set_err(st, STAGE_E_BUSY, "another call is in progress");
+  const stage_model_cfg& c = st->cfg;
+  if (global_layer < st->begin || global_layer >= st->end || seq_id < 0 || seq_id >= c.max_seqs || pos0 < 0 ||
+      n_pos < 0 || !k_host || !v_host)
+    return set_err(st, STAGE_E_INVALID, "bad KV write arguments");
+  if ((long long)pos0 + n_pos > c.max_seq_len)
+    return set_err(st, STAGE_E_POSITION, "positions [%d, %d) pass max_seq_len %d", pos0, pos0 + n_pos, c.max_seq_len);
+  if (pos0 > st->pending[seq_id])
+    return set_err(st, STAGE_E_POSITION, "write at %d leaves a gap after position %d", pos0, st->pending[seq_id]);
+  cudaError_t e = cudaStreamSynchronize(st->stream);
+  const size_t row = (size_t)c.head_dim;
+  for (int h = 0; e == cudaSuccess && h < c.n_kv_heads; ++h) {
+    const size_t off = (size_t)(global_layer - st->begin) * st->layer_kv +
+                       (((size_t)seq_id * c.n_kv_heads + h) * c.max_seq_len + pos0) * row;
+    e = cudaMemcpy(st->kc + off, k_host + (size_t)h * n_pos * row, (size_t)n_pos * row * 2, cudaMemcpyHostToDevice);
+    if (e == cudaSuccess)
+      e = cudaMemcpy(st->vc + off, v_host + (size_t)h * n_pos * row, (size_t)n_pos * row * 2, cudaMemcpyHostToDevice);
+  }
+  if (e != cudaSuccess) return cuda_err(st, e, "write kv");
+  st->pending[seq_id] = std::max(st->pending[seq_id], pos0 + n_pos);
+  return STAGE_OK;
+}
+
 int stage_gemm_mode(stage_t st, int n_tokens, int* mode_out) {
   if (!st || !mode_out) return STAGE_E_INVALID;
   *mode_out = use_tc(st, n_tokens) ? 1 : (n_tokens == 1 && st->mega) ? 2 : 0;

@@ -1,0 +1,114 @@
+"""The 70B-shape batched decode at full width against the oracle, through the C ABI.
+
+Hidden 8192, 64 q / 8 kv heads x 128, SwiGLU 28672, vocab 128256, int8 block-32 weights;
+64 sequences whose KV lengths are uniform in [128, 4096]; 4 stages chained, one block each
+(the model's depth is reduced to 4 blocks: every block has the same shapes).  The caches
+start from seeded fp16 N(0, 1) rows written through stage_write_kv (and into the oracle's
+caches; every block gets the same rows), then one decode step of 64 tokens -- one per
+sequence, at its own position -- runs through the 4 stages.  The first and the last stage
+are checked against the oracle's block fed the GPU's own input (relative L2 <= 1e-3, the
+float32 tolerance; the last stage's input is the handoff of the two middle stages); the
+readout against the oracle's on
+sampled vocabulary rows (max-abs <= 2e-2) and the greedy tokens against the oracle's full
+argmax wherever its top-2 margin exceeds that tolerance.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+HIDDEN_RTOL = 1e-3
+LOGIT_ATOL = 2e-2
+NSEQ = 64
+
+
+def rel_l2(a, b):
+    a, b = np.asarray(a, np.float64), np.asarray(b, np.float64)
+    return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-30))
+
+
+def kv_rows(model, seq, n):
+    """Seeded fp16 K and V rows [Hkv, n, D] of one sequence."""
+    shape = (model.n_kv_heads, n, model.head_dim)
+    size = model.n_kv_heads * n * model.head_dim
+    k = synth.normal_f32(synth.key(4400, seq, 0), 0, size, 1.0).reshape(shape).astype(np.float16)
+    v = synth.normal_f32(synth.key(4400, seq, 1), 0, size, 1.0).reshape(shape).astype(np.float16)
+    return k, v
+
+
+def test_70b_shape_batched_decode_ragged_64(cuda):
+    from layer_range_stage_gb300 import binding as B
+    model = synth.reduced(synth.CONFIGS[4], 4)
+    lens = np.random.default_rng(4401).integers(128, 4097, NSEQ)
+    max_len = int(lens.max()) + 1
+    cfgc = B.make_cfg(model, NSEQ, max_len, NSEQ)
+    seqs = np.arange(NSEQ)
+    toks = np.random.default_rng(4402).integers(0, model.vocab, NSEQ)
+    stages, ws = [], [synth.stage_weights(model, li, li + 1) for li in range(4)]
+    kv = [kv_rows(model, s, int(lens[s])) for s in range(NSEQ)]
+    try:
+        hs = []
+        for li in range(4):
+            st = B.stage_create(cfgc, li, li + 1, ws[li])
+            stages.append(st)
+            for s in range(NSEQ):
+                B.stage_write_kv(st, li, s, 0, kv[s][0], kv[s][1])
+            B.stage_commit(st, seqs, lens)
+            h = torch.empty((NSEQ, model.hidden), dtype=torch.float32, device="cuda")
+            if li == 0:
+                B.stage_decode(st, seqs, lens, tokens=toks, hidden_out=h)
+            else:
+                B.stage_decode(st, seqs, lens, hidden_in=hs[-1], hidden_out=h)
+            hs.append(h)
+        lg = torch.empty((NSEQ, model.vocab), dtype=torch.float32, device="cuda")
+        am = torch.empty((NSEQ,), dtype=torch.int32, device="cuda")
+        B.stage_logits(stages[-1], np.arange(NSEQ), lg, am)
+        torch.cuda.synchronize()
+        hg = [h.cpu().numpy() for h in hs]
+        logits, argmax = lg.cpu().numpy(), am.cpu().numpy()
+    finally:
+        for st in stages:
+            B.stage_destroy(st)
+
+    # the oracle on the first and the last stage, each fed the GPU's input to that stage
+    for li in (0, 3):
+        w = ws[li]
+        ost = oracle.Stage(model, li, li + 1, w, max_seqs=NSEQ, max_len=max_len, cache_dequant=False)
+        for s in range(NSEQ):
+            ost.k_cache[0, s, :, :lens[s]] = kv[s][0]
+            ost.v_cache[0, s, :, :lens[s]] = kv[s][1]
+        if li == 0:
+            ref = ost.forward(seqs, lens, tokens=toks)
+        else:
+            ref = ost.forward(seqs, lens, hidden_in=hg[li - 1])
+        assert rel_l2(hg[li], ref) <= HIDDEN_RTOL, li
+        if li == 3:
+            head = w.lm_head
+            feats = hg[3].astype(np.float64)  # the readout of the GPU's own features
+            rng = np.random.default_rng(4403)
+            sample = np.unique(np.concatenate([rng.integers(0, model.vocab, 512), argmax]))
+            lo = oracle.matvec(oracle.dequant(head.q[sample], head.s[sample]), feats)
+            assert np.abs(logits[:, sample] - lo).max() <= LOGIT_ATOL
+            # full argmax of the oracle, in chunks of vocabulary rows
+            best = np.full(NSEQ, -np.inf)
+            second = np.full(NSEQ, -np.inf)
+            arg = np.zeros(NSEQ, dtype=np.int64)
+            for r0 in range(0, model.vocab, 8192):
+                r1 = min(model.vocab, r0 + 8192)
+                chunk = oracle.matvec(oracle.dequant(head.q[r0:r1], head.s[r0:r1]), feats)
+                for t in range(NSEQ):
+                    c = chunk[t]
+                    j = int(np.argmax(c))
+                    top2 = np.sort(c)[-2:]
+                    if c[j] > best[t]:
+                        second[t] = max(best[t], top2[0])
+                        best[t], arg[t] = c[j], r0 + j
+                    else:
+                        second[t] = max(second[t], c[j])
+            for t in range(NSEQ):
+                if best[t] - second[t] > 2 * LOGIT_ATOL:
+                    assert argmax[t] == arg[t], t
