@@ -1,0 +1,74 @@
+"""The dense 8B-shape model at full depth (32 blocks) in the benchmark's configuration --
+2 stages of 16 blocks, single-token decode on the persistent kernel -- against the oracle,
+and staged against unstaged.
+
+A 64-token prompt, then 4 greedy decode steps.  Feeding the GPU's greedy tokens back, the
+5 steps are one causal pass over 68 positions, so the oracle computes them block by block
+in a single pass (each block's weights dequantised once).  Tolerances as for the float32
+path: logits max-abs <= 2e-2 at every step, final features relative L2 <= 1e-3, greedy
+tokens identical wherever the oracle's top-2 margin exceeds the logit tolerance; the
+unstaged GPU run equals the staged one bit for bit.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+LOGIT_ATOL = 2e-2
+HIDDEN_RTOL = 1e-3
+
+
+def rel_l2(a, b):
+    a, b = np.asarray(a, np.float64), np.asarray(b, np.float64)
+    return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-30))
+
+
+def gpu_run(model, bounds, prompt, n_new):
+    import layer_range_stage_gb300 as L
+    from layer_range_stage_gb300.pipeline import StagePipeline
+    with StagePipeline(model, bounds, lambda l: synth.layer_weights(model, l),
+                       lambda a, b: synth.stage_weights(model, a, b, with_layers=False),
+                       max_seq_len=128, max_tokens=64) as gp:
+        assert L.stage_gemm_mode(gp.stages[-1], 1) == 2
+        n = len(prompt)
+        lg = torch.empty((1, model.vocab), dtype=torch.float32, device="cuda")
+        tok = gp.step(True, np.zeros(n), np.arange(n), prompt, rows=[n - 1], logits_out=lg)
+        toks, logits = [int(tok[0])], [lg.cpu().numpy().copy()]
+        for t in range(n_new):
+            tok = gp.step(False, [0], [n + t], [toks[-1]], rows=[0], logits_out=lg)
+            toks.append(int(tok[0]))
+            logits.append(lg.cpu().numpy().copy())
+        k, v = L.stage_read_kv(gp.stages[-1], model.n_layers - 1, 0, n + n_new, model.n_kv_heads, model.head_dim)
+    return toks, logits, (k.view(np.uint16).copy(), v.view(np.uint16).copy())
+
+
+def test_dense_8b_full_depth_matches_oracle_and_unstaged(cuda):
+    model = synth.CONFIGS[1]
+    prompt = synth.prompt_tokens(model, 9, 64)
+    n, n_new = len(prompt), 4
+    toks, logits, kv = gpu_run(model, [0, 16, 32], prompt, n_new)
+    toks1, logits1, kv1 = gpu_run(model, [0, 32], prompt, n_new)
+    assert toks1 == toks
+    for a, b in zip(logits1, logits):
+        assert np.array_equal(a, b)
+    assert np.array_equal(kv1[0], kv[0]) and np.array_equal(kv1[1], kv[1])
+
+    # oracle: the prompt and the GPU's greedy tokens as one causal pass of 68 positions
+    ids = np.concatenate([prompt, np.array(toks[:n_new])])
+    m = len(ids)
+    seq, pos = np.zeros(m, dtype=np.int64), np.arange(m)
+    x = None
+    for l in range(model.n_layers):
+        st = oracle.Stage(model, l, l + 1, synth.stage_weights(model, l, l + 1), max_seqs=1, max_len=128,
+                          cache_dequant=False)
+        x = st.forward(seq, pos, tokens=ids) if l == 0 else st.forward(seq, pos, hidden_in=x)
+    lo = st.logits(np.arange(n - 1, m))  # the last prompt token, then every decode step
+    for t in range(n_new + 1):
+        assert np.abs(logits[t][0] - lo[t]).max() <= LOGIT_ATOL, t
+        top2 = np.sort(lo[t])[-2:]
+        if top2[1] - top2[0] > 2 * LOGIT_ATOL:
+            assert toks[t] == int(np.argmax(lo[t])), t
