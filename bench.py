@@ -261,8 +261,8 @@ def run_gpu(args):
     # the dominant kernel timed with CUDA events recorded around each of its launches inside
     # a second run of the same graph-replayed steps (events between kernels cost overlap, so
     # the headline number above comes from the run without them): on dense stages the
-    # persistent decode kernel (one launch per stage per token), on MoE stages the expert
-    # gate/up GEMV
+    # persistent decode kernel (one launch per stage per token; the mean over the stages'
+    # launches)
     gp.kernel_timing(True)
     nxt = gp.generate([0], last, 4, use_graph=True)[-1]
     torch.cuda.synchronize()
@@ -290,15 +290,17 @@ def run_gpu(args):
     peaks = measured_peaks()
     peak = peaks.get("hbm_gbs")
     H = model.hidden
-    if model.is_moe:
-        kernel = "expert gate/up GEMV (gathered rows + RMSNorm prologue + SwiGLU epilogue)"
-        k_bytes = model.top_k * 2 * model.expert_ffn * H * 1.0625 + H * 4  # weights + scales once, input row
+    blocks = model.n_layers / (len(bounds) - 1)  # mean blocks per launch
+    per_block = (model.q_dim + 2 * model.kv_dim) * H + H * model.q_dim
+    if model.is_moe:  # the router once, the selected experts' gate/up and down rows
+        kernel = (f"persistent decode of one stage (blocks {'/'.join(str(b - a) for a, b in zip(bounds, bounds[1:]))}: "
+                  "QKV, attention, O, router + top-k, gathered expert gate/up, gathered expert down)")
+        per_block += model.n_experts * H + model.top_k * 3 * model.expert_ffn * H
     else:
         kernel = "persistent decode of one stage (16 blocks: QKV, attention, O, gate/up, down)"
-        blocks = bounds[1] - bounds[0]
-        per_block = ((model.q_dim + 2 * model.kv_dim) * H + H * model.q_dim + 3 * model.ffn * H) * 1.0625
-        kv_block = 2 * model.n_kv_heads * (context + warmup + steps + 2) * model.head_dim * 2
-        k_bytes = blocks * (per_block + kv_block)
+        per_block += 3 * model.ffn * H
+    kv_block = 2 * model.n_kv_heads * (context + warmup + steps + 2) * model.head_dim * 2
+    k_bytes = blocks * (per_block * 1.0625 + kv_block)
     k_gbs = k_bytes / (k_us * 1e-6) / 1e9 if k_us else None
     line = {
         "metric": "decode tok/s",
@@ -321,7 +323,7 @@ def run_gpu(args):
         "e2e": e2e,
         "prefill": prefill,
         "clocks": clk,
-        "gpu_launches": steps * ((1 + model.n_layers * 7 + 4) if model.is_moe else (1 + (len(bounds) - 1) + 4)),
+        "gpu_launches": steps * (1 + (len(bounds) - 1) + 4),
         "build_s": round(build_s, 1),
     }
     if args.layers or args.context:

@@ -198,9 +198,10 @@ STAGE_API int stage_write_kv(stage_t st, int global_layer, int seq_id, int pos0,
                              const uint16_t* v_host);
 
 /* Which path a call with n_tokens tokens takes: 0 = float32 dequant-fused GEMV kernels,
- * 1 = bf16 tensor-core GEMMs, 2 = float32 persistent decode (a single-token call on a dense
- * stage: every block of the stage in one cooperative launch; same arithmetic per weight as
- * 0, its own fixed summation order).  The environment variable LRS_PERSISTENT=0, read at
+ * 1 = bf16 tensor-core GEMMs (dense stages), 2 = float32 persistent decode (a single-token
+ * call: every block of the stage in one cooperative launch, on MoE stages with the router
+ * and top-k computed inside it; same arithmetic per weight as 0, its own fixed summation
+ * order).  The environment variable LRS_PERSISTENT=0, read at
  * stage_create, turns mode 2 off. */
 STAGE_API int stage_gemm_mode(stage_t st, int n_tokens, int* mode_out);
 

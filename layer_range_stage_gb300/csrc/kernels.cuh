@@ -118,7 +118,8 @@ cudaError_t launch_rows_to_bf16(const float* x, int ld_in, int K, const float* g
 // epilogue), down GEMV + residual.  Weight rows stream through a per-warp ring of bulk
 // copies that runs ahead across phases and blocks.
 struct MegaLayer {
-  DevQ8 wqkv, wo, wgu, wdown;
+  DevQ8 wqkv, wo, wgu, wdown;  // dense FFN (wgu, wdown) ...
+  DevQ8 router, egu, edown;    // ... or routed experts (stacked as in the stage's layout)
   const float* attn_norm = nullptr;
   const float* ffn_norm = nullptr;
   __half* kc = nullptr;  // [max_seqs][Hkv][max_len][D] of this block
@@ -139,13 +140,15 @@ struct MegaArgs {
   const int* pos = nullptr;    // device [1]
   const float2* rope = nullptr;
   int H = 0, Hq = 0, Hkv = 0, D = 0, F = 0, max_len = 0, n_chunks = 1;
+  int n_experts = 0, top_k = 0, EF = 0;  // MoE stages: experts, selected per token, expert FFN width
   float eps = 1e-5f, scale = 1.f;
   unsigned* bar = nullptr;  // [64]: grid barrier counter, exit counter, per-KV-head attention
                             // counters; zero between launches (the last CTA out re-zeroes)
   int* err = nullptr;
 };
-// Whether the persistent decode covers this shape (and the shared memory it needs fits).
-bool mega_supported(int H, int q_dim, int F, int head_dim, int group);
+// Whether the persistent decode covers this shape (and the shared memory it needs fits).  MoE:
+// n_experts > 0, F = top_k * expert FFN width (the gathered down input).
+bool mega_supported(int H, int q_dim, int F, int head_dim, int group, int n_experts = 0, int top_k = 0);
 // Attention chunks per KV head used by the persistent decode (about one item per SM).
 int mega_chunks(int n_kv_heads);
 cudaError_t launch_mega_decode(const MegaArgs& a, cudaStream_t st);

@@ -22,6 +22,12 @@
 // the matrix.  A warp sums its pieces in order and reduces with shuffles: every output has
 // one fixed summation order.
 //
+// MoE stages: after the O projection every CTA computes the router itself (logits of all
+// experts from the normalised residual, top-k with ties to the lower id, softmax over the
+// selected) -- the same arithmetic on the same data, so every CTA picks the same experts --
+// and the gate/up and down slices of the selected experts stream in once it is known
+// (the weight stream pauses there: those slices depend on the routing).
+//
 // Grid barrier: a counter that only grows within a launch (release add, acquire polling,
 // bounded by time) and is reset by the last CTA to leave.  Every wait is bounded; a CTA
 // that runs out of time sets the error word, waits (bounded) for its own copies in flight
@@ -54,7 +60,10 @@ constexpr size_t kOffRingQ = 0;
 constexpr size_t kOffRingS = kOffRingQ + (size_t)kMW * kDepth * kSlotQ;
 constexpr size_t kOffBars = kOffRingS + (size_t)kMW * kDepth * kSlotS;  // kMW*kDepth slot barriers + 1
 constexpr size_t kOffRed = kOffBars + 512;                               // 32 floats + flags
-constexpr size_t kOffXraw = kOffRed + 512;                                // [Kp(H)] floats
+constexpr size_t kOffMoe = kOffRed + 512;                                 // routing (MoE stages)
+constexpr int kMaxExperts = 256, kMaxTopK = 32;
+constexpr size_t kOffShapes = kOffMoe + (kMaxExperts + 4 * kMaxTopK + 4) * 4;  // [4] projection shapes
+constexpr size_t kOffXraw = kOffMoe + 2048;                               // [Kp(H)] floats
 
 __host__ __device__ constexpr int pad256(int k) { return (k + 255) / 256 * 256; }
 
@@ -75,26 +84,6 @@ struct AttnLayout {
   static_assert((size_t)(G * D + 64) * 4 <= (size_t)2 * T * D * 2, "merge slice scratch over the K/V tiles");
 };
 
-struct Ph {  // one projection of a block as the weight stream sees it
-  const uint8_t* q;
-  const uint16_t* s;
-  int N, Kp, R, P, PS;
-};
-
-__device__ __forceinline__ Ph phase_of(const MegaArgs& a, int l, int ph) {
-  const MegaLayer& L = a.layers[l];
-  const DevQ8& w = ph == 0 ? L.wqkv : ph == 1 ? L.wo : ph == 2 ? L.wgu : L.wdown;
-  Ph p;
-  p.q = w.q;
-  p.s = w.s;
-  p.N = w.N;
-  p.Kp = w.Kp;
-  p.R = (ph == 0 || ph == 2) ? 2 : 1;
-  p.P = (w.Kp + kSlotQ - 1) / kSlotQ;
-  p.PS = ((w.Kp / p.P + 255) / 256) * 256;
-  return p;
-}
-
 __device__ __forceinline__ void red_release_add(unsigned* p, unsigned v) {
   asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
@@ -111,8 +100,24 @@ struct Stream {
   int issued, consumed;
 };
 
+// One projection's shape as the weight stream sees it: the same in every block of a stage.
+struct Shape {
+  int N, Kp;          // rows (of the projection as computed); row stride in bytes (scales: Kp / 32)
+  int T;              // tasks: N / R
+  int klen;           // bytes of a row's K range
+  int R, P, PS;       // rows per task, pieces per row, piece bytes
+  int B;              // pieces per ring slot (several whole pieces share a slot)
+  int mode;           // 0 plain rows; 1 rows of the selected experts (rps rows each); 2 piece j of a
+                      // row from selected expert j (K gathered over the experts)
+  int rps;
+};
+
 struct Ctx {
   const MegaArgs* a;
+  const Shape* shape;          // [4] in shared memory
+  const int* moe_ids;          // [top_k] experts of the current block (MoE stages)
+  const float* moe_wts;        // [top_k] their routing weights
+  volatile int* moe_ready;     // last block whose routing is known
   unsigned char* ringq;
   unsigned char* rings;
   uint64_t* bars;   // [kMW][kDepth] slot barriers, then the attention barrier
@@ -121,10 +126,92 @@ struct Ctx {
   int lane, warp, gw, GW;
 };
 
+// ph: 0 QKV, 1 O, 2 gate/up (dense, or the selected experts'), 3 down (dense, or gathered).
+// Computed once per launch (from block 0: every block has the same shapes).
+__device__ Shape shape_of(const MegaArgs& a, int ph) {
+  const MegaLayer& L = a.layers[0];
+  Shape p;
+  p.mode = 0;
+  p.rps = 0;
+  const DevQ8* w;
+  if (a.n_experts > 0 && ph >= 2) {
+    if (ph == 2) {
+      w = &L.egu;
+      p.N = a.top_k * 2 * a.EF;
+      p.mode = 1;
+      p.rps = 2 * a.EF;
+    } else {
+      w = &L.edown;
+      p.N = a.H;
+      p.mode = 2;
+    }
+  } else {
+    w = ph == 0 ? &L.wqkv : ph == 1 ? &L.wo : ph == 2 ? &L.wgu : &L.wdown;
+    p.N = w->N;
+  }
+  p.Kp = w->Kp;
+  p.R = (ph == 0 || ph == 2) ? 2 : 1;
+  p.T = p.N / p.R;
+  if (p.mode == 2) {
+    p.P = a.top_k;
+    p.PS = w->Kp;
+    p.klen = p.P * p.PS;
+  } else {
+    p.klen = w->Kp;
+    p.P = (w->Kp + kSlotQ - 1) / kSlotQ;
+    p.PS = ((w->Kp / p.P + 255) / 256) * 256;
+  }
+  p.B = (p.klen % p.PS == 0) ? max(1, kSlotQ / p.PS) : 1;
+  return p;
+}
+
+struct Ph : Shape {  // one projection of a block: its shape and its weights
+  const uint8_t* q;
+  const uint16_t* s;
+};
+
+__device__ __forceinline__ Ph phase_of(const Ctx& c, int l, int ph) {
+  const MegaLayer& L = c.a->layers[l];
+  const DevQ8& w = (c.a->n_experts > 0 && ph >= 2) ? (ph == 2 ? L.egu : L.edown)
+                   : ph == 0 ? L.wqkv : ph == 1 ? L.wo : ph == 2 ? L.wgu : L.wdown;
+  Ph p;
+  static_cast<Shape&>(p) = c.shape[ph];
+  p.q = w.q;
+  p.s = w.s;
+  return p;
+}
+
+// Row-in-task and piece of slot j of a task (R is 1 or 2, j < R * P).
+__device__ __forceinline__ void split_j(const Shape& p, int j, int& rr, int& pc) {
+  rr = j >= p.P;
+  pc = j - rr * p.P;
+}
+
+// Pieces of this warp's share of a phase from task t, piece j on, counted up to `cap`.
+__device__ __forceinline__ int pieces_upto(const Ctx& c, const Shape& p, int t, int j, int cap) {
+  int n = p.R * p.P - j;
+  for (int tt = t + c.GW; n < cap && tt < p.T; tt += c.GW) n += p.R * p.P;
+  return min(n, cap);
+}
+
+// Global addresses of piece (row, pc) of a phase.
+__device__ __forceinline__ void piece_src(const Ctx& c, const Ph& p, int row, int pc, const uint8_t*& q,
+                                          const uint16_t*& sc) {
+  if (p.mode == 2) {
+    const size_t r = (size_t)c.moe_ids[pc] * p.N + row;
+    q = p.q + r * p.PS;
+    sc = p.s + r * (p.PS / 32);
+    return;
+  }
+  size_t r = row;
+  if (p.mode == 1) r = (size_t)c.moe_ids[row / p.rps] * p.rps + row % p.rps;
+  q = p.q + r * p.Kp + (size_t)pc * p.PS;
+  sc = p.s + r * (p.Kp / 32) + (size_t)pc * p.PS / 32;
+}
+
 __device__ __forceinline__ void stream_normalise(const Ctx& c, Stream& s) {
   while (s.l < c.a->nl) {
-    const Ph p = phase_of(*c.a, s.l, s.ph);
-    if (s.t < p.N / p.R) return;
+    if (s.t < c.shape[s.ph].T) return;
     s.j = 0;
     s.t = c.gw;
     if (++s.ph == 4) {
@@ -143,25 +230,72 @@ __device__ __forceinline__ void stream_step(const Ctx& c, Stream& s, const Ph& p
   }
 }
 
-// Issue the next slot of this warp's stream (if any) into the ring.
+// Issue the next slot of this warp's stream (if any) into the ring: one piece, or up to B
+// whole pieces of the same phase.  Slices of the selected experts wait until the routing of
+// their block is known.
 __device__ __forceinline__ void stream_issue(const Ctx& c, Stream& s) {
   if (s.l >= c.a->nl) return;
-  const Ph p = phase_of(*c.a, s.l, s.ph);
-  const int rr = s.j / p.P, pc = s.j - rr * p.P;
-  const int row = s.t * p.R + rr;
-  const int off = pc * p.PS, bytes = min(p.PS, p.Kp - off);
+  if (c.a->n_experts > 0 && s.ph >= 2 && s.l > *c.moe_ready) return;
+  const Ph p = phase_of(c, s.l, s.ph);
+  if (p.B == 1 && p.mode == 0) {  // one piece of a plain row per slot
+    int rr, pc;
+    split_j(p, s.j, rr, pc);
+    const int row = s.t * p.R + rr;
+    const int off = pc * p.PS, bytes = min(p.PS, p.klen - off);
+    const int slot = s.issued % kDepth;
+    if (c.lane == 0) {
+      uint64_t* bar = c.bars + c.warp * kDepth + slot;
+      fence_async_smem();
+      mbar_arrive_expect_tx(bar, (uint32_t)(bytes + bytes / 16));
+      bulk_g2s(c.ringq + (size_t)(c.warp * kDepth + slot) * kSlotQ, p.q + (size_t)row * p.Kp + off, (uint32_t)bytes,
+               bar);
+      bulk_g2s(c.rings + (size_t)(c.warp * kDepth + slot) * kSlotS, p.s + (size_t)row * (p.Kp / 32) + off / 32,
+               (uint32_t)(bytes / 16), bar);
+    }
+    ++s.issued;
+    stream_step(c, s, p);
+    return;
+  }
+  const int nb = p.B == 1 ? 1 : pieces_upto(c, p, s.t, s.j, p.B);
   const int slot = s.issued % kDepth;
+  uint64_t* bar = c.bars + c.warp * kDepth + slot;
+  unsigned char* dq = c.ringq + (size_t)(c.warp * kDepth + slot) * kSlotQ;
+  unsigned char* ds = c.rings + (size_t)(c.warp * kDepth + slot) * kSlotS;
   if (c.lane == 0) {
-    uint64_t* bar = c.bars + c.warp * kDepth + slot;
     fence_async_smem();  // the slot's previous contents were read through the generic proxy
-    mbar_arrive_expect_tx(bar, (uint32_t)(bytes + bytes / 16));
-    bulk_g2s(c.ringq + (size_t)(c.warp * kDepth + slot) * kSlotQ, p.q + (size_t)row * p.Kp + off, (uint32_t)bytes,
-             bar);
-    bulk_g2s(c.rings + (size_t)(c.warp * kDepth + slot) * kSlotS, p.s + (size_t)row * (p.Kp / 32) + off / 32,
-             (uint32_t)(bytes / 16), bar);
+    int rr0, pc0;
+    split_j(p, s.j, rr0, pc0);
+    const int bytes0 = min(p.PS, p.klen - pc0 * p.PS);
+    mbar_arrive_expect_tx(bar, (uint32_t)(nb == 1 ? bytes0 + bytes0 / 16 : nb * (p.PS + p.PS / 16)));
+  }
+  for (int u = 0; u < nb; ++u) {
+    int rr, pc;
+    split_j(p, s.j, rr, pc);
+    const int row = s.t * p.R + rr;
+    const int bytes = min(p.PS, p.klen - pc * p.PS);
+    if (c.lane == 0) {
+      const uint8_t* q;
+      const uint16_t* sc;
+      piece_src(c, p, row, pc, q, sc);
+      bulk_g2s(dq + u * p.PS, q, (uint32_t)bytes, bar);
+      bulk_g2s(ds + u * (p.PS / 16), sc, (uint32_t)(bytes / 16), bar);
+    }
+    if (u + 1 < nb && ++s.j == p.R * p.P) {  // stays inside the phase: nb counted its pieces left
+      s.j = 0;
+      s.t += c.GW;
+    }
   }
   ++s.issued;
   stream_step(c, s, p);
+}
+
+// Top the ring up to kDepth slots (after the routing of a block became known).
+__device__ __forceinline__ void stream_refill(const Ctx& c, Stream& s) {
+  while (s.issued - s.consumed < kDepth && s.l < c.a->nl) {
+    const int before = s.issued;
+    stream_issue(c, s);
+    if (s.issued == before) break;
+  }
 }
 
 // After a failed wait: wait (bounded) for this warp's copies still in flight.
@@ -291,26 +425,35 @@ __device__ void stage_input(const Ctx& c, const float* x, int K, int Kp, const f
 
 // One projection of block l: consume this warp's tasks from the ring, refill behind.
 // Returns false (for the whole warp) after a timed-out wait (error set, copies drained);
-// the caller makes the outcome CTA-uniform.
-__device__ bool gemv_phase(const Ctx& c, Stream& s, int l, int ph, const float* xs, const float* xc,
-                           const float* xraw, int pos, int sid) {
+// the caller makes the outcome CTA-uniform.  BATCH: several pieces share a ring slot.
+template <bool BATCH>
+__device__ bool gemv_phase_t(const Ctx& c, Stream& s, int l, int ph, const float* xs, const float* xc,
+                             const float* xraw, int pos, int sid) {
   const MegaArgs& a = *c.a;
-  const Ph p = phase_of(a, l, ph);
-  const int T = p.N / p.R, nsl = p.R * p.P;
+  const Ph p = phase_of(c, l, ph);
+  const bool moe = a.n_experts > 0;
+  const int T = p.T, nsl = p.R * p.P;
+  int left = BATCH && c.gw < T ? ((T - 1 - c.gw) / c.GW + 1) * nsl : 0;  // this warp's pieces of the phase
+  int uin = 0, ucap = 1;  // position in, and pieces of, the current slot
   for (int t = c.gw; t < T; t += c.GW) {
     float acc0 = 0.f, acc1 = 0.f;
     for (int j = 0; j < nsl; ++j) {
-      const int rr = j / p.P, pc = j - rr * p.P;
-      const int off = pc * p.PS, bytes = min(p.PS, p.Kp - off);
+      int rr, pc;
+      split_j(p, j, rr, pc);
+      const int off = pc * p.PS, bytes = min(p.PS, p.klen - off);
       const int slot = s.consumed % kDepth;
-      const bool landed = mbar_wait(c.bars + c.warp * kDepth + slot, (unsigned)(s.consumed / kDepth) & 1u, kWaitNs);
-      if (!__all_sync(0xffffffffu, landed)) {  // warp-uniform decision
-        if (c.lane == 0) set_error(c);
-        stream_drain(c, s);
-        return false;
+      if (!BATCH || uin == 0) {
+        if (BATCH) ucap = min(p.B, left);
+        const bool landed = mbar_wait(c.bars + c.warp * kDepth + slot, (unsigned)(s.consumed / kDepth) & 1u, kWaitNs);
+        if (!__all_sync(0xffffffffu, landed)) {  // warp-uniform decision
+          if (c.lane == 0) set_error(c);
+          stream_drain(c, s);
+          return false;
+        }
       }
-      const unsigned char* sq = c.ringq + (size_t)(c.warp * kDepth + slot) * kSlotQ;
-      const unsigned char* ssc = c.rings + (size_t)(c.warp * kDepth + slot) * kSlotS;
+      const int u = BATCH ? uin : 0;
+      const unsigned char* sq = c.ringq + (size_t)(c.warp * kDepth + slot) * kSlotQ + u * p.PS;
+      const unsigned char* ssc = c.rings + (size_t)(c.warp * kDepth + slot) * kSlotS + u * (p.PS / 16);
       float acc = rr ? acc1 : acc0;
       const int nch = bytes >> 4, cb = off >> 4;
 #pragma unroll 2
@@ -327,9 +470,13 @@ __device__ bool gemv_phase(const Ctx& c, Stream& s, int l, int ph, const float* 
         acc1 = acc;
       else
         acc0 = acc;
-      __syncwarp();
-      ++s.consumed;
-      stream_issue(c, s);
+      if (BATCH) --left;
+      if (!BATCH || ++uin == ucap) {  // the slot is consumed: refill it
+        uin = 0;
+        __syncwarp();
+        ++s.consumed;
+        stream_issue(c, s);
+      }
     }
     acc0 = warp_sum(acc0);
     if (p.R == 2) acc1 = warp_sum(acc1);
@@ -359,12 +506,88 @@ __device__ bool gemv_phase(const Ctx& c, Stream& s, int l, int ph, const float* 
     } else if (ph == 1) {
       a.x1[t] = __fadd_rn(xraw[t], acc0);
     } else if (ph == 2) {
-      a.abuf[t] = silu(acc0) * acc1;
+      if (moe) {  // pair t: expert slot t / EF, unit t % EF; scaled by the routing weight
+        const int slot = t / a.EF, i = t - slot * a.EF;
+        a.abuf[(size_t)slot * pad256(a.EF) + i] = silu(acc0) * acc1 * c.moe_wts[slot];
+      } else {
+        a.abuf[t] = silu(acc0) * acc1;
+      }
     } else {
       a.hout[t] = __fadd_rn(xraw[t], acc0);
     }
   }
   return true;
+}
+
+__device__ bool gemv_phase(const Ctx& c, Stream& s, int l, int ph, const float* xs, const float* xc,
+                           const float* xraw, int pos, int sid) {
+  return c.shape[ph].B > 1 ? gemv_phase_t<true>(c, s, l, ph, xs, xc, xraw, pos, sid)
+                           : gemv_phase_t<false>(c, s, l, ph, xs, xc, xraw, pos, sid);
+}
+
+// The router of MoE block l, computed by every CTA from the staged normalised residual:
+// logits of all experts (same per-chunk arithmetic as the projections), the top_k by rank
+// (ties to the lower id), their softmax; ids, weights and the ready block into shared memory.
+__device__ void route(const Ctx& c, int l, const float* xs, const float* xc, float* logits, float* sel, int* sel_id,
+                      int* ids, float* wts) {
+  const MegaArgs& a = *c.a;
+  const DevQ8& r = a.layers[l].router;
+  const int E = a.n_experts, k = a.top_k, nchunk = r.Kp >> 4;
+  // warp w: experts w, w + 16, ... (up to 8 per pass); per chunk, the 8 experts' loads are
+  // issued together
+  constexpr int EPW = 8;
+  for (int e0 = c.warp; e0 < E; e0 += kMW * EPW) {
+    float acc[EPW];
+#pragma unroll
+    for (int i = 0; i < EPW; ++i) acc[i] = 0.f;
+    for (int ch = c.lane; ch < nchunk; ch += 32) {
+      const int sw = (ch >> 1) & 3;
+      const float4* xp = reinterpret_cast<const float4*>(xs + ch * 16);
+      const float4 x0 = xp[0 ^ sw], x1 = xp[1 ^ sw], x2 = xp[2 ^ sw], x3 = xp[3 ^ sw];
+      const float corr = -128.0f * xc[ch];
+      uint4 w[EPW];
+      uint16_t sc[EPW];
+#pragma unroll
+      for (int i = 0; i < EPW; ++i) {
+        const int e = min(e0 + i * kMW, E - 1);
+        w[i] = ld_stream_u4(r.q + (size_t)e * r.Kp + (size_t)ch * 16);
+        sc[i] = ld_stream_u16(r.s + (size_t)e * (r.Kp / 32) + (ch >> 1));
+      }
+#pragma unroll
+      for (int i = 0; i < EPW; ++i)
+        acc[i] = fmaf(h2f_bits(sc[i]), fmaf(dot16_u8(w[i], x0, x1, x2, x3), kPScale, corr), acc[i]);
+    }
+#pragma unroll
+    for (int i = 0; i < EPW; ++i) {
+      const float v = warp_sum(acc[i]);
+      if (c.lane == 0 && e0 + i * kMW < E) logits[e0 + i * kMW] = v;
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += kMT) {
+    const float v = logits[e];
+    int rank = 0;
+    for (int f = 0; f < E; ++f) {
+      const float u = logits[f];
+      rank += (u > v) || (u == v && f < e);
+    }
+    if (rank < k) {
+      sel[rank] = v;
+      sel_id[rank] = e;
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const float m = sel[0];
+    float z = 0.f;
+    for (int j = 0; j < k; ++j) z += expf(sel[j] - m);
+    for (int j = 0; j < k; ++j) {
+      ids[j] = sel_id[j];
+      wts[j] = expf(sel[j] - m) / z;
+    }
+    *c.moe_ready = l;
+  }
+  __syncthreads();
 }
 
 // Positions [c0, c1) of attention item `it` (KV head it % Hkv, chunk it / Hkv).
@@ -597,6 +820,17 @@ __global__ void __launch_bounds__(kMT, 1) mega_decode_kernel(const MegaArgs a) {
   c.bars = reinterpret_cast<uint64_t*>(sm + kOffBars);
   c.red = reinterpret_cast<float*>(sm + kOffRed);
   c.flag = reinterpret_cast<volatile int*>(sm + kOffRed + 256);
+  float* moe_logits = reinterpret_cast<float*>(sm + kOffMoe);  // [kMaxExperts]
+  int* moe_ids = reinterpret_cast<int*>(moe_logits + kMaxExperts);
+  float* moe_wts = reinterpret_cast<float*>(moe_ids + kMaxTopK);
+  float* moe_sel = moe_wts + kMaxTopK;
+  int* moe_sel_id = reinterpret_cast<int*>(moe_sel + kMaxTopK);
+  c.moe_ids = moe_ids;
+  c.moe_wts = moe_wts;
+  c.moe_ready = reinterpret_cast<volatile int*>(moe_sel_id + kMaxTopK);
+  static_assert(kOffShapes + 4 * sizeof(Shape) <= kOffXraw, "shapes");
+  Shape* shapes = reinterpret_cast<Shape*>(sm + kOffShapes);
+  c.shape = shapes;
   c.lane = threadIdx.x & 31;
   c.warp = threadIdx.x >> 5;
   c.gw = c.warp * gridDim.x + blockIdx.x;
@@ -612,7 +846,9 @@ __global__ void __launch_bounds__(kMT, 1) mega_decode_kernel(const MegaArgs a) {
   if (threadIdx.x == 0) {
     c.flag[0] = 0;
     c.flag[1] = 0;
+    *c.moe_ready = -1;
   }
+  if (threadIdx.x < 4) shapes[threadIdx.x] = shape_of(a, threadIdx.x);
   mbar_fence_init();
   __syncthreads();
   const int pos = __ldcg(a.pos), sid = __ldcg(a.seq);
@@ -629,49 +865,51 @@ __global__ void __launch_bounds__(kMT, 1) mega_decode_kernel(const MegaArgs a) {
 
   unsigned nbar = 0, aphase = 0;
   bool ok = true;
+  // one call site per step (the projection step is the same code for all four projections:
+  // the kernel stays small enough for the instruction cache)
   for (int l = 0; l < a.nl && ok; ++l) {
     const MegaLayer& L = a.layers[l];
-    // QKV (RMSNorm with gamma_1), RoPE, K/V append
-    stage_input(c, l == 0 ? a.hin : a.hout, a.H, KpH, L.attn_norm, a.eps, xs, xc, xraw);
-    ok = __syncthreads_and(gemv_phase(c, s, l, 0, xs, xc, xraw, pos, sid));
-    // tile 0 of this CTA's first attention item (positions of earlier steps) streams in
-    // while the grid meets
-    bool pre = false;
-    if (ok && (int)blockIdx.x < a.Hkv * a.n_chunks) {
-      int kvh, chunk, c0, c1;
-      item_range(a, blockIdx.x, pos, kvh, chunk, c0, c1);
-      if (c0 < c1) {
-        pre = true;
-        if (threadIdx.x == 0) {
-          const __half* kb = L.kc + ((size_t)sid * a.Hkv + kvh) * (size_t)a.max_len * D;
-          const __half* vb = L.vc + ((size_t)sid * a.Hkv + kvh) * (size_t)a.max_len * D;
-          const int np = min(AttnLayout<D, G>::T, c1 - c0);
-          attn_issue<D, G>(c, area, kb, vb, c0, max(0, min(np, pos - c0)));
-        }
+    for (int ph = 0; ph < 4 && ok; ++ph) {
+      // the projection's input: QKV and gate/up normalise the residual (gamma_1, gamma_2; the
+      // raw residual is kept for the residual adds), O and down take the attention output and
+      // the SwiGLU output as they are
+      const float* in = ph == 0 ? (l == 0 ? a.hin : a.hout) : ph == 1 ? a.obuf : ph == 2 ? a.x1 : a.abuf;
+      const int K = ph == 1 ? a.Hq * a.D : ph == 3 ? a.F : a.H;
+      const int Kp = ph == 1 ? KpQ : ph == 3 ? KpF : KpH;
+      const float* gamma = ph == 0 ? L.attn_norm : ph == 2 ? L.ffn_norm : nullptr;
+      stage_input(c, in, K, Kp, gamma, a.eps, xs, xc, (ph & 1) ? nullptr : xraw);
+      if (ph == 2 && a.n_experts > 0) {  // routing, then the selected experts' slices stream in
+        route(c, l, xs, xc, moe_logits, moe_sel, moe_sel_id, moe_ids, moe_wts);
+        stream_refill(c, s);
       }
+      ok = __syncthreads_and(gemv_phase(c, s, l, ph, xs, xc, xraw, pos, sid));
+      if (ph == 0) {
+        // tile 0 of this CTA's first attention item (positions of earlier steps) streams in
+        // while the grid meets
+        bool pre = false;
+        if (ok && (int)blockIdx.x < a.Hkv * a.n_chunks) {
+          int kvh, chunk, c0, c1;
+          item_range(a, blockIdx.x, pos, kvh, chunk, c0, c1);
+          if (c0 < c1) {
+            pre = true;
+            if (threadIdx.x == 0) {
+              const __half* kb = L.kc + ((size_t)sid * a.Hkv + kvh) * (size_t)a.max_len * D;
+              const __half* vb = L.vc + ((size_t)sid * a.Hkv + kvh) * (size_t)a.max_len * D;
+              const int np = min(AttnLayout<D, G>::T, c1 - c0);
+              attn_issue<D, G>(c, area, kb, vb, c0, max(0, min(np, pos - c0)));
+            }
+          }
+        }
+        if (ok) ok = grid_barrier(c, ++nbar);
+        if (!ok) {
+          if (pre && threadIdx.x == 0) mbar_wait(c.bars + kMW * kDepth, aphase & 1u, kWaitNs);
+          break;
+        }
+        ok = attention_phase<D, G>(c, l, area, aphase, pre, pos, sid);
+      }
+      // the residual after the last projection of the last block is the launch's output
+      if (ok && (ph < 3 || l + 1 < a.nl)) ok = grid_barrier(c, ++nbar);
     }
-    if (ok) ok = grid_barrier(c, ++nbar);
-    if (!ok) {
-      if (pre && threadIdx.x == 0) mbar_wait(c.bars + kMW * kDepth, aphase & 1u, kWaitNs);
-      break;
-    }
-    ok = attention_phase<D, G>(c, l, area, aphase, pre, pos, sid);
-    if (ok) ok = grid_barrier(c, ++nbar);
-    if (!ok) break;
-    // O projection + residual -> x1
-    stage_input(c, a.obuf, a.Hq * a.D, KpQ, nullptr, 0.f, xs, xc, nullptr);
-    ok = __syncthreads_and(gemv_phase(c, s, l, 1, xs, xc, xraw, pos, sid));
-    if (ok) ok = grid_barrier(c, ++nbar);
-    if (!ok) break;
-    // gate/up (RMSNorm with gamma_2), SwiGLU -> abuf; x1 kept for the down residual
-    stage_input(c, a.x1, a.H, KpH, L.ffn_norm, a.eps, xs, xc, xraw);
-    ok = __syncthreads_and(gemv_phase(c, s, l, 2, xs, xc, xraw, pos, sid));
-    if (ok) ok = grid_barrier(c, ++nbar);
-    if (!ok) break;
-    // down + residual -> hout
-    stage_input(c, a.abuf, a.F, KpF, nullptr, 0.f, xs, xc, nullptr);
-    ok = __syncthreads_and(gemv_phase(c, s, l, 3, xs, xc, xraw, pos, sid));
-    if (ok && l + 1 < a.nl) ok = grid_barrier(c, ++nbar);
   }
   if (!ok) stream_drain(c, s);
   grid_leave(c);
@@ -713,8 +951,10 @@ bool g_mega_ready = false;
 
 }  // namespace
 
-bool mega_supported(int H, int q_dim, int F, int head_dim, int group) {
+bool mega_supported(int H, int q_dim, int F, int head_dim, int group, int n_experts, int top_k) {
   if (!g_mega_ready) return false;
+  if (n_experts > kMaxExperts || top_k > kMaxTopK || (n_experts > 0 && top_k < 1)) return false;
+  if (n_experts > 0 && (F % top_k || F / top_k > kSlotQ)) return false;  // one expert's down row fits a slot
   if (head_dim != 64 && head_dim != 128) return false;
   if (group != 1 && group != 2 && group != 4 && group != 8) return false;
   if (q_dim / head_dim / group > 62) return false;  // per-KV-head counters in the 64-word barrier block
@@ -746,7 +986,7 @@ cudaError_t prepare_mega() {
 
 cudaError_t launch_mega_decode(const MegaArgs& a, cudaStream_t st) {
   const int G = a.Hq / a.Hkv;
-  if (!mega_supported(a.H, a.Hq * a.D, a.F, a.D, G)) return cudaErrorInvalidValue;
+  if (!mega_supported(a.H, a.Hq * a.D, a.F, a.D, G, a.n_experts, a.top_k)) return cudaErrorInvalidValue;
   if (a.n_chunks < 1 || a.n_chunks > kAttnMaxChunks) return cudaErrorInvalidValue;
   const size_t smem = mega_smem(a.H, a.Hq * a.D, a.F, a.D, G);
   if (a.D == 64) {

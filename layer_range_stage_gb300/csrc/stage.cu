@@ -106,11 +106,10 @@ void walk_plan(const stage_model_cfg& c, int begin, int end, std::vector<LayerDe
   f(T * 4, (void**)d_tok);
   f(T * 4, (void**)d_rows);
   f(4, (void**)err_word);
-  if (!moe) {  // persistent decode: block descriptors, post-attention residual, grid barrier
-    f((size_t)(end - begin) * sizeof(lrs::MegaLayer), (void**)mlayers);
-    f((size_t)H * 4, (void**)mega_x1);
-    f(256, (void**)mega_bar);
-  }
+  // persistent decode: block descriptors, post-attention residual, grid barrier
+  f((size_t)(end - begin) * sizeof(lrs::MegaLayer), (void**)mlayers);
+  f((size_t)H * 4, (void**)mega_x1);
+  f(256, (void**)mega_bar);
   if (!moe && c.gemm_bf16_min_tokens > 0) {  // bf16 operands of the tensor-core GEMMs
     f(T * (size_t)std::max(kpad(H), kpad(Hq * D)) * 2, (void**)act_bf16);
     f(T * (size_t)kpad(c.ffn) * 2, (void**)ffn_bf16);
@@ -277,6 +276,24 @@ int upload_stack(stage* st, const stage_q8& src, const DevQ8& whole, int row0, i
   return upload_q8(st, src, part, rows, [](int i) { return (int64_t)i; }, name);
 }
 
+// The persistent decode's descriptor of block gl: its device weights, norms and KV cache.
+int upload_descriptor(stage* st, int gl, const LayerDev& L) {
+  lrs::MegaLayer ml;
+  ml.wqkv = L.wqkv;
+  ml.wo = L.wo;
+  ml.wgu = L.wgu;
+  ml.wdown = L.wdown;
+  ml.router = L.router;
+  ml.egu = L.egu;
+  ml.edown = L.edown;
+  ml.attn_norm = L.attn_norm;
+  ml.ffn_norm = L.ffn_norm;
+  ml.kc = st->kc + (size_t)(gl - st->begin) * st->layer_kv;
+  ml.vc = st->vc + (size_t)(gl - st->begin) * st->layer_kv;
+  const cudaError_t ce = cudaMemcpy(st->mlayers + (gl - st->begin), &ml, sizeof ml, cudaMemcpyHostToDevice);
+  return ce == cudaSuccess ? STAGE_OK : cuda_err(st, ce, "block descriptor");
+}
+
 int load_layer(stage* st, int gl, const stage_layer_w* w) {
   const stage_model_cfg& c = st->cfg;
   if (gl < st->begin || gl >= st->end) return set_err(st, STAGE_E_INVALID, "layer %d outside the owned range [%d, %d)", gl, st->begin, st->end);
@@ -335,6 +352,7 @@ int load_layer(stage* st, int gl, const stage_layer_w* w) {
       if (ce != cudaSuccess) return cuda_err(st, ce, "expert gate/up");
       if ((rc = upload_stack(st, w->e_down[e], L.edown, e * H, H, "expert down"))) return rc;
     }
+    if ((rc = upload_descriptor(st, gl, L))) return rc;
   } else {
     const int F = c.ffn;
     std::vector<uint8_t> q((size_t)2 * F * L.wgu.Kp, 0);
@@ -355,17 +373,7 @@ int load_layer(stage* st, int gl, const stage_layer_w* w) {
     if (ce == cudaSuccess) ce = cudaMemcpy(L.wgu.s, s.data(), s.size() * 2, cudaMemcpyHostToDevice);
     if (ce != cudaSuccess) return cuda_err(st, ce, "gate/up");
     if ((rc = upload_plain(st, w->w_down, L.wdown, "w_down"))) return rc;
-    lrs::MegaLayer ml;
-    ml.wqkv = L.wqkv;
-    ml.wo = L.wo;
-    ml.wgu = L.wgu;
-    ml.wdown = L.wdown;
-    ml.attn_norm = L.attn_norm;
-    ml.ffn_norm = L.ffn_norm;
-    ml.kc = st->kc + (size_t)(gl - st->begin) * st->layer_kv;
-    ml.vc = st->vc + (size_t)(gl - st->begin) * st->layer_kv;
-    ce = cudaMemcpy(st->mlayers + (gl - st->begin), &ml, sizeof ml, cudaMemcpyHostToDevice);
-    if (ce != cudaSuccess) return cuda_err(st, ce, "block descriptor");
+    if ((rc = upload_descriptor(st, gl, L))) return rc;
   }
   L.loaded = true;
   return STAGE_OK;
@@ -537,7 +545,11 @@ int forward_dev(stage* st, int n, const int* d_seq, const int* d_pos, const int*
     m.Hq = Hq;
     m.Hkv = Hkv;
     m.D = D;
-    m.F = c.ffn;
+    const bool moe = c.n_experts > 0;
+    m.F = moe ? c.top_k * kpad(c.expert_ffn) : c.ffn;
+    m.n_experts = c.n_experts;
+    m.top_k = c.top_k;
+    m.EF = c.expert_ffn;
     m.max_len = c.max_seq_len;
     m.n_chunks = lrs::mega_chunks(Hkv);
     m.eps = c.rms_eps;
@@ -883,9 +895,11 @@ int stage_create(const stage_model_cfg* cfg, stage_layer_range range, const stag
   }
   {
     const char* mg = getenv("LRS_PERSISTENT");
-    st->mega = cfg->n_experts == 0 && !(mg && mg[0] == '0') &&
-               lrs::mega_supported(cfg->hidden, cfg->n_q_heads * cfg->head_dim, cfg->ffn, cfg->head_dim,
-                                   cfg->n_q_heads / cfg->n_kv_heads);
+    const bool moe = cfg->n_experts > 0;
+    st->mega = !(mg && mg[0] == '0') &&
+               lrs::mega_supported(cfg->hidden, cfg->n_q_heads * cfg->head_dim,
+                                   moe ? cfg->top_k * kpad(cfg->expert_ffn) : cfg->ffn, cfg->head_dim,
+                                   cfg->n_q_heads / cfg->n_kv_heads, cfg->n_experts, cfg->top_k);
   }
   if (e == cudaSuccess) e = cudaMallocHost(&st->h_stage, (size_t)4 * cfg->max_tokens * 4);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&st->staged, cudaEventDisableTiming);
