@@ -18,7 +18,7 @@ LIB_DIR = os.path.join(HERE, "_lib")
 LIB = os.path.join(LIB_DIR, "libstage.so")
 ROOT = os.path.dirname(HERE)
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["kernels_decode.cu", "kernels_prefill.cu", "kernels_mega.cu", "stage.cu", "ops.cu"]
+SOURCES = ["kernels_decode.cu", "kernels_prefill.cu", "kernels_mega.cu", "kernels_mega_moe.cu", "stage.cu", "ops.cu"]
 
 
 def nvcc() -> str:

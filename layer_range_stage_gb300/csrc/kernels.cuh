@@ -141,6 +141,7 @@ struct MegaArgs {
   const float2* rope = nullptr;
   int H = 0, Hq = 0, Hkv = 0, D = 0, F = 0, max_len = 0, n_chunks = 1;
   int n_experts = 0, top_k = 0, EF = 0;  // MoE stages: experts, selected per token, expert FFN width
+  float* logits = nullptr;                // MoE stages: [n_experts] router logits of the current block
   float eps = 1e-5f, scale = 1.f;
   unsigned* bar = nullptr;  // [64]: grid barrier counter, exit counter, per-KV-head attention
                             // counters; zero between launches (the last CTA out re-zeroes)

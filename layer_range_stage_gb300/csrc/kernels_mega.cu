@@ -1,951 +1,10 @@
-// Persistent decode of a dense stage (sm_103a): every block of the stage for one token in
-// one cooperative launch, one CTA per SM.
-//
-// What it computes is the decode block loop of "41. Many GPUs: tensor, pipeline, expert
-// and data parallelism", section "Pipeline parallelism" (add_norm, attention, add_norm,
-// MLP per block, the residual stream carried through), with the split-KV attention merge
-// of section "Ring attention for very long contexts".  The arithmetic per weight is the
-// dequant-fused dot product of q8dot.cuh.
-//
-// Why one launch: a batch-1 decode step is a chain of small dependent matrix-vector
-// products.  Launched one kernel each, every product pays its own ramp and tail while HBM
-// idles, and a successor cannot start streaming until its predecessor's CTAs leave the
-// SMs.  Here the weight stream never stops: each warp owns a fixed sequence of weight
-// slices (its share of every projection of every block, known before the first
-// activation exists) and keeps two of them in flight as bulk copies into shared memory,
-// running ahead across phases and blocks; the activations meet the weights at five grid
-// barriers per block.
-//
-// Work split of a projection with N rows: a task is R consecutive rows (R = 2 where the
-// epilogue needs a row pair: RoPE, SwiGLU) cut into P pieces of at most 4 KB each; task t
-// belongs to warp t mod (warps of the grid), so at any moment the grid reads one window of
-// the matrix.  A warp sums its pieces in order and reduces with shuffles: every output has
-// one fixed summation order.
-//
-// MoE stages: after the O projection every CTA computes the router itself (logits of all
-// experts from the normalised residual, top-k with ties to the lower id, softmax over the
-// selected) -- the same arithmetic on the same data, so every CTA picks the same experts --
-// and the gate/up and down slices of the selected experts stream in once it is known
-// (the weight stream pauses there: those slices depend on the routing).
-//
-// Grid barrier: a counter that only grows within a launch (release add, acquire polling,
-// bounded by time) and is reset by the last CTA to leave.  Every wait is bounded; a CTA
-// that runs out of time sets the error word, waits (bounded) for its own copies in flight
-// and leaves.
+// Persistent decode: the dense kernels and the host entry points (the kernel itself is in
+// mega_impl.cuh).
 
-#include <algorithm>
-#include <cfloat>
-
-#include "common.cuh"
-#include "kernels.cuh"
-#include "q8dot.cuh"
+#include "mega_impl.cuh"
 
 namespace lrs {
 namespace {
-
-constexpr int kMW = 16;                       // warps per CTA
-constexpr int kMT = kMW * 32;                 // threads per CTA
-constexpr int kDepth = 2;                     // weight slots per warp
-constexpr int kSlotQ = 4096;                  // weight bytes per slot
-constexpr int kSlotS = kSlotQ / 16;           // scale bytes per slot (one fp16 per 32 weights)
-template <int D>
-constexpr int attn_tile() { return D == 64 ? 256 : 128; }  // attention positions per tile (64 KB of K + V)
-constexpr int kMaxKp = 16384;                 // largest projection input (floats in shared memory)
-constexpr int kMaxPieces = 8;
-constexpr uint64_t kWaitNs = 200000000ull;    // bound of every wait: 0.2 s
-constexpr size_t kMaxSmem = 227 * 1024;
-
-// shared memory, from a 1024-byte aligned base
-constexpr size_t kOffRingQ = 0;
-constexpr size_t kOffRingS = kOffRingQ + (size_t)kMW * kDepth * kSlotQ;
-constexpr size_t kOffBars = kOffRingS + (size_t)kMW * kDepth * kSlotS;  // kMW*kDepth slot barriers + 1
-constexpr size_t kOffRed = kOffBars + 512;                               // 32 floats + flags
-constexpr size_t kOffMoe = kOffRed + 512;                                 // routing (MoE stages)
-constexpr int kMaxExperts = 256, kMaxTopK = 32;
-constexpr size_t kOffShapes = kOffMoe + (kMaxExperts + 4 * kMaxTopK + 4) * 4;  // [4] projection shapes
-constexpr size_t kOffXraw = kOffMoe + 2048;                               // [Kp(H)] floats
-
-__host__ __device__ constexpr int pad256(int k) { return (k + 255) / 256 * 256; }
-
-template <int D, int G>
-struct AttnLayout {
-  static constexpr int T = attn_tile<D>();
-  static constexpr size_t ks = 0;                                // K tile [T][D] fp16
-  static constexpr size_t vs = ks + (size_t)T * D * 2;           // V tile [T][D] fp16
-  static constexpr size_t qs = vs + (size_t)T * D * 2;           // q [G][D] f32
-  static constexpr size_t sc = qs + (size_t)G * D * 4;           // scores / probabilities [G][T]
-  static constexpr size_t st = sc + (size_t)G * T * 4;           // m, l, alpha, merged sum [4][G]
-  static constexpr size_t total = st + (size_t)4 * G * 4;
-  // merge, after the tiles: (m, l) [G][64] and chunk weights [64][G] over q and the scores;
-  // this CTA's slice of every chunk partial [n_chunks][ceil(G * D / n_chunks)] over the K/V tiles
-  static constexpr size_t mls = qs;
-  static constexpr size_t wts = qs + (size_t)G * 64 * 8;
-  static_assert(wts + (size_t)64 * G * 4 <= st, "merge scratch");
-  static_assert((size_t)(G * D + 64) * 4 <= (size_t)2 * T * D * 2, "merge slice scratch over the K/V tiles");
-};
-
-__device__ __forceinline__ void red_release_add(unsigned* p, unsigned v) {
-  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
-  unsigned v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
-// The weight stream of one warp: producer cursor (block l, projection ph, task t, slot j)
-// and the counts of slots issued and consumed.
-struct Stream {
-  int l, ph, t, j;
-  int issued, consumed;
-};
-
-// One projection's shape as the weight stream sees it: the same in every block of a stage.
-struct Shape {
-  int N, Kp;          // rows (of the projection as computed); row stride in bytes (scales: Kp / 32)
-  int T;              // tasks: N / R
-  int klen;           // bytes of a row's K range
-  int R, P, PS;       // rows per task, pieces per row, piece bytes
-  int B;              // pieces per ring slot (several whole pieces share a slot)
-  int mode;           // 0 plain rows; 1 rows of the selected experts (rps rows each); 2 piece j of a
-                      // row from selected expert j (K gathered over the experts)
-  int rps;
-};
-
-struct Ctx {
-  const MegaArgs* a;
-  const Shape* shape;          // [4] in shared memory
-  const int* moe_ids;          // [top_k] experts of the current block (MoE stages)
-  const float* moe_wts;        // [top_k] their routing weights
-  volatile int* moe_ready;     // last block whose routing is known
-  unsigned char* ringq;
-  unsigned char* rings;
-  uint64_t* bars;   // [kMW][kDepth] slot barriers, then the attention barrier
-  float* red;       // [32] block reduction scratch
-  volatile int* flag;  // [0] error seen by this CTA, [1] last-arriver flag
-  int lane, warp, gw, GW;
-};
-
-// ph: 0 QKV, 1 O, 2 gate/up (dense, or the selected experts'), 3 down (dense, or gathered).
-// Computed once per launch (from block 0: every block has the same shapes).
-__device__ Shape shape_of(const MegaArgs& a, int ph) {
-  const MegaLayer& L = a.layers[0];
-  Shape p;
-  p.mode = 0;
-  p.rps = 0;
-  const DevQ8* w;
-  if (a.n_experts > 0 && ph >= 2) {
-    if (ph == 2) {
-      w = &L.egu;
-      p.N = a.top_k * 2 * a.EF;
-      p.mode = 1;
-      p.rps = 2 * a.EF;
-    } else {
-      w = &L.edown;
-      p.N = a.H;
-      p.mode = 2;
-    }
-  } else {
-    w = ph == 0 ? &L.wqkv : ph == 1 ? &L.wo : ph == 2 ? &L.wgu : &L.wdown;
-    p.N = w->N;
-  }
-  p.Kp = w->Kp;
-  p.R = (ph == 0 || ph == 2) ? 2 : 1;
-  p.T = p.N / p.R;
-  if (p.mode == 2) {
-    p.P = a.top_k;
-    p.PS = w->Kp;
-    p.klen = p.P * p.PS;
-  } else {
-    p.klen = w->Kp;
-    p.P = (w->Kp + kSlotQ - 1) / kSlotQ;
-    p.PS = ((w->Kp / p.P + 255) / 256) * 256;
-  }
-  p.B = (p.klen % p.PS == 0) ? max(1, kSlotQ / p.PS) : 1;
-  return p;
-}
-
-struct Ph : Shape {  // one projection of a block: its shape and its weights
-  const uint8_t* q;
-  const uint16_t* s;
-};
-
-__device__ __forceinline__ Ph phase_of(const Ctx& c, int l, int ph) {
-  const MegaLayer& L = c.a->layers[l];
-  const DevQ8& w = (c.a->n_experts > 0 && ph >= 2) ? (ph == 2 ? L.egu : L.edown)
-                   : ph == 0 ? L.wqkv : ph == 1 ? L.wo : ph == 2 ? L.wgu : L.wdown;
-  Ph p;
-  static_cast<Shape&>(p) = c.shape[ph];
-  p.q = w.q;
-  p.s = w.s;
-  return p;
-}
-
-// Row-in-task and piece of slot j of a task (R is 1 or 2, j < R * P).
-__device__ __forceinline__ void split_j(const Shape& p, int j, int& rr, int& pc) {
-  rr = j >= p.P;
-  pc = j - rr * p.P;
-}
-
-// Pieces of this warp's share of a phase from task t, piece j on, counted up to `cap`.
-__device__ __forceinline__ int pieces_upto(const Ctx& c, const Shape& p, int t, int j, int cap) {
-  int n = p.R * p.P - j;
-  for (int tt = t + c.GW; n < cap && tt < p.T; tt += c.GW) n += p.R * p.P;
-  return min(n, cap);
-}
-
-// Global addresses of piece (row, pc) of a phase.
-__device__ __forceinline__ void piece_src(const Ctx& c, const Ph& p, int row, int pc, const uint8_t*& q,
-                                          const uint16_t*& sc) {
-  if (p.mode == 2) {
-    const size_t r = (size_t)c.moe_ids[pc] * p.N + row;
-    q = p.q + r * p.PS;
-    sc = p.s + r * (p.PS / 32);
-    return;
-  }
-  size_t r = row;
-  if (p.mode == 1) r = (size_t)c.moe_ids[row / p.rps] * p.rps + row % p.rps;
-  q = p.q + r * p.Kp + (size_t)pc * p.PS;
-  sc = p.s + r * (p.Kp / 32) + (size_t)pc * p.PS / 32;
-}
-
-__device__ __forceinline__ void stream_normalise(const Ctx& c, Stream& s) {
-  while (s.l < c.a->nl) {
-    if (s.t < c.shape[s.ph].T) return;
-    s.j = 0;
-    s.t = c.gw;
-    if (++s.ph == 4) {
-      s.ph = 0;
-      ++s.l;
-    }
-  }
-}
-
-// Advance a cursor past its current slot (no copy).
-__device__ __forceinline__ void stream_step(const Ctx& c, Stream& s, const Ph& p) {
-  if (++s.j == p.R * p.P) {
-    s.j = 0;
-    s.t += c.GW;
-    stream_normalise(c, s);
-  }
-}
-
-// Issue the next slot of this warp's stream (if any) into the ring: one piece, or up to B
-// whole pieces of the same phase.  Slices of the selected experts wait until the routing of
-// their block is known.
-__device__ __forceinline__ void stream_issue(const Ctx& c, Stream& s) {
-  if (s.l >= c.a->nl) return;
-  if (c.a->n_experts > 0 && s.ph >= 2 && s.l > *c.moe_ready) return;
-  const Ph p = phase_of(c, s.l, s.ph);
-  if (p.B == 1 && p.mode == 0) {  // one piece of a plain row per slot
-    int rr, pc;
-    split_j(p, s.j, rr, pc);
-    const int row = s.t * p.R + rr;
-    const int off = pc * p.PS, bytes = min(p.PS, p.klen - off);
-    const int slot = s.issued % kDepth;
-    if (c.lane == 0) {
-      uint64_t* bar = c.bars + c.warp * kDepth + slot;
-      fence_async_smem();
-      mbar_arrive_expect_tx(bar, (uint32_t)(bytes + bytes / 16));
-      bulk_g2s(c.ringq + (size_t)(c.warp * kDepth + slot) * kSlotQ, p.q + (size_t)row * p.Kp + off, (uint32_t)bytes,
-               bar);
-      bulk_g2s(c.rings + (size_t)(c.warp * kDepth + slot) * kSlotS, p.s + (size_t)row * (p.Kp / 32) + off / 32,
-               (uint32_t)(bytes / 16), bar);
-    }
-    ++s.issued;
-    stream_step(c, s, p);
-    return;
-  }
-  const int nb = p.B == 1 ? 1 : pieces_upto(c, p, s.t, s.j, p.B);
-  const int slot = s.issued % kDepth;
-  uint64_t* bar = c.bars + c.warp * kDepth + slot;
-  unsigned char* dq = c.ringq + (size_t)(c.warp * kDepth + slot) * kSlotQ;
-  unsigned char* ds = c.rings + (size_t)(c.warp * kDepth + slot) * kSlotS;
-  if (c.lane == 0) {
-    fence_async_smem();  // the slot's previous contents were read through the generic proxy
-    int rr0, pc0;
-    split_j(p, s.j, rr0, pc0);
-    const int bytes0 = min(p.PS, p.klen - pc0 * p.PS);
-    mbar_arrive_expect_tx(bar, (uint32_t)(nb == 1 ? bytes0 + bytes0 / 16 : nb * (p.PS + p.PS / 16)));
-  }
-  for (int u = 0; u < nb; ++u) {
-    int rr, pc;
-    split_j(p, s.j, rr, pc);
-    const int row = s.t * p.R + rr;
-    const int bytes = min(p.PS, p.klen - pc * p.PS);
-    if (c.lane == 0) {
-      const uint8_t* q;
-      const uint16_t* sc;
-      piece_src(c, p, row, pc, q, sc);
-      bulk_g2s(dq + u * p.PS, q, (uint32_t)bytes, bar);
-      bulk_g2s(ds + u * (p.PS / 16), sc, (uint32_t)(bytes / 16), bar);
-    }
-    if (u + 1 < nb && ++s.j == p.R * p.P) {  // stays inside the phase: nb counted its pieces left
-      s.j = 0;
-      s.t += c.GW;
-    }
-  }
-  ++s.issued;
-  stream_step(c, s, p);
-}
-
-// Top the ring up to kDepth slots (after the routing of a block became known).
-__device__ __forceinline__ void stream_refill(const Ctx& c, Stream& s) {
-  while (s.issued - s.consumed < kDepth && s.l < c.a->nl) {
-    const int before = s.issued;
-    stream_issue(c, s);
-    if (s.issued == before) break;
-  }
-}
-
-// After a failed wait: wait (bounded) for this warp's copies still in flight.
-__device__ void stream_drain(const Ctx& c, Stream& s) {
-  for (int k = s.consumed; k < s.issued; ++k)
-    mbar_wait(c.bars + c.warp * kDepth + k % kDepth, (unsigned)(k / kDepth) & 1u, kWaitNs);
-  s.consumed = s.issued;
-}
-
-__device__ __forceinline__ void set_error(const Ctx& c) {
-  atomicExch(c.a->err, 1);
-  c.flag[0] = 1;
-}
-
-// Grid barrier number `k` (1-based) of this launch; false when the wait ran out.
-__device__ bool grid_barrier(const Ctx& c, unsigned k) {
-  __syncthreads();
-  if (threadIdx.x == 0 && !c.flag[0]) {
-    const unsigned target = k * gridDim.x;
-    red_release_add(c.a->bar, 1u);
-    if (ld_acquire_u32(c.a->bar) < target) {
-      const uint64_t t0 = global_ns();
-      while (ld_acquire_u32(c.a->bar) < target)
-        if (global_ns() - t0 > kWaitNs) {
-          set_error(c);
-          break;
-        }
-    }
-  }
-  __syncthreads();
-  return !c.flag[0];
-}
-
-// Leaving: the last CTA out resets the barrier counters for the next launch (every CTA has
-// stopped polling by the time it counts itself out).
-__device__ void grid_leave(const Ctx& c) {
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    const unsigned prev = atomicAdd(c.a->bar + 1, 1u);
-    if (prev == gridDim.x - 1) {
-      atomicExch(c.a->bar, 0u);
-      for (int h = 0; h < c.a->Hkv; ++h) atomicExch(c.a->bar + 2 + h, 0u);
-      atomicExch(c.a->bar + 1, 0u);
-    }
-  }
-}
-
-// A projection input from global memory (written earlier in this launch: read through L2)
-// into shared memory: normalised by RMSNorm with gamma when given, scaled by 2^64,
-// swizzled per 16-float chunk, with chunk sums; the raw values also into xraw when given.
-// Thread `tid` owns chunks tid and tid + kMT: every load (x and gamma) is issued before
-// any is used, so the staging costs one round trip to L2.
-__device__ void stage_input(const Ctx& c, const float* x, int K, int Kp, const float* gamma, float eps, float* xs,
-                            float* xc, float* xraw) {
-  constexpr int CPT = kMaxKp / 16 / kMT;  // chunks per thread
-  const int tid = threadIdx.x, nchunk = Kp >> 4;
-  const float4* x4 = reinterpret_cast<const float4*>(x);
-  const float4* g4 = reinterpret_cast<const float4*>(gamma);
-  float4 v[CPT][4], gm[CPT][4];
-#pragma unroll
-  for (int k2 = 0; k2 < CPT; ++k2) {
-    const int ch = tid + k2 * kMT;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int k = ch * 16 + 4 * j;  // K is a multiple of 4: a float4 lies wholly inside or outside
-      const bool in = ch < nchunk && k < K;
-      v[k2][j] = in ? __ldcg(x4 + (k >> 2)) : make_float4(0.f, 0.f, 0.f, 0.f);
-      gm[k2][j] = (in && gamma) ? __ldg(g4 + (k >> 2)) : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-  }
-  float rinv = 1.0f;
-  if (gamma) {
-    float ss = 0.f;
-#pragma unroll
-    for (int k2 = 0; k2 < CPT; ++k2)
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        ss = fmaf(v[k2][j].x, v[k2][j].x, ss);
-        ss = fmaf(v[k2][j].y, v[k2][j].y, ss);
-        ss = fmaf(v[k2][j].z, v[k2][j].z, ss);
-        ss = fmaf(v[k2][j].w, v[k2][j].w, ss);
-      }
-    ss = warp_sum(ss);
-    if (c.lane == 0) c.red[c.warp] = ss;
-    __syncthreads();
-    float tot = 0.f;
-#pragma unroll
-    for (int w = 0; w < kMW; ++w) tot += c.red[w];
-    rinv = 1.0f / sqrtf(tot / (float)K + eps);
-  }
-#pragma unroll
-  for (int k2 = 0; k2 < CPT; ++k2) {
-    const int ch = tid + k2 * kMT;
-    if (ch >= nchunk) continue;
-    if (xraw)
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        if (ch * 16 + 4 * j < K) reinterpret_cast<float4*>(xraw)[ch * 4 + j] = v[k2][j];
-    float h[16];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      h[4 * j] = v[k2][j].x;
-      h[4 * j + 1] = v[k2][j].y;
-      h[4 * j + 2] = v[k2][j].z;
-      h[4 * j + 3] = v[k2][j].w;
-      if (gamma) {
-        h[4 * j] = h[4 * j] * rinv * gm[k2][j].x;
-        h[4 * j + 1] = h[4 * j + 1] * rinv * gm[k2][j].y;
-        h[4 * j + 2] = h[4 * j + 2] * rinv * gm[k2][j].z;
-        h[4 * j + 3] = h[4 * j + 3] * rinv * gm[k2][j].w;
-      }
-    }
-    float sum = 0.f;
-#pragma unroll
-    for (int j = 0; j < 16; ++j) sum += h[j];
-    const int sw = (ch >> 1) & 3;
-    float* xp = xs + ch * 16;
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-      reinterpret_cast<float4*>(xp)[j ^ sw] =
-          make_float4(h[4 * j] * kXScale, h[4 * j + 1] * kXScale, h[4 * j + 2] * kXScale, h[4 * j + 3] * kXScale);
-    xc[ch] = sum;
-  }
-  __syncthreads();
-}
-
-// One projection of block l: consume this warp's tasks from the ring, refill behind.
-// Returns false (for the whole warp) after a timed-out wait (error set, copies drained);
-// the caller makes the outcome CTA-uniform.  BATCH: several pieces share a ring slot.
-template <bool BATCH>
-__device__ bool gemv_phase_t(const Ctx& c, Stream& s, int l, int ph, const float* xs, const float* xc,
-                             const float* xraw, int pos, int sid) {
-  const MegaArgs& a = *c.a;
-  const Ph p = phase_of(c, l, ph);
-  const bool moe = a.n_experts > 0;
-  const int T = p.T, nsl = p.R * p.P;
-  int left = BATCH && c.gw < T ? ((T - 1 - c.gw) / c.GW + 1) * nsl : 0;  // this warp's pieces of the phase
-  int uin = 0, ucap = 1;  // position in, and pieces of, the current slot
-  for (int t = c.gw; t < T; t += c.GW) {
-    float acc0 = 0.f, acc1 = 0.f;
-    for (int j = 0; j < nsl; ++j) {
-      int rr, pc;
-      split_j(p, j, rr, pc);
-      const int off = pc * p.PS, bytes = min(p.PS, p.klen - off);
-      const int slot = s.consumed % kDepth;
-      if (!BATCH || uin == 0) {
-        if (BATCH) ucap = min(p.B, left);
-        const bool landed = mbar_wait(c.bars + c.warp * kDepth + slot, (unsigned)(s.consumed / kDepth) & 1u, kWaitNs);
-        if (!__all_sync(0xffffffffu, landed)) {  // warp-uniform decision
-          if (c.lane == 0) set_error(c);
-          stream_drain(c, s);
-          return false;
-        }
-      }
-      const int u = BATCH ? uin : 0;
-      const unsigned char* sq = c.ringq + (size_t)(c.warp * kDepth + slot) * kSlotQ + u * p.PS;
-      const unsigned char* ssc = c.rings + (size_t)(c.warp * kDepth + slot) * kSlotS + u * (p.PS / 16);
-      float acc = rr ? acc1 : acc0;
-      const int nch = bytes >> 4, cb = off >> 4;
-#pragma unroll 2
-      for (int cl = c.lane; cl < nch; cl += 32) {
-        const int ch = cb + cl;
-        const int sw = (ch >> 1) & 3;
-        const float4* xp = reinterpret_cast<const float4*>(xs + ch * 16);
-        const float4 x0 = xp[0 ^ sw], x1 = xp[1 ^ sw], x2 = xp[2 ^ sw], x3 = xp[3 ^ sw];
-        const uint4 w = *reinterpret_cast<const uint4*>(sq + cl * 16);
-        const float scl = h2f_bits(*reinterpret_cast<const uint16_t*>(ssc + (cl >> 1) * 2));
-        acc = fmaf(scl, fmaf(dot16_u8(w, x0, x1, x2, x3), kPScale, -128.0f * xc[ch]), acc);
-      }
-      if (rr)
-        acc1 = acc;
-      else
-        acc0 = acc;
-      if (BATCH) --left;
-      if (!BATCH || ++uin == ucap) {  // the slot is consumed: refill it
-        uin = 0;
-        __syncwarp();
-        ++s.consumed;
-        stream_issue(c, s);
-      }
-    }
-    acc0 = warp_sum(acc0);
-    if (p.R == 2) acc1 = warp_sum(acc1);
-    if (c.lane != 0) continue;
-    const MegaLayer& L = a.layers[l];
-    if (ph == 0) {  // rows (2t, 2t+1) are dims (i, i + D/2) of one head: RoPE, then q or fp16 K/V
-      const int hd = a.D >> 1, head = t / hd, i = t - head * hd;
-      const float y0 = acc0, y1 = acc1;
-      if (head < a.Hq) {
-        const float2 cs = a.rope[(size_t)pos * hd + i];
-        float* qo = a.qbuf + (size_t)head * a.D;
-        qo[i] = y0 * cs.x - y1 * cs.y;
-        qo[i + hd] = y1 * cs.x + y0 * cs.y;
-      } else {
-        const bool is_k = head < a.Hq + a.Hkv;
-        const int kvh = head - a.Hq - (is_k ? 0 : a.Hkv);
-        const size_t base = (((size_t)sid * a.Hkv + kvh) * a.max_len + pos) * a.D;
-        if (is_k) {
-          const float2 cs = a.rope[(size_t)pos * hd + i];
-          L.kc[base + i] = __float2half_rn(y0 * cs.x - y1 * cs.y);
-          L.kc[base + i + hd] = __float2half_rn(y1 * cs.x + y0 * cs.y);
-        } else {
-          L.vc[base + i] = __float2half_rn(y0);
-          L.vc[base + i + hd] = __float2half_rn(y1);
-        }
-      }
-    } else if (ph == 1) {
-      a.x1[t] = __fadd_rn(xraw[t], acc0);
-    } else if (ph == 2) {
-      if (moe) {  // pair t: expert slot t / EF, unit t % EF; scaled by the routing weight
-        const int slot = t / a.EF, i = t - slot * a.EF;
-        a.abuf[(size_t)slot * pad256(a.EF) + i] = silu(acc0) * acc1 * c.moe_wts[slot];
-      } else {
-        a.abuf[t] = silu(acc0) * acc1;
-      }
-    } else {
-      a.hout[t] = __fadd_rn(xraw[t], acc0);
-    }
-  }
-  return true;
-}
-
-__device__ bool gemv_phase(const Ctx& c, Stream& s, int l, int ph, const float* xs, const float* xc,
-                           const float* xraw, int pos, int sid) {
-  return c.shape[ph].B > 1 ? gemv_phase_t<true>(c, s, l, ph, xs, xc, xraw, pos, sid)
-                           : gemv_phase_t<false>(c, s, l, ph, xs, xc, xraw, pos, sid);
-}
-
-// The router of MoE block l, computed by every CTA from the staged normalised residual:
-// logits of all experts (same per-chunk arithmetic as the projections), the top_k by rank
-// (ties to the lower id), their softmax; ids, weights and the ready block into shared memory.
-__device__ void route(const Ctx& c, int l, const float* xs, const float* xc, float* logits, float* sel, int* sel_id,
-                      int* ids, float* wts) {
-  const MegaArgs& a = *c.a;
-  const DevQ8& r = a.layers[l].router;
-  const int E = a.n_experts, k = a.top_k, nchunk = r.Kp >> 4;
-  // warp w: experts w, w + 16, ... (up to 8 per pass); per chunk, the 8 experts' loads are
-  // issued together
-  constexpr int EPW = 8;
-  for (int e0 = c.warp; e0 < E; e0 += kMW * EPW) {
-    float acc[EPW];
-#pragma unroll
-    for (int i = 0; i < EPW; ++i) acc[i] = 0.f;
-    for (int ch = c.lane; ch < nchunk; ch += 32) {
-      const int sw = (ch >> 1) & 3;
-      const float4* xp = reinterpret_cast<const float4*>(xs + ch * 16);
-      const float4 x0 = xp[0 ^ sw], x1 = xp[1 ^ sw], x2 = xp[2 ^ sw], x3 = xp[3 ^ sw];
-      const float corr = -128.0f * xc[ch];
-      uint4 w[EPW];
-      uint16_t sc[EPW];
-#pragma unroll
-      for (int i = 0; i < EPW; ++i) {
-        const int e = min(e0 + i * kMW, E - 1);
-        w[i] = ld_stream_u4(r.q + (size_t)e * r.Kp + (size_t)ch * 16);
-        sc[i] = ld_stream_u16(r.s + (size_t)e * (r.Kp / 32) + (ch >> 1));
-      }
-#pragma unroll
-      for (int i = 0; i < EPW; ++i)
-        acc[i] = fmaf(h2f_bits(sc[i]), fmaf(dot16_u8(w[i], x0, x1, x2, x3), kPScale, corr), acc[i]);
-    }
-#pragma unroll
-    for (int i = 0; i < EPW; ++i) {
-      const float v = warp_sum(acc[i]);
-      if (c.lane == 0 && e0 + i * kMW < E) logits[e0 + i * kMW] = v;
-    }
-  }
-  __syncthreads();
-  for (int e = threadIdx.x; e < E; e += kMT) {
-    const float v = logits[e];
-    int rank = 0;
-    for (int f = 0; f < E; ++f) {
-      const float u = logits[f];
-      rank += (u > v) || (u == v && f < e);
-    }
-    if (rank < k) {
-      sel[rank] = v;
-      sel_id[rank] = e;
-    }
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    const float m = sel[0];
-    float z = 0.f;
-    for (int j = 0; j < k; ++j) z += expf(sel[j] - m);
-    for (int j = 0; j < k; ++j) {
-      ids[j] = sel_id[j];
-      wts[j] = expf(sel[j] - m) / z;
-    }
-    *c.moe_ready = l;
-  }
-  __syncthreads();
-}
-
-// Positions [c0, c1) of attention item `it` (KV head it % Hkv, chunk it / Hkv).
-__device__ __forceinline__ void item_range(const MegaArgs& a, int it, int pos, int& kvh, int& chunk, int& c0,
-                                           int& c1) {
-  kvh = it % a.Hkv;
-  chunk = it / a.Hkv;
-  const int L = pos + 1, clen = (L + a.n_chunks - 1) / a.n_chunks;
-  c0 = min(L, chunk * clen);
-  c1 = min(L, c0 + clen);
-}
-
-// Thread 0: bulk copies of the K and V rows [p0, p0 + nold) (positions written by earlier
-// steps) into the attention tile; completes on the attention barrier.
-template <int D, int G>
-__device__ __forceinline__ void attn_issue(const Ctx& c, unsigned char* area, const __half* kb, const __half* vb,
-                                           int p0, int nold) {
-  using AL = AttnLayout<D, G>;
-  uint64_t* bar = c.bars + kMW * kDepth;
-  fence_async_smem();
-  mbar_arrive_expect_tx(bar, (uint32_t)(2 * nold * D * 2));
-  if (nold > 0) {
-    bulk_g2s(area + AL::ks, kb + (size_t)p0 * D, (uint32_t)(nold * D * 2), bar);
-    bulk_g2s(area + AL::vs, vb + (size_t)p0 * D, (uint32_t)(nold * D * 2), bar);
-  }
-}
-
-// Split-K attention of block l over this CTA's items; the last chunk of a KV head to finish
-// together with the other chunks of its head merges a slice of the head's outputs into
-// obuf.  `prefetched`: tile 0 of the first item was issued before the preceding barrier.
-template <int D, int G>
-__device__ bool attention_phase(const Ctx& c, int l, unsigned char* area, unsigned& aphase, bool prefetched, int pos,
-                                int sid) {
-  using AL = AttnLayout<D, G>;
-  constexpr int T = AL::T, OPT = (G * D + kMT - 1) / kMT;
-  const MegaArgs& a = *c.a;
-  const MegaLayer& Ly = a.layers[l];
-  __half* Ks = reinterpret_cast<__half*>(area + AL::ks);
-  __half* Vs = reinterpret_cast<__half*>(area + AL::vs);
-  float* qs = reinterpret_cast<float*>(area + AL::qs);
-  float* S = reinterpret_cast<float*>(area + AL::sc);
-  float* st_m = reinterpret_cast<float*>(area + AL::st);
-  float* st_l = st_m + G;
-  float* st_a = st_l + G;
-  float* st_L = st_a + G;
-  const int tid = threadIdx.x;
-  const int nch = a.n_chunks, items = a.Hkv * nch;
-  uint64_t* abar = c.bars + kMW * kDepth;
-  for (int it = blockIdx.x; it < items; it += gridDim.x) {
-    int kvh, chunk, c0, c1;
-    item_range(a, it, pos, kvh, chunk, c0, c1);
-    const __half* kb = Ly.kc + ((size_t)sid * a.Hkv + kvh) * (size_t)a.max_len * D;
-    const __half* vb = Ly.vc + ((size_t)sid * a.Hkv + kvh) * (size_t)a.max_len * D;
-    for (int i = tid; i < G * D; i += kMT) qs[i] = __ldcg(a.qbuf + (size_t)kvh * G * D + i);
-    if (tid < G) {
-      st_m[tid] = -INFINITY;
-      st_l[tid] = 0.f;
-    }
-    float o[OPT];
-#pragma unroll
-    for (int k = 0; k < OPT; ++k) o[k] = 0.f;
-    for (int p0 = c0; p0 < c1; p0 += T) {
-      const int np = min(T, c1 - p0);
-      const int nold = max(0, min(np, pos - p0));
-      if (!(prefetched && p0 == c0 && it == (int)blockIdx.x) && tid == 0) attn_issue<D, G>(c, area, kb, vb, p0, nold);
-      if (nold < np) {  // the current position: written by this launch's QKV phase, read through L2
-        const int r = pos - p0;
-        for (int i = tid; i < D / 8; i += kMT) {
-          reinterpret_cast<uint4*>(Ks + (size_t)r * D)[i] = __ldcg(reinterpret_cast<const uint4*>(kb + (size_t)pos * D) + i);
-          reinterpret_cast<uint4*>(Vs + (size_t)r * D)[i] = __ldcg(reinterpret_cast<const uint4*>(vb + (size_t)pos * D) + i);
-        }
-      }
-      const bool landed = mbar_wait(abar, aphase & 1u, kWaitNs);
-      if (!__syncthreads_and(landed)) {  // CTA-uniform decision (also orders the row copy above)
-        if (tid == 0) set_error(c);
-        return false;
-      }
-      ++aphase;
-      // scores: thread -> (head g, position p); the 16-byte pieces of a K row are walked in a
-      // rotated order so that the lanes' rows fall in distinct banks
-      for (int idx = tid; idx < G * T; idx += kMT) {
-        const int g = idx / T, p = idx - g * T;
-        if (p < np) {
-          const __half* kr = Ks + (size_t)p * D;
-          const float* qg = qs + g * D;
-          float sc = 0.f;
-#pragma unroll 4
-          for (int i = 0; i < D / 8; ++i) {
-            const int j = (i + p) & (D / 8 - 1);
-            const uint4 kk = *reinterpret_cast<const uint4*>(kr + 8 * j);
-            const float4 qa = *reinterpret_cast<const float4*>(qg + 8 * j);
-            const float4 qb = *reinterpret_cast<const float4*>(qg + 8 * j + 4);
-            const float2 k01 = __half22float2(*reinterpret_cast<const __half2*>(&kk.x));
-            const float2 k23 = __half22float2(*reinterpret_cast<const __half2*>(&kk.y));
-            const float2 k45 = __half22float2(*reinterpret_cast<const __half2*>(&kk.z));
-            const float2 k67 = __half22float2(*reinterpret_cast<const __half2*>(&kk.w));
-            sc = fmaf(qa.x, k01.x, sc);
-            sc = fmaf(qa.y, k01.y, sc);
-            sc = fmaf(qa.z, k23.x, sc);
-            sc = fmaf(qa.w, k23.y, sc);
-            sc = fmaf(qb.x, k45.x, sc);
-            sc = fmaf(qb.y, k45.y, sc);
-            sc = fmaf(qb.z, k67.x, sc);
-            sc = fmaf(qb.w, k67.y, sc);
-          }
-          S[g * T + p] = sc * a.scale;
-        }
-      }
-      __syncthreads();
-      if (c.warp < G) {  // warp g: tile max, probabilities, running (max, sum) of head g
-        const int g = c.warp;
-        float sv[T / 32];
-        float mt = -INFINITY;
-#pragma unroll
-        for (int k2 = 0; k2 < T / 32; ++k2) {
-          const int p = c.lane + 32 * k2;
-          sv[k2] = p < np ? S[g * T + p] : -INFINITY;
-          mt = fmaxf(mt, sv[k2]);
-        }
-        mt = warp_max(mt);
-        const float mold = st_m[g];
-        const float mnew = fmaxf(mold, mt);
-        float lsum = 0.f;
-#pragma unroll
-        for (int k2 = 0; k2 < T / 32; ++k2) {
-          const int p = c.lane + 32 * k2;
-          const float e = p < np ? expf(sv[k2] - mnew) : 0.f;
-          S[g * T + p] = e;
-          lsum += e;
-        }
-        const float lt = warp_sum(lsum);
-        if (c.lane == 0) {
-          const float alpha = (mold == -INFINITY) ? 0.f : expf(mold - mnew);
-          st_a[g] = alpha;
-          st_l[g] = st_l[g] * alpha + lt;
-          st_m[g] = mnew;
-        }
-      }
-      __syncthreads();
-#pragma unroll
-      for (int k = 0; k < OPT; ++k) {
-        const int idx = tid + k * kMT;
-        if (idx < G * D) {
-          const int g = idx / D, d = idx - g * D;
-          float v = o[k] * st_a[g];
-          for (int p = 0; p < np; ++p) v = fmaf(S[g * T + p], __half2float(Vs[(size_t)p * D + d]), v);
-          o[k] = v;
-        }
-      }
-      __syncthreads();  // the tile is consumed before the next one lands
-    }
-    // partial of this chunk (token 0 of the AttnArgs layout), then arrive on the head's counter
-    float* po = a.part_o + ((size_t)kvh * nch + chunk) * (G * D);
-#pragma unroll
-    for (int k = 0; k < OPT; ++k) {
-      const int idx = tid + k * kMT;
-      if (idx < G * D) po[idx] = o[k];
-    }
-    if (tid < G) a.part_ml[((size_t)kvh * G + tid) * nch + chunk] = make_float2(st_m[tid], st_l[tid]);
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) red_release_add(a.bar + 2 + kvh, 1u);
-  }
-  // Merge, spread over the chunks: once every chunk of its head has arrived, the CTA of
-  // chunk j merges outputs [j SL, (j + 1) SL) of the head -- weights e^(m_c - M) per head,
-  // weighted sums in chunk order.  (Every CTA arrives on all of its items before waiting.)
-  constexpr int GD = G * D;
-  const int SL = (GD + nch - 1) / nch;
-  for (int it = blockIdx.x; it < items; it += gridDim.x) {
-    int kvh, chunk, c0, c1;
-    item_range(a, it, pos, kvh, chunk, c0, c1);
-    if (tid == 0) {
-      const unsigned target = (unsigned)(l + 1) * (unsigned)nch;
-      const unsigned* hc = a.bar + 2 + kvh;
-      if (ld_acquire_u32(hc) < target) {
-        const uint64_t t0 = global_ns();
-        while (ld_acquire_u32(hc) < target)
-          if (global_ns() - t0 > kWaitNs) {
-            set_error(c);
-            break;
-          }
-      }
-    }
-    __syncthreads();
-    if (c.flag[0]) return false;
-    const int i0 = min(GD, chunk * SL), n = min(GD, i0 + SL) - i0;
-    float2* mls = reinterpret_cast<float2*>(area + AL::mls);  // [G][nch]
-    float* wts = reinterpret_cast<float*>(area + AL::wts);    // [nch][G]
-    float* pst = reinterpret_cast<float*>(area + AL::ks);     // [nch][SL] this slice of every partial
-    for (int i = tid; i < G * nch; i += kMT) mls[i] = __ldcg(a.part_ml + (size_t)kvh * G * nch + i);
-    for (int i = tid; i < nch * n; i += kMT) {
-      const int ck = i / n, k = i - ck * n;
-      pst[ck * SL + k] = __ldcg(a.part_o + ((size_t)kvh * nch + ck) * GD + i0 + k);
-    }
-    __syncthreads();
-    if (tid < G) {
-      float M = -INFINITY;
-      for (int ck = 0; ck < nch; ++ck) M = fmaxf(M, mls[tid * nch + ck].x);
-      float Ls = 0.f;
-      for (int ck = 0; ck < nch; ++ck) {
-        const float2 mc = mls[tid * nch + ck];
-        const float w = mc.y > 0.f ? expf(mc.x - M) : 0.f;
-        wts[ck * G + tid] = w;
-        Ls = fmaf(mc.y, w, Ls);
-      }
-      st_L[tid] = Ls;
-    }
-    __syncthreads();
-    for (int k = tid; k < n; k += kMT) {
-      const int g = (i0 + k) / D;
-      float acc = 0.f;
-      for (int ck = 0; ck < nch; ++ck) acc = fmaf(wts[ck * G + g], pst[ck * SL + k], acc);
-      a.obuf[(size_t)kvh * GD + i0 + k] = acc / st_L[g];
-    }
-    __syncthreads();
-  }
-  return true;
-}
-
-template <int D, int G>
-__global__ void __launch_bounds__(kMT, 1) mega_decode_kernel(const MegaArgs a) {
-  extern __shared__ unsigned char mg_raw[];
-  unsigned char* sm = reinterpret_cast<unsigned char*>(((uintptr_t)mg_raw + 1023) & ~(uintptr_t)1023);
-  const int KpH = pad256(a.H);
-  const size_t off_u = (kOffXraw + (size_t)KpH * 4 + 1023) & ~(size_t)1023;
-  Ctx c;
-  c.a = &a;
-  c.ringq = sm + kOffRingQ;
-  c.rings = sm + kOffRingS;
-  c.bars = reinterpret_cast<uint64_t*>(sm + kOffBars);
-  c.red = reinterpret_cast<float*>(sm + kOffRed);
-  c.flag = reinterpret_cast<volatile int*>(sm + kOffRed + 256);
-  float* moe_logits = reinterpret_cast<float*>(sm + kOffMoe);  // [kMaxExperts]
-  int* moe_ids = reinterpret_cast<int*>(moe_logits + kMaxExperts);
-  float* moe_wts = reinterpret_cast<float*>(moe_ids + kMaxTopK);
-  float* moe_sel = moe_wts + kMaxTopK;
-  int* moe_sel_id = reinterpret_cast<int*>(moe_sel + kMaxTopK);
-  c.moe_ids = moe_ids;
-  c.moe_wts = moe_wts;
-  c.moe_ready = reinterpret_cast<volatile int*>(moe_sel_id + kMaxTopK);
-  static_assert(kOffShapes + 4 * sizeof(Shape) <= kOffXraw, "shapes");
-  Shape* shapes = reinterpret_cast<Shape*>(sm + kOffShapes);
-  c.shape = shapes;
-  c.lane = threadIdx.x & 31;
-  c.warp = threadIdx.x >> 5;
-  c.gw = c.warp * gridDim.x + blockIdx.x;
-  c.GW = kMW * gridDim.x;
-  float* xraw = reinterpret_cast<float*>(sm + kOffXraw);
-  unsigned char* area = sm + off_u;  // union: projection input, or attention tiles
-  const int KpQ = pad256(a.Hq * a.D), KpF = pad256(a.F);
-  const int Kx = max(KpH, max(KpQ, KpF));
-  float* xs = reinterpret_cast<float*>(area);
-  float* xc = xs + Kx;
-
-  if (threadIdx.x < kMW * kDepth + 1) mbar_init(c.bars + threadIdx.x, 1);
-  if (threadIdx.x == 0) {
-    c.flag[0] = 0;
-    c.flag[1] = 0;
-    *c.moe_ready = -1;
-  }
-  if (threadIdx.x < 4) shapes[threadIdx.x] = shape_of(a, threadIdx.x);
-  mbar_fence_init();
-  __syncthreads();
-  const int pos = __ldcg(a.pos), sid = __ldcg(a.seq);
-
-  Stream s;
-  s.l = 0;
-  s.ph = 0;
-  s.t = c.gw;
-  s.j = 0;
-  s.issued = 0;
-  s.consumed = 0;
-  stream_normalise(c, s);
-  for (int d = 0; d < kDepth; ++d) stream_issue(c, s);
-
-  unsigned nbar = 0, aphase = 0;
-  bool ok = true;
-  // one call site per step (the projection step is the same code for all four projections:
-  // the kernel stays small enough for the instruction cache)
-  for (int l = 0; l < a.nl && ok; ++l) {
-    const MegaLayer& L = a.layers[l];
-    for (int ph = 0; ph < 4 && ok; ++ph) {
-      // the projection's input: QKV and gate/up normalise the residual (gamma_1, gamma_2; the
-      // raw residual is kept for the residual adds), O and down take the attention output and
-      // the SwiGLU output as they are
-      const float* in = ph == 0 ? (l == 0 ? a.hin : a.hout) : ph == 1 ? a.obuf : ph == 2 ? a.x1 : a.abuf;
-      const int K = ph == 1 ? a.Hq * a.D : ph == 3 ? a.F : a.H;
-      const int Kp = ph == 1 ? KpQ : ph == 3 ? KpF : KpH;
-      const float* gamma = ph == 0 ? L.attn_norm : ph == 2 ? L.ffn_norm : nullptr;
-      stage_input(c, in, K, Kp, gamma, a.eps, xs, xc, (ph & 1) ? nullptr : xraw);
-      if (ph == 2 && a.n_experts > 0) {  // routing, then the selected experts' slices stream in
-        route(c, l, xs, xc, moe_logits, moe_sel, moe_sel_id, moe_ids, moe_wts);
-        stream_refill(c, s);
-      }
-      ok = __syncthreads_and(gemv_phase(c, s, l, ph, xs, xc, xraw, pos, sid));
-      if (ph == 0) {
-        // tile 0 of this CTA's first attention item (positions of earlier steps) streams in
-        // while the grid meets
-        bool pre = false;
-        if (ok && (int)blockIdx.x < a.Hkv * a.n_chunks) {
-          int kvh, chunk, c0, c1;
-          item_range(a, blockIdx.x, pos, kvh, chunk, c0, c1);
-          if (c0 < c1) {
-            pre = true;
-            if (threadIdx.x == 0) {
-              const __half* kb = L.kc + ((size_t)sid * a.Hkv + kvh) * (size_t)a.max_len * D;
-              const __half* vb = L.vc + ((size_t)sid * a.Hkv + kvh) * (size_t)a.max_len * D;
-              const int np = min(AttnLayout<D, G>::T, c1 - c0);
-              attn_issue<D, G>(c, area, kb, vb, c0, max(0, min(np, pos - c0)));
-            }
-          }
-        }
-        if (ok) ok = grid_barrier(c, ++nbar);
-        if (!ok) {
-          if (pre && threadIdx.x == 0) mbar_wait(c.bars + kMW * kDepth, aphase & 1u, kWaitNs);
-          break;
-        }
-        ok = attention_phase<D, G>(c, l, area, aphase, pre, pos, sid);
-      }
-      // the residual after the last projection of the last block is the launch's output
-      if (ok && (ph < 3 || l + 1 < a.nl)) ok = grid_barrier(c, ++nbar);
-    }
-  }
-  if (!ok) stream_drain(c, s);
-  grid_leave(c);
-}
-
-size_t mega_smem(int H, int q_dim, int F, int D, int G) {
-  const int KpH = pad256(H), Kx = std::max(KpH, std::max(pad256(q_dim), pad256(F)));
-  const size_t off_u = (kOffXraw + (size_t)KpH * 4 + 1023) & ~(size_t)1023;
-  size_t attn = 0;
-  if (D == 64) attn = G == 1 ? AttnLayout<64, 1>::total : G == 2 ? AttnLayout<64, 2>::total
-                    : G == 4 ? AttnLayout<64, 4>::total : AttnLayout<64, 8>::total;
-  else attn = G == 1 ? AttnLayout<128, 1>::total : G == 2 ? AttnLayout<128, 2>::total
-            : G == 4 ? AttnLayout<128, 4>::total : AttnLayout<128, 8>::total;
-  const size_t u = std::max((size_t)Kx * 4 + (size_t)(Kx / 16) * 4, attn);
-  return off_u + u + 1024;  // + alignment of the dynamic base
-}
-
-template <int D, int G>
-cudaError_t prepare_mega_dg() {
-  return cudaFuncSetAttribute(mega_decode_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMaxSmem);
-}
-
-template <int D, int G>
-cudaError_t launch_mega_dg(const MegaArgs& a, size_t smem, cudaStream_t st) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(sm_count());
-  cfg.blockDim = dim3(kMT);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, mega_decode_kernel<D, G>, a);
-}
 
 bool g_mega_ready = false;
 
@@ -972,13 +31,9 @@ cudaError_t prepare_mega() {
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
   if (e != cudaSuccess) return e;
   if (!coop) return cudaSuccess;  // persistent decode unavailable: mega_supported() stays false
-  const cudaError_t r[] = {prepare_mega_dg<64, 1>(),  prepare_mega_dg<64, 2>(),  prepare_mega_dg<64, 4>(),
-                           prepare_mega_dg<64, 8>(),  prepare_mega_dg<128, 1>(), prepare_mega_dg<128, 2>(),
-                           prepare_mega_dg<128, 4>(), prepare_mega_dg<128, 8>()};
-  for (cudaError_t x : r)
-    if (x != cudaSuccess) return x;
+  if ((e = prepare_mega_all<false>()) != cudaSuccess || (e = prepare_mega_moe()) != cudaSuccess) return e;
   int nb = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, mega_decode_kernel<128, 4>, kMT, kMaxSmem - 1024);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, mega_decode_kernel<128, 4, false>, kMT, kMaxSmem - 1024);
   if (e != cudaSuccess) return e;
   g_mega_ready = nb >= 1;
   return cudaSuccess;
@@ -989,20 +44,7 @@ cudaError_t launch_mega_decode(const MegaArgs& a, cudaStream_t st) {
   if (!mega_supported(a.H, a.Hq * a.D, a.F, a.D, G, a.n_experts, a.top_k)) return cudaErrorInvalidValue;
   if (a.n_chunks < 1 || a.n_chunks > kAttnMaxChunks) return cudaErrorInvalidValue;
   const size_t smem = mega_smem(a.H, a.Hq * a.D, a.F, a.D, G);
-  if (a.D == 64) {
-    switch (G) {
-      case 1: return launch_mega_dg<64, 1>(a, smem, st);
-      case 2: return launch_mega_dg<64, 2>(a, smem, st);
-      case 4: return launch_mega_dg<64, 4>(a, smem, st);
-      default: return launch_mega_dg<64, 8>(a, smem, st);
-    }
-  }
-  switch (G) {
-    case 1: return launch_mega_dg<128, 1>(a, smem, st);
-    case 2: return launch_mega_dg<128, 2>(a, smem, st);
-    case 4: return launch_mega_dg<128, 4>(a, smem, st);
-    default: return launch_mega_dg<128, 8>(a, smem, st);
-  }
+  return a.n_experts > 0 ? launch_mega_moe(a, smem, st) : launch_mega_all<false>(a, smem, st);
 }
 
 }  // namespace lrs

@@ -550,6 +550,7 @@ int forward_dev(stage* st, int n, const int* d_seq, const int* d_pos, const int*
     m.n_experts = c.n_experts;
     m.top_k = c.top_k;
     m.EF = c.expert_ffn;
+    m.logits = st->moe_logits;
     m.max_len = c.max_seq_len;
     m.n_chunks = lrs::mega_chunks(Hkv);
     m.eps = c.rms_eps;
