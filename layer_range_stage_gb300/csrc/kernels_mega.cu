@@ -33,7 +33,7 @@ cudaError_t prepare_mega() {
   if (!coop) return cudaSuccess;  // persistent decode unavailable: mega_supported() stays false
   if ((e = prepare_mega_all<false>()) != cudaSuccess || (e = prepare_mega_moe()) != cudaSuccess) return e;
   int nb = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, mega_decode_kernel<128, 4, false>, kMT, kMaxSmem - 1024);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, mega_decode_kernel<128, 4, false>, kMT, kMaxSmem - 128);
   if (e != cudaSuccess) return e;
   g_mega_ready = nb >= 1;
   return cudaSuccess;

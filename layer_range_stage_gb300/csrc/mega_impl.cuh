@@ -62,17 +62,21 @@ constexpr int kMaxPieces = 8;
 constexpr uint64_t kWaitNs = 200000000ull;    // bound of every wait: 0.2 s
 constexpr size_t kMaxSmem = 227 * 1024;
 
-// shared memory, from a 1024-byte aligned base
+// shared memory, from a 128-byte aligned base (bulk copies want 16 bytes, float4 16)
 constexpr size_t kOffRingQ = 0;
 constexpr size_t kOffRingS = kOffRingQ + (size_t)kMW * kDepth * kSlotQ;
 constexpr size_t kOffBars = kOffRingS + (size_t)kMW * kDepth * kSlotS;  // kMW*kDepth slot barriers + 1
 constexpr size_t kOffRed = kOffBars + 512;                               // 32 floats + flags
 constexpr size_t kOffMoe = kOffRed + 512;                                 // routing (MoE stages)
 constexpr int kMaxExperts = 256, kMaxTopK = 32;
+constexpr size_t kOffLogits = kOffMoe, kOffIds = kOffLogits + kMaxExperts * 4, kOffWts = kOffIds + kMaxTopK * 4,
+                 kOffSel = kOffWts + kMaxTopK * 4, kOffSelId = kOffSel + kMaxTopK * 4,
+                 kOffReady = kOffSelId + kMaxTopK * 4;
 constexpr size_t kOffShapes = kOffMoe + (kMaxExperts + 4 * kMaxTopK + 4) * 4;  // [kPhases] shapes
+constexpr size_t kOffWptr = kOffShapes + 256;                             // [kMW][2] stream pointers
 // the phases of a block's weight stream
 constexpr int kPhQKV = 0, kPhO = 1, kPhRouter = 2, kPhGU = 3, kPhDown = 4, kPhases = 5;
-constexpr size_t kOffXraw = kOffMoe + 2048;                               // [Kp(H)] floats
+constexpr size_t kOffXraw = kOffMoe + 2304;                               // [Kp(H)] floats
 
 __host__ __device__ constexpr int pad256(int k) { return (k + 255) / 256 * 256; }
 
@@ -134,19 +138,31 @@ struct Shape {
   int rps;
 };
 
+// Everything in shared memory is at a fixed offset from one base (no pointer per region
+// kept in registers).
 struct Ctx {
   const MegaArgs* a;
-  const Shape* shape;          // [kPhases] in shared memory
-  float* logits;               // [n_experts] router logits of the current block (MoE stages)
-  const int* moe_ids;          // [top_k] experts of the current block (MoE stages)
-  const float* moe_wts;        // [top_k] their routing weights
-  volatile int* moe_ready;     // last block whose routing is known
-  unsigned char* ringq;
-  unsigned char* rings;
-  uint64_t* bars;   // [kMW][kDepth] slot barriers, then the attention barrier
-  float* red;       // [32] block reduction scratch
-  volatile int* flag;  // [0] error seen by this CTA, [1] last-arriver flag
+  unsigned char* sm;
   int lane, warp, gw, GW;
+  __device__ unsigned char* ringq() const { return sm + kOffRingQ; }
+  __device__ unsigned char* rings() const { return sm + kOffRingS; }
+  __device__ uint64_t* bars() const { return reinterpret_cast<uint64_t*>(sm + kOffBars); }  // [kMW][kDepth], attention
+  __device__ float* red() const { return reinterpret_cast<float*>(sm + kOffRed); }          // [32] reduction scratch
+  __device__ volatile int* flag() const {  // [0] error seen by this CTA, [1] last-arriver flag
+    return reinterpret_cast<volatile int*>(sm + kOffRed + 256);
+  }
+  __device__ float* logits() const { return reinterpret_cast<float*>(sm + kOffLogits); }  // [n_experts] (MoE)
+  __device__ int* moe_ids() const { return reinterpret_cast<int*>(sm + kOffIds); }        // [top_k] selected experts
+  __device__ float* moe_wts() const { return reinterpret_cast<float*>(sm + kOffWts); }    // [top_k] their weights
+  __device__ float* sel() const { return reinterpret_cast<float*>(sm + kOffSel); }        // [top_k] ranking scratch
+  __device__ int* sel_id() const { return reinterpret_cast<int*>(sm + kOffSelId); }
+  __device__ volatile int* moe_ready() const {  // last block whose routing is known
+    return reinterpret_cast<volatile int*>(sm + kOffReady);
+  }
+  __device__ const Shape* shape() const { return reinterpret_cast<const Shape*>(sm + kOffShapes); }  // [kPhases]
+  // [kMW][2] weights and scales of each warp's stream cursor (l, ph): an issue reads them
+  // here, not from the block descriptor
+  __device__ const void** wptr() const { return reinterpret_cast<const void**>(sm + kOffWptr); }
 };
 
 // ph: kPhQKV, kPhO, kPhRouter (MoE stages: one logit per task, into global memory), kPhGU
@@ -211,7 +227,7 @@ __device__ __forceinline__ Ph phase_of(const Ctx& c, int l, int ph) {
                    : (MOE && ph >= kPhGU)   ? (ph == kPhGU ? L.egu : L.edown)
                    : ph == kPhQKV ? L.wqkv : ph == kPhO ? L.wo : ph == kPhGU ? L.wgu : L.wdown;
   Ph p;
-  static_cast<Shape&>(p) = c.shape[ph];
+  static_cast<Shape&>(p) = c.shape()[ph];
   p.q = w.q;
   p.s = w.s;
   return p;
@@ -235,35 +251,44 @@ template <bool MOE>
 __device__ __forceinline__ void piece_src(const Ctx& c, const Ph& p, int row, int pc, const uint8_t*& q,
                                           const uint16_t*& sc) {
   if (MOE && p.mode == 2) {
-    const size_t r = (size_t)c.moe_ids[pc] * p.N + row;
+    const size_t r = (size_t)c.moe_ids()[pc] * p.N + row;
     q = p.q + r * p.PS;
     sc = p.s + r * (p.PS / 32);
     return;
   }
   size_t r = row;
-  if (MOE && p.mode == 1) r = (size_t)c.moe_ids[row / p.rps] * p.rps + row % p.rps;
+  if (MOE && p.mode == 1) r = (size_t)c.moe_ids()[row / p.rps] * p.rps + row % p.rps;
   q = p.q + r * p.Kp + (size_t)pc * p.PS;
   sc = p.s + r * (p.Kp / 32) + (size_t)pc * p.PS / 32;
 }
 
+template <bool MOE>
 __device__ __forceinline__ void stream_normalise(const Ctx& c, Stream& s) {
+  bool moved = false;
   while (s.l < c.a->nl) {
-    if (s.t < c.shape[s.ph].T) return;
+    if (s.t < c.shape()[s.ph].T) break;
     s.j = 0;
     if (++s.ph == kPhases) {
       s.ph = 0;
       ++s.l;
     }
     s.t = c.gw;
+    moved = true;
+  }
+  if (moved && s.l < c.a->nl) {
+    const Ph p = phase_of<MOE>(c, s.l, s.ph);
+    c.wptr()[2 * c.warp] = p.q;
+    c.wptr()[2 * c.warp + 1] = p.s;
   }
 }
 
 // Advance a cursor past its current slot (no copy).
-__device__ __forceinline__ void stream_step(const Ctx& c, Stream& s, const Ph& p) {
+template <bool MOE>
+__device__ __forceinline__ void stream_step(const Ctx& c, Stream& s, const Shape& p) {
   if (++s.j == p.R * p.P) {
     s.j = 0;
     s.t += c.GW;
-    stream_normalise(c, s);
+    stream_normalise<MOE>(c, s);
   }
 }
 
@@ -273,8 +298,11 @@ __device__ __forceinline__ void stream_step(const Ctx& c, Stream& s, const Ph& p
 template <bool MOE>
 __device__ __forceinline__ void stream_issue(const Ctx& c, Stream& s) {
   if (s.l >= c.a->nl) return;
-  if (MOE && s.ph >= kPhGU && s.l > *c.moe_ready) return;
-  const Ph p = phase_of<MOE>(c, s.l, s.ph);
+  if (MOE && s.ph >= kPhGU && s.l > *c.moe_ready()) return;
+  Ph p;
+  static_cast<Shape&>(p) = c.shape()[s.ph];
+  p.q = static_cast<const uint8_t*>(c.wptr()[2 * c.warp]);
+  p.s = static_cast<const uint16_t*>(c.wptr()[2 * c.warp + 1]);
   if (p.B == 1 && p.mode == 0) {  // one piece of a plain row per slot
     int rr, pc;
     split_j(p, s.j, rr, pc);
@@ -282,23 +310,23 @@ __device__ __forceinline__ void stream_issue(const Ctx& c, Stream& s) {
     const int off = pc * p.PS, bytes = min(p.PS, p.klen - off);
     const int slot = s.issued % kDepth;
     if (c.lane == 0) {
-      uint64_t* bar = c.bars + c.warp * kDepth + slot;
+      uint64_t* bar = c.bars() + c.warp * kDepth + slot;
       fence_async_smem();
       mbar_arrive_expect_tx(bar, (uint32_t)(bytes + bytes / 16));
-      bulk_g2s(c.ringq + (size_t)(c.warp * kDepth + slot) * kSlotQ, p.q + (size_t)row * p.Kp + off, (uint32_t)bytes,
+      bulk_g2s(c.ringq() + (size_t)(c.warp * kDepth + slot) * kSlotQ, p.q + (size_t)row * p.Kp + off, (uint32_t)bytes,
                bar);
-      bulk_g2s(c.rings + (size_t)(c.warp * kDepth + slot) * kSlotS, p.s + (size_t)row * (p.Kp / 32) + off / 32,
+      bulk_g2s(c.rings() + (size_t)(c.warp * kDepth + slot) * kSlotS, p.s + (size_t)row * (p.Kp / 32) + off / 32,
                (uint32_t)(bytes / 16), bar);
     }
     ++s.issued;
-    stream_step(c, s, p);
+    stream_step<MOE>(c, s, p);
     return;
   }
   const int nb = p.B == 1 ? 1 : pieces_upto(c, p, s.t, s.j, p.B);
   const int slot = s.issued % kDepth;
-  uint64_t* bar = c.bars + c.warp * kDepth + slot;
-  unsigned char* dq = c.ringq + (size_t)(c.warp * kDepth + slot) * kSlotQ;
-  unsigned char* ds = c.rings + (size_t)(c.warp * kDepth + slot) * kSlotS;
+  uint64_t* bar = c.bars() + c.warp * kDepth + slot;
+  unsigned char* dq = c.ringq() + (size_t)(c.warp * kDepth + slot) * kSlotQ;
+  unsigned char* ds = c.rings() + (size_t)(c.warp * kDepth + slot) * kSlotS;
   if (c.lane == 0) {
     fence_async_smem();  // the slot's previous contents were read through the generic proxy
     int rr0, pc0;
@@ -324,7 +352,7 @@ __device__ __forceinline__ void stream_issue(const Ctx& c, Stream& s) {
     }
   }
   ++s.issued;
-  stream_step(c, s, p);
+  stream_step<MOE>(c, s, p);
 }
 
 // Top the ring up to kDepth slots (after the routing of a block became known).
@@ -340,19 +368,19 @@ __device__ __forceinline__ void stream_refill(const Ctx& c, Stream& s) {
 // After a failed wait: wait (bounded) for this warp's copies still in flight.
 __device__ void stream_drain(const Ctx& c, Stream& s) {
   for (int k = s.consumed; k < s.issued; ++k)
-    mbar_wait(c.bars + c.warp * kDepth + k % kDepth, (unsigned)(k / kDepth) & 1u, kWaitNs);
+    mbar_wait(c.bars() + c.warp * kDepth + k % kDepth, (unsigned)(k / kDepth) & 1u, kWaitNs);
   s.consumed = s.issued;
 }
 
 __device__ __forceinline__ void set_error(const Ctx& c) {
   atomicExch(c.a->err, 1);
-  c.flag[0] = 1;
+  c.flag()[0] = 1;
 }
 
 // Grid barrier number `k` (1-based) of this launch; false when the wait ran out.
 __device__ bool grid_barrier(const Ctx& c, unsigned k) {
   __syncthreads();
-  if (threadIdx.x == 0 && !c.flag[0]) {
+  if (threadIdx.x == 0 && !c.flag()[0]) {
     const unsigned target = k * gridDim.x;
     red_release_add(c.a->bar, 1u);
     if (ld_acquire_u32(c.a->bar) < target) {
@@ -365,7 +393,7 @@ __device__ bool grid_barrier(const Ctx& c, unsigned k) {
     }
   }
   __syncthreads();
-  return !c.flag[0];
+  return !c.flag()[0];
 }
 
 // Leaving: the last CTA out resets the barrier counters for the next launch (every CTA has
@@ -419,11 +447,11 @@ __device__ void stage_input(const Ctx& c, const float* x, int K, int Kp, const f
         ss = fmaf(v[k2][j].w, v[k2][j].w, ss);
       }
     ss = warp_sum(ss);
-    if (c.lane == 0) c.red[c.warp] = ss;
+    if (c.lane == 0) c.red()[c.warp] = ss;
     __syncthreads();
     float tot = 0.f;
 #pragma unroll
-    for (int w = 0; w < kMW; ++w) tot += c.red[w];
+    for (int w = 0; w < kMW; ++w) tot += c.red()[w];
     rinv = 1.0f / sqrtf(tot / (float)K + eps);
   }
 #pragma unroll
@@ -483,7 +511,7 @@ __device__ bool gemv_phase_t(const Ctx& c, Stream& s, int l, int ph, const float
       const int slot = s.consumed % kDepth;
       if (!BATCH || uin == 0) {
         if (BATCH) ucap = min(p.B, left);
-        const bool landed = mbar_wait(c.bars + c.warp * kDepth + slot, (unsigned)(s.consumed / kDepth) & 1u, kWaitNs);
+        const bool landed = mbar_wait(c.bars() + c.warp * kDepth + slot, (unsigned)(s.consumed / kDepth) & 1u, kWaitNs);
         if (!__all_sync(0xffffffffu, landed)) {  // warp-uniform decision
           if (c.lane == 0) set_error(c);
           stream_drain(c, s);
@@ -491,8 +519,8 @@ __device__ bool gemv_phase_t(const Ctx& c, Stream& s, int l, int ph, const float
         }
       }
       const int u = BATCH ? uin : 0;
-      const unsigned char* sq = c.ringq + (size_t)(c.warp * kDepth + slot) * kSlotQ + u * p.PS;
-      const unsigned char* ssc = c.rings + (size_t)(c.warp * kDepth + slot) * kSlotS + u * (p.PS / 16);
+      const unsigned char* sq = c.ringq() + (size_t)(c.warp * kDepth + slot) * kSlotQ + u * p.PS;
+      const unsigned char* ssc = c.rings() + (size_t)(c.warp * kDepth + slot) * kSlotS + u * (p.PS / 16);
       float acc = rr ? acc1 : acc0;
       const int nch = bytes >> 4, cb = off >> 4;
 #pragma unroll 2
@@ -549,7 +577,7 @@ __device__ bool gemv_phase_t(const Ctx& c, Stream& s, int l, int ph, const float
     } else if (ph == kPhGU) {
       if (moe) {  // pair t: expert slot t / EF, unit t % EF; scaled by the routing weight
         const int slot = t / a.EF, i = t - slot * a.EF;
-        a.abuf[(size_t)slot * pad256(a.EF) + i] = silu(acc0) * acc1 * c.moe_wts[slot];
+        a.abuf[(size_t)slot * pad256(a.EF) + i] = silu(acc0) * acc1 * c.moe_wts()[slot];
       } else {
         a.abuf[t] = silu(acc0) * acc1;
       }
@@ -563,7 +591,7 @@ __device__ bool gemv_phase_t(const Ctx& c, Stream& s, int l, int ph, const float
 template <bool MOE>
 __device__ bool gemv_phase(const Ctx& c, Stream& s, int l, int ph, const float* xs, const float* xc,
                            const float* xraw, int pos, int sid) {
-  return c.shape[ph].B > 1 ? gemv_phase_t<true, MOE>(c, s, l, ph, xs, xc, xraw, pos, sid)
+  return c.shape()[ph].B > 1 ? gemv_phase_t<true, MOE>(c, s, l, ph, xs, xc, xraw, pos, sid)
                            : gemv_phase_t<false, MOE>(c, s, l, ph, xs, xc, xraw, pos, sid);
 }
 
@@ -571,11 +599,15 @@ __device__ bool gemv_phase(const Ctx& c, Stream& s, int l, int ph, const float* 
 // wrote the logits to global memory): every CTA reads all logits, takes the top_k by rank
 // (ties to the lower id) and their softmax; ids, weights and the ready block into shared
 // memory.
-__device__ void rank_experts(const Ctx& c, int l, float* sel, int* sel_id, int* ids, float* wts) {
+__device__ void rank_experts(const Ctx& c, int l) {
   const MegaArgs& a = *c.a;
+  float* sel = c.sel();
+  int* sel_id = c.sel_id();
+  int* ids = c.moe_ids();
+  float* wts = c.moe_wts();
   const int E = a.n_experts, k = a.top_k;
   if (threadIdx.x < k) sel_id[threadIdx.x] = threadIdx.x;  // valid ids whatever the logits hold
-  for (int e = threadIdx.x; e < E; e += kMT) c.logits[e] = __ldcg(a.logits + e);
+  for (int e = threadIdx.x; e < E; e += kMT) c.logits()[e] = __ldcg(a.logits + e);
   __syncthreads();
   // rank of expert e: 4 threads, each counting over a quarter of the experts
   const int qlen = (E + 3) >> 2;
@@ -584,10 +616,10 @@ __device__ void rank_experts(const Ctx& c, int l, float* sel, int* sel_id, int* 
     float v = 0.f;
     int rank = 0;
     if (e < E) {
-      v = c.logits[e];
+      v = c.logits()[e];
       const int f1 = min(E, (qq + 1) * qlen);
       for (int f = qq * qlen; f < f1; ++f) {
-        const float u = c.logits[f];
+        const float u = c.logits()[f];
         rank += (u > v) || (u == v && f < e);
       }
     }
@@ -607,7 +639,7 @@ __device__ void rank_experts(const Ctx& c, int l, float* sel, int* sel_id, int* 
       ids[c.lane] = sel_id[c.lane];
       wts[c.lane] = ev / z;
     }
-    if (c.lane == 0) *c.moe_ready = l;
+    if (c.lane == 0) *c.moe_ready() = l;
   }
   __syncthreads();
 }
@@ -628,7 +660,7 @@ template <int D, int G>
 __device__ __forceinline__ void attn_issue(const Ctx& c, unsigned char* area, const __half* kb, const __half* vb,
                                            int p0, int nold) {
   using AL = AttnLayout<D, G>;
-  uint64_t* bar = c.bars + kMW * kDepth;
+  uint64_t* bar = c.bars() + kMW * kDepth;
   fence_async_smem();
   mbar_arrive_expect_tx(bar, (uint32_t)(2 * nold * D * 2));
   if (nold > 0) {
@@ -659,7 +691,7 @@ __device__ bool attention_phase(const Ctx& c, int l, unsigned char* area, unsign
   float* red = reinterpret_cast<float*>(area + AL::ks);  // [PG][G][D] after the last tile
   const int tid = threadIdx.x;
   const int nch = a.n_chunks, items = a.Hkv * nch;
-  uint64_t* abar = c.bars + kMW * kDepth;
+  uint64_t* abar = c.bars() + kMW * kDepth;
   // PV: dims (2 dp, 2 dp + 1) of heads hg HPV .. hg HPV + HPV - 1, positions pg + PG k
   const int dp = tid % DP, hg = (tid / DP) % NHG, pg = tid / (DP * NHG);
   for (int it = blockIdx.x; it < items; it += gridDim.x) {
@@ -822,7 +854,7 @@ __device__ bool attention_phase(const Ctx& c, int l, unsigned char* area, unsign
       }
     }
     __syncthreads();
-    if (c.flag[0]) return false;
+    if (c.flag()[0]) return false;
     const int i0 = min(GD, chunk * SL), n = min(GD, i0 + SL) - i0;
     float2* mls = reinterpret_cast<float2*>(area + AL::mls);  // [G][nch]
     float* wts = reinterpret_cast<float*>(area + AL::wts);    // [nch][G]
@@ -866,28 +898,16 @@ __device__ bool attention_phase(const Ctx& c, int l, unsigned char* area, unsign
 template <int D, int G, bool MOE>
 __global__ void __launch_bounds__(kMT, 1) mega_decode_kernel(const MegaArgs a) {
   extern __shared__ unsigned char mg_raw[];
-  unsigned char* sm = reinterpret_cast<unsigned char*>(((uintptr_t)mg_raw + 1023) & ~(uintptr_t)1023);
+  unsigned char* sm = reinterpret_cast<unsigned char*>(((uintptr_t)mg_raw + 127) & ~(uintptr_t)127);
   const int KpH = pad256(a.H);
-  const size_t off_u = (kOffXraw + (size_t)KpH * 4 + 1023) & ~(size_t)1023;
+  const size_t off_u = (kOffXraw + (size_t)KpH * 4 + 127) & ~(size_t)127;
   Ctx c;
   c.a = &a;
-  c.ringq = sm + kOffRingQ;
-  c.rings = sm + kOffRingS;
-  c.bars = reinterpret_cast<uint64_t*>(sm + kOffBars);
-  c.red = reinterpret_cast<float*>(sm + kOffRed);
-  c.flag = reinterpret_cast<volatile int*>(sm + kOffRed + 256);
-  float* moe_logits = reinterpret_cast<float*>(sm + kOffMoe);  // [kMaxExperts]
-  int* moe_ids = reinterpret_cast<int*>(moe_logits + kMaxExperts);
-  float* moe_wts = reinterpret_cast<float*>(moe_ids + kMaxTopK);
-  float* moe_sel = moe_wts + kMaxTopK;
-  int* moe_sel_id = reinterpret_cast<int*>(moe_sel + kMaxTopK);
-  c.moe_ids = moe_ids;
-  c.moe_wts = moe_wts;
-  c.moe_ready = reinterpret_cast<volatile int*>(moe_sel_id + kMaxTopK);
-  c.logits = moe_logits;
-  static_assert(kOffShapes + kPhases * sizeof(Shape) <= kOffXraw, "shapes");
+  c.sm = sm;
+  static_assert(kOffReady + 4 <= kOffShapes, "routing scratch");
+  static_assert(kOffShapes + kPhases * sizeof(Shape) <= kOffWptr, "shapes");
+  static_assert(kOffWptr % 16 == 0 && kOffWptr + kMW * 2 * sizeof(void*) <= kOffXraw, "stream pointers");
   Shape* shapes = reinterpret_cast<Shape*>(sm + kOffShapes);
-  c.shape = shapes;
   c.lane = threadIdx.x & 31;
   c.warp = threadIdx.x >> 5;
   c.gw = c.warp * gridDim.x + blockIdx.x;
@@ -899,11 +919,11 @@ __global__ void __launch_bounds__(kMT, 1) mega_decode_kernel(const MegaArgs a) {
   float* xs = reinterpret_cast<float*>(area);
   float* xc = xs + Kx;
 
-  if (threadIdx.x < kMW * kDepth + 1) mbar_init(c.bars + threadIdx.x, 1);
+  if (threadIdx.x < kMW * kDepth + 1) mbar_init(c.bars() + threadIdx.x, 1);
   if (threadIdx.x == 0) {
-    c.flag[0] = 0;
-    c.flag[1] = 0;
-    *c.moe_ready = -1;
+    c.flag()[0] = 0;
+    c.flag()[1] = 0;
+    *c.moe_ready() = -1;
   }
   if (threadIdx.x < kPhases) shapes[threadIdx.x] = shape_of(a, threadIdx.x);
   mbar_fence_init();
@@ -917,7 +937,12 @@ __global__ void __launch_bounds__(kMT, 1) mega_decode_kernel(const MegaArgs a) {
   s.j = 0;
   s.issued = 0;
   s.consumed = 0;
-  stream_normalise(c, s);
+  stream_normalise<MOE>(c, s);
+  if (s.l < a.nl) {
+    const Ph p0 = phase_of<MOE>(c, s.l, s.ph);
+    c.wptr()[2 * c.warp] = p0.q;
+    c.wptr()[2 * c.warp + 1] = p0.s;
+  }
   for (int d = 0; d < kDepth; ++d) stream_issue<MOE>(c, s);
 
   unsigned nbar = 0, aphase = 0;
@@ -963,14 +988,14 @@ __global__ void __launch_bounds__(kMT, 1) mega_decode_kernel(const MegaArgs a) {
         }
         if (ok) ok = grid_barrier(c, ++nbar);
         if (!ok) {
-          if (pre && threadIdx.x == 0) mbar_wait(c.bars + kMW * kDepth, aphase & 1u, kWaitNs);
+          if (pre && threadIdx.x == 0) mbar_wait(c.bars() + kMW * kDepth, aphase & 1u, kWaitNs);
           break;
         }
         ok = attention_phase<D, G>(c, l, area, aphase, pre, pos, sid);
       }
       // the residual after the last projection of the last block is the launch's output
       if (ok && (ph < kPhDown || l + 1 < a.nl)) ok = grid_barrier(c, ++nbar);
-      if (MOE && ok && ph == kPhRouter) rank_experts(c, l, moe_sel, moe_sel_id, moe_ids, moe_wts);
+      if (MOE && ok && ph == kPhRouter) rank_experts(c, l);
     }
   }
   if (!ok) stream_drain(c, s);
@@ -979,14 +1004,14 @@ __global__ void __launch_bounds__(kMT, 1) mega_decode_kernel(const MegaArgs a) {
 
 size_t mega_smem(int H, int q_dim, int F, int D, int G) {
   const int KpH = pad256(H), Kx = std::max(KpH, std::max(pad256(q_dim), pad256(F)));
-  const size_t off_u = (kOffXraw + (size_t)KpH * 4 + 1023) & ~(size_t)1023;
+  const size_t off_u = (kOffXraw + (size_t)KpH * 4 + 127) & ~(size_t)127;
   size_t attn = 0;
   if (D == 64) attn = G == 1 ? AttnLayout<64, 1>::total : G == 2 ? AttnLayout<64, 2>::total
                     : G == 4 ? AttnLayout<64, 4>::total : AttnLayout<64, 8>::total;
   else attn = G == 1 ? AttnLayout<128, 1>::total : G == 2 ? AttnLayout<128, 2>::total
             : G == 4 ? AttnLayout<128, 4>::total : AttnLayout<128, 8>::total;
   const size_t u = std::max((size_t)Kx * 4 + (size_t)(Kx / 16) * 4, attn);
-  return off_u + u + 1024;  // + alignment of the dynamic base
+  return off_u + u + 128;  // + alignment of the dynamic base
 }
 
 template <int D, int G, bool MOE>
