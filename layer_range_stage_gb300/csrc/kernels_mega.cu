@@ -13,13 +13,14 @@ bool g_mega_ready = false;
 bool mega_supported(int H, int q_dim, int F, int head_dim, int group, int n_experts, int top_k) {
   if (!g_mega_ready) return false;
   if (n_experts > kMaxExperts || top_k > kMaxTopK || (n_experts > 0 && top_k < 1)) return false;
-  if (n_experts > 0 && (F % top_k || F / top_k > kSlotQ)) return false;  // one expert's down row fits a slot
+  if (n_experts > 0 && (F % top_k || F / top_k > kSlotQ / 2)) return false;  // a row pair's expert piece fits a slot
+  if (n_experts & 1) return false;  // router rows go in pairs
   if (head_dim != 64 && head_dim != 128) return false;
   if (group != 1 && group != 2 && group != 4 && group != 8) return false;
   if (q_dim / head_dim / group > 62) return false;  // per-KV-head counters in the 64-word barrier block
   if ((H & 3) || (q_dim & 3) || (F & 3)) return false;
   const int Kx = std::max(pad256(H), std::max(pad256(q_dim), pad256(F)));
-  if (Kx > kMaxKp || (Kx + kSlotQ - 1) / kSlotQ > kMaxPieces) return false;
+  if (Kx > kMaxKp || (Kx + kSlotQ / 2 - 1) / (kSlotQ / 2) > kMaxPieces) return false;
   return mega_smem(H, q_dim, F, head_dim, group) <= kMaxSmem;
 }
 

@@ -16,11 +16,12 @@
 // running ahead across phases and blocks; the activations meet the weights at five grid
 // barriers per block (six in MoE stages).
 //
-// Work split of a projection with N rows: a task is R consecutive rows (R = 2 where the
-// epilogue needs a row pair: RoPE, SwiGLU) cut into P pieces of at most 4 KB each; task t
-// belongs to warp t mod (warps of the grid), so at any moment the grid reads one window of
-// the matrix.  A warp sums its pieces in order and reduces with shuffles: every output has
-// one fixed summation order.
+// Work split of a projection with N rows: a task is a row pair (2t, 2t + 1) -- the pairs the
+// RoPE and SwiGLU epilogues need, and for the other projections two rows that share each
+// load of the staged input -- cut into P column blocks of at most 2 KB per row; a ring slot
+// holds a block's two row pieces side by side.  Task t belongs to warp t mod (warps of the
+// grid), so at any moment the grid reads one window of the matrix.  A warp sums its blocks
+// in order and reduces with shuffles: every output has one fixed summation order.
 //
 // MoE stages: the router rows are a phase of the weight stream like the projections (a logit
 // per task, written to global memory); after one more grid barrier every CTA ranks all the
@@ -131,8 +132,8 @@ struct Shape {
   int N, Kp;          // rows (of the projection as computed); row stride in bytes (scales: Kp / 32)
   int T;              // tasks: N / R
   int klen;           // bytes of a row's K range
-  int R, P, PS;       // rows per task, pieces per row, piece bytes
-  int B;              // pieces per ring slot (several whole pieces share a slot)
+  int R, P, PS;       // rows per task (2), column blocks per task, bytes per row of a block
+  int B;              // column blocks per ring slot (several whole blocks share a slot)
   int mode;           // 0 plain rows; 1 rows of the selected experts (rps rows each); 2 piece j of a
                       // row from selected expert j (K gathered over the experts)
   int rps;
@@ -174,7 +175,7 @@ __device__ Shape shape_of(const MegaArgs& a, int ph) {
   Shape p;
   p.mode = 0;
   p.rps = 0;
-  p.R = (ph == kPhQKV || ph == kPhGU) ? 2 : 1;
+  p.R = 2;  // every task is a row pair: each load of the staged input serves both rows
   if (ph == kPhRouter && !moe) {  // dense stages: no router tasks
     p.N = p.T = 0;
     p.Kp = p.klen = p.PS = 256;
@@ -208,10 +209,10 @@ __device__ Shape shape_of(const MegaArgs& a, int ph) {
     p.klen = p.P * p.PS;
   } else {
     p.klen = w->Kp;
-    p.P = (w->Kp + kSlotQ - 1) / kSlotQ;
+    p.P = (w->Kp + kSlotQ / 2 - 1) / (kSlotQ / 2);
     p.PS = ((w->Kp / p.P + 255) / 256) * 256;
   }
-  p.B = (p.klen % p.PS == 0) ? max(1, kSlotQ / p.PS) : 1;
+  p.B = (p.klen % p.PS == 0) ? max(1, kSlotQ / (2 * p.PS)) : 1;
   return p;
 }
 
@@ -233,16 +234,10 @@ __device__ __forceinline__ Ph phase_of(const Ctx& c, int l, int ph) {
   return p;
 }
 
-// Row-in-task and piece of slot j of a task (R is 1 or 2, j < R * P).
-__device__ __forceinline__ void split_j(const Shape& p, int j, int& rr, int& pc) {
-  rr = j >= p.P;
-  pc = j - rr * p.P;
-}
-
-// Pieces of this warp's share of a phase from task t, piece j on, counted up to `cap`.
-__device__ __forceinline__ int pieces_upto(const Ctx& c, const Shape& p, int t, int j, int cap) {
-  int n = p.R * p.P - j;
-  for (int tt = t + c.GW; n < cap && tt < p.T; tt += c.GW) n += p.R * p.P;
+// Column blocks of this warp's share of a phase from task t, block j on, counted up to `cap`.
+__device__ __forceinline__ int blocks_upto(const Ctx& c, const Shape& p, int t, int j, int cap) {
+  int n = p.P - j;
+  for (int tt = t + c.GW; n < cap && tt < p.T; tt += c.GW) n += p.P;
   return min(n, cap);
 }
 
@@ -285,16 +280,16 @@ __device__ __forceinline__ void stream_normalise(const Ctx& c, Stream& s) {
 // Advance a cursor past its current slot (no copy).
 template <bool MOE>
 __device__ __forceinline__ void stream_step(const Ctx& c, Stream& s, const Shape& p) {
-  if (++s.j == p.R * p.P) {
+  if (++s.j == p.P) {
     s.j = 0;
     s.t += c.GW;
     stream_normalise<MOE>(c, s);
   }
 }
 
-// Issue the next slot of this warp's stream (if any) into the ring: one piece, or up to B
-// whole pieces of the same phase.  Slices of the selected experts wait until the routing of
-// their block is known.
+// Issue the next slot of this warp's stream (if any) into the ring: one column block of a
+// row pair (the two rows' pieces side by side), or up to B whole blocks of the same phase.
+// Slices of the selected experts wait until the routing of their block is known.
 template <bool MOE>
 __device__ __forceinline__ void stream_issue(const Ctx& c, Stream& s) {
   if (s.l >= c.a->nl) return;
@@ -303,50 +298,44 @@ __device__ __forceinline__ void stream_issue(const Ctx& c, Stream& s) {
   static_cast<Shape&>(p) = c.shape()[s.ph];
   p.q = static_cast<const uint8_t*>(c.wptr()[2 * c.warp]);
   p.s = static_cast<const uint16_t*>(c.wptr()[2 * c.warp + 1]);
-  if (p.B == 1 && p.mode == 0) {  // one piece of a plain row per slot
-    int rr, pc;
-    split_j(p, s.j, rr, pc);
-    const int row = s.t * p.R + rr;
-    const int off = pc * p.PS, bytes = min(p.PS, p.klen - off);
-    const int slot = s.issued % kDepth;
+  const int slot = s.issued % kDepth;
+  uint64_t* bar = c.bars() + c.warp * kDepth + slot;
+  unsigned char* dq = c.ringq() + (size_t)(c.warp * kDepth + slot) * kSlotQ;
+  unsigned char* ds = c.rings() + (size_t)(c.warp * kDepth + slot) * kSlotS;
+  if (p.B == 1 && p.mode == 0) {  // one block of two plain rows
+    const int row = 2 * s.t, off = s.j * p.PS, bytes = min(p.PS, p.klen - off);
     if (c.lane == 0) {
-      uint64_t* bar = c.bars() + c.warp * kDepth + slot;
-      fence_async_smem();
-      mbar_arrive_expect_tx(bar, (uint32_t)(bytes + bytes / 16));
-      bulk_g2s(c.ringq() + (size_t)(c.warp * kDepth + slot) * kSlotQ, p.q + (size_t)row * p.Kp + off, (uint32_t)bytes,
-               bar);
-      bulk_g2s(c.rings() + (size_t)(c.warp * kDepth + slot) * kSlotS, p.s + (size_t)row * (p.Kp / 32) + off / 32,
-               (uint32_t)(bytes / 16), bar);
+      const uint8_t* q = p.q + (size_t)row * p.Kp + off;
+      const uint16_t* sc = p.s + (size_t)row * (p.Kp / 32) + off / 32;
+      fence_async_smem();  // the slot's previous contents were read through the generic proxy
+      mbar_arrive_expect_tx(bar, (uint32_t)(2 * (bytes + bytes / 16)));
+      bulk_g2s(dq, q, (uint32_t)bytes, bar);
+      bulk_g2s(dq + p.PS, q + p.Kp, (uint32_t)bytes, bar);
+      bulk_g2s(ds, sc, (uint32_t)(bytes / 16), bar);
+      bulk_g2s(ds + p.PS / 16, sc + p.Kp / 32, (uint32_t)(bytes / 16), bar);
     }
     ++s.issued;
     stream_step<MOE>(c, s, p);
     return;
   }
-  const int nb = p.B == 1 ? 1 : pieces_upto(c, p, s.t, s.j, p.B);
-  const int slot = s.issued % kDepth;
-  uint64_t* bar = c.bars() + c.warp * kDepth + slot;
-  unsigned char* dq = c.ringq() + (size_t)(c.warp * kDepth + slot) * kSlotQ;
-  unsigned char* ds = c.rings() + (size_t)(c.warp * kDepth + slot) * kSlotS;
+  const int nb = p.B == 1 ? 1 : blocks_upto(c, p, s.t, s.j, p.B);
   if (c.lane == 0) {
-    fence_async_smem();  // the slot's previous contents were read through the generic proxy
-    int rr0, pc0;
-    split_j(p, s.j, rr0, pc0);
-    const int bytes0 = min(p.PS, p.klen - pc0 * p.PS);
-    mbar_arrive_expect_tx(bar, (uint32_t)(nb == 1 ? bytes0 + bytes0 / 16 : nb * (p.PS + p.PS / 16)));
+    fence_async_smem();
+    const int bytes0 = min(p.PS, p.klen - s.j * p.PS);
+    mbar_arrive_expect_tx(bar, (uint32_t)(nb == 1 ? 2 * (bytes0 + bytes0 / 16) : nb * 2 * (p.PS + p.PS / 16)));
   }
   for (int u = 0; u < nb; ++u) {
-    int rr, pc;
-    split_j(p, s.j, rr, pc);
-    const int row = s.t * p.R + rr;
-    const int bytes = min(p.PS, p.klen - pc * p.PS);
+    const int pc = s.j, row = 2 * s.t, bytes = min(p.PS, p.klen - pc * p.PS);
     if (c.lane == 0) {
-      const uint8_t* q;
-      const uint16_t* sc;
-      piece_src<MOE>(c, p, row, pc, q, sc);
-      bulk_g2s(dq + u * p.PS, q, (uint32_t)bytes, bar);
-      bulk_g2s(ds + u * (p.PS / 16), sc, (uint32_t)(bytes / 16), bar);
+      for (int rr = 0; rr < 2; ++rr) {
+        const uint8_t* q;
+        const uint16_t* sc;
+        piece_src<MOE>(c, p, row + rr, pc, q, sc);
+        bulk_g2s(dq + (2 * u + rr) * p.PS, q, (uint32_t)bytes, bar);
+        bulk_g2s(ds + (2 * u + rr) * (p.PS / 16), sc, (uint32_t)(bytes / 16), bar);
+      }
     }
-    if (u + 1 < nb && ++s.j == p.R * p.P) {  // stays inside the phase: nb counted its pieces left
+    if (u + 1 < nb && ++s.j == p.P) {  // stays inside the phase: nb counted its blocks left
       s.j = 0;
       s.t += c.GW;
     }
@@ -490,23 +479,23 @@ __device__ void stage_input(const Ctx& c, const float* x, int K, int Kp, const f
   __syncthreads();
 }
 
-// One projection of block l: consume this warp's tasks from the ring, refill behind.
-// Returns false (for the whole warp) after a timed-out wait (error set, copies drained);
-// the caller makes the outcome CTA-uniform.  BATCH: several pieces share a ring slot.
+// One projection of block l: consume this warp's tasks (row pairs) from the ring, refill
+// behind; both rows of a column block are summed in one pass, so each chunk of the staged
+// input is read once for the pair.  Returns false (for the whole warp) after a timed-out
+// wait (error set, copies drained); the caller makes the outcome CTA-uniform.  BATCH:
+// several column blocks share a ring slot.
 template <bool BATCH, bool MOE>
 __device__ bool gemv_phase_t(const Ctx& c, Stream& s, int l, int ph, const float* xs, const float* xc,
                              const float* xraw, int pos, int sid) {
   const MegaArgs& a = *c.a;
   const Ph p = phase_of<MOE>(c, l, ph);
   constexpr bool moe = MOE;
-  const int T = p.T, nsl = p.R * p.P, t0 = c.gw, dt = c.GW;
-  int left = BATCH && t0 < T ? ((T - 1 - t0) / dt + 1) * nsl : 0;  // this warp's pieces of the phase
-  int uin = 0, ucap = 1;  // position in, and pieces of, the current slot
+  const int T = p.T, P = p.P, t0 = c.gw, dt = c.GW;
+  int left = BATCH && t0 < T ? ((T - 1 - t0) / dt + 1) * P : 0;  // this warp's blocks of the phase
+  int uin = 0, ucap = 1;  // position in, and blocks of, the current slot
   for (int t = t0; t < T; t += dt) {
     float acc0 = 0.f, acc1 = 0.f;
-    for (int j = 0; j < nsl; ++j) {
-      int rr, pc;
-      split_j(p, j, rr, pc);
+    for (int pc = 0; pc < P; ++pc) {
       const int off = pc * p.PS, bytes = min(p.PS, p.klen - off);
       const int slot = s.consumed % kDepth;
       if (!BATCH || uin == 0) {
@@ -519,9 +508,10 @@ __device__ bool gemv_phase_t(const Ctx& c, Stream& s, int l, int ph, const float
         }
       }
       const int u = BATCH ? uin : 0;
-      const unsigned char* sq = c.ringq() + (size_t)(c.warp * kDepth + slot) * kSlotQ + u * p.PS;
-      const unsigned char* ssc = c.rings() + (size_t)(c.warp * kDepth + slot) * kSlotS + u * (p.PS / 16);
-      float acc = rr ? acc1 : acc0;
+      const unsigned char* q0 = c.ringq() + (size_t)(c.warp * kDepth + slot) * kSlotQ + 2 * u * p.PS;
+      const unsigned char* q1 = q0 + p.PS;
+      const unsigned char* s0 = c.rings() + (size_t)(c.warp * kDepth + slot) * kSlotS + 2 * u * (p.PS / 16);
+      const unsigned char* s1 = s0 + p.PS / 16;
       const int nch = bytes >> 4, cb = off >> 4;
 #pragma unroll 2
       for (int cl = c.lane; cl < nch; cl += 32) {
@@ -529,14 +519,14 @@ __device__ bool gemv_phase_t(const Ctx& c, Stream& s, int l, int ph, const float
         const int sw = (ch >> 1) & 3;
         const float4* xp = reinterpret_cast<const float4*>(xs + ch * 16);
         const float4 x0 = xp[0 ^ sw], x1 = xp[1 ^ sw], x2 = xp[2 ^ sw], x3 = xp[3 ^ sw];
-        const uint4 w = *reinterpret_cast<const uint4*>(sq + cl * 16);
-        const float scl = h2f_bits(*reinterpret_cast<const uint16_t*>(ssc + (cl >> 1) * 2));
-        acc = fmaf(scl, fmaf(dot16_u8(w, x0, x1, x2, x3), kPScale, -128.0f * xc[ch]), acc);
+        const float corr = -128.0f * xc[ch];
+        const uint4 w0 = *reinterpret_cast<const uint4*>(q0 + cl * 16);
+        const uint4 w1 = *reinterpret_cast<const uint4*>(q1 + cl * 16);
+        const float f0 = h2f_bits(*reinterpret_cast<const uint16_t*>(s0 + (cl >> 1) * 2));
+        const float f1 = h2f_bits(*reinterpret_cast<const uint16_t*>(s1 + (cl >> 1) * 2));
+        acc0 = fmaf(f0, fmaf(dot16_u8(w0, x0, x1, x2, x3), kPScale, corr), acc0);
+        acc1 = fmaf(f1, fmaf(dot16_u8(w1, x0, x1, x2, x3), kPScale, corr), acc1);
       }
-      if (rr)
-        acc1 = acc;
-      else
-        acc0 = acc;
       if (BATCH) --left;
       if (!BATCH || ++uin == ucap) {  // the slot is consumed: refill it
         uin = 0;
@@ -546,7 +536,7 @@ __device__ bool gemv_phase_t(const Ctx& c, Stream& s, int l, int ph, const float
       }
     }
     acc0 = warp_sum(acc0);
-    if (p.R == 2) acc1 = warp_sum(acc1);
+    acc1 = warp_sum(acc1);
     if (c.lane != 0) continue;
     const MegaLayer& L = a.layers[l];
     if (ph == kPhQKV) {  // rows (2t, 2t+1) are dims (i, i + D/2) of one head: RoPE, then q or fp16 K/V
@@ -571,9 +561,11 @@ __device__ bool gemv_phase_t(const Ctx& c, Stream& s, int l, int ph, const float
         }
       }
     } else if (ph == kPhO) {
-      a.x1[t] = __fadd_rn(xraw[t], acc0);
+      a.x1[2 * t] = __fadd_rn(xraw[2 * t], acc0);
+      a.x1[2 * t + 1] = __fadd_rn(xraw[2 * t + 1], acc1);
     } else if (MOE && ph == kPhRouter) {
-      a.logits[t] = acc0;
+      a.logits[2 * t] = acc0;
+      a.logits[2 * t + 1] = acc1;
     } else if (ph == kPhGU) {
       if (moe) {  // pair t: expert slot t / EF, unit t % EF; scaled by the routing weight
         const int slot = t / a.EF, i = t - slot * a.EF;
@@ -582,7 +574,8 @@ __device__ bool gemv_phase_t(const Ctx& c, Stream& s, int l, int ph, const float
         a.abuf[t] = silu(acc0) * acc1;
       }
     } else {
-      a.hout[t] = __fadd_rn(xraw[t], acc0);
+      a.hout[2 * t] = __fadd_rn(xraw[2 * t], acc0);
+      a.hout[2 * t + 1] = __fadd_rn(xraw[2 * t + 1], acc1);
     }
   }
   return true;
