@@ -47,10 +47,11 @@ CONTEXT = 2048
 PREFILL = dict(seqs=4, prompt=512, min_tokens=64,
                name="dense 8B-shape prefill, 2 stages 16/16, 4 prompts x 512 tokens in one step, "
                     "bf16 tcgen05 GEMMs with int8 block-32 weights dequantised in shared memory")
-# DRAM bytes (read + write) per launch of the dominant kernel: the persistent stage decode of
-# the dense workload, from an ncu capture of one block in the same launch configuration scaled
-# by the 16 blocks of a launch (profiles/mega_decode_small.md).
-TRAFFIC = {1: 3_903_004_672}
+# DRAM bytes (read + write) per launch of the dominant kernel, the persistent stage decode:
+# an ncu capture of one block in the same launch configuration (the bytes of a block do not
+# depend on its index), scaled by the blocks of a launch -- 16 for the dense workload, 20 on
+# average for the MoE one (stages of 21 and 19 blocks).
+TRAFFIC = {1: 3_900_780_544, 2: 1_394_913_280}
 
 
 def dist_env():
@@ -313,7 +314,7 @@ def run_gpu(args):
         "hbm_gbs_achieved": round(gbs, 1),
         "roofline": {"bound": "hbm", "achieved": round(k_gbs, 1) if k_gbs else None, "peak": peak, "unit": "GB/s",
                      "frac": round(k_gbs / peak, 4) if (peak and k_gbs) else None,
-                     "traffic": TRAFFIC.get(args.config) if not args.layers else None,
+                     "traffic": TRAFFIC.get(args.config) if not (args.layers or args.context) else None,
                      "kernel": kernel,
                      "bytes_per_launch": round(k_bytes), "mean_launch_us": round(k_us, 3), "launches_timed": k_n,
                      "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs)" if peak else "fallback"},
