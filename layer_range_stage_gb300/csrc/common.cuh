@@ -95,6 +95,11 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
                : "memory");
 }
 
+// Fetch the 128-byte line holding p into L2, marked to be evicted last.
+__device__ __forceinline__ void prefetch_l2_last(const void* p) {
+  asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(p));
+}
+
 // Orders this thread's generic-proxy shared-memory accesses before its later async-proxy
 // ones (bulk copies, tensor-core operand reads).
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }

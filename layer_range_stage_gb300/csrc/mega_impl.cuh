@@ -959,6 +959,12 @@ __global__ void __launch_bounds__(kMT, 1) mega_decode_kernel(const MegaArgs a) {
         const int K = ph == kPhO ? a.Hq * a.D : ph == kPhDown ? a.F : a.H;
         const int Kp = ph == kPhO ? KpQ : ph == kPhDown ? KpF : KpH;
         const float* gamma = ph == kPhQKV ? L.attn_norm : norm2 ? L.ffn_norm : nullptr;
+        // the gamma of the next normalising stage is fetched into L2 one phase ahead (the weight
+        // stream evicts it between blocks): one 128-byte line per CTA
+        if (threadIdx.x == 0 && (ph == kPhO || ph == kPhDown)) {
+          const float* g = ph == kPhO ? L.ffn_norm : (l + 1 < a.nl ? a.layers[l + 1].attn_norm : nullptr);
+          for (int i = blockIdx.x * 32; g && i < a.H; i += gridDim.x * 32) prefetch_l2_last(g + i);
+        }
         stage_input(c, in, K, Kp, gamma, a.eps, xs, xc, (ph == kPhO || ph == kPhDown) ? nullptr : xraw);
       }
       ok = __syncthreads_and(gemv_phase<MOE>(c, s, l, ph, xs, xc, xraw, pos, sid));
