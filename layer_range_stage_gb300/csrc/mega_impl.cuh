@@ -822,7 +822,8 @@ __device__ bool attention_phase(const Ctx& c, int l, unsigned char* area, unsign
       po[i] = v;
     }
     if (tid < G) a.part_ml[((size_t)kvh * G + tid) * nch + chunk] = make_float2(st_m[tid], st_l[tid]);
-    __threadfence();
+    // the CTA barrier orders every thread's partial writes before thread 0's release (cumulative
+    // at GPU scope), which the merging CTAs acquire
     __syncthreads();
     if (tid == 0) red_release_add(a.bar + 2 + kvh, 1u);
   }
