@@ -232,7 +232,9 @@ STAGE_API int stage_pipeline_create(stage_t* stages, int n_stages, stage_pipelin
 /* One step of all stages: prefill (is_prefill = 1) or decode, then the readout of
  * rows row_index_host[0..n_rows) on the last stage.  logits_out (device, may be
  * NULL), next_tokens_host (host int32 [n_rows], may be NULL: the greedy tokens,
- * read back after the step).  Commits every stage to the new lengths on success. */
+ * read back after the step, with every stage's error word).  Every stage's call is
+ * validated and its inputs copied in before the first launch, so a call that fails
+ * validation runs no stage.  Commits every stage to the new lengths on success. */
 STAGE_API int stage_pipeline_step(stage_pipeline_t p, int is_prefill, int n_tokens, const int32_t* seq_ids_host,
                         const int32_t* positions_host, const int32_t* tokens_host, int n_rows,
                         const int32_t* row_index_host, float* logits_out, int32_t* next_tokens_host);

@@ -196,7 +196,8 @@ struct stage {
   std::vector<cudaEvent_t> tev;  // measurement: event pair around each FFN up-projection launch
   bool timing = false;
   int timed_pairs = 0;           // event pairs recorded by the last forward
-  int32_t* h_stage = nullptr;  // pinned host staging [4][max_tokens]
+  int32_t* h_stage = nullptr;  // pinned host staging [4][max_tokens] (seq, pos, tok, rows), then
+                               // [max_tokens] read-back tokens and the read-back error word
   cudaEvent_t staged = nullptr;  // recorded after the last copy out of h_stage
   std::vector<int> committed, pending;
   int last_n = 0;
@@ -771,18 +772,19 @@ int validate_call(stage* st, bool decode, int n, const int32_t* seq, const int32
   return STAGE_OK;
 }
 
-int run_forward(stage* st, bool decode, int n, const int32_t* seq, const int32_t* pos, const int32_t* tok,
-                const stage_act* hin, const stage_act* hout) {
+// Validate a forward call and copy its arrays in (through pinned memory into fixed device
+// buffers, on the stage's stream); *max_len receives the longest context of the call.
+int stage_call_inputs(stage* st, bool decode, int n, const int32_t* seq, const int32_t* pos, const int32_t* tok,
+                      const stage_act* hin, const stage_act* hout, int* max_len) {
   if (!weights_ready(st)) return set_err(st, STAGE_E_STATE, "weights not loaded");
-  int max_len = 0, rc;
-  if ((rc = validate_call(st, decode, n, seq, pos, tok, hin, hout, &max_len))) return rc;
+  int rc;
+  if ((rc = validate_call(st, decode, n, seq, pos, tok, hin, hout, max_len))) return rc;
   if (st->fail_next) {
     const int code = st->fail_next;
     st->fail_next = 0;
     return set_err(st, code, "injected failure");
   }
-  // stage the call's arrays through pinned memory into fixed device buffers; the previous
-  // copies out of the staging area must have finished before it is overwritten
+  // the previous copies out of the staging area must have finished before it is overwritten
   const int T = st->cfg.max_tokens;
   cudaError_t e = cudaEventSynchronize(st->staged);
   if (e != cudaSuccess) return cuda_err(st, e, "staging");
@@ -794,12 +796,25 @@ int run_forward(stage* st, bool decode, int n, const int32_t* seq, const int32_t
   if (e == cudaSuccess && tok) e = cudaMemcpyAsync(st->d_tok, st->h_stage + 2 * T, n * 4, cudaMemcpyHostToDevice, st->stream);
   if (e == cudaSuccess) e = cudaEventRecord(st->staged, st->stream);
   if (e != cudaSuccess) return cuda_err(st, e, "stage inputs");
+  return STAGE_OK;
+}
+
+// The launches of a forward call whose inputs are in (stage_call_inputs).
+int stage_call_launch(stage* st, bool decode, int n, const int32_t* seq, const int32_t* pos, const stage_act* hin,
+                      const stage_act* hout, int max_len) {
   st->call_prefill = !decode;
-  rc = forward_dev(st, n, st->d_seq, st->d_pos, st->d_tok, hin ? hin->data : nullptr, hout->data,
-                   attn_chunks(st, n, max_len), st->stream);
+  const int rc = forward_dev(st, n, st->d_seq, st->d_pos, st->d_tok, hin ? hin->data : nullptr, hout->data,
+                             attn_chunks(st, n, max_len), st->stream);
   if (rc) return rc;
   for (int i = 0; i < n; ++i) st->pending[seq[i]] = std::max(st->pending[seq[i]], pos[i] + 1);
   return STAGE_OK;
+}
+
+int run_forward(stage* st, bool decode, int n, const int32_t* seq, const int32_t* pos, const int32_t* tok,
+                const stage_act* hin, const stage_act* hout) {
+  int max_len = 0;
+  const int rc = stage_call_inputs(st, decode, n, seq, pos, tok, hin, hout, &max_len);
+  return rc ? rc : stage_call_launch(st, decode, n, seq, pos, hin, hout, max_len);
 }
 
 }  // namespace
@@ -902,7 +917,7 @@ int stage_create(const stage_model_cfg* cfg, stage_layer_range range, const stag
                                    moe ? cfg->top_k * kpad(cfg->expert_ffn) : cfg->ffn, cfg->head_dim,
                                    cfg->n_q_heads / cfg->n_kv_heads, cfg->n_experts, cfg->top_k);
   }
-  if (e == cudaSuccess) e = cudaMallocHost(&st->h_stage, (size_t)4 * cfg->max_tokens * 4);
+  if (e == cudaSuccess) e = cudaMallocHost(&st->h_stage, ((size_t)5 * cfg->max_tokens + 16) * 4);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&st->staged, cudaEventDisableTiming);
   if (e != cudaSuccess) {
     g_create_error = std::string("stage setup: ") + cudaGetErrorString(e);
@@ -1214,16 +1229,25 @@ int stage_pipeline_step(stage_pipeline_t p, int is_prefill, int n_tokens, const 
   const int H = p->stages[0]->cfg.hidden;
   if (n_tokens <= 0 || n_tokens > p->max_tokens) return pset(p, STAGE_E_INVALID, "n_tokens %d", n_tokens);
   stage_act act{p->hbuf, n_tokens, H};
-  // run every stage; nothing is committed unless all succeed
-  for (size_t i = 0; i < p->stages.size(); ++i) {
+  // every stage's inputs are validated and copied in before the first launch (no copy sits
+  // between two stages' kernels on the stream); nothing is committed unless all succeed
+  const size_t ns = p->stages.size();
+  std::vector<int> max_len(ns, 0);
+  for (size_t i = 0; i < ns; ++i) {
     stage* st = p->stages[i];
-    const int rc = run_forward(st, !is_prefill, n_tokens, seq_ids_host, positions_host, i == 0 ? tokens_host : nullptr,
-                               i == 0 ? nullptr : &act, &act);
+    const int rc = stage_call_inputs(st, !is_prefill, n_tokens, seq_ids_host, positions_host,
+                                     i == 0 ? tokens_host : nullptr, i == 0 ? nullptr : &act, &act, &max_len[i]);
+    if (rc) return pset(p, rc, "stage %zu [%d, %d): %s", i, st->begin, st->end, st->err.c_str());
+  }
+  for (size_t i = 0; i < ns; ++i) {
+    stage* st = p->stages[i];
+    const int rc = stage_call_launch(st, !is_prefill, n_tokens, seq_ids_host, positions_host, i == 0 ? nullptr : &act,
+                                     &act, max_len[i]);
     if (rc) {
       for (stage* s : p->stages) std::copy(s->committed.begin(), s->committed.end(), s->pending.begin());
       return pset(p, rc, "stage %zu [%d, %d): %s", i, st->begin, st->end, st->err.c_str());
     }
-    if (i + 1 < p->stages.size()) {
+    if (i + 1 < ns) {
       p->calls[i] += 1;
       p->bytes[i] += (int64_t)n_tokens * H * 4;
     }
@@ -1244,11 +1268,23 @@ int stage_pipeline_step(stage_pipeline_t p, int is_prefill, int n_tokens, const 
     int rc = logits_dev(last, n_rows, last->d_rows, logits_out, nullptr, last->stream);
     if (rc) return pset(p, rc, "%s", last->err.c_str());
     if (next_tokens_host) {
-      e = cudaMemcpyAsync(next_tokens_host, last->argmax, n_rows * 4, cudaMemcpyDeviceToHost, last->stream);
+      // the tokens and every stage's error word come back through pinned memory, then one wait
+      const int T = last->cfg.max_tokens;
+      int32_t* h_tok = last->h_stage + 4 * T;
+      e = cudaMemcpyAsync(h_tok, last->argmax, n_rows * 4, cudaMemcpyDeviceToHost, last->stream);
+      for (stage* s2 : p->stages)
+        if (e == cudaSuccess)
+          e = cudaMemcpyAsync(s2->h_stage + 5 * s2->cfg.max_tokens, s2->err_word, 4, cudaMemcpyDeviceToHost,
+                              last->stream);
       if (e == cudaSuccess) e = cudaStreamSynchronize(last->stream);
       if (e != cudaSuccess) return pset(p, STAGE_E_CUDA, "tokens: %s", cudaGetErrorString(e));
       for (stage* s2 : p->stages)
-        if (check_device_error(s2)) return pset(p, STAGE_E_CUDA, "%s", s2->err.c_str());
+        if (s2->h_stage[5 * s2->cfg.max_tokens] != 0) {
+          cudaMemset(s2->err_word, 0, 4);
+          set_err(s2, STAGE_E_CUDA, "a kernel's bounded wait timed out; its outputs are invalid");
+          return pset(p, STAGE_E_CUDA, "%s", s2->err.c_str());
+        }
+      std::memcpy(next_tokens_host, h_tok, n_rows * 4);
     }
   }
   // joint publication

@@ -281,5 +281,6 @@ def test_injected_failure_publishes_nothing_and_retry_is_identical(cuda):
         gp.step(True, np.zeros(10), np.arange(10), prompt, rows=[9], logits_out=lg)
         assert np.array_equal(ref, lg.cpu().numpy())
         calls, nbytes = gp.handoff_stats(0)
-        # five handoffs: the failed step's stage 0 still handed its activation over
-        assert calls == 5 and nbytes == (10 + 1 + 1 + 1 + 10) * model.hidden * 4
+        # four handoffs: the failed step ran no stage (every stage's call is validated
+        # before the first launch)
+        assert calls == 4 and nbytes == (10 + 1 + 1 + 10) * model.hidden * 4
