@@ -132,6 +132,22 @@ typedef struct {
  * device layout), KV cache, RoPE table and workspace.  0 if cfg/range are invalid. */
 STAGE_API size_t stage_required_bytes(const stage_model_cfg* cfg, stage_layer_range range);
 
+/* Placement of the model's blocks over n_devices stages (stage k on device k, in order),
+ * from the device budgets alone: contiguous ranges, at least one block per stage, and a
+ * placement is legal only if every stage's stage_required_bytes fits its own device's
+ * budget -- never the summed memory (RFC page, "Heterogeneous GPUs"; TensorSharp page,
+ * "Layer split": balance estimated resident bytes, contiguous layers, at least one layer
+ * per selected GPU).  Among the legal placements it returns one that minimises the largest
+ * required / budget ratio over the stages (for equal budgets: the most balanced resident
+ * bytes), the earliest cut on ties.  Pure host code, no device access.
+ * device_budgets: host [n_devices] usable bytes per device.  bounds_out: host int32
+ * [n_devices + 1], 0 = b[0] < b[1] < ... < b[n] = n_layers; stage k owns [b[k], b[k+1]).
+ * required_out: host [n_devices] or NULL, each stage's stage_required_bytes.
+ * Returns STAGE_OK, STAGE_E_INVALID (bad cfg or pointers, n_devices outside [1, n_layers]),
+ * or STAGE_E_DOES_NOT_FIT (no legal placement). */
+STAGE_API int stage_plan_placement(const stage_model_cfg* cfg, int n_devices, const size_t* device_budgets,
+                                   int32_t* bounds_out, size_t* required_out);
+
 /* Create a stage on the current CUDA device.  Fails with STAGE_E_DOES_NOT_FIT --
  * before allocating anything -- when stage_required_bytes exceeds
  * device_budget_bytes or the device's free memory (the per-device fit rule of the

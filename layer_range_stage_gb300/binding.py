@@ -69,6 +69,8 @@ _lib = None
 
 _SIGS = {
     "stage_required_bytes": (C.c_size_t, [C.POINTER(stage_model_cfg), stage_layer_range]),
+    "stage_plan_placement": (C.c_int, [C.POINTER(stage_model_cfg), C.c_int, C.POINTER(C.c_size_t),
+                                       C.POINTER(C.c_int32), C.POINTER(C.c_size_t)]),
     "stage_create": (C.c_int, [C.POINTER(stage_model_cfg), stage_layer_range, C.c_void_p, C.c_size_t, C.c_void_p,
                                C.POINTER(C.c_void_p)]),
     "stage_load_layer": (C.c_int, [C.c_void_p, C.c_int, C.c_void_p]),
@@ -225,6 +227,19 @@ def _stream(stream) -> Optional[int]:
 
 def stage_required_bytes(cfg: stage_model_cfg, begin: int, end: int) -> int:
     return int(lib().stage_required_bytes(C.byref(cfg), stage_layer_range(begin, end)))
+
+
+def stage_plan_placement(cfg: stage_model_cfg, budgets) -> tuple:
+    """Block bounds [n_devices + 1] and each stage's required bytes for the given per-device
+    budgets (see include/stage.h); raises StageError (DoesNotFit when no placement is legal)."""
+    n = len(budgets)
+    bud = (C.c_size_t * max(n, 1))(*[int(b) for b in budgets])
+    bounds = (C.c_int32 * (n + 1))()
+    req = (C.c_size_t * max(n, 1))()
+    rc = lib().stage_plan_placement(C.byref(cfg), n, bud, bounds, req)
+    if rc != STAGE_OK:
+        raise StageError(rc, "no legal placement" if rc == STAGE_E_DOES_NOT_FIT else "invalid placement request")
+    return [int(b) for b in bounds], [int(r) for r in req[:n]]
 
 
 def stage_create(cfg: stage_model_cfg, begin: int, end: int, weights=None, budget: Optional[int] = None, stream=None):

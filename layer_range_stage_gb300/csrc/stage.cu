@@ -16,6 +16,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <limits>
 #include <mutex>
 #include <new>
 #include <string>
@@ -826,6 +827,47 @@ extern "C" {
 size_t stage_required_bytes(const stage_model_cfg* cfg, stage_layer_range range) {
   if (!cfg_valid(cfg, range, nullptr)) return 0;
   return plan_bytes(*cfg, range.begin, range.end);
+}
+
+int stage_plan_placement(const stage_model_cfg* cfg, int n_devices, const size_t* device_budgets,
+                         int32_t* bounds_out, size_t* required_out) {
+  if (!cfg || !device_budgets || !bounds_out) return STAGE_E_INVALID;
+  const int n = cfg->n_layers, S = n_devices;
+  if (S < 1 || S > n || !cfg_valid(cfg, stage_layer_range{0, n}, nullptr)) return STAGE_E_INVALID;
+  // req[a][b]: bytes of a stage owning [a, b) (endpoints, KV and workspace included)
+  std::vector<size_t> req((size_t)(n + 1) * (n + 1), 0);
+  for (int a = 0; a < n; ++a)
+    for (int b = a + 1; b <= n; ++b) req[(size_t)a * (n + 1) + b] = plan_bytes(*cfg, a, b);
+  // best[k][b]: the smallest achievable max ratio for stages 0..k-1 covering [0, b); cut[k][b]
+  // the start of stage k-1 there.  Ratios compare exactly as required * (1 / budget) in double.
+  const double inf = std::numeric_limits<double>::infinity();
+  std::vector<double> best((size_t)(S + 1) * (n + 1), inf);
+  std::vector<int> cut((size_t)(S + 1) * (n + 1), -1);
+  best[0] = 0.0;
+  for (int k = 1; k <= S; ++k) {
+    const size_t budget = device_budgets[k - 1];
+    for (int b = k; b <= n - (S - k); ++b) {
+      for (int a = k - 1; a < b; ++a) {
+        const double prev = best[(size_t)(k - 1) * (n + 1) + a];
+        const size_t r = req[(size_t)a * (n + 1) + b];
+        if (prev == inf || r > budget) continue;
+        const double cost = std::max(prev, (double)r / (double)std::max<size_t>(budget, 1));
+        if (cost < best[(size_t)k * (n + 1) + b]) {
+          best[(size_t)k * (n + 1) + b] = cost;
+          cut[(size_t)k * (n + 1) + b] = a;
+        }
+      }
+    }
+  }
+  if (best[(size_t)S * (n + 1) + n] == inf) return STAGE_E_DOES_NOT_FIT;
+  bounds_out[S] = n;
+  for (int k = S, b = n; k >= 1; --k) {
+    const int a = cut[(size_t)k * (n + 1) + b];
+    bounds_out[k - 1] = a;
+    if (required_out) required_out[k - 1] = req[(size_t)a * (n + 1) + b];
+    b = a;
+  }
+  return STAGE_OK;
 }
 
 int stage_create(const stage_model_cfg* cfg, stage_layer_range range, const stage_weights* weights,
