@@ -649,14 +649,24 @@ cudaError_t launch_attn_decode(const AttnArgs& a, cudaStream_t st) {
 // Embedding row gather: x[t][k] = scale[tok][k/32] * q[tok][k] (exact in float32).  The
 // table is stored biased like every weight matrix (byte = q + 128).
 
+// One token per CTA; a thread dequantises 16 consecutive weights from one 16-byte load.
 __global__ void embed_kernel(const DevQ8 tab, const int* tok, float* out, int ldo) {
   pdl_trigger();
   pdl_wait();
   const int t = blockIdx.x, row = tok[t];
   const uint8_t* q = tab.q + (size_t)row * tab.Kp;
   const uint16_t* s = tab.s + (size_t)row * (tab.Kp >> 5);
-  for (int k = threadIdx.x; k < tab.K; k += blockDim.x)
-    out[(size_t)t * ldo + k] = h2f_bits(s[k >> 5]) * (float)((int)q[k] - 128);
+  float* o = out + (size_t)t * ldo;
+  for (int k0 = threadIdx.x * 16; k0 < tab.K; k0 += blockDim.x * 16) {
+    const uint4 w = __ldg(reinterpret_cast<const uint4*>(q + k0));
+    const float sc = h2f_bits(s[k0 >> 5]);
+    const uint32_t words[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int k = k0 + j;
+      if (k < tab.K) o[k] = sc * (float)((int)((words[j >> 2] >> (8 * (j & 3))) & 0xFFu) - 128);
+    }
+  }
 }
 
 cudaError_t launch_embed(const DevQ8& table, const int* tok, int ntok, float* out, int ldo, cudaStream_t st) {
@@ -669,36 +679,46 @@ cudaError_t launch_embed(const DevQ8& table, const int* tok, int ntok, float* ou
 // stage's feature buffer and to the caller's hidden_out.  Same reduction order as the GEMV
 // prologue.
 
-__global__ void final_norm_kernel(const float* x, int ldx, const float* gamma, float eps, int H, float* feat,
-                                  float* out, int ldo) {
-  __shared__ float nrm[8];
+// One token per CTA of kFinalNormThreads; float4 accesses (H, ldx and ldo are multiples of 4).
+constexpr int kFinalNormThreads = 1024;
+__global__ void __launch_bounds__(kFinalNormThreads) final_norm_kernel(const float* x, int ldx, const float* gamma,
+                                                                      float eps, int H, float* feat, float* out,
+                                                                      int ldo) {
+  __shared__ float nrm[kFinalNormThreads / 32];
   pdl_trigger();
   pdl_wait();
-  const int t = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const float* xr = x + (size_t)t * ldx;
+  const int t = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, H4 = H >> 2;
+  const float4* xr = reinterpret_cast<const float4*>(x + (size_t)t * ldx);
   float ss = 0.f;
-  for (int k = tid; k < H; k += 256) {
-    const float v = xr[k];
-    ss = fmaf(v, v, ss);
+  for (int k = tid; k < H4; k += kFinalNormThreads) {
+    const float4 v = xr[k];
+    ss = fmaf(v.x, v.x, ss);
+    ss = fmaf(v.y, v.y, ss);
+    ss = fmaf(v.z, v.z, ss);
+    ss = fmaf(v.w, v.w, ss);
   }
   ss = warp_sum(ss);
   if (lane == 0) nrm[warp] = ss;
   __syncthreads();
   float tot = 0.f;
 #pragma unroll
-  for (int w = 0; w < 8; ++w) tot += nrm[w];
+  for (int w = 0; w < kFinalNormThreads / 32; ++w) tot += nrm[w];
   const float rinv = 1.0f / sqrtf(tot / (float)H + eps);
-  for (int k = tid; k < H; k += 256) {
-    const float f = xr[k] * rinv * gamma[k];
-    feat[(size_t)t * H + k] = f;
-    out[(size_t)t * ldo + k] = f;
+  const float4* g4 = reinterpret_cast<const float4*>(gamma);
+  for (int k = tid; k < H4; k += kFinalNormThreads) {
+    const float4 v = xr[k], g = g4[k];
+    const float4 f = make_float4(v.x * rinv * g.x, v.y * rinv * g.y, v.z * rinv * g.z, v.w * rinv * g.w);
+    reinterpret_cast<float4*>(feat + (size_t)t * H)[k] = f;
+    reinterpret_cast<float4*>(out + (size_t)t * ldo)[k] = f;
   }
 }
 
 cudaError_t launch_final_norm(const float* x, int ldx, const float* gamma, float eps, int H, int ntok, float* feat,
                               float* out, int ldo, cudaStream_t st) {
   if (ntok <= 0) return cudaSuccess;
-  return launch_k(final_norm_kernel, dim3(ntok), dim3(256), 0, st, x, ldx, gamma, eps, H, feat, out, ldo);
+  if ((H | ldx | ldo) & 3) return cudaErrorInvalidValue;
+  return launch_k(final_norm_kernel, dim3(ntok), dim3(kFinalNormThreads), 0, st, x, ldx, gamma, eps, H, feat, out,
+                  ldo);
 }
 
 // ------------------------------------------------------------------------------------------
@@ -720,7 +740,19 @@ __global__ void argmax_kernel(const float* logits, int V, int* out) {
   const float* lg = logits + (size_t)r * V;
   float v = -INFINITY;
   int idx = INT_MAX;
-  for (int k = tid; k < V; k += blockDim.x) better(v, idx, lg[k], k);
+  // float4 loads, several in flight per thread (rows are 16-byte aligned when V % 4 == 0); the
+  // comparison keeps the largest value and the lowest index on ties whatever the visit order
+  const int V4 = (V & 3) ? 0 : V >> 2;
+  const float4* lg4 = reinterpret_cast<const float4*>(lg);
+#pragma unroll 8
+  for (int k = tid; k < V4; k += blockDim.x) {
+    const float4 q = __ldcg(lg4 + k);
+    better(v, idx, q.x, 4 * k);
+    better(v, idx, q.y, 4 * k + 1);
+    better(v, idx, q.z, 4 * k + 2);
+    better(v, idx, q.w, 4 * k + 3);
+  }
+  for (int k = 4 * V4 + tid; k < V; k += blockDim.x) better(v, idx, lg[k], k);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     const float v2 = __shfl_xor_sync(0xffffffffu, v, o);
