@@ -51,7 +51,7 @@ PREFILL = dict(seqs=4, prompt=512, min_tokens=64,
 # an ncu capture of one block in the same launch configuration (the bytes of a block do not
 # depend on its index), scaled by the blocks of a launch -- 16 for the dense workload, 20 on
 # average for the MoE one (stages of 21 and 19 blocks).
-TRAFFIC = {1: 3_900_780_544, 2: 1_394_913_280}
+TRAFFIC = {1: 3_904_675_840, 2: 1_395_256_320}
 
 
 def dist_env():
