@@ -20,7 +20,7 @@ bool mega_supported(int H, int q_dim, int F, int head_dim, int group, int n_expe
   if (q_dim / head_dim / group > 62) return false;  // per-KV-head counters in the 64-word barrier block
   if ((H & 3) || (q_dim & 3) || (F & 3)) return false;
   const int Kx = std::max(pad256(H), std::max(pad256(q_dim), pad256(F)));
-  if (Kx > kMaxKp || (Kx + kSlotQ / 2 - 1) / (kSlotQ / 2) > kMaxPieces) return false;
+  if (Kx > kMaxKp || (Kx + kSlotQ / 2 - 1) / (kSlotQ / 2) > kMaxBlocks) return false;
   return mega_smem(H, q_dim, F, head_dim, group) <= kMaxSmem;
 }
 

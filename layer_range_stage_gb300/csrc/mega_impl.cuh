@@ -59,7 +59,7 @@ constexpr int kSlotS = kSlotQ / 16;           // scale bytes per slot (one fp16 
 template <int D>
 constexpr int attn_tile() { return D == 64 ? 256 : 128; }  // attention positions per tile (64 KB of K + V)
 constexpr int kMaxKp = 16384;                 // largest projection input (floats in shared memory)
-constexpr int kMaxPieces = 8;
+constexpr int kMaxBlocks = 8;  // column blocks per row of a projection
 constexpr uint64_t kWaitNs = 200000000ull;    // bound of every wait: 0.2 s
 constexpr size_t kMaxSmem = 227 * 1024;
 
