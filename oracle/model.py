@@ -26,7 +26,7 @@ F64 = np.float64
 
 __all__ = [
     "f32", "f16", "bf16", "dequant", "rmsnorm", "rope_rotate", "rope_inv_freq", "attention_partial",
-    "merge_partials", "attention", "silu", "swiglu", "moe_route", "moe_ffn", "Stage", "Pipeline",
+    "merge_partials", "attention", "silu", "swiglu", "moe_route", "moe_ffn", "shared_expert", "Stage", "Pipeline",
     "greedy", "matvec",
 ]
 
@@ -208,7 +208,8 @@ def moe_route(logits: np.ndarray, top_k: int) -> Tuple[np.ndarray, np.ndarray]:
 
     [BOOK] "MoE layers under tensor parallelism": the gate returns (weights, experts)
     per token.  Reading: softmax over all experts, then top-k, then renormalise over the
-    selected k (A3B-style), no shared expert."""
+    selected k (A3B-style); a shared expert, when the model has one, is added outside the
+    routed mix (shared_expert)."""
     z = np.asarray(logits, dtype=F64)
     p = np.exp(z - np.max(z))
     p = p / np.sum(p)
@@ -216,6 +217,19 @@ def moe_route(logits: np.ndarray, top_k: int) -> Tuple[np.ndarray, np.ndarray]:
     idx = order[:top_k]
     w = p[idx] / np.sum(p[idx])
     return idx, w
+
+
+def shared_expert(h: np.ndarray, score: np.ndarray, w_gate: np.ndarray, w_up: np.ndarray, w_down: np.ndarray,
+                  gemm_round=None) -> np.ndarray:
+    """The shared expert of a MoE layer for tokens h [n, H]: sigmoid(score . h_t) *
+    SwiGLU_shared(h_t).  [BOOK] "MoE layers under tensor parallelism" and "Expert parallelism
+    with all-to-all": the layer output adds sigmoid(shared_gate(x)) times shared(x) to the
+    routed experts' sum.  ``score`` is the scalar gate's weights [1, H]; its logit is
+    materialised in float32 like the router logits.  Returns [n, H] float64."""
+    s = f32(matvec(score, h))[:, 0].astype(F64)
+    with np.errstate(over="ignore"):  # exp(-s) = inf for s << 0 gives the exact limit 0
+        sig = 1.0 / (1.0 + np.exp(-s))
+    return sig[:, None] * swiglu(h, w_gate, w_up, w_down, gemm_round)
 
 
 def moe_ffn(h: np.ndarray, router: np.ndarray, e_gate: Sequence[np.ndarray], e_up: Sequence[np.ndarray],
@@ -341,6 +355,9 @@ class Stage:
             if c.is_moe:
                 ffn, _, _ = moe_ffn(h, deq(lw.router) if gemm != "bf16" else self._deq(lw.router), lambda e: deq(lw.e_gate[e]),
                                     lambda e: deq(lw.e_up[e]), lambda e: deq(lw.e_down[e]), c.top_k, rnd)
+                if getattr(c, "shared_ffn", 0):
+                    ffn = ffn + shared_expert(h, self._deq(lw.shared_score), deq(lw.shared_gate), deq(lw.shared_up),
+                                              deq(lw.shared_down), rnd)
             else:
                 ffn = swiglu(h, deq(lw.w_gate), deq(lw.w_up), deq(lw.w_down), rnd)
             x = f32(x + ffn)

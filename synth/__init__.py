@@ -88,6 +88,7 @@ class ModelCfg:
     expert_ffn: int = 0
     rms_eps: float = 1e-5
     rope_theta: float = 10000.0
+    shared_ffn: int = 0  # MoE only: width of the shared expert (0 = none)
 
     @property
     def is_moe(self) -> bool:
@@ -123,6 +124,7 @@ BOOK_CPU = ModelCfg("book-cpu-4L", 9, 4, 512, 8, 4, 64, 1376, 1024)
 T_EMBED, T_HEAD, T_FINAL_NORM = 0, 1, 2
 T_ATTN_NORM, T_FFN_NORM, T_WQ, T_WK, T_WV, T_WO = 10, 11, 12, 13, 14, 15
 T_GATE, T_UP, T_DOWN, T_ROUTER, T_EGATE, T_EUP, T_EDOWN = 16, 17, 18, 19, 20, 21, 22
+T_SSCORE, T_SGATE, T_SUP, T_SDOWN = 23, 24, 25, 26
 T_PROMPT, T_KVFILL = 100, 101
 
 WEIGHT_SIGMA = 0.02
@@ -221,6 +223,10 @@ class LayerWeights:
     e_gate: List[Q8] = field(default_factory=list)
     e_up: List[Q8] = field(default_factory=list)
     e_down: List[Q8] = field(default_factory=list)
+    shared_score: Optional[Q8] = None  # [1 x hidden], the shared expert's scalar gate
+    shared_gate: Optional[Q8] = None
+    shared_up: Optional[Q8] = None
+    shared_down: Optional[Q8] = None
 
 
 @dataclass
@@ -262,6 +268,11 @@ def layer_weights(cfg: ModelCfg, layer: int, seed: int = DEFAULT_SEED, gamma_mod
             lw.e_gate.append(mat(T_EGATE, c.expert_ffn, c.hidden, e))
             lw.e_up.append(mat(T_EUP, c.expert_ffn, c.hidden, e))
             lw.e_down.append(mat(T_EDOWN, c.hidden, c.expert_ffn, e))
+        if c.shared_ffn:
+            lw.shared_score = mat(T_SSCORE, 1, c.hidden)
+            lw.shared_gate = mat(T_SGATE, c.shared_ffn, c.hidden)
+            lw.shared_up = mat(T_SUP, c.shared_ffn, c.hidden)
+            lw.shared_down = mat(T_SDOWN, c.hidden, c.shared_ffn)
     else:
         lw.w_gate = mat(T_GATE, c.ffn, c.hidden)
         lw.w_up = mat(T_UP, c.ffn, c.hidden)
