@@ -69,7 +69,10 @@ typedef struct stage* stage_t;
 
 /* Model shape.  Dense models set n_experts = top_k = expert_ffn = 0.  ffn and
  * expert_ffn need not be multiples of 32 (the last weight block of a row is then
- * partial).  max_seqs / max_seq_len size the KV cache; max_tokens bounds the
+ * partial).  shared_ffn (MoE only, 0 = none): width of a shared expert added to every
+ * token's expert mix with weight sigmoid(shared_score . h) ("41. Many GPUs: tensor,
+ * pipeline, expert and data parallelism", the MoE layer listings:
+ * out + sigmoid(shared_gate(x)) * shared(x)); stages with one decode on the GEMV path.  max_seqs / max_seq_len size the KV cache; max_tokens bounds the
  * tokens of one prefill or decode call.  gemm_bf16_min_tokens: on dense models, calls
  * with at least this many tokens run their projections on the tensor cores (tcgen05)
  * with bf16 operands -- activations rounded to bf16, weights as bf16(f32(scale) * q) --
@@ -81,6 +84,7 @@ typedef struct {
   float rms_eps, rope_theta;
   int max_seqs, max_seq_len, max_tokens;
   int gemm_bf16_min_tokens;
+  int shared_ffn;
 } stage_model_cfg;
 
 /* Global block range [begin, end): begin == 0 => the stage embeds; end == n_layers
@@ -101,13 +105,16 @@ typedef struct {
 /* Host weights of one block.  Shapes: norms [hidden] f32; wq [Hq*D x hidden];
  * wk, wv [Hkv*D x hidden]; wo [hidden x Hq*D]; dense: w_gate, w_up [ffn x hidden],
  * w_down [hidden x ffn]; MoE: router [n_experts x hidden] and arrays of n_experts
- * matrices e_gate, e_up [expert_ffn x hidden], e_down [hidden x expert_ffn]. */
+ * matrices e_gate, e_up [expert_ffn x hidden], e_down [hidden x expert_ffn]; with a
+ * shared expert also shared_score [1 x hidden] (the page's shared_gate, a scalar gate),
+ * shared_gate, shared_up [shared_ffn x hidden] and shared_down [hidden x shared_ffn]. */
 typedef struct {
   const float *attn_norm, *ffn_norm;
   stage_q8 wq, wk, wv, wo;
   stage_q8 w_gate, w_up, w_down;
   stage_q8 router;
   const stage_q8 *e_gate, *e_up, *e_down;
+  stage_q8 shared_score, shared_gate, shared_up, shared_down;
 } stage_layer_w;
 
 /* Host weights of a stage: embed [vocab x hidden] only if begin == 0; final_norm

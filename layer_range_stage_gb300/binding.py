@@ -40,7 +40,7 @@ class stage_model_cfg(C.Structure):
     _fields_ = [(n, C.c_int) for n in ("n_layers", "hidden", "n_q_heads", "n_kv_heads", "head_dim", "ffn", "vocab",
                                        "n_experts", "top_k", "expert_ffn")] + \
                [("rms_eps", C.c_float), ("rope_theta", C.c_float)] + \
-               [(n, C.c_int) for n in ("max_seqs", "max_seq_len", "max_tokens", "gemm_bf16_min_tokens")]
+               [(n, C.c_int) for n in ("max_seqs", "max_seq_len", "max_tokens", "gemm_bf16_min_tokens", "shared_ffn")]
 
 
 class stage_layer_range(C.Structure):
@@ -54,7 +54,8 @@ class stage_q8(C.Structure):
 class stage_layer_w(C.Structure):
     _fields_ = [("attn_norm", C.c_void_p), ("ffn_norm", C.c_void_p)] + \
                [(n, stage_q8) for n in ("wq", "wk", "wv", "wo", "w_gate", "w_up", "w_down", "router")] + \
-               [("e_gate", C.c_void_p), ("e_up", C.c_void_p), ("e_down", C.c_void_p)]
+               [("e_gate", C.c_void_p), ("e_up", C.c_void_p), ("e_down", C.c_void_p)] + \
+               [(n, stage_q8) for n in ("shared_score", "shared_gate", "shared_up", "shared_down")]
 
 
 class stage_weights(C.Structure):
@@ -157,7 +158,8 @@ def make_cfg(model, max_seqs: int, max_seq_len: int, max_tokens: int, gemm_bf16_
     """stage_model_cfg from any object with the model's shape fields (e.g. synth.ModelCfg)."""
     return stage_model_cfg(model.n_layers, model.hidden, model.n_q_heads, model.n_kv_heads, model.head_dim,
                            model.ffn, model.vocab, model.n_experts, model.top_k, model.expert_ffn,
-                           model.rms_eps, model.rope_theta, max_seqs, max_seq_len, max_tokens, gemm_bf16_min_tokens)
+                           model.rms_eps, model.rope_theta, max_seqs, max_seq_len, max_tokens, gemm_bf16_min_tokens,
+                           getattr(model, "shared_ffn", 0))
 
 
 class _Keep:
@@ -184,7 +186,8 @@ class _Keep:
     def layer(self, lw) -> stage_layer_w:
         w = stage_layer_w()
         w.attn_norm, w.ffn_norm = self.f32(lw.attn_norm), self.f32(lw.ffn_norm)
-        for n in ("wq", "wk", "wv", "wo", "w_gate", "w_up", "w_down", "router"):
+        for n in ("wq", "wk", "wv", "wo", "w_gate", "w_up", "w_down", "router", "shared_score", "shared_gate",
+                  "shared_up", "shared_down"):
             setattr(w, n, self.q8(getattr(lw, n, None)))
         for n in ("e_gate", "e_up", "e_down"):
             mats = getattr(lw, n, None) or []

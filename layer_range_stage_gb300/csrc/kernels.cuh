@@ -178,6 +178,10 @@ cudaError_t launch_argmax(const float* logits, int V, int n_rows, int* out, cuda
 cudaError_t launch_advance(int* pos, const int* tok, int* hist, int* step, int batch, cudaStream_t st);
 // Top-k routing of each token over n_experts router logits [ntok][n_experts]: the k largest
 // (ties to the lower expert id) in descending order, weights softmax over the selected k.
-cudaError_t launch_topk(const float* logits, int n_experts, int k, int ntok, int* ids, float* wts, cudaStream_t st);
+// Top-k routing of ntok tokens: logits [ntok][ld] (entries 0..n_experts-1 ranked), ids and
+// weights [ntok][kw]; kw == k + 1: weight slot k is sigmoid(logits[t][n_experts]) (a shared
+// expert's gate).
+cudaError_t launch_topk(const float* logits, int ld, int n_experts, int k, int ntok, int kw, int* ids, float* wts,
+                        cudaStream_t st);
 
 }  // namespace lrs

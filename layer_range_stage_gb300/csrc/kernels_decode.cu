@@ -803,16 +803,19 @@ cudaError_t launch_advance(int* pos, const int* tok, int* hist, int* step, int b
 // per expert: an expert's rank is the number of experts with a larger logit, or an equal
 // one and a lower id; the k lowest ranks are selected, in rank order.  Softmax over all
 // experts followed by renormalisation over the selected k equals a softmax over the
-// selected logits, which is what is computed.
+// selected logits, which is what is computed.  Logit rows have stride ld; ids and weights
+// rows have stride kw.  kw > k: the model has a shared expert whose scalar gate logit is
+// row entry E, and weight slot k receives sigmoid of it (section "Expert parallelism with
+// all-to-all": the shared expert is added with sigmoid(shared_gate(x))).
 
-__global__ void topk_kernel(const float* logits, int E, int k, int* ids, float* wts) {
+__global__ void topk_kernel(const float* logits, int ld, int E, int k, int kw, int* ids, float* wts) {
   extern __shared__ float lg[];
   __shared__ float sel[32];
   __shared__ int sel_id[32];
   pdl_trigger();
   pdl_wait();
   const int t = blockIdx.x;
-  for (int e = threadIdx.x; e < E; e += blockDim.x) lg[e] = logits[(size_t)t * E + e];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) lg[e] = logits[(size_t)t * ld + e];
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     const float v = lg[e];
@@ -832,17 +835,21 @@ __global__ void topk_kernel(const float* logits, int E, int k, int* ids, float* 
     float z = 0.f;
     for (int j = 0; j < k; ++j) z += expf(sel[j] - m);
     for (int j = 0; j < k; ++j) {
-      ids[(size_t)t * k + j] = sel_id[j];
-      wts[(size_t)t * k + j] = expf(sel[j] - m) / z;
+      ids[(size_t)t * kw + j] = sel_id[j];
+      wts[(size_t)t * kw + j] = expf(sel[j] - m) / z;
     }
+    if (kw > k) wts[(size_t)t * kw + k] = 1.0f / (1.0f + expf(-logits[(size_t)t * ld + E]));
   }
 }
 
-cudaError_t launch_topk(const float* logits, int n_experts, int k, int ntok, int* ids, float* wts, cudaStream_t st) {
+cudaError_t launch_topk(const float* logits, int ld, int n_experts, int k, int ntok, int kw, int* ids, float* wts,
+                        cudaStream_t st) {
   if (ntok <= 0) return cudaSuccess;
-  if (k < 1 || k > 32 || k > n_experts) return cudaErrorInvalidValue;
+  if (k < 1 || k > 32 || k > n_experts || ld < n_experts || kw < k || kw > k + 1 || (kw > k && ld <= n_experts))
+    return cudaErrorInvalidValue;
   const int threads = std::min(1024, ((n_experts + 31) / 32) * 32);
-  return launch_k(topk_kernel, dim3(ntok), dim3(threads), (size_t)n_experts * 4, st, logits, n_experts, k, ids, wts);
+  return launch_k(topk_kernel, dim3(ntok), dim3(threads), (size_t)n_experts * 4, st, logits, ld, n_experts, k, kw,
+                  ids, wts);
 }
 
 cudaError_t prepare_kernels() {

@@ -41,7 +41,9 @@ struct LayerDev {
   float* attn_norm = nullptr;
   float* ffn_norm = nullptr;
   DevQ8 wqkv, wo, wgu, wdown;  // dense (wgu interleaves gate/up rows)
-  DevQ8 router, egu, edown;    // MoE: experts stacked, egu [E][2*EF][Kp(H)], edown [E][H][Kp(EF)]
+  DevQ8 router, egu, edown;    // MoE: experts stacked, egu [E][2*EF][Kp(H)], edown [E][H][Kp(EF)];
+                               // router [E (+1: the shared expert's scalar gate)][Kp(H)]
+  DevQ8 sgu, sdown;            // shared expert: gate/up interleaved [2*SF][Kp(H)], down [H][Kp(SF)]
   bool loaded = false;
 };
 
@@ -52,7 +54,8 @@ void walk_plan(const stage_model_cfg& c, int begin, int end, std::vector<LayerDe
                float** obuf, float** abuf, float** feat, float** logits, int** argmax, float** part_o,
                float2** part_ml, int** counters, int** d_seq, int** d_pos, int** d_tok, int** d_rows, int** err_word,
                float** moe_logits, int** moe_ids, float** moe_wts, __nv_bfloat16** act_bf16,
-               __nv_bfloat16** ffn_bf16, lrs::MegaLayer** mlayers, float** mega_x1, unsigned** mega_bar, F&& f) {
+               __nv_bfloat16** ffn_bf16, lrs::MegaLayer** mlayers, float** mega_x1, unsigned** mega_bar,
+               int** shared_id0, F&& f) {
   auto q8 = [&](DevQ8* m, int N, int K) {
     if (m) {
       m->N = N;
@@ -64,6 +67,7 @@ void walk_plan(const stage_model_cfg& c, int begin, int end, std::vector<LayerDe
   };
   const int H = c.hidden, D = c.head_dim, Hq = c.n_q_heads, Hkv = c.n_kv_heads;
   const bool moe = c.n_experts > 0;
+  const int sh = c.shared_ffn > 0 ? 1 : 0;  // a shared expert: one more router row and weight slot
   for (int l = begin; l < end; ++l) {
     LayerDev* L = layers ? &(*layers)[l - begin] : nullptr;
     f((size_t)H * 4, L ? (void**)&L->attn_norm : nullptr);
@@ -71,9 +75,13 @@ void walk_plan(const stage_model_cfg& c, int begin, int end, std::vector<LayerDe
     q8(L ? &L->wqkv : nullptr, (Hq + 2 * Hkv) * D, H);
     q8(L ? &L->wo : nullptr, H, Hq * D);
     if (moe) {
-      q8(L ? &L->router : nullptr, c.n_experts, H);
+      q8(L ? &L->router : nullptr, c.n_experts + sh, H);
       q8(L ? &L->egu : nullptr, c.n_experts * 2 * c.expert_ffn, H);
       q8(L ? &L->edown : nullptr, c.n_experts * H, c.expert_ffn);
+      if (sh) {
+        q8(L ? &L->sgu : nullptr, 2 * c.shared_ffn, H);
+        q8(L ? &L->sdown : nullptr, H, c.shared_ffn);
+      }
     } else {
       q8(L ? &L->wgu : nullptr, 2 * c.ffn, H);
       q8(L ? &L->wdown : nullptr, H, c.ffn);
@@ -89,7 +97,7 @@ void walk_plan(const stage_model_cfg& c, int begin, int end, std::vector<LayerDe
   f(kv, (void**)vc);
   f((size_t)c.max_seq_len * (D / 2) * 8, (void**)rope);
   const size_t T = (size_t)c.max_tokens;
-  const int ffn_w = moe ? c.top_k * kpad(c.expert_ffn) : c.ffn;
+  const int ffn_w = moe ? c.top_k * kpad(c.expert_ffn) + (sh ? kpad(c.shared_ffn) : 0) : c.ffn;
   f(T * Hq * D * 4, (void**)qbuf);
   f(T * Hq * D * 4, (void**)obuf);
   f(T * (size_t)std::max(ffn_w, H) * 4, (void**)abuf);
@@ -116,9 +124,10 @@ void walk_plan(const stage_model_cfg& c, int begin, int end, std::vector<LayerDe
     f(T * (size_t)kpad(c.ffn) * 2, (void**)ffn_bf16);
   }
   if (moe) {
-    f(T * c.n_experts * 4, (void**)moe_logits);
-    f(T * c.top_k * 4, (void**)moe_ids);
-    f(T * c.top_k * 4, (void**)moe_wts);
+    f(T * (c.n_experts + sh) * 4, (void**)moe_logits);
+    f(T * (c.top_k + sh) * 4, (void**)moe_ids);
+    f(T * (c.top_k + sh) * 4, (void**)moe_wts);
+    if (sh) f(4, (void**)shared_id0);  // expert id 0 of the shared expert's one-slot gate/up launch
   }
 }
 
@@ -128,7 +137,7 @@ size_t plan_bytes(const stage_model_cfg& c, int begin, int end) {
   size_t total = 0;
   walk_plan(c, begin, end, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
             nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
-            nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
+            nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
             [&](size_t b, void**) { total += round_up(b, kAlign); });
   return total;
 }
@@ -151,6 +160,8 @@ bool cfg_valid(const stage_model_cfg* c, stage_layer_range r, std::string* why) 
   if (moe && (c->top_k <= 0 || c->top_k > c->n_experts || c->expert_ffn <= 0 || c->top_k > 32))
     return bad("bad MoE shape");
   if (!moe && (c->ffn <= 0 || c->top_k != 0 || c->expert_ffn != 0)) return bad("bad dense FFN shape");
+  if (c->shared_ffn < 0 || (c->shared_ffn > 0 && (!moe || c->shared_ffn % 4)))
+    return bad("shared_ffn: MoE models only, a multiple of 4");
   if (c->max_seqs <= 0 || c->max_seq_len <= 0 || c->max_tokens <= 0) return bad("non-positive capacity");
   if (c->max_seq_len > (1 << 24) || c->max_tokens > (1 << 20) || c->max_seqs > (1 << 16)) return bad("capacity too large");
   if (!(c->rms_eps > 0.f) || !(c->rope_theta > 0.f)) return bad("rms_eps and rope_theta must be positive");
@@ -184,6 +195,7 @@ struct stage {
   int* counters = nullptr;
   int *d_seq = nullptr, *d_pos = nullptr, *d_tok = nullptr, *d_rows = nullptr;
   int* err_word = nullptr;     // device: set by a kernel whose bounded wait timed out
+  int* shared_id0 = nullptr;   // device: a zero expert id (the shared expert's gate/up launch)
   float* moe_logits = nullptr;  // [max_tokens][n_experts] router logits
   int* moe_ids = nullptr;       // [max_tokens][top_k] selected experts
   float* moe_wts = nullptr;     // [max_tokens][top_k] routing weights
@@ -278,6 +290,27 @@ int upload_stack(stage* st, const stage_q8& src, const DevQ8& whole, int row0, i
   return upload_q8(st, src, part, rows, [](int i) { return (int64_t)i; }, name);
 }
 
+// Gate and up matrices [F x K] interleaved into device rows (2j, 2j+1) = (gate_j, up_j) of dst.
+int upload_gate_up(stage* st, const stage_q8& gate, const stage_q8& up, const DevQ8& dst, int F, const char* name) {
+  const int K = dst.K, nb_src = (K + 31) / 32, nb = dst.Kp / 32;
+  std::vector<uint8_t> q((size_t)2 * F * dst.Kp, 0);
+  std::vector<uint16_t> s((size_t)2 * F * nb, 0);
+  const stage_q8* srcs[2] = {&gate, &up};
+  for (int which = 0; which < 2; ++which) {
+    const stage_q8& m = *srcs[which];
+    if (!m.q || !m.scale || m.rows != F || m.cols != K)
+      return set_err(st, STAGE_E_INVALID, "%s (%s): bad shape or null", name, which ? "up" : "gate");
+    for (int j = 0; j < F; ++j) {
+      std::memcpy(&q[(size_t)(2 * j + which) * dst.Kp], m.q + (int64_t)j * K, K);
+      std::memcpy(&s[(size_t)(2 * j + which) * nb], m.scale + (int64_t)j * nb_src, (size_t)nb_src * 2);
+    }
+  }
+  bias_bytes(q);
+  cudaError_t ce = cudaMemcpy(dst.q, q.data(), q.size(), cudaMemcpyHostToDevice);
+  if (ce == cudaSuccess) ce = cudaMemcpy(dst.s, s.data(), s.size() * 2, cudaMemcpyHostToDevice);
+  return ce == cudaSuccess ? STAGE_OK : cuda_err(st, ce, name);
+}
+
 // The persistent decode's descriptor of block gl: its device weights, norms and KV cache.
 int upload_descriptor(stage* st, int gl, const LayerDev& L) {
   lrs::MegaLayer ml;
@@ -325,7 +358,12 @@ int load_layer(stage* st, int gl, const stage_layer_w* w) {
   }
   if ((rc = upload_plain(st, w->wo, L.wo, "wo"))) return rc;
   if (c.n_experts > 0) {
-    if ((rc = upload_plain(st, w->router, L.router, "router"))) return rc;
+    if ((rc = upload_stack(st, w->router, L.router, 0, c.n_experts, "router"))) return rc;
+    if (c.shared_ffn > 0) {  // the shared expert: its scalar gate as the router's last row
+      if ((rc = upload_stack(st, w->shared_score, L.router, c.n_experts, 1, "shared_score"))) return rc;
+      if ((rc = upload_gate_up(st, w->shared_gate, w->shared_up, L.sgu, c.shared_ffn, "shared gate/up"))) return rc;
+      if ((rc = upload_plain(st, w->shared_down, L.sdown, "shared_down"))) return rc;
+    }
     if (!w->e_gate || !w->e_up || !w->e_down) return set_err(st, STAGE_E_INVALID, "null expert arrays");
     const int EF = c.expert_ffn;
     for (int e = 0; e < c.n_experts; ++e) {
@@ -634,6 +672,8 @@ int forward_dev(stage* st, int n, const int* d_seq, const int* d_pos, const int*
       // experts' gate/up (row gather, SwiGLU scaled by the routing weight) and down
       // (K gather over the k slots, residual add)
       const int E = c.n_experts, kk = c.top_k, EF = c.expert_ffn, KpE = kpad(EF);
+      const int SF = c.shared_ffn, sh = SF > 0 ? 1 : 0, kw = kk + sh;  // ids / weights per token
+      const int ffn_w = kk * KpE + (sh ? kpad(SF) : 0);                  // abuf per token
       lrs::GemvArgs r;
       r.w = L.router;
       r.x = hout;
@@ -643,10 +683,10 @@ int forward_dev(stage* st, int n, const int* d_seq, const int* d_pos, const int*
       r.eps = c.rms_eps;
       r.epi = lrs::EPI_STORE;
       r.out = st->moe_logits;
-      r.ldo = E;
+      r.ldo = E + sh;
       r.err = st->err_word;
       if ((e = lrs::launch_gemv(r, s)) != cudaSuccess) return cuda_err(st, e, "router");
-      if ((e = lrs::launch_topk(st->moe_logits, E, kk, n, st->moe_ids, st->moe_wts, s)) != cudaSuccess)
+      if ((e = lrs::launch_topk(st->moe_logits, E + sh, E, kk, n, kw, st->moe_ids, st->moe_wts, s)) != cudaSuccess)
         return cuda_err(st, e, "top-k");
       for (int t = 0; t < n; ++t) {
         lrs::GemvArgs gu;
@@ -658,21 +698,31 @@ int forward_dev(stage* st, int n, const int* d_seq, const int* d_pos, const int*
         gu.gamma = L.ffn_norm;
         gu.eps = c.rms_eps;
         gu.epi = lrs::EPI_MOE_SWIGLU;
-        gu.out = st->abuf + (size_t)t * kk * KpE;
-        gu.ids = st->moe_ids + (size_t)t * kk;
-        gu.slot_w = st->moe_wts + (size_t)t * kk;
+        gu.out = st->abuf + (size_t)t * ffn_w;
+        gu.ids = st->moe_ids + (size_t)t * kw;
+        gu.slot_w = st->moe_wts + (size_t)t * kw;
         gu.rows_per_slot = 2 * EF;
         gu.ldo_slot = KpE;
         gu.err = st->err_word;
         if (st->timing && t == 0) timing_mark(st->tev[2 * li], s);
         if ((e = lrs::launch_gemv(gu, s)) != cudaSuccess) return cuda_err(st, e, "expert gate_up");
         if (st->timing && t == 0) timing_mark(st->tev[2 * li + 1], s);
+        if (sh) {  // the shared expert's SwiGLU, scaled by sigmoid of its gate (weight slot kk)
+          lrs::GemvArgs sg = gu;
+          sg.w = L.sgu;
+          sg.out = st->abuf + (size_t)t * ffn_w + (size_t)kk * KpE;
+          sg.ids = st->shared_id0;
+          sg.slot_w = st->moe_wts + (size_t)t * kw + kk;
+          sg.rows_per_slot = 2 * SF;
+          sg.ldo_slot = kpad(SF);
+          if ((e = lrs::launch_gemv(sg, s)) != cudaSuccess) return cuda_err(st, e, "shared gate_up");
+        }
         lrs::GemvArgs dn;
         dn.w = L.edown;
         dn.w.N = H;
         dn.w.K = kk * KpE;
         dn.w.Kp = kk * KpE;
-        dn.x = st->abuf + (size_t)t * kk * KpE;
+        dn.x = st->abuf + (size_t)t * ffn_w;
         dn.ldx = kk * KpE;
         dn.ntok = 1;
         dn.epi = lrs::EPI_RESID;
@@ -680,11 +730,25 @@ int forward_dev(stage* st, int n, const int* d_seq, const int* d_pos, const int*
         dn.ldr = H;
         dn.out = hout + (size_t)t * H;
         dn.ldo = H;
-        dn.ids = st->moe_ids + (size_t)t * kk;
+        dn.ids = st->moe_ids + (size_t)t * kw;
         dn.seg_chunks = KpE / 16;
         dn.seg_rows = H;
         dn.err = st->err_word;
         if ((e = lrs::launch_gemv(dn, s)) != cudaSuccess) return cuda_err(st, e, "expert down");
+        if (sh) {  // + the shared expert's down projection
+          lrs::GemvArgs sd;
+          sd.w = L.sdown;
+          sd.x = st->abuf + (size_t)t * ffn_w + (size_t)kk * KpE;
+          sd.ldx = kpad(SF);
+          sd.ntok = 1;
+          sd.epi = lrs::EPI_RESID;
+          sd.resid = hout + (size_t)t * H;
+          sd.ldr = H;
+          sd.out = hout + (size_t)t * H;
+          sd.ldo = H;
+          sd.err = st->err_word;
+          if ((e = lrs::launch_gemv(sd, s)) != cudaSuccess) return cuda_err(st, e, "shared down");
+        }
       }
       continue;
     }
@@ -932,7 +996,7 @@ int stage_create(const stage_model_cfg* cfg, stage_layer_range range, const stag
             &st->rope, &st->qbuf, &st->obuf, &st->abuf, &st->feat, &st->logits, &st->argmax, &st->part_o,
             &st->part_ml, &st->counters, &st->d_seq, &st->d_pos, &st->d_tok, &st->d_rows, &st->err_word,
             &st->moe_logits, &st->moe_ids, &st->moe_wts, &st->act_bf16, &st->ffn_bf16, &st->mlayers, &st->mega_x1,
-            &st->mega_bar, [&](size_t b, void** slot) {
+            &st->mega_bar, &st->shared_id0, [&](size_t b, void** slot) {
               if (slot) *slot = st->arena + off;
               off += round_up(b, kAlign);
             });
@@ -954,7 +1018,7 @@ int stage_create(const stage_model_cfg* cfg, stage_layer_range range, const stag
   {
     const char* mg = getenv("LRS_PERSISTENT");
     const bool moe = cfg->n_experts > 0;
-    st->mega = !(mg && mg[0] == '0') &&
+    st->mega = !(mg && mg[0] == '0') && cfg->shared_ffn == 0 &&
                lrs::mega_supported(cfg->hidden, cfg->n_q_heads * cfg->head_dim,
                                    moe ? cfg->top_k * kpad(cfg->expert_ffn) : cfg->ffn, cfg->head_dim,
                                    cfg->n_q_heads / cfg->n_kv_heads, cfg->n_experts, cfg->top_k);

@@ -96,3 +96,19 @@ def test_moe_full_width_two_blocks(cuda):
     for a, b in zip(logits, logits_o):
         assert np.abs(a - b).max() <= LOGIT_ATOL
     assert toks.tolist() == toks_o.tolist()
+
+
+def test_small_moe_with_shared_expert_matches_oracle(cuda):
+    """A shared expert beside the routed ones (its scalar gate as the router's last row,
+    its SwiGLU and down projection after the routed experts'): logits and greedy tokens
+    against the oracle; such stages decode on the GEMV path (no persistent kernel)."""
+    from layer_range_stage_gb300 import binding as B
+    model = synth.reduced(small_moe(), 2, shared_ffn=96)
+    prompt = synth.prompt_tokens(model, 0, 12)
+    gp, op = pipelines(model, [0, 1, 2])
+    with gp:
+        assert B.stage_gemm_mode(gp.stages[0], 1) == 0
+        toks, logits, toks_o, logits_o = run(gp, op, model, prompt, 5)
+    for a, b in zip(logits, logits_o):
+        assert np.abs(a - b).max() <= LOGIT_ATOL
+    assert toks.tolist() == toks_o.tolist()
