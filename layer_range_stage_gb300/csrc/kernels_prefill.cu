@@ -430,61 +430,82 @@ cudaError_t launch_rows_to_bf16(const float* x, int ld_in, int K, const float* g
 }
 
 // ------------------------------------------------------------------------------------------
-// Causal attention of a prefill call, tiled (CUDA cores, f32 math over the fp16 cache).
+// Causal attention of a prefill call on the tensor cores (mma m16n8k16: fp16 operands, f32
+// accumulation).
 //
 // "41. Many GPUs: tensor, pipeline, expert and data parallelism", section "Ring attention for
 // very long contexts": softmax(q k^T / sqrt(D)) v with a running max and sum over tiles of
 // positions (the same log-sum-exp recurrence its merge uses), here over the tiles of one
 // sequence in order.  A CTA takes 64 query rows -- the G query heads of one KV head for 64 / G
-// consecutive tokens of the call -- and every K/V tile of 64 positions it loads serves all of
-// them.  Token t attends to positions 0..pos[t] of sequence seq[t]; a block that spans two
-// sequences walks each sequence's tiles in turn with the other rows masked.  The tokens' own
-// K/V rows are already in the cache (written by the QKV projection).
+// consecutive tokens of the call -- in four warps of 16 rows; every K/V tile of 64 positions
+// it loads serves all of them.  K and V are the fp16 cache as stored; q is rounded to fp16
+// once, the probabilities to fp16 per tile, every sum is f32.  Token t attends to positions
+// 0..pos[t] of sequence seq[t]; a block that spans two sequences walks each sequence's tiles
+// in turn with the other rows masked.  The tokens' own K/V rows are already in the cache.
 
-constexpr int kPR = 64;       // query rows per CTA
-constexpr int kPT = 32;       // positions per K/V tile
-constexpr int kPThreads = 256;
+constexpr int kPR = 64;        // query rows per CTA (four warps of 16)
+constexpr int kPT = 64;        // positions per K/V tile
+constexpr int kPThreads = 128;
 
 template <int D>
 struct PrefillSmem {
-  static constexpr int QROW = D + 4;    // floats per q / K / V row (bank offset between rows)
-  static constexpr int HROW = D + 8;    // halves per raw K/V row (16-byte pad)
-  static constexpr int SROW = kPT + 4;  // floats per probability row
-  static constexpr size_t q = (size_t)kPR * QROW * 4;
-  static constexpr size_t kf = (size_t)kPT * QROW * 4;      // K tile, f32
-  static constexpr size_t raw = (size_t)2 * kPT * HROW * 2;  // one raw K + V tile, fp16
-  static constexpr size_t p = (size_t)kPR * SROW * 4;
-  static constexpr size_t total = q + 2 * kf + 2 * raw + p + 2 * kPR * 4;
+  static constexpr int HROW = D + 8;                       // halves per row: conflict-free ldmatrix
+  static constexpr size_t q = (size_t)kPR * HROW * 2;      // q rows, fp16
+  static constexpr size_t tile = (size_t)kPT * HROW * 2;   // one K or V tile
+  static constexpr size_t kv = 2 * 2 * tile;               // [2 buffers][K, V]
+  static constexpr size_t total = q + kv + 2 * kPR * 4;    // + each row's sequence and position
 };
 
-// Thread (tr, tc) = (tid / 8, tid % 8): query rows tr and tr + 32; scores at positions
-// tc + 8 j of a tile; output dims 4 tc + 32 m + e.  K and V tiles are converted to f32 in
-// shared memory once (one copy for all threads); the raw fp16 rows of the next tile stream in
-// with cp.async meanwhile.
+__device__ __forceinline__ void ldsm_x4(uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3, const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(smem_u32(p)));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3, const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(smem_u32(p)));
+}
+// c (16 x 8, f32) += a (16 x 16, fp16, row-major fragments) * b (16 x 8, fp16, column fragments)
+__device__ __forceinline__ void mma_16816(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
+  asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+               "{%0,%1,%2,%3};"
+               : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+               : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t half2_bits(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// Lane l of a warp holds rows (l / 4) and (l / 4 + 8) of its 16, positions / dims 2 (l % 4) and
+// + 1 of every 8-column tile (the accumulator layout of mma m16n8k16).
 template <int D, int G>
-__global__ void __launch_bounds__(kPThreads, 2) attn_prefill_kernel(const AttnArgs a) {
+__global__ void __launch_bounds__(kPThreads) attn_prefill_kernel(const AttnArgs a) {
   using S = PrefillSmem<D>;
-  constexpr int QB = kPR / G;    // tokens per CTA
-  constexpr int NM = D / 32;     // float4 groups of output dims per thread
+  constexpr int QB = kPR / G;          // tokens per CTA
+  constexpr int HROW = S::HROW;
+  constexpr int KS = D / 16;           // k steps of q k^T
+  constexpr int NT = D / 8;            // 8-dim tiles of the output
+  constexpr int PN = kPT / 8;          // 8-position tiles of the scores
   extern __shared__ __align__(16) unsigned char ps_raw[];
-  float* qs = reinterpret_cast<float*>(ps_raw);
-  float* kf = reinterpret_cast<float*>(ps_raw + S::q);
-  float* vf = kf + kPT * S::QROW;
-  __half* rawb = reinterpret_cast<__half*>(ps_raw + S::q + 2 * S::kf);  // [2 buffers][K, V][kPT][HROW]
-  float* pr = reinterpret_cast<float*>(ps_raw + S::q + 2 * S::kf + 2 * S::raw);
-  int* rseq = reinterpret_cast<int*>(pr + kPR * S::SROW);  // [kPR] sequence of the row's token (-1: none)
-  int* rpos = rseq + kPR;                                   // [kPR] its position
+  __half* qs = reinterpret_cast<__half*>(ps_raw);
+  __half* kvs = reinterpret_cast<__half*>(ps_raw + S::q);  // [buffer][K, V][kPT][HROW]
+  int* rseq = reinterpret_cast<int*>(ps_raw + S::q + S::kv);  // [kPR] sequence of the row's token (-1: none)
+  int* rpos = rseq + kPR;                                      // [kPR] its position
   pdl_trigger();
   pdl_wait();
-  const int tid = threadIdx.x, tr = tid >> 3, tc = tid & 7;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int kvh = blockIdx.y, t0 = blockIdx.x * QB;
-  // rows r = i * G + g: token t0 + i, query head kvh * G + g
+  // rows r = i * G + g: token t0 + i, query head kvh * G + g; q to fp16
   for (int i = tid; i < kPR * (D / 4); i += kPThreads) {
     const int r = i / (D / 4), c4 = i - r * (D / 4);
     const int t = t0 + r / G, g = r % G;
     float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
     if (t < a.ntok) v = reinterpret_cast<const float4*>(a.q + ((size_t)t * a.Hq + (size_t)kvh * G + g) * D)[c4];
-    *reinterpret_cast<float4*>(qs + r * S::QROW + 4 * c4) = v;
+    __half2* dst = reinterpret_cast<__half2*>(qs + r * HROW + 4 * c4);
+    dst[0] = __floats2half2_rn(v.x, v.y);
+    dst[1] = __floats2half2_rn(v.z, v.w);
   }
   for (int r = tid; r < kPR; r += kPThreads) {
     const int t = t0 + r / G;
@@ -492,12 +513,18 @@ __global__ void __launch_bounds__(kPThreads, 2) attn_prefill_kernel(const AttnAr
     rpos[r] = t < a.ntok ? a.pos[t] : -1;
   }
   __syncthreads();
-  const int r0 = tr, r1 = tr + 32;
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-  float4 o0[NM], o1[NM];
+  const int mi = lane >> 3, mr = lane & 7;  // ldmatrix: the matrix and row this lane addresses
+  uint32_t qf[KS][4];                       // this warp's 16 q rows as A fragments
 #pragma unroll
-  for (int m = 0; m < NM; ++m) o0[m] = o1[m] = make_float4(0.f, 0.f, 0.f, 0.f);
-  const int sq0 = rseq[r0], sq1 = rseq[r1], pp0 = rpos[r0], pp1 = rpos[r1];
+  for (int ks = 0; ks < KS; ++ks)
+    ldsm_x4(qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3],
+            qs + (warp * 16 + mr + (mi & 1) * 8) * HROW + ks * 16 + (mi >> 1) * 8);
+  const int ra = warp * 16 + (lane >> 2), rb = ra + 8;
+  const int sqa = rseq[ra], sqb = rseq[rb], ppa = rpos[ra], ppb = rpos[rb];
+  float o[NT][4];
+#pragma unroll
+  for (int n = 0; n < NT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+  float ma = -INFINITY, mb = -INFINITY, la = 0.f, lb = 0.f;
 
   // walk the distinct sequences of the block in order of first appearance (rows of one
   // sequence need not be adjacent); every thread reads the same row table, so the walk is
@@ -513,19 +540,24 @@ __global__ void __launch_bounds__(kPThreads, 2) attn_prefill_kernel(const AttnAr
       if (rseq[r] == sid) maxpos = max(maxpos, rpos[r]);
     const __half* kb = a.kc + ((size_t)sid * a.Hkv + kvh) * (size_t)a.max_len * D;
     const __half* vb = a.vc + ((size_t)sid * a.Hkv + kvh) * (size_t)a.max_len * D;
-    const bool own0 = sq0 == sid, own1 = sq1 == sid;
-    auto fetch = [&](int p0, int buf) {  // raw fp16 rows of the tile at p0 into buffer buf
+    const bool owna = sqa == sid, ownb = sqb == sid;
+    auto fetch = [&](int p0, int buf) {  // the tile at p0 into buffer buf; rows past the sequence are zero
       const int np = min(kPT, maxpos + 1 - p0);
-      __half* rk = rawb + (size_t)buf * 2 * kPT * S::HROW;
-      __half* rv = rk + kPT * S::HROW;
-      for (int i = tid; i < np * (D / 8); i += kPThreads) {
+      __half* tk = kvs + (size_t)buf * 2 * kPT * HROW;
+      __half* tv = tk + kPT * HROW;
+      for (int i = tid; i < kPT * (D / 8); i += kPThreads) {
         const int r = i / (D / 8), c = i - r * (D / 8);
-        cp_async16(rk + r * S::HROW + c * 8, kb + (size_t)(p0 + r) * D + c * 8);
-        cp_async16(rv + r * S::HROW + c * 8, vb + (size_t)(p0 + r) * D + c * 8);
+        if (r < np) {
+          cp_async16(tk + r * HROW + c * 8, kb + (size_t)(p0 + r) * D + c * 8);
+          cp_async16(tv + r * HROW + c * 8, vb + (size_t)(p0 + r) * D + c * 8);
+        } else {
+          *reinterpret_cast<uint4*>(tk + r * HROW + c * 8) = make_uint4(0u, 0u, 0u, 0u);
+          *reinterpret_cast<uint4*>(tv + r * HROW + c * 8) = make_uint4(0u, 0u, 0u, 0u);
+        }
       }
       cp_async_commit();
     };
-    __syncthreads();  // the previous walk is done with the raw buffers
+    __syncthreads();  // the previous walk is done with the tile buffers
     fetch(0, 0);
     int buf = 0;
     for (int p0 = 0; p0 <= maxpos; p0 += kPT, buf ^= 1) {
@@ -536,131 +568,99 @@ __global__ void __launch_bounds__(kPThreads, 2) attn_prefill_kernel(const AttnAr
       } else {
         cp_async_wait_group<0>();
       }
-      __syncthreads();  // raw tile `buf` landed for every thread; the previous f32 tile is consumed
-      {  // convert to f32 (rows beyond np are zero)
-        const __half* rk = rawb + (size_t)buf * 2 * kPT * S::HROW;
-        const __half* rv = rk + kPT * S::HROW;
-        for (int i = tid; i < kPT * (D / 8); i += kPThreads) {
-          const int r = i / (D / 8), c = i - r * (D / 8);
-          float4 k0 = make_float4(0.f, 0.f, 0.f, 0.f), k1 = k0, v0 = k0, v1 = k0;
-          if (r < np) {
-            const uint4 kk = *reinterpret_cast<const uint4*>(rk + r * S::HROW + c * 8);
-            const uint4 vv = *reinterpret_cast<const uint4*>(rv + r * S::HROW + c * 8);
-            const float2 a0 = __half22float2(*reinterpret_cast<const __half2*>(&kk.x));
-            const float2 a1 = __half22float2(*reinterpret_cast<const __half2*>(&kk.y));
-            const float2 a2 = __half22float2(*reinterpret_cast<const __half2*>(&kk.z));
-            const float2 a3 = __half22float2(*reinterpret_cast<const __half2*>(&kk.w));
-            const float2 b0 = __half22float2(*reinterpret_cast<const __half2*>(&vv.x));
-            const float2 b1 = __half22float2(*reinterpret_cast<const __half2*>(&vv.y));
-            const float2 b2 = __half22float2(*reinterpret_cast<const __half2*>(&vv.z));
-            const float2 b3 = __half22float2(*reinterpret_cast<const __half2*>(&vv.w));
-            k0 = make_float4(a0.x, a0.y, a1.x, a1.y);
-            k1 = make_float4(a2.x, a2.y, a3.x, a3.y);
-            v0 = make_float4(b0.x, b0.y, b1.x, b1.y);
-            v1 = make_float4(b2.x, b2.y, b3.x, b3.y);
-          }
-          *reinterpret_cast<float4*>(kf + r * S::QROW + c * 8) = k0;
-          *reinterpret_cast<float4*>(kf + r * S::QROW + c * 8 + 4) = k1;
-          *reinterpret_cast<float4*>(vf + r * S::QROW + c * 8) = v0;
-          *reinterpret_cast<float4*>(vf + r * S::QROW + c * 8 + 4) = v1;
+      __syncthreads();  // tile `buf` landed (and its zero rows are written) for every thread
+      const __half* tk = kvs + (size_t)buf * 2 * kPT * HROW;
+      const __half* tv = tk + kPT * HROW;
+      // scores: s[n] is the 16 x 8 tile of positions p0 + 8 n .. + 7
+      float sc[PN][4];
+#pragma unroll
+      for (int n = 0; n < PN; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
+#pragma unroll
+      for (int n2 = 0; n2 < PN / 2; ++n2)
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+          uint32_t b0, b1, b2, b3;  // K rows [pos][dim] are the column fragments of k^T
+          ldsm_x4(b0, b1, b2, b3, tk + (n2 * 16 + mr + (mi >> 1) * 8) * HROW + ks * 16 + (mi & 1) * 8);
+          mma_16816(sc[2 * n2], qf[ks], b0, b1);
+          mma_16816(sc[2 * n2 + 1], qf[ks], b2, b3);
+        }
+      // scale, causal mask (own sequence, position in the tile and <= the row's), running max
+      float mta = -INFINITY, mtb = -INFINITY;
+#pragma unroll
+      for (int n = 0; n < PN; ++n)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int c = n * 8 + (lane & 3) * 2 + e, p = p0 + c;
+          sc[n][e] = (owna && c < np && p <= ppa) ? sc[n][e] * a.scale : -INFINITY;
+          sc[n][2 + e] = (ownb && c < np && p <= ppb) ? sc[n][2 + e] * a.scale : -INFINITY;
+          mta = fmaxf(mta, sc[n][e]);
+          mtb = fmaxf(mtb, sc[n][2 + e]);
+        }
+#pragma unroll
+      for (int off = 1; off < 4; off <<= 1) {  // the four lanes of a row
+        mta = fmaxf(mta, __shfl_xor_sync(0xffffffffu, mta, off));
+        mtb = fmaxf(mtb, __shfl_xor_sync(0xffffffffu, mtb, off));
+      }
+      const float mna = fmaxf(ma, mta), mnb = fmaxf(mb, mtb);
+      const float ala = ma == -INFINITY ? 0.f : expf(ma - mna);
+      const float alb = mb == -INFINITY ? 0.f : expf(mb - mnb);
+      float lsa = 0.f, lsb = 0.f;
+#pragma unroll
+      for (int n = 0; n < PN; ++n)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          sc[n][e] = sc[n][e] == -INFINITY ? 0.f : expf(sc[n][e] - mna);
+          sc[n][2 + e] = sc[n][2 + e] == -INFINITY ? 0.f : expf(sc[n][2 + e] - mnb);
+          lsa += sc[n][e];
+          lsb += sc[n][2 + e];
+        }
+#pragma unroll
+      for (int off = 1; off < 4; off <<= 1) {
+        lsa += __shfl_xor_sync(0xffffffffu, lsa, off);
+        lsb += __shfl_xor_sync(0xffffffffu, lsb, off);
+      }
+      la = la * ala + lsa;
+      lb = lb * alb + lsb;
+      ma = mna;
+      mb = mnb;
+#pragma unroll
+      for (int n = 0; n < NT; ++n) {
+        o[n][0] *= ala;
+        o[n][1] *= ala;
+        o[n][2] *= alb;
+        o[n][3] *= alb;
+      }
+      // o += p v: the probabilities of positions 16 k .. + 15 as an A fragment, V through
+      // transposed loads (rows [pos][dim] are the row fragments of v)
+#pragma unroll
+      for (int k = 0; k < PN / 2; ++k) {
+        const uint32_t pf[4] = {half2_bits(sc[2 * k][0], sc[2 * k][1]), half2_bits(sc[2 * k][2], sc[2 * k][3]),
+                                half2_bits(sc[2 * k + 1][0], sc[2 * k + 1][1]),
+                                half2_bits(sc[2 * k + 1][2], sc[2 * k + 1][3])};
+#pragma unroll
+        for (int n2 = 0; n2 < NT / 2; ++n2) {
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4_t(b0, b1, b2, b3, tv + (k * 16 + mr + (mi & 1) * 8) * HROW + n2 * 16 + (mi >> 1) * 8);
+          mma_16816(o[2 * n2], pf, b0, b1);
+          mma_16816(o[2 * n2 + 1], pf, b2, b3);
         }
       }
-      __syncthreads();
-      // scores of rows r0, r1 at positions tc + 8 j
-      float s0[kPT / 8], s1[kPT / 8];
-#pragma unroll
-      for (int j = 0; j < kPT / 8; ++j) s0[j] = s1[j] = 0.f;
-      const float* q0 = qs + r0 * S::QROW;
-      const float* q1 = qs + r1 * S::QROW;
-#pragma unroll 4
-      for (int d = 0; d < D; d += 4) {
-        const float4 qa = *reinterpret_cast<const float4*>(q0 + d);
-        const float4 qb = *reinterpret_cast<const float4*>(q1 + d);
-#pragma unroll
-        for (int j = 0; j < kPT / 8; ++j) {
-          const float4 kk = *reinterpret_cast<const float4*>(kf + (tc + 8 * j) * S::QROW + d);
-          s0[j] = fmaf(qa.x, kk.x, s0[j]);
-          s0[j] = fmaf(qa.y, kk.y, s0[j]);
-          s0[j] = fmaf(qa.z, kk.z, s0[j]);
-          s0[j] = fmaf(qa.w, kk.w, s0[j]);
-          s1[j] = fmaf(qb.x, kk.x, s1[j]);
-          s1[j] = fmaf(qb.y, kk.y, s1[j]);
-          s1[j] = fmaf(qb.z, kk.z, s1[j]);
-          s1[j] = fmaf(qb.w, kk.w, s1[j]);
-        }
-      }
-      // causal mask, running max and sum per row (the 8 lanes of a row agree via shuffles)
-      float mt0 = -INFINITY, mt1 = -INFINITY;
-#pragma unroll
-      for (int j = 0; j < kPT / 8; ++j) {
-        const int p = p0 + tc + 8 * j;
-        s0[j] = (own0 && tc + 8 * j < np && p <= pp0) ? s0[j] * a.scale : -INFINITY;
-        s1[j] = (own1 && tc + 8 * j < np && p <= pp1) ? s1[j] * a.scale : -INFINITY;
-        mt0 = fmaxf(mt0, s0[j]);
-        mt1 = fmaxf(mt1, s1[j]);
-      }
-#pragma unroll
-      for (int o = 1; o < 8; o <<= 1) {
-        mt0 = fmaxf(mt0, __shfl_xor_sync(0xffffffffu, mt0, o));
-        mt1 = fmaxf(mt1, __shfl_xor_sync(0xffffffffu, mt1, o));
-      }
-      const float mn0 = fmaxf(m0, mt0), mn1 = fmaxf(m1, mt1);
-      const float al0 = (mn0 == -INFINITY || m0 == -INFINITY) ? (m0 == -INFINITY ? 0.f : 1.f) : expf(m0 - mn0);
-      const float al1 = (mn1 == -INFINITY || m1 == -INFINITY) ? (m1 == -INFINITY ? 0.f : 1.f) : expf(m1 - mn1);
-      float ls0 = 0.f, ls1 = 0.f;
-#pragma unroll
-      for (int j = 0; j < kPT / 8; ++j) {
-        const float e0 = s0[j] == -INFINITY ? 0.f : expf(s0[j] - mn0);
-        const float e1 = s1[j] == -INFINITY ? 0.f : expf(s1[j] - mn1);
-        pr[r0 * S::SROW + tc + 8 * j] = e0;
-        pr[r1 * S::SROW + tc + 8 * j] = e1;
-        ls0 += e0;
-        ls1 += e1;
-      }
-#pragma unroll
-      for (int o = 1; o < 8; o <<= 1) {
-        ls0 += __shfl_xor_sync(0xffffffffu, ls0, o);
-        ls1 += __shfl_xor_sync(0xffffffffu, ls1, o);
-      }
-      l0 = l0 * al0 + ls0;
-      l1 = l1 * al1 + ls1;
-      m0 = mn0;
-      m1 = mn1;
-      __syncwarp();  // the row's 8 lanes are in this warp: their probabilities are written
-#pragma unroll
-      for (int m = 0; m < NM; ++m) {
-        o0[m].x *= al0; o0[m].y *= al0; o0[m].z *= al0; o0[m].w *= al0;
-        o1[m].x *= al1; o1[m].y *= al1; o1[m].z *= al1; o1[m].w *= al1;
-      }
-      for (int p = 0; p < np; ++p) {
-        const float w0 = pr[r0 * S::SROW + p], w1 = pr[r1 * S::SROW + p];
-        const float* vr = vf + p * S::QROW + 4 * tc;
-#pragma unroll
-        for (int m = 0; m < NM; ++m) {
-          const float4 v = *reinterpret_cast<const float4*>(vr + 32 * m);
-          o0[m].x = fmaf(w0, v.x, o0[m].x); o0[m].y = fmaf(w0, v.y, o0[m].y);
-          o0[m].z = fmaf(w0, v.z, o0[m].z); o0[m].w = fmaf(w0, v.w, o0[m].w);
-          o1[m].x = fmaf(w1, v.x, o1[m].x); o1[m].y = fmaf(w1, v.y, o1[m].y);
-          o1[m].z = fmaf(w1, v.z, o1[m].z); o1[m].w = fmaf(w1, v.w, o1[m].w);
-        }
-      }
+      __syncthreads();  // the tile is consumed before the buffer is refilled
     }
   }
   // normalise and store
-  const int ta = t0 + r0 / G, tb = t0 + r1 / G;
-  if (sq0 >= 0 && ta < a.ntok) {
-    float* out = a.out + ((size_t)ta * a.Hq + (size_t)kvh * G + r0 % G) * D + 4 * tc;
-    const float inv = 1.0f / l0;
+  const int ta = t0 + ra / G, tb = t0 + rb / G;
+  if (sqa >= 0 && ta < a.ntok) {
+    float* out = a.out + ((size_t)ta * a.Hq + (size_t)kvh * G + ra % G) * D + (lane & 3) * 2;
+    const float inv = 1.0f / la;
 #pragma unroll
-    for (int m = 0; m < NM; ++m)
-      *reinterpret_cast<float4*>(out + 32 * m) = make_float4(o0[m].x * inv, o0[m].y * inv, o0[m].z * inv, o0[m].w * inv);
+    for (int n = 0; n < NT; ++n) *reinterpret_cast<float2*>(out + n * 8) = make_float2(o[n][0] * inv, o[n][1] * inv);
   }
-  if (sq1 >= 0 && tb < a.ntok) {
-    float* out = a.out + ((size_t)tb * a.Hq + (size_t)kvh * G + r1 % G) * D + 4 * tc;
-    const float inv = 1.0f / l1;
+  if (sqb >= 0 && tb < a.ntok) {
+    float* out = a.out + ((size_t)tb * a.Hq + (size_t)kvh * G + rb % G) * D + (lane & 3) * 2;
+    const float inv = 1.0f / lb;
 #pragma unroll
-    for (int m = 0; m < NM; ++m)
-      *reinterpret_cast<float4*>(out + 32 * m) = make_float4(o1[m].x * inv, o1[m].y * inv, o1[m].z * inv, o1[m].w * inv);
+    for (int n = 0; n < NT; ++n) *reinterpret_cast<float2*>(out + n * 8) = make_float2(o[n][2] * inv, o[n][3] * inv);
   }
 }
 
