@@ -40,6 +40,9 @@ WORKLOADS = {
             name="dense 8B-shape decode, 32 blocks as 2 stages 16/16, batch 1, context 2048"),
     2: dict(context=4096, bounds=[0, 21, 40],
             name="MoE 40-block decode (128 experts top-8), 2 stages 21/19, batch 1, context 4096"),
+    4: dict(context=None, bounds=[0, 20, 40, 60, 80], seqs=64,
+            name="dense 70B-shape batched decode, 80 blocks as 4 stages 20/20/20/20, 64 sequences with KV "
+                 "lengths uniform in 128-4096"),
 }
 CFG_ID = 1
 CONTEXT = 2048
@@ -337,6 +340,142 @@ def run_gpu(args):
         dist.destroy_process_group()
 
 
+def batched_lens(nseq):
+    """Seeded KV lengths of the batched workload: uniform in [128, 4096]."""
+    return np.random.default_rng(4401).integers(128, 4097, nseq)
+
+
+def run_batched(args):
+    """The 70B-shape batched decode: 4 stages of 20 blocks, 64 sequences of ragged context,
+    one token per sequence per step (all stages, the final norm, the readout of the 64 rows
+    and their argmax), on the float32 GEMV path and on the tensor-core path (bf16 operands,
+    f32 accumulation: the stage's GEMM threshold set to the batch).  One seeded block of
+    weights is loaded into every block (each block has its own device copy, so the bytes a
+    step moves are those of 80 distinct blocks); every sequence's cache holds seeded fp16
+    N(0, 1) K and V rows up to its length."""
+    import torch
+    from layer_range_stage_gb300 import binding as B
+    from layer_range_stage_gb300.pipeline import StagePipeline
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dist = init_dist(world, "nccl")  # replicas only
+    wl = WORKLOADS[4]
+    model, bounds = synth.CONFIGS[4], wl["bounds"]
+    if args.layers:  # reduced depth: profiling of a small case only, never a bench line
+        model = synth.reduced(model, args.layers)
+        bounds = sorted(set(int(round(x)) for x in np.linspace(0, args.layers, min(4, args.layers) + 1)))
+    nseq = wl["seqs"]
+    lens = batched_lens(nseq)
+    seqs = np.arange(nseq)
+    steps, warmup, n_timing, n_e2e = args.steps, args.warmup, 2, 4
+    max_len = int(lens.max()) + warmup + steps + n_timing + n_e2e + 8
+    t_build = time.time()
+    block = synth.layer_weights(model, 0)
+    kmax = int(lens.max())
+    shape = (model.n_kv_heads, kmax, model.head_dim)
+    size = int(np.prod(shape))
+    kall = synth.normal_f32(synth.key(4400, 0, 0), 0, size, 1.0).reshape(shape).astype(np.float16)
+    vall = synth.normal_f32(synth.key(4400, 0, 1), 0, size, 1.0).reshape(shape).astype(np.float16)
+    kv = [(np.ascontiguousarray(kall[:, :n]), np.ascontiguousarray(vall[:, :n])) for n in lens]
+    first = np.random.default_rng(4402).integers(0, model.vocab, nseq)
+    H, D, F = model.hidden, model.head_dim, model.ffn
+    per_layer = (model.q_dim + 2 * model.kv_dim) * H + H * model.q_dim + 3 * F * H
+    w_bytes = (per_layer * model.n_layers + model.vocab * H + nseq * H) * 1.0625
+    ctx = lens + warmup + steps / 2.0  # positions attended, mean over the timed steps
+    kv_bytes = model.n_layers * 2 * model.n_kv_heads * D * 2 * float(np.sum(ctx + 1))
+    peak = measured_peaks().get("hbm_gbs")
+    stream = torch.cuda.current_stream()
+    paths = {}
+    for path, min_tok in (("f32", 0), ("bf16", nseq)):
+        gp = StagePipeline(model, bounds, lambda l: block, lambda a, b: synth.stage_weights(model, a, b, with_layers=False),
+                           max_seqs=nseq, max_seq_len=max_len, max_tokens=nseq, gemm_bf16_min_tokens=min_tok)
+        try:
+            for st, a, b in zip(gp.stages, bounds, bounds[1:]):
+                for l in range(a, b):
+                    for sq in range(nseq):
+                        B.stage_write_kv(st, l, sq, 0, kv[sq][0], kv[sq][1])
+                B.stage_commit(st, seqs, lens)
+            torch.cuda.synchronize()
+            tok = gp.generate(seqs, first, warmup, use_graph=True)[-1]
+            if dist:
+                dist.barrier()
+            clocks = ClockSampler()
+            clocks.start()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            last = gp.generate(seqs, tok, steps, use_graph=True)[-1]
+            e1.record(stream)
+            torch.cuda.synchronize()
+            clk = clocks.stop()
+            ms = max_over_ranks(e0.elapsed_time(e1), dist, "cuda")
+            # the dominant kernel, the FFN gate/up launch of every block, timed with events
+            # around each launch in a separate run of the same steps
+            gp.kernel_timing(True)
+            last = gp.generate(seqs, last, n_timing, use_graph=True)[-1]
+            torch.cuda.synchronize()
+            k_us, k_n = gp.kernel_time()
+            gp.kernel_timing(False)
+            # e2e: stage_pipeline_step with host arrays (64 ids, positions, tokens in; 64 tokens out)
+            pos = lens + warmup + steps + n_timing
+            tk = last
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            for i in range(n_e2e):
+                tk = gp.step(False, seqs, pos + i, tk, rows=seqs)
+            e2e_s = time.perf_counter() - t0
+        finally:
+            gp.close()
+        ms_step = ms / steps
+        act = 4 if path == "f32" else 2  # the gate/up input and SwiGLU output: f32 rows, or bf16
+        k_bytes = 2 * F * H * 1.0625 + nseq * H * act + nseq * F * act
+        k_gbs = k_bytes / (k_us * 1e-6) / 1e9 if k_us else None
+        paths[path] = {
+            "value": round(aggregate_rate(nseq * steps, ms * 1e-3, world), 1), "ms_per_step": round(ms_step, 3),
+            "hbm_gbs_achieved": round((w_bytes + kv_bytes) / (ms_step * 1e-3) / 1e9, 1),
+            "roofline": {"bound": "hbm", "achieved": round(k_gbs, 1) if k_gbs else None, "peak": peak, "unit": "GB/s",
+                         "frac": round(k_gbs / peak, 4) if (peak and k_gbs) else None, "traffic": None,
+                         "kernel": ("FFN gate/up GEMV, 4 tokens per pass over the weights (SwiGLU epilogue)"
+                                    if path == "f32" else "FFN gate/up tcgen05 GEMM, bf16 operands (SwiGLU epilogue)"),
+                         "bytes_per_launch": round(k_bytes), "mean_launch_us": round(k_us, 2), "launches_timed": k_n,
+                         "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs)" if peak else "fallback"},
+            "e2e": {"value": round(n_e2e * nseq * world / e2e_s, 1), "unit": "tok/s",
+                    "h2d_bytes_per_step": 4 * 3 * nseq + 4 * nseq, "d2h_bytes_per_step": 4 * nseq, "steps": n_e2e},
+            "clocks": clk,
+            # per step: the embedding, per block 5 launches (QKV, attention, O, gate/up, down; the
+            # tensor-core path adds 3 bf16 operand conversions), final norm, readout, argmax, advance
+            "gpu_launches": steps * (1 + model.n_layers * (5 if path == "f32" else 8) + 4),
+        }
+    best = max(paths, key=lambda k: paths[k]["value"])
+    b = paths[best]
+    line = {
+        "metric": "decode tok/s", "value": b["value"], "unit": "tok/s", "n_gpus": world, "steps": steps,
+        "warmup": warmup, "ms_per_step": b["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32 (int8 block-32 weights, fp16 KV)" if best == "f32" else
+                 "bf16 GEMM operands, f32 accumulation (int8 block-32 weights, fp16 KV)",
+        "data": "synthetic (one seeded N(0,0.02) block loaded into all 80; seeded fp16 N(0,1) KV rows)",
+        "config": {"workload": wl["name"], "path": best,
+                   "parallelism": "replicas only" if world > 1 else f"single GPU, {len(bounds) - 1} chained stages",
+                   "l2": f"inputs larger than L2: {w_bytes / 1e9:.1f} GB of weights and {kv_bytes / 1e9:.1f} GB of KV "
+                         "per step"},
+        "hbm_gbs_achieved": b["hbm_gbs_achieved"],
+        "roofline": b["roofline"],
+        "step_roofline": {"bound": "hbm", "achieved": b["hbm_gbs_achieved"], "peak": peak, "unit": "GB/s",
+                          "frac": round(b["hbm_gbs_achieved"] / peak, 4) if peak else None,
+                          "bytes_per_step": round(w_bytes + kv_bytes)},
+        "e2e": b["e2e"], "clocks": b["clocks"], "gpu_launches": b["gpu_launches"],
+        "paths": paths, "wall_s": round(time.time() - t_build, 1),
+    }
+    if args.layers:
+        line["config"]["profiling_case"] = f"{model.n_layers} blocks: not the benchmark workload"
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
 def cpu_baseline(args, budget_s=None):
     """The oracle as it stands, on a bounded sample: decode tokens through 2 of the 32
     blocks at context 2048 (KV filled with seeded fp16 values; the oracle's time does not
@@ -396,13 +535,16 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=0, help="reduced depth, for profiling small cases only")
     ap.add_argument("--context", type=int, default=0, help="decode context (default: the workload's)")
-    ap.add_argument("--config", type=int, default=1, choices=sorted(WORKLOADS), help="1: dense 8B-shape, 2: MoE")
+    ap.add_argument("--config", type=int, default=1, choices=sorted(WORKLOADS),
+                    help="1: dense 8B-shape, 2: MoE, 4: dense 70B-shape batched decode (64 sequences)")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work in the CPU baseline")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.config == 4:
+        run_batched(args)
     else:
         run_gpu(args)
 

@@ -438,14 +438,15 @@ bool weights_ready(stage* st) {
   return true;
 }
 
-// Split-K factor of decode attention: about one CTA per SM, chunks of >= 32 positions,
-// bounded by the partial-result scratch.
+// Split-K factor of decode attention: at least about one CTA per SM, and chunks of at most
+// ~512 positions for the longest sequence of the call (a batch of ragged contexts is as slow
+// as its longest chunk), chunks of >= 32 positions, bounded by the partial-result scratch.
 int attn_chunks(const stage* st, int ntok, int max_len_in_call) {
   const size_t pairs = std::max((size_t)st->cfg.max_seqs * kMaxChunks, (size_t)st->cfg.max_tokens * 4);
   int n = (max_len_in_call + 31) / 32;
   const int work = std::max(1, ntok * st->cfg.n_kv_heads);
   const int fill = std::max(1, (lrs::sm_count() + work - 1) / work);  // about one wave
-  n = std::min(n, fill);
+  n = std::min(n, std::max(fill, (max_len_in_call + 511) / 512));
   n = std::min<int>(n, (int)std::min<size_t>(kMaxChunks, pairs / (size_t)ntok));
   return std::max(1, n);
 }

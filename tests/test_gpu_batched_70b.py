@@ -11,6 +11,12 @@ float32 tolerance; the last stage's input is the handoff of the two middle stage
 readout against the oracle's on
 sampled vocabulary rows (max-abs <= 2e-2) and the greedy tokens against the oracle's full
 argmax wherever its top-2 margin exceeds that tolerance.
+
+Both decode paths of a 64-token call: the float32 GEMV path, and the tensor-core path (the
+stage's GEMM threshold set to 64: every projection a tcgen05 GEMM with bf16 operands and f32
+accumulation) against the oracle with every GEMM operand rounded to bf16, where a block
+output is held to one bf16 ulp (2^-8) in relative L2 -- the bf16 tolerance of the prefill
+tests.  The readout is the float32 GEMV on both paths.
 """
 import numpy as np
 import pytest
@@ -21,7 +27,7 @@ import synth
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
-HIDDEN_RTOL = 1e-3
+HIDDEN_RTOL = {"f32": 1e-3, "bf16": 2.0 ** -8}
 LOGIT_ATOL = 2e-2
 NSEQ = 64
 
@@ -40,12 +46,13 @@ def kv_rows(model, seq, n):
     return k, v
 
 
-def test_70b_shape_batched_decode_ragged_64(cuda):
+@pytest.mark.parametrize("path", ["f32", "bf16"])
+def test_70b_shape_batched_decode_ragged_64(cuda, path):
     from layer_range_stage_gb300 import binding as B
     model = synth.reduced(synth.CONFIGS[4], 4)
     lens = np.random.default_rng(4401).integers(128, 4097, NSEQ)
     max_len = int(lens.max()) + 1
-    cfgc = B.make_cfg(model, NSEQ, max_len, NSEQ)
+    cfgc = B.make_cfg(model, NSEQ, max_len, NSEQ, NSEQ if path == "bf16" else 0)
     seqs = np.arange(NSEQ)
     toks = np.random.default_rng(4402).integers(0, model.vocab, NSEQ)
     stages, ws = [], [synth.stage_weights(model, li, li + 1) for li in range(4)]
@@ -55,6 +62,7 @@ def test_70b_shape_batched_decode_ragged_64(cuda):
         for li in range(4):
             st = B.stage_create(cfgc, li, li + 1, ws[li])
             stages.append(st)
+            assert B.stage_gemm_mode(st, NSEQ) == (1 if path == "bf16" else 0)
             for s in range(NSEQ):
                 B.stage_write_kv(st, li, s, 0, kv[s][0], kv[s][1])
             B.stage_commit(st, seqs, lens)
@@ -82,10 +90,10 @@ def test_70b_shape_batched_decode_ragged_64(cuda):
             ost.k_cache[0, s, :, :lens[s]] = kv[s][0]
             ost.v_cache[0, s, :, :lens[s]] = kv[s][1]
         if li == 0:
-            ref = ost.forward(seqs, lens, tokens=toks)
+            ref = ost.forward(seqs, lens, tokens=toks, gemm=path)
         else:
-            ref = ost.forward(seqs, lens, hidden_in=hg[li - 1])
-        assert rel_l2(hg[li], ref) <= HIDDEN_RTOL, li
+            ref = ost.forward(seqs, lens, hidden_in=hg[li - 1], gemm=path)
+        assert rel_l2(hg[li], ref) <= HIDDEN_RTOL[path], li
         if li == 3:
             head = w.lm_head
             feats = hg[3].astype(np.float64)  # the readout of the GPU's own features
