@@ -1,5 +1,6 @@
 // Prefill-path kernels (sm_103a): the tcgen05 tensor-core GEMM with int8 -> bf16 weight
-// dequantisation in shared memory, and the bf16 conversion of activations.
+// dequantisation in shared memory, the bf16 conversion of activations, and the causal
+// attention of a prefill call on the tensor cores.
 //
 // "41. Many GPUs: tensor, pipeline, expert and data parallelism", section "Pipeline
 // parallelism": a prefill step is the same block loop as decode over all prompt tokens;
