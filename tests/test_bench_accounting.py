@@ -10,6 +10,7 @@ import numpy as np
 import bench
 import synth
 
+
 def test_dense_8b_token_bytes():
     # per block: QKV (32 + 2 * 8) * 128 = 6144 rows x 4096 = 25,165,824; O 4096 x 4096 =
     # 16,777,216; gate, up, down 3 x 14336 x 4096 = 176,160,768 -> 218,103,808 parameters;
