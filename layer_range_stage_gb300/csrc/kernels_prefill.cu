@@ -448,13 +448,17 @@ constexpr int kPR = 64;        // query rows per CTA (four warps of 16)
 constexpr int kPT = 64;        // positions per K/V tile
 constexpr int kPThreads = 128;
 
+// The q rows are staged over the first K/V buffer: they are read into registers before the
+// barrier that opens every sequence's walk, and the walk's first tile lands after it.  68.5 KB
+// per CTA: three CTAs per SM (the registers allow three as well).
 template <int D>
 struct PrefillSmem {
   static constexpr int HROW = D + 8;                       // halves per row: conflict-free ldmatrix
-  static constexpr size_t q = (size_t)kPR * HROW * 2;      // q rows, fp16
+  static constexpr size_t q = (size_t)kPR * HROW * 2;      // q rows, fp16 (over the K/V buffers)
   static constexpr size_t tile = (size_t)kPT * HROW * 2;   // one K or V tile
   static constexpr size_t kv = 2 * 2 * tile;               // [2 buffers][K, V]
-  static constexpr size_t total = q + kv + 2 * kPR * 4;    // + each row's sequence and position
+  static constexpr size_t total = kv + 2 * kPR * 4;        // + each row's sequence and position
+  static_assert(q <= kv, "q staging over the K/V buffers");
 };
 
 __device__ __forceinline__ void ldsm_x4(uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3, const void* p) {
@@ -490,9 +494,9 @@ __global__ void __launch_bounds__(kPThreads) attn_prefill_kernel(const AttnArgs 
   constexpr int NT = D / 8;            // 8-dim tiles of the output
   constexpr int PN = kPT / 8;          // 8-position tiles of the scores
   extern __shared__ __align__(16) unsigned char ps_raw[];
-  __half* qs = reinterpret_cast<__half*>(ps_raw);
-  __half* kvs = reinterpret_cast<__half*>(ps_raw + S::q);  // [buffer][K, V][kPT][HROW]
-  int* rseq = reinterpret_cast<int*>(ps_raw + S::q + S::kv);  // [kPR] sequence of the row's token (-1: none)
+  __half* kvs = reinterpret_cast<__half*>(ps_raw);          // [buffer][K, V][kPT][HROW]
+  __half* qs = kvs;                                           // q rows until the first walk
+  int* rseq = reinterpret_cast<int*>(ps_raw + S::kv);         // [kPR] sequence of the row's token (-1: none)
   int* rpos = rseq + kPR;                                      // [kPR] its position
   pdl_trigger();
   pdl_wait();
@@ -558,7 +562,7 @@ __global__ void __launch_bounds__(kPThreads) attn_prefill_kernel(const AttnArgs 
       }
       cp_async_commit();
     };
-    __syncthreads();  // the previous walk is done with the tile buffers
+    __syncthreads();  // the q staging, or the previous walk, is done with the tile buffers
     fetch(0, 0);
     int buf = 0;
     for (int p0 = 0; p0 <= maxpos; p0 += kPT, buf ^= 1) {
