@@ -118,3 +118,25 @@ def test_moe_stage_routes_and_runs():
     assert np.array_equal(toks, toks_u)
     for a, b in zip(logits, logits_u):
         assert np.array_equal(a, b)
+
+
+def test_batched_ragged_decode_equals_each_sequence_alone():
+    """A decode step of several sequences at their own positions (ragged contexts, listed out
+    of order) computes, row for row, what each sequence's step computes alone: the batched
+    70B-shape parity rests on the oracle keeping the rows of a batch independent."""
+    cfg = synth.CONFIGS[0]
+    lens = [5, 17, 11]
+    prompts = [synth.prompt_tokens(cfg, 20 + s, n) for s, n in enumerate(lens)]
+
+    def prefilled():
+        p = build_pipeline(cfg, [0, 2, 4], gamma_mode="seeded", max_seqs=3)
+        for s, pr in enumerate(prompts):
+            p.forward(np.full(len(pr), s), np.arange(len(pr)), pr)
+        return p
+
+    order = [2, 0, 1]
+    toks = [int(prompts[s][-1]) for s in order]
+    batched = prefilled().forward(order, [lens[s] for s in order], toks)
+    for row, s in enumerate(order):
+        alone = prefilled().forward([s], [lens[s]], [toks[row]])
+        assert np.allclose(batched[row], alone[0], rtol=1e-12, atol=1e-12), s
