@@ -225,7 +225,10 @@ STAGE_API int stage_write_kv(stage_t st, int global_layer, int seq_id, int pos0,
  * call: every block of the stage in one cooperative launch, on MoE stages with the router
  * and top-k computed inside it; same arithmetic per weight as 0, its own fixed summation
  * order).  The environment variable LRS_PERSISTENT=0, read at
- * stage_create, turns mode 2 off. */
+ * stage_create, turns mode 2 off.  LRS_PDL=0, also read at stage_create, launches the
+ * per-kernel paths (modes 0 and 1) without programmatic dependent launch: each kernel then
+ * starts only after its predecessor on the stream has finished, instead of overlapping its
+ * weight-only prologue with the predecessor's tail (process-wide; for measurement). */
 STAGE_API int stage_gemm_mode(stage_t st, int n_tokens, int* mode_out);
 
 STAGE_API const char* stage_last_error(stage_t st);
@@ -237,7 +240,13 @@ STAGE_API void stage_destroy(stage_t st);
 
 /* Host-side fault injection for tests (no GPU fault is ever caused):
  *   what = 1: mark the stage busy (value 1) or idle (value 0) as if a call were in progress;
- *   what = 2: the next prefill/decode returns STAGE_E_INJECTED before launching anything. */
+ *   what = 2: the next prefill/decode returns STAGE_E_INJECTED before launching anything;
+ *   what = 3 (value 1): the next single-token decode that runs on the persistent kernel (outside
+ *     stream capture) waits at its grid barriers for one CTA more than the grid holds.  Every
+ *     such wait runs out after its time limit (0.2 s); the kernel then sets the stage's error
+ *     word, waits (bounded) for its own copies in flight and leaves, so the call reports
+ *     STAGE_E_CUDA when its error word is read and the next call runs normally.  This tests
+ *     the device-side timeout path without faulting or hanging the GPU. */
 STAGE_API int stage_debug_inject(stage_t st, int what, int value);
 
 /* ------------------------------------------------------------------------- pipeline

@@ -24,6 +24,15 @@ STAGE_API int stage_op_q8_device_bytes(int64_t rows, int64_t cols, size_t* q_byt
  * Synchronous. */
 STAGE_API int stage_op_q8_pack(const stage_q8* host, void* q_dev, void* s_dev);
 
+/* Embedding rows: out[t][c] = scale(tok[t], c / 32) * q[tok[t]][c] for t < n_tok, c < cols --
+ * the dequantised row of each token, as the first stage embeds its tokens ("RFC: pipeline
+ * placement across multiple GPUs for models larger than one device", section "What I found":
+ * the first stage embeds).  W is a packed [rows x cols] matrix (stage_op_q8_pack); tok_dev:
+ * device int32 [n_tok], every entry in [0, rows) (not checked on the device); out_dev: f32
+ * [n_tok][cols], 16-byte aligned, cols a multiple of 4.  Runs on `stream`. */
+STAGE_API int stage_op_embed(const void* q_dev, const void* s_dev, int64_t rows, int64_t cols, const int32_t* tok_dev,
+                             int n_tok, float* out_dev, void* stream);
+
 /* y[t][r] = sum_k W[r][k] * h[t][k] for t < n_tok, r < rows, where h = x, or
  * h = x / sqrt(mean(x^2) + eps) * gamma when gamma_dev is not NULL (the RMSNorm that
  * precedes every projection of a block: "41. Many GPUs: tensor, pipeline, expert and

@@ -101,6 +101,8 @@ _SIGS = {
     "stage_pipeline_destroy": (None, [C.c_void_p]),
     "stage_op_q8_device_bytes": (C.c_int, [C.c_int64, C.c_int64, C.POINTER(C.c_size_t), C.POINTER(C.c_size_t)]),
     "stage_op_q8_pack": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p]),
+    "stage_op_embed": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int64, C.c_int64, C.c_void_p, C.c_int, C.c_void_p,
+                                 C.c_void_p]),
     "stage_op_gemv": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int64, C.c_int64, C.c_void_p, C.c_int, C.c_void_p,
                                 C.c_float, C.c_void_p, C.c_void_p]),
     "stage_op_attention_workspace_bytes": (C.c_size_t, [C.c_int] * 5),
@@ -420,6 +422,12 @@ def stage_op_q8_pack(m, q_dev, s_dev) -> None:
     keep = _Keep()
     h = keep.q8(m)
     _opcheck(lib().stage_op_q8_pack(C.byref(h), q_dev.data_ptr(), s_dev.data_ptr()))
+
+
+def stage_op_embed(q_dev, s_dev, rows: int, cols: int, tok, out, stream=None) -> None:
+    """tok: int32 device tensor [n_tok]; out: f32 device tensor [n_tok, cols]."""
+    _opcheck(lib().stage_op_embed(q_dev.data_ptr(), s_dev.data_ptr(), rows, cols, tok.data_ptr(), tok.shape[0],
+                                  out.data_ptr(), _stream(stream)))
 
 
 def stage_op_gemv(q_dev, s_dev, rows: int, cols: int, x, y, gamma=None, eps: float = 1e-5, stream=None) -> None:

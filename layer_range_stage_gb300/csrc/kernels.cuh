@@ -146,6 +146,7 @@ struct MegaArgs {
   unsigned* bar = nullptr;  // [64]: grid barrier counter, exit counter, per-KV-head attention
                             // counters; zero between launches (the last CTA out re-zeroes)
   int* err = nullptr;
+  unsigned bar_extra = 0;  // tests: arrivals every grid barrier waits for beyond the grid (0 in use)
 };
 // Whether the persistent decode covers this shape (and the shared memory it needs fits).  MoE:
 // n_experts > 0, F = top_k * expert FFN width (the gathered down input).

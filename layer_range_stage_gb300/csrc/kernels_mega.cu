@@ -13,14 +13,23 @@ bool g_mega_ready = false;
 bool mega_supported(int H, int q_dim, int F, int head_dim, int group, int n_experts, int top_k) {
   if (!g_mega_ready) return false;
   if (n_experts > kMaxExperts || top_k > kMaxTopK || (n_experts > 0 && top_k < 1)) return false;
-  if (n_experts > 0 && (F % top_k || F / top_k > kSlotQ / 2)) return false;  // a row pair's expert piece fits a slot
+  if (n_experts > 0 && F % top_k) return false;
   if (n_experts & 1) return false;  // router rows go in pairs
   if (head_dim != 64 && head_dim != 128) return false;
   if (group != 1 && group != 2 && group != 4 && group != 8) return false;
   if (q_dim / head_dim / group > 62) return false;  // per-KV-head counters in the 64-word barrier block
   if ((H & 3) || (q_dim & 3) || (F & 3)) return false;
   const int Kx = std::max(pad256(H), std::max(pad256(q_dim), pad256(F)));
-  if (Kx > kMaxKp || (Kx + kSlotQ / 2 - 1) / (kSlotQ / 2) > kMaxBlocks) return false;
+  if (Kx > kMaxKp) return false;
+  // the pieces of a warp's range in its largest projection (rows: gate/up 2F or the expert rows)
+  const int G = sm_count();
+  const int rows[] = {q_dim + 2 * (q_dim / group), H, n_experts, 2 * F, H};
+  const int kp[] = {pad256(H), pad256(q_dim), pad256(H), pad256(H), pad256(F)};
+  for (int i = 0; i < 5; ++i) {
+    const long long np = (rows[i] / 2 + G - 1) / G;  // pairs of the fullest CTA
+    const long long cols = (np * kp[i] / kUnit + kMW - 1) / kMW * kUnit;
+    if (np > kMaxCtaPairs || cols / kp[i] + 2 > kMaxPieces) return false;
+  }
   return mega_smem(H, q_dim, F, head_dim, group) <= kMaxSmem;
 }
 

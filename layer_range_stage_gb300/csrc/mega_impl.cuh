@@ -59,7 +59,6 @@ constexpr int kSlotS = kSlotQ / 16;           // scale bytes per slot (one fp16 
 template <int D>
 constexpr int attn_tile() { return D == 64 ? 256 : 128; }  // attention positions per tile (64 KB of K + V)
 constexpr int kMaxKp = 16384;                 // largest projection input (floats in shared memory)
-constexpr int kMaxBlocks = 8;  // column blocks per row of a projection
 constexpr uint64_t kWaitNs = 200000000ull;    // bound of every wait: 0.2 s
 constexpr size_t kMaxSmem = 227 * 1024;
 
@@ -73,11 +72,11 @@ constexpr int kMaxExperts = 256, kMaxTopK = 32;
 constexpr size_t kOffLogits = kOffMoe, kOffIds = kOffLogits + kMaxExperts * 4, kOffWts = kOffIds + kMaxTopK * 4,
                  kOffSel = kOffWts + kMaxTopK * 4, kOffSelId = kOffSel + kMaxTopK * 4,
                  kOffReady = kOffSelId + kMaxTopK * 4;
-constexpr size_t kOffShapes = kOffMoe + (kMaxExperts + 4 * kMaxTopK + 4) * 4;  // [kPhases] shapes
-constexpr size_t kOffWptr = kOffShapes + 256;                             // [kMW][2] stream pointers
+constexpr size_t kOffSplit = kOffMoe + (kMaxExperts + 4 * kMaxTopK + 4) * 4;  // [kPhases] Split
+constexpr size_t kOffWptr = kOffSplit + 224;                               // [kMW][2] stream pointers
 // the phases of a block's weight stream
 constexpr int kPhQKV = 0, kPhO = 1, kPhRouter = 2, kPhGU = 3, kPhDown = 4, kPhases = 5;
-constexpr size_t kOffXraw = kOffMoe + 2304;                               // [Kp(H)] floats
+constexpr size_t kOffXraw = kOffMoe + 2048;                               // [Kp(H)] floats
 
 __host__ __device__ constexpr int pad256(int k) { return (k + 255) / 256 * 256; }
 
@@ -120,23 +119,50 @@ __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
   return v;
 }
 
-// The weight stream of one warp: producer cursor (block l, projection ph, task t, slot j)
-// and the counts of slots issued and consumed.
-struct Stream {
-  int l, ph, t, j;
-  int issued, consumed;
+// How a projection is dealt over the grid.  Rows go in pairs (2P, 2P + 1): the pairs the RoPE
+// and SwiGLU epilogues need, and for the other projections two rows that share each load of
+// the staged input.  CTA c owns pairs [p0, p0 + np) with p0 = c * NP / G, so every CTA holds
+// the same number of pairs to within one.  Inside a CTA the pairs' K ranges are laid end to end
+// (np * Kp columns) and cut into 16 contiguous warp ranges of whole 256-column units, so a
+// warp may hold the tail of one pair, some whole pairs and the head of another; each warp sums
+// its pieces, and after the phase the CTA adds, per pair, the pieces of the warps that hold
+// it in warp order -- one fixed summation order per output.
+struct Split {
+  int NP;    // pairs of the projection
+  int Kp;    // columns of a pair's K range (mode 2: top_k expert pieces of PS columns)
+  int seg;   // columns between source discontinuities (Kp, or PS in mode 2)
+  int mode;  // 0 plain rows; 1 rows of the selected experts (rps rows each); 2 piece j of a row
+             // from selected expert j (K gathered over the experts)
+  int rps;
+  int p0, np;  // this CTA's pairs: p0 + i * pstride for i < np
+  int pstride;
+  int upp;     // units (256 columns) of a pair: Kp / 256
+  int U;       // this CTA's units: np * upp
 };
 
-// One projection's shape as the weight stream sees it: the same in every block of a stage.
-struct Shape {
-  int N, Kp;          // rows (of the projection as computed); row stride in bytes (scales: Kp / 32)
-  int T;              // tasks: N / R
-  int klen;           // bytes of a row's K range
-  int R, P, PS;       // rows per task (2), column blocks per task, bytes per row of a block
-  int B;              // column blocks per ring slot (several whole blocks share a slot)
-  int mode;           // 0 plain rows; 1 rows of the selected experts (rps rows each); 2 piece j of a
-                      // row from selected expert j (K gathered over the experts)
-  int rps;
+constexpr int kUnit = 256;             // columns of a unit (warp ranges and segments are whole units)
+constexpr int kSlotCols = kSlotQ / 2;  // columns of each row in a ring slot
+constexpr int kMaxPieces = 16;         // pairs a warp's range may touch in one projection
+constexpr int kMaxCtaPairs = 256;      // pairs a CTA may hold in one projection
+// per-projection scratch after the staged input: warp partials, piece counters, the warp
+// ranges, the RoPE factors of the CTA's QKV pairs
+constexpr size_t kPsPart = 0, kPsCnt = kPsPart + (size_t)kMW * kMaxPieces * 8, kPsWu0 = kPsCnt + kMaxCtaPairs * 4,
+                 kPsPf = kPsWu0 + 128, kPsRope = kPsPf + 128, kPsBytes = kPsRope + (size_t)kMaxCtaPairs * 8;
+
+// A position in a warp's range of one projection: CTA-local pair pr, column k of the pair, ks =
+// column within its source segment, and the columns of the range still to go.  The issuer and
+// the consumer of a warp's ring walk the same sequence of cursors, so a slot's contents never
+// have to be written down.
+struct Cur {
+  int pr, k, ks, left;
+};
+
+// The weight stream of one warp: block l, projection ph, the cursor of the next slot, and the
+// counts of slots issued and consumed.
+struct Stream {
+  int l, ph;
+  Cur q;
+  int issued, consumed;
 };
 
 // Everything in shared memory is at a fixed offset from one base (no pointer per region
@@ -144,7 +170,14 @@ struct Shape {
 struct Ctx {
   const MegaArgs* a;
   unsigned char* sm;
-  int lane, warp, gw, GW;
+  unsigned char* ps;  // per-projection scratch after the staged input (see kPs*)
+  int lane, warp;
+  // [kMW][kMaxPieces] partial sums (rows 2P, 2P + 1) of pairs split between warps
+  __device__ float2* part() const { return reinterpret_cast<float2*>(ps + kPsPart); }
+  __device__ int* cnt() const { return reinterpret_cast<int*>(ps + kPsCnt); }     // [kMaxCtaPairs] pieces done
+  __device__ int* wu0() const { return reinterpret_cast<int*>(ps + kPsWu0); }     // [kMW + 1] first unit of each warp
+  __device__ int* pf() const { return reinterpret_cast<int*>(ps + kPsPf); }       // [kMW] first pair of each warp
+  __device__ float2* rope_s() const { return reinterpret_cast<float2*>(ps + kPsRope); }  // [kMaxCtaPairs] (QKV)
   __device__ unsigned char* ringq() const { return sm + kOffRingQ; }
   __device__ unsigned char* rings() const { return sm + kOffRingS; }
   __device__ uint64_t* bars() const { return reinterpret_cast<uint64_t*>(sm + kOffBars); }  // [kMW][kDepth], attention
@@ -160,188 +193,159 @@ struct Ctx {
   __device__ volatile int* moe_ready() const {  // last block whose routing is known
     return reinterpret_cast<volatile int*>(sm + kOffReady);
   }
-  __device__ const Shape* shape() const { return reinterpret_cast<const Shape*>(sm + kOffShapes); }  // [kPhases]
+  __device__ const Split* split() const { return reinterpret_cast<const Split*>(sm + kOffSplit); }  // [kPhases]
   // [kMW][2] weights and scales of each warp's stream cursor (l, ph): an issue reads them
   // here, not from the block descriptor
   __device__ const void** wptr() const { return reinterpret_cast<const void**>(sm + kOffWptr); }
 };
 
-// ph: kPhQKV, kPhO, kPhRouter (MoE stages: one logit per task, into global memory), kPhGU
+// The projections of a block: weights of phase ph.
+template <bool MOE>
+__device__ __forceinline__ const DevQ8& phase_w(const MegaLayer& L, int ph) {
+  if (MOE && ph == kPhRouter) return L.router;
+  if (MOE && ph >= kPhGU) return ph == kPhGU ? L.egu : L.edown;
+  return ph == kPhQKV ? L.wqkv : ph == kPhO ? L.wo : ph == kPhGU ? L.wgu : L.wdown;
+}
+
+// ph: kPhQKV, kPhO, kPhRouter (MoE stages: one logit per row, into global memory), kPhGU
 // (dense, or the selected experts' rows), kPhDown (dense, or gathered over the experts).
 // Computed once per launch (from block 0: every block has the same shapes).
-__device__ Shape shape_of(const MegaArgs& a, int ph) {
+__device__ Split split_of(const MegaArgs& a, int ph, int cta, int G) {
   const MegaLayer& L = a.layers[0];
   const bool moe = a.n_experts > 0;
-  Shape p;
+  Split p;
   p.mode = 0;
   p.rps = 0;
-  p.R = 2;  // every task is a row pair: each load of the staged input serves both rows
-  if (ph == kPhRouter && !moe) {  // dense stages: no router tasks
-    p.N = p.T = 0;
-    p.Kp = p.klen = p.PS = 256;
-    p.P = p.B = 1;
-    return p;
-  }
-  const DevQ8* w;
-  if (ph == kPhRouter) {
-    w = &L.router;
-    p.N = a.n_experts;
-  } else if (moe && ph >= kPhGU) {
-    if (ph == kPhGU) {
-      w = &L.egu;
-      p.N = a.top_k * 2 * a.EF;
+  if (ph == kPhRouter && !moe) {  // dense stages: no router rows
+    p.NP = 0;
+    p.Kp = p.seg = kUnit;
+  } else {
+    const DevQ8& w = moe ? phase_w<true>(L, ph) : phase_w<false>(L, ph);
+    int N = w.N;
+    p.Kp = p.seg = w.Kp;
+    if (moe && ph == kPhGU) {
+      N = a.top_k * 2 * a.EF;
       p.mode = 1;
       p.rps = 2 * a.EF;
-    } else {
-      w = &L.edown;
-      p.N = a.H;
+    } else if (moe && ph == kPhDown) {
+      N = a.H;
       p.mode = 2;
+      p.Kp = a.top_k * w.Kp;
     }
-  } else {
-    w = ph == kPhQKV ? &L.wqkv : ph == kPhO ? &L.wo : ph == kPhGU ? &L.wgu : &L.wdown;
-    p.N = w->N;
+    p.NP = N / 2;
   }
-  p.Kp = w->Kp;
-  p.T = p.N / p.R;
-  if (p.mode == 2) {
-    p.P = a.top_k;
-    p.PS = w->Kp;
-    p.klen = p.P * p.PS;
-  } else {
-    p.klen = w->Kp;
-    p.P = (w->Kp + kSlotQ / 2 - 1) / (kSlotQ / 2);
-    p.PS = ((w->Kp / p.P + 255) / 256) * 256;
-  }
-  p.B = (p.klen % p.PS == 0) ? max(1, kSlotQ / (2 * p.PS)) : 1;
+  p.p0 = (int)((long long)cta * p.NP / G);
+  p.pstride = 1;
+  p.np = (int)((long long)(cta + 1) * p.NP / G) - p.p0;
+  p.upp = p.Kp / kUnit;
+  p.U = p.np * p.upp;
   return p;
 }
 
-struct Ph : Shape {  // one projection of a block: its shape and its weights
-  const uint8_t* q;
-  const uint16_t* s;
-};
+// Units [u0, u1) of warp w in a projection.
+__device__ __forceinline__ int warp_u0(const Split& p, int w) { return w * p.U / kMW; }
 
-template <bool MOE>
-__device__ __forceinline__ Ph phase_of(const Ctx& c, int l, int ph) {
-  const MegaLayer& L = c.a->layers[l];
-  const DevQ8& w = (MOE && ph == kPhRouter) ? L.router
-                   : (MOE && ph >= kPhGU)   ? (ph == kPhGU ? L.egu : L.edown)
-                   : ph == kPhQKV ? L.wqkv : ph == kPhO ? L.wo : ph == kPhGU ? L.wgu : L.wdown;
-  Ph p;
-  static_cast<Shape&>(p) = c.shape()[ph];
-  p.q = w.q;
-  p.s = w.s;
-  return p;
+// The cursor at the start of warp w's range in projection p.
+__device__ __forceinline__ Cur cur_start(const Split& p, int w) {
+  const int u0 = warp_u0(p, w), u1 = warp_u0(p, w + 1);
+  Cur q;
+  q.pr = u0 / p.upp;
+  q.k = (u0 - q.pr * p.upp) * kUnit;
+  q.ks = q.k % p.seg;
+  q.left = (u1 - u0) * kUnit;
+  return q;
 }
 
-// Column blocks of this warp's share of a phase from task t, block j on, counted up to `cap`.
-__device__ __forceinline__ int blocks_upto(const Ctx& c, const Shape& p, int t, int j, int cap) {
-  int n = p.P - j;
-  for (int tt = t + c.GW; n < cap && tt < p.T; tt += c.GW) n += p.P;
-  return min(n, cap);
+// Columns of the slot at q: to the end of the range, of the pair or of the source segment, at
+// most kSlotCols.
+__device__ __forceinline__ int cur_len(const Split& p, const Cur& q) {
+  return min(min(q.left, kSlotCols), min(p.Kp - q.k, p.seg - q.ks));
 }
 
-// Global addresses of piece (row, pc) of a phase.
+__device__ __forceinline__ void cur_advance(const Split& p, Cur& q, int len) {
+  q.left -= len;
+  q.k += len;
+  q.ks += len;
+  if (q.ks == p.seg) q.ks = 0;
+  if (q.k == p.Kp) {
+    q.k = 0;
+    q.ks = 0;
+    ++q.pr;
+  }
+}
+
+// Global addresses of rows (2P, 2P + 1) of a projection at column k (P phase-global).
 template <bool MOE>
-__device__ __forceinline__ void piece_src(const Ctx& c, const Ph& p, int row, int pc, const uint8_t*& q,
-                                          const uint16_t*& sc) {
-  if (MOE && p.mode == 2) {
-    const size_t r = (size_t)c.moe_ids()[pc] * p.N + row;
-    q = p.q + r * p.PS;
-    sc = p.s + r * (p.PS / 32);
+__device__ __forceinline__ void pair_src(const Ctx& c, const Split& p, const uint8_t* wq, const uint16_t* ws, int P,
+                                         int k, int kk, const uint8_t*& q, const uint16_t*& sc, size_t& qstride,
+                                         size_t& sstride) {
+  if (MOE && p.mode == 2) {  // K gathered: columns [j PS, (j + 1) PS) from selected expert j; kk = k % PS
+    const int j = (k - kk) / p.seg;
+    const size_t r = (size_t)c.moe_ids()[j] * (size_t)(2 * p.NP) + 2 * P;
+    q = wq + r * p.seg + kk;
+    sc = ws + r * (p.seg / 32) + kk / 32;
+    qstride = p.seg;
+    sstride = p.seg / 32;
     return;
   }
-  size_t r = row;
-  if (MOE && p.mode == 1) r = (size_t)c.moe_ids()[row / p.rps] * p.rps + row % p.rps;
-  q = p.q + r * p.Kp + (size_t)pc * p.PS;
-  sc = p.s + r * (p.Kp / 32) + (size_t)pc * p.PS / 32;
+  size_t r = 2 * (size_t)P;
+  if (MOE && p.mode == 1) r = (size_t)c.moe_ids()[2 * P / p.rps] * p.rps + (2 * P) % p.rps;
+  q = wq + r * p.Kp + k;
+  sc = ws + r * (p.Kp / 32) + k / 32;
+  qstride = p.Kp;
+  sstride = p.Kp / 32;
 }
 
+// Move a cursor to the first non-empty warp range at or after (l, ph).
 template <bool MOE>
 __device__ __forceinline__ void stream_normalise(const Ctx& c, Stream& s) {
   bool moved = false;
-  while (s.l < c.a->nl) {
-    if (s.t < c.shape()[s.ph].T) break;
-    s.j = 0;
+  while (s.l < c.a->nl && s.q.left == 0) {
     if (++s.ph == kPhases) {
       s.ph = 0;
       ++s.l;
     }
-    s.t = c.gw;
+    s.q = cur_start(c.split()[s.ph], c.warp);
     moved = true;
   }
-  if (moved && s.l < c.a->nl) {
-    const Ph p = phase_of<MOE>(c, s.l, s.ph);
-    c.wptr()[2 * c.warp] = p.q;
-    c.wptr()[2 * c.warp + 1] = p.s;
+  if (moved && s.l < c.a->nl && c.lane == 0) {
+    const DevQ8& w = phase_w<MOE>(c.a->layers[s.l], s.ph);
+    c.wptr()[2 * c.warp] = w.q;
+    c.wptr()[2 * c.warp + 1] = w.s;
   }
+  __syncwarp();
 }
 
-// Advance a cursor past its current slot (no copy).
-template <bool MOE>
-__device__ __forceinline__ void stream_step(const Ctx& c, Stream& s, const Shape& p) {
-  if (++s.j == p.P) {
-    s.j = 0;
-    s.t += c.GW;
-    stream_normalise<MOE>(c, s);
-  }
-}
-
-// Issue the next slot of this warp's stream (if any) into the ring: one column block of a
-// row pair (the two rows' pieces side by side), or up to B whole blocks of the same phase.
+// Issue the next slot of this warp's stream (if any) into the ring: cur_len columns of one pair
+// from the cursor, row 2P's bytes at the start of the slot and row 2P + 1's at kSlotCols.
 // Slices of the selected experts wait until the routing of their block is known.
 template <bool MOE>
 __device__ __forceinline__ void stream_issue(const Ctx& c, Stream& s) {
   if (s.l >= c.a->nl) return;
   if (MOE && s.ph >= kPhGU && s.l > *c.moe_ready()) return;
-  Ph p;
-  static_cast<Shape&>(p) = c.shape()[s.ph];
-  p.q = static_cast<const uint8_t*>(c.wptr()[2 * c.warp]);
-  p.s = static_cast<const uint16_t*>(c.wptr()[2 * c.warp + 1]);
+  const Split& p = c.split()[s.ph];
   const int slot = s.issued % kDepth;
-  uint64_t* bar = c.bars() + c.warp * kDepth + slot;
-  unsigned char* dq = c.ringq() + (size_t)(c.warp * kDepth + slot) * kSlotQ;
-  unsigned char* ds = c.rings() + (size_t)(c.warp * kDepth + slot) * kSlotS;
-  if (p.B == 1 && p.mode == 0) {  // one block of two plain rows
-    const int row = 2 * s.t, off = s.j * p.PS, bytes = min(p.PS, p.klen - off);
-    if (c.lane == 0) {
-      const uint8_t* q = p.q + (size_t)row * p.Kp + off;
-      const uint16_t* sc = p.s + (size_t)row * (p.Kp / 32) + off / 32;
-      fence_async_smem();  // the slot's previous contents were read through the generic proxy
-      mbar_arrive_expect_tx(bar, (uint32_t)(2 * (bytes + bytes / 16)));
-      bulk_g2s(dq, q, (uint32_t)bytes, bar);
-      bulk_g2s(dq + p.PS, q + p.Kp, (uint32_t)bytes, bar);
-      bulk_g2s(ds, sc, (uint32_t)(bytes / 16), bar);
-      bulk_g2s(ds + p.PS / 16, sc + p.Kp / 32, (uint32_t)(bytes / 16), bar);
-    }
-    ++s.issued;
-    stream_step<MOE>(c, s, p);
-    return;
-  }
-  const int nb = p.B == 1 ? 1 : blocks_upto(c, p, s.t, s.j, p.B);
+  const int len = cur_len(p, s.q);
   if (c.lane == 0) {
-    fence_async_smem();
-    const int bytes0 = min(p.PS, p.klen - s.j * p.PS);
-    mbar_arrive_expect_tx(bar, (uint32_t)(nb == 1 ? 2 * (bytes0 + bytes0 / 16) : nb * 2 * (p.PS + p.PS / 16)));
-  }
-  for (int u = 0; u < nb; ++u) {
-    const int pc = s.j, row = 2 * s.t, bytes = min(p.PS, p.klen - pc * p.PS);
-    if (c.lane == 0) {
-      for (int rr = 0; rr < 2; ++rr) {
-        const uint8_t* q;
-        const uint16_t* sc;
-        piece_src<MOE>(c, p, row + rr, pc, q, sc);
-        bulk_g2s(dq + (2 * u + rr) * p.PS, q, (uint32_t)bytes, bar);
-        bulk_g2s(ds + (2 * u + rr) * (p.PS / 16), sc, (uint32_t)(bytes / 16), bar);
-      }
-    }
-    if (u + 1 < nb && ++s.j == p.P) {  // stays inside the phase: nb counted its blocks left
-      s.j = 0;
-      s.t += c.GW;
-    }
+    const uint8_t* q;
+    const uint16_t* sc;
+    size_t qst, sst;
+    pair_src<MOE>(c, p, static_cast<const uint8_t*>(c.wptr()[2 * c.warp]),
+                  static_cast<const uint16_t*>(c.wptr()[2 * c.warp + 1]), p.p0 + s.q.pr * p.pstride, s.q.k, s.q.ks,
+                  q, sc, qst, sst);
+    uint64_t* bar = c.bars() + c.warp * kDepth + slot;
+    unsigned char* dq = c.ringq() + (size_t)(c.warp * kDepth + slot) * kSlotQ;
+    unsigned char* ds = c.rings() + (size_t)(c.warp * kDepth + slot) * kSlotS;
+    fence_async_smem();  // the slot's previous contents were read through the generic proxy
+    mbar_arrive_expect_tx(bar, (uint32_t)(2 * (len + len / 16)));
+    bulk_g2s(dq, q, (uint32_t)len, bar);
+    bulk_g2s(dq + kSlotCols, q + qst, (uint32_t)len, bar);
+    bulk_g2s(ds, sc, (uint32_t)(len / 16), bar);
+    bulk_g2s(ds + kSlotCols / 16, sc + sst, (uint32_t)(len / 16), bar);
   }
   ++s.issued;
-  stream_step<MOE>(c, s, p);
+  cur_advance(p, s.q, len);
+  if (s.q.left == 0) stream_normalise<MOE>(c, s);
 }
 
 // Top the ring up to kDepth slots (after the routing of a block became known).
@@ -370,7 +374,7 @@ __device__ __forceinline__ void set_error(const Ctx& c) {
 __device__ bool grid_barrier(const Ctx& c, unsigned k) {
   __syncthreads();
   if (threadIdx.x == 0 && !c.flag()[0]) {
-    const unsigned target = k * gridDim.x;
+    const unsigned target = k * gridDim.x + c.a->bar_extra;
     red_release_add(c.a->bar, 1u);
     if (ld_acquire_u32(c.a->bar) < target) {
       const uint64_t t0 = global_ns();
@@ -402,39 +406,42 @@ __device__ void grid_leave(const Ctx& c) {
 
 // A projection input from global memory (written earlier in this launch: read through L2)
 // into shared memory: normalised by RMSNorm with gamma when given, scaled by 2^64,
-// swizzled per 16-float chunk, with chunk sums; the raw values also into xraw when given.
-// Thread `tid` owns chunks tid and tid + kMT: every load (x and gamma) is issued before
-// any is used, so the staging costs one round trip to L2.
-__device__ void stage_input(const Ctx& c, const float* x, int K, int Kp, const float* gamma, float eps, float* xs,
-                            float* xc, float* xraw) {
-  constexpr int CPT = kMaxKp / 16 / kMT;  // chunks per thread
-  const int tid = threadIdx.x, nchunk = Kp >> 4;
-  const float4* x4 = reinterpret_cast<const float4*>(x);
-  const float4* g4 = reinterpret_cast<const float4*>(gamma);
-  float4 v[CPT][4], gm[CPT][4];
-#pragma unroll
-  for (int k2 = 0; k2 < CPT; ++k2) {
-    const int ch = tid + k2 * kMT;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int k = ch * 16 + 4 * j;  // K is a multiple of 4: a float4 lies wholly inside or outside
-      const bool in = ch < nchunk && k < K;
-      v[k2][j] = in ? __ldcg(x4 + (k >> 2)) : make_float4(0.f, 0.f, 0.f, 0.f);
-      gm[k2][j] = (in && gamma) ? __ldg(g4 + (k >> 2)) : make_float4(0.f, 0.f, 0.f, 0.f);
+// swizzled per 16-float chunk, with chunk sums.  With gamma the raw values land in xraw
+// (kept for the residual adds) and gamma in xs, which is then overwritten in place; without,
+// the raw values land in xs.  Every 16-byte piece is an asynchronous copy issued before any
+// is waited for (stage_finish), so the staging costs one round trip to L2 and no registers.
+__device__ void stage_issue(const float* x, int K, int Kp, const float* gamma, float* xs, float* xraw) {
+  const int tid = threadIdx.x;
+  float* raw = gamma ? xraw : xs;
+  for (int i = tid; i < (Kp >> 2); i += kMT) {  // K is a multiple of 4: a piece lies wholly inside or outside
+    if (4 * i < K) {
+      cp_async16(raw + 4 * i, x + 4 * i);
+      if (gamma) cp_async16(xs + 4 * i, gamma + 4 * i);
+    } else {
+      reinterpret_cast<float4*>(raw)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (gamma) reinterpret_cast<float4*>(xs)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
   }
+}
+
+// The second half of the staging (after stage_issue and any other loads of the phase's setup):
+// wait for the copies, then RMSNorm, scaling, swizzle and chunk sums in place.
+__device__ void stage_finish(const Ctx& c, int K, int Kp, const float* gamma, float eps, float* xs, float* xc,
+                             float* xraw) {
+  const int tid = threadIdx.x, nchunk = Kp >> 4;
+  const float* raw = gamma ? xraw : xs;
+  cp_async_wait_all();
+  __syncthreads();
   float rinv = 1.0f;
   if (gamma) {
     float ss = 0.f;
-#pragma unroll
-    for (int k2 = 0; k2 < CPT; ++k2)
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        ss = fmaf(v[k2][j].x, v[k2][j].x, ss);
-        ss = fmaf(v[k2][j].y, v[k2][j].y, ss);
-        ss = fmaf(v[k2][j].z, v[k2][j].z, ss);
-        ss = fmaf(v[k2][j].w, v[k2][j].w, ss);
-      }
+    for (int i = tid; i < (K >> 2); i += kMT) {
+      const float4 v = reinterpret_cast<const float4*>(xraw)[i];
+      ss = fmaf(v.x, v.x, ss);
+      ss = fmaf(v.y, v.y, ss);
+      ss = fmaf(v.z, v.z, ss);
+      ss = fmaf(v.w, v.w, ss);
+    }
     ss = warp_sum(ss);
     if (c.lane == 0) c.red()[c.warp] = ss;
     __syncthreads();
@@ -443,26 +450,21 @@ __device__ void stage_input(const Ctx& c, const float* x, int K, int Kp, const f
     for (int w = 0; w < kMW; ++w) tot += c.red()[w];
     rinv = 1.0f / sqrtf(tot / (float)K + eps);
   }
-#pragma unroll
-  for (int k2 = 0; k2 < CPT; ++k2) {
-    const int ch = tid + k2 * kMT;
-    if (ch >= nchunk) continue;
-    if (xraw)
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        if (ch * 16 + 4 * j < K) reinterpret_cast<float4*>(xraw)[ch * 4 + j] = v[k2][j];
+  for (int ch = tid; ch < nchunk; ch += kMT) {
     float h[16];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      h[4 * j] = v[k2][j].x;
-      h[4 * j + 1] = v[k2][j].y;
-      h[4 * j + 2] = v[k2][j].z;
-      h[4 * j + 3] = v[k2][j].w;
+      const float4 v = reinterpret_cast<const float4*>(raw)[ch * 4 + j];
+      h[4 * j] = v.x;
+      h[4 * j + 1] = v.y;
+      h[4 * j + 2] = v.z;
+      h[4 * j + 3] = v.w;
       if (gamma) {
-        h[4 * j] = h[4 * j] * rinv * gm[k2][j].x;
-        h[4 * j + 1] = h[4 * j + 1] * rinv * gm[k2][j].y;
-        h[4 * j + 2] = h[4 * j + 2] * rinv * gm[k2][j].z;
-        h[4 * j + 3] = h[4 * j + 3] * rinv * gm[k2][j].w;
+        const float4 g = reinterpret_cast<const float4*>(xs)[ch * 4 + j];
+        h[4 * j] = h[4 * j] * rinv * g.x;
+        h[4 * j + 1] = h[4 * j + 1] * rinv * g.y;
+        h[4 * j + 2] = h[4 * j + 2] * rinv * g.z;
+        h[4 * j + 3] = h[4 * j + 3] * rinv * g.w;
       }
     }
     float sum = 0.f;
@@ -479,40 +481,174 @@ __device__ void stage_input(const Ctx& c, const float* x, int K, int Kp, const f
   __syncthreads();
 }
 
-// One projection of block l: consume this warp's tasks (row pairs) from the ring, refill
-// behind; both rows of a column block are summed in one pass, so each chunk of the staged
-// input is read once for the pair.  Returns false (for the whole warp) after a timed-out
-// wait (error set, copies drained); the caller makes the outcome CTA-uniform.  BATCH:
-// several column blocks share a ring slot.
-template <bool BATCH, bool MOE>
-__device__ bool gemv_phase_t(const Ctx& c, Stream& s, int l, int ph, const float* xs, const float* xc,
-                             const float* xraw, int pos, int sid) {
+// Both rows of a 16-weight chunk against one 16-float chunk of the staged input: the sums
+// b_j x'_j 2^-149 of q8dot.cuh, each over two independent pairs of packed products (depth 4).
+__device__ __forceinline__ void dot16x2(const uint4 wa, const uint4 wb, const float4 x0, const float4 x1,
+                                        const float4 x2, const float4 x3, float& da, float& db) {
+  const float2 xa0 = make_float2(x0.x, x0.y), xb0 = make_float2(x0.z, x0.w);
+  const float2 xa1 = make_float2(x1.x, x1.y), xb1 = make_float2(x1.z, x1.w);
+  const float2 xa2 = make_float2(x2.x, x2.y), xb2 = make_float2(x2.z, x2.w);
+  const float2 xa3 = make_float2(x3.x, x3.y), xb3 = make_float2(x3.z, x3.w);
+  float2 a0 = __fmul2_rn(make_float2(q8_b0(wa.x), q8_b1(wa.x)), xa0);
+  float2 a1 = __fmul2_rn(make_float2(q8_b2(wa.x), q8_b3(wa.x)), xb0);
+  float2 b0 = __fmul2_rn(make_float2(q8_b0(wb.x), q8_b1(wb.x)), xa0);
+  float2 b1 = __fmul2_rn(make_float2(q8_b2(wb.x), q8_b3(wb.x)), xb0);
+  a0 = __ffma2_rn(make_float2(q8_b0(wa.y), q8_b1(wa.y)), xa1, a0);
+  a1 = __ffma2_rn(make_float2(q8_b2(wa.y), q8_b3(wa.y)), xb1, a1);
+  b0 = __ffma2_rn(make_float2(q8_b0(wb.y), q8_b1(wb.y)), xa1, b0);
+  b1 = __ffma2_rn(make_float2(q8_b2(wb.y), q8_b3(wb.y)), xb1, b1);
+  a0 = __ffma2_rn(make_float2(q8_b0(wa.z), q8_b1(wa.z)), xa2, a0);
+  a1 = __ffma2_rn(make_float2(q8_b2(wa.z), q8_b3(wa.z)), xb2, a1);
+  b0 = __ffma2_rn(make_float2(q8_b0(wb.z), q8_b1(wb.z)), xa2, b0);
+  b1 = __ffma2_rn(make_float2(q8_b2(wb.z), q8_b3(wb.z)), xb2, b1);
+  a0 = __ffma2_rn(make_float2(q8_b0(wa.w), q8_b1(wa.w)), xa3, a0);
+  a1 = __ffma2_rn(make_float2(q8_b2(wa.w), q8_b3(wa.w)), xb3, a1);
+  b0 = __ffma2_rn(make_float2(q8_b0(wb.w), q8_b1(wb.w)), xa3, b0);
+  b1 = __ffma2_rn(make_float2(q8_b2(wb.w), q8_b3(wb.w)), xb3, b1);
+  da = (a0.x + a0.y) + (a1.x + a1.y);
+  db = (b0.x + b0.y) + (b1.x + b1.y);
+}
+
+// The epilogue of pair i (CTA-local) of projection ph of block l, from its row sums.
+template <bool MOE>
+__device__ __forceinline__ void epilogue_pair(const Ctx& c, int l, int ph, int i, float y0, float y1,
+                                              const float* xraw, int pos, int sid) {
   const MegaArgs& a = *c.a;
-  const Ph p = phase_of<MOE>(c, l, ph);
-  constexpr bool moe = MOE;
-  const int T = p.T, P = p.P, t0 = c.gw, dt = c.GW;
-  int left = BATCH && t0 < T ? ((T - 1 - t0) / dt + 1) * P : 0;  // this warp's blocks of the phase
-  int uin = 0, ucap = 1;  // position in, and blocks of, the current slot
-  for (int t = t0; t < T; t += dt) {
-    float acc0 = 0.f, acc1 = 0.f;
-    for (int pc = 0; pc < P; ++pc) {
-      const int off = pc * p.PS, bytes = min(p.PS, p.klen - off);
-      const int slot = s.consumed % kDepth;
-      if (!BATCH || uin == 0) {
-        if (BATCH) ucap = min(p.B, left);
-        const bool landed = mbar_wait(c.bars() + c.warp * kDepth + slot, (unsigned)(s.consumed / kDepth) & 1u, kWaitNs);
-        if (!__all_sync(0xffffffffu, landed)) {  // warp-uniform decision
-          if (c.lane == 0) set_error(c);
-          stream_drain(c, s);
-          return false;
-        }
+  const Split& p = c.split()[ph];
+  const int t = p.p0 + i * p.pstride;  // the pair, projection-wide
+  if (ph == kPhQKV) {  // rows (2t, 2t+1) are dims (j, j + D/2) of one head: RoPE, then q or fp16 K/V
+    const int hd = a.D >> 1, head = t / hd, j = t - head * hd;
+    if (head < a.Hq) {
+      const float2 cs = c.rope_s()[i];
+      float* qo = a.qbuf + (size_t)head * a.D;
+      qo[j] = y0 * cs.x - y1 * cs.y;
+      qo[j + hd] = y1 * cs.x + y0 * cs.y;
+    } else {
+      const bool is_k = head < a.Hq + a.Hkv;
+      const int kvh = head - a.Hq - (is_k ? 0 : a.Hkv);
+      const MegaLayer& L = a.layers[l];
+      const size_t base = (((size_t)sid * a.Hkv + kvh) * a.max_len + pos) * a.D;
+      if (is_k) {
+        const float2 cs = c.rope_s()[i];
+        L.kc[base + j] = __float2half_rn(y0 * cs.x - y1 * cs.y);
+        L.kc[base + j + hd] = __float2half_rn(y1 * cs.x + y0 * cs.y);
+      } else {
+        L.vc[base + j] = __float2half_rn(y0);
+        L.vc[base + j + hd] = __float2half_rn(y1);
       }
-      const int u = BATCH ? uin : 0;
-      const unsigned char* q0 = c.ringq() + (size_t)(c.warp * kDepth + slot) * kSlotQ + 2 * u * p.PS;
-      const unsigned char* q1 = q0 + p.PS;
-      const unsigned char* s0 = c.rings() + (size_t)(c.warp * kDepth + slot) * kSlotS + 2 * u * (p.PS / 16);
-      const unsigned char* s1 = s0 + p.PS / 16;
-      const int nch = bytes >> 4, cb = off >> 4;
+    }
+  } else if (ph == kPhO) {
+    a.x1[2 * t] = __fadd_rn(xraw[2 * t], y0);
+    a.x1[2 * t + 1] = __fadd_rn(xraw[2 * t + 1], y1);
+  } else if (MOE && ph == kPhRouter) {
+    a.logits[2 * t] = y0;
+    a.logits[2 * t + 1] = y1;
+  } else if (ph == kPhGU) {
+    if (MOE) {  // pair t: expert slot t / EF, unit t % EF; scaled by the routing weight
+      const int slot = t / a.EF, j = t - slot * a.EF;
+      a.abuf[(size_t)slot * pad256(a.EF) + j] = silu(y0) * y1 * c.moe_wts()[slot];
+    } else {
+      a.abuf[t] = silu(y0) * y1;
+    }
+  } else {
+    a.hout[2 * t] = __fadd_rn(xraw[2 * t], y0);
+    a.hout[2 * t + 1] = __fadd_rn(xraw[2 * t + 1], y1);
+  }
+}
+
+// This warp's piece of pair i (CTA-local) is summed.  A pair held by one warp goes straight to
+// its epilogue; a pair split between warps is finished by the warp whose piece completes it
+// (a shared-memory counter per pair): it adds the warps' pieces in a fixed order -- a tree over
+// the 16 warp slots, absent warps contributing zero -- so every output has one summation order
+// whichever warp finishes it.
+template <bool MOE>
+__device__ __forceinline__ void finish_piece(const Ctx& c, int l, int ph, int i, int pfirst, float acc0, float acc1,
+                                             const float* xraw, int pos, int sid) {
+  const Split& p = c.split()[ph];
+  acc0 = warp_sum(acc0);
+  acc1 = warp_sum(acc1);
+  const int ua = i * p.upp, ub = ua + p.upp;
+  bool holds = false;
+  if (c.lane < kMW) {
+    const int w0 = c.wu0()[c.lane], w1 = c.wu0()[c.lane + 1];
+    holds = w0 < w1 && w0 < ub && w1 > ua;
+  }
+  const int nw = __popc(__ballot_sync(0xffffffffu, holds));
+  float y0 = acc0, y1 = acc1;
+  if (nw > 1) {
+    int done = 0;
+    if (c.lane == 0) {
+      c.part()[c.warp * kMaxPieces + i - pfirst] = make_float2(acc0, acc1);
+      __threadfence_block();
+      done = atomicAdd(c.cnt() + i, 1);
+    }
+    done = __shfl_sync(0xffffffffu, done, 0);
+    if (done != nw - 1) return;  // another warp's piece completes the pair
+    __threadfence_block();
+    float2 v = make_float2(0.f, 0.f);
+    if (holds) v = c.part()[c.lane * kMaxPieces + i - c.pf()[c.lane]];
+#pragma unroll
+    for (int o = kMW / 2; o > 0; o >>= 1) {
+      v.x += __shfl_xor_sync(0xffffffffu, v.x, o);
+      v.y += __shfl_xor_sync(0xffffffffu, v.y, o);
+    }
+    y0 = v.x;
+    y1 = v.y;
+  }
+  if (c.lane == 0) epilogue_pair<MOE>(c, l, ph, i, y0, y1, xraw, pos, sid);
+}
+
+// The per-projection scratch of phase ph: piece counters, warp ranges and (QKV) the RoPE factors
+// of the CTA's q and k pairs.  A CTA barrier must follow before the projection.
+__device__ void phase_setup(const Ctx& c, int ph, int pos) {
+  const MegaArgs& a = *c.a;
+  const Split& p = c.split()[ph];
+  const int tid = threadIdx.x;
+  for (int i = tid; i < p.np; i += kMT) c.cnt()[i] = 0;
+  if (tid <= kMW) c.wu0()[tid] = tid * p.U / kMW;
+  if (tid < kMW) c.pf()[tid] = tid * p.U / kMW / p.upp;
+  if (ph == kPhQKV) {
+    const int hd = a.D >> 1;
+    for (int i = tid; i < p.np; i += kMT) {
+      const int t = p.p0 + i * p.pstride, head = t / hd;
+      if (head < a.Hq + a.Hkv) c.rope_s()[i] = __ldg(a.rope + (size_t)pos * hd + (t - head * hd));
+    }
+  }
+}
+
+// One projection of block l: consume this warp's range from the ring, refilling behind; each
+// finished pair piece goes to finish_piece.  Returns false (for the whole warp) after a
+// timed-out wait (error set, copies drained); the caller makes the outcome CTA-uniform.
+template <bool MOE>
+__device__ bool gemv_phase(const Ctx& c, Stream& s, int l, int ph, const float* xs, const float* xc,
+                           const float* xraw, int pos, int sid) {
+  const Split& p = c.split()[ph];
+  Cur q = cur_start(p, c.warp);
+  const int pfirst = q.pr;
+  float acc0 = 0.f, acc1 = 0.f;
+  int cur = -1;
+  while (q.left > 0) {
+    const int slot = s.consumed % kDepth;
+    const bool landed = mbar_wait(c.bars() + c.warp * kDepth + slot, (unsigned)(s.consumed / kDepth) & 1u, kWaitNs);
+    if (!__all_sync(0xffffffffu, landed)) {  // warp-uniform decision
+      if (c.lane == 0) set_error(c);
+      stream_drain(c, s);
+      return false;
+    }
+    const unsigned char* sq = c.ringq() + (size_t)(c.warp * kDepth + slot) * kSlotQ;
+    const unsigned char* ss = c.rings() + (size_t)(c.warp * kDepth + slot) * kSlotS;
+    const int len = cur_len(p, q), k = q.k;
+    {
+      if (q.pr != cur) {
+        if (cur >= 0) finish_piece<MOE>(c, l, ph, cur, pfirst, acc0, acc1, xraw, pos, sid);
+        acc0 = acc1 = 0.f;
+        cur = q.pr;
+      }
+      const unsigned char* q0 = sq;
+      const unsigned char* q1 = q0 + kSlotCols;
+      const unsigned char* s0 = ss;
+      const unsigned char* s1 = s0 + kSlotCols / 16;
+      const int nch = len >> 4, cb = k >> 4;
 #pragma unroll 2
       for (int cl = c.lane; cl < nch; cl += 32) {
         const int ch = cb + cl;
@@ -524,68 +660,19 @@ __device__ bool gemv_phase_t(const Ctx& c, Stream& s, int l, int ph, const float
         const uint4 w1 = *reinterpret_cast<const uint4*>(q1 + cl * 16);
         const float f0 = h2f_bits(*reinterpret_cast<const uint16_t*>(s0 + (cl >> 1) * 2));
         const float f1 = h2f_bits(*reinterpret_cast<const uint16_t*>(s1 + (cl >> 1) * 2));
-        acc0 = fmaf(f0, fmaf(dot16_u8(w0, x0, x1, x2, x3), kPScale, corr), acc0);
-        acc1 = fmaf(f1, fmaf(dot16_u8(w1, x0, x1, x2, x3), kPScale, corr), acc1);
+        float d0, d1;
+        dot16x2(w0, w1, x0, x1, x2, x3, d0, d1);
+        acc0 = fmaf(f0, fmaf(d0, kPScale, corr), acc0);
+        acc1 = fmaf(f1, fmaf(d1, kPScale, corr), acc1);
       }
-      if (BATCH) --left;
-      if (!BATCH || ++uin == ucap) {  // the slot is consumed: refill it
-        uin = 0;
-        __syncwarp();
-        ++s.consumed;
-        stream_issue<MOE>(c, s);
-      }
+      cur_advance(p, q, len);
     }
-    acc0 = warp_sum(acc0);
-    acc1 = warp_sum(acc1);
-    if (c.lane != 0) continue;
-    const MegaLayer& L = a.layers[l];
-    if (ph == kPhQKV) {  // rows (2t, 2t+1) are dims (i, i + D/2) of one head: RoPE, then q or fp16 K/V
-      const int hd = a.D >> 1, head = t / hd, i = t - head * hd;
-      const float y0 = acc0, y1 = acc1;
-      if (head < a.Hq) {
-        const float2 cs = a.rope[(size_t)pos * hd + i];
-        float* qo = a.qbuf + (size_t)head * a.D;
-        qo[i] = y0 * cs.x - y1 * cs.y;
-        qo[i + hd] = y1 * cs.x + y0 * cs.y;
-      } else {
-        const bool is_k = head < a.Hq + a.Hkv;
-        const int kvh = head - a.Hq - (is_k ? 0 : a.Hkv);
-        const size_t base = (((size_t)sid * a.Hkv + kvh) * a.max_len + pos) * a.D;
-        if (is_k) {
-          const float2 cs = a.rope[(size_t)pos * hd + i];
-          L.kc[base + i] = __float2half_rn(y0 * cs.x - y1 * cs.y);
-          L.kc[base + i + hd] = __float2half_rn(y1 * cs.x + y0 * cs.y);
-        } else {
-          L.vc[base + i] = __float2half_rn(y0);
-          L.vc[base + i + hd] = __float2half_rn(y1);
-        }
-      }
-    } else if (ph == kPhO) {
-      a.x1[2 * t] = __fadd_rn(xraw[2 * t], acc0);
-      a.x1[2 * t + 1] = __fadd_rn(xraw[2 * t + 1], acc1);
-    } else if (MOE && ph == kPhRouter) {
-      a.logits[2 * t] = acc0;
-      a.logits[2 * t + 1] = acc1;
-    } else if (ph == kPhGU) {
-      if (moe) {  // pair t: expert slot t / EF, unit t % EF; scaled by the routing weight
-        const int slot = t / a.EF, i = t - slot * a.EF;
-        a.abuf[(size_t)slot * pad256(a.EF) + i] = silu(acc0) * acc1 * c.moe_wts()[slot];
-      } else {
-        a.abuf[t] = silu(acc0) * acc1;
-      }
-    } else {
-      a.hout[2 * t] = __fadd_rn(xraw[2 * t], acc0);
-      a.hout[2 * t + 1] = __fadd_rn(xraw[2 * t + 1], acc1);
-    }
+    __syncwarp();  // the slot is consumed: refill it
+    ++s.consumed;
+    stream_issue<MOE>(c, s);
   }
+  if (cur >= 0) finish_piece<MOE>(c, l, ph, cur, pfirst, acc0, acc1, xraw, pos, sid);
   return true;
-}
-
-template <bool MOE>
-__device__ bool gemv_phase(const Ctx& c, Stream& s, int l, int ph, const float* xs, const float* xc,
-                           const float* xraw, int pos, int sid) {
-  return c.shape()[ph].B > 1 ? gemv_phase_t<true, MOE>(c, s, l, ph, xs, xc, xraw, pos, sid)
-                           : gemv_phase_t<false, MOE>(c, s, l, ph, xs, xc, xraw, pos, sid);
 }
 
 // Routing of MoE block l, after the grid barrier that follows the router phase (whose tasks
@@ -898,20 +985,19 @@ __global__ void __launch_bounds__(kMT, 1) mega_decode_kernel(const MegaArgs a) {
   Ctx c;
   c.a = &a;
   c.sm = sm;
-  static_assert(kOffReady + 4 <= kOffShapes, "routing scratch");
-  static_assert(kOffShapes + kPhases * sizeof(Shape) <= kOffWptr, "shapes");
+  static_assert(kOffReady + 4 <= kOffSplit, "routing scratch");
+  static_assert(kOffSplit + kPhases * sizeof(Split) <= kOffWptr, "splits");
   static_assert(kOffWptr % 16 == 0 && kOffWptr + kMW * 2 * sizeof(void*) <= kOffXraw, "stream pointers");
-  Shape* shapes = reinterpret_cast<Shape*>(sm + kOffShapes);
+  Split* splits = reinterpret_cast<Split*>(sm + kOffSplit);
   c.lane = threadIdx.x & 31;
   c.warp = threadIdx.x >> 5;
-  c.gw = c.warp * gridDim.x + blockIdx.x;
-  c.GW = kMW * gridDim.x;
   float* xraw = reinterpret_cast<float*>(sm + kOffXraw);
-  unsigned char* area = sm + off_u;  // union: projection input, or attention tiles
+  unsigned char* area = sm + off_u;  // union: projection input and warp partials, or attention tiles
   const int KpQ = pad256(a.Hq * a.D), KpF = pad256(a.F);
   const int Kx = max(KpH, max(KpQ, KpF));
   float* xs = reinterpret_cast<float*>(area);
   float* xc = xs + Kx;
+  c.ps = reinterpret_cast<unsigned char*>(xc + Kx / 16);
 
   if (threadIdx.x < kMW * kDepth + 1) mbar_init(c.bars() + threadIdx.x, 1);
   if (threadIdx.x == 0) {
@@ -919,7 +1005,7 @@ __global__ void __launch_bounds__(kMT, 1) mega_decode_kernel(const MegaArgs a) {
     c.flag()[1] = 0;
     *c.moe_ready() = -1;
   }
-  if (threadIdx.x < kPhases) shapes[threadIdx.x] = shape_of(a, threadIdx.x);
+  if (threadIdx.x < kPhases) splits[threadIdx.x] = split_of(a, threadIdx.x, blockIdx.x, gridDim.x);
   mbar_fence_init();
   __syncthreads();
   const int pos = __ldcg(a.pos), sid = __ldcg(a.seq);
@@ -927,16 +1013,16 @@ __global__ void __launch_bounds__(kMT, 1) mega_decode_kernel(const MegaArgs a) {
   Stream s;
   s.l = 0;
   s.ph = 0;
-  s.t = c.gw;
-  s.j = 0;
+  s.q = cur_start(splits[0], c.warp);
   s.issued = 0;
   s.consumed = 0;
-  stream_normalise<MOE>(c, s);
-  if (s.l < a.nl) {
-    const Ph p0 = phase_of<MOE>(c, s.l, s.ph);
-    c.wptr()[2 * c.warp] = p0.q;
-    c.wptr()[2 * c.warp + 1] = p0.s;
+  if (c.lane == 0 && a.nl > 0) {
+    const DevQ8& w0 = phase_w<MOE>(a.layers[0], 0);
+    c.wptr()[2 * c.warp] = w0.q;
+    c.wptr()[2 * c.warp + 1] = w0.s;
   }
+  __syncwarp();
+  if (s.q.left == 0) stream_normalise<MOE>(c, s);
   for (int d = 0; d < kDepth; ++d) stream_issue<MOE>(c, s);
 
   unsigned nbar = 0, aphase = 0;
@@ -950,6 +1036,8 @@ __global__ void __launch_bounds__(kMT, 1) mega_decode_kernel(const MegaArgs a) {
       if (ph == kPhRouter && !moe) continue;
       if (ph == kPhGU && moe) {
         stream_refill<MOE>(c, s);  // the routing is known: the selected experts' slices stream in
+        phase_setup(c, ph, pos);
+        __syncthreads();
       } else {
         // the projection's input: QKV and the router (or the dense gate/up) normalise the
         // residual (gamma_1, gamma_2; the raw residual is kept for the residual adds), O and
@@ -966,7 +1054,9 @@ __global__ void __launch_bounds__(kMT, 1) mega_decode_kernel(const MegaArgs a) {
           const float* g = ph == kPhO ? L.ffn_norm : (l + 1 < a.nl ? a.layers[l + 1].attn_norm : nullptr);
           for (int i = blockIdx.x * 32; g && i < a.H; i += gridDim.x * 32) prefetch_l2_last(g + i);
         }
-        stage_input(c, in, K, Kp, gamma, a.eps, xs, xc, (ph == kPhO || ph == kPhDown) ? nullptr : xraw);
+        stage_issue(in, K, Kp, gamma, xs, xraw);
+        phase_setup(c, ph, pos);
+        stage_finish(c, K, Kp, gamma, a.eps, xs, xc, xraw);
       }
       ok = __syncthreads_and(gemv_phase<MOE>(c, s, l, ph, xs, xc, xraw, pos, sid));
       if (ph == kPhQKV) {
@@ -1010,7 +1100,7 @@ size_t mega_smem(int H, int q_dim, int F, int D, int G) {
                     : G == 4 ? AttnLayout<64, 4>::total : AttnLayout<64, 8>::total;
   else attn = G == 1 ? AttnLayout<128, 1>::total : G == 2 ? AttnLayout<128, 2>::total
             : G == 4 ? AttnLayout<128, 4>::total : AttnLayout<128, 8>::total;
-  const size_t u = std::max((size_t)Kx * 4 + (size_t)(Kx / 16) * 4, attn);
+  const size_t u = std::max((size_t)Kx * 4 + (size_t)(Kx / 16) * 4 + kPsBytes, attn);
   return off_u + u + 128;  // + alignment of the dynamic base
 }
 

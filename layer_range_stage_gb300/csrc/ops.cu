@@ -100,6 +100,25 @@ int stage_op_q8_pack(const stage_q8* host, void* q_dev, void* s_dev) {
   return e == cudaSuccess ? STAGE_OK : op_cuda(e, "pack");
 }
 
+int stage_op_embed(const void* q_dev, const void* s_dev, int64_t rows, int64_t cols, const int32_t* tok_dev,
+                   int n_tok, float* out_dev, void* stream) {
+  if (!q_dev || !s_dev || !tok_dev || !out_dev) return op_err(STAGE_E_INVALID, "null pointer");
+  if (rows <= 0 || cols <= 0 || rows > (1 << 30) || cols > (1 << 24) || n_tok <= 0 || n_tok > 65535)
+    return op_err(STAGE_E_INVALID, "bad shape");
+  if (cols % 4) return op_err(STAGE_E_INVALID, "cols must be a multiple of 4");
+  if (!aligned16(q_dev) || !aligned16(s_dev) || !aligned16(out_dev)) return op_err(STAGE_E_INVALID, "unaligned pointer");
+  cudaError_t e = lrs::prepare_kernels();
+  if (e != cudaSuccess) return op_cuda(e, "kernel setup");
+  lrs::DevQ8 w;
+  w.q = (uint8_t*)q_dev;
+  w.s = (uint16_t*)s_dev;
+  w.N = (int)rows;
+  w.K = (int)cols;
+  w.Kp = lrs::row_pad((int)cols);
+  e = lrs::launch_embed(w, tok_dev, n_tok, out_dev, (int)cols, (cudaStream_t)stream);
+  return e == cudaSuccess ? STAGE_OK : op_cuda(e, "embed");
+}
+
 int stage_op_gemv(const void* q_dev, const void* s_dev, int64_t rows, int64_t cols, const float* x_dev, int n_tok,
                   const float* gamma_dev, float eps, float* y_dev, void* stream) {
   if (!q_dev || !s_dev || !x_dev || !y_dev) return op_err(STAGE_E_INVALID, "null pointer");

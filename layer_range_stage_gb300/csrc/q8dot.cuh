@@ -18,6 +18,12 @@ namespace lrs {
 constexpr float kXScale = 18446744073709551616.0f;        // 2^64
 constexpr float kPScale = 38685626227668133590597632.0f;  // 2^85
 
+// Byte j of a word as the denormal b_j * 2^-149 (one instruction each).
+__device__ __forceinline__ float q8_b0(unsigned w) { return __uint_as_float(w & 0xFFu); }
+__device__ __forceinline__ float q8_b1(unsigned w) { return __uint_as_float(__byte_perm(w, 0u, 0x4441)); }
+__device__ __forceinline__ float q8_b2(unsigned w) { return __uint_as_float(__byte_perm(w, 0u, 0x4442)); }
+__device__ __forceinline__ float q8_b3(unsigned w) { return __uint_as_float(w >> 24); }
+
 // sum_j b_j * x'_j * 2^-149 over the 16 biased weight bytes of w (see above).
 __device__ __forceinline__ float dot16_u8(const uint4 w, const float4 x0, const float4 x1, const float4 x2,
                                           const float4 x3) {

@@ -216,6 +216,7 @@ struct stage {
   int last_n = 0;
   std::atomic<int> busy{0};
   int fail_next = 0;
+  int stall_barrier = 0;  // tests: the next persistent launch's grid barriers wait for one CTA too many
   std::string err;
 };
 
@@ -598,6 +599,13 @@ int forward_dev(stage* st, int n, const int* d_seq, const int* d_pos, const int*
     m.scale = (float)(1.0 / std::sqrt((double)D));
     m.bar = st->mega_bar;
     m.err = st->err_word;
+    if (st->stall_barrier) {  // never baked into a captured graph
+      cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+      if (cudaStreamIsCapturing(s, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusNone) {
+        m.bar_extra = 1;
+        st->stall_barrier = 0;
+      }
+    }
     if (st->timing) timing_mark(st->tev[0], s);
     if ((e = lrs::launch_mega_decode(m, s)) != cudaSuccess) return cuda_err(st, e, "persistent decode");
     if (st->timing) timing_mark(st->tev[1], s);
@@ -1233,6 +1241,10 @@ int stage_debug_inject(stage_t st, int what, int value) {
   }
   if (what == 2) {
     st->fail_next = value ? value : STAGE_E_INJECTED;
+    return STAGE_OK;
+  }
+  if (what == 3) {
+    st->stall_barrier = value ? 1 : 0;
     return STAGE_OK;
   }
   return STAGE_E_INVALID;
