@@ -130,7 +130,7 @@ struct MegaArgs {
   int nl = 0;
   const float* hin = nullptr;  // [H] block input of the first block (may equal hout)
   float* hout = nullptr;       // [H] residual stream after the last block
-  float* x1 = nullptr;         // [H] scratch: residual after attention
+  unsigned long long* tags = nullptr;  // the tagged vectors between steps (mega_tag_entries entries)
   float* qbuf = nullptr;       // [Hq * D] rotated q
   float* obuf = nullptr;       // [Hq * D] attention output
   float* abuf = nullptr;       // [F] SwiGLU output
@@ -143,14 +143,17 @@ struct MegaArgs {
   int n_experts = 0, top_k = 0, EF = 0;  // MoE stages: experts, selected per token, expert FFN width
   float* logits = nullptr;                // MoE stages: [n_experts] router logits of the current block
   float eps = 1e-5f, scale = 1.f;
-  unsigned* bar = nullptr;  // [64]: grid barrier counter, exit counter, per-KV-head attention
-                            // counters; zero between launches (the last CTA out re-zeroes)
+  unsigned* bar = nullptr;  // [64]: [0] CTAs done with the SwiGLU step, [1] exit counter, [2 + h]
+                            // attention counter of KV head h (zero between launches: the last CTA
+                            // out re-zeroes), [63] launch sequence
   int* err = nullptr;
-  unsigned bar_extra = 0;  // tests: arrivals every grid barrier waits for beyond the grid (0 in use)
+  unsigned bar_extra = 0;  // tests: added to the tag the attention waits for (0 in use)
 };
 // Whether the persistent decode covers this shape (and the shared memory it needs fits).  MoE:
 // n_experts > 0, F = top_k * expert FFN width (the gathered down input).
 bool mega_supported(int H, int q_dim, int F, int head_dim, int group, int n_experts = 0, int top_k = 0);
+// Entries of MegaArgs::tags for a stage of these shapes.
+size_t mega_tag_entries(int H, int q_dim, int kv_dim, int n_experts);
 // Attention chunks per KV head used by the persistent decode (about one item per SM).
 int mega_chunks(int n_kv_heads);
 cudaError_t launch_mega_decode(const MegaArgs& a, cudaStream_t st);

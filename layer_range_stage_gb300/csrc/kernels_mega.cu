@@ -21,16 +21,18 @@ bool mega_supported(int H, int q_dim, int F, int head_dim, int group, int n_expe
   if ((H & 3) || (q_dim & 3) || (F & 3)) return false;
   const int Kx = std::max(pad256(H), std::max(pad256(q_dim), pad256(F)));
   if (Kx > kMaxKp) return false;
-  // the pieces of a warp's range in its largest projection (rows: gate/up 2F or the expert rows)
+  // pairs of the fullest CTA in each projection (rows: QKV, O, router, gate/up or the selected
+  // experts' rows, down)
   const int G = sm_count();
   const int rows[] = {q_dim + 2 * (q_dim / group), H, n_experts, 2 * F, H};
-  const int kp[] = {pad256(H), pad256(q_dim), pad256(H), pad256(H), pad256(F)};
-  for (int i = 0; i < 5; ++i) {
-    const long long np = (rows[i] / 2 + G - 1) / G;  // pairs of the fullest CTA
-    const long long cols = (np * kp[i] / kUnit + kMW - 1) / kMW * kUnit;
-    if (np > kMaxCtaPairs || cols / kp[i] + 2 > kMaxPieces) return false;
-  }
+  for (int r : rows)
+    if ((r / 2 + G - 1) / G > kMaxCtaPairs) return false;
+  if (n_experts > 0 && F / top_k > kSlotCols) return false;  // an expert's down piece fits a slot
   return mega_smem(H, q_dim, F, head_dim, group) <= kMaxSmem;
+}
+
+size_t mega_tag_entries(int H, int q_dim, int kv_dim, int n_experts) {
+  return (size_t)2 * q_dim + 2 * (size_t)kv_dim + 2 * (size_t)H + ((n_experts + 1) & ~1);
 }
 
 int mega_chunks(int n_kv_heads) { return std::max(1, std::min(kAttnMaxChunks, sm_count() / std::max(1, n_kv_heads))); }
@@ -52,7 +54,7 @@ cudaError_t prepare_mega() {
 cudaError_t launch_mega_decode(const MegaArgs& a, cudaStream_t st) {
   const int G = a.Hq / a.Hkv;
   if (!mega_supported(a.H, a.Hq * a.D, a.F, a.D, G, a.n_experts, a.top_k)) return cudaErrorInvalidValue;
-  if (a.n_chunks < 1 || a.n_chunks > kAttnMaxChunks) return cudaErrorInvalidValue;
+  if (a.n_chunks < 1 || a.n_chunks > kAttnMaxChunks || a.nl > 255 || !a.tags) return cudaErrorInvalidValue;
   const size_t smem = mega_smem(a.H, a.Hq * a.D, a.F, a.D, G);
   return a.n_experts > 0 ? launch_mega_moe(a, smem, st) : launch_mega_all<false>(a, smem, st);
 }

@@ -73,10 +73,11 @@ constexpr size_t kOffLogits = kOffMoe, kOffIds = kOffLogits + kMaxExperts * 4, k
                  kOffSel = kOffWts + kMaxTopK * 4, kOffSelId = kOffSel + kMaxTopK * 4,
                  kOffReady = kOffSelId + kMaxTopK * 4;
 constexpr size_t kOffSplit = kOffMoe + (kMaxExperts + 4 * kMaxTopK + 4) * 4;  // [kPhases] Split
-constexpr size_t kOffWptr = kOffSplit + 224;                               // [kMW][2] stream pointers
+constexpr size_t kOffWptr = kOffSplit + 256;                               // [kMW][2] stream pointers
 // the phases of a block's weight stream
 constexpr int kPhQKV = 0, kPhO = 1, kPhRouter = 2, kPhGU = 3, kPhDown = 4, kPhases = 5;
-constexpr size_t kOffXraw = kOffMoe + 2048;                               // [Kp(H)] floats
+constexpr int kSeqWord = 63;  // word of the counter block holding the launch sequence
+constexpr size_t kOffXraw = kOffMoe + 2176;                               // [Kp(H)] floats
 
 __host__ __device__ constexpr int pad256(int k) { return (k + 255) / 256 * 256; }
 
@@ -100,6 +101,7 @@ struct AttnLayout {
   static_assert(wts + (size_t)64 * G * 4 <= st, "merge scratch");
   static_assert((size_t)(G * D + 64) * 4 <= (size_t)2 * T * D * 2, "merge slice scratch over the K/V tiles");
   static_assert((size_t)PG * G * D * 4 <= (size_t)2 * T * D * 2, "PV partial sums over the K/V tiles");
+  static_assert(G * D <= 2 * kMT && (2 * T * D * 2) / (G * D * 4) >= 1, "merge: two outputs per thread, a chunk batch");
 };
 
 // Where dim d of a head's q sits in shared memory: per 8-dim chunk j the low four dims at
@@ -119,14 +121,35 @@ __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
   return v;
 }
 
+// Tagged values: the vectors handed from one step of a block to the next are written as 64-bit
+// words (tag << 32 | f32 bits), tag = launch sequence * 256 + block + 1, with single 64-bit
+// stores, so a reader that sees the tag it expects has the value too.  A reader polls exactly
+// the entries it needs -- no grid barrier, one round trip to L2 once the last of them is in.
+typedef unsigned long long tagged_t;
+
+__device__ __forceinline__ void st_tag(tagged_t* p, float v, unsigned tag) {
+  const tagged_t w = ((tagged_t)tag << 32) | __float_as_uint(v);
+  asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(w) : "memory");
+}
+__device__ __forceinline__ ulonglong2 ld_tag2(const tagged_t* p) {  // two entries, 16-byte aligned
+  ulonglong2 r;
+  asm volatile("ld.relaxed.gpu.global.v2.b64 {%0, %1}, [%2];" : "=l"(r.x), "=l"(r.y) : "l"(p) : "memory");
+  return r;
+}
+__device__ __forceinline__ unsigned tag_of(tagged_t w) { return (unsigned)(w >> 32); }
+__device__ __forceinline__ float val_of(tagged_t w) { return __uint_as_float((unsigned)w); }
+
 // How a projection is dealt over the grid.  Rows go in pairs (2P, 2P + 1): the pairs the RoPE
 // and SwiGLU epilogues need, and for the other projections two rows that share each load of
 // the staged input.  CTA c owns pairs [p0, p0 + np) with p0 = c * NP / G, so every CTA holds
-// the same number of pairs to within one.  Inside a CTA the pairs' K ranges are laid end to end
-// (np * Kp columns) and cut into 16 contiguous warp ranges of whole 256-column units, so a
-// warp may hold the tail of one pair, some whole pairs and the head of another; each warp sums
-// its pieces, and after the phase the CTA adds, per pair, the pieces of the warps that hold
-// it in warp order -- one fixed summation order per output.
+// the same number of pairs to within one.  A pair's K range is cut into slots of at most
+// kSlotCols columns (one ring slot each: a column block of both rows).  The CTA's slots, in
+// memory order, form groups of gs consecutive slots -- a whole pair (gs = slots per pair), or
+// one slot when whole pairs would leave the CTA's warps unevenly loaded -- and group g goes to
+// warp g mod 16.  At any moment the CTA's warps read one dense window of the matrix (DRAM rows
+// are opened once for many requests), and every warp holds the same number of slots to within
+// one group.  A pair split between warps is finished by the warp that completes it: the slots'
+// partial sums are added in slot order.
 struct Split {
   int NP;    // pairs of the projection
   int Kp;    // columns of a pair's K range (mode 2: top_k expert pieces of PS columns)
@@ -134,27 +157,26 @@ struct Split {
   int mode;  // 0 plain rows; 1 rows of the selected experts (rps rows each); 2 piece j of a row
              // from selected expert j (K gathered over the experts)
   int rps;
-  int p0, np;  // this CTA's pairs: p0 + i * pstride for i < np
-  int pstride;
-  int upp;     // units (256 columns) of a pair: Kp / 256
-  int U;       // this CTA's units: np * upp
+  int p0, np;  // this CTA's pairs
+  int sp;      // slots of a pair
+  int gs;      // slots of a group: sp, or 1
+  int ng;      // this CTA's groups: np * sp / gs
+  int dq, dr;  // gs == 1: kMW slots further on is dq pairs and dr slots further on
 };
 
-constexpr int kUnit = 256;             // columns of a unit (warp ranges and segments are whole units)
 constexpr int kSlotCols = kSlotQ / 2;  // columns of each row in a ring slot
-constexpr int kMaxPieces = 16;         // pairs a warp's range may touch in one projection
-constexpr int kMaxCtaPairs = 256;      // pairs a CTA may hold in one projection
-// per-projection scratch after the staged input: warp partials, piece counters, the warp
-// ranges, the RoPE factors of the CTA's QKV pairs
-constexpr size_t kPsPart = 0, kPsCnt = kPsPart + (size_t)kMW * kMaxPieces * 8, kPsWu0 = kPsCnt + kMaxCtaPairs * 4,
-                 kPsPf = kPsWu0 + 128, kPsRope = kPsPf + 128, kPsBytes = kPsRope + (size_t)kMaxCtaPairs * 8;
+constexpr int kMaxCtaPairs = 256;      // pairs (and split-pair slots) a CTA may hold in one projection
+// per-projection scratch after the staged input: slot partials, slot counters of split pairs,
+// the RoPE factors of the CTA's QKV pairs
+constexpr size_t kPsPart = 0, kPsCnt = kPsPart + (size_t)kMaxCtaPairs * 8, kPsRope = kPsCnt + kMaxCtaPairs * 4,
+                 kPsBytes = kPsRope + (size_t)kMaxCtaPairs * 8;
 
-// A position in a warp's range of one projection: CTA-local pair pr, column k of the pair, ks =
-// column within its source segment, and the columns of the range still to go.  The issuer and
-// the consumer of a warp's ring walk the same sequence of cursors, so a slot's contents never
-// have to be written down.
+// A warp's position in one projection: its group count m (groups w + 16 m are its own), the
+// current slot (CTA-local pair pr, slot j of the pair) and r, the slot's place in its group.
+// The issuer and the consumer of a warp's ring walk the same sequence of cursors, so a slot's
+// contents never have to be written down.
 struct Cur {
-  int pr, k, ks, left;
+  int m, pr, j, r;
 };
 
 // The weight stream of one warp: block l, projection ph, the cursor of the next slot, and the
@@ -172,11 +194,19 @@ struct Ctx {
   unsigned char* sm;
   unsigned char* ps;  // per-projection scratch after the staged input (see kPs*)
   int lane, warp;
-  // [kMW][kMaxPieces] partial sums (rows 2P, 2P + 1) of pairs split between warps
+  unsigned seq;  // this launch's sequence number (tags: seq * 256 + block + 1)
+  __device__ unsigned tag(int l) const { return seq * 256u + (unsigned)l + 1u; }
+  // the tagged vectors (layout of mega_tag_entries): q [Hq * D], the current K and V rows
+  // [2][Hkv * D], attention output [Hq * D], x1 [H], block output [H], router logits [n_experts]
+  __device__ tagged_t* tq() const { return a->tags; }
+  __device__ tagged_t* tkv() const { return a->tags + (size_t)a->Hq * a->D; }
+  __device__ tagged_t* to() const { return tkv() + (size_t)2 * a->Hkv * a->D; }
+  __device__ tagged_t* tx1() const { return to() + (size_t)a->Hq * a->D; }
+  __device__ tagged_t* th() const { return tx1() + a->H; }
+  __device__ tagged_t* tlog() const { return th() + a->H; }
+  // [np * sp] partial sums (rows 2P, 2P + 1) of the slots of pairs split between warps
   __device__ float2* part() const { return reinterpret_cast<float2*>(ps + kPsPart); }
   __device__ int* cnt() const { return reinterpret_cast<int*>(ps + kPsCnt); }     // [kMaxCtaPairs] pieces done
-  __device__ int* wu0() const { return reinterpret_cast<int*>(ps + kPsWu0); }     // [kMW + 1] first unit of each warp
-  __device__ int* pf() const { return reinterpret_cast<int*>(ps + kPsPf); }       // [kMW] first pair of each warp
   __device__ float2* rope_s() const { return reinterpret_cast<float2*>(ps + kPsRope); }  // [kMaxCtaPairs] (QKV)
   __device__ unsigned char* ringq() const { return sm + kOffRingQ; }
   __device__ unsigned char* rings() const { return sm + kOffRingS; }
@@ -218,7 +248,7 @@ __device__ Split split_of(const MegaArgs& a, int ph, int cta, int G) {
   p.rps = 0;
   if (ph == kPhRouter && !moe) {  // dense stages: no router rows
     p.NP = 0;
-    p.Kp = p.seg = kUnit;
+    p.Kp = p.seg = kSlotCols;
   } else {
     const DevQ8& w = moe ? phase_w<true>(L, ph) : phase_w<false>(L, ph);
     int N = w.N;
@@ -235,52 +265,64 @@ __device__ Split split_of(const MegaArgs& a, int ph, int cta, int G) {
     p.NP = N / 2;
   }
   p.p0 = (int)((long long)cta * p.NP / G);
-  p.pstride = 1;
   p.np = (int)((long long)(cta + 1) * p.NP / G) - p.p0;
-  p.upp = p.Kp / kUnit;
-  p.U = p.np * p.upp;
+  p.sp = p.mode == 2 ? p.Kp / p.seg : (p.Kp + kSlotCols - 1) / kSlotCols;
+  // whole pairs per warp unless single slots spread the CTA's slots more evenly
+  const int by_pair = (p.np + kMW - 1) / kMW * p.sp, by_slot = (p.np * p.sp + kMW - 1) / kMW;
+  p.gs = (by_slot < by_pair && p.np * p.sp <= kMaxCtaPairs) ? 1 : p.sp;
+  p.ng = p.np * p.sp / p.gs;
+  p.dq = kMW / p.sp;
+  p.dr = kMW % p.sp;
   return p;
 }
 
-// Units [u0, u1) of warp w in a projection.
-__device__ __forceinline__ int warp_u0(const Split& p, int w) { return w * p.U / kMW; }
-
-// The cursor at the start of warp w's range in projection p.
+// The cursor of warp w's first slot in projection p (valid while w + 16 m < ng).
 __device__ __forceinline__ Cur cur_start(const Split& p, int w) {
-  const int u0 = warp_u0(p, w), u1 = warp_u0(p, w + 1);
   Cur q;
-  q.pr = u0 / p.upp;
-  q.k = (u0 - q.pr * p.upp) * kUnit;
-  q.ks = q.k % p.seg;
-  q.left = (u1 - u0) * kUnit;
+  q.m = 0;
+  q.r = 0;
+  const int g = w * p.gs;
+  q.pr = g / p.sp;
+  q.j = g - q.pr * p.sp;
   return q;
 }
 
-// Columns of the slot at q: to the end of the range, of the pair or of the source segment, at
-// most kSlotCols.
-__device__ __forceinline__ int cur_len(const Split& p, const Cur& q) {
-  return min(min(q.left, kSlotCols), min(p.Kp - q.k, p.seg - q.ks));
+__device__ __forceinline__ bool cur_valid(const Split& p, const Cur& q, int w) { return w + kMW * q.m < p.ng; }
+
+// First column and columns of slot j of a pair.
+__device__ __forceinline__ int slot_k(const Split& p, int j) { return j * (p.mode == 2 ? p.seg : kSlotCols); }
+__device__ __forceinline__ int slot_len(const Split& p, int j) {
+  return p.mode == 2 ? p.seg : min(kSlotCols, p.Kp - j * kSlotCols);
 }
 
-__device__ __forceinline__ void cur_advance(const Split& p, Cur& q, int len) {
-  q.left -= len;
-  q.k += len;
-  q.ks += len;
-  if (q.ks == p.seg) q.ks = 0;
-  if (q.k == p.Kp) {
-    q.k = 0;
-    q.ks = 0;
-    ++q.pr;
+__device__ __forceinline__ void cur_advance(const Split& p, Cur& q) {
+  if (++q.r < p.gs) {  // the next slot of a whole-pair group
+    ++q.j;
+    return;
+  }
+  q.r = 0;
+  ++q.m;
+  if (p.gs == p.sp) {  // the warp's next pair
+    q.pr += kMW;
+    q.j = 0;
+  } else {  // single slots: kMW slots further on
+    q.pr += p.dq;
+    q.j += p.dr;
+    if (q.j >= p.sp) {
+      q.j -= p.sp;
+      ++q.pr;
+    }
   }
 }
 
 // Global addresses of rows (2P, 2P + 1) of a projection at column k (P phase-global).
 template <bool MOE>
 __device__ __forceinline__ void pair_src(const Ctx& c, const Split& p, const uint8_t* wq, const uint16_t* ws, int P,
-                                         int k, int kk, const uint8_t*& q, const uint16_t*& sc, size_t& qstride,
+                                         int j, const uint8_t*& q, const uint16_t*& sc, size_t& qstride,
                                          size_t& sstride) {
-  if (MOE && p.mode == 2) {  // K gathered: columns [j PS, (j + 1) PS) from selected expert j; kk = k % PS
-    const int j = (k - kk) / p.seg;
+  const int k = slot_k(p, j);
+  if (MOE && p.mode == 2) {  // K gathered: slot j is the row's piece from selected expert j
+    const int kk = 0;
     const size_t r = (size_t)c.moe_ids()[j] * (size_t)(2 * p.NP) + 2 * P;
     q = wq + r * p.seg + kk;
     sc = ws + r * (p.seg / 32) + kk / 32;
@@ -296,11 +338,11 @@ __device__ __forceinline__ void pair_src(const Ctx& c, const Split& p, const uin
   sstride = p.Kp / 32;
 }
 
-// Move a cursor to the first non-empty warp range at or after (l, ph).
+// Move a cursor to the first projection at or after (l, ph) in which this warp holds slots.
 template <bool MOE>
 __device__ __forceinline__ void stream_normalise(const Ctx& c, Stream& s) {
   bool moved = false;
-  while (s.l < c.a->nl && s.q.left == 0) {
+  while (s.l < c.a->nl && !cur_valid(c.split()[s.ph], s.q, c.warp)) {
     if (++s.ph == kPhases) {
       s.ph = 0;
       ++s.l;
@@ -316,23 +358,22 @@ __device__ __forceinline__ void stream_normalise(const Ctx& c, Stream& s) {
   __syncwarp();
 }
 
-// Issue the next slot of this warp's stream (if any) into the ring: cur_len columns of one pair
-// from the cursor, row 2P's bytes at the start of the slot and row 2P + 1's at kSlotCols.
-// Slices of the selected experts wait until the routing of their block is known.
+// Issue the next slot of this warp's stream (if any) into the ring: slot j of pair pr, row 2P's
+// bytes at the start of the ring slot and row 2P + 1's at kSlotCols.  Slices of the selected
+// experts wait until the routing of their block is known.
 template <bool MOE>
 __device__ __forceinline__ void stream_issue(const Ctx& c, Stream& s) {
   if (s.l >= c.a->nl) return;
   if (MOE && s.ph >= kPhGU && s.l > *c.moe_ready()) return;
   const Split& p = c.split()[s.ph];
   const int slot = s.issued % kDepth;
-  const int len = cur_len(p, s.q);
   if (c.lane == 0) {
+    const int len = slot_len(p, s.q.j);
     const uint8_t* q;
     const uint16_t* sc;
     size_t qst, sst;
     pair_src<MOE>(c, p, static_cast<const uint8_t*>(c.wptr()[2 * c.warp]),
-                  static_cast<const uint16_t*>(c.wptr()[2 * c.warp + 1]), p.p0 + s.q.pr * p.pstride, s.q.k, s.q.ks,
-                  q, sc, qst, sst);
+                  static_cast<const uint16_t*>(c.wptr()[2 * c.warp + 1]), p.p0 + s.q.pr, s.q.j, q, sc, qst, sst);
     uint64_t* bar = c.bars() + c.warp * kDepth + slot;
     unsigned char* dq = c.ringq() + (size_t)(c.warp * kDepth + slot) * kSlotQ;
     unsigned char* ds = c.rings() + (size_t)(c.warp * kDepth + slot) * kSlotS;
@@ -344,8 +385,8 @@ __device__ __forceinline__ void stream_issue(const Ctx& c, Stream& s) {
     bulk_g2s(ds + kSlotCols / 16, sc + sst, (uint32_t)(len / 16), bar);
   }
   ++s.issued;
-  cur_advance(p, s.q, len);
-  if (s.q.left == 0) stream_normalise<MOE>(c, s);
+  cur_advance(p, s.q);
+  if (!cur_valid(p, s.q, c.warp)) stream_normalise<MOE>(c, s);
 }
 
 // Top the ring up to kDepth slots (after the routing of a block became known).
@@ -370,27 +411,9 @@ __device__ __forceinline__ void set_error(const Ctx& c) {
   c.flag()[0] = 1;
 }
 
-// Grid barrier number `k` (1-based) of this launch; false when the wait ran out.
-__device__ bool grid_barrier(const Ctx& c, unsigned k) {
-  __syncthreads();
-  if (threadIdx.x == 0 && !c.flag()[0]) {
-    const unsigned target = k * gridDim.x + c.a->bar_extra;
-    red_release_add(c.a->bar, 1u);
-    if (ld_acquire_u32(c.a->bar) < target) {
-      const uint64_t t0 = global_ns();
-      while (ld_acquire_u32(c.a->bar) < target)
-        if (global_ns() - t0 > kWaitNs) {
-          set_error(c);
-          break;
-        }
-    }
-  }
-  __syncthreads();
-  return !c.flag()[0];
-}
-
-// Leaving: the last CTA out resets the barrier counters for the next launch (every CTA has
-// stopped polling by the time it counts itself out).
+// Leaving: the last CTA out resets the SwiGLU and attention counters and advances the launch
+// sequence
+// (every CTA has stopped polling by the time it counts itself out).
 __device__ void grid_leave(const Ctx& c) {
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -399,6 +422,7 @@ __device__ void grid_leave(const Ctx& c) {
     if (prev == gridDim.x - 1) {
       atomicExch(c.a->bar, 0u);
       for (int h = 0; h < c.a->Hkv; ++h) atomicExch(c.a->bar + 2 + h, 0u);
+      atomicExch(c.a->bar + kSeqWord, c.seq + 1u);
       atomicExch(c.a->bar + 1, 0u);
     }
   }
@@ -424,8 +448,119 @@ __device__ void stage_issue(const float* x, int K, int Kp, const float* gamma, f
   }
 }
 
+// One pair of entries (16-byte aligned) of a tagged vector, waited for (bounded).
+__device__ __forceinline__ bool poll_pair(const Ctx& c, const tagged_t* p, unsigned tag, float2& v) {
+  ulonglong2 w = ld_tag2(p);
+  uint64_t t0 = 0;
+  while (tag_of(w.x) != tag || tag_of(w.y) != tag) {
+    const uint64_t now = global_ns();
+    if (!t0) {
+      t0 = now;
+    } else if (now - t0 > kWaitNs) {
+      set_error(c);
+      return false;
+    }
+    __nanosleep(64);
+    w = ld_tag2(p);
+  }
+  v = make_float2(val_of(w.x), val_of(w.y));
+  return true;
+}
+
+// Wait (bounded) until entries [0, n) of a tagged vector carry `tag` and put their values in
+// dst; entries whose index within a piece of `piece` entries is `valid` or more are never
+// written and read as zero.  n, piece and valid are even.  All entries are fetched at once with
+// asynchronous copies into `scratch` (shared memory, n tagged entries); the pairs not yet
+// carrying the tag are fetched again, all at once, round after round (one L2 round trip per
+// round).  n <= 128 kMT.  Returns false after a timed-out wait
+// (error set); the caller makes the outcome CTA-uniform.
+__device__ bool gather_tagged(const Ctx& c, const tagged_t* src, int n, int piece, int valid, unsigned tag,
+                              tagged_t* scratch, float* dst) {
+  const int npair = n >> 1;
+  // the pairs of this thread (i = threadIdx.x + kMT k) still to come, one bit per k (n <= 64 kMT)
+  unsigned long long pending = 0;
+  for (int k = 0, i = threadIdx.x; i < npair; ++k, i += kMT) {
+    if ((2 * i) % piece < valid) {
+      cp_async16(scratch + 2 * i, src + 2 * i);
+      pending |= 1ull << k;
+    } else {
+      dst[2 * i] = 0.f;
+      dst[2 * i + 1] = 0.f;
+    }
+  }
+  uint64_t t0 = 0;
+  while (true) {
+    cp_async_wait_all();
+    unsigned long long left = 0;
+    for (unsigned long long m = pending; m; m &= m - 1) {  // the pairs fetched in this round
+      const int k = __ffsll((long long)m) - 1, i = threadIdx.x + kMT * k;
+      const tagged_t w0 = scratch[2 * i], w1 = scratch[2 * i + 1];
+      if (tag_of(w0) == tag && tag_of(w1) == tag) {
+        dst[2 * i] = val_of(w0);
+        dst[2 * i + 1] = val_of(w1);
+      } else {
+        left |= 1ull << k;
+      }
+    }
+    if (!left) return true;
+    const uint64_t now = global_ns();
+    if (!t0) {
+      t0 = now;
+    } else if (now - t0 > kWaitNs) {
+      set_error(c);
+      return false;
+    }
+    pending = left;  // one more round: every missing pair fetched again at once
+    for (unsigned long long m = pending; m; m &= m - 1) {
+      const int i = threadIdx.x + kMT * (__ffsll((long long)m) - 1);
+      cp_async16(scratch + 2 * i, src + 2 * i);
+    }
+  }
+}
+
+// The staging of a projection whose input is a tagged vector of this launch: gamma (when given)
+// is issued first, then the input is gathered as its entries arrive (into xraw with gamma, else
+// into xs), zero beyond K up to Kp.  `scratch`: 2K floats of shared memory that hold nothing
+// else during the gather.  Returns false (CTA-uniform) after a timed-out wait.
+__device__ bool stage_gather(const Ctx& c, const tagged_t* x, int K, int Kp, int piece, int valid, unsigned tag,
+                             const float* gamma, float* xs, float* xraw, tagged_t* scratch) {
+  const int tid = threadIdx.x;
+  float* raw = gamma ? xraw : xs;
+  if (gamma)
+    for (int i = tid; i < (Kp >> 2); i += kMT) {
+      if (4 * i < K) cp_async16(xs + 4 * i, gamma + 4 * i);
+      else reinterpret_cast<float4*>(xs)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  const bool ok = gather_tagged(c, x, K, piece, valid, tag, scratch, raw);
+  for (int i = K + tid; i < Kp; i += kMT) raw[i] = 0.f;
+  return __syncthreads_and(ok);
+}
+
+// The staging of a projection whose input is written by every CTA before it counts itself done
+// on `counter` (the SwiGLU output, too wide to carry tags in shared memory): wait (thread 0,
+// bounded) for `target` arrivals, then copy the input in as stage_issue does.  Returns false
+// (CTA-uniform) after a timed-out wait.
+__device__ bool stage_counted(const Ctx& c, const unsigned* counter, unsigned target, const float* x, int K, int Kp,
+                              float* xs, float* xraw) {
+  if (threadIdx.x == 0 && ld_acquire_u32(counter) < target) {
+    const uint64_t t0 = global_ns();
+    while (ld_acquire_u32(counter) < target) {
+      if (global_ns() - t0 > kWaitNs) {
+        set_error(c);
+        break;
+      }
+      __nanosleep(64);
+    }
+  }
+  __syncthreads();
+  if (c.flag()[0]) return false;
+  stage_issue(x, K, Kp, nullptr, xs, xraw);
+  return true;
+}
+
 // The second half of the staging (after stage_issue and any other loads of the phase's setup):
-// wait for the copies, then RMSNorm, scaling, swizzle and chunk sums in place.
+// wait for the copies, then RMSNorm and the integer form of every 16-input chunk (q8dot.cuh) in
+// place: 64 bytes per chunk, as many as its floats.
 __device__ void stage_finish(const Ctx& c, int K, int Kp, const float* gamma, float eps, float* xs, float* xc,
                              float* xraw) {
   const int tid = threadIdx.x, nchunk = Kp >> 4;
@@ -467,16 +602,12 @@ __device__ void stage_finish(const Ctx& c, int K, int Kp, const float* gamma, fl
         h[4 * j + 3] = h[4 * j + 3] * rinv * g.w;
       }
     }
-    float sum = 0.f;
+    uint4 q[4];
+    q8_chunk_encode(h, q[0], q[1], q[2], q[3]);
+    const int sw = (ch >> 1) & 3;  // the chunk's four 16-byte pieces, swizzled: lanes reading
+    uint4* xp = reinterpret_cast<uint4*>(xs + ch * 16);  // consecutive chunks hit distinct banks
 #pragma unroll
-    for (int j = 0; j < 16; ++j) sum += h[j];
-    const int sw = (ch >> 1) & 3;
-    float* xp = xs + ch * 16;
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-      reinterpret_cast<float4*>(xp)[j ^ sw] =
-          make_float4(h[4 * j] * kXScale, h[4 * j + 1] * kXScale, h[4 * j + 2] * kXScale, h[4 * j + 3] * kXScale);
-    xc[ch] = sum;
+    for (int j = 0; j < 4; ++j) xp[j ^ sw] = q[j];
   }
   __syncthreads();
 }
@@ -515,103 +646,107 @@ __device__ __forceinline__ void epilogue_pair(const Ctx& c, int l, int ph, int i
                                               const float* xraw, int pos, int sid) {
   const MegaArgs& a = *c.a;
   const Split& p = c.split()[ph];
-  const int t = p.p0 + i * p.pstride;  // the pair, projection-wide
+  const int t = p.p0 + i;  // the pair, projection-wide
   if (ph == kPhQKV) {  // rows (2t, 2t+1) are dims (j, j + D/2) of one head: RoPE, then q or fp16 K/V
     const int hd = a.D >> 1, head = t / hd, j = t - head * hd;
+    const unsigned tg = c.tag(l);
     if (head < a.Hq) {
       const float2 cs = c.rope_s()[i];
-      float* qo = a.qbuf + (size_t)head * a.D;
-      qo[j] = y0 * cs.x - y1 * cs.y;
-      qo[j + hd] = y1 * cs.x + y0 * cs.y;
+      tagged_t* qo = c.tq() + (size_t)head * a.D;
+      st_tag(qo + j, y0 * cs.x - y1 * cs.y, tg);
+      st_tag(qo + j + hd, y1 * cs.x + y0 * cs.y, tg);
     } else {
+      // the fp16 cache row, and its values (as rounded) tagged for this launch's attention
       const bool is_k = head < a.Hq + a.Hkv;
       const int kvh = head - a.Hq - (is_k ? 0 : a.Hkv);
       const MegaLayer& L = a.layers[l];
       const size_t base = (((size_t)sid * a.Hkv + kvh) * a.max_len + pos) * a.D;
+      __half h0, h1;
       if (is_k) {
         const float2 cs = c.rope_s()[i];
-        L.kc[base + j] = __float2half_rn(y0 * cs.x - y1 * cs.y);
-        L.kc[base + j + hd] = __float2half_rn(y1 * cs.x + y0 * cs.y);
+        h0 = __float2half_rn(y0 * cs.x - y1 * cs.y);
+        h1 = __float2half_rn(y1 * cs.x + y0 * cs.y);
       } else {
-        L.vc[base + j] = __float2half_rn(y0);
-        L.vc[base + j + hd] = __float2half_rn(y1);
+        h0 = __float2half_rn(y0);
+        h1 = __float2half_rn(y1);
       }
+      __half* cache = is_k ? L.kc : L.vc;
+      cache[base + j] = h0;
+      cache[base + j + hd] = h1;
+      tagged_t* kv = c.tkv() + ((size_t)(is_k ? 0 : a.Hkv) + kvh) * a.D;
+      st_tag(kv + j, __half2float(h0), tg);
+      st_tag(kv + j + hd, __half2float(h1), tg);
     }
   } else if (ph == kPhO) {
-    a.x1[2 * t] = __fadd_rn(xraw[2 * t], y0);
-    a.x1[2 * t + 1] = __fadd_rn(xraw[2 * t + 1], y1);
+    st_tag(c.tx1() + 2 * t, __fadd_rn(xraw[2 * t], y0), c.tag(l));
+    st_tag(c.tx1() + 2 * t + 1, __fadd_rn(xraw[2 * t + 1], y1), c.tag(l));
   } else if (MOE && ph == kPhRouter) {
-    a.logits[2 * t] = y0;
-    a.logits[2 * t + 1] = y1;
-  } else if (ph == kPhGU) {
+    st_tag(c.tlog() + 2 * t, y0, c.tag(l));
+    st_tag(c.tlog() + 2 * t + 1, y1, c.tag(l));
+  } else if (ph == kPhGU) {  // plain stores: the CTA counts itself done after the projection
     if (MOE) {  // pair t: expert slot t / EF, unit t % EF; scaled by the routing weight
       const int slot = t / a.EF, j = t - slot * a.EF;
       a.abuf[(size_t)slot * pad256(a.EF) + j] = silu(y0) * y1 * c.moe_wts()[slot];
     } else {
       a.abuf[t] = silu(y0) * y1;
     }
-  } else {
+  } else if (l + 1 < a.nl) {  // the block output: the next block's input
+    st_tag(c.th() + 2 * t, __fadd_rn(xraw[2 * t], y0), c.tag(l));
+    st_tag(c.th() + 2 * t + 1, __fadd_rn(xraw[2 * t + 1], y1), c.tag(l));
+  } else {  // the launch's output
     a.hout[2 * t] = __fadd_rn(xraw[2 * t], y0);
     a.hout[2 * t + 1] = __fadd_rn(xraw[2 * t + 1], y1);
   }
 }
 
-// This warp's piece of pair i (CTA-local) is summed.  A pair held by one warp goes straight to
-// its epilogue; a pair split between warps is finished by the warp whose piece completes it
-// (a shared-memory counter per pair): it adds the warps' pieces in a fixed order -- a tree over
-// the 16 warp slots, absent warps contributing zero -- so every output has one summation order
-// whichever warp finishes it.
+// This warp's slot j of pair i (CTA-local) is summed.  A whole-pair group (gs == sp) goes
+// straight to the epilogue once its last slot is in; a pair dealt slot by slot is finished by
+// the warp whose slot completes it (a shared-memory counter per pair), which adds the slots'
+// sums in slot order, so every output has one summation order whichever warp finishes it.
 template <bool MOE>
-__device__ __forceinline__ void finish_piece(const Ctx& c, int l, int ph, int i, int pfirst, float acc0, float acc1,
-                                             const float* xraw, int pos, int sid) {
+__device__ __forceinline__ void finish_slot(const Ctx& c, int l, int ph, int i, int j, float& acc0, float& acc1,
+                                            const float* xraw, int pos, int sid) {
   const Split& p = c.split()[ph];
-  acc0 = warp_sum(acc0);
-  acc1 = warp_sum(acc1);
-  const int ua = i * p.upp, ub = ua + p.upp;
-  bool holds = false;
-  if (c.lane < kMW) {
-    const int w0 = c.wu0()[c.lane], w1 = c.wu0()[c.lane + 1];
-    holds = w0 < w1 && w0 < ub && w1 > ua;
+  if (p.gs == p.sp) {
+    if (j != p.sp - 1) return;  // the pair goes on in this warp's next slot
+    const float y0 = warp_sum(acc0), y1 = warp_sum(acc1);
+    acc0 = acc1 = 0.f;
+    if (c.lane == 0) epilogue_pair<MOE>(c, l, ph, i, y0, y1, xraw, pos, sid);
+    return;
   }
-  const int nw = __popc(__ballot_sync(0xffffffffu, holds));
-  float y0 = acc0, y1 = acc1;
-  if (nw > 1) {
-    int done = 0;
-    if (c.lane == 0) {
-      c.part()[c.warp * kMaxPieces + i - pfirst] = make_float2(acc0, acc1);
-      __threadfence_block();
-      done = atomicAdd(c.cnt() + i, 1);
-    }
-    done = __shfl_sync(0xffffffffu, done, 0);
-    if (done != nw - 1) return;  // another warp's piece completes the pair
+  const float y0 = warp_sum(acc0), y1 = warp_sum(acc1);
+  acc0 = acc1 = 0.f;
+  if (c.lane == 0) {
+    float2* part = c.part() + i * p.sp;
+    part[j] = make_float2(y0, y1);
     __threadfence_block();
-    float2 v = make_float2(0.f, 0.f);
-    if (holds) v = c.part()[c.lane * kMaxPieces + i - c.pf()[c.lane]];
-#pragma unroll
-    for (int o = kMW / 2; o > 0; o >>= 1) {
-      v.x += __shfl_xor_sync(0xffffffffu, v.x, o);
-      v.y += __shfl_xor_sync(0xffffffffu, v.y, o);
+    if (atomicAdd(c.cnt() + i, 1) == p.sp - 1) {  // the pair's last slot
+      __threadfence_block();
+      float2 v = part[0];
+      for (int u = 1; u < p.sp; ++u) {
+        const float2 w = part[u];
+        v.x += w.x;
+        v.y += w.y;
+      }
+      epilogue_pair<MOE>(c, l, ph, i, v.x, v.y, xraw, pos, sid);
     }
-    y0 = v.x;
-    y1 = v.y;
   }
-  if (c.lane == 0) epilogue_pair<MOE>(c, l, ph, i, y0, y1, xraw, pos, sid);
 }
 
-// The per-projection scratch of phase ph: piece counters, warp ranges and (QKV) the RoPE factors
-// of the CTA's q and k pairs.  A CTA barrier must follow before the projection.
+// The per-projection scratch of phase ph: slot counters of split pairs and (QKV) the RoPE factors
+// of the CTA's q and k pairs (asynchronous copies, completed by the staging's wait).  A CTA
+// barrier must follow before the projection.
 __device__ void phase_setup(const Ctx& c, int ph, int pos) {
   const MegaArgs& a = *c.a;
   const Split& p = c.split()[ph];
   const int tid = threadIdx.x;
-  for (int i = tid; i < p.np; i += kMT) c.cnt()[i] = 0;
-  if (tid <= kMW) c.wu0()[tid] = tid * p.U / kMW;
-  if (tid < kMW) c.pf()[tid] = tid * p.U / kMW / p.upp;
+  if (p.gs != p.sp)
+    for (int i = tid; i < p.np; i += kMT) c.cnt()[i] = 0;
   if (ph == kPhQKV) {
     const int hd = a.D >> 1;
     for (int i = tid; i < p.np; i += kMT) {
-      const int t = p.p0 + i * p.pstride, head = t / hd;
-      if (head < a.Hq + a.Hkv) c.rope_s()[i] = __ldg(a.rope + (size_t)pos * hd + (t - head * hd));
+      const int t = p.p0 + i, head = t / hd;
+      if (head < a.Hq + a.Hkv) cp_async8(c.rope_s() + i, a.rope + (size_t)pos * hd + (t - head * hd));
     }
   }
 }
@@ -623,11 +758,8 @@ template <bool MOE>
 __device__ bool gemv_phase(const Ctx& c, Stream& s, int l, int ph, const float* xs, const float* xc,
                            const float* xraw, int pos, int sid) {
   const Split& p = c.split()[ph];
-  Cur q = cur_start(p, c.warp);
-  const int pfirst = q.pr;
   float acc0 = 0.f, acc1 = 0.f;
-  int cur = -1;
-  while (q.left > 0) {
+  for (Cur q = cur_start(p, c.warp); cur_valid(p, q, c.warp); cur_advance(p, q)) {
     const int slot = s.consumed % kDepth;
     const bool landed = mbar_wait(c.bars() + c.warp * kDepth + slot, (unsigned)(s.consumed / kDepth) & 1u, kWaitNs);
     if (!__all_sync(0xffffffffu, landed)) {  // warp-uniform decision
@@ -635,51 +767,50 @@ __device__ bool gemv_phase(const Ctx& c, Stream& s, int l, int ph, const float* 
       stream_drain(c, s);
       return false;
     }
+    // the slot's bytes go to registers (lane: chunks lane + 32 u of both rows) and the ring slot
+    // is refilled at once, so the ring keeps kDepth slots in flight while this one is summed
     const unsigned char* sq = c.ringq() + (size_t)(c.warp * kDepth + slot) * kSlotQ;
     const unsigned char* ss = c.rings() + (size_t)(c.warp * kDepth + slot) * kSlotS;
-    const int len = cur_len(p, q), k = q.k;
-    {
-      if (q.pr != cur) {
-        if (cur >= 0) finish_piece<MOE>(c, l, ph, cur, pfirst, acc0, acc1, xraw, pos, sid);
-        acc0 = acc1 = 0.f;
-        cur = q.pr;
+    const int nch = slot_len(p, q.j) >> 4, cb = slot_k(p, q.j) >> 4;
+    constexpr int U = kSlotCols / 16 / 32;  // chunks of a row per lane
+    uint4 wa[U], wb[U];
+    uint32_t sab[U];  // the two rows' fp16 scales of each chunk
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int cl = c.lane + 32 * u;
+      if (cl < nch) {
+        wa[u] = *reinterpret_cast<const uint4*>(sq + cl * 16);
+        wb[u] = *reinterpret_cast<const uint4*>(sq + kSlotCols + cl * 16);
+        sab[u] = (uint32_t)*reinterpret_cast<const uint16_t*>(ss + (cl >> 1) * 2) |
+                 ((uint32_t)*reinterpret_cast<const uint16_t*>(ss + kSlotCols / 16 + (cl >> 1) * 2) << 16);
       }
-      const unsigned char* q0 = sq;
-      const unsigned char* q1 = q0 + kSlotCols;
-      const unsigned char* s0 = ss;
-      const unsigned char* s1 = s0 + kSlotCols / 16;
-      const int nch = len >> 4, cb = k >> 4;
-#pragma unroll 2
-      for (int cl = c.lane; cl < nch; cl += 32) {
-        const int ch = cb + cl;
-        const int sw = (ch >> 1) & 3;
-        const float4* xp = reinterpret_cast<const float4*>(xs + ch * 16);
-        const float4 x0 = xp[0 ^ sw], x1 = xp[1 ^ sw], x2 = xp[2 ^ sw], x3 = xp[3 ^ sw];
-        const float corr = -128.0f * xc[ch];
-        const uint4 w0 = *reinterpret_cast<const uint4*>(q0 + cl * 16);
-        const uint4 w1 = *reinterpret_cast<const uint4*>(q1 + cl * 16);
-        const float f0 = h2f_bits(*reinterpret_cast<const uint16_t*>(s0 + (cl >> 1) * 2));
-        const float f1 = h2f_bits(*reinterpret_cast<const uint16_t*>(s1 + (cl >> 1) * 2));
-        float d0, d1;
-        dot16x2(w0, w1, x0, x1, x2, x3, d0, d1);
-        acc0 = fmaf(f0, fmaf(d0, kPScale, corr), acc0);
-        acc1 = fmaf(f1, fmaf(d1, kPScale, corr), acc1);
-      }
-      cur_advance(p, q, len);
     }
-    __syncwarp();  // the slot is consumed: refill it
+    __syncwarp();  // the slot is read: refill it
     ++s.consumed;
     stream_issue<MOE>(c, s);
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int cl = c.lane + 32 * u;
+      if (cl < nch) {
+        const int ch = cb + cl;
+        const int sw = (ch >> 1) & 3;
+        const uint4* xp = reinterpret_cast<const uint4*>(xs + ch * 16);
+        const uint4 l0 = xp[0 ^ sw], l1 = xp[1 ^ sw], l2 = xp[2 ^ sw], k = xp[3 ^ sw];
+        const float ek = __uint_as_float(k.w);  // the chunk's unit u
+        const float f0 = h2f_bits((uint16_t)(sab[u] & 0xFFFFu)) * ek, f1 = h2f_bits((uint16_t)(sab[u] >> 16)) * ek;
+        acc0 = fmaf(f0, q8_chunk_dot(wa[u], l0, l1, l2, k), acc0);
+        acc1 = fmaf(f1, q8_chunk_dot(wb[u], l0, l1, l2, k), acc1);
+      }
+    }
+    finish_slot<MOE>(c, l, ph, q.pr, q.j, acc0, acc1, xraw, pos, sid);
   }
-  if (cur >= 0) finish_piece<MOE>(c, l, ph, cur, pfirst, acc0, acc1, xraw, pos, sid);
   return true;
 }
 
-// Routing of MoE block l, after the grid barrier that follows the router phase (whose tasks
-// wrote the logits to global memory): every CTA reads all logits, takes the top_k by rank
-// (ties to the lower id) and their softmax; ids, weights and the ready block into shared
-// memory.
-__device__ void rank_experts(const Ctx& c, int l) {
+// Routing of MoE block l: every CTA gathers all router logits (tagged, as they arrive), takes
+// the top_k by rank (ties to the lower id) and their softmax; ids, weights and the ready block
+// into shared memory.  False after a timed-out wait (CTA-uniform).
+__device__ bool rank_experts(const Ctx& c, int l) {
   const MegaArgs& a = *c.a;
   float* sel = c.sel();
   int* sel_id = c.sel_id();
@@ -687,8 +818,9 @@ __device__ void rank_experts(const Ctx& c, int l) {
   float* wts = c.moe_wts();
   const int E = a.n_experts, k = a.top_k;
   if (threadIdx.x < k) sel_id[threadIdx.x] = threadIdx.x;  // valid ids whatever the logits hold
-  for (int e = threadIdx.x; e < E; e += kMT) c.logits()[e] = __ldcg(a.logits + e);
-  __syncthreads();
+  // the slot partials' region is free between the router projection and the experts' setup
+  const bool got = gather_tagged(c, c.tlog(), E, E, E, c.tag(l), reinterpret_cast<tagged_t*>(c.part()), c.logits());
+  if (!__syncthreads_and(got)) return false;
   // rank of expert e: 4 threads, each counting over a quarter of the experts
   const int qlen = (E + 3) >> 2;
   for (int base = c.warp * 32; base < E * 4; base += kMT) {
@@ -722,6 +854,7 @@ __device__ void rank_experts(const Ctx& c, int l) {
     if (c.lane == 0) *c.moe_ready() = l;
   }
   __syncthreads();
+  return true;
 }
 
 // Positions [c0, c1) of attention item `it` (KV head it % Hkv, chunk it / Hkv).
@@ -749,9 +882,12 @@ __device__ __forceinline__ void attn_issue(const Ctx& c, unsigned char* area, co
   }
 }
 
-// Split-K attention of block l over this CTA's items; the last chunk of a KV head to finish
-// together with the other chunks of its head merges a slice of the head's outputs into
-// obuf.  `prefetched`: tile 0 of the first item was issued before the preceding barrier.
+// Split-K attention of block l over this CTA's items (KV head, chunk of positions): q of the
+// head's group and (for the chunk holding the current position) the current K and V rows are
+// gathered from their tagged vectors as they arrive; the chunk's partial (running max and sum,
+// unnormalised output) goes to global memory, and the chunk that arrives last on its head's
+// counter merges all of the head's chunks (weights e^(m_c - M), sums in chunk order) into the
+// tagged attention output.  `prefetched`: tile 0 of the first item was issued earlier.
 template <int D, int G>
 __device__ bool attention_phase(const Ctx& c, int l, unsigned char* area, unsigned& aphase, bool prefetched, int pos,
                                 int sid) {
@@ -779,9 +915,14 @@ __device__ bool attention_phase(const Ctx& c, int l, unsigned char* area, unsign
     item_range(a, it, pos, kvh, chunk, c0, c1);
     const __half* kb = Ly.kc + ((size_t)sid * a.Hkv + kvh) * (size_t)a.max_len * D;
     const __half* vb = Ly.vc + ((size_t)sid * a.Hkv + kvh) * (size_t)a.max_len * D;
-    for (int i = tid; i < G * D; i += kMT) {
-      const int g = i / D, d = i - g * D;
-      qs[g * D + q_slot<D>(d)] = __ldcg(a.qbuf + (size_t)kvh * G * D + i);
+    const unsigned tg = c.tag(l) + a.bar_extra;
+    bool got = true;
+    for (int i = tid; 2 * i < G * D && got; i += kMT) {  // q of the group, as it arrives
+      const int g = 2 * i / D, d = 2 * i - g * D;
+      float2 v;
+      got = poll_pair(c, c.tq() + (size_t)kvh * G * D + 2 * i, tg, v);
+      qs[g * D + q_slot<D>(d)] = v.x;
+      qs[g * D + q_slot<D>(d + 1)] = v.y;
     }
     if (tid < G) {
       st_m[tid] = -INFINITY;
@@ -794,15 +935,18 @@ __device__ bool attention_phase(const Ctx& c, int l, unsigned char* area, unsign
       const int np = min(T, c1 - p0);
       const int nold = max(0, min(np, pos - p0));
       if (!(prefetched && p0 == c0 && it == (int)blockIdx.x) && tid == 0) attn_issue<D, G>(c, area, kb, vb, p0, nold);
-      if (nold < np) {  // the current position: written by this launch's QKV phase, read through L2
+      if (nold < np) {  // the current position: this launch's K and V rows, from their tagged copies
         const int r = pos - p0;
-        for (int i = tid; i < D / 8; i += kMT) {
-          reinterpret_cast<uint4*>(Ks + (size_t)r * D)[i] = __ldcg(reinterpret_cast<const uint4*>(kb + (size_t)pos * D) + i);
-          reinterpret_cast<uint4*>(Vs + (size_t)r * D)[i] = __ldcg(reinterpret_cast<const uint4*>(vb + (size_t)pos * D) + i);
+        for (int i = tid; 2 * i < 2 * D && got; i += kMT) {
+          const bool is_v = 2 * i >= D;
+          const int d = 2 * i - (is_v ? D : 0);
+          float2 v;
+          got = poll_pair(c, c.tkv() + ((size_t)(is_v ? a.Hkv : 0) + kvh) * D + d, tg, v);
+          *reinterpret_cast<__half2*>((is_v ? Vs : Ks) + (size_t)r * D + d) = __floats2half2_rn(v.x, v.y);
         }
       }
       const bool landed = mbar_wait(abar, aphase & 1u, kWaitNs);
-      if (!__syncthreads_and(landed)) {  // CTA-uniform decision (also orders the row copy above)
+      if (!__syncthreads_and(landed && got)) {  // CTA-uniform decision (also orders the row copy above)
         if (tid == 0) set_error(c);
         return false;
       }
@@ -909,42 +1053,26 @@ __device__ bool attention_phase(const Ctx& c, int l, unsigned char* area, unsign
       po[i] = v;
     }
     if (tid < G) a.part_ml[((size_t)kvh * G + tid) * nch + chunk] = make_float2(st_m[tid], st_l[tid]);
-    // the CTA barrier orders every thread's partial writes before thread 0's release (cumulative
-    // at GPU scope), which the merging CTAs acquire
+    // every thread's partial writes, then one arrival on the head's counter (monotonic within a
+    // launch); the chunk that completes the head merges it
     __syncthreads();
-    if (tid == 0) red_release_add(a.bar + 2 + kvh, 1u);
-  }
-  // Merge, spread over the chunks: once every chunk of its head has arrived, the CTA of
-  // chunk j merges outputs [j SL, (j + 1) SL) of the head -- weights e^(m_c - M) per head,
-  // weighted sums in chunk order.  (Every CTA arrives on all of its items before waiting.)
-  constexpr int GD = G * D;
-  const int SL = (GD + nch - 1) / nch;
-  for (int it = blockIdx.x; it < items; it += gridDim.x) {
-    int kvh, chunk, c0, c1;
-    item_range(a, it, pos, kvh, chunk, c0, c1);
     if (tid == 0) {
-      const unsigned target = (unsigned)(l + 1) * (unsigned)nch;
-      const unsigned* hc = a.bar + 2 + kvh;
-      if (ld_acquire_u32(hc) < target) {
-        const uint64_t t0 = global_ns();
-        while (ld_acquire_u32(hc) < target)
-          if (global_ns() - t0 > kWaitNs) {
-            set_error(c);
-            break;
-          }
-      }
+      __threadfence();
+      c.flag()[1] = atomicAdd(a.bar + 2 + kvh, 1u) == (unsigned)(l + 1) * (unsigned)nch - 1u;
     }
     __syncthreads();
-    if (c.flag()[0]) return false;
-    const int i0 = min(GD, chunk * SL), n = min(GD, i0 + SL) - i0;
+    if (!c.flag()[1]) continue;
+    __threadfence();
+    constexpr int GD = G * D;
+    constexpr int CB = (2 * T * D * 2) / (GD * 4);  // chunk partials that fit over the K/V tiles
     float2* mls = reinterpret_cast<float2*>(area + AL::mls);  // [G][nch]
     float* wts = reinterpret_cast<float*>(area + AL::wts);    // [nch][G]
-    float* pst = reinterpret_cast<float*>(area + AL::ks);     // [nch][SL] this slice of every partial
-    for (int i = tid; i < G * nch; i += kMT) mls[i] = __ldcg(a.part_ml + (size_t)kvh * G * nch + i);
-    for (int i = tid; i < nch * n; i += kMT) {
-      const int ck = i / n, k = i - ck * n;
-      pst[ck * SL + k] = __ldcg(a.part_o + ((size_t)kvh * nch + ck) * GD + i0 + k);
-    }
+    float* pst = reinterpret_cast<float*>(area + AL::ks);     // [CB][GD] chunk partials
+    const float* pk = a.part_o + (size_t)kvh * nch * GD;
+    // the (max, sum) pairs and the first chunks' partials of the head, each fetched at once
+    for (int i = tid; i < G * nch; i += kMT) cp_async8(mls + i, a.part_ml + (size_t)kvh * G * nch + i);
+    for (int i = tid; i < min(nch, CB) * GD / 4; i += kMT) cp_async16(pst + 4 * i, pk + 4 * i);
+    cp_async_wait_all();
     __syncthreads();
     if (c.warp < G) {  // warp g: the chunk weights of head g (lanes over the chunks)
       const int g = c.warp;
@@ -962,14 +1090,25 @@ __device__ bool attention_phase(const Ctx& c, int l, unsigned char* area, unsign
       if (c.lane == 0) st_L[g] = Ls;
     }
     __syncthreads();
-    for (int k = c.warp; k < n; k += kMW) {  // a warp per output, lanes over the chunks
-      const int g = (i0 + k) / D;
-      float acc = 0.f;
-      for (int ck = c.lane; ck < nch; ck += 32) acc = fmaf(wts[ck * G + g], pst[ck * SL + k], acc);
-      acc = warp_sum(acc);
-      if (c.lane == 0) a.obuf[(size_t)kvh * GD + i0 + k] = acc / st_L[g];
+    // a thread per output (GD <= 2 kMT), the chunks in order, CB chunks per batch
+    float acc0 = 0.f, acc1 = 0.f;
+    for (int ck0 = 0; ck0 < nch; ck0 += CB) {
+      if (ck0 > 0) {
+        __syncthreads();  // the previous batch is read
+        for (int i = tid; i < min(CB, nch - ck0) * GD / 4; i += kMT)
+          cp_async16(pst + 4 * i, pk + (size_t)ck0 * GD + 4 * i);
+        cp_async_wait_all();
+        __syncthreads();
+      }
+      for (int ck = ck0; ck < min(nch, ck0 + CB); ++ck) {
+        const float* pc = pst + (size_t)(ck - ck0) * GD;
+        acc0 = fmaf(wts[ck * G + tid / D], pc[tid], acc0);
+        if (tid + kMT < GD) acc1 = fmaf(wts[ck * G + (tid + kMT) / D], pc[tid + kMT], acc1);
+      }
     }
-    __syncthreads();
+    if (tid < GD) st_tag(c.to() + (size_t)kvh * GD + tid, acc0 / st_L[tid / D], c.tag(l));
+    if (tid + kMT < GD) st_tag(c.to() + (size_t)kvh * GD + tid + kMT, acc1 / st_L[(tid + kMT) / D], c.tag(l));
+    __syncthreads();  // the merge scratch is read before the next item's tile lands
   }
   return true;
 }
@@ -995,9 +1134,11 @@ __global__ void __launch_bounds__(kMT, 1) mega_decode_kernel(const MegaArgs a) {
   unsigned char* area = sm + off_u;  // union: projection input and warp partials, or attention tiles
   const int KpQ = pad256(a.Hq * a.D), KpF = pad256(a.F);
   const int Kx = max(KpH, max(KpQ, KpF));
-  float* xs = reinterpret_cast<float*>(area);
+  // the union area: the per-projection scratch, then the staged input and its chunk sums (a
+  // tagged input is gathered beyond the current projection's Kp), or the attention tiles
+  c.ps = area;
+  float* xs = reinterpret_cast<float*>(area + kPsBytes);
   float* xc = xs + Kx;
-  c.ps = reinterpret_cast<unsigned char*>(xc + Kx / 16);
 
   if (threadIdx.x < kMW * kDepth + 1) mbar_init(c.bars() + threadIdx.x, 1);
   if (threadIdx.x == 0) {
@@ -1009,6 +1150,7 @@ __global__ void __launch_bounds__(kMT, 1) mega_decode_kernel(const MegaArgs a) {
   mbar_fence_init();
   __syncthreads();
   const int pos = __ldcg(a.pos), sid = __ldcg(a.seq);
+  c.seq = __ldcg(a.bar + kSeqWord);
 
   Stream s;
   s.l = 0;
@@ -1022,48 +1164,63 @@ __global__ void __launch_bounds__(kMT, 1) mega_decode_kernel(const MegaArgs a) {
     c.wptr()[2 * c.warp + 1] = w0.s;
   }
   __syncwarp();
-  if (s.q.left == 0) stream_normalise<MOE>(c, s);
+  if (!cur_valid(splits[0], s.q, c.warp)) stream_normalise<MOE>(c, s);
   for (int d = 0; d < kDepth; ++d) stream_issue<MOE>(c, s);
 
-  unsigned nbar = 0, aphase = 0;
+  unsigned aphase = 0;
   bool ok = true;
   constexpr bool moe = MOE;
-  // one call site per step (the projection step is the same code for every phase: the kernel
-  // stays small enough for the instruction cache)
+  // One call site per step (the projection step is the same code for every phase: the kernel
+  // stays small enough for the instruction cache).  No grid barrier: each step waits for the
+  // tagged entries it reads, and a CTA reads a step's input only if it has work in the step --
+  // so every reader of a vector produces a share of what the vector's next writers wait for.
   for (int l = 0; l < a.nl && ok; ++l) {
     const MegaLayer& L = a.layers[l];
     for (int ph = 0; ph < kPhases && ok; ++ph) {
       if (ph == kPhRouter && !moe) continue;
+      const Split& sp = splits[ph];
       if (ph == kPhGU && moe) {
         stream_refill<MOE>(c, s);  // the routing is known: the selected experts' slices stream in
         phase_setup(c, ph, pos);
         __syncthreads();
-      } else {
+      } else if (sp.np > 0 || (MOE && ph == kPhRouter)) {  // MoE: every CTA stages the router input
         // the projection's input: QKV and the router (or the dense gate/up) normalise the
         // residual (gamma_1, gamma_2; the raw residual is kept for the residual adds), O and
         // down take the attention output and the SwiGLU output as they are; the experts'
         // gate/up reuses the router's input
         const bool norm2 = ph == kPhRouter || ph == kPhGU;
-        const float* in = ph == kPhQKV ? (l == 0 ? a.hin : a.hout) : ph == kPhO ? a.obuf : ph == kPhDown ? a.abuf : a.x1;
         const int K = ph == kPhO ? a.Hq * a.D : ph == kPhDown ? a.F : a.H;
         const int Kp = ph == kPhO ? KpQ : ph == kPhDown ? KpF : KpH;
         const float* gamma = ph == kPhQKV ? L.attn_norm : norm2 ? L.ffn_norm : nullptr;
-        // the gamma of the next normalising stage is fetched into L2 one phase ahead (the weight
+        // the gamma of the next normalising step is fetched into L2 one step ahead (the weight
         // stream evicts it between blocks): one 128-byte line per CTA
         if (threadIdx.x == 0 && (ph == kPhO || ph == kPhDown)) {
           const float* g = ph == kPhO ? L.ffn_norm : (l + 1 < a.nl ? a.layers[l + 1].attn_norm : nullptr);
           for (int i = blockIdx.x * 32; g && i < a.H; i += gridDim.x * 32) prefetch_l2_last(g + i);
         }
-        stage_issue(in, K, Kp, gamma, xs, xraw);
         phase_setup(c, ph, pos);
+        if (ph == kPhQKV && l == 0) {  // the launch's input, written before the launch
+          stage_issue(a.hin, K, Kp, gamma, xs, xraw);
+        } else if (ph == kPhDown) {  // the SwiGLU output of every CTA
+          ok = stage_counted(c, a.bar, (unsigned)(l + 1) * gridDim.x, a.abuf, K, Kp, xs, xraw);
+        } else {
+          const tagged_t* in = ph == kPhQKV ? c.th() : ph == kPhO ? c.to() : c.tx1();
+          ok = stage_gather(c, in, K, Kp, K, K, c.tag(ph == kPhQKV ? l - 1 : l), gamma, xs, xraw,
+                            reinterpret_cast<tagged_t*>(xs + Kp));
+        }
+        if (!ok) break;
         stage_finish(c, K, Kp, gamma, a.eps, xs, xc, xraw);
       }
       ok = __syncthreads_and(gemv_phase<MOE>(c, s, l, ph, xs, xc, xraw, pos, sid));
-      if (ph == kPhQKV) {
+      if (ok && ph == kPhGU && threadIdx.x == 0) {  // this CTA's SwiGLU outputs are written
+        __threadfence();
+        red_release_add(a.bar, 1u);
+      }
+      if (ok && ph == kPhQKV) {
         // tile 0 of this CTA's first attention item (positions of earlier steps) streams in
-        // while the grid meets
+        // while q, k and v arrive
         bool pre = false;
-        if (ok && (int)blockIdx.x < a.Hkv * a.n_chunks) {
+        if ((int)blockIdx.x < a.Hkv * a.n_chunks) {
           int kvh, chunk, c0, c1;
           item_range(a, blockIdx.x, pos, kvh, chunk, c0, c1);
           if (c0 < c1) {
@@ -1076,16 +1233,10 @@ __global__ void __launch_bounds__(kMT, 1) mega_decode_kernel(const MegaArgs a) {
             }
           }
         }
-        if (ok) ok = grid_barrier(c, ++nbar);
-        if (!ok) {
-          if (pre && threadIdx.x == 0) mbar_wait(c.bars() + kMW * kDepth, aphase & 1u, kWaitNs);
-          break;
-        }
         ok = attention_phase<D, G>(c, l, area, aphase, pre, pos, sid);
+        if (!ok && pre && threadIdx.x == 0) mbar_wait(c.bars() + kMW * kDepth, aphase & 1u, kWaitNs);
       }
-      // the residual after the last projection of the last block is the launch's output
-      if (ok && (ph < kPhDown || l + 1 < a.nl)) ok = grid_barrier(c, ++nbar);
-      if (MOE && ok && ph == kPhRouter) rank_experts(c, l);
+      if (MOE && ok && ph == kPhRouter) ok = rank_experts(c, l);
     }
   }
   if (!ok) stream_drain(c, s);
@@ -1100,7 +1251,10 @@ size_t mega_smem(int H, int q_dim, int F, int D, int G) {
                     : G == 4 ? AttnLayout<64, 4>::total : AttnLayout<64, 8>::total;
   else attn = G == 1 ? AttnLayout<128, 1>::total : G == 2 ? AttnLayout<128, 2>::total
             : G == 4 ? AttnLayout<128, 4>::total : AttnLayout<128, 8>::total;
-  const size_t u = std::max((size_t)Kx * 4 + (size_t)(Kx / 16) * 4 + kPsBytes, attn);
+  // the staged input with its chunk sums, or a tagged input (H or q_dim entries of 8 bytes)
+  // gathered beyond the projection's Kp floats
+  const size_t gather = std::max((size_t)pad256(H) * 4 + (size_t)H * 8, (size_t)pad256(q_dim) * 4 + (size_t)q_dim * 8);
+  const size_t u = std::max(kPsBytes + std::max((size_t)Kx * 4 + (size_t)(Kx / 16) * 4, gather), attn);
   return off_u + u + 128;  // + alignment of the dynamic base
 }
 

@@ -54,7 +54,7 @@ void walk_plan(const stage_model_cfg& c, int begin, int end, std::vector<LayerDe
                float** obuf, float** abuf, float** feat, float** logits, int** argmax, float** part_o,
                float2** part_ml, int** counters, int** d_seq, int** d_pos, int** d_tok, int** d_rows, int** err_word,
                float** moe_logits, int** moe_ids, float** moe_wts, __nv_bfloat16** act_bf16,
-               __nv_bfloat16** ffn_bf16, lrs::MegaLayer** mlayers, float** mega_x1, unsigned** mega_bar,
+               __nv_bfloat16** ffn_bf16, lrs::MegaLayer** mlayers, unsigned long long** mega_tags, unsigned** mega_bar,
                int** shared_id0, F&& f) {
   auto q8 = [&](DevQ8* m, int N, int K) {
     if (m) {
@@ -115,9 +115,9 @@ void walk_plan(const stage_model_cfg& c, int begin, int end, std::vector<LayerDe
   f(T * 4, (void**)d_tok);
   f(T * 4, (void**)d_rows);
   f(4, (void**)err_word);
-  // persistent decode: block descriptors, post-attention residual, grid barrier
+  // persistent decode: block descriptors, the tagged vectors between its steps, counters
   f((size_t)(end - begin) * sizeof(lrs::MegaLayer), (void**)mlayers);
-  f((size_t)H * 4, (void**)mega_x1);
+  f(lrs::mega_tag_entries(H, Hq * D, Hkv * D, c.n_experts) * 8, (void**)mega_tags);
   f(256, (void**)mega_bar);
   if (!moe && c.gemm_bf16_min_tokens > 0) {  // bf16 operands of the tensor-core GEMMs
     f(T * (size_t)std::max(kpad(H), kpad(Hq * D)) * 2, (void**)act_bf16);
@@ -202,8 +202,8 @@ struct stage {
   __nv_bfloat16* act_bf16 = nullptr;  // [max_tokens][Kp] bf16 GEMM operand (normed x, attention out)
   __nv_bfloat16* ffn_bf16 = nullptr;  // [max_tokens][Kp(ffn)] bf16 SwiGLU output
   lrs::MegaLayer* mlayers = nullptr;  // device block descriptors of the persistent decode
-  float* mega_x1 = nullptr;           // [H] its post-attention residual
-  unsigned* mega_bar = nullptr;       // its grid barrier counters
+  unsigned long long* mega_tags = nullptr;  // its tagged vectors between steps
+  unsigned* mega_bar = nullptr;       // its counters (exit, attention, launch sequence)
   bool mega = false;                  // single-token decode calls use the persistent kernel
   bool call_prefill = false;          // the current forward is a prefill call (causal attention kernel)
   std::vector<cudaEvent_t> tev;  // measurement: event pair around each FFN up-projection launch
@@ -574,7 +574,7 @@ int forward_dev(stage* st, int n, const int* d_seq, const int* d_pos, const int*
     m.nl = st->end - st->begin;
     m.hin = st->first ? hout : hin;
     m.hout = hout;
-    m.x1 = st->mega_x1;
+    m.tags = st->mega_tags;
     m.qbuf = st->qbuf;
     m.obuf = st->obuf;
     m.abuf = st->abuf;
@@ -1004,7 +1004,7 @@ int stage_create(const stage_model_cfg* cfg, stage_layer_range range, const stag
   walk_plan(*cfg, range.begin, range.end, &st->layers, &st->embed, &st->head, &st->final_norm, &st->kc, &st->vc,
             &st->rope, &st->qbuf, &st->obuf, &st->abuf, &st->feat, &st->logits, &st->argmax, &st->part_o,
             &st->part_ml, &st->counters, &st->d_seq, &st->d_pos, &st->d_tok, &st->d_rows, &st->err_word,
-            &st->moe_logits, &st->moe_ids, &st->moe_wts, &st->act_bf16, &st->ffn_bf16, &st->mlayers, &st->mega_x1,
+            &st->moe_logits, &st->moe_ids, &st->moe_wts, &st->act_bf16, &st->ffn_bf16, &st->mlayers, &st->mega_tags,
             &st->mega_bar, &st->shared_id0, [&](size_t b, void** slot) {
               if (slot) *slot = st->arena + off;
               off += round_up(b, kAlign);
@@ -1027,7 +1027,7 @@ int stage_create(const stage_model_cfg* cfg, stage_layer_range range, const stag
   {
     const char* mg = getenv("LRS_PERSISTENT");
     const bool moe = cfg->n_experts > 0;
-    st->mega = !(mg && mg[0] == '0') && cfg->shared_ffn == 0 &&
+    st->mega = !(mg && mg[0] == '0') && cfg->shared_ffn == 0 && (!moe || cfg->expert_ffn % 2 == 0) &&
                lrs::mega_supported(cfg->hidden, cfg->n_q_heads * cfg->head_dim,
                                    moe ? cfg->top_k * kpad(cfg->expert_ffn) : cfg->ffn, cfg->head_dim,
                                    cfg->n_q_heads / cfg->n_kv_heads, cfg->n_experts, cfg->top_k);
