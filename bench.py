@@ -15,6 +15,9 @@ roofline: bytes per token (weights once + KV at the context) / step time against
 prefill: on the same dense stages, 4 prompts x 512 tokens as one step (every projection a
         tcgen05 GEMM with bf16 operands), prefill tok/s and the gate/up GEMM's TFLOP/s
         against the measured bf16 peak.
+moe_decode, batched_70b_decode: the MoE 40-block decoder (2 stages 21/19, context 4096) and
+        the 70B-shape batched decode (4 stages of 20 blocks, 64 ragged sequences), each as a
+        record of the same line with its own roofline, e2e and clocks.
 --impl reference: the CPU oracle on the host cores, on a bounded sample of the workload.
 """
 from __future__ import annotations
@@ -207,15 +210,16 @@ def run_prefill(gp, model, warm=2, reps=3):
                               "flops_per_step": gemm_flops_per_token(model) * T}}
 
 
-def run_gpu(args):
+def run_gpu(args, config=None, dist=None):
+    """One decode workload (cfg1 dense, cfg2 MoE): the bench line's fields, as a dict."""
     import torch
     import layer_range_stage_gb300 as L  # noqa: F401
 
     rank, world, local = dist_env()
     torch.cuda.set_device(local)
-    dist = init_dist(world, "nccl")  # replicas only: the process group carries timing, no data
-    wl = WORKLOADS[args.config]
-    model = synth.CONFIGS[args.config]
+    config = config or args.config
+    wl = WORKLOADS[config]
+    model = synth.CONFIGS[config]
     bounds = wl["bounds"]
     context = args.context or wl["context"]
     if args.layers:  # reduced depth: profiling of a small case only, never a bench line
@@ -231,7 +235,7 @@ def run_gpu(args):
     else:
         gp = build_gpu_pipeline(model, bounds, max_len, max_tokens=512)
     build_s = time.time() - t_build
-    prefill = run_prefill(gp, model) if dense else None
+    prefill = run_prefill(gp, model) if (dense and not getattr(args, "no_prefill", False)) else None
     # prefill the seeded context in chunks of 512 tokens through the stages
     prompt = synth.prompt_tokens(model, rank, context)
     tok = None
@@ -317,7 +321,7 @@ def run_gpu(args):
         "hbm_gbs_achieved": round(gbs, 1),
         "roofline": {"bound": "hbm", "achieved": round(k_gbs, 1) if k_gbs else None, "peak": peak, "unit": "GB/s",
                      "frac": round(k_gbs / peak, 4) if (peak and k_gbs) else None,
-                     "traffic": TRAFFIC.get(args.config) if not (args.layers or args.context) else None,
+                     "traffic": TRAFFIC.get(config) if not (args.layers or args.context) else None,
                      "kernel": kernel,
                      "bytes_per_launch": round(k_bytes), "mean_launch_us": round(k_us, 3), "launches_timed": k_n,
                      "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs)" if peak else "fallback"},
@@ -332,12 +336,7 @@ def run_gpu(args):
     }
     if args.layers or args.context:
         line["config"]["profiling_case"] = f"{model.n_layers} blocks, context {context}: not the benchmark workload"
-    if rank == 0 and not args.no_cpu_baseline and world == 1 and args.config == 1:
-        line["cpu_baseline"] = cpu_baseline(args)
-    if rank == 0:
-        print(json.dumps(line), flush=True)
-    if dist:
-        dist.destroy_process_group()
+    return line
 
 
 def batched_lens(nseq):
@@ -345,7 +344,7 @@ def batched_lens(nseq):
     return np.random.default_rng(4401).integers(128, 4097, nseq)
 
 
-def run_batched(args):
+def run_batched(args, dist=None):
     """The 70B-shape batched decode: 4 stages of 20 blocks, 64 sequences of ragged context,
     one token per sequence per step (all stages, the final norm, the readout of the 64 rows
     and their argmax), on the float32 GEMV path and on the tensor-core path (bf16 operands,
@@ -359,7 +358,6 @@ def run_batched(args):
 
     rank, world, local = dist_env()
     torch.cuda.set_device(local)
-    dist = init_dist(world, "nccl")  # replicas only
     wl = WORKLOADS[4]
     model, bounds = synth.CONFIGS[4], wl["bounds"]
     if args.layers:  # reduced depth: profiling of a small case only, never a bench line
@@ -368,7 +366,7 @@ def run_batched(args):
     nseq = wl["seqs"]
     lens = batched_lens(nseq)
     seqs = np.arange(nseq)
-    steps, warmup, n_timing, n_e2e = args.steps, args.warmup, 2, 4
+    steps, warmup, n_timing, n_e2e = getattr(args, "batched_steps", None) or args.steps, args.warmup, 2, 4
     max_len = int(lens.max()) + warmup + steps + n_timing + n_e2e + 8
     t_build = time.time()
     block = synth.layer_weights(model, 0)
@@ -470,17 +468,57 @@ def run_batched(args):
     }
     if args.layers:
         line["config"]["profiling_case"] = f"{model.n_layers} blocks: not the benchmark workload"
-    if rank == 0:
-        print(json.dumps(line), flush=True)
-    if dist:
-        dist.destroy_process_group()
+    return line
 
 
-def cpu_baseline(args, budget_s=None):
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.strip().lower().startswith("model name"):
+                return ln.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        for ln in open("/proc/cpuinfo"):
+            if ln.lower().startswith(("model name", "cpu model")):
+                return ln.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return None
+
+
+def blas_threads():
+    """Threads the oracle's BLAS runs on: the thread-count variables OpenBLAS/OpenMP read,
+    else every core (their default)."""
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        v = os.environ.get(var)
+        if v and v.isdigit():
+            return int(v)
+    return os.cpu_count()
+
+
+def cpu_baseline_one_thread(budget_s):
+    """The same sample on one thread: a child process with the BLAS limited to one thread
+    (the limit takes effect only when the BLAS starts)."""
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    code = ("import json, sys; sys.path.insert(0, %r); import bench; "
+            "print(json.dumps(bench.cpu_baseline(None, %r, one_thread_child=True)))" % (ROOT, budget_s))
+    try:
+        r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=600)
+        return json.loads(r.stdout.strip().splitlines()[-1])
+    except Exception as e:  # reported, not fatal
+        return {"error": str(e)[:200]}
+
+
+def cpu_baseline(args, budget_s=None, one_thread_child=False):
     """The oracle as it stands, on a bounded sample: decode tokens through 2 of the 32
     blocks at context 2048 (KV filled with seeded fp16 values; the oracle's time does not
     depend on their values), repeated at successive positions until about budget_s seconds
-    have passed, plus one readout; the mean block time is scaled to the 32-block token."""
+    have passed, plus one readout; the mean block time is scaled to the 32-block token.
+    Reported with the core count, the CPU model, the BLAS thread count and (unless this is
+    the one-thread child) the same sample on one thread."""
     import oracle
     if budget_s is None:
         budget_s = getattr(args, "cpu_budget", 12.0)
@@ -503,10 +541,15 @@ def cpu_baseline(args, budget_s=None):
     st.logits()
     t_head = time.perf_counter() - t0
     per_token = t_blocks / n_tok * model.n_layers / n_blk + t_head
-    return {"value": round(1.0 / per_token, 5), "unit": "tok/s", "cores": cores, "kind": "oracle",
-            "sample": f"{n_tok} decode tokens through {n_blk} of {model.n_layers} blocks at context {CONTEXT}.., "
-                      f"+ one readout; block time scaled x{model.n_layers // n_blk}; "
-                      f"measured {t_blocks + t_head:.1f} s"}
+    res = {"value": round(1.0 / per_token, 5), "unit": "tok/s", "cores": cores, "kind": "oracle",
+           "threads": 1 if one_thread_child else blas_threads(), "cpu_model": cpu_model(),
+           "sample": f"{n_tok} decode tokens through {n_blk} of {model.n_layers} blocks at context {CONTEXT}.., "
+                     f"+ one readout; block time scaled x{model.n_layers // n_blk}; "
+                     f"measured {t_blocks + t_head:.1f} s"}
+    if not one_thread_child:
+        one = cpu_baseline_one_thread(budget_s)
+        res["one_thread"] = {k: one.get(k) for k in ("value", "unit", "threads", "sample", "error") if k in one}
+    return res
 
 
 def run_reference(args):
@@ -538,15 +581,37 @@ def main():
     ap.add_argument("--config", type=int, default=1, choices=sorted(WORKLOADS),
                     help="1: dense 8B-shape, 2: MoE, 4: dense 70B-shape batched decode (64 sequences)")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work in the CPU baseline")
+    ap.add_argument("--no-subrecords", action="store_true",
+                    help="the dense decode line only (without the MoE and 70B-shape batched records)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
-    elif args.config == 4:
-        run_batched(args)
+        return
+    rank, world, _ = dist_env()
+    dist = init_dist(world, "nccl")  # replicas only: the process group carries timing, no data
+    if args.config == 4:
+        line = run_batched(args, dist)
     else:
-        run_gpu(args)
+        line = run_gpu(args, args.config, dist)
+        if args.config == 1 and not (args.layers or args.context or args.no_subrecords):
+            # the other decode workloads, each a record of its own in the same line
+            moe = run_gpu(argparse.Namespace(**{**vars(args), "no_prefill": True}), 2, dist)
+            line["moe_decode"] = {k: moe[k] for k in ("metric", "value", "unit", "ms_per_step", "steps", "warmup",
+                                                      "dtype", "config", "hbm_gbs_achieved", "roofline",
+                                                      "step_roofline", "e2e", "clocks", "gpu_launches")}
+            b70 = run_batched(argparse.Namespace(**{**vars(args), "batched_steps": max(3, args.steps // 4)}), dist)
+            line["batched_70b_decode"] = {k: b70[k] for k in ("metric", "value", "unit", "ms_per_step", "steps",
+                                                              "warmup", "dtype", "config", "hbm_gbs_achieved",
+                                                              "roofline", "step_roofline", "e2e", "clocks",
+                                                              "gpu_launches", "paths")}
+    if rank == 0 and not args.no_cpu_baseline and world == 1 and args.config == 1:
+        line["cpu_baseline"] = cpu_baseline(args)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
 
 
 if __name__ == "__main__":

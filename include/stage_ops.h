@@ -82,7 +82,11 @@ STAGE_API int stage_op_attention_decode(const float* q_dev, const uint16_t* k_ca
  *     resident on every GPU that loads the library until the process exits.  A request
  *     needing more (stage_op_attention_workspace_bytes) fails with STAGE_E_INVALID.
  *   - The first call on a device looks up that device's address of the array (with the
- *     device current); make that first call before any stream capture.
+ *     device current); make that first call before any stream capture.  The address is kept
+ *     for the device's primary context (the one the CUDA runtime uses): it does not follow
+ *     a cudaDeviceReset, after which the library's device code is loaded again, nor a
+ *     driver context other than the primary one made current by the caller -- after either,
+ *     reload the library before calling this entry point again.
  *   - Every call reuses the same array and clears its counters on `stream` before the
  *     kernel.  Calls whose kernels overlap on the GPU (on different streams, or different
  *     host threads) race on the array and give wrong results: serialise them.

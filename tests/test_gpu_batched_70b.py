@@ -5,10 +5,9 @@ Hidden 8192, 64 q / 8 kv heads x 128, SwiGLU 28672, vocab 128256, int8 block-32 
 (the model's depth is reduced to 4 blocks: every block has the same shapes).  The caches
 start from seeded fp16 N(0, 1) rows written through stage_write_kv (and into the oracle's
 caches; every block gets the same rows), then one decode step of 64 tokens -- one per
-sequence, at its own position -- runs through the 4 stages.  The first and the last stage
-are checked against the oracle's block fed the GPU's own input (relative L2 <= 1e-3, the
-float32 tolerance; the last stage's input is the handoff of the two middle stages); the
-readout against the oracle's on
+sequence, at its own position -- runs through the 4 stages.  Every stage is checked against
+the oracle's block fed the GPU's own input to that stage (teacher-forced: relative L2 <= 1e-3,
+the float32 tolerance); the readout against the oracle's on
 sampled vocabulary rows (max-abs <= 2e-2) and the greedy tokens against the oracle's full
 argmax wherever its top-2 margin exceeds that tolerance.
 
@@ -82,8 +81,8 @@ def test_70b_shape_batched_decode_ragged_64(cuda, path):
         for st in stages:
             B.stage_destroy(st)
 
-    # the oracle on the first and the last stage, each fed the GPU's input to that stage
-    for li in (0, 3):
+    # the oracle on every stage, each fed the GPU's input to that stage
+    for li in range(4):
         w = ws[li]
         ost = oracle.Stage(model, li, li + 1, w, max_seqs=NSEQ, max_len=max_len, cache_dequant=False)
         for s in range(NSEQ):

@@ -5,7 +5,9 @@ Both GPU paths compute the same float32 dequant-fused dot products in different 
 orders, so they agree to float32 accumulation error: logits relative L2 <= 1e-5 between
 them; against the oracle the float32 tolerances of the stage tests hold (final features
 relative L2 <= 1e-3, logits max-abs <= 2e-2).  The 8B-width case runs at context 2048 --
-the benchmark's context, with its attention split (19 chunks per KV head on 152 SMs).
+the benchmark's context, with its attention split (19 chunks per KV head on 152 SMs); there
+the decode steps start from the GPU's prompt cache, whose block-0 rows are themselves checked
+against the oracle at sampled positions.
 """
 import os
 
@@ -57,6 +59,21 @@ def decode_run(gp, model, prompt, n_new, chunk=512):
     return toks, logits
 
 
+def check_block0_prompt_kv(model, prompt, k, v):
+    """Block 0's K/V of the prompt on the GPU against the oracle's, at sampled positions.
+    They depend only on each position's token (embedding, RMSNorm, K/V projection, RoPE at
+    the position, fp16 rounding), so the oracle computes just the sampled rows; fp16
+    rounding of the same float32 values: relative L2 <= 1e-3."""
+    n = len(prompt)
+    rng = np.random.default_rng(n)
+    ps = np.unique(np.concatenate([[0, 1, n // 2, n - 1], rng.integers(0, n, 28)]))
+    st = oracle.Stage(model, 0, 1, synth.stage_weights(model, 0, 1, gamma_mode="seeded"), max_seqs=1, max_len=n + 8)
+    st.forward(np.zeros(len(ps)), ps, tokens=prompt[ps])
+    ko, vo = st.k_cache[0, 0][:, ps].astype(np.float64), st.v_cache[0, 0][:, ps].astype(np.float64)
+    kg, vg = k.view(np.float16)[:, ps].astype(np.float64), v.view(np.float16)[:, ps].astype(np.float64)
+    assert rel_l2(kg, ko) <= 1e-3 and rel_l2(vg, vo) <= 1e-3
+
+
 def test_tiny_persistent_equals_per_kernel_path(cuda):
     import layer_range_stage_gb300 as L
     model = synth.CONFIGS[0]
@@ -91,6 +108,7 @@ def test_dense_8b_width_context_2048_matches_oracle(cuda):
     assert toks == res[False][0]
     for a, b in zip(logits, res[False][1]):
         assert rel_l2(a, b) <= 1e-5
+    check_block0_prompt_kv(model, prompt, *kv[0])
     stages = [oracle.Stage(model, a, b, synth.stage_weights(model, a, b, gamma_mode="seeded"), max_seqs=1,
                            max_len=n + 8) for a, b in ((0, 1), (1, 2))]
     for st, (k, v) in zip(stages, kv):
@@ -151,6 +169,7 @@ def test_moe_full_width_context_1024_matches_oracle(cuda, monkeypatch):
             gaps.append(s[model.top_k - 1] - s[model.top_k])
         return real(h, router, *args, **kw)
 
+    check_block0_prompt_kv(model, prompt, *kv[0])
     monkeypatch.setattr(oracle.model, "moe_ffn", spy)
     stages = [oracle.Stage(model, a, b, synth.stage_weights(model, a, b, gamma_mode="seeded"), max_seqs=1,
                            max_len=n + 8) for a, b in ((0, 1), (1, 2))]

@@ -305,3 +305,23 @@ def test_moe_all_experts_equal_logits_is_average():
     assert list(ids[0]) == [0, 1, 2, 3]
     avg = sum(oracle.swiglu(h, *e) for e in ex) / E
     assert np.allclose(out, avg, rtol=1e-12)
+
+
+# ----------------------------------------------------------------------------- greedy readout
+
+def test_greedy_is_the_lowest_index_of_the_maximum():
+    """Brute force over rows full of ties (small integers): the greedy token is the first
+    index holding the row's maximum, also when the tie sits at the ends of the row, and a
+    single maximum wins wherever it is."""
+    rows = RNG.integers(-3, 4, (400, 17)).astype(np.float32)
+    rows[0] = 5.0            # all equal: index 0
+    rows[1, [3, 16]] = 9.0   # a tie with the last index
+    rows[2, [0, 16]] = 9.0   # a tie between the two ends
+    rows[3, 11] = 9.0        # a single maximum
+    want = []
+    for r in rows:
+        m = max(r)
+        want.append(next(i for i, v in enumerate(r) if v == m))
+    got = oracle.greedy(rows)
+    assert got.tolist() == want
+    assert got[0] == 0 and got[1] == 3 and got[2] == 0 and got[3] == 11
