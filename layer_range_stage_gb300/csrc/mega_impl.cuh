@@ -73,7 +73,7 @@ constexpr size_t kOffLogits = kOffMoe, kOffIds = kOffLogits + kMaxExperts * 4, k
                  kOffSel = kOffWts + kMaxTopK * 4, kOffSelId = kOffSel + kMaxTopK * 4,
                  kOffReady = kOffSelId + kMaxTopK * 4;
 constexpr size_t kOffSplit = kOffMoe + (kMaxExperts + 4 * kMaxTopK + 4) * 4;  // [kPhases] Split
-constexpr size_t kOffWptr = kOffSplit + 256;                               // [kMW][2] stream pointers
+constexpr size_t kOffWptr = kOffSplit + 272;                               // [kMW][2] stream pointers
 // the phases of a block's weight stream
 constexpr int kPhQKV = 0, kPhO = 1, kPhRouter = 2, kPhGU = 3, kPhDown = 4, kPhases = 5;
 constexpr int kSeqWord = 63;  // word of the counter block holding the launch sequence
@@ -159,6 +159,7 @@ struct Split {
   int rps;
   int p0, np;  // this CTA's pairs
   int sp;      // slots of a pair
+  int sl;      // columns of a slot (the last of a pair may be shorter), a multiple of 256
   int gs;      // slots of a group: sp, or 1
   int ng;      // this CTA's groups: np * sp / gs
   int dq, dr;  // gs == 1: kMW slots further on is dq pairs and dr slots further on
@@ -266,7 +267,9 @@ __device__ Split split_of(const MegaArgs& a, int ph, int cta, int G) {
   }
   p.p0 = (int)((long long)cta * p.NP / G);
   p.np = (int)((long long)(cta + 1) * p.NP / G) - p.p0;
+  // slots of sl columns: a source piece (mode 2), else kSlotCols
   p.sp = p.mode == 2 ? p.Kp / p.seg : (p.Kp + kSlotCols - 1) / kSlotCols;
+  p.sl = p.mode == 2 ? p.seg : min(kSlotCols, p.Kp);  // the last slot of a pair may be shorter
   // whole pairs per warp unless single slots spread the CTA's slots more evenly
   const int by_pair = (p.np + kMW - 1) / kMW * p.sp, by_slot = (p.np * p.sp + kMW - 1) / kMW;
   p.gs = (by_slot < by_pair && p.np * p.sp <= kMaxCtaPairs) ? 1 : p.sp;
@@ -290,10 +293,8 @@ __device__ __forceinline__ Cur cur_start(const Split& p, int w) {
 __device__ __forceinline__ bool cur_valid(const Split& p, const Cur& q, int w) { return w + kMW * q.m < p.ng; }
 
 // First column and columns of slot j of a pair.
-__device__ __forceinline__ int slot_k(const Split& p, int j) { return j * (p.mode == 2 ? p.seg : kSlotCols); }
-__device__ __forceinline__ int slot_len(const Split& p, int j) {
-  return p.mode == 2 ? p.seg : min(kSlotCols, p.Kp - j * kSlotCols);
-}
+__device__ __forceinline__ int slot_k(const Split& p, int j) { return j * p.sl; }
+__device__ __forceinline__ int slot_len(const Split& p, int j) { return min(p.sl, p.Kp - j * p.sl); }
 
 __device__ __forceinline__ void cur_advance(const Split& p, Cur& q) {
   if (++q.r < p.gs) {  // the next slot of a whole-pair group
@@ -951,35 +952,52 @@ __device__ bool attention_phase(const Ctx& c, int l, unsigned char* area, unsign
         return false;
       }
       ++aphase;
-      // scores: the 16-byte pieces of a K row are walked in a rotated order so that the lanes'
-      // rows fall in distinct banks
-      for (int idx = tid; idx < G * T; idx += kMT) {
-        const int g = idx / T, p = idx - g * T;
+      // scores: four lanes per position, a quarter of the dims each, all G heads of the group at
+      // once (every K element read once); the 16-byte pieces of a quarter are walked in a
+      // rotated order so that the lanes' rows fall in distinct banks; the quarters are added
+      // with two shuffles
+      constexpr int QD = D / 4, QP = QD / 8;
+      for (int idx = tid; idx < 4 * T; idx += kMT) {
+        const int p = idx >> 2, qt = idx & 3;
+        float acc[G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) acc[g] = 0.f;
         if (p < np) {
-          const __half* kr = Ks + (size_t)p * D;
-          const float* qg = qs + g * D;
-          float sc = 0.f;
-#pragma unroll 4
-          for (int i = 0; i < D / 8; ++i) {
-            const int j = (i + p) & (D / 8 - 1);
+          const __half* kr = Ks + (size_t)p * D + qt * QD;
+#pragma unroll 1
+          for (int i = 0; i < QP; ++i) {
+            const int j = (i + p) & (QP - 1);
             const uint4 kk = *reinterpret_cast<const uint4*>(kr + 8 * j);
-            const float4 qa = *reinterpret_cast<const float4*>(qg + 4 * j);
-            const float4 qb = *reinterpret_cast<const float4*>(qg + D / 2 + 4 * j);
             const float2 k01 = __half22float2(*reinterpret_cast<const __half2*>(&kk.x));
             const float2 k23 = __half22float2(*reinterpret_cast<const __half2*>(&kk.y));
             const float2 k45 = __half22float2(*reinterpret_cast<const __half2*>(&kk.z));
             const float2 k67 = __half22float2(*reinterpret_cast<const __half2*>(&kk.w));
-            sc = fmaf(qa.x, k01.x, sc);
-            sc = fmaf(qa.y, k01.y, sc);
-            sc = fmaf(qa.z, k23.x, sc);
-            sc = fmaf(qa.w, k23.y, sc);
-            sc = fmaf(qb.x, k45.x, sc);
-            sc = fmaf(qb.y, k45.y, sc);
-            sc = fmaf(qb.z, k67.x, sc);
-            sc = fmaf(qb.w, k67.y, sc);
+            const int m = qt * QP + j;  // the 8-dim piece of the head's D dims
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+              const float4 qa = *reinterpret_cast<const float4*>(qs + g * D + 4 * m);
+              const float4 qb = *reinterpret_cast<const float4*>(qs + g * D + D / 2 + 4 * m);
+              float sc = acc[g];
+              sc = fmaf(qa.x, k01.x, sc);
+              sc = fmaf(qa.y, k01.y, sc);
+              sc = fmaf(qa.z, k23.x, sc);
+              sc = fmaf(qa.w, k23.y, sc);
+              sc = fmaf(qb.x, k45.x, sc);
+              sc = fmaf(qb.y, k45.y, sc);
+              sc = fmaf(qb.z, k67.x, sc);
+              sc = fmaf(qb.w, k67.y, sc);
+              acc[g] = sc;
+            }
           }
-          S[g * T + p] = sc * a.scale;
         }
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          acc[g] += __shfl_xor_sync(0xffffffffu, acc[g], 1);
+          acc[g] += __shfl_xor_sync(0xffffffffu, acc[g], 2);
+        }
+        if (qt == 0 && p < np)
+#pragma unroll
+          for (int g = 0; g < G; ++g) S[g * T + p] = acc[g] * a.scale;
       }
       __syncthreads();
       if (c.warp < G) {  // warp g: tile max, probabilities, running (max, sum) of head g
