@@ -586,59 +586,34 @@ __device__ void stage_finish(const Ctx& c, int K, int Kp, const float* gamma, fl
     for (int w = 0; w < kMW; ++w) tot += c.red()[w];
     rinv = 1.0f / sqrtf(tot / (float)K + eps);
   }
-  for (int ch = tid; ch < nchunk; ch += kMT) {
-    float h[16];
+  // two lanes per chunk (2 nchunk is a multiple of 32: whole warps); each lane reads its eight
+  // inputs before the pair's first shuffle and writes after it, so the in-place form is safe
+  for (int t = tid; t < 2 * nchunk; t += kMT) {
+    const int ch = t >> 1, half = t & 1;
+    float h[8];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float4 v = reinterpret_cast<const float4*>(raw)[ch * 4 + j];
+    for (int j = 0; j < 2; ++j) {
+      const float4 v = reinterpret_cast<const float4*>(raw)[ch * 4 + half * 2 + j];
       h[4 * j] = v.x;
       h[4 * j + 1] = v.y;
       h[4 * j + 2] = v.z;
       h[4 * j + 3] = v.w;
       if (gamma) {
-        const float4 g = reinterpret_cast<const float4*>(xs)[ch * 4 + j];
+        const float4 g = reinterpret_cast<const float4*>(xs)[ch * 4 + half * 2 + j];
         h[4 * j] = h[4 * j] * rinv * g.x;
         h[4 * j + 1] = h[4 * j + 1] * rinv * g.y;
         h[4 * j + 2] = h[4 * j + 2] * rinv * g.z;
         h[4 * j + 3] = h[4 * j + 3] * rinv * g.w;
       }
     }
-    uint4 q[4];
-    q8_chunk_encode(h, q[0], q[1], q[2], q[3]);
+    uint2 q[4];
+    q8_chunk_encode2(h, half, q[0], q[1], q[2], q[3]);
     const int sw = (ch >> 1) & 3;  // the chunk's four 16-byte pieces, swizzled: lanes reading
-    uint4* xp = reinterpret_cast<uint4*>(xs + ch * 16);  // consecutive chunks hit distinct banks
+    uint2* xp = reinterpret_cast<uint2*>(xs + ch * 16);  // consecutive chunks hit distinct banks
 #pragma unroll
-    for (int j = 0; j < 4; ++j) xp[j ^ sw] = q[j];
+    for (int j = 0; j < 4; ++j) xp[2 * (j ^ sw) + half] = q[j];
   }
   __syncthreads();
-}
-
-// Both rows of a 16-weight chunk against one 16-float chunk of the staged input: the sums
-// b_j x'_j 2^-149 of q8dot.cuh, each over two independent pairs of packed products (depth 4).
-__device__ __forceinline__ void dot16x2(const uint4 wa, const uint4 wb, const float4 x0, const float4 x1,
-                                        const float4 x2, const float4 x3, float& da, float& db) {
-  const float2 xa0 = make_float2(x0.x, x0.y), xb0 = make_float2(x0.z, x0.w);
-  const float2 xa1 = make_float2(x1.x, x1.y), xb1 = make_float2(x1.z, x1.w);
-  const float2 xa2 = make_float2(x2.x, x2.y), xb2 = make_float2(x2.z, x2.w);
-  const float2 xa3 = make_float2(x3.x, x3.y), xb3 = make_float2(x3.z, x3.w);
-  float2 a0 = __fmul2_rn(make_float2(q8_b0(wa.x), q8_b1(wa.x)), xa0);
-  float2 a1 = __fmul2_rn(make_float2(q8_b2(wa.x), q8_b3(wa.x)), xb0);
-  float2 b0 = __fmul2_rn(make_float2(q8_b0(wb.x), q8_b1(wb.x)), xa0);
-  float2 b1 = __fmul2_rn(make_float2(q8_b2(wb.x), q8_b3(wb.x)), xb0);
-  a0 = __ffma2_rn(make_float2(q8_b0(wa.y), q8_b1(wa.y)), xa1, a0);
-  a1 = __ffma2_rn(make_float2(q8_b2(wa.y), q8_b3(wa.y)), xb1, a1);
-  b0 = __ffma2_rn(make_float2(q8_b0(wb.y), q8_b1(wb.y)), xa1, b0);
-  b1 = __ffma2_rn(make_float2(q8_b2(wb.y), q8_b3(wb.y)), xb1, b1);
-  a0 = __ffma2_rn(make_float2(q8_b0(wa.z), q8_b1(wa.z)), xa2, a0);
-  a1 = __ffma2_rn(make_float2(q8_b2(wa.z), q8_b3(wa.z)), xb2, a1);
-  b0 = __ffma2_rn(make_float2(q8_b0(wb.z), q8_b1(wb.z)), xa2, b0);
-  b1 = __ffma2_rn(make_float2(q8_b2(wb.z), q8_b3(wb.z)), xb2, b1);
-  a0 = __ffma2_rn(make_float2(q8_b0(wa.w), q8_b1(wa.w)), xa3, a0);
-  a1 = __ffma2_rn(make_float2(q8_b2(wa.w), q8_b3(wa.w)), xb3, a1);
-  b0 = __ffma2_rn(make_float2(q8_b0(wb.w), q8_b1(wb.w)), xa3, b0);
-  b1 = __ffma2_rn(make_float2(q8_b2(wb.w), q8_b3(wb.w)), xb3, b1);
-  da = (a0.x + a0.y) + (a1.x + a1.y);
-  db = (b0.x + b0.y) + (b1.x + b1.y);
 }
 
 // The epilogue of pair i (CTA-local) of projection ph of block l, from its row sums.

@@ -68,37 +68,46 @@ __device__ __forceinline__ int dp4a_us(unsigned a, unsigned b, int c) {
   return d;
 }
 
-// The limbs (l0, l1, l2: byte j of word j / 4 is input j's) and k = (the three dp4a starting
-// values, bits of u) of a chunk of 16 inputs.
-__device__ __forceinline__ void q8_chunk_encode(const float h[16], uint4& l0, uint4& l1, uint4& l2, uint4& k) {
+// The chunk form of 16 inputs: limbs l0, l1, l2 (byte j of word j / 4 is input j's) and
+// k = (the three dp4a starting values, bits of u), computed by two adjacent lanes
+// (half = lane & 1), each holding inputs 8 half .. 8 half + 7 of the chunk in h: words 2 half
+// and 2 half + 1 of l0, l1, l2 and of k come back in (lw0, lw1, lw2, kw).  Both lanes must
+// call it together.  The three limbs of N_j are the bytes of N_j + 0x808080 (each limb plus
+// 128: a base-256 representation with digits in [0, 255], and below 2^24 since
+// |N_j| < 2^23), so they are picked out by byte permutes and their bias removed by one XOR per
+// word; the limb sums are dp4a against ones.
+__device__ __forceinline__ void q8_chunk_encode2(const float h[8], int half, uint2& lw0, uint2& lw1, uint2& lw2,
+                                                 uint2& kw) {
   float m = 0.f;
 #pragma unroll
-  for (int j = 0; j < 16; ++j) m = fmaxf(m, fabsf(h[j]));
-  // m = f 2^e with f in [0.5, 1); chunks below 2^-100 keep e = -100 (their integers are 0)
+  for (int j = 0; j < 8; ++j) m = fmaxf(m, fabsf(h[j]));
+  m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
   const int e = max((int)((__float_as_uint(m) >> 23) & 0xFFu) - 126, -100);
-  const float sc = __int_as_float((unsigned)(127 + 23 - e) << 23) * 0.9921875f;  // 1 / u = (127/128) 2^(23 - e)
-  unsigned w0[4] = {0u, 0u, 0u, 0u}, w1[4] = {0u, 0u, 0u, 0u}, w2[4] = {0u, 0u, 0u, 0u};
-  int s0 = 0, s1 = 0, s2 = 0;
+  const float sc = __int_as_float((unsigned)(127 + 23 - e) << 23) * 0.9921875f;
+  unsigned w[3][2];
 #pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    const int n = __float2int_rn(h[j] * sc);
-    const int b2 = ((n + 128) & 255) - 128;
-    const int n1 = (n - b2) >> 8;
-    const int b1 = ((n1 + 128) & 255) - 128;
-    const int b0 = (n1 - b1) >> 8;
-    s0 += b0;
-    s1 += b1;
-    s2 += b2;
-    w0[j >> 2] |= ((unsigned)b0 & 0xFFu) << (8 * (j & 3));
-    w1[j >> 2] |= ((unsigned)b1 & 0xFFu) << (8 * (j & 3));
-    w2[j >> 2] |= ((unsigned)b2 & 0xFFu) << (8 * (j & 3));
+  for (int q = 0; q < 2; ++q) {
+    unsigned v[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) v[j] = (unsigned)(__float2int_rn(h[4 * q + j] * sc) + 0x808080);
+    const unsigned ablo = __byte_perm(v[0], v[1], 0x5140), abhi = __byte_perm(v[0], v[1], 0x7362);
+    const unsigned cdlo = __byte_perm(v[2], v[3], 0x5140), cdhi = __byte_perm(v[2], v[3], 0x7362);
+    w[0][q] = __byte_perm(abhi, cdhi, 0x5410) ^ 0x80808080u;  // byte 2: l0
+    w[1][q] = __byte_perm(ablo, cdlo, 0x7632) ^ 0x80808080u;  // byte 1: l1
+    w[2][q] = __byte_perm(ablo, cdlo, 0x5410) ^ 0x80808080u;  // byte 0: l2
   }
-  l0 = make_uint4(w0[0], w0[1], w0[2], w0[3]);
-  l1 = make_uint4(w1[0], w1[1], w1[2], w1[3]);
-  l2 = make_uint4(w2[0], w2[1], w2[2], w2[3]);
-  k = make_uint4((unsigned)(0x4B400000 - 128 * s0), (unsigned)(0x4B400000 - 128 * s1),
-                 (unsigned)(0x4B400000 - 128 * s2),
-                 __float_as_uint(__int_as_float((unsigned)(127 + e - 23) << 23) * (128.0f / 127.0f)));
+  int s[3];
+#pragma unroll
+  for (int i = 0; i < 3; ++i) {
+    s[i] = __dp4a((int)w[i][1], 0x01010101, __dp4a((int)w[i][0], 0x01010101, 0));
+    s[i] += __shfl_xor_sync(0xffffffffu, s[i], 1);
+  }
+  lw0 = make_uint2(w[0][0], w[0][1]);
+  lw1 = make_uint2(w[1][0], w[1][1]);
+  lw2 = make_uint2(w[2][0], w[2][1]);
+  const unsigned unit = __float_as_uint(__int_as_float((unsigned)(127 + e - 23) << 23) * (128.0f / 127.0f));
+  kw = half ? make_uint2((unsigned)(0x4B400000 - 128 * s[2]), unit)
+            : make_uint2((unsigned)(0x4B400000 - 128 * s[0]), (unsigned)(0x4B400000 - 128 * s[1]));
 }
 
 // 2^16 D0 + 2^8 D1 + D2 (see above) for the 16 biased weight bytes of w.
