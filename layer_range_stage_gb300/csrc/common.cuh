@@ -106,6 +106,16 @@ __device__ __forceinline__ void prefetch_l2_last(const void* p) {
   asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(p));
 }
 
+// Tile (x, y) of a two-dimensional tensor map (x in elements: x times the element size must be
+// a multiple of 16 bytes) into shared memory, completing on an mbarrier.
+__device__ __forceinline__ void tma_load_2d(void* dst, const void* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
+          "r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // Orders this thread's generic-proxy shared-memory accesses before its later async-proxy
 // ones (bulk copies, tensor-core operand reads).
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }

@@ -1,6 +1,7 @@
 // Launch interface of the stage kernels (host side).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -124,7 +125,16 @@ struct MegaLayer {
   const float* ffn_norm = nullptr;
   __half* kc = nullptr;  // [max_seqs][Hkv][max_len][D] of this block
   __half* vc = nullptr;
+  // Per projection step (QKV, O, router, gate/up, down): the tensor maps of its weight bytes and
+  // of its scales, each a box of two rows (a pair) by one ring slot of columns (mega_tensor_maps).
+  alignas(64) CUtensorMap tmap[2 * 5];
 };
+// Fills ml.tmap from the matrices of ml (MoE stages: n_experts > 0).  False if a matrix cannot
+// be described (unaligned base).
+bool mega_tensor_maps(MegaLayer& ml, bool moe);
+// A two-dimensional tiled tensor map (no interleave, L2 promotion of 256 bytes, zero fill).
+bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
+               uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw);
 struct MegaArgs {
   const MegaLayer* layers = nullptr;  // device [nl]
   int nl = 0;

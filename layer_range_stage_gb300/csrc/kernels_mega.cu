@@ -1,6 +1,8 @@
 // Persistent decode: the dense kernels and the host entry points (the kernel itself is in
 // mega_impl.cuh).
 
+#include <cstring>
+
 #include "mega_impl.cuh"
 
 namespace lrs {
@@ -29,6 +31,26 @@ bool mega_supported(int H, int q_dim, int F, int head_dim, int group, int n_expe
     if ((r / 2 + G - 1) / G > kMaxCtaPairs) return false;
   if (n_experts > 0 && F / top_k > kSlotCols) return false;  // an expert's down piece fits a slot
   return mega_smem(H, q_dim, F, head_dim, group) <= kMaxSmem;
+}
+
+bool mega_tensor_maps(MegaLayer& ml, bool moe) {
+  std::memset(static_cast<void*>(ml.tmap), 0, sizeof ml.tmap);
+  const DevQ8* m[kPhases] = {&ml.wqkv, &ml.wo, moe ? &ml.router : nullptr, moe ? &ml.egu : &ml.wgu,
+                             moe ? &ml.edown : &ml.wdown};
+  for (int ph = 0; ph < kPhases; ++ph) {
+    if (!m[ph] || !m[ph]->q || m[ph]->N <= 0) continue;
+    const DevQ8& w = *m[ph];
+    // a ring slot of two rows (the last slot of a row may reach past Kp: zero filled); the
+    // bytes and the fp16 scales as 8-byte elements
+    const int sl = std::min(kSlotCols, w.Kp);
+    if (w.Kp % 256 || ((uintptr_t)w.q & 15) || ((uintptr_t)w.s & 15)) return false;
+    if (!encode_2d(&ml.tmap[2 * ph], CU_TENSOR_MAP_DATA_TYPE_UINT64, w.q, (uint64_t)w.Kp / 8, (uint64_t)w.N,
+                   (uint64_t)w.Kp, (uint32_t)sl / 8, 2, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_2d(&ml.tmap[2 * ph + 1], CU_TENSOR_MAP_DATA_TYPE_UINT64, w.s, (uint64_t)w.Kp / 128, (uint64_t)w.N,
+                   (uint64_t)w.Kp / 16, (uint32_t)sl / 128, 2, CU_TENSOR_MAP_SWIZZLE_NONE))
+      return false;
+  }
+  return true;
 }
 
 size_t mega_tag_entries(int H, int q_dim, int kv_dim, int n_experts) {

@@ -225,8 +225,8 @@ struct Ctx {
     return reinterpret_cast<volatile int*>(sm + kOffReady);
   }
   __device__ const Split* split() const { return reinterpret_cast<const Split*>(sm + kOffSplit); }  // [kPhases]
-  // [kMW][2] weights and scales of each warp's stream cursor (l, ph): an issue reads them
-  // here, not from the block descriptor
+  // [kMW][2] tensor maps (weights, scales) of each warp's stream cursor (l, ph): an issue reads
+  // them here, not from the block descriptor
   __device__ const void** wptr() const { return reinterpret_cast<const void**>(sm + kOffWptr); }
 };
 
@@ -317,26 +317,18 @@ __device__ __forceinline__ void cur_advance(const Split& p, Cur& q) {
 }
 
 // Global addresses of rows (2P, 2P + 1) of a projection at column k (P phase-global).
+// Row (the pair's first) and first column of slot j of pair P in the matrix of projection p
+// (MoE: the stacked experts' rows).
 template <bool MOE>
-__device__ __forceinline__ void pair_src(const Ctx& c, const Split& p, const uint8_t* wq, const uint16_t* ws, int P,
-                                         int j, const uint8_t*& q, const uint16_t*& sc, size_t& qstride,
-                                         size_t& sstride) {
-  const int k = slot_k(p, j);
+__device__ __forceinline__ void pair_rc(const Ctx& c, const Split& p, int P, int j, int& r, int& k) {
   if (MOE && p.mode == 2) {  // K gathered: slot j is the row's piece from selected expert j
-    const int kk = 0;
-    const size_t r = (size_t)c.moe_ids()[j] * (size_t)(2 * p.NP) + 2 * P;
-    q = wq + r * p.seg + kk;
-    sc = ws + r * (p.seg / 32) + kk / 32;
-    qstride = p.seg;
-    sstride = p.seg / 32;
+    r = c.moe_ids()[j] * (2 * p.NP) + 2 * P;
+    k = 0;
     return;
   }
-  size_t r = 2 * (size_t)P;
-  if (MOE && p.mode == 1) r = (size_t)c.moe_ids()[2 * P / p.rps] * p.rps + (2 * P) % p.rps;
-  q = wq + r * p.Kp + k;
-  sc = ws + r * (p.Kp / 32) + k / 32;
-  qstride = p.Kp;
-  sstride = p.Kp / 32;
+  r = 2 * P;
+  if (MOE && p.mode == 1) r = c.moe_ids()[2 * P / p.rps] * p.rps + (2 * P) % p.rps;
+  k = slot_k(p, j);
 }
 
 // Move a cursor to the first projection at or after (l, ph) in which this warp holds slots.
@@ -352,16 +344,16 @@ __device__ __forceinline__ void stream_normalise(const Ctx& c, Stream& s) {
     moved = true;
   }
   if (moved && s.l < c.a->nl && c.lane == 0) {
-    const DevQ8& w = phase_w<MOE>(c.a->layers[s.l], s.ph);
-    c.wptr()[2 * c.warp] = w.q;
-    c.wptr()[2 * c.warp + 1] = w.s;
+    c.wptr()[2 * c.warp] = &c.a->layers[s.l].tmap[2 * s.ph];
+    c.wptr()[2 * c.warp + 1] = &c.a->layers[s.l].tmap[2 * s.ph + 1];
   }
   __syncwarp();
 }
 
 // Issue the next slot of this warp's stream (if any) into the ring: slot j of pair pr, row 2P's
-// bytes at the start of the ring slot and row 2P + 1's at kSlotCols.  Slices of the selected
-// experts wait until the routing of their block is known.
+// bytes at the start of the ring slot and row 2P + 1's sl bytes further on (two tensor-map
+// boxes: bytes and scales).  Slices of the selected experts wait until the routing of their
+// block is known.
 template <bool MOE>
 __device__ __forceinline__ void stream_issue(const Ctx& c, Stream& s) {
   if (s.l >= c.a->nl) return;
@@ -369,21 +361,17 @@ __device__ __forceinline__ void stream_issue(const Ctx& c, Stream& s) {
   const Split& p = c.split()[s.ph];
   const int slot = s.issued % kDepth;
   if (c.lane == 0) {
-    const int len = slot_len(p, s.q.j);
-    const uint8_t* q;
-    const uint16_t* sc;
-    size_t qst, sst;
-    pair_src<MOE>(c, p, static_cast<const uint8_t*>(c.wptr()[2 * c.warp]),
-                  static_cast<const uint16_t*>(c.wptr()[2 * c.warp + 1]), p.p0 + s.q.pr, s.q.j, q, sc, qst, sst);
+    int r, k;
+    pair_rc<MOE>(c, p, p.p0 + s.q.pr, s.q.j, r, k);
     uint64_t* bar = c.bars() + c.warp * kDepth + slot;
     unsigned char* dq = c.ringq() + (size_t)(c.warp * kDepth + slot) * kSlotQ;
     unsigned char* ds = c.rings() + (size_t)(c.warp * kDepth + slot) * kSlotS;
     fence_async_smem();  // the slot's previous contents were read through the generic proxy
-    mbar_arrive_expect_tx(bar, (uint32_t)(2 * (len + len / 16)));
-    bulk_g2s(dq, q, (uint32_t)len, bar);
-    bulk_g2s(dq + kSlotCols, q + qst, (uint32_t)len, bar);
-    bulk_g2s(ds, sc, (uint32_t)(len / 16), bar);
-    bulk_g2s(ds + kSlotCols / 16, sc + sst, (uint32_t)(len / 16), bar);
+    // one box of the pair's two rows for the bytes and one for the scales (8-byte elements): row
+    // 2P + 1 lands sl bytes (sl / 16 scale bytes) after row 2P; columns past Kp read as zero
+    mbar_arrive_expect_tx(bar, (uint32_t)(2 * (p.sl + p.sl / 16)));
+    tma_load_2d(dq, c.wptr()[2 * c.warp], k >> 3, r, bar);
+    tma_load_2d(ds, c.wptr()[2 * c.warp + 1], k >> 7, r, bar);
   }
   ++s.issued;
   cur_advance(p, s.q);
@@ -756,9 +744,9 @@ __device__ bool gemv_phase(const Ctx& c, Stream& s, int l, int ph, const float* 
       const int cl = c.lane + 32 * u;
       if (cl < nch) {
         wa[u] = *reinterpret_cast<const uint4*>(sq + cl * 16);
-        wb[u] = *reinterpret_cast<const uint4*>(sq + kSlotCols + cl * 16);
+        wb[u] = *reinterpret_cast<const uint4*>(sq + p.sl + cl * 16);
         sab[u] = (uint32_t)*reinterpret_cast<const uint16_t*>(ss + (cl >> 1) * 2) |
-                 ((uint32_t)*reinterpret_cast<const uint16_t*>(ss + kSlotCols / 16 + (cl >> 1) * 2) << 16);
+                 ((uint32_t)*reinterpret_cast<const uint16_t*>(ss + p.sl / 16 + (cl >> 1) * 2) << 16);
       }
     }
     __syncwarp();  // the slot is read: refill it
@@ -1152,9 +1140,8 @@ __global__ void __launch_bounds__(kMT, 1) mega_decode_kernel(const MegaArgs a) {
   s.issued = 0;
   s.consumed = 0;
   if (c.lane == 0 && a.nl > 0) {
-    const DevQ8& w0 = phase_w<MOE>(a.layers[0], 0);
-    c.wptr()[2 * c.warp] = w0.q;
-    c.wptr()[2 * c.warp + 1] = w0.s;
+    c.wptr()[2 * c.warp] = &a.layers[0].tmap[0];
+    c.wptr()[2 * c.warp + 1] = &a.layers[0].tmap[1];
   }
   __syncwarp();
   if (!cur_valid(splits[0], s.q, c.warp)) stream_normalise<MOE>(c, s);

@@ -326,6 +326,8 @@ int upload_descriptor(stage* st, int gl, const LayerDev& L) {
   ml.ffn_norm = L.ffn_norm;
   ml.kc = st->kc + (size_t)(gl - st->begin) * st->layer_kv;
   ml.vc = st->vc + (size_t)(gl - st->begin) * st->layer_kv;
+  if (!lrs::mega_tensor_maps(ml, st->cfg.n_experts > 0))
+    return set_err(st, STAGE_E_CUDA, "block %d: tensor maps of the persistent decode", gl);
   const cudaError_t ce = cudaMemcpy(st->mlayers + (gl - st->begin), &ml, sizeof ml, cudaMemcpyHostToDevice);
   return ce == cudaSuccess ? STAGE_OK : cuda_err(st, ce, "block descriptor");
 }
