@@ -104,13 +104,26 @@ struct GemmArgs {
   const float2* rope = nullptr;
   int n_q_heads = 0, n_kv_heads = 0, head_dim = 0, max_len = 0;
   int* err = nullptr;
+  // Calls of at most kGemmSmallTokens tokens (gemm_small_splits): the K-split partials
+  // [splits][kGemmSmallTokens][N] f32 and one arrival counter per 128-row weight tile (zero
+  // between launches: the last CTA of a tile re-zeroes its counter).  Without them the K range
+  // is not split.
+  float* ws = nullptr;
+  unsigned* tile_cnt = nullptr;
 };
 cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t st);
+// The weight-streaming GEMM of small calls: at most this many tokens, weight tiles of 128 rows.
+constexpr int kGemmSmallTokens = 64;
+constexpr int kGemmSmallRows = 128;
+// K splits of a small call's GEMM of an N x Kp matrix (1 when the weight tiles alone fill the
+// SMs), and the workspace its split needs (0 without a split).
+int gemm_small_splits(int N, int Kp);
+size_t gemm_small_ws_bytes(int N, int Kp);
 cudaError_t prepare_gemm_tc();
 // RMSNorm (gamma != nullptr) or plain copy of f32 rows [ntok][ld_in] to bf16 rows [ntok][ld_out],
-// zero-filled from K to ld_out.
+// zero-filled from K to ld_out; with `rows`, output row t is input row rows[t].
 cudaError_t launch_rows_to_bf16(const float* x, int ld_in, int K, const float* gamma, float eps, int ntok,
-                                __nv_bfloat16* out, int ld_out, cudaStream_t st);
+                                __nv_bfloat16* out, int ld_out, cudaStream_t st, const int* rows = nullptr);
 
 // Persistent decode of a dense stage: every block of the stage for one token in one
 // cooperative launch (one CTA per SM).  Per block, five phases separated by grid barriers:
@@ -127,7 +140,7 @@ struct MegaLayer {
   __half* vc = nullptr;
   // Per projection step (QKV, O, router, gate/up, down): the tensor maps of its weight bytes and
   // of its scales, each a box of two rows (a pair) by one ring slot of columns (mega_tensor_maps).
-  alignas(64) CUtensorMap tmap[2 * 5];
+  CUtensorMap tmap[2 * 5];
 };
 // Fills ml.tmap from the matrices of ml (MoE stages: n_experts > 0).  False if a matrix cannot
 // be described (unaligned base).

@@ -315,9 +315,317 @@ __global__ void __launch_bounds__(kGThreads, 1)
   if (warp == 0) tmem_dealloc(tmem, kGTmemCols);
 }
 
+// ------------------------------------------------------------------------------------------
+// The GEMM of a call of at most kGemmSmallTokens tokens (batched decode, and the readout of
+// such a call).  Every weight is read once, so the operands are swapped: A = 128 dequantised
+// weight rows (the MMA's M), B = the tokens' activations (N = 64, zero beyond M); D[row][token]
+// sits in 64 TMEM columns.  The K range of a weight tile may be split over `splits` CTAs (the
+// grid's y), so that projections with few weight tiles still cover the SMs: each writes its
+// f32 partial to the workspace, and the last CTA of the tile to arrive adds the partials in
+// split order and runs the epilogue (one summation order whatever the arrival order).  Roles
+// as in gemm_tc_kernel, with two dequantising threads per weight row (32 of K each).
+constexpr int kSN = kGemmSmallRows, kST = kGemmSmallTokens, kSK = 64;
+constexpr int kSSA = 4;  // activation stages
+constexpr int kSSR = 4;  // raw weight stages of 256 columns (one scale group): 256-byte row runs
+constexpr int kSSB = 3;  // dequantised weight buffers of one K step
+constexpr uint32_t kSTileW = kSN * kSK * 2;  // 16 KB bf16 weights, 128B-swizzled K-major
+constexpr uint32_t kSTileA = kST * kSK * 2;  // 8 KB bf16 activations, 128B-swizzled K-major
+constexpr uint32_t kSRawBox = kSN * 128;     // 16 KB int8: 128 columns of the tile's rows, 128B-swizzled
+constexpr uint32_t kSRawW = 2 * kSRawBox;    // a raw stage: 256 columns
+constexpr uint32_t kSRawS = kSN * 16;        // its 8 fp16 scales per row
+constexpr uint32_t kSOffW = 0;                             // dequantised weight buffers
+constexpr uint32_t kSOffA = kSOffW + kSSB * kSTileW;       // activation stages
+constexpr uint32_t kSOffRW = kSOffA + kSSA * kSTileA;      // raw weight stages
+constexpr uint32_t kSOffRS = kSOffRW + kSSR * kSRawW;      // the raw stages' scales
+constexpr uint32_t kSOffBar = kSOffRS + kSSR * kSRawS;
+constexpr uint32_t kSSmem = kSOffBar + 512 + 1024;         // + barriers, tmem slot, flags, alignment slack
+constexpr uint32_t kSTmemCols = 64;
+
+struct SBars {
+  uint64_t a_full[kSSA], a_empty[kSSA], r_full[kSSR], r_empty[kSSR];
+  uint64_t b_full[kSSB], b_empty[kSSB], acc_full, mma_drain;
+};
+
+__global__ void __launch_bounds__(kGThreads, 1)
+    gemm_small_kernel(const GemmArgs a, const __grid_constant__ CUtensorMap tA, const __grid_constant__ CUtensorMap tW,
+                      const __grid_constant__ CUtensorMap tS, int splits) {
+  extern __shared__ unsigned char g_raw[];
+  unsigned char* sm = reinterpret_cast<unsigned char*>(((uintptr_t)g_raw + 1023) & ~(uintptr_t)1023);
+  SBars* B = reinterpret_cast<SBars*>(sm + kSOffBar);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kSOffBar + sizeof(SBars));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kSOffBar + sizeof(SBars) + 8);
+  volatile int* last_flag = abort_flag + 1;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int n0 = blockIdx.x * kSN, split = blockIdx.y;
+  const int N = a.w.N, M = a.M;
+  // this CTA's K steps: whole scale groups (4 steps of 64) of its split
+  const int ng = a.w.Kp / 256;
+  const int kt0 = 4 * (int)((long long)split * ng / splits), kt1 = 4 * (int)((long long)(split + 1) * ng / splits);
+  const int nk = kt1 - kt0;
+
+  if (tid == 0) {
+    for (int i = 0; i < kSSA; ++i) {
+      mbar_init(&B->a_full[i], 1);
+      mbar_init(&B->a_empty[i], 1);
+    }
+    for (int i = 0; i < kSSR; ++i) {
+      mbar_init(&B->r_full[i], 1);
+      mbar_init(&B->r_empty[i], kGDeq);
+    }
+    for (int i = 0; i < kSSB; ++i) {
+      mbar_init(&B->b_full[i], kGDeq);
+      mbar_init(&B->b_empty[i], 1);
+    }
+    mbar_init(&B->acc_full, 1);
+    mbar_init(&B->mma_drain, 1);
+    *abort_flag = 0;
+    *last_flag = 0;
+    mbar_fence_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, kSTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  pdl_trigger();
+
+  if (warp == 8) {
+    // ---------------- activation loads (the call's tokens, zero beyond M) ----------------
+    if (lane == 0) {
+      int ia = 0;
+      pdl_wait();  // the activations are the previous kernel's output
+      for (int i = 0; i < nk; ++i) {
+        const int s = i % kSSA;
+        if (i >= kSSA && !gwait(&B->a_empty[s], (uint32_t)((i / kSSA) + 1) & 1u, abort_flag, a.err)) break;
+        mbar_arrive_expect_tx(&B->a_full[s], kSTileA);
+        tma_load_2d(sm + kSOffA + s * kSTileA, &tA, (kt0 + i) * kSK, 0, &B->a_full[s]);
+        ++ia;
+      }
+      if (*abort_flag)  // nothing may still be landing in shared memory when the CTA leaves
+        for (int k = max(0, ia - kSSA); k < ia; ++k)
+          mbar_wait(&B->a_full[k % kSSA], (uint32_t)(k / kSSA) & 1u, kGDrainNs);
+    }
+  } else if (warp == 10) {
+    // ---------------- weight loads: a raw stage is 256 columns (two swizzled boxes) and their scales ----------------
+    if (lane == 0) {
+      int ir = 0;
+      for (int g = 0; g < nk / 4; ++g) {
+        const int r = g % kSSR, kc = (kt0 >> 2) + g;  // the scale group
+        if (g >= kSSR && !gwait(&B->r_empty[r], (uint32_t)((g / kSSR) + 1) & 1u, abort_flag, a.err)) break;
+        mbar_arrive_expect_tx(&B->r_full[r], kSRawW + kSRawS);
+        unsigned char* rw = sm + kSOffRW + r * kSRawW;
+        tma_load_2d(rw, &tW, kc * 256, n0, &B->r_full[r]);
+        tma_load_2d(rw + kSRawBox, &tW, kc * 256 + 128, n0, &B->r_full[r]);
+        tma_load_2d(sm + kSOffRS + r * kSRawS, &tS, kc * 8, n0, &B->r_full[r]);
+        ++ir;
+      }
+      if (*abort_flag)
+        for (int k = max(0, ir - kSSR); k < ir; ++k)
+          mbar_wait(&B->r_full[k % kSSR], (uint32_t)(k / kSSR) & 1u, kGDrainNs);
+    }
+  } else if (warp < 8) {
+    // ---------------- dequantise: half `hf` (32 of K) of weight row `row` of every tile ----------------
+    const int row = tid >> 1, hf = tid & 1;
+    constexpr float kBias = 8388736.0f;  // 2^23 + 128 (see gemm_tc_kernel)
+    bool go = true;
+    for (int g = 0; g < nk / 4 && go; ++g) {
+      const int r = g % kSSR;
+      if (!gwait(&B->r_full[r], (uint32_t)(g / kSSR) & 1u, abort_flag, a.err)) break;
+      const unsigned char* rw = sm + kSOffRW + r * kSRawW;
+      const unsigned char* rs = sm + kSOffRS + r * kSRawS;
+      for (int u = 0; u < 4; ++u) {  // the K steps of the stage
+        const int i = 4 * g + u, bb = i % kSSB;
+        if (i >= kSSB && !gwait(&B->b_empty[bb], (uint32_t)((i / kSSB) + 1) & 1u, abort_flag, a.err)) {
+          go = false;
+          break;
+        }
+        unsigned char* wt = sm + kSOffW + bb * kSTileW;
+        const float sc =
+            __half2float(__ushort_as_half(*reinterpret_cast<const uint16_t*>(rs + row * 16 + (2 * u + hf) * 2)));
+        const unsigned char* rb = rw + (u >> 1) * kSRawBox + row * 128;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const int c = (u & 1) * 4 + hf * 2 + j;  // the 16-byte chunk of the box row (swizzled by row)
+          const uint4 w = *reinterpret_cast<const uint4*>(rb + ((c ^ (row & 7)) << 4));
+          const uint32_t wd[4] = {w.x, w.y, w.z, w.w};
+          uint32_t o[8];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {  // two weights per packed subtract and multiply (exact, as above)
+            const uint32_t x = wd[q];
+            const float2 lo = __fmul2_rn(__fadd2_rn(make_float2(__uint_as_float(__byte_perm(x, 0x4B000000u, 0x7440)),
+                                                               __uint_as_float(__byte_perm(x, 0x4B000000u, 0x7441))),
+                                                   make_float2(-kBias, -kBias)),
+                                        make_float2(sc, sc));
+            const float2 hi = __fmul2_rn(__fadd2_rn(make_float2(__uint_as_float(__byte_perm(x, 0x4B000000u, 0x7442)),
+                                                               __uint_as_float(__byte_perm(x, 0x4B000000u, 0x7443))),
+                                                   make_float2(-kBias, -kBias)),
+                                        make_float2(sc, sc));
+            o[2 * q] = pack_bf16x2(lo.x, lo.y);
+            o[2 * q + 1] = pack_bf16x2(hi.x, hi.y);
+          }
+          const int col = hf * 32 + j * 16;
+          *reinterpret_cast<uint4*>(wt + sw128_offset(row, col)) = make_uint4(o[0], o[1], o[2], o[3]);
+          *reinterpret_cast<uint4*>(wt + sw128_offset(row, col + 8)) = make_uint4(o[4], o[5], o[6], o[7]);
+        }
+        fence_async_smem();  // the bf16 tile is read next by the tensor core (async proxy)
+        mbar_arrive(&B->b_full[bb]);
+      }
+      if (go) mbar_arrive(&B->r_empty[r]);
+    }
+  } else if (warp == 9) {
+    // ---------------- MMA issue: D[128 rows][64 tokens] += W_tile * A_tile^T ----------------
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(kSN, kST);
+      int issued = 0;
+      for (int i = 0; i < nk; ++i) {
+        const int s = i % kSSA, bb = i % kSSB;
+        if (!gwait(&B->a_full[s], (uint32_t)(i / kSSA) & 1u, abort_flag, a.err)) break;
+        if (!gwait(&B->b_full[bb], (uint32_t)(i / kSSB) & 1u, abort_flag, a.err)) break;
+        tc_fence_after();
+        const uint32_t w_base = smem_u32(sm + kSOffW + bb * kSTileW);
+        const uint32_t a_base = smem_u32(sm + kSOffA + s * kSTileA);
+#pragma unroll
+        for (int kk = 0; kk < kSK / 16; ++kk)
+          umma_bf16(tmem, desc_sw128(w_base + kk * 32), desc_sw128(a_base + kk * 32), idesc, (i > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(&B->a_empty[s]);
+        umma_commit(&B->b_empty[bb]);
+        ++issued;
+      }
+      if (issued == nk) {
+        umma_commit(&B->acc_full);
+      } else if (issued > 0) {  // given up: let the MMAs already issued finish before TMEM is released
+        umma_commit(&B->mma_drain);
+        mbar_wait(&B->mma_drain, 0u, kGDrainNs);
+      }
+    }
+  }
+  __syncthreads();
+  if (tid == 0 && !*abort_flag) gwait(&B->acc_full, 0u, abort_flag, a.err);
+  __syncthreads();
+  const bool ok = !*abort_flag;
+  tc_fence_after();
+  pdl_wait();  // the epilogue reads the residual / writes outputs the previous kernel may touch
+
+  // ---- epilogue (warps 0-7): warp w holds weight rows n0 + 32 (w % 4) + lane (TMEM lanes) and
+  // tokens t0 .. t0 + 31, t0 = 32 (w / 4) (TMEM columns); a store of one token is 32 rows wide ----
+  const int row = n0 + 32 * (warp & 3) + lane, t0 = 32 * ((warp >> 2) & 1);
+  float v[32];
+  if (warp < 8) {
+    uint32_t r[32];
+    tmem_ld32(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)t0, r);
+    tmem_wait_ld();
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+  }
+  bool run = ok;
+  if (splits > 1) {
+    if (warp < 8 && row < N)
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (t0 + i < M) a.ws[((size_t)split * kST + t0 + i) * N + row] = v[i];
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+      const bool last = atomicAdd(a.tile_cnt + blockIdx.x, 1u) == (unsigned)splits - 1;
+      if (last) a.tile_cnt[blockIdx.x] = 0u;  // every split of the tile has arrived: ready for the next launch
+      *last_flag = last;
+    }
+    __syncthreads();
+    run = ok && *last_flag;
+    if (run) {
+      __threadfence();
+      if (warp < 8 && row < N)
+#pragma unroll 4
+        for (int i = 0; i < 32; ++i) {
+          float acc = 0.f;
+          if (t0 + i < M)
+            for (int sp = 0; sp < splits; ++sp) acc += a.ws[((size_t)sp * kST + t0 + i) * N + row];
+          v[i] = acc;
+        }
+    }
+  }
+  if (run && warp < 8) {
+    if (a.epi == EPI_QKV) {  // rows (2P, 2P+1) of a head are its dims (i, i + D/2): lane pairs
+      const int hd = a.head_dim >> 1, P = row >> 1, head = P / hd, ii = P - head * hd;
+#pragma unroll 4
+      for (int i = 0; i < 32; ++i) {
+        const float y0 = v[i], y1 = __shfl_down_sync(0xffffffffu, v[i], 1);
+        const int t = t0 + i;
+        if ((lane & 1) || t >= M || row >= N) continue;
+        const int pp = a.pos[t];
+        if (head < a.n_q_heads) {
+          const float2 cs = a.rope[(size_t)pp * hd + ii];
+          float* qo = a.qout + ((size_t)t * a.n_q_heads + head) * a.head_dim;
+          qo[ii] = y0 * cs.x - y1 * cs.y;
+          qo[ii + hd] = y1 * cs.x + y0 * cs.y;
+        } else {
+          const bool is_k = head < a.n_q_heads + a.n_kv_heads;
+          const int kvh = head - a.n_q_heads - (is_k ? 0 : a.n_kv_heads);
+          const size_t base = (((size_t)a.seq[t] * a.n_kv_heads + kvh) * a.max_len + pp) * a.head_dim;
+          if (is_k) {
+            const float2 cs = a.rope[(size_t)pp * hd + ii];
+            a.kc[base + ii] = __float2half_rn(y0 * cs.x - y1 * cs.y);
+            a.kc[base + ii + hd] = __float2half_rn(y1 * cs.x + y0 * cs.y);
+          } else {
+            a.vc[base + ii] = __float2half_rn(y0);
+            a.vc[base + ii + hd] = __float2half_rn(y1);
+          }
+        }
+      }
+    } else if (a.epi == EPI_SWIGLU_BF16) {  // rows (2j, 2j+1) are (gate_j, up_j): lane pairs
+#pragma unroll 4
+      for (int i = 0; i < 32; ++i) {
+        const float g = v[i], u = __shfl_down_sync(0xffffffffu, v[i], 1);
+        const int t = t0 + i;
+        if (!(lane & 1) && t < M && row < N) a.out_bf16[(size_t)t * a.ldo_bf16 + (row >> 1)] = __float2bfloat16_rn(silu(g) * u);
+      }
+    } else {  // EPI_STORE / EPI_RESID
+#pragma unroll 4
+      for (int i = 0; i < 32; ++i) {
+        const int t = t0 + i;
+        if (t >= M || row >= N) continue;
+        float y = v[i];
+        if (a.epi == EPI_RESID) y = __fadd_rn(a.resid[(size_t)t * a.ldr + row], y);
+        a.out[(size_t)t * a.ldo + row] = y;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, kSTmemCols);
+}
+
 cudaError_t prepare_gemm_tc() {
   static_assert(sizeof(GBars) + 16 <= 256, "barrier block");
-  return cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGSmem);
+  static_assert(sizeof(SBars) + 16 <= 512, "barrier block of the small-call GEMM");
+  static_assert(kSSmem <= 227 * 1024, "shared memory of the small-call GEMM");
+  cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGSmem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(gemm_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSSmem);
+  return e;
+}
+
+int gemm_small_splits(int N, int Kp) {
+  // the split count with the fewest waves of full-K time: ceil(tiles * S / SMs) / S
+  const int tiles = (N + kSN - 1) / kSN, ng = Kp / 256, G = std::max(1, sm_count());
+  int best = 1;
+  double best_cost = (double)((tiles + G - 1) / G);
+  for (int S = 2; S <= std::min(8, ng); ++S) {
+    const double cost = (double)((tiles * S + G - 1) / G) / S;
+    if (cost < best_cost - 1e-9) {
+      best = S;
+      best_cost = cost;
+    }
+  }
+  return best;
+}
+
+size_t gemm_small_ws_bytes(int N, int Kp) {
+  const int S = gemm_small_splits(N, Kp);
+  return S > 1 ? (size_t)S * kST * (size_t)N * 4 : 0;
 }
 
 namespace {
@@ -354,6 +662,27 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t st) {
       ((uintptr_t)a.w.s & 15))
     return cudaErrorInvalidValue;
   CUtensorMap tA, tB, tS;
+  if (a.M <= kST) {  // a small call: the weight-streaming kernel
+    const int S = (a.ws && a.tile_cnt) ? gemm_small_splits(a.w.N, a.w.Kp) : 1;
+    if (!encode_2d(&tA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.a, (uint64_t)a.w.Kp, (uint64_t)a.M, (uint64_t)a.lda * 2,
+                   kSK, kST, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&tB, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.w.q, (uint64_t)a.w.Kp, (uint64_t)a.w.N, (uint64_t)a.w.Kp,
+                   128, kSN, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&tS, CU_TENSOR_MAP_DATA_TYPE_UINT16, a.w.s, (uint64_t)(a.w.Kp / 32), (uint64_t)a.w.N,
+                   (uint64_t)(a.w.Kp / 16), 8, kSN, CU_TENSOR_MAP_SWIZZLE_NONE))
+      return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((a.w.N + kSN - 1) / kSN, S);
+    cfg.blockDim = dim3(kGThreads);
+    cfg.dynamicSmemBytes = kSSmem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_enabled() ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, gemm_small_kernel, a, tA, tB, tS, S);
+  }
   if (!encode_2d(&tA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.a, (uint64_t)a.w.Kp, (uint64_t)a.M, (uint64_t)a.lda * 2,
                  kGBK, kGBM, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_2d(&tB, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.w.q, (uint64_t)a.w.Kp, (uint64_t)a.w.N, (uint64_t)a.w.Kp,
@@ -380,12 +709,12 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t st) {
 // reduction order matches the GEMV prologue.
 
 __global__ void rows_to_bf16_kernel(const float* x, int ld_in, int K, const float* gamma, float eps,
-                                    __nv_bfloat16* out, int ld_out) {
+                                    __nv_bfloat16* out, int ld_out, const int* rows) {
   __shared__ float nrm[8];
   pdl_trigger();
   pdl_wait();
   const int t = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const float* xr = x + (size_t)t * ld_in;
+  const float* xr = x + (size_t)(rows ? rows[t] : t) * ld_in;
   float rinv = 1.0f;
   if (gamma) {
     float ss = 0.f;
@@ -410,7 +739,7 @@ __global__ void rows_to_bf16_kernel(const float* x, int ld_in, int K, const floa
 }
 
 cudaError_t launch_rows_to_bf16(const float* x, int ld_in, int K, const float* gamma, float eps, int ntok,
-                                __nv_bfloat16* out, int ld_out, cudaStream_t st) {
+                                __nv_bfloat16* out, int ld_out, cudaStream_t st, const int* rows) {
   if (ntok <= 0) return cudaSuccess;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(ntok);
@@ -421,7 +750,7 @@ cudaError_t launch_rows_to_bf16(const float* x, int ld_in, int K, const float* g
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl_enabled() ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, rows_to_bf16_kernel, x, ld_in, K, gamma, eps, out, ld_out);
+  return cudaLaunchKernelEx(&cfg, rows_to_bf16_kernel, x, ld_in, K, gamma, eps, out, ld_out, rows);
 }
 
 // ------------------------------------------------------------------------------------------

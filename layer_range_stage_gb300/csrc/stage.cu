@@ -55,7 +55,7 @@ void walk_plan(const stage_model_cfg& c, int begin, int end, std::vector<LayerDe
                float2** part_ml, int** counters, int** d_seq, int** d_pos, int** d_tok, int** d_rows, int** err_word,
                float** moe_logits, int** moe_ids, float** moe_wts, __nv_bfloat16** act_bf16,
                __nv_bfloat16** ffn_bf16, lrs::MegaLayer** mlayers, unsigned long long** mega_tags, unsigned** mega_bar,
-               int** shared_id0, F&& f) {
+               int** shared_id0, float** gemm_ws, unsigned** gemm_cnt, F&& f) {
   auto q8 = [&](DevQ8* m, int N, int K) {
     if (m) {
       m->N = N;
@@ -122,6 +122,21 @@ void walk_plan(const stage_model_cfg& c, int begin, int end, std::vector<LayerDe
   if (!moe && c.gemm_bf16_min_tokens > 0) {  // bf16 operands of the tensor-core GEMMs
     f(T * (size_t)std::max(kpad(H), kpad(Hq * D)) * 2, (void**)act_bf16);
     f(T * (size_t)kpad(c.ffn) * 2, (void**)ffn_bf16);
+    if (c.gemm_bf16_min_tokens <= lrs::kGemmSmallTokens) {
+      // calls of at most kGemmSmallTokens tokens: K-split partials of the weight-streaming GEMM
+      // (the largest of the stage's projections and readout) and the tiles' arrival counters
+      const int mats[][2] = {{(Hq + 2 * Hkv) * D, H}, {H, Hq * D}, {2 * c.ffn, H}, {H, c.ffn},
+                             {end == c.n_layers ? c.vocab : 0, H}};
+      size_t ws = 0;
+      int tiles = 1;
+      for (const auto& m : mats)
+        if (m[0] > 0) {
+          ws = std::max(ws, lrs::gemm_small_ws_bytes(m[0], kpad(m[1])));
+          tiles = std::max(tiles, (m[0] + lrs::kGemmSmallRows - 1) / lrs::kGemmSmallRows);
+        }
+      f(ws, (void**)gemm_ws);
+      f((size_t)tiles * 4, (void**)gemm_cnt);
+    }
   }
   if (moe) {
     f(T * (c.n_experts + sh) * 4, (void**)moe_logits);
@@ -137,7 +152,7 @@ size_t plan_bytes(const stage_model_cfg& c, int begin, int end) {
   size_t total = 0;
   walk_plan(c, begin, end, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
             nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
-            nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
+            nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
             [&](size_t b, void**) { total += round_up(b, kAlign); });
   return total;
 }
@@ -196,6 +211,8 @@ struct stage {
   int *d_seq = nullptr, *d_pos = nullptr, *d_tok = nullptr, *d_rows = nullptr;
   int* err_word = nullptr;     // device: set by a kernel whose bounded wait timed out
   int* shared_id0 = nullptr;   // device: a zero expert id (the shared expert's gate/up launch)
+  float* gemm_ws = nullptr;     // K-split partials of the small calls' GEMMs (lrs::GemmArgs::ws)
+  unsigned* gemm_cnt = nullptr;  // their weight tiles' arrival counters
   float* moe_logits = nullptr;  // [max_tokens][n_experts] router logits
   int* moe_ids = nullptr;       // [max_tokens][top_k] selected experts
   float* moe_wts = nullptr;     // [max_tokens][top_k] routing weights
@@ -497,6 +514,8 @@ int block_tc(stage* st, int li, LayerDev& L, int n, const int* d_seq, const int*
   g.head_dim = D;
   g.max_len = c.max_seq_len;
   g.err = st->err_word;
+  g.ws = st->gemm_ws;
+  g.tile_cnt = st->gemm_cnt;
   if ((e = lrs::launch_gemm_tc(g, s)) != cudaSuccess) return cuda_err(st, e, "qkv gemm");
   lrs::AttnArgs at;
   at.q = st->qbuf;
@@ -530,6 +549,8 @@ int block_tc(stage* st, int li, LayerDev& L, int n, const int* d_seq, const int*
   o.out = hout;
   o.ldo = H;
   o.err = st->err_word;
+  o.ws = st->gemm_ws;
+  o.tile_cnt = st->gemm_cnt;
   if ((e = lrs::launch_gemm_tc(o, s)) != cudaSuccess) return cuda_err(st, e, "o gemm");
   if ((e = lrs::launch_rows_to_bf16(hout, H, H, L.ffn_norm, c.rms_eps, n, st->act_bf16, ldh, s)) != cudaSuccess)
     return cuda_err(st, e, "norm 2");
@@ -542,6 +563,8 @@ int block_tc(stage* st, int li, LayerDev& L, int n, const int* d_seq, const int*
   gu.out_bf16 = st->ffn_bf16;
   gu.ldo_bf16 = ldf;
   gu.err = st->err_word;
+  gu.ws = st->gemm_ws;
+  gu.tile_cnt = st->gemm_cnt;
   if (st->timing) timing_mark(st->tev[2 * li], s);
   if ((e = lrs::launch_gemm_tc(gu, s)) != cudaSuccess) return cuda_err(st, e, "gate_up gemm");
   if (st->timing) timing_mark(st->tev[2 * li + 1], s);
@@ -556,6 +579,8 @@ int block_tc(stage* st, int li, LayerDev& L, int n, const int* d_seq, const int*
   dn.out = hout;
   dn.ldo = H;
   dn.err = st->err_word;
+  dn.ws = st->gemm_ws;
+  dn.tile_cnt = st->gemm_cnt;
   if ((e = lrs::launch_gemm_tc(dn, s)) != cudaSuccess) return cuda_err(st, e, "down gemm");
   return STAGE_OK;
 }
@@ -1007,7 +1032,7 @@ int stage_create(const stage_model_cfg* cfg, stage_layer_range range, const stag
             &st->rope, &st->qbuf, &st->obuf, &st->abuf, &st->feat, &st->logits, &st->argmax, &st->part_o,
             &st->part_ml, &st->counters, &st->d_seq, &st->d_pos, &st->d_tok, &st->d_rows, &st->err_word,
             &st->moe_logits, &st->moe_ids, &st->moe_wts, &st->act_bf16, &st->ffn_bf16, &st->mlayers, &st->mega_tags,
-            &st->mega_bar, &st->shared_id0, [&](size_t b, void** slot) {
+            &st->mega_bar, &st->shared_id0, &st->gemm_ws, &st->gemm_cnt, [&](size_t b, void** slot) {
               if (slot) *slot = st->arena + off;
               off += round_up(b, kAlign);
             });
@@ -1091,18 +1116,38 @@ static int logits_dev(stage* st, int n_rows, const int* d_rows, float* logits_ou
                       cudaStream_t s) {
   const stage_model_cfg& c = st->cfg;
   float* lg = logits_out ? logits_out : st->logits;
-  lrs::GemvArgs h;
-  h.w = st->head;
-  h.x = st->feat;
-  h.ldx = c.hidden;
-  h.x_rows = d_rows;
-  h.ntok = n_rows;
-  h.epi = lrs::EPI_STORE;
-  h.out = lg;
-  h.ldo = c.vocab;
-  h.err = st->err_word;
-  cudaError_t e = lrs::launch_gemv(h, s);
-  if (e != cudaSuccess) return cuda_err(st, e, "lm_head");
+  cudaError_t e;
+  if (use_tc(st, n_rows) && n_rows <= lrs::kGemmSmallTokens) {
+    // the rows' features in bf16, then the weight-streaming GEMM: the head is read once
+    const int ldh = kpad(c.hidden);
+    if ((e = lrs::launch_rows_to_bf16(st->feat, c.hidden, c.hidden, nullptr, 0.f, n_rows, st->act_bf16, ldh, s,
+                                      d_rows)) != cudaSuccess)
+      return cuda_err(st, e, "readout operand");
+    lrs::GemmArgs g;
+    g.a = st->act_bf16;
+    g.lda = ldh;
+    g.w = st->head;
+    g.M = n_rows;
+    g.epi = lrs::EPI_STORE;
+    g.out = lg;
+    g.ldo = c.vocab;
+    g.err = st->err_word;
+    g.ws = st->gemm_ws;
+    g.tile_cnt = st->gemm_cnt;
+    if ((e = lrs::launch_gemm_tc(g, s)) != cudaSuccess) return cuda_err(st, e, "lm_head");
+  } else {
+    lrs::GemvArgs h;
+    h.w = st->head;
+    h.x = st->feat;
+    h.ldx = c.hidden;
+    h.x_rows = d_rows;
+    h.ntok = n_rows;
+    h.epi = lrs::EPI_STORE;
+    h.out = lg;
+    h.ldo = c.vocab;
+    h.err = st->err_word;
+    if ((e = lrs::launch_gemv(h, s)) != cudaSuccess) return cuda_err(st, e, "lm_head");
+  }
   e = lrs::launch_argmax(lg, c.vocab, n_rows, argmax_out ? argmax_out : st->argmax, s);
   if (e != cudaSuccess) return cuda_err(st, e, "argmax");
   return STAGE_OK;

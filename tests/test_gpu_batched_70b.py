@@ -15,7 +15,10 @@ Both decode paths of a 64-token call: the float32 GEMV path, and the tensor-core
 stage's GEMM threshold set to 64: every projection a tcgen05 GEMM with bf16 operands and f32
 accumulation) against the oracle with every GEMM operand rounded to bf16, where a block
 output is held to one bf16 ulp (2^-8) in relative L2 -- the bf16 tolerance of the prefill
-tests.  The readout is the float32 GEMV on both paths.
+tests.  A call of at most 64 tokens takes the weight-streaming GEMM (128 weight rows against
+the call's tokens, K split over several CTAs where the weight tiles are few).  The readout is
+the float32 GEMV on the f32 path and that bf16 GEMM on the tensor-core path, held to the same
+logit tolerance.
 """
 import numpy as np
 import pytest
