@@ -221,10 +221,12 @@ STAGE_API int stage_write_kv(stage_t st, int global_layer, int seq_id, int pos0,
                              const uint16_t* v_host);
 
 /* Which path a call with n_tokens tokens takes: 0 = float32 dequant-fused GEMV kernels,
- * 1 = bf16 tensor-core GEMMs (dense stages), 2 = float32 persistent decode (a single-token
- * call: every block of the stage in one cooperative launch, on MoE stages with the router
- * and top-k computed inside it; same arithmetic per weight as 0, its own fixed summation
- * order).  The environment variable LRS_PERSISTENT=0, read at
+ * 1 = bf16 tensor-core GEMMs (dense stages; calls of at most 64 tokens stream each weight
+ * once against all their tokens), 2 = float32 persistent decode (a single-token call: every
+ * block of the stage in one cooperative launch, on MoE stages with the router and top-k
+ * computed inside it; the staged input held as three signed bytes per value with one
+ * exponent per 16 values, each dot exact in integers before its float32 scaling, so it
+ * agrees with 0 to float32 rounding; its own fixed summation order).  The environment variable LRS_PERSISTENT=0, read at
  * stage_create, turns mode 2 off.  LRS_PDL=0, also read at stage_create, launches the
  * per-kernel paths (modes 0 and 1) without programmatic dependent launch: each kernel then
  * starts only after its predecessor on the stream has finished, instead of overlapping its
