@@ -250,38 +250,60 @@ __global__ void __launch_bounds__(kGThreads, 1)
   for (int h = 0; h < 2 && ok && warp < 8; ++h) {
     const int rbase = m0 + h * 128 + 32 * p;
 #pragma unroll 1
+    // the rows' positions and sequences (QKV), one load per lane, shared by shuffles below
+    const int prow = rbase + lane;
+    const int pos_l = (a.epi == EPI_QKV && prow < M) ? a.pos[prow] : 0;
+    const int seq_l = (a.epi == EPI_QKV && prow < M) ? a.seq[prow] : 0;
+#pragma unroll 1
     for (int cc = 0; cc < 4; ++cc) {
       const int c0 = chalf * 128 + cc * 32;
+      const int gn0 = n0 + c0;
+      const int gn = gn0 + lane;
+      // the global inputs of the epilogue are requested before the accumulators are read, all
+      // at once (every load of the block in flight together, not one per row)
+      float rv[32];
+      if (a.epi == EPI_RESID) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          rv[j] = (rbase + j < M && gn < N) ? a.resid[(size_t)(rbase + j) * a.ldr + gn] : 0.f;
+      }
+      const int qi = lane & 15, qhalf = lane >> 4;  // QKV: column pair qi, rows 2 jj + qhalf
+      const int hd = a.head_dim >> 1, qP = (gn0 >> 1) + qi, qhead = hd ? qP / hd : 0, qii = qP - qhead * hd;
+      float2 cs[16];
+      if (a.epi == EPI_QKV) {
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) {
+          const int jr = 2 * jj + qhalf;
+          const int pp = __shfl_sync(0xffffffffu, pos_l, jr);
+          cs[jj] = (qhead < a.n_q_heads + a.n_kv_heads && rbase + jr < M) ? a.rope[(size_t)pp * hd + qii]
+                                                                          : make_float2(1.f, 0.f);
+        }
+      }
       uint32_t r[32];
       tmem_ld32(tmem + ((uint32_t)(32 * p) << 16) + (uint32_t)(h * kGBN + c0), r);
       tmem_wait_ld();
-      const int gn0 = n0 + c0;
 #pragma unroll
       for (int i = 0; i < 32; ++i) stg[lane * 33 + i] = __uint_as_float(r[i]);
       __syncwarp();
-      const int gn = gn0 + lane;
       if (a.epi == EPI_QKV) {  // column pairs (2i, 2i+1) of a head are its dims (i, i + D/2)
-        const int i = lane & 15, half = lane >> 4;  // two rows per pass, 16 pairs each
-        const int hd = a.head_dim >> 1, P = (gn0 >> 1) + i, head = P / hd, ii = P - head * hd;
-#pragma unroll 2
-        for (int j = 0; j < 32; j += 2) {
-          const int jr = j + half, gm = rbase + jr;
+        const int i = qi, half = qhalf, head = qhead, ii = qii;  // two rows per pass, 16 pairs each
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) {
+          const int jr = 2 * jj + half, gm = rbase + jr;
+          const int pp = __shfl_sync(0xffffffffu, pos_l, jr), sq = __shfl_sync(0xffffffffu, seq_l, jr);
           if (gm >= M || gn0 + 2 * i >= N) continue;
           const float y0 = stg[jr * 33 + 2 * i], y1 = stg[jr * 33 + 2 * i + 1];
-          const int pp = a.pos[gm];
           if (head < a.n_q_heads) {
-            const float2 cs = a.rope[(size_t)pp * hd + ii];
             float* qo = a.qout + ((size_t)gm * a.n_q_heads + head) * a.head_dim;
-            qo[ii] = y0 * cs.x - y1 * cs.y;
-            qo[ii + hd] = y1 * cs.x + y0 * cs.y;
+            qo[ii] = y0 * cs[jj].x - y1 * cs[jj].y;
+            qo[ii + hd] = y1 * cs[jj].x + y0 * cs[jj].y;
           } else {
             const bool is_k = head < a.n_q_heads + a.n_kv_heads;
             const int kvh = head - a.n_q_heads - (is_k ? 0 : a.n_kv_heads);
-            const size_t base = (((size_t)a.seq[gm] * a.n_kv_heads + kvh) * a.max_len + pp) * a.head_dim;
+            const size_t base = (((size_t)sq * a.n_kv_heads + kvh) * a.max_len + pp) * a.head_dim;
             if (is_k) {
-              const float2 cs = a.rope[(size_t)pp * hd + ii];
-              a.kc[base + ii] = __float2half_rn(y0 * cs.x - y1 * cs.y);
-              a.kc[base + ii + hd] = __float2half_rn(y1 * cs.x + y0 * cs.y);
+              a.kc[base + ii] = __float2half_rn(y0 * cs[jj].x - y1 * cs[jj].y);
+              a.kc[base + ii + hd] = __float2half_rn(y1 * cs[jj].x + y0 * cs[jj].y);
             } else {
               a.vc[base + ii] = __float2half_rn(y0);
               a.vc[base + ii + hd] = __float2half_rn(y1);
@@ -298,12 +320,12 @@ __global__ void __launch_bounds__(kGThreads, 1)
           if (gm < M && gn0 + 2 * i < N) a.out_bf16[(size_t)gm * a.ldo_bf16 + go] = __float2bfloat16_rn(silu(g) * u);
         }
       } else {  // EPI_STORE / EPI_RESID
-#pragma unroll 4
+#pragma unroll
         for (int j = 0; j < 32; ++j) {
           const int gm = rbase + j;
           if (gm >= M || gn >= N) continue;
           float v = stg[j * 33 + lane];
-          if (a.epi == EPI_RESID) v = __fadd_rn(a.resid[(size_t)gm * a.ldr + gn], v);
+          if (a.epi == EPI_RESID) v = __fadd_rn(rv[j], v);
           a.out[(size_t)gm * a.ldo + gn] = v;
         }
       }
