@@ -559,41 +559,54 @@ __global__ void __launch_bounds__(kGThreads, 1)
     run = ok && *last_flag;
     if (run) {
       __threadfence();
-      if (warp < 8 && row < N)
-#pragma unroll 4
-        for (int i = 0; i < 32; ++i) {
-          float acc = 0.f;
-          if (t0 + i < M)
-            for (int sp = 0; sp < splits; ++sp) acc += a.ws[((size_t)sp * kST + t0 + i) * N + row];
-          v[i] = acc;
-        }
+      if (warp < 8 && row < N) {  // split by split, the 32 tokens' partials in flight together
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = 0.f;
+        for (int sp = 0; sp < splits; ++sp)
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (t0 + i < M) v[i] += a.ws[((size_t)sp * kST + t0 + i) * N + row];
+      }
     }
   }
   if (run && warp < 8) {
+    // the tokens' positions and sequences: one load per lane (token t0 + lane), then shuffles
+    const int pos_l = (a.epi == EPI_QKV && t0 + lane < M) ? a.pos[t0 + lane] : 0;
+    const int seq_l = (a.epi == EPI_QKV && t0 + lane < M) ? a.seq[t0 + lane] : 0;
     if (a.epi == EPI_QKV) {  // rows (2P, 2P+1) of a head are its dims (i, i + D/2): lane pairs
       const int hd = a.head_dim >> 1, P = row >> 1, head = P / hd, ii = P - head * hd;
-#pragma unroll 4
-      for (int i = 0; i < 32; ++i) {
-        const float y0 = v[i], y1 = __shfl_down_sync(0xffffffffu, v[i], 1);
-        const int t = t0 + i;
-        if ((lane & 1) || t >= M || row >= N) continue;
-        const int pp = a.pos[t];
-        if (head < a.n_q_heads) {
-          const float2 cs = a.rope[(size_t)pp * hd + ii];
-          float* qo = a.qout + ((size_t)t * a.n_q_heads + head) * a.head_dim;
-          qo[ii] = y0 * cs.x - y1 * cs.y;
-          qo[ii + hd] = y1 * cs.x + y0 * cs.y;
-        } else {
-          const bool is_k = head < a.n_q_heads + a.n_kv_heads;
-          const int kvh = head - a.n_q_heads - (is_k ? 0 : a.n_kv_heads);
-          const size_t base = (((size_t)a.seq[t] * a.n_kv_heads + kvh) * a.max_len + pp) * a.head_dim;
-          if (is_k) {
-            const float2 cs = a.rope[(size_t)pp * hd + ii];
-            a.kc[base + ii] = __float2half_rn(y0 * cs.x - y1 * cs.y);
-            a.kc[base + ii + hd] = __float2half_rn(y1 * cs.x + y0 * cs.y);
+      const bool rotated = head < a.n_q_heads + a.n_kv_heads;
+#pragma unroll 8
+      for (int i0 = 0; i0 < 32; i0 += 8) {
+        float2 cs[8];  // the RoPE factors of eight tokens, requested together
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int pp = __shfl_sync(0xffffffffu, pos_l, i0 + k);
+          cs[k] = (rotated && !(lane & 1) && t0 + i0 + k < M && row < N) ? a.rope[(size_t)pp * hd + ii]
+                                                                         : make_float2(1.f, 0.f);
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int i = i0 + k;
+          const float y0 = v[i], y1 = __shfl_down_sync(0xffffffffu, v[i], 1);
+          const int pp = __shfl_sync(0xffffffffu, pos_l, i), sq = __shfl_sync(0xffffffffu, seq_l, i);
+          const int t = t0 + i;
+          if ((lane & 1) || t >= M || row >= N) continue;
+          if (head < a.n_q_heads) {
+            float* qo = a.qout + ((size_t)t * a.n_q_heads + head) * a.head_dim;
+            qo[ii] = y0 * cs[k].x - y1 * cs[k].y;
+            qo[ii + hd] = y1 * cs[k].x + y0 * cs[k].y;
           } else {
-            a.vc[base + ii] = __float2half_rn(y0);
-            a.vc[base + ii + hd] = __float2half_rn(y1);
+            const bool is_k = head < a.n_q_heads + a.n_kv_heads;
+            const int kvh = head - a.n_q_heads - (is_k ? 0 : a.n_kv_heads);
+            const size_t base = (((size_t)sq * a.n_kv_heads + kvh) * a.max_len + pp) * a.head_dim;
+            if (is_k) {
+              a.kc[base + ii] = __float2half_rn(y0 * cs[k].x - y1 * cs[k].y);
+              a.kc[base + ii + hd] = __float2half_rn(y1 * cs[k].x + y0 * cs[k].y);
+            } else {
+              a.vc[base + ii] = __float2half_rn(y0);
+              a.vc[base + ii + hd] = __float2half_rn(y1);
+            }
           }
         }
       }
@@ -604,13 +617,17 @@ __global__ void __launch_bounds__(kGThreads, 1)
         const int t = t0 + i;
         if (!(lane & 1) && t < M && row < N) a.out_bf16[(size_t)t * a.ldo_bf16 + (row >> 1)] = __float2bfloat16_rn(silu(g) * u);
       }
-    } else {  // EPI_STORE / EPI_RESID
-#pragma unroll 4
+    } else {  // EPI_STORE / EPI_RESID: the residuals of the 32 tokens requested together
+      float rv[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        rv[i] = (a.epi == EPI_RESID && t0 + i < M && row < N) ? a.resid[(size_t)(t0 + i) * a.ldr + row] : 0.f;
+#pragma unroll
       for (int i = 0; i < 32; ++i) {
         const int t = t0 + i;
         if (t >= M || row >= N) continue;
         float y = v[i];
-        if (a.epi == EPI_RESID) y = __fadd_rn(a.resid[(size_t)t * a.ldr + row], y);
+        if (a.epi == EPI_RESID) y = __fadd_rn(rv[i], y);
         a.out[(size_t)t * a.ldo + row] = y;
       }
     }
