@@ -50,6 +50,13 @@ __device__ __forceinline__ void cp_async8(void* smem, const void* gmem) {
 }
 
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+// Close the thread's current group of asynchronous copies; wait until at most N groups are
+// still in flight (the older ones complete first).
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 
 // Programmatic dependent launch: a kernel launched with programmatic stream serialization
 // may start before its predecessor on the stream has finished.  Everything it reads that

@@ -17,8 +17,9 @@ accumulation) against the oracle with every GEMM operand rounded to bf16, where 
 output is held to one bf16 ulp (2^-8) in relative L2 -- the bf16 tolerance of the prefill
 tests.  A call of at most 64 tokens takes the weight-streaming GEMM (128 weight rows against
 the call's tokens, K split over several CTAs where the weight tiles are few).  The readout is
-the float32 GEMV on the f32 path and that bf16 GEMM on the tensor-core path, held to the same
-logit tolerance.
+the float32 GEMV on the f32 path and that bf16 GEMM on the tensor-core path; like every GEMM
+of that path it is checked against the oracle with its operands (features and dequantised head)
+rounded to bf16, to the same logit tolerance.
 """
 import numpy as np
 import pytest
@@ -98,10 +99,14 @@ def test_70b_shape_batched_decode_ragged_64(cuda, path):
         assert rel_l2(hg[li], ref) <= HIDDEN_RTOL[path], li
         if li == 3:
             head = w.lm_head
-            feats = hg[3].astype(np.float64)  # the readout of the GPU's own features
+            # the readout of the GPU's own features; on the tensor-core path the readout is a
+            # GEMM like the others, so its operands are rounded to bf16 on the oracle's side too
+            feats = hg[3].astype(np.float64)
+            rd = (lambda m: oracle.bf16(m)) if path == "bf16" else (lambda m: m)
+            feats = rd(feats)
             rng = np.random.default_rng(4403)
             sample = np.unique(np.concatenate([rng.integers(0, model.vocab, 512), argmax]))
-            lo = oracle.matvec(oracle.dequant(head.q[sample], head.s[sample]), feats)
+            lo = oracle.matvec(rd(oracle.dequant(head.q[sample], head.s[sample])), feats)
             assert np.abs(logits[:, sample] - lo).max() <= LOGIT_ATOL
             # full argmax of the oracle, in chunks of vocabulary rows
             best = np.full(NSEQ, -np.inf)
@@ -109,7 +114,7 @@ def test_70b_shape_batched_decode_ragged_64(cuda, path):
             arg = np.zeros(NSEQ, dtype=np.int64)
             for r0 in range(0, model.vocab, 8192):
                 r1 = min(model.vocab, r0 + 8192)
-                chunk = oracle.matvec(oracle.dequant(head.q[r0:r1], head.s[r0:r1]), feats)
+                chunk = oracle.matvec(rd(oracle.dequant(head.q[r0:r1], head.s[r0:r1])), feats)
                 for t in range(NSEQ):
                     c = chunk[t]
                     j = int(np.argmax(c))
