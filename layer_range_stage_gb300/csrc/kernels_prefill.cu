@@ -249,7 +249,6 @@ __global__ void __launch_bounds__(kGThreads, 1)
 #pragma unroll 1
   for (int h = 0; h < 2 && ok && warp < 8; ++h) {
     const int rbase = m0 + h * 128 + 32 * p;
-#pragma unroll 1
     // the rows' positions and sequences (QKV), one load per lane, shared by shuffles below
     const int prow = rbase + lane;
     const int pos_l = (a.epi == EPI_QKV && prow < M) ? a.pos[prow] : 0;
@@ -863,7 +862,9 @@ __global__ void __launch_bounds__(kPThreads) attn_prefill_kernel(const AttnArgs 
   pdl_trigger();
   pdl_wait();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int kvh = blockIdx.y, t0 = blockIdx.x * QB;
+  // the grid runs the blocks of later tokens first (KV head fastest): within a sequence they
+  // walk the most tiles, so the last CTAs to start are the shortest ones
+  const int kvh = blockIdx.x, t0 = (gridDim.y - 1 - blockIdx.y) * QB;
   // rows r = i * G + g: token t0 + i, query head kvh * G + g; q to fp16
   for (int i = tid; i < kPR * (D / 4); i += kPThreads) {
     const int r = i / (D / 4), c4 = i - r * (D / 4);
@@ -1051,7 +1052,7 @@ template <int D, int G>
 static cudaError_t launch_attn_prefill_dg(const AttnArgs& a, cudaStream_t st) {
   constexpr int QB = kPR / G;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((a.ntok + QB - 1) / QB, a.Hkv);
+  cfg.gridDim = dim3(a.Hkv, (a.ntok + QB - 1) / QB);
   cfg.blockDim = dim3(kPThreads);
   cfg.dynamicSmemBytes = PrefillSmem<D>::total;
   cfg.stream = st;
