@@ -753,7 +753,47 @@ __global__ void rows_to_bf16_kernel(const float* x, int ld_in, int K, const floa
   pdl_wait();
   const int t = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const float* xr = x + (size_t)(rows ? rows[t] : t) * ld_in;
+  __nv_bfloat16* orow = out + (size_t)t * ld_out;
+  // rows of at most 8192 values in 16-byte pieces: each thread keeps its (at most eight) float4
+  // pieces in registers between the sum of squares and the output
+  constexpr int NV = 8;
+  const bool vec = K <= 256 * 4 * NV && ((K | ld_in | ld_out) & 3) == 0 &&
+                   !(((uintptr_t)x | (uintptr_t)(gamma ? gamma : x)) & 15) && !((uintptr_t)out & 7);
   float rinv = 1.0f;
+  if (vec) {
+    const int n4 = K >> 2;
+    float4 v[NV];
+    float ss = 0.f;
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+      const int i = tid + 256 * j;
+      v[j] = i < n4 ? reinterpret_cast<const float4*>(xr)[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+      ss = fmaf(v[j].x, v[j].x, fmaf(v[j].y, v[j].y, fmaf(v[j].z, v[j].z, fmaf(v[j].w, v[j].w, ss))));
+    }
+    if (gamma) {
+      ss = warp_sum(ss);
+      if (lane == 0) nrm[warp] = ss;
+      __syncthreads();
+      float tot = 0.f;
+#pragma unroll
+      for (int w = 0; w < 8; ++w) tot += nrm[w];
+      rinv = 1.0f / sqrtf(tot / (float)K + eps);
+    }
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+      const int i = tid + 256 * j;
+      if (4 * i >= ld_out) break;
+      float4 y = v[j];
+      if (gamma && i < n4) {
+        const float4 g = reinterpret_cast<const float4*>(gamma)[i];
+        y = make_float4(y.x * rinv * g.x, y.y * rinv * g.y, y.z * rinv * g.z, y.w * rinv * g.w);
+      }
+      reinterpret_cast<uint2*>(orow)[i] = make_uint2(pack_bf16x2(y.x, y.y), pack_bf16x2(y.z, y.w));
+    }
+    for (int i = tid + 256 * NV; 4 * i < ld_out; i += 256)  // zero beyond the kept pieces
+      reinterpret_cast<uint2*>(orow)[i] = make_uint2(0u, 0u);
+    return;
+  }
   if (gamma) {
     float ss = 0.f;
     for (int k = tid; k < K; k += 256) {
@@ -768,7 +808,6 @@ __global__ void rows_to_bf16_kernel(const float* x, int ld_in, int K, const floa
     for (int w = 0; w < 8; ++w) tot += nrm[w];
     rinv = 1.0f / sqrtf(tot / (float)K + eps);
   }
-  __nv_bfloat16* orow = out + (size_t)t * ld_out;
   for (int k = tid; k < ld_out; k += 256) {
     float v = 0.f;
     if (k < K) v = gamma ? xr[k] * rinv * gamma[k] : xr[k];
