@@ -647,8 +647,10 @@ cudaError_t prepare_gemm_tc() {
 }
 
 int gemm_small_splits(int N, int Kp) {
-  // the split count with the fewest waves of full-K time: ceil(tiles * S / SMs) / S
+  // only when the weight tiles alone leave SMs idle: then the split count with the fewest
+  // waves of full-K time, ceil(tiles * S / SMs) / S
   const int tiles = (N + kSN - 1) / kSN, ng = Kp / 256, G = std::max(1, sm_count());
+  if (tiles >= G) return 1;
   int best = 1;
   double best_cost = (double)((tiles + G - 1) / G);
   for (int S = 2; S <= std::min(8, ng); ++S) {
