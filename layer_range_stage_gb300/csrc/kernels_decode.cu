@@ -377,16 +377,19 @@ cudaError_t launch_gemv(const GemvArgs& a, cudaStream_t st) {
 // ------------------------------------------------------------------------------------------
 // Split-K GQA decode attention.  Grid (n_chunks, Hkv, ntok), 128 threads, about one wave of
 // CTAs.  The CTA takes the G = Hq / Hkv query heads that share KV head blockIdx.y and the
-// positions of its chunk of 0..pos[t].  It walks the chunk in tiles of 128 positions: all
+// positions of its chunk of 0..pos[t].  It walks the chunk in tiles of 64 positions: all
 // threads first copy the K and V rows of the tile into shared memory with cp.async (every
-// copy of the tile in flight at once), then thread p scores position p for every head, a
-// running max / sum per head is kept, and the probability-weighted V rows accumulate.  The
+// copy of the tile in flight at once), then threads 2p and 2p + 1 score position p for every
+// head (half of the dims each), a running max / sum per head is kept, and the
+// probability-weighted V rows accumulate.  Shared memory is kept to ~43 KB (the PV sums of the
+// position groups reuse the tile area at the end) so that five CTAs share an SM and one CTA's
+// copies overlap the others' arithmetic.  The
 // chunk's partial (unnormalised output, max, sum) goes to scratch; the last CTA of a
 // (token, kv head) to finish -- found with one integer atomic, no waiting -- merges the
 // chunks in chunk order after copying every partial into shared memory in one round trip.
 
 constexpr int kAttnThreads = 128;
-constexpr int kAttnTile = 128;
+constexpr int kAttnTile = 64;
 
 template <int D, int G>
 struct AttnSmem {
@@ -399,7 +402,9 @@ struct AttnSmem {
   static constexpr size_t o = (size_t)NPG * G * D * 4;
   static constexpr size_t w = (size_t)kAttnMaxChunks * G * 4;
   static constexpr size_t stats = (size_t)4 * G * 4;
-  static constexpr size_t total = 2 * kv + q + p + o + w + stats;
+  static constexpr size_t total = 2 * kv + q + p + w + stats;  // o reuses the K/V tile area
+  static_assert(o <= 2 * kv, "PV sums of the position groups over the K/V tiles");
+  static_assert((size_t)G * kAttnMaxChunks * 8 <= q + p, "merge (max, sum) pairs over q and the scores");
   // chunks whose partials fit in the K/V tile area for the one-shot merge
   static constexpr int merge_chunks = (int)((2 * kv) / ((size_t)G * D * 4));
 };
@@ -413,8 +418,8 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const AttnArg
   __half* vs = ks + TP * KROW;
   float* qs = reinterpret_cast<float*>(sm_raw + 2 * S::kv);
   float* ps = qs + G * D;                   // [G][TP]
-  float* ored = ps + G * TP;                // [NPG][G][D]
-  float* wts = ored + NPG * G * D;          // [n_chunks][G]
+  float* ored = reinterpret_cast<float*>(sm_raw);  // [NPG][G][D] after the last tile
+  float* wts = ps + G * TP;                 // [n_chunks][G]
   float* st_m = wts + kAttnMaxChunks * G;   // [G] running max
   float* st_l = st_m + G;                   // [G] running sum
   float* st_a = st_l + G;                   // [G] rescale of this tile
@@ -457,14 +462,15 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const AttnArg
     }
     cp_async_wait_all();
     __syncthreads();
-    // scores: thread tid -> position tid, every head
-    if (tid < np) {
+    // scores: threads 2p and 2p + 1 -> position p, half of the dims each, every head
+    {
+      const int pp = tid >> 1, hf = tid & 1;
       float sc[G];
 #pragma unroll
       for (int g = 0; g < G; ++g) sc[g] = 0.f;
-      const __half* kr = ks + tid * KROW;
+      const __half* kr = ks + pp * KROW + hf * (D / 2);
 #pragma unroll 4
-      for (int i = 0; i < D / 8; ++i) {
+      for (int i = 0; i < (pp < np ? D / 16 : 0); ++i) {
         const uint4 kk = *reinterpret_cast<const uint4*>(kr + 8 * i);
         const float2 k01 = __half22float2(*reinterpret_cast<const __half2*>(&kk.x));
         const float2 k23 = __half22float2(*reinterpret_cast<const __half2*>(&kk.y));
@@ -472,8 +478,8 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const AttnArg
         const float2 k67 = __half22float2(*reinterpret_cast<const __half2*>(&kk.w));
 #pragma unroll
         for (int g = 0; g < G; ++g) {
-          const float4 qa = *reinterpret_cast<const float4*>(qs + g * D + 8 * i);
-          const float4 qb = *reinterpret_cast<const float4*>(qs + g * D + 8 * i + 4);
+          const float4 qa = *reinterpret_cast<const float4*>(qs + g * D + hf * (D / 2) + 8 * i);
+          const float4 qb = *reinterpret_cast<const float4*>(qs + g * D + hf * (D / 2) + 8 * i + 4);
           float s = sc[g];
           s = fmaf(qa.x, k01.x, s);
           s = fmaf(qa.y, k01.y, s);
@@ -487,7 +493,10 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const AttnArg
         }
       }
 #pragma unroll
-      for (int g = 0; g < G; ++g) ps[g * TP + tid] = sc[g] * a.scale;
+      for (int g = 0; g < G; ++g) sc[g] += __shfl_xor_sync(0xffffffffu, sc[g], 1);
+      if (pp < np && hf == 0)
+#pragma unroll
+        for (int g = 0; g < G; ++g) ps[g * TP + pp] = sc[g] * a.scale;
     }
     __syncthreads();
     // per head: tile max, probabilities, running (max, sum); warp w handles heads w, w + 4, ...
@@ -573,7 +582,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const AttnArg
   float* pst = reinterpret_cast<float*>(sm_raw);  // [nch][G*D] partials, over the K/V tiles
   if (staged)
     for (int i = tid; i < nch * G * D / 4; i += NT) cp_async16(pst + 4 * i, pbase + 4 * i);
-  float2* mls = reinterpret_cast<float2*>(ored);  // [G][nch] (max, sum), reusing the PV scratch
+  float2* mls = reinterpret_cast<float2*>(qs);  // [G][nch] (max, sum), over q and the scores (read by now)
   for (int i = tid; i < G * nch; i += NT) mls[i] = __ldcg(a.part_ml + head0 * nch + i);
   __syncthreads();
   if (tid < G) {
