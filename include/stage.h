@@ -244,11 +244,11 @@ STAGE_API void stage_destroy(stage_t st);
  *   what = 1: mark the stage busy (value 1) or idle (value 0) as if a call were in progress;
  *   what = 2: the next prefill/decode returns STAGE_E_INJECTED before launching anything;
  *   what = 3 (value 1): the next single-token decode that runs on the persistent kernel (outside
- *     stream capture) waits at its grid barriers for one CTA more than the grid holds.  Every
- *     such wait runs out after its time limit (0.2 s); the kernel then sets the stage's error
- *     word, waits (bounded) for its own copies in flight and leaves, so the call reports
- *     STAGE_E_CUDA when its error word is read and the next call runs normally.  This tests
- *     the device-side timeout path without faulting or hanging the GPU. */
+ *     stream capture) waits, in its attention step, for a tag that no step of the launch
+ *     writes.  Every such wait runs out after its time limit (0.2 s); the kernel then sets the
+ *     stage's error word, waits (bounded) for its own copies in flight and leaves, so the call
+ *     reports STAGE_E_CUDA when its error word is read and the next call runs normally.  This
+ *     tests the device-side timeout path without faulting or hanging the GPU. */
 STAGE_API int stage_debug_inject(stage_t st, int what, int value);
 
 /* ------------------------------------------------------------------------- pipeline

@@ -125,12 +125,12 @@ cudaError_t prepare_gemm_tc();
 cudaError_t launch_rows_to_bf16(const float* x, int ld_in, int K, const float* gamma, float eps, int ntok,
                                 __nv_bfloat16* out, int ld_out, cudaStream_t st, const int* rows = nullptr);
 
-// Persistent decode of a dense stage: every block of the stage for one token in one
-// cooperative launch (one CTA per SM).  Per block, five phases separated by grid barriers:
-// QKV GEMV (RMSNorm prologue; RoPE + fp16 KV append epilogue), split-K attention with the
-// last-arriving chunk merging, O GEMV + residual, gate/up GEMV (RMSNorm prologue, SwiGLU
-// epilogue), down GEMV + residual.  Weight rows stream through a per-warp ring of bulk
-// copies that runs ahead across phases and blocks.
+// Persistent decode of a stage: every block of the stage for one token in one cooperative
+// launch (one CTA per SM).  Per block: QKV GEMV (RMSNorm; RoPE + fp16 KV append epilogue),
+// split-K attention with the last-arriving chunk merging, O GEMV + residual, (MoE) router and
+// ranking, gate/up GEMV (RMSNorm, SwiGLU epilogue), down GEMV + residual; the steps hand their
+// vectors over as tagged entries (no grid barrier).  Weight rows stream through a per-warp ring
+// of tensor copies that runs ahead across steps and blocks.
 struct MegaLayer {
   DevQ8 wqkv, wo, wgu, wdown;  // dense FFN (wgu, wdown) ...
   DevQ8 router, egu, edown;    // ... or routed experts (stacked as in the stage's layout)

@@ -12,28 +12,30 @@
 // idles, and a successor cannot start streaming until its predecessor's CTAs leave the
 // SMs.  Here the weight stream never stops: each warp owns a fixed sequence of weight
 // slices (its share of every projection of every block, known before the first
-// activation exists) and keeps two of them in flight as bulk copies into shared memory,
-// running ahead across phases and blocks; the activations meet the weights at five grid
-// barriers per block (six in MoE stages).
+// activation exists) and keeps two of them in flight as tensor copies into shared memory,
+// running ahead across projections and blocks.
 //
-// Work split of a projection with N rows: a task is a row pair (2t, 2t + 1) -- the pairs the
-// RoPE and SwiGLU epilogues need, and for the other projections two rows that share each
-// load of the staged input -- cut into P column blocks of at most 2 KB per row; a ring slot
-// holds a block's two row pieces side by side.  Task t belongs to warp t mod (warps of the
-// grid), so at any moment the grid reads one window of the matrix.  A warp sums its blocks
-// in order and reduces with shuffles: every output has one fixed summation order.
+// Work split of a projection: CTA c owns a contiguous range of row pairs (2t, 2t + 1) -- the
+// pairs the RoPE and SwiGLU epilogues need, and for the other projections two rows that share
+// each read of the staged input -- cut into slots of at most 2048 columns; the CTA's slots, in
+// memory order, are dealt to its warps in groups (see Split).  Every output has one fixed
+// summation order.
 //
-// MoE stages: the router rows are a phase of the weight stream like the projections (a logit
-// per task, written to global memory); after one more grid barrier every CTA ranks all the
-// logits itself (top-k with ties to the lower id, softmax over the selected: the same
-// arithmetic on the same data, so every CTA picks the same experts), and the gate/up and
-// down slices of the selected experts stream in once it is known (the weight stream pauses
-// there: those slices depend on the routing).
+// Hand-offs without grid barriers: every vector one step passes to the next (q, the current K
+// and V rows, the attention output, the post-attention residual, the block output, the router
+// logits) is written as tagged 64-bit entries (launch sequence and block in the high word), and
+// a consumer waits only for the entries it reads; the SwiGLU output goes by plain stores and a
+// counter.  A CTA reads a step's input only if it has work in the step, so every reader of a
+// vector contributes to what that vector's next writers wait for.
 //
-// Grid barrier: a counter that only grows within a launch (release add, acquire polling,
-// bounded by time) and is reset by the last CTA to leave.  Every wait is bounded; a CTA
-// that runs out of time sets the error word, waits (bounded) for its own copies in flight
-// and leaves.
+// MoE stages: the router rows are a projection of the weight stream like the others (tagged
+// logits); every CTA gathers the logits and ranks them itself (top-k with ties to the lower id,
+// softmax over the selected: the same arithmetic on the same data, so every CTA picks the same
+// experts), and the gate/up and down slices of the selected experts stream in once it is known
+// (the weight stream pauses there: those slices depend on the routing).
+//
+// Every wait is bounded by time; a CTA that runs out sets the error word, waits (bounded) for
+// its own copies in flight and leaves, and the last CTA to leave resets the counters.
 
 // This header holds the kernel and its device code; kernels_mega.cu instantiates the dense
 // kernels and holds the host entry points, kernels_mega_moe.cu the MoE kernels.

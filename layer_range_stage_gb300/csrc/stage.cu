@@ -233,7 +233,7 @@ struct stage {
   int last_n = 0;
   std::atomic<int> busy{0};
   int fail_next = 0;
-  int stall_barrier = 0;  // tests: the next persistent launch's grid barriers wait for one CTA too many
+  int stall_barrier = 0;  // tests: the next persistent launch's attention waits for a tag never written
   std::string err;
 };
 
