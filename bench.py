@@ -435,7 +435,9 @@ def run_batched(args, dist=None):
             "roofline": {"bound": "hbm", "achieved": round(k_gbs, 1) if k_gbs else None, "peak": peak, "unit": "GB/s",
                          "frac": round(k_gbs / peak, 4) if (peak and k_gbs) else None, "traffic": None,
                          "kernel": ("FFN gate/up GEMV, 4 tokens per pass over the weights (SwiGLU epilogue)"
-                                    if path == "f32" else "FFN gate/up tcgen05 GEMM, bf16 operands (SwiGLU epilogue)"),
+                                    if path == "f32" else
+                                    "FFN gate/up tcgen05 small-call GEMM: 128 weight rows x 64 tokens, bf16 operands "
+                                    "(SwiGLU epilogue)"),
                          "bytes_per_launch": round(k_bytes), "mean_launch_us": round(k_us, 2), "launches_timed": k_n,
                          "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs)" if peak else "fallback"},
             "e2e": {"value": round(n_e2e * nseq * world / e2e_s, 1), "unit": "tok/s",
