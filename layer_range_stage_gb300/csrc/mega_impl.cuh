@@ -114,8 +114,17 @@ __device__ __forceinline__ int q_slot(int d) {
   return ((d & 4) ? D / 2 : 0) + ((d >> 3) << 2) + (d & 3);
 }
 
+// The counters: after a CTA barrier, one thread's release (or acquire-release) operation at GPU
+// scope publishes every write the CTA made before the barrier (release is cumulative), and an
+// acquire by one thread followed by a CTA barrier orders every thread's later reads after the
+// writes it observed -- no separate fence on either side.
 __device__ __forceinline__ void red_release_add(unsigned* p, unsigned v) {
   asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ unsigned atom_add_acq_rel(unsigned* p, unsigned v) {
+  unsigned old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
 }
 __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
   unsigned v;
@@ -1039,13 +1048,9 @@ __device__ bool attention_phase(const Ctx& c, int l, unsigned char* area, unsign
     // every thread's partial writes, then one arrival on the head's counter (monotonic within a
     // launch); the chunk that completes the head merges it
     __syncthreads();
-    if (tid == 0) {
-      __threadfence();
-      c.flag()[1] = atomicAdd(a.bar + 2 + kvh, 1u) == (unsigned)(l + 1) * (unsigned)nch - 1u;
-    }
+    if (tid == 0) c.flag()[1] = atom_add_acq_rel(a.bar + 2 + kvh, 1u) == (unsigned)(l + 1) * (unsigned)nch - 1u;
     __syncthreads();
     if (!c.flag()[1]) continue;
-    __threadfence();
     constexpr int GD = G * D;
     constexpr int CB = (2 * T * D * 2) / (GD * 4);  // chunk partials that fit over the K/V tiles
     float2* mls = reinterpret_cast<float2*>(area + AL::mls);  // [G][nch]
@@ -1194,10 +1199,8 @@ __global__ void __launch_bounds__(kMT, 1) mega_decode_kernel(const MegaArgs a) {
         stage_finish(c, K, Kp, gamma, a.eps, xs, xc, xraw);
       }
       ok = __syncthreads_and(gemv_phase<MOE>(c, s, l, ph, xs, xc, xraw, pos, sid));
-      if (ok && ph == kPhGU && threadIdx.x == 0) {  // this CTA's SwiGLU outputs are written
-        __threadfence();
+      if (ok && ph == kPhGU && threadIdx.x == 0)  // this CTA's SwiGLU outputs are written (barrier above)
         red_release_add(a.bar, 1u);
-      }
       if (ok && ph == kPhQKV) {
         // tile 0 of this CTA's first attention item (positions of earlier steps) streams in
         // while q, k and v arrive
