@@ -50,6 +50,15 @@ __device__ __forceinline__ void cp_async8(void* smem, const void* gmem) {
 }
 
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+// Add at GPU scope with acquire-release semantics; returns the old value.  After a CTA
+// barrier, one thread's release publishes every write the CTA made before the barrier (release
+// is cumulative); its acquire followed by a CTA barrier orders the other threads' later reads.
+__device__ __forceinline__ unsigned atom_add_acq_rel(unsigned* p, unsigned v) {
+  unsigned old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
 // Close the thread's current group of asynchronous copies; wait until at most N groups are
 // still in flight (the older ones complete first).
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }

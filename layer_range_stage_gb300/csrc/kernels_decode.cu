@@ -566,15 +566,13 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const AttnArg
   }
   if (tid < G) a.part_ml[(head0 + tid) * a.n_chunks + chunk] = make_float2(st_m[tid], st_l[tid]);
 
-  __threadfence();
-  __syncthreads();
+  __syncthreads();  // every partial write, then one acquire-release arrival (no separate fence)
   if (tid == 0) {
-    const int prev = atomicAdd(&a.counters[(size_t)t * a.Hkv + kvh], 1);
+    const int prev = (int)atom_add_acq_rel(reinterpret_cast<unsigned*>(&a.counters[(size_t)t * a.Hkv + kvh]), 1u);
     is_last = (prev == a.n_chunks - 1);
   }
   __syncthreads();
   if (!is_last) return;
-  __threadfence();
   // merge: chunk weights e^(m_c - M) per head, then the weighted sums in chunk order
   const int nch = a.n_chunks;
   const float* pbase = a.part_o + ((size_t)t * a.Hkv + kvh) * nch * (G * D);

@@ -547,24 +547,22 @@ __global__ void __launch_bounds__(kGThreads, 1)
 #pragma unroll
       for (int i = 0; i < 32; ++i)
         if (t0 + i < M) a.ws[((size_t)split * kST + t0 + i) * N + row] = v[i];
-    __threadfence();
-    __syncthreads();
+    __syncthreads();  // every partial write, then one acquire-release arrival (no separate fence)
     if (tid == 0) {
-      const bool last = atomicAdd(a.tile_cnt + blockIdx.x, 1u) == (unsigned)splits - 1;
+      const bool last = atom_add_acq_rel(a.tile_cnt + blockIdx.x, 1u) == (unsigned)splits - 1;
       if (last) a.tile_cnt[blockIdx.x] = 0u;  // every split of the tile has arrived: ready for the next launch
       *last_flag = last;
     }
     __syncthreads();
     run = ok && *last_flag;
     if (run) {
-      __threadfence();
       if (warp < 8 && row < N) {  // split by split, the 32 tokens' partials in flight together
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = 0.f;
         for (int sp = 0; sp < splits; ++sp)
 #pragma unroll
           for (int i = 0; i < 32; ++i)
-            if (t0 + i < M) v[i] += a.ws[((size_t)sp * kST + t0 + i) * N + row];
+            if (t0 + i < M) v[i] += __ldcg(a.ws + ((size_t)sp * kST + t0 + i) * N + row);
       }
     }
   }
