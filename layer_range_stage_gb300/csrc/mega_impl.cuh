@@ -467,8 +467,8 @@ __device__ __forceinline__ bool poll_pair(const Ctx& c, const tagged_t* p, unsig
 // dst; entries whose index within a piece of `piece` entries is `valid` or more are never
 // written and read as zero.  n, piece and valid are even.  All entries are fetched at once with
 // asynchronous copies into `scratch` (shared memory, n tagged entries); the pairs not yet
-// carrying the tag are fetched again, all at once, round after round (one L2 round trip per
-// round).  n <= 128 kMT.  Returns false after a timed-out wait
+// carrying the tag are fetched again, all at once, pass after pass (one L2 round trip per
+// pass).  n <= 128 kMT.  Returns false after a timed-out wait
 // (error set); the caller makes the outcome CTA-uniform.
 __device__ bool gather_tagged(const Ctx& c, const tagged_t* src, int n, int piece, int valid, unsigned tag,
                               tagged_t* scratch, float* dst) {
@@ -488,7 +488,7 @@ __device__ bool gather_tagged(const Ctx& c, const tagged_t* src, int n, int piec
   while (true) {
     cp_async_wait_all();
     unsigned long long left = 0;
-    for (unsigned long long m = pending; m; m &= m - 1) {  // the pairs fetched in this round
+    for (unsigned long long m = pending; m; m &= m - 1) {  // the pairs fetched in this pass
       const int k = __ffsll((long long)m) - 1, i = threadIdx.x + kMT * k;
       const tagged_t w0 = scratch[2 * i], w1 = scratch[2 * i + 1];
       if (tag_of(w0) == tag && tag_of(w1) == tag) {
@@ -506,7 +506,7 @@ __device__ bool gather_tagged(const Ctx& c, const tagged_t* src, int n, int piec
       set_error(c);
       return false;
     }
-    pending = left;  // one more round: every missing pair fetched again at once
+    pending = left;  // one more pass: every missing pair fetched again at once
     for (unsigned long long m = pending; m; m &= m - 1) {
       const int i = threadIdx.x + kMT * (__ffsll((long long)m) - 1);
       cp_async16(scratch + 2 * i, src + 2 * i);
