@@ -57,9 +57,10 @@ __device__ __forceinline__ float dot16_u8(const uint4 w, const float4 x0, const 
 // each D_i an exact integer (|D_i| < 2^19) from four dp4a instructions on the weight words as
 // they are: no weight is converted.  Starting a dp4a chain at 0x4B400000 - 128 sum_j li_j makes
 // its result the float bits of 1.5 * 2^23 + D_i (exact while |D_i| < 2^22), so one FADD recovers
-// D_i as a float.  Beyond float32 accumulation the roundings are those of N_j (at most u / 2 per
-// input: relative 2^-23 of the chunk's largest input, where float32 keeps 2^-24) and of u
-// itself (relative 2^-24, the same for the whole chunk).
+// D_i as a float.  Beyond float32 accumulation the roundings are those of N_j, rint of the
+// float32 product h_j * (1/u) (at most u / 2 + 2^-24 |h_j| per input: below 1.51 * 2^-23 of the
+// chunk's largest input, where float32 keeps 2^-24), and of u itself (relative 2^-24, the same
+// for the whole chunk).
 constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
 
 __device__ __forceinline__ int dp4a_us(unsigned a, unsigned b, int c) {
