@@ -12,6 +12,8 @@ The per-function pins check each step alone; these check how Stage.forward compo
         x <- x + [mean_{j <= p} fp16(h_j)[kv(g)] for each q head g],  kv(g) = g // (Hq / Hkv),
     so a wrong head-to-group map, an off-by-one window or another sequence's rows show up.
     The result must not depend on W_k at all.
+  - a last stage with such an identity block and the readout W_head = I: the logits of a row
+    are its final features rmsnorm(x) * gamma_f followed by zeros.
 """
 import numpy as np
 
@@ -138,3 +140,26 @@ def test_the_closed_form_separates_the_plausible_mistakes():
     y1 = st1.forward(seq0, pos0, hidden_in=x).astype(np.float64)
     assert np.abs((y1 - x64) - right).max() <= 2e-3 * np.abs(right).max()
     assert got.shape == x.shape
+
+
+def test_last_stage_with_identity_blocks_and_readout_gives_the_normed_input_as_logits():
+    """A last stage whose block adds zero and whose readout is I (V x H, V > H): the final
+    features are rmsnorm(x) * gamma_f, the logits of a row are those features followed by
+    V - H zeros, and greedy picks the largest feature ([RFC] "What I found": the last stage
+    applies the norm and the readout)."""
+    lw = synth.layer_weights(CFG, 3, gamma_mode="seeded")
+    lw.wo = zero_q8(CFG.hidden, CFG.q_dim)
+    lw.w_down = zero_q8(CFG.hidden, CFG.ffn)
+    sw = synth.StageWeights(CFG, 3, 4, [lw], final_norm=synth.gamma(synth.DEFAULT_SEED, CFG, 0, 99, "seeded"),
+                            lm_head=eye_q8(CFG.vocab, CFG.hidden))
+    st = oracle.Stage(CFG, 3, 4, sw, max_seqs=1, max_len=32)
+    x = hidden(5, 5)
+    f = st.forward(np.zeros(5, int), np.arange(5), hidden_in=x)
+    x64 = x.astype(np.float64)
+    want = x64 / np.sqrt(np.mean(x64 * x64, axis=1, keepdims=True) + CFG.rms_eps) * sw.final_norm
+    assert np.abs(f - want).max() <= 1e-6 * np.abs(want).max()
+    rows = [4, 1]
+    lg = st.logits(rows)
+    assert lg.shape == (2, CFG.vocab) and not lg[:, CFG.hidden:].any()
+    assert np.array_equal(lg[:, :CFG.hidden], f[rows])
+    assert list(oracle.greedy(lg)) == [int(np.argmax(f[r])) for r in rows]
