@@ -425,10 +425,10 @@ __device__ void grid_leave(const Ctx& c) {
 }
 
 // A projection input from global memory (written earlier in this launch: read through L2)
-// into shared memory: normalised by RMSNorm with gamma when given, scaled by 2^64,
-// swizzled per 16-float chunk, with chunk sums.  With gamma the raw values land in xraw
-// (kept for the residual adds) and gamma in xs, which is then overwritten in place; without,
-// the raw values land in xs.  Every 16-byte piece is an asynchronous copy issued before any
+// into shared memory, for stage_finish to turn into the integer form of every 16-input chunk
+// (RMSNorm with gamma first, when given).  With gamma the raw values land in xraw (kept for
+// the residual adds) and gamma in xs, which is then overwritten in place; without, the raw
+// values land in xs.  Every 16-byte piece is an asynchronous copy issued before any
 // is waited for (stage_finish), so the staging costs one round trip to L2 and no registers.
 __device__ void stage_issue(const float* x, int K, int Kp, const float* gamma, float* xs, float* xraw) {
   const int tid = threadIdx.x;
@@ -557,8 +557,7 @@ __device__ bool stage_counted(const Ctx& c, const unsigned* counter, unsigned ta
 // The second half of the staging (after stage_issue and any other loads of the phase's setup):
 // wait for the copies, then RMSNorm and the integer form of every 16-input chunk (q8dot.cuh) in
 // place: 64 bytes per chunk, as many as its floats.
-__device__ void stage_finish(const Ctx& c, int K, int Kp, const float* gamma, float eps, float* xs, float* xc,
-                             float* xraw) {
+__device__ void stage_finish(const Ctx& c, int K, int Kp, const float* gamma, float eps, float* xs, float* xraw) {
   const int tid = threadIdx.x, nchunk = Kp >> 4;
   const float* raw = gamma ? xraw : xs;
   cp_async_wait_all();
@@ -726,7 +725,7 @@ __device__ void phase_setup(const Ctx& c, int ph, int pos) {
 // finished pair piece goes to finish_piece.  Returns false (for the whole warp) after a
 // timed-out wait (error set, copies drained); the caller makes the outcome CTA-uniform.
 template <bool MOE>
-__device__ bool gemv_phase(const Ctx& c, Stream& s, int l, int ph, const float* xs, const float* xc,
+__device__ bool gemv_phase(const Ctx& c, Stream& s, int l, int ph, const float* xs,
                            const float* xraw, int pos, int sid) {
   const Split& p = c.split()[ph];
   float acc0 = 0.f, acc1 = 0.f;
@@ -1117,12 +1116,10 @@ __global__ void __launch_bounds__(kMT, 1) mega_decode_kernel(const MegaArgs a) {
   float* xraw = reinterpret_cast<float*>(sm + kOffXraw);
   unsigned char* area = sm + off_u;  // union: projection input and warp partials, or attention tiles
   const int KpQ = pad256(a.Hq * a.D), KpF = pad256(a.F);
-  const int Kx = max(KpH, max(KpQ, KpF));
-  // the union area: the per-projection scratch, then the staged input and its chunk sums (a
-  // tagged input is gathered beyond the current projection's Kp), or the attention tiles
+  // the union area: the per-projection scratch, then the staged input (a tagged input is
+  // gathered beyond the current projection's Kp), or the attention tiles
   c.ps = area;
   float* xs = reinterpret_cast<float*>(area + kPsBytes);
-  float* xc = xs + Kx;
 
   if (threadIdx.x < kMW * kDepth + 1) mbar_init(c.bars() + threadIdx.x, 1);
   if (threadIdx.x == 0) {
@@ -1192,9 +1189,9 @@ __global__ void __launch_bounds__(kMT, 1) mega_decode_kernel(const MegaArgs a) {
                             reinterpret_cast<tagged_t*>(xs + Kp));
         }
         if (!ok) break;
-        stage_finish(c, K, Kp, gamma, a.eps, xs, xc, xraw);
+        stage_finish(c, K, Kp, gamma, a.eps, xs, xraw);
       }
-      ok = __syncthreads_and(gemv_phase<MOE>(c, s, l, ph, xs, xc, xraw, pos, sid));
+      ok = __syncthreads_and(gemv_phase<MOE>(c, s, l, ph, xs, xraw, pos, sid));
       if (ok && ph == kPhGU && threadIdx.x == 0)  // this CTA's SwiGLU outputs are written (barrier above)
         red_release_add(a.bar, 1u);
       if (ok && ph == kPhQKV) {
@@ -1232,10 +1229,10 @@ size_t mega_smem(int H, int q_dim, int F, int D, int G) {
                     : G == 4 ? AttnLayout<64, 4>::total : AttnLayout<64, 8>::total;
   else attn = G == 1 ? AttnLayout<128, 1>::total : G == 2 ? AttnLayout<128, 2>::total
             : G == 4 ? AttnLayout<128, 4>::total : AttnLayout<128, 8>::total;
-  // the staged input with its chunk sums, or a tagged input (H or q_dim entries of 8 bytes)
-  // gathered beyond the projection's Kp floats
+  // the staged input (the integer form: as many bytes as its floats), or a tagged input (H or
+  // q_dim entries of 8 bytes) gathered beyond the projection's Kp floats
   const size_t gather = std::max((size_t)pad256(H) * 4 + (size_t)H * 8, (size_t)pad256(q_dim) * 4 + (size_t)q_dim * 8);
-  const size_t u = std::max(kPsBytes + std::max((size_t)Kx * 4 + (size_t)(Kx / 16) * 4, gather), attn);
+  const size_t u = std::max(kPsBytes + std::max((size_t)Kx * 4, gather), attn);
   return off_u + u + 128;  // + alignment of the dynamic base
 }
 
