@@ -37,8 +37,10 @@ STAGE_API int stage_op_embed(const void* q_dev, const void* s_dev, int64_t rows,
  * h = x / sqrt(mean(x^2) + eps) * gamma when gamma_dev is not NULL (the RMSNorm that
  * precedes every projection of a block: "41. Many GPUs: tensor, pipeline, expert and
  * data parallelism", section "Pipeline parallelism").  W is a packed matrix
- * (stage_op_q8_pack).  x_dev: f32 [n_tok][cols]; y_dev: f32 [n_tok][rows].  Runs on
- * `stream` (a cudaStream_t); no allocation, no synchronisation. */
+ * (stage_op_q8_pack).  x_dev: f32 [n_tok][cols]; y_dev: f32 [n_tok][rows].  Every |h| must
+ * be below 2^64 (the dot product takes its inputs scaled by 2^64 in float32); float32
+ * rounding error, relative to sum_k (q + 128) |h_k| + 128 |sum_k h_k| per 16-input chunk.
+ * Runs on `stream` (a cudaStream_t); no allocation, no synchronisation. */
 STAGE_API int stage_op_gemv(const void* q_dev, const void* s_dev, int64_t rows, int64_t cols, const float* x_dev,
                             int n_tok, const float* gamma_dev, float eps, float* y_dev, void* stream);
 

@@ -6,9 +6,12 @@
 //   sum_j w_j x_j = s * (sum_j b_j x_j - 128 * X),   X = sum_j x_j (per 16-input chunk).
 // b_j is turned into a float without any arithmetic: the byte moved into an otherwise
 // zero word is the denormal b_j * 2^-149, exactly.  With inputs pre-scaled by 2^64 the
-// products b_j * x_j * 2^-85 are normal floats, so one FFMA per weight accumulates them
-// (IEEE denormal operands, no flush-to-zero); the chunk sum is rescaled by 2^85 (exact) and
-// corrected by -128 X in one FFMA, then multiplied by the block scale.
+// products b_j * x_j * 2^-85 are normal floats for |x_j| >= 2^-41, so one FFMA per weight
+// accumulates them (IEEE denormal operands, no flush-to-zero); the chunk sum is rescaled by
+// 2^85 (exact) and corrected by -128 X in one FFMA, then multiplied by the block scale.
+// Smaller inputs give denormal products, off by at most 2^-65 s each after the rescale; inputs
+// must stay below 2^64 in magnitude (the scaled input overflows there).  The error is float32
+// rounding measured against the biased magnitudes, sum_j b_j |x_j| + 128 |X|.
 #pragma once
 
 #include <stdint.h>
