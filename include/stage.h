@@ -25,7 +25,8 @@
  *
  * Conventions for every function below:
  *   - Return 0 (STAGE_OK) on success, a negative STAGE_E_* code on failure.  No
- *     C++ exception crosses this boundary.  stage_last_error() gives a message.
+ *     C++ exception crosses this boundary: a host allocation that fails inside a call
+ *     returns STAGE_E_HOST.  stage_last_error() gives a message.
  *   - After any error no committed sequence length changes; KV rows written by a
  *     failed or uncommitted call are simply overwritten by the retry.
  *   - Arrays named *_host are read on the host before the call returns; device
@@ -62,7 +63,9 @@ enum {
   STAGE_E_NOT_LAST = -6,     /* readout requested from a stage that does not own it */
   STAGE_E_CUDA = -7,         /* a CUDA runtime error; the message is in stage_last_error */
   STAGE_E_STATE = -8,        /* weights not loaded, or commit beyond what was written */
-  STAGE_E_INJECTED = -9      /* host-side fault injection (stage_debug_inject) */
+  STAGE_E_INJECTED = -9,     /* host-side fault injection (stage_debug_inject) */
+  STAGE_E_HOST = -10         /* a host allocation failed (a weight staging buffer, a table): no C++
+                                exception leaves the library; the message is in the last-error string */
 };
 
 typedef struct stage* stage_t;
@@ -72,8 +75,9 @@ typedef struct stage* stage_t;
  * partial).  shared_ffn (MoE only, 0 = none): width of a shared expert added to every
  * token's expert mix with weight sigmoid(shared_score . h) ("41. Many GPUs: tensor,
  * pipeline, expert and data parallelism", the MoE layer listings:
- * out + sigmoid(shared_gate(x)) * shared(x)); stages with one decode on the GEMV path.  max_seqs / max_seq_len size the KV cache; max_tokens bounds the
- * tokens of one prefill or decode call.  gemm_bf16_min_tokens: on dense models, calls
+ * out + sigmoid(shared_gate(x)) * shared(x)); stages with one decode on the GEMV path.
+ * n_layers is at most 65536.  max_seqs / max_seq_len size the KV cache (at most 65536
+ * and 2^24); max_tokens (at most 2^20) bounds the tokens of one prefill or decode call.  gemm_bf16_min_tokens: on dense models, calls
  * with at least this many tokens run their projections on the tensor cores (tcgen05)
  * with bf16 operands -- activations rounded to bf16, weights as bf16(f32(scale) * q) --
  * and f32 accumulation; smaller calls, and every call of a MoE model, use the float32
@@ -150,8 +154,9 @@ STAGE_API size_t stage_required_bytes(const stage_model_cfg* cfg, stage_layer_ra
  * device_budgets: host [n_devices] usable bytes per device.  bounds_out: host int32
  * [n_devices + 1], 0 = b[0] < b[1] < ... < b[n] = n_layers; stage k owns [b[k], b[k+1]).
  * required_out: host [n_devices] or NULL, each stage's stage_required_bytes.
- * Returns STAGE_OK, STAGE_E_INVALID (bad cfg or pointers, n_devices outside [1, n_layers]),
- * or STAGE_E_DOES_NOT_FIT (no legal placement). */
+ * Returns STAGE_OK, STAGE_E_INVALID (bad cfg or pointers, n_devices outside [1, n_layers],
+ * n_layers above 4096: the tables grow as n_layers^2), or STAGE_E_DOES_NOT_FIT (no legal
+ * placement). */
 STAGE_API int stage_plan_placement(const stage_model_cfg* cfg, int n_devices, const size_t* device_budgets,
                                    int32_t* bounds_out, size_t* required_out);
 

@@ -4,8 +4,9 @@
  * The two dominant steps of a stage forward, callable on their own with caller-owned
  * device buffers: the dequant-fused int8 block-32 GEMV and split-K grouped-query decode
  * attention.  These run the same kernels stage_decode launches.  Return codes are the
- * STAGE_* codes of stage.h; messages are read with stage_op_last_error().  All device
- * pointers must be 16-byte aligned.
+ * STAGE_* codes of stage.h (no C++ exception crosses this boundary: stage_op_q8_pack's host
+ * staging buffer that cannot be allocated gives STAGE_E_HOST); messages are read with
+ * stage_op_last_error().  All device pointers must be 16-byte aligned.
  */
 #ifndef LAYER_RANGE_STAGE_OPS_H
 #define LAYER_RANGE_STAGE_OPS_H

@@ -25,9 +25,10 @@ STAGE_E_NOT_LAST = -6
 STAGE_E_CUDA = -7
 STAGE_E_STATE = -8
 STAGE_E_INJECTED = -9
+STAGE_E_HOST = -10
 ERROR_NAMES = {0: "STAGE_OK", -1: "STAGE_E_INVALID", -2: "STAGE_E_DOES_NOT_FIT", -3: "STAGE_E_HANDOFF",
                -4: "STAGE_E_POSITION", -5: "STAGE_E_BUSY", -6: "STAGE_E_NOT_LAST", -7: "STAGE_E_CUDA",
-               -8: "STAGE_E_STATE", -9: "STAGE_E_INJECTED"}
+               -8: "STAGE_E_STATE", -9: "STAGE_E_INJECTED", -10: "STAGE_E_HOST"}
 
 
 class StageError(RuntimeError):

@@ -34,6 +34,17 @@ int op_err(int code, const char* fmt, ...) {
 
 int op_cuda(cudaError_t e, const char* where) { return op_err(STAGE_E_CUDA, "%s: %s", where, cudaGetErrorString(e)); }
 
+// A C++ exception inside an entry point (a host staging buffer that could not be allocated)
+// ends the call with STAGE_E_HOST instead of crossing the C ABI; recording the message may
+// itself fail, which is ignored.
+int host_failure(const char* what) noexcept {
+  try {
+    g_op_error = std::string("host: ") + what;
+  } catch (...) {
+  }
+  return STAGE_E_HOST;
+}
+
 bool aligned16(const void* p) { return ((uintptr_t)p & 15) == 0; }
 
 constexpr int kMaxDevices = 64;
@@ -75,15 +86,19 @@ extern "C" {
 
 const char* stage_op_last_error(void) { return g_op_error.c_str(); }
 
-int stage_op_q8_device_bytes(int64_t rows, int64_t cols, size_t* q_bytes, size_t* s_bytes) {
+int stage_op_q8_device_bytes(int64_t rows, int64_t cols, size_t* q_bytes, size_t* s_bytes) try {
   if (rows <= 0 || cols <= 0 || cols > (1 << 30) || !q_bytes || !s_bytes) return op_err(STAGE_E_INVALID, "bad shape");
   const int64_t kp = lrs::row_pad((int)cols);
   *q_bytes = (size_t)(rows * kp);
   *s_bytes = (size_t)(rows * (kp / 32) * 2);
   return STAGE_OK;
+} catch (const std::exception& ex) {
+  return host_failure(ex.what());
+} catch (...) {
+  return host_failure("unknown exception");
 }
 
-int stage_op_q8_pack(const stage_q8* host, void* q_dev, void* s_dev) {
+int stage_op_q8_pack(const stage_q8* host, void* q_dev, void* s_dev) try {
   if (!host || !host->q || !host->scale || !q_dev || !s_dev) return op_err(STAGE_E_INVALID, "null pointer");
   size_t qb = 0, sb = 0;
   if (int rc = stage_op_q8_device_bytes(host->rows, host->cols, &qb, &sb)) return rc;
@@ -98,10 +113,14 @@ int stage_op_q8_pack(const stage_q8* host, void* q_dev, void* s_dev) {
   cudaError_t e = cudaMemcpy(q_dev, q.data(), qb, cudaMemcpyHostToDevice);
   if (e == cudaSuccess) e = cudaMemcpy(s_dev, s.data(), sb, cudaMemcpyHostToDevice);
   return e == cudaSuccess ? STAGE_OK : op_cuda(e, "pack");
+} catch (const std::exception& ex) {
+  return host_failure(ex.what());
+} catch (...) {
+  return host_failure("unknown exception");
 }
 
 int stage_op_embed(const void* q_dev, const void* s_dev, int64_t rows, int64_t cols, const int32_t* tok_dev,
-                   int n_tok, float* out_dev, void* stream) {
+                   int n_tok, float* out_dev, void* stream) try {
   if (!q_dev || !s_dev || !tok_dev || !out_dev) return op_err(STAGE_E_INVALID, "null pointer");
   if (rows <= 0 || cols <= 0 || rows > (1 << 30) || cols > (1 << 24) || n_tok <= 0 || n_tok > 65535)
     return op_err(STAGE_E_INVALID, "bad shape");
@@ -117,10 +136,14 @@ int stage_op_embed(const void* q_dev, const void* s_dev, int64_t rows, int64_t c
   w.Kp = lrs::row_pad((int)cols);
   e = lrs::launch_embed(w, tok_dev, n_tok, out_dev, (int)cols, (cudaStream_t)stream);
   return e == cudaSuccess ? STAGE_OK : op_cuda(e, "embed");
+} catch (const std::exception& ex) {
+  return host_failure(ex.what());
+} catch (...) {
+  return host_failure("unknown exception");
 }
 
 int stage_op_gemv(const void* q_dev, const void* s_dev, int64_t rows, int64_t cols, const float* x_dev, int n_tok,
-                  const float* gamma_dev, float eps, float* y_dev, void* stream) {
+                  const float* gamma_dev, float eps, float* y_dev, void* stream) try {
   if (!q_dev || !s_dev || !x_dev || !y_dev) return op_err(STAGE_E_INVALID, "null pointer");
   if (rows <= 0 || cols <= 0 || rows > (1 << 30) || cols > (1 << 24) || n_tok <= 0)
     return op_err(STAGE_E_INVALID, "bad shape");
@@ -144,10 +167,14 @@ int stage_op_gemv(const void* q_dev, const void* s_dev, int64_t rows, int64_t co
   g.ldo = (int)rows;
   e = lrs::launch_gemv(g, (cudaStream_t)stream);
   return e == cudaSuccess ? STAGE_OK : op_cuda(e, "gemv");
+} catch (const std::exception& ex) {
+  return host_failure(ex.what());
+} catch (...) {
+  return host_failure("unknown exception");
 }
 
 int stage_op_gemm_bf16(const uint16_t* a_dev, int lda, int M, const void* q_dev, const void* s_dev, int64_t rows,
-                       int64_t cols, float* y_dev, void* stream) {
+                       int64_t cols, float* y_dev, void* stream) try {
   if (!a_dev || !q_dev || !s_dev || !y_dev) return op_err(STAGE_E_INVALID, "null pointer");
   if (M <= 0 || rows <= 0 || cols <= 0 || rows > (1 << 30) || cols > (1 << 24)) return op_err(STAGE_E_INVALID, "bad shape");
   const int kp = lrs::row_pad((int)cols);
@@ -169,6 +196,10 @@ int stage_op_gemm_bf16(const uint16_t* a_dev, int lda, int M, const void* q_dev,
   g.ldo = (int)rows;
   e = lrs::launch_gemm_tc(g, (cudaStream_t)stream);
   return e == cudaSuccess ? STAGE_OK : op_cuda(e, "gemm");
+} catch (const std::exception& ex) {
+  return host_failure(ex.what());
+} catch (...) {
+  return host_failure("unknown exception");
 }
 
 size_t stage_op_attention_workspace_bytes(int n_tok, int n_q_heads, int n_kv_heads, int head_dim, int n_chunks) {
@@ -182,7 +213,7 @@ size_t stage_op_attention_workspace_bytes(int n_tok, int n_q_heads, int n_kv_hea
 int stage_op_attention_decode(const float* q_dev, const uint16_t* k_cache_dev, const uint16_t* v_cache_dev,
                               const int32_t* seq_dev, const int32_t* pos_dev, int n_tok, int n_q_heads, int n_kv_heads,
                               int head_dim, int max_len, int n_chunks, float* out_dev, void* workspace_dev,
-                              size_t workspace_bytes, void* stream) {
+                              size_t workspace_bytes, void* stream) try {
   if (int rc = check_attention(q_dev, k_cache_dev, v_cache_dev, seq_dev, pos_dev, n_tok, n_q_heads, n_kv_heads, head_dim,
                                max_len, n_chunks, out_dev))
     return rc;
@@ -213,12 +244,16 @@ int stage_op_attention_decode(const float* q_dev, const uint16_t* k_cache_dev, c
   a.scale = (float)(1.0 / std::sqrt((double)head_dim));
   e = lrs::launch_attn_decode(a, (cudaStream_t)stream);
   return e == cudaSuccess ? STAGE_OK : op_cuda(e, "attention");
+} catch (const std::exception& ex) {
+  return host_failure(ex.what());
+} catch (...) {
+  return host_failure("unknown exception");
 }
 
 int stage_op_attention_decode_static(const float* q_dev, const uint16_t* k_cache_dev, const uint16_t* v_cache_dev,
                                      const int32_t* seq_dev, const int32_t* pos_dev, int n_tok, int n_q_heads,
                                      int n_kv_heads, int head_dim, int max_len, int n_chunks, float* out_dev,
-                                     void* stream) {
+                                     void* stream) try {
   if (int rc = check_attention(q_dev, k_cache_dev, v_cache_dev, seq_dev, pos_dev, n_tok, n_q_heads, n_kv_heads, head_dim,
                                max_len, n_chunks, out_dev))
     return rc;
@@ -236,6 +271,10 @@ int stage_op_attention_decode_static(const float* q_dev, const uint16_t* k_cache
   if (e != cudaSuccess) return op_cuda(e, "clear scratch counters");
   return stage_op_attention_decode(q_dev, k_cache_dev, v_cache_dev, seq_dev, pos_dev, n_tok, n_q_heads, n_kv_heads,
                                    head_dim, max_len, n_chunks, out_dev, scratch, STAGE_OP_STATIC_SCRATCH_BYTES, stream);
+} catch (const std::exception& ex) {
+  return host_failure(ex.what());
+} catch (...) {
+  return host_failure("unknown exception");
 }
 
 }  // extern "C"

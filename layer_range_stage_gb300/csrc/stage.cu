@@ -17,6 +17,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <limits>
+#include <memory>
 #include <mutex>
 #include <new>
 #include <string>
@@ -33,6 +34,8 @@ namespace {
 
 constexpr int kMaxChunks = lrs::kAttnMaxChunks;
 constexpr size_t kAlign = 256;
+constexpr int kMaxLayers = 1 << 16;    // blocks of a model: keeps every layer-count product in range
+constexpr int kMaxPlanLayers = 4096;   // the placement planner's tables grow as n_layers^2
 
 inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 inline int kpad(int k) { return lrs::row_pad(k); }
@@ -166,6 +169,7 @@ bool cfg_valid(const stage_model_cfg* c, stage_layer_range r, std::string* why) 
   if (c->n_layers <= 0 || c->hidden <= 0 || c->n_q_heads <= 0 || c->n_kv_heads <= 0 || c->head_dim <= 0 ||
       c->vocab <= 0)
     return bad("non-positive model dimension");
+  if (c->n_layers > kMaxLayers) return bad("n_layers too large (at most 65536)");
   if (c->n_q_heads % c->n_kv_heads) return bad("n_q_heads must be a multiple of n_kv_heads");
   // every GEMV input row is staged with 16-byte copies
   if (c->hidden % 4 || c->ffn % 4 || c->expert_ffn % 4) return bad("hidden, ffn and expert_ffn must be multiples of 4");
@@ -182,6 +186,17 @@ bool cfg_valid(const stage_model_cfg* c, stage_layer_range r, std::string* why) 
   if (!(c->rms_eps > 0.f) || !(c->rope_theta > 0.f)) return bad("rms_eps and rope_theta must be positive");
   if (r.begin < 0 || r.end > c->n_layers || r.begin >= r.end) return bad("layer range must satisfy 0 <= begin < end <= n_layers");
   return true;
+}
+
+// A C++ exception inside an entry point -- in practice a host allocation that failed (a weight
+// staging buffer, a table) -- ends the call with STAGE_E_HOST instead of crossing the C ABI.
+// Recording the message may itself fail; that is ignored.
+int host_failure(std::string* msg, const char* what) noexcept {
+  try {
+    if (msg) *msg = std::string("host: ") + what;
+  } catch (...) {
+  }
+  return STAGE_E_HOST;
 }
 
 }  // namespace
@@ -449,6 +464,17 @@ int load_endpoints(stage* st, const stage_weights* w) {
   }
   st->endpoints_loaded = true;
   return STAGE_OK;
+}
+
+// Weight uploads stage each matrix in a host buffer (up to the size of the readout); a failed
+// allocation there ends the upload with STAGE_E_HOST and leaves the stage usable.
+template <class F>
+int guarded_upload(stage* st, F&& f) {
+  try {
+    return f();
+  } catch (const std::exception& ex) {
+    return host_failure(&st->err, ex.what());
+  }
 }
 
 bool weights_ready(stage* st) {
@@ -924,16 +950,20 @@ int run_forward(stage* st, bool decode, int n, const int32_t* seq, const int32_t
 
 extern "C" {
 
-size_t stage_required_bytes(const stage_model_cfg* cfg, stage_layer_range range) {
+size_t stage_required_bytes(const stage_model_cfg* cfg, stage_layer_range range) try {
   if (!cfg_valid(cfg, range, nullptr)) return 0;
   return plan_bytes(*cfg, range.begin, range.end);
+} catch (const std::exception& ex) {
+  return 0;  // as for an invalid request
+} catch (...) {
+  return 0;
 }
 
 int stage_plan_placement(const stage_model_cfg* cfg, int n_devices, const size_t* device_budgets,
-                         int32_t* bounds_out, size_t* required_out) {
+                         int32_t* bounds_out, size_t* required_out) try {
   if (!cfg || !device_budgets || !bounds_out) return STAGE_E_INVALID;
   const int n = cfg->n_layers, S = n_devices;
-  if (S < 1 || S > n || !cfg_valid(cfg, stage_layer_range{0, n}, nullptr)) return STAGE_E_INVALID;
+  if (S < 1 || S > n || n > kMaxPlanLayers || !cfg_valid(cfg, stage_layer_range{0, n}, nullptr)) return STAGE_E_INVALID;
   // req[a][b]: bytes of a stage owning [a, b) (endpoints, KV and workspace included)
   std::vector<size_t> req((size_t)(n + 1) * (n + 1), 0);
   for (int a = 0; a < n; ++a)
@@ -968,10 +998,14 @@ int stage_plan_placement(const stage_model_cfg* cfg, int n_devices, const size_t
     b = a;
   }
   return STAGE_OK;
+} catch (const std::exception& ex) {
+  return host_failure(nullptr, ex.what());
+} catch (...) {
+  return host_failure(nullptr, "unknown exception");
 }
 
 int stage_create(const stage_model_cfg* cfg, stage_layer_range range, const stage_weights* weights,
-                 size_t device_budget_bytes, void* cuda_stream, stage_t* out) {
+                 size_t device_budget_bytes, void* cuda_stream, stage_t* out) try {
   if (!out) return STAGE_E_INVALID;
   *out = nullptr;
   std::string why;
@@ -1017,9 +1051,14 @@ int stage_create(const stage_model_cfg* cfg, stage_layer_range range, const stag
   st->last = range.end == cfg->n_layers;
   st->stream = (cudaStream_t)cuda_stream;
   cudaGetDevice(&st->device);
-  st->layers.resize(range.end - range.begin);
-  st->committed.assign(cfg->max_seqs, 0);
-  st->pending.assign(cfg->max_seqs, 0);
+  try {
+    st->layers.resize(range.end - range.begin);
+    st->committed.assign(cfg->max_seqs, 0);
+    st->pending.assign(cfg->max_seqs, 0);
+  } catch (const std::exception& ex) {
+    delete st;
+    return host_failure(&g_create_error, ex.what());
+  }
   cudaError_t e = cudaMalloc(&st->arena, need);
   if (e != cudaSuccess) {
     g_create_error = std::string("cudaMalloc: ") + cudaGetErrorString(e);
@@ -1042,14 +1081,19 @@ int stage_create(const stage_model_cfg* cfg, stage_layer_range range, const stag
   // RoPE table: cos/sin of pos * theta^(-2i/D), computed in double on the host
   if (e == cudaSuccess) {
     const int hd = cfg->head_dim / 2;
-    std::vector<float2> tab((size_t)cfg->max_seq_len * hd);
+    const size_t n_tab = (size_t)cfg->max_seq_len * hd;
+    std::unique_ptr<float2[]> tab(new (std::nothrow) float2[n_tab]);
+    if (!tab) {
+      stage_destroy(st);
+      return host_failure(&g_create_error, "RoPE table allocation failed");
+    }
     for (int p = 0; p < cfg->max_seq_len; ++p)
       for (int i = 0; i < hd; ++i) {
         const double inv = std::pow((double)cfg->rope_theta, -2.0 * i / cfg->head_dim);
         const double ang = (double)p * inv;
         tab[(size_t)p * hd + i] = make_float2((float)std::cos(ang), (float)std::sin(ang));
       }
-    e = cudaMemcpy(st->rope, tab.data(), tab.size() * sizeof(float2), cudaMemcpyHostToDevice);
+    e = cudaMemcpy(st->rope, tab.get(), n_tab * sizeof(float2), cudaMemcpyHostToDevice);
   }
   {
     const char* mg = getenv("LRS_PERSISTENT");
@@ -1067,10 +1111,10 @@ int stage_create(const stage_model_cfg* cfg, stage_layer_range range, const stag
     return STAGE_E_CUDA;
   }
   if (weights) {
-    int rc = load_endpoints(st, weights);
+    int rc = guarded_upload(st, [&] { return load_endpoints(st, weights); });
     for (int l = range.begin; !rc && l < range.end; ++l) {
       if (!weights->layers) rc = set_err(st, STAGE_E_INVALID, "null layers");
-      else rc = load_layer(st, l, &weights->layers[l - range.begin]);
+      else rc = guarded_upload(st, [&] { return load_layer(st, l, &weights->layers[l - range.begin]); });
     }
     if (rc) {
       g_create_error = st->err;
@@ -1080,36 +1124,56 @@ int stage_create(const stage_model_cfg* cfg, stage_layer_range range, const stag
   }
   *out = st;
   return STAGE_OK;
+} catch (const std::exception& ex) {
+  return host_failure(&g_create_error, ex.what());
+} catch (...) {
+  return host_failure(&g_create_error, "unknown exception");
 }
 
-int stage_load_layer(stage_t st, int global_layer, const stage_layer_w* w) {
+int stage_load_layer(stage_t st, int global_layer, const stage_layer_w* w) try {
   if (!st) return STAGE_E_INVALID;
   BusyGuard g(st);
   if (!g.ok) return set_err(st, STAGE_E_BUSY, "another call is in progress");
   return load_layer(st, global_layer, w);
+} catch (const std::exception& ex) {
+  return host_failure(st ? &st->err : nullptr, ex.what());
+} catch (...) {
+  return host_failure(st ? &st->err : nullptr, "unknown exception");
 }
 
-int stage_load_endpoints(stage_t st, const stage_weights* w) {
+int stage_load_endpoints(stage_t st, const stage_weights* w) try {
   if (!st) return STAGE_E_INVALID;
   BusyGuard g(st);
   if (!g.ok) return set_err(st, STAGE_E_BUSY, "another call is in progress");
   return load_endpoints(st, w);
+} catch (const std::exception& ex) {
+  return host_failure(st ? &st->err : nullptr, ex.what());
+} catch (...) {
+  return host_failure(st ? &st->err : nullptr, "unknown exception");
 }
 
 int stage_prefill(stage_t st, int n_tokens, const int32_t* seq_ids_host, const int32_t* positions_host,
-                  const int32_t* tokens_host, const stage_act* hidden_in, const stage_act* hidden_out) {
+                  const int32_t* tokens_host, const stage_act* hidden_in, const stage_act* hidden_out) try {
   if (!st) return STAGE_E_INVALID;
   BusyGuard g(st);
   if (!g.ok) return set_err(st, STAGE_E_BUSY, "another call is in progress");
   return run_forward(st, false, n_tokens, seq_ids_host, positions_host, tokens_host, hidden_in, hidden_out);
+} catch (const std::exception& ex) {
+  return host_failure(st ? &st->err : nullptr, ex.what());
+} catch (...) {
+  return host_failure(st ? &st->err : nullptr, "unknown exception");
 }
 
 int stage_decode(stage_t st, int batch, const int32_t* seq_ids_host, const int32_t* positions_host,
-                 const int32_t* tokens_host, const stage_act* hidden_in, const stage_act* hidden_out) {
+                 const int32_t* tokens_host, const stage_act* hidden_in, const stage_act* hidden_out) try {
   if (!st) return STAGE_E_INVALID;
   BusyGuard g(st);
   if (!g.ok) return set_err(st, STAGE_E_BUSY, "another call is in progress");
   return run_forward(st, true, batch, seq_ids_host, positions_host, tokens_host, hidden_in, hidden_out);
+} catch (const std::exception& ex) {
+  return host_failure(st ? &st->err : nullptr, ex.what());
+} catch (...) {
+  return host_failure(st ? &st->err : nullptr, "unknown exception");
 }
 
 static int logits_dev(stage* st, int n_rows, const int* d_rows, float* logits_out, int32_t* argmax_out,
@@ -1153,7 +1217,7 @@ static int logits_dev(stage* st, int n_rows, const int* d_rows, float* logits_ou
   return STAGE_OK;
 }
 
-int stage_logits(stage_t st, int n_rows, const int32_t* row_index_host, float* logits_out, int32_t* argmax_out) {
+int stage_logits(stage_t st, int n_rows, const int32_t* row_index_host, float* logits_out, int32_t* argmax_out) try {
   if (!st) return STAGE_E_INVALID;
   BusyGuard g(st);
   if (!g.ok) return set_err(st, STAGE_E_BUSY, "another call is in progress");
@@ -1169,9 +1233,13 @@ int stage_logits(stage_t st, int n_rows, const int32_t* row_index_host, float* l
   if (e == cudaSuccess) e = cudaEventRecord(st->staged, st->stream);
   if (e != cudaSuccess) return cuda_err(st, e, "rows");
   return logits_dev(st, n_rows, st->d_rows, logits_out, argmax_out, st->stream);
+} catch (const std::exception& ex) {
+  return host_failure(st ? &st->err : nullptr, ex.what());
+} catch (...) {
+  return host_failure(st ? &st->err : nullptr, "unknown exception");
 }
 
-int stage_commit(stage_t st, int n, const int32_t* seq_ids_host, const int32_t* new_len_host) {
+int stage_commit(stage_t st, int n, const int32_t* seq_ids_host, const int32_t* new_len_host) try {
   if (!st) return STAGE_E_INVALID;
   BusyGuard g(st);
   if (!g.ok) return set_err(st, STAGE_E_BUSY, "another call is in progress");
@@ -1185,9 +1253,13 @@ int stage_commit(stage_t st, int n, const int32_t* seq_ids_host, const int32_t* 
   }
   for (int i = 0; i < n; ++i) st->committed[seq_ids_host[i]] = new_len_host[i];
   return STAGE_OK;
+} catch (const std::exception& ex) {
+  return host_failure(st ? &st->err : nullptr, ex.what());
+} catch (...) {
+  return host_failure(st ? &st->err : nullptr, "unknown exception");
 }
 
-int stage_truncate(stage_t st, int seq_id, int len) {
+int stage_truncate(stage_t st, int seq_id, int len) try {
   if (!st) return STAGE_E_INVALID;
   BusyGuard g(st);
   if (!g.ok) return set_err(st, STAGE_E_BUSY, "another call is in progress");
@@ -1196,24 +1268,36 @@ int stage_truncate(stage_t st, int seq_id, int len) {
   st->committed[seq_id] = len;
   st->pending[seq_id] = len;
   return STAGE_OK;
+} catch (const std::exception& ex) {
+  return host_failure(st ? &st->err : nullptr, ex.what());
+} catch (...) {
+  return host_failure(st ? &st->err : nullptr, "unknown exception");
 }
 
-int stage_reset(stage_t st) {
+int stage_reset(stage_t st) try {
   if (!st) return STAGE_E_INVALID;
   BusyGuard g(st);
   if (!g.ok) return set_err(st, STAGE_E_BUSY, "another call is in progress");
   std::fill(st->committed.begin(), st->committed.end(), 0);
   std::fill(st->pending.begin(), st->pending.end(), 0);
   return STAGE_OK;
+} catch (const std::exception& ex) {
+  return host_failure(st ? &st->err : nullptr, ex.what());
+} catch (...) {
+  return host_failure(st ? &st->err : nullptr, "unknown exception");
 }
 
-int stage_committed_len(stage_t st, int seq_id, int* len_out) {
+int stage_committed_len(stage_t st, int seq_id, int* len_out) try {
   if (!st || !len_out || seq_id < 0 || seq_id >= st->cfg.max_seqs) return STAGE_E_INVALID;
   *len_out = st->committed[seq_id];
   return STAGE_OK;
+} catch (const std::exception& ex) {
+  return host_failure(st ? &st->err : nullptr, ex.what());
+} catch (...) {
+  return host_failure(st ? &st->err : nullptr, "unknown exception");
 }
 
-int stage_read_kv(stage_t st, int global_layer, int seq_id, int n_pos, uint16_t* k_host, uint16_t* v_host) {
+int stage_read_kv(stage_t st, int global_layer, int seq_id, int n_pos, uint16_t* k_host, uint16_t* v_host) try {
   if (!st) return STAGE_E_INVALID;
   BusyGuard g(st);
   if (!g.ok) return set_err(st, STAGE_E_BUSY, "another call is in progress");
@@ -1231,10 +1315,14 @@ int stage_read_kv(stage_t st, int global_layer, int seq_id, int n_pos, uint16_t*
       e = cudaMemcpy(v_host + (size_t)h * n_pos * row, st->vc + off, (size_t)n_pos * row * 2, cudaMemcpyDeviceToHost);
   }
   return e == cudaSuccess ? check_device_error(st) : cuda_err(st, e, "read kv");
+} catch (const std::exception& ex) {
+  return host_failure(st ? &st->err : nullptr, ex.what());
+} catch (...) {
+  return host_failure(st ? &st->err : nullptr, "unknown exception");
 }
 
 int stage_write_kv(stage_t st, int global_layer, int seq_id, int pos0, int n_pos, const uint16_t* k_host,
-                   const uint16_t* v_host) {
+                   const uint16_t* v_host) try {
   if (!st) return STAGE_E_INVALID;
   BusyGuard g(st);
   if (!g.ok) return set_err(st, STAGE_E_BUSY, "another call is in progress");
@@ -1258,12 +1346,20 @@ int stage_write_kv(stage_t st, int global_layer, int seq_id, int pos0, int n_pos
   if (e != cudaSuccess) return cuda_err(st, e, "write kv");
   st->pending[seq_id] = std::max(st->pending[seq_id], pos0 + n_pos);
   return STAGE_OK;
+} catch (const std::exception& ex) {
+  return host_failure(st ? &st->err : nullptr, ex.what());
+} catch (...) {
+  return host_failure(st ? &st->err : nullptr, "unknown exception");
 }
 
-int stage_gemm_mode(stage_t st, int n_tokens, int* mode_out) {
+int stage_gemm_mode(stage_t st, int n_tokens, int* mode_out) try {
   if (!st || !mode_out) return STAGE_E_INVALID;
   *mode_out = use_tc(st, n_tokens) ? 1 : (n_tokens == 1 && st->mega) ? 2 : 0;
   return STAGE_OK;
+} catch (const std::exception& ex) {
+  return host_failure(st ? &st->err : nullptr, ex.what());
+} catch (...) {
+  return host_failure(st ? &st->err : nullptr, "unknown exception");
 }
 
 const char* stage_last_error(stage_t st) { return st ? st->err.c_str() : "null stage"; }
@@ -1280,7 +1376,7 @@ void stage_destroy(stage_t st) {
   delete st;
 }
 
-int stage_debug_inject(stage_t st, int what, int value) {
+int stage_debug_inject(stage_t st, int what, int value) try {
   if (!st) return STAGE_E_INVALID;
   if (what == 1) {
     st->busy.store(value ? 1 : 0);
@@ -1295,6 +1391,10 @@ int stage_debug_inject(stage_t st, int what, int value) {
     return STAGE_OK;
   }
   return STAGE_E_INVALID;
+} catch (const std::exception& ex) {
+  return host_failure(st ? &st->err : nullptr, ex.what());
+} catch (...) {
+  return host_failure(st ? &st->err : nullptr, "unknown exception");
 }
 
 }  // extern "C"
@@ -1354,7 +1454,7 @@ struct AllBusy {
 
 extern "C" {
 
-int stage_pipeline_create(stage_t* stages, int n_stages, stage_pipeline_t* out) {
+int stage_pipeline_create(stage_t* stages, int n_stages, stage_pipeline_t* out) try {
   if (!out || !stages || n_stages <= 0) return STAGE_E_INVALID;
   *out = nullptr;
   const stage_model_cfg& c0 = stages[0]->cfg;
@@ -1384,11 +1484,15 @@ int stage_pipeline_create(stage_t* stages, int n_stages, stage_pipeline_t* out) 
   p->d_step = p->d_seq + 3 * c0.max_seqs;
   *out = p;
   return STAGE_OK;
+} catch (const std::exception& ex) {
+  return host_failure(nullptr, ex.what());
+} catch (...) {
+  return host_failure(nullptr, "unknown exception");
 }
 
 int stage_pipeline_step(stage_pipeline_t p, int is_prefill, int n_tokens, const int32_t* seq_ids_host,
                         const int32_t* positions_host, const int32_t* tokens_host, int n_rows,
-                        const int32_t* row_index_host, float* logits_out, int32_t* next_tokens_host) {
+                        const int32_t* row_index_host, float* logits_out, int32_t* next_tokens_host) try {
   if (!p) return STAGE_E_INVALID;
   AllBusy busy(p->stages);
   if (!busy.ok) return pset(p, STAGE_E_BUSY, "a stage of the pipeline is busy");
@@ -1459,10 +1563,14 @@ int stage_pipeline_step(stage_pipeline_t p, int is_prefill, int n_tokens, const 
     std::copy(s->committed.begin(), s->committed.end(), s->pending.begin());
   }
   return STAGE_OK;
+} catch (const std::exception& ex) {
+  return host_failure(p ? &p->err : nullptr, ex.what());
+} catch (...) {
+  return host_failure(p ? &p->err : nullptr, "unknown exception");
 }
 
 int stage_pipeline_generate(stage_pipeline_t p, int batch, const int32_t* seq_ids_host, const int32_t* first_tokens_host,
-                            int n_steps, int use_graph, int32_t* tokens_out_host) {
+                            int n_steps, int use_graph, int32_t* tokens_out_host) try {
   if (!p) return STAGE_E_INVALID;
   AllBusy busy(p->stages);
   if (!busy.ok) return pset(p, STAGE_E_BUSY, "a stage of the pipeline is busy");
@@ -1570,9 +1678,13 @@ int stage_pipeline_generate(stage_pipeline_t p, int batch, const int32_t* seq_id
       st->pending[seq_ids_host[i]] = st->committed[seq_ids_host[i]];
     }
   return STAGE_OK;
+} catch (const std::exception& ex) {
+  return host_failure(p ? &p->err : nullptr, ex.what());
+} catch (...) {
+  return host_failure(p ? &p->err : nullptr, "unknown exception");
 }
 
-int stage_pipeline_kernel_timing(stage_pipeline_t p, int enable) {
+int stage_pipeline_kernel_timing(stage_pipeline_t p, int enable) try {
   if (!p) return STAGE_E_INVALID;
   for (stage* st : p->stages) {
     if (enable && st->tev.empty()) {
@@ -1585,9 +1697,13 @@ int stage_pipeline_kernel_timing(stage_pipeline_t p, int enable) {
   if (p->graph) cudaGraphExecDestroy(p->graph);  // recapture with (or without) the event nodes
   p->graph = nullptr;
   return STAGE_OK;
+} catch (const std::exception& ex) {
+  return host_failure(p ? &p->err : nullptr, ex.what());
+} catch (...) {
+  return host_failure(p ? &p->err : nullptr, "unknown exception");
 }
 
-int stage_pipeline_kernel_time(stage_pipeline_t p, float* mean_us, int* count) {
+int stage_pipeline_kernel_time(stage_pipeline_t p, float* mean_us, int* count) try {
   if (!p || !mean_us || !count) return STAGE_E_INVALID;
   double sum = 0;
   int n = 0;
@@ -1603,13 +1719,21 @@ int stage_pipeline_kernel_time(stage_pipeline_t p, float* mean_us, int* count) {
   *count = n;
   *mean_us = n ? (float)(sum * 1000.0 / n) : 0.f;
   return STAGE_OK;
+} catch (const std::exception& ex) {
+  return host_failure(p ? &p->err : nullptr, ex.what());
+} catch (...) {
+  return host_failure(p ? &p->err : nullptr, "unknown exception");
 }
 
-int stage_pipeline_handoff_stats(stage_pipeline_t p, int boundary, int64_t* calls, int64_t* bytes) {
+int stage_pipeline_handoff_stats(stage_pipeline_t p, int boundary, int64_t* calls, int64_t* bytes) try {
   if (!p || boundary < 0 || boundary + 1 >= (int)p->stages.size() || !calls || !bytes) return STAGE_E_INVALID;
   *calls = p->calls[boundary];
   *bytes = p->bytes[boundary];
   return STAGE_OK;
+} catch (const std::exception& ex) {
+  return host_failure(p ? &p->err : nullptr, ex.what());
+} catch (...) {
+  return host_failure(p ? &p->err : nullptr, "unknown exception");
 }
 
 const char* stage_pipeline_last_error(stage_pipeline_t p) { return p ? p->err.c_str() : "null pipeline"; }

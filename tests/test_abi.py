@@ -95,3 +95,41 @@ def test_does_not_fit_is_per_device_not_summed():
     with pytest.raises(L.StageError) as e:
         L.stage_create(c, 0, 21, budget=s0 - 1, stream=0)
     assert e.value.code == L.STAGE_E_DOES_NOT_FIT
+
+
+def test_error_codes_of_the_header_and_the_binding_agree():
+    import re
+    text = open(os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "stage.h")).read()
+    codes = {name: int(val) for name, val in re.findall(r"\b(STAGE_(?:OK|E_[A-Z_]+))\s*=\s*(-?\d+)", text)}
+    assert codes["STAGE_OK"] == 0 and len(codes) >= 11
+    for name, val in codes.items():
+        assert getattr(L, name) == val, name
+        assert L.binding.ERROR_NAMES[val] == name
+
+
+def test_a_failed_host_allocation_returns_an_error_instead_of_escaping():
+    """A staging buffer of 2^62 bytes cannot be mapped in any 48- to 56-bit virtual address
+    space, so the allocation fails before any byte is touched; the entry point must return
+    STAGE_E_HOST (no C++ exception crosses the C ABI) and the library keeps working."""
+    lib = L.lib()
+    q = (ctypes.c_int8 * 32)()
+    s = (ctypes.c_uint16 * 1)()
+    h = L.binding.stage_q8(ctypes.cast(q, ctypes.c_void_p), ctypes.cast(s, ctypes.c_void_p), 1 << 42, 1 << 20)
+    qb, sb = L.stage_op_q8_device_bytes(1 << 42, 1 << 20)
+    assert qb == 1 << 62
+    rc = lib.stage_op_q8_pack(ctypes.byref(h), ctypes.c_void_p(16), ctypes.c_void_p(16))
+    assert rc == L.STAGE_E_HOST
+    assert lib.stage_op_last_error().decode().startswith("host:")
+    assert L.stage_op_q8_device_bytes(64, 100) == (64 * 256, 64 * 8 * 2)
+
+
+def test_layer_counts_beyond_the_limits_are_rejected_before_any_allocation():
+    m = synth.CONFIGS[0]
+    c = cfg_of(m)
+    c.n_layers = (1 << 16) + 1
+    assert L.stage_required_bytes(c, 0, 4) == 0
+    c.n_layers = 5000  # a valid model, but beyond the planner's 4096 blocks
+    assert L.stage_required_bytes(c, 0, 4) > 0
+    with pytest.raises(L.StageError) as e:
+        L.stage_plan_placement(c, [1 << 40, 1 << 40])
+    assert e.value.code == L.STAGE_E_INVALID
