@@ -14,6 +14,10 @@ The per-function pins check each step alone; these check how Stage.forward compo
     The result must not depend on W_k at all.
   - a last stage with such an identity block and the readout W_head = I: the logits of a row
     are its final features rmsnorm(x) * gamma_f followed by zeros.
+  - W_o = 0 with identity gate, twice-identity up and identity down: a block adds
+    silu(h) * 2h with h the FFN-normed residual, element by element.
+  - a MoE stage whose experts are all one SwiGLU equals the dense stage with it, whatever the
+    router selects.
 """
 import numpy as np
 
@@ -163,3 +167,75 @@ def test_last_stage_with_identity_blocks_and_readout_gives_the_normed_input_as_l
     assert lg.shape == (2, CFG.vocab) and not lg[:, CFG.hidden:].any()
     assert np.array_equal(lg[:, :CFG.hidden], f[rows])
     assert list(oracle.greedy(lg)) == [int(np.argmax(f[r])) for r in rows]
+
+
+def test_moe_stage_with_identical_experts_equals_the_dense_stage():
+    """Every expert holding the same gate/up/down: whatever the router picks, the renormalised
+    top-k weights sum to 1 over copies of one SwiGLU, so a MoE stage must return what the dense
+    stage with those matrices returns ("41. Many GPUs: tensor, pipeline, expert and data
+    parallelism", the MoE layer: top-k experts mixed with renormalised router weights).  The
+    router is seeded and random, so the selected experts differ from token to token."""
+    shape = dict(hidden=256, n_q_heads=4, n_kv_heads=2, head_dim=64, vocab=512)
+    moe = synth.reduced(synth.CONFIGS[2], 4, n_experts=8, top_k=2, expert_ffn=64, **shape)
+    dense = synth.reduced(synth.CONFIGS[0], 4, ffn=64, **shape)
+    layers_m, layers_d = [], []
+    for l in (1, 2):
+        lm = synth.layer_weights(moe, l, gamma_mode="seeded")
+        ld = synth.layer_weights(dense, l, gamma_mode="seeded")
+        for name in ("attn_norm", "ffn_norm", "wq", "wk", "wv", "wo"):
+            setattr(ld, name, getattr(lm, name))
+        lm.e_gate = [lm.e_gate[0]] * moe.n_experts
+        lm.e_up = [lm.e_up[0]] * moe.n_experts
+        lm.e_down = [lm.e_down[0]] * moe.n_experts
+        ld.w_gate, ld.w_up, ld.w_down = lm.e_gate[0], lm.e_up[0], lm.e_down[0]
+        layers_m.append(lm)
+        layers_d.append(ld)
+    x = hidden(6, 7)
+    sm = oracle.Stage(moe, 1, 3, synth.StageWeights(moe, 1, 3, layers_m), max_seqs=1, max_len=16)
+    sd = oracle.Stage(dense, 1, 3, synth.StageWeights(dense, 1, 3, layers_d), max_seqs=1, max_len=16)
+    ym = sm.forward(np.zeros(6, int), np.arange(6), hidden_in=x).astype(np.float64)
+    yd = sd.forward(np.zeros(6, int), np.arange(6), hidden_in=x).astype(np.float64)
+    assert np.abs(ym - yd).max() <= 1e-6 * np.abs(yd).max()
+    # the router does select different experts for different inputs
+    picks = {tuple(sorted(r[0])) for r in sm.route(0, oracle.f32(x))[0]}
+    assert len(picks) > 1
+
+
+def scaled_eye_q8(rows, cols, k):
+    m = eye_q8(rows, cols)
+    m.q[np.arange(min(rows, cols)), np.arange(min(rows, cols))] = k
+    return m
+
+
+def test_zero_attention_and_identity_ffn_give_the_swiglu_of_the_normed_input():
+    """W_o = 0 removes the attention half; W_gate = I, W_up = 2 I, W_down = I (exact int8 rows,
+    F > H so the extra gate/up rows are zero and silu(0) * 0 = 0) reduce the FFN half to
+        x <- x + silu(h) * 2 h,   h = x / sqrt(mean(x^2) + eps) * gamma_2,
+    element by element, block after block ("41. Many GPUs: tensor, pipeline, expert and data
+    parallelism", section "Pipeline parallelism": add_norm, then the MLP on the normed
+    residual).  Gate and up swapped would give silu(2h) * h; the attention norm's gain in
+    place of gamma_2, or a lost residual, fail too."""
+    layers = []
+    for l in (1, 2):
+        lw = synth.layer_weights(CFG, l, gamma_mode="seeded")
+        lw.wo = zero_q8(CFG.hidden, CFG.q_dim)
+        lw.w_gate = eye_q8(CFG.ffn, CFG.hidden)
+        lw.w_up = scaled_eye_q8(CFG.ffn, CFG.hidden, 2)
+        lw.w_down = eye_q8(CFG.hidden, CFG.ffn)
+        layers.append(lw)
+    assert CFG.ffn > CFG.hidden
+    st = stage(layers)
+    x = hidden(5, 8)
+    y = st.forward(np.zeros(5, int), np.arange(5), hidden_in=x).astype(np.float64)
+    want = x.astype(np.float64)
+    for lw in layers:
+        h = (want / np.sqrt(np.mean(want * want, axis=1, keepdims=True) + CFG.rms_eps) * lw.ffn_norm)
+        h = h.astype(np.float32).astype(np.float64)
+        a = (h / (1.0 + np.exp(-h)) * 2.0 * h).astype(np.float32).astype(np.float64)
+        want = (want + a).astype(np.float32).astype(np.float64)
+    assert np.abs(y - want).max() <= 1e-5 * np.abs(want).max()
+    swapped = x.astype(np.float64)
+    for lw in layers:
+        h = swapped / np.sqrt(np.mean(swapped * swapped, axis=1, keepdims=True) + CFG.rms_eps) * lw.ffn_norm
+        swapped = swapped + 2.0 * h / (1.0 + np.exp(-2.0 * h)) * h
+    assert np.abs(want - swapped).max() > 100 * 1e-5 * np.abs(want).max()
