@@ -18,6 +18,8 @@ The per-function pins check each step alone; these check how Stage.forward compo
     silu(h) * 2h with h the FFN-normed residual, element by element.
   - a MoE stage whose experts are all one SwiGLU equals the dense stage with it, whatever the
     router selects.
+  - the identity FFN with the GEMMs in bf16: exactly the bf16 roundings of h and of the SwiGLU
+    output, nothing else.
 """
 import numpy as np
 
@@ -239,3 +241,38 @@ def test_zero_attention_and_identity_ffn_give_the_swiglu_of_the_normed_input():
         h = swapped / np.sqrt(np.mean(swapped * swapped, axis=1, keepdims=True) + CFG.rms_eps) * lw.ffn_norm
         swapped = swapped + 2.0 * h / (1.0 + np.exp(-2.0 * h)) * h
     assert np.abs(want - swapped).max() > 100 * 1e-5 * np.abs(want).max()
+
+
+def bf16_round(v):
+    u = np.asarray(v, np.float32).view(np.uint32).astype(np.uint64)
+    r = ((u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000).astype(np.uint32)
+    return r.view(np.float32).astype(np.float64)
+
+
+def test_bf16_mode_rounds_the_gemm_operands_of_the_identity_ffn():
+    """The same reduction with the stage's GEMMs in bf16 (prefill numerics): the GEMM operands
+    -- the normed input h and the SwiGLU output a -- are rounded to bf16 (ties to even), the
+    weights (0, 1, 2) are exact, and the residual stays float32:
+        x <- x + bf16(f32(silu(bf16(h)) * 2 bf16(h)))."""
+    layers = []
+    for l in (1, 2):
+        lw = synth.layer_weights(CFG, l, gamma_mode="seeded")
+        lw.wo = zero_q8(CFG.hidden, CFG.q_dim)
+        lw.w_gate = eye_q8(CFG.ffn, CFG.hidden)
+        lw.w_up = scaled_eye_q8(CFG.ffn, CFG.hidden, 2)
+        lw.w_down = eye_q8(CFG.hidden, CFG.ffn)
+        layers.append(lw)
+    st = stage(layers)
+    x = hidden(5, 9)
+    y = st.forward(np.zeros(5, int), np.arange(5), hidden_in=x, gemm="bf16").astype(np.float64)
+    want = x.astype(np.float64)
+    unrounded = x.astype(np.float64)
+    for lw in layers:
+        h = (want / np.sqrt(np.mean(want * want, axis=1, keepdims=True) + CFG.rms_eps) * lw.ffn_norm)
+        hb = bf16_round(h.astype(np.float32))
+        a = (hb / (1.0 + np.exp(-hb)) * 2.0 * hb).astype(np.float32)
+        want = (want + bf16_round(a)).astype(np.float32).astype(np.float64)
+        h2 = unrounded / np.sqrt(np.mean(unrounded * unrounded, axis=1, keepdims=True) + CFG.rms_eps) * lw.ffn_norm
+        unrounded = unrounded + h2 / (1.0 + np.exp(-h2)) * 2.0 * h2
+    assert np.abs(y - want).max() <= 1e-6 * np.abs(want).max()
+    assert np.abs(unrounded - want).max() > 1e-4 * np.abs(want).max()  # the roundings are visible
