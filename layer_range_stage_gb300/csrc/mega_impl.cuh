@@ -239,7 +239,7 @@ struct Ctx {
 
 // The projections of a block: weights of phase ph.
 template <bool MOE>
-__device__ __forceinline__ const DevQ8& phase_w(const MegaLayer& L, int ph) {
+__host__ __device__ __forceinline__ const DevQ8& phase_w(const MegaLayer& L, int ph) {
   if (MOE && ph == kPhRouter) return L.router;
   if (MOE && ph >= kPhGU) return ph == kPhGU ? L.egu : L.edown;
   return ph == kPhQKV ? L.wqkv : ph == kPhO ? L.wo : ph == kPhGU ? L.wgu : L.wdown;
@@ -247,8 +247,9 @@ __device__ __forceinline__ const DevQ8& phase_w(const MegaLayer& L, int ph) {
 
 // ph: kPhQKV, kPhO, kPhRouter (MoE stages: one logit per row, into global memory), kPhGU
 // (dense, or the selected experts' rows), kPhDown (dense, or gathered over the experts).
-// Computed once per launch (from block 0: every block has the same shapes).
-__device__ Split split_of(const MegaArgs& a, int ph, int cta, int G) {
+// Computed once per launch (from block 0: every block has the same shapes).  Host-callable too,
+// so that its cover of every pair and slot is checked on the host for every shape.
+__host__ __device__ Split split_of(const MegaArgs& a, int ph, int cta, int G) {
   const MegaLayer& L = a.layers[0];
   const bool moe = a.n_experts > 0;
   Split p;
@@ -287,7 +288,7 @@ __device__ Split split_of(const MegaArgs& a, int ph, int cta, int G) {
 }
 
 // The cursor of warp w's first slot in projection p (valid while w + 16 m < ng).
-__device__ __forceinline__ Cur cur_start(const Split& p, int w) {
+__host__ __device__ __forceinline__ Cur cur_start(const Split& p, int w) {
   Cur q;
   q.m = 0;
   q.r = 0;
@@ -297,13 +298,13 @@ __device__ __forceinline__ Cur cur_start(const Split& p, int w) {
   return q;
 }
 
-__device__ __forceinline__ bool cur_valid(const Split& p, const Cur& q, int w) { return w + kMW * q.m < p.ng; }
+__host__ __device__ __forceinline__ bool cur_valid(const Split& p, const Cur& q, int w) { return w + kMW * q.m < p.ng; }
 
 // First column and columns of slot j of a pair.
-__device__ __forceinline__ int slot_k(const Split& p, int j) { return j * p.sl; }
-__device__ __forceinline__ int slot_len(const Split& p, int j) { return min(p.sl, p.Kp - j * p.sl); }
+__host__ __device__ __forceinline__ int slot_k(const Split& p, int j) { return j * p.sl; }
+__host__ __device__ __forceinline__ int slot_len(const Split& p, int j) { return min(p.sl, p.Kp - j * p.sl); }
 
-__device__ __forceinline__ void cur_advance(const Split& p, Cur& q) {
+__host__ __device__ __forceinline__ void cur_advance(const Split& p, Cur& q) {
   if (++q.r < p.gs) {  // the next slot of a whole-pair group
     ++q.j;
     return;
