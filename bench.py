@@ -514,6 +514,22 @@ def cpu_baseline_one_thread(budget_s):
         return {"error": str(e)[:200]}
 
 
+def oracle_sample_stage(max_new):
+    """The oracle over 2 of the 32 blocks of the dense 8B shape (the first two, so it embeds and
+    reads out), its KV filled with seeded fp16 values up to the decode context (the oracle's
+    time does not depend on their values), room for max_new more tokens."""
+    import oracle
+    model = synth.CONFIGS[CFG_ID]
+    n_blk = 2
+    sub = synth.reduced(model, n_blk)
+    w = synth.stage_weights(sub, 0, n_blk)
+    st = oracle.Stage(sub, 0, n_blk, w, max_len=CONTEXT + max_new)
+    rng = np.random.default_rng(0)
+    st.k_cache[:] = rng.standard_normal(st.k_cache.shape).astype(np.float16)
+    st.v_cache[:] = rng.standard_normal(st.v_cache.shape).astype(np.float16)
+    return model, n_blk, st
+
+
 def cpu_baseline(args, budget_s=None, one_thread_child=False):
     """The oracle as it stands, on a bounded sample: decode tokens through 2 of the 32
     blocks at context 2048 (KV filled with seeded fp16 values; the oracle's time does not
@@ -521,18 +537,10 @@ def cpu_baseline(args, budget_s=None, one_thread_child=False):
     have passed, plus one readout; the mean block time is scaled to the 32-block token.
     Reported with the core count, the CPU model, the BLAS thread count and (unless this is
     the one-thread child) the same sample on one thread."""
-    import oracle
     if budget_s is None:
         budget_s = getattr(args, "cpu_budget", 12.0)
-    model = synth.CONFIGS[CFG_ID]
-    n_blk = 2
+    model, n_blk, st = oracle_sample_stage(max_new=64)
     cores = os.cpu_count()
-    sub = synth.reduced(model, n_blk)
-    w = synth.stage_weights(sub, 0, n_blk)
-    st = oracle.Stage(sub, 0, n_blk, w, max_len=CONTEXT + 64)
-    rng = np.random.default_rng(0)
-    st.k_cache[:] = rng.standard_normal(st.k_cache.shape).astype(np.float16)
-    st.v_cache[:] = rng.standard_normal(st.v_cache.shape).astype(np.float16)
     t_blocks, n_tok = 0.0, 0
     while n_tok < 2 or (t_blocks < budget_s and n_tok < 60):
         t0 = time.perf_counter()
@@ -555,18 +563,38 @@ def cpu_baseline(args, budget_s=None, one_thread_child=False):
 
 
 def run_reference(args):
-    """The reference arm: the oracle on the host cores; under a multi-process launch rank 0
-    alone runs it and prints, the other ranks leave without work."""
+    """The reference arm: the oracle as it stands on the host cores, in steps like the GPU arm's:
+    W untimed decode tokens, then K timed ones.  A step is one decode token at context 2048 on
+    a bounded sample of the workload -- 2 of the 32 blocks, their time scaled to 32 -- plus that
+    token's readout.  Under a multi-process launch rank 0 alone runs it and prints; the other
+    ranks leave without work."""
     rank, world, _ = dist_env()
     if rank != 0:
         return
-    cb = cpu_baseline(args)
+    model, n_blk, st = oracle_sample_stage(max_new=args.warmup + args.steps)
+    scale = model.n_layers // n_blk
+    times = []
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        st.forward([0], [CONTEXT + i], tokens=[1 + i], cache_dequant=False)
+        t1 = time.perf_counter()
+        st.logits()
+        t2 = time.perf_counter()
+        if i >= args.warmup:
+            times.append((t1 - t0) * scale + (t2 - t1))
+    per_step = sum(times) / len(times)
+    value = round(1.0 / per_step, 5)
+    cb = {"value": value, "unit": "tok/s", "cores": os.cpu_count(), "threads": blas_threads(),
+          "cpu_model": cpu_model(), "kind": "oracle",
+          "sample": f"{args.steps} timed decode tokens (after {args.warmup} untimed) at context {CONTEXT}.. through "
+                    f"{n_blk} of {model.n_layers} blocks, block time scaled x{scale}, each with its readout"}
     line = {"impl": "reference", "metric": "decode tok/s",
-            "value": cb["value"], "unit": "tok/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+            "value": value, "unit": "tok/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(per_step * 1e3, 1),
+            "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": WORKLOADS[1]["name"]},
-            "cpu_baseline": cb, "e2e": {"value": cb["value"], "unit": "tok/s", "h2d_bytes_per_step": 0,
+            "cpu_baseline": cb, "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0,
                                         "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
