@@ -45,3 +45,21 @@ def test_batched_70b_workload_recipe():
     per = (m.q_dim + 2 * m.kv_dim) * H + H * m.q_dim + 3 * m.ffn * H
     assert per == 855_638_016
     assert per * m.n_layers + m.vocab * H == 69_501_714_432
+
+
+def test_clock_record_from_sampled_rows():
+    """The clocks record of a timed region from nvidia-smi rows (sm, max sm, then the
+    hw_slowdown, hw_thermal_slowdown, sw_thermal_slowdown and sw_power_cap states): the median
+    SM clock under load, the highest max clock, every reason seen Active (never 'Not Active'),
+    and rows with unreadable numbers skipped."""
+    import bench
+    cs = bench.ClockSampler()
+    cs.samples = [["2070", "2070", "Not Active", "Not Active", "Not Active", "Not Active"],
+                  ["1965", "2070", "Not Active", "Not Active", "Not Active", "Active"],
+                  ["2055", "2070", "Not Active", "Not Active", "Not Active", "Not Active"],
+                  ["[N/A]", "[N/A]", "Not Active", "Active", "Not Active", "Not Active"]]
+    rec = cs.stop()
+    assert rec["sm_mhz"] == 2055.0 and rec["sm_max_mhz"] == 2070.0
+    assert rec["reasons"] == ["hw_thermal_slowdown", "sw_power_cap"]
+    assert rec["samples"] == 4
+    assert bench.ClockSampler().stop() == {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
