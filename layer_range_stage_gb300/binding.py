@@ -344,6 +344,14 @@ def stage_gemm_mode(st, n_tokens: int) -> int:
     return v.value
 
 
+def stage_last_error(st) -> str:
+    return lib().stage_last_error(st).decode()
+
+
+def stage_create_error() -> str:
+    return lib().stage_create_error().decode()
+
+
 def stage_destroy(st) -> None:
     lib().stage_destroy(st)
 
@@ -402,11 +410,19 @@ def stage_pipeline_kernel_time(p):
     return m.value, n.value
 
 
+def stage_pipeline_last_error(p) -> str:
+    return lib().stage_pipeline_last_error(p).decode()
+
+
 def stage_pipeline_destroy(p) -> None:
     lib().stage_pipeline_destroy(p)
 
 
 # ----------------------------------------------------------------------------- kernel-level entry points
+
+def stage_op_last_error() -> str:
+    return lib().stage_op_last_error().decode()
+
 
 def _opcheck(rc):
     if rc != STAGE_OK:

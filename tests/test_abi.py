@@ -133,3 +133,12 @@ def test_layer_counts_beyond_the_limits_are_rejected_before_any_allocation():
     with pytest.raises(L.StageError) as e:
         L.stage_plan_placement(c, [1 << 40, 1 << 40])
     assert e.value.code == L.STAGE_E_INVALID
+
+
+def test_binding_has_every_entry_point_under_its_c_name():
+    from layer_range_stage_gb300 import binding as B
+    for name in L.declared_symbols():
+        assert callable(getattr(B, name, None)), name
+        assert name in B._SIGS, name
+    assert B.stage_create_error() == "" or isinstance(B.stage_create_error(), str)
+    assert isinstance(B.stage_op_last_error(), str)
