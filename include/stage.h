@@ -171,10 +171,15 @@ STAGE_API int stage_plan_placement(const stage_model_cfg* cfg, int n_devices, co
 STAGE_API int stage_create(const stage_model_cfg* cfg, stage_layer_range range, const stage_weights* weights,
                  size_t device_budget_bytes, void* cuda_stream, stage_t* out);
 
-/* Import the weights of one owned block (global index in [begin, end)). */
+/* Import the weights of one owned block (global index in [begin, end)), copied from the
+ * host (the caller may free them after return; synchronous).  Errors: STAGE_E_INVALID (block
+ * not owned, a null or mis-shaped matrix), STAGE_E_BUSY, STAGE_E_HOST (the host staging
+ * buffer of a matrix), STAGE_E_CUDA.  A failed import leaves the block unloaded, so a
+ * forward returns STAGE_E_STATE until it is imported again. */
 STAGE_API int stage_load_layer(stage_t st, int global_layer, const stage_layer_w* w);
 
-/* Import the embedding (first stage) and/or final norm + readout (last stage). */
+/* Import the embedding (first stage) and/or final norm + readout (last stage), with the
+ * errors of stage_load_layer (STAGE_E_INVALID for a missing endpoint the stage owns). */
 STAGE_API int stage_load_endpoints(stage_t st, const stage_weights* w);
 
 /* Prefill / refill: n_tokens tokens, possibly of several sequences.  For each
@@ -184,35 +189,52 @@ STAGE_API int stage_load_endpoints(stage_t st, const stage_weights* w);
  * hidden_in [n_tokens x hidden].  hidden_out [n_tokens x hidden] receives the
  * residual stream (last stage: the final features rmsnorm(x) * gamma_f); it may be
  * the same buffer as hidden_in.  K/V of every token are written to the cache;
- * attention is causal within each sequence. */
+ * attention is causal within each sequence.  Nothing is published: stage_commit does that.
+ * Errors, all before any launch unless noted: STAGE_E_STATE (weights not all loaded),
+ * STAGE_E_INVALID (n_tokens outside [1, max_tokens], a seq_id outside [0, max_seqs), a
+ * token outside [0, vocab)), STAGE_E_HANDOFF (tokens on a later stage or a hidden on the
+ * first, a missing input, hidden shapes other than [n_tokens x hidden]), STAGE_E_POSITION
+ * (positions not committed_len + i per sequence, or reaching max_seq_len), STAGE_E_BUSY,
+ * STAGE_E_INJECTED, STAGE_E_CUDA (a launch failed, or a persistent launch's bounded wait ran
+ * out; the retry overwrites the uncommitted rows). */
 STAGE_API int stage_prefill(stage_t st, int n_tokens, const int32_t* seq_ids_host, const int32_t* positions_host,
                   const int32_t* tokens_host, const stage_act* hidden_in, const stage_act* hidden_out);
 
 /* Decode: one token for each of `batch` distinct sequences, at position
- * committed_len[seq].  Same conventions as stage_prefill. */
+ * committed_len[seq].  Same conventions and errors as stage_prefill, and STAGE_E_INVALID
+ * when batch exceeds max_seqs. */
 STAGE_API int stage_decode(stage_t st, int batch, const int32_t* seq_ids_host, const int32_t* positions_host,
                  const int32_t* tokens_host, const stage_act* hidden_in, const stage_act* hidden_out);
 
 /* Readout of the last stage for rows row_index_host[0..n_rows) of its last forward:
  * logits = W_head * features.  logits_out: device f32 [n_rows x vocab] or NULL;
- * argmax_out: device int32 [n_rows] or NULL (greedy token, lowest index on ties). */
+ * argmax_out: device int32 [n_rows] or NULL (greedy token, lowest index on ties).
+ * Errors: STAGE_E_NOT_LAST (a stage without the readout), STAGE_E_INVALID (n_rows outside
+ * [1, max_tokens], a row outside the last forward's tokens), STAGE_E_BUSY, STAGE_E_CUDA. */
 STAGE_API int stage_logits(stage_t st, int n_rows, const int32_t* row_index_host, float* logits_out, int32_t* argmax_out);
 
 /* Publish the written rows: committed_len[seq_ids[i]] = new_len[i].  new_len must
- * lie between the committed length and the highest position written since. */
+ * lie between the committed length and the highest position written since.  All or
+ * nothing: STAGE_E_INVALID (null arrays, a seq_id outside [0, max_seqs)) or STAGE_E_STATE
+ * (a length outside that window) changes no length; STAGE_E_BUSY. */
 STAGE_API int stage_commit(stage_t st, int n, const int32_t* seq_ids_host, const int32_t* new_len_host);
 
-/* Truncate one sequence to len <= committed_len (later rows are overwritten). */
+/* Truncate one sequence to len <= committed_len (later rows are overwritten).  Errors:
+ * STAGE_E_INVALID (seq_id), STAGE_E_POSITION (len outside [0, committed_len]), STAGE_E_BUSY. */
 STAGE_API int stage_truncate(stage_t st, int seq_id, int len);
 
-/* Forget every sequence (committed lengths to 0). */
+/* Forget every sequence (committed lengths to 0).  Errors: STAGE_E_BUSY. */
 STAGE_API int stage_reset(stage_t st);
 
+/* The committed length of one sequence into *len_out.  STAGE_E_INVALID for a null stage or
+ * pointer, or a seq_id outside [0, max_seqs). */
 STAGE_API int stage_committed_len(stage_t st, int seq_id, int* len_out);
 
 /* Copy the cached K and V of one owned block and sequence to the host: positions
  * [0, n_pos) of every KV head, fp16 bit patterns, each [n_kv_heads x n_pos x head_dim].
- * Synchronises the stage's stream.  For inspection and equivalence checks. */
+ * Synchronises the stage's stream.  For inspection and equivalence checks.  Errors:
+ * STAGE_E_INVALID (block not owned, seq_id, n_pos outside [0, max_seq_len], null buffers),
+ * STAGE_E_BUSY, STAGE_E_CUDA (including an error word left by an earlier launch). */
 STAGE_API int stage_read_kv(stage_t st, int global_layer, int seq_id, int n_pos, uint16_t* k_host, uint16_t* v_host);
 
 /* Copy K and V rows from the host into the cache of one owned block and sequence:
@@ -221,7 +243,9 @@ STAGE_API int stage_read_kv(stage_t st, int global_layer, int seq_id, int n_pos,
  * saved with stage_read_kv, or for starting from a given cache.  pos0 may not leave a gap
  * after the positions already written (STAGE_E_POSITION); the rows count as written, so a
  * following stage_commit of the sequence up to pos0 + n_pos publishes them, jointly with
- * the other stages.  Synchronises the stage's stream. */
+ * the other stages.  Synchronises the stage's stream.  Errors: STAGE_E_INVALID (block not
+ * owned, seq_id, negative pos0 or n_pos, null buffers), STAGE_E_POSITION (past max_seq_len,
+ * or a gap), STAGE_E_BUSY, STAGE_E_CUDA. */
 STAGE_API int stage_write_kv(stage_t st, int global_layer, int seq_id, int pos0, int n_pos, const uint16_t* k_host,
                              const uint16_t* v_host);
 
@@ -235,14 +259,19 @@ STAGE_API int stage_write_kv(stage_t st, int global_layer, int seq_id, int pos0,
  * stage_create, turns mode 2 off.  LRS_PDL=0, also read at stage_create, launches the
  * per-kernel paths (modes 0 and 1) without programmatic dependent launch: each kernel then
  * starts only after its predecessor on the stream has finished, instead of overlapping its
- * weight-only prologue with the predecessor's tail (process-wide; for measurement). */
+ * weight-only prologue with the predecessor's tail (process-wide; for measurement).
+ * STAGE_E_INVALID for a null stage or pointer. */
 STAGE_API int stage_gemm_mode(stage_t st, int n_tokens, int* mode_out);
 
+/* Message of the stage's last failed call ("" if none; "null stage" for NULL).  Owned by the
+ * stage, valid until its next call. */
 STAGE_API const char* stage_last_error(stage_t st);
 
 /* Message of the last failed stage_create on the calling thread ("" if none). */
 STAGE_API const char* stage_create_error(void);
 
+/* Wait for the stage's stream, then free its device memory, pinned staging and events.
+ * NULL is accepted.  Buffers the caller owns (hidden activations, logits) are untouched. */
 STAGE_API void stage_destroy(stage_t st);
 
 /* Host-side fault injection for tests (no GPU fault is ever caused):
@@ -265,7 +294,9 @@ STAGE_API int stage_debug_inject(stage_t st, int what, int value);
 typedef struct stage_pipeline* stage_pipeline_t;
 
 /* stages: n_stages created stages whose ranges tile [0, n_layers) in order, on one
- * device and stream.  The pipeline does not own them. */
+ * device and stream.  The pipeline does not own them.  Errors: STAGE_E_INVALID (ranges that
+ * do not tile the model, differing configs, streams or devices, null pointers), STAGE_E_CUDA
+ * (its buffers), STAGE_E_HOST. */
 STAGE_API int stage_pipeline_create(stage_t* stages, int n_stages, stage_pipeline_t* out);
 
 /* One step of all stages: prefill (is_prefill = 1) or decode, then the readout of
@@ -273,7 +304,9 @@ STAGE_API int stage_pipeline_create(stage_t* stages, int n_stages, stage_pipelin
  * NULL), next_tokens_host (host int32 [n_rows], may be NULL: the greedy tokens,
  * read back after the step, with every stage's error word).  Every stage's call is
  * validated and its inputs copied in before the first launch, so a call that fails
- * validation runs no stage.  Commits every stage to the new lengths on success. */
+ * validation runs no stage.  Commits every stage to the new lengths on success.  Errors:
+ * any stage's stage_prefill / stage_decode errors (nothing is committed on any stage),
+ * STAGE_E_INVALID (a readout row outside the step's tokens), STAGE_E_BUSY (a stage busy). */
 STAGE_API int stage_pipeline_step(stage_pipeline_t p, int is_prefill, int n_tokens, const int32_t* seq_ids_host,
                         const int32_t* positions_host, const int32_t* tokens_host, int n_rows,
                         const int32_t* row_index_host, float* logits_out, int32_t* next_tokens_host);
@@ -282,7 +315,9 @@ STAGE_API int stage_pipeline_step(stage_pipeline_t p, int is_prefill, int n_toke
  * on the device.  first_tokens_host: the token to feed at each sequence's committed
  * length.  tokens_out_host: host int32 [n_steps x batch], the greedy token of each
  * step.  use_graph = 1 replays one captured CUDA graph per step.  Commits n_steps
- * positions on every stage at the end. */
+ * positions on every stage at the end.  Errors: STAGE_E_INVALID (batch, seq_ids, tokens),
+ * STAGE_E_POSITION (a sequence would pass max_seq_len), STAGE_E_BUSY, STAGE_E_CUDA (graph
+ * capture or launch, or a kernel's error word); nothing is committed on failure. */
 STAGE_API int stage_pipeline_generate(stage_pipeline_t p, int batch, const int32_t* seq_ids_host,
                             const int32_t* first_tokens_host, int n_steps, int use_graph,
                             int32_t* tokens_out_host);
@@ -294,12 +329,17 @@ STAGE_API int stage_pipeline_generate(stage_pipeline_t p, int batch, const int32
  * (microseconds) of those launches in the last step and their count.  Events sit between kernels, so a timed launch
  * does not overlap its predecessor; leave timing off for the headline measurement. */
 STAGE_API int stage_pipeline_kernel_timing(stage_pipeline_t p, int enable);
+/* Count 0 while timing is off; STAGE_E_STATE when timing is on but no timed step has run;
+ * STAGE_E_INVALID for null pointers. */
 STAGE_API int stage_pipeline_kernel_time(stage_pipeline_t p, float* mean_us, int* count);
 
-/* Bytes handed across boundary k (0-based) so far, and the number of handoffs. */
+/* Bytes handed across boundary k (0-based) so far, and the number of handoffs.
+ * STAGE_E_INVALID for a boundary outside [0, n_stages - 1) or null pointers. */
 STAGE_API int stage_pipeline_handoff_stats(stage_pipeline_t p, int boundary, int64_t* calls, int64_t* bytes);
 
+/* Message of the pipeline's last failed call ("" if none), owned by the pipeline. */
 STAGE_API const char* stage_pipeline_last_error(stage_pipeline_t p);
+/* Free the pipeline's own buffers and graphs (not the stages).  NULL is accepted. */
 STAGE_API void stage_pipeline_destroy(stage_pipeline_t p);
 
 #ifdef __cplusplus

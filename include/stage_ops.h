@@ -18,11 +18,13 @@ extern "C" {
 #endif
 
 /* Device bytes of a packed [rows x cols] int8 block-32 matrix: the weight bytes (biased,
- * rows padded to a multiple of 256 weights) and the fp16 scale bytes. */
+ * rows padded to a multiple of 256 weights) and the fp16 scale bytes.  STAGE_E_INVALID for
+ * rows < 1, cols outside [1, 2^30] or null pointers. */
 STAGE_API int stage_op_q8_device_bytes(int64_t rows, int64_t cols, size_t* q_bytes, size_t* s_bytes);
 
 /* Pack a host matrix (layout of stage_q8) into caller device buffers of the sizes above.
- * Synchronous. */
+ * Synchronous.  Errors: STAGE_E_INVALID (null pointers, a shape stage_op_q8_device_bytes
+ * rejects), STAGE_E_HOST (the host staging buffer), STAGE_E_CUDA (the copies). */
 STAGE_API int stage_op_q8_pack(const stage_q8* host, void* q_dev, void* s_dev);
 
 /* Embedding rows: out[t][c] = scale(tok[t], c / 32) * q[tok[t]][c] for t < n_tok, c < cols --
@@ -30,7 +32,9 @@ STAGE_API int stage_op_q8_pack(const stage_q8* host, void* q_dev, void* s_dev);
  * placement across multiple GPUs for models larger than one device", section "What I found":
  * the first stage embeds).  W is a packed [rows x cols] matrix (stage_op_q8_pack); tok_dev:
  * device int32 [n_tok], every entry in [0, rows) (not checked on the device); out_dev: f32
- * [n_tok][cols], 16-byte aligned, cols a multiple of 4.  Runs on `stream`. */
+ * [n_tok][cols], 16-byte aligned, cols a multiple of 4.  Runs on `stream`.  Errors:
+ * STAGE_E_INVALID (null or unaligned pointers, rows outside [1, 2^30], cols outside
+ * [1, 2^24] or not a multiple of 4, n_tok outside [1, 65535]), STAGE_E_CUDA (the launch). */
 STAGE_API int stage_op_embed(const void* q_dev, const void* s_dev, int64_t rows, int64_t cols, const int32_t* tok_dev,
                              int n_tok, float* out_dev, void* stream);
 
@@ -41,7 +45,9 @@ STAGE_API int stage_op_embed(const void* q_dev, const void* s_dev, int64_t rows,
  * (stage_op_q8_pack).  x_dev: f32 [n_tok][cols]; y_dev: f32 [n_tok][rows].  Every |h| must
  * be below 2^64 (the dot product takes its inputs scaled by 2^64 in float32); float32
  * rounding error, relative to sum_k (q + 128) |h_k| + 128 |sum_k h_k| per 16-input chunk.
- * Runs on `stream` (a cudaStream_t); no allocation, no synchronisation. */
+ * Runs on `stream` (a cudaStream_t); no allocation, no synchronisation.  Errors:
+ * STAGE_E_INVALID (null or unaligned pointers, rows outside [1, 2^30], cols outside [1, 2^24]
+ * or not a multiple of 4, n_tok < 1), STAGE_E_CUDA (the launch). */
 STAGE_API int stage_op_gemv(const void* q_dev, const void* s_dev, int64_t rows, int64_t cols, const float* x_dev,
                             int n_tok, const float* gamma_dev, float eps, float* y_dev, void* stream);
 
@@ -49,11 +55,14 @@ STAGE_API int stage_op_gemv(const void* q_dev, const void* s_dev, int64_t rows, 
  * with A bf16 (bit patterns) [M][lda] on the device, lda >= the packed row length
  * (cols rounded up to 256) and multiple of 8, zero beyond cols; W a packed matrix whose
  * weights are rounded to bf16 (bf16(f32(scale) * q)); f32 accumulation (tcgen05, TMEM).
- * y_dev: f32 [M][rows].  Runs on `stream`. */
+ * y_dev: f32 [M][rows].  Runs on `stream`.  Errors: STAGE_E_INVALID (null or unaligned
+ * pointers, M < 1, rows outside [1, 2^30], cols outside [1, 2^24], lda too small or not a
+ * multiple of 8), STAGE_E_CUDA (tensor maps or the launch). */
 STAGE_API int stage_op_gemm_bf16(const uint16_t* a_dev, int lda, int M, const void* q_dev, const void* s_dev,
                                  int64_t rows, int64_t cols, float* y_dev, void* stream);
 
-/* Scratch bytes stage_op_attention_decode needs for these sizes. */
+/* Scratch bytes stage_op_attention_decode needs for these sizes (0 for a non-positive
+ * size). */
 STAGE_API size_t stage_op_attention_workspace_bytes(int n_tok, int n_q_heads, int n_kv_heads, int head_dim,
                                                     int n_chunks);
 
@@ -69,7 +78,10 @@ STAGE_API size_t stage_op_attention_workspace_bytes(int n_tok, int n_q_heads, in
  *   n_chunks in [1, 64]: the positions of each token are split in n_chunks chunks;
  *   workspace_dev: stage_op_attention_workspace_bytes(...) bytes of device scratch whose
  *     contents must be zero before the first call (each call leaves it ready for the next).
- * head_dim 64 or 128; n_q_heads / n_kv_heads in {1, 2, 4, 8}.  Runs on `stream`. */
+ * head_dim 64 or 128; n_q_heads / n_kv_heads in {1, 2, 4, 8}.  Runs on `stream`.  Errors:
+ * STAGE_E_INVALID (null or unaligned pointers, a non-positive size, an unsupported head_dim
+ * or group, n_chunks outside [1, 64], n_tok above 65535, a workspace unaligned or smaller
+ * than needed), STAGE_E_CUDA (the launch). */
 STAGE_API int stage_op_attention_decode(const float* q_dev, const uint16_t* k_cache_dev, const uint16_t* v_cache_dev,
                                         const int32_t* seq_dev, const int32_t* pos_dev, int n_tok, int n_q_heads,
                                         int n_kv_heads, int head_dim, int max_len, int n_chunks, float* out_dev,
@@ -93,7 +105,10 @@ STAGE_API int stage_op_attention_decode(const float* q_dev, const uint16_t* k_ca
  *   - Every call reuses the same array and clears its counters on `stream` before the
  *     kernel.  Calls whose kernels overlap on the GPU (on different streams, or different
  *     host threads) race on the array and give wrong results: serialise them.
- *   - No cudaMalloc, cudaFree or allocating library call is made. */
+ *   - No cudaMalloc, cudaFree or allocating library call is made.
+ *   - Errors: those of stage_op_attention_decode other than the workspace's, STAGE_E_INVALID
+ *     for scratch beyond the array or a device ordinal of 64 or more, STAGE_E_CUDA when the
+ *     array's device address cannot be looked up. */
 #define STAGE_OP_STATIC_SCRATCH_BYTES (4u << 20)
 STAGE_API int stage_op_attention_decode_static(const float* q_dev, const uint16_t* k_cache_dev,
                                                const uint16_t* v_cache_dev, const int32_t* seq_dev,

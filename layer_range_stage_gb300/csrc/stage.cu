@@ -1457,6 +1457,8 @@ extern "C" {
 int stage_pipeline_create(stage_t* stages, int n_stages, stage_pipeline_t* out) try {
   if (!out || !stages || n_stages <= 0) return STAGE_E_INVALID;
   *out = nullptr;
+  for (int i = 0; i < n_stages; ++i)
+    if (!stages[i]) return STAGE_E_INVALID;
   const stage_model_cfg& c0 = stages[0]->cfg;
   if (stages[0]->begin != 0 || !stages[n_stages - 1]->last) return STAGE_E_INVALID;
   for (int i = 0; i < n_stages; ++i) {
