@@ -142,3 +142,41 @@ def test_binding_has_every_entry_point_under_its_c_name():
         assert name in B._SIGS, name
     assert B.stage_create_error() == "" or isinstance(B.stage_create_error(), str)
     assert isinstance(B.stage_op_last_error(), str)
+
+
+def test_entry_points_reject_bad_arguments_before_any_device_call():
+    """The host-side checks the headers document, on a machine without a GPU: every call below
+    must fail with STAGE_E_INVALID and a message before touching the device."""
+    lib = L.lib()
+    v = ctypes.c_void_p
+    buf = (ctypes.c_float * 64)()
+    p = ctypes.cast(buf, v)                                # 16-byte aligned host memory
+    odd = v(p.value + 4)                                   # not 16-byte aligned
+    tok = (ctypes.c_int32 * 4)()
+    cases = [
+        lambda: lib.stage_op_embed(None, p, 10, 64, ctypes.cast(tok, v), 1, p, None),
+        lambda: lib.stage_op_embed(p, p, 10, 66, ctypes.cast(tok, v), 1, p, None),       # cols % 4
+        lambda: lib.stage_op_embed(p, p, 10, 64, ctypes.cast(tok, v), 70000, p, None),   # n_tok
+        lambda: lib.stage_op_gemv(p, p, 8, 64, odd, 1, None, ctypes.c_float(1e-5), p, None),
+        lambda: lib.stage_op_gemv(p, p, 0, 64, p, 1, None, ctypes.c_float(1e-5), p, None),
+        lambda: lib.stage_op_gemm_bf16(p, 100, 4, p, p, 8, 64, p, None),                  # lda < 256
+        lambda: lib.stage_op_attention_decode(p, p, p, p, p, 1, 4, 2, 96, 16, 1, p, p, 1 << 20, None),
+        lambda: lib.stage_op_attention_decode(p, p, p, p, p, 1, 4, 2, 64, 16, 65, p, p, 1 << 20, None),
+        lambda: lib.stage_op_attention_decode(p, p, p, p, p, 1, 4, 2, 64, 16, 1, p, p, 16, None),
+        lambda: lib.stage_op_attention_decode_static(p, p, p, p, p, 1, 4, 3, 64, 16, 1, p, None),
+    ]
+    for i, call in enumerate(cases):
+        assert call() == L.STAGE_E_INVALID, i
+        assert lib.stage_op_last_error().decode(), i
+    assert lib.stage_op_attention_workspace_bytes(0, 4, 2, 64, 1) == 0
+    out = v()
+    assert lib.stage_pipeline_create(None, 2, ctypes.byref(out)) == L.STAGE_E_INVALID
+    null_stages = (v * 2)()
+    assert lib.stage_pipeline_create(null_stages, 2, ctypes.byref(out)) == L.STAGE_E_INVALID
+    n = ctypes.c_int()
+    assert lib.stage_committed_len(None, 0, ctypes.byref(n)) == L.STAGE_E_INVALID
+    assert lib.stage_gemm_mode(None, 1, ctypes.byref(n)) == L.STAGE_E_INVALID
+    assert lib.stage_last_error(None).decode() == "null stage"
+    assert lib.stage_pipeline_last_error(None).decode() == "null pipeline"
+    lib.stage_destroy(None)
+    lib.stage_pipeline_destroy(None)
