@@ -11,7 +11,10 @@ logits) and K/V are rounded to float16 when stored.  Where the pages leave a ste
 open the plainest reading is taken; each such reading is marked "Reading:".
 
 Parity status: every function here is pinned by a test in tests/test_oracle_*.py
-against a closed form, an invariant, a special case or a brute-force loop.  The
+against a closed form, an invariant, a special case or a brute-force loop, and
+Stage.forward as a whole by weights that reduce a block to a closed form
+(tests/test_oracle_block_reductions.py: identity blocks, uniform attention, an
+identity SwiGLU in float32 and bf16, identical experts, an identity readout).  The
 end-to-end logits and greedy tokens of a seeded model are pinned only through
 those parts and through the staged-vs-unstaged invariant (no page prints values
 for a seeded model).
