@@ -1,11 +1,12 @@
-// Persistent decode of a dense stage (sm_103a): every block of the stage for one token in
-// one cooperative launch, one CTA per SM.
+// Persistent decode of a stage, dense or MoE (sm_103a): every block of the stage for one token
+// in one cooperative launch, one CTA per SM.
 //
 // What it computes is the decode block loop of "41. Many GPUs: tensor, pipeline, expert
 // and data parallelism", section "Pipeline parallelism" (add_norm, attention, add_norm,
 // MLP per block, the residual stream carried through), with the split-KV attention merge
 // of section "Ring attention for very long contexts".  The arithmetic per weight is the
-// dequant-fused dot product of q8dot.cuh.
+// integer-form dot product of q8dot.cuh: dp4a on the stored weight bytes against three signed
+// bytes per staged input, exact before its float32 scaling.
 //
 // Why one launch: a batch-1 decode step is a chain of small dependent matrix-vector
 // products.  Launched one kernel each, every product pays its own ramp and tail while HBM
