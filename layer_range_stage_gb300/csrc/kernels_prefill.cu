@@ -1,6 +1,8 @@
 // Prefill-path kernels (sm_103a): the tcgen05 tensor-core GEMM with int8 -> bf16 weight
-// dequantisation in shared memory, the bf16 conversion of activations, and the causal
-// attention of a prefill call on the tensor cores.
+// dequantisation in shared memory, its variant for calls of at most 64 tokens (batched
+// decode: the weights as the 128-row MMA operand, each read once, K split over CTAs where the
+// weight tiles are few), the bf16 conversion of activations, and the causal attention of a
+// prefill call on the tensor cores.
 //
 // "41. Many GPUs: tensor, pipeline, expert and data parallelism", section "Pipeline
 // parallelism": a prefill step is the same block loop as decode over all prompt tokens;
