@@ -43,7 +43,10 @@ __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem) : "memory");
 }
 
-// 8-byte asynchronous global -> shared copy (cached in L1: for read-only tables).
+// 8-byte asynchronous global -> shared copy, cached in L1: for tables that are read-only
+// during the kernel, or for data other CTAs wrote in this launch when an acquire at GPU scope
+// (then a CTA barrier) orders the copy after those writes -- the memory model then forbids a
+// stale value, whatever this SM's L1 held before.
 __device__ __forceinline__ void cp_async8(void* smem, const void* gmem) {
   const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
   asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(s), "l"(gmem) : "memory");
